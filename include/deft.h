@@ -1,0 +1,209 @@
+/*
+ * deft.h -- C ABI of the GB300 DeFT tree-attention decode library.
+ *
+ * The operation (DeFT: Decoding with Flash Tree-attention, arXiv 2404.00242,
+ * abstract; aifetchly "DeFT Guide: Flash Tree-Attention for LLM Serving",
+ * sections "The DeFT Architecture" and "Deep Dive: Mathematical Formulation"):
+ * queries sitting at nodes of a token tree attend, with one softmax each, to
+ * the KV tokens of every node on their root-to-node path (the node itself
+ * included).  The library splits the tree's KV into chunks (Flattened Tree KV
+ * Splitting), reads each chunk once for all queries whose path covers it
+ * (KV-Guided Grouping, recorded as a per-segment query bitmask), computes a
+ * partial softmax attention with its log-sum-exp per (chunk, query, head)
+ * and merges the partials per query by lse weight.
+ *
+ * Conventions shared by every call:
+ *   - Tree: parent[n] (int32, -1 = root; forests allowed), node_len[n] (int32
+ *     tokens, >= 0), query_node[q] (int32 node index).  Host memory.
+ *   - KV cache (device, bf16, caller-owned): k_pages and v_pages are
+ *     [num_pages][num_kv_heads][page_size][head_dim].  Token t of node n lives
+ *     in physical page page_id[node_page_off[n] + t / page_size], slot
+ *     t % page_size.  node_page_off is int32 [num_nodes + 1], page_id int32
+ *     (both device memory).  Slots past a node's last token are never read.
+ *   - q: bf16 [num_queries][num_q_heads][head_dim] (device).
+ *   - out: [num_queries][num_q_heads][head_dim], bf16 (DEFT_OUT_BF16) or fp32
+ *     (DEFT_OUT_F32); lse: fp32 [num_queries][num_q_heads], natural log of
+ *     the softmax normaliser of the scaled logits (device).  A query whose
+ *     path holds no token gets out = 0 and lse = -inf.
+ *   - Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - Every call returns a deft_status; none aborts or prints.
+ */
+#ifndef DEFT_H
+#define DEFT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum deft_status {
+    DEFT_OK = 0,
+    DEFT_EINVAL = -1,        /* null pointer, non-positive size or bad enum value   */
+    DEFT_ECYCLE = -2,        /* parent[] does not describe a forest                 */
+    DEFT_ERANGE = -3,        /* an index (parent, query_node, ...) is out of range  */
+    DEFT_ENOMEM = -4,        /* host or device allocation failed                    */
+    DEFT_EUNSUPPORTED = -5,  /* head_dim / page_size / GQA group not compiled in    */
+    DEFT_ECUDA = -6,         /* a CUDA runtime call or kernel launch failed          */
+    DEFT_EWORKSPACE = -7,    /* workspace null, too small or not 256-byte aligned   */
+    DEFT_ESTATE = -8         /* plan not uploaded, or built for another GQA group   */
+} deft_status;
+
+enum { DEFT_OUT_BF16 = 0, DEFT_OUT_F32 = 1 };
+
+/* Opaque plan: the flattened chunk list, segment bitmasks and per-query
+ * partial-slot lists of one tree.  Library-owned; free with deft_plan_free. */
+typedef struct deft_plan_t deft_plan_t;
+
+typedef struct deft_plan_stats {
+    int32_t num_nodes;
+    int32_t num_queries;
+    int32_t gqa_group;
+    int32_t chunk_target;
+    int32_t mask_words;          /* ceil(num_queries / 64): words per bitmask           */
+    int32_t num_chunks;          /* KV chunks of the tree plan                          */
+    int32_t num_segments;        /* (node, token range) pieces; never cross a node      */
+    int32_t num_slots;           /* sum over chunks of |Q_c|: partial results per head  */
+    int32_t num_fma_items;       /* phase-1 work items with < 16 rows (CUDA-core path)  */
+    int32_t num_mma_items;       /* phase-1 work items with >= 16 rows (tensor path)    */
+    int32_t num_fallback_items;  /* the >= 16-row chunks cut into <= 16-row items       */
+    int32_t max_chunk_tokens;
+    int32_t max_slots_per_query;
+    int32_t naive_num_chunks;    /* per-query flash-decoding partition                  */
+    int32_t naive_num_slots;
+    int32_t naive_num_segments;
+    int64_t unique_tokens;       /* tokens on at least one query path                   */
+    int64_t naive_tokens;        /* sum over queries of their path tokens               */
+    int64_t planned_tokens;      /* sum of chunk lengths; equals unique_tokens          */
+    int64_t pair_tokens;         /* sum over chunks of tokens * |Q_c| (incl. masked)    */
+} deft_plan_stats;
+
+/* Arrays a plan exposes through deft_plan_get (host copies, for tests and
+ * tools).  Element type and count are given beside each name. */
+typedef enum deft_plan_array {
+    DEFT_A_CHUNK_SEG_OFF = 0,   /* int32  [num_chunks + 1]  segment range of chunk c          */
+    DEFT_A_CHUNK_Q_OFF = 1,     /* int32  [num_chunks + 1]  range of chunk c in CHUNK_Q       */
+    DEFT_A_CHUNK_Q = 2,         /* int32  [num_slots]       query ids; the index is the slot  */
+    DEFT_A_SEG_NODE = 3,        /* int32  [num_segments]                                      */
+    DEFT_A_SEG_TOK_BEGIN = 4,   /* int32  [num_segments]    first token inside the node       */
+    DEFT_A_SEG_TOK_LEN = 5,     /* int32  [num_segments]                                      */
+    DEFT_A_SEG_MASK = 6,        /* uint64 [num_segments * mask_words]  queries that see it    */
+    DEFT_A_CHUNK_MASK = 7,      /* uint64 [num_chunks * mask_words]    union over segments    */
+    DEFT_A_Q_SLOT_OFF = 8,      /* int32  [num_queries + 1]                                   */
+    DEFT_A_Q_SLOT = 9,          /* int32  [num_slots]       partial slots of each query       */
+    DEFT_A_NODE_COVER = 10,     /* uint64 [num_nodes * mask_words]     coverage bitsets       */
+    DEFT_A_NODE_ORDER = 11,     /* int32  [num_nodes]       DFS preorder of all nodes         */
+    DEFT_A_FMA_ITEMS = 12,      /* int32  [num_fma_items * 3]  (chunk, q_begin, q_end)        */
+    DEFT_A_MMA_ITEMS = 13,      /* int32  [num_mma_items * 3]  q range local to the chunk     */
+    DEFT_A_FALLBACK_ITEMS = 14, /* int32  [num_fallback_items * 3]                            */
+    DEFT_A_NAIVE_CHUNK_SEG_OFF = 15, /* int32 [naive_num_chunks + 1]                          */
+    DEFT_A_NAIVE_CHUNK_Q = 16,       /* int32 [naive_num_slots] (one query per chunk)         */
+    DEFT_A_NAIVE_SEG_NODE = 17,      /* int32 [naive_num_segments]                            */
+    DEFT_A_NAIVE_SEG_TOK_BEGIN = 18, /* int32 [naive_num_segments]                            */
+    DEFT_A_NAIVE_SEG_TOK_LEN = 19,   /* int32 [naive_num_segments]                            */
+    DEFT_A_NAIVE_Q_SLOT_OFF = 20,    /* int32 [num_queries + 1]                               */
+    DEFT_A_NAIVE_Q_SLOT = 21,        /* int32 [naive_num_slots]                               */
+    DEFT_A_COUNT = 22
+} deft_plan_array;
+
+/*
+ * deft_plan -- build the plan of one tree (host only, no CUDA call).
+ * Follows the DeFT abstract (KV-Guided Grouping; Flattened Tree KV
+ * Splitting) and the Guide's section "The DeFT Architecture".
+ *   - Validates the tree: parent in [-1, num_nodes) (DEFT_ERANGE) and not a
+ *     cycle (DEFT_ECYCLE), node_len >= 0 (DEFT_EINVAL), query_node in
+ *     [0, num_nodes) (DEFT_ERANGE), num_nodes >= 1, num_queries >= 0.
+ *   - cover[n]: bit q set iff n lies on query q's root-to-node path.
+ *   - Flattens nodes in DFS preorder (roots, then children, ascending id),
+ *     cuts every node's tokens into segments and packs short segments into
+ *     chunks of at most chunk_target tokens (1 <= chunk_target <= 8192); a
+ *     heavily shared node gets longer chunks so that its partial-result
+ *     traffic stays small next to its KV traffic.  Every (query, node on its
+ *     path, token) triple lands in exactly one chunk that lists the query.
+ *   - gqa_group = num_q_heads / num_kv_heads of the layer the plan will run
+ *     (decides which chunks reach 16 rows = |Q_c| * gqa_group); 1..128.
+ *   - The naive per-query partition (deft_naive_attn) cuts each query's
+ *     path tokens into pieces of chunk_target tokens.
+ * On success *out owns the plan (free with deft_plan_free).  The input arrays
+ * are not retained.
+ */
+int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+              const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
+              int32_t gqa_group, deft_plan_t **out);
+
+/* Plan statistics (host).  DEFT_EINVAL on null arguments. */
+int deft_plan_stats_get(const deft_plan_t *plan, deft_plan_stats *out);
+
+/* Copy one plan array (see deft_plan_array for type and length) to host
+ * memory `dst` of `bytes` bytes.  DEFT_EINVAL if `bytes` is smaller than the
+ * array or `which` is unknown. */
+int deft_plan_get(const deft_plan_t *plan, int32_t which, void *dst, size_t bytes);
+
+/* Copy the plan to device memory owned by the plan (allocated on the first
+ * call, on the current device).  Enqueued on `stream` (a cudaStream_t, NULL =
+ * legacy default stream); the plan's host copy stays alive, so the call may
+ * return before the copy ends.  Call before deft_tree_attn / deft_naive_attn
+ * on the same device. */
+int deft_plan_upload(deft_plan_t *plan, void *stream);
+
+/* Bytes of device workspace deft_tree_attn and deft_naive_attn need for this
+ * plan: fp32 partial outputs and lse values for every slot and query head of
+ * either partition (the larger).  Returns 0 on bad arguments. */
+size_t deft_workspace_bytes(const deft_plan_t *plan, int32_t num_q_heads, int32_t head_dim);
+
+/*
+ * deft_tree_attn -- one tree-attention decode step (DeFT Guide, "Deep Dive":
+ * online-softmax tile accumulation; DeFT abstract: partial results merged
+ * per query).  Phase 1 reads every chunk's KV once per KV head and writes
+ * (o, lse) partials for each (chunk, query, query head) into the
+ * workspace; phase 2 merges each query's partials by lse weight into out
+ * and lse.  Chunks with >= 16 rows run on tcgen05 tensor cores (head_dim
+ * 128), the others on CUDA-core FMA.
+ *   q, k_pages, v_pages, node_page_off, page_id, out, lse, workspace: device
+ *     pointers as described at the top of this file; workspace must be
+ *     256-byte aligned and hold deft_workspace_bytes(plan, num_q_heads,
+ *     head_dim) bytes; its contents need not be initialised.  num_pages
+ *     bounds page_id's values (checked only by a debug build).
+ *   head_dim in {64, 128}; page_size 16; num_q_heads a multiple of
+ *     num_kv_heads whose quotient equals the plan's gqa_group (else
+ *     DEFT_ESTATE); scale > 0 multiplies q.k (pass 1/sqrt(head_dim)).
+ * Never allocates, never synchronises the host; stream-ordered on `stream`.
+ * Launch failures return DEFT_ECUDA.
+ */
+int deft_tree_attn(const void *q, const void *k_pages, const void *v_pages,
+                   const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
+                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                   int32_t page_size, float scale, const deft_plan_t *plan, void *out,
+                   int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                   void *stream);
+
+/*
+ * deft_naive_attn -- the same step computed the per-query flash-decoding way
+ * (DeFT Guide, "The Tree-Attention Bottleneck": every branch re-reads the
+ * shared prefix): each query's path is split into pieces of chunk_target
+ * tokens, each piece read for that query alone, then the same merge.  Same
+ * arguments, results and rules as deft_tree_attn; the in-run IO comparison.
+ */
+int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
+                    const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
+                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t page_size, float scale, const deft_plan_t *plan, void *out,
+                    int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/* Free a plan and its device copy (the caller must ensure no kernel using it
+ * is still running).  NULL is a no-op. */
+void deft_plan_free(deft_plan_t *plan);
+
+/* Static English text of a status code. */
+const char *deft_status_str(int status);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int deft_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DEFT_H */

@@ -1,0 +1,242 @@
+"""Python binding of the GB300 DeFT tree-attention decode library.
+
+A thin ctypes layer over the C ABI in include/deft.h (libdeft.so, built by
+`shared_prefix_kv_deft_gb300.build.build()`): the functions below have the
+C names and only marshal arguments.  PyTorch provides device memory and the
+current CUDA stream; every step of the computation runs in the library's
+CUDA kernels.  There is no fallback: if libdeft.so is missing or a call
+fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_build", "libdeft.so")
+
+DEFT_OUT_BF16 = 0
+DEFT_OUT_F32 = 1
+
+# deft_plan_array values (include/deft.h)
+ARRAYS = {
+    "chunk_seg_off": (0, np.int32), "chunk_q_off": (1, np.int32), "chunk_q": (2, np.int32),
+    "seg_node": (3, np.int32), "seg_tok_begin": (4, np.int32), "seg_tok_len": (5, np.int32),
+    "seg_mask": (6, np.uint64), "chunk_mask": (7, np.uint64), "q_slot_off": (8, np.int32),
+    "q_slot": (9, np.int32), "node_cover": (10, np.uint64), "node_order": (11, np.int32),
+    "fma_items": (12, np.int32), "mma_items": (13, np.int32), "fallback_items": (14, np.int32),
+    "naive_chunk_seg_off": (15, np.int32), "naive_chunk_q": (16, np.int32),
+    "naive_seg_node": (17, np.int32), "naive_seg_tok_begin": (18, np.int32),
+    "naive_seg_tok_len": (19, np.int32), "naive_q_slot_off": (20, np.int32),
+    "naive_q_slot": (21, np.int32),
+}
+
+# Symbols the header declares (checked by the tests).
+EXPORTS = ["deft_plan", "deft_plan_stats_get", "deft_plan_get", "deft_plan_upload",
+           "deft_workspace_bytes", "deft_tree_attn", "deft_naive_attn", "deft_plan_free",
+           "deft_status_str", "deft_version"]
+
+
+class DeftError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {status} ({status_str(status)})")
+        self.status = status
+
+
+class PlanStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_nodes", "num_queries", "gqa_group", "chunk_target", "mask_words", "num_chunks",
+        "num_segments", "num_slots", "num_fma_items", "num_mma_items", "num_fallback_items",
+        "max_chunk_tokens", "max_slots_per_query", "naive_num_chunks", "naive_num_slots",
+        "naive_num_segments")] + [(n, ctypes.c_int64) for n in (
+        "unique_tokens", "naive_tokens", "planned_tokens", "pair_tokens")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libdeft.so; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with "
+                           "shared_prefix_kv_deft_gb300.build.build() (no fallback exists)")
+    lib = ctypes.CDLL(path)
+    P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
+    lib.deft_plan.argtypes = [P, P, i32, P, i32, i32, i32, ctypes.POINTER(P)]
+    lib.deft_plan_stats_get.argtypes = [P, ctypes.POINTER(PlanStats)]
+    lib.deft_plan_get.argtypes = [P, i32, P, sz]
+    lib.deft_plan_upload.argtypes = [P, P]
+    lib.deft_workspace_bytes.argtypes = [P, i32, i32]
+    lib.deft_workspace_bytes.restype = sz
+    attn = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, i32, P, P, sz, P]
+    lib.deft_tree_attn.argtypes = attn
+    lib.deft_naive_attn.argtypes = attn
+    lib.deft_plan_free.argtypes = [P]
+    lib.deft_plan_free.restype = None
+    lib.deft_status_str.argtypes = [ctypes.c_int]
+    lib.deft_status_str.restype = ctypes.c_char_p
+    lib.deft_version.argtypes = []
+    for fn in ("deft_plan", "deft_plan_stats_get", "deft_plan_get", "deft_plan_upload",
+               "deft_tree_attn", "deft_naive_attn", "deft_version"):
+        getattr(lib, fn).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_str(status: int) -> str:
+    return load().deft_status_str(int(status)).decode()
+
+
+def _check(fn: str, rc: int):
+    if rc != 0:
+        raise DeftError(fn, rc)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Plan:
+    """Owner of a deft_plan_t handle (deft_plan ... deft_plan_free)."""
+
+    def __init__(self, parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1):
+        lib = load()
+        self._parent, self._len, self._qn = _i32(parent), _i32(node_len), _i32(query_node)
+        h = ctypes.c_void_p()
+        _check("deft_plan", lib.deft_plan(_ptr(self._parent), _ptr(self._len),
+                                          int(self._parent.shape[0]), _ptr(self._qn),
+                                          int(self._qn.shape[0]), int(chunk_target),
+                                          int(gqa_group), ctypes.byref(h)))
+        self.handle = h
+        st = PlanStats()
+        _check("deft_plan_stats_get", lib.deft_plan_stats_get(self.handle, ctypes.byref(st)))
+        self.stats = st.as_dict()
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            _lib.deft_plan_free(h)
+            self.handle = None
+
+    def _count(self, name: str) -> int:
+        s = self.stats
+        W, C, S = s["mask_words"], s["num_chunks"], s["num_segments"]
+        counts = {
+            "chunk_seg_off": C + 1, "chunk_q_off": C + 1, "chunk_q": s["num_slots"],
+            "seg_node": S, "seg_tok_begin": S, "seg_tok_len": S, "seg_mask": S * W,
+            "chunk_mask": C * W, "q_slot_off": s["num_queries"] + 1, "q_slot": s["num_slots"],
+            "node_cover": s["num_nodes"] * W, "node_order": s["num_nodes"],
+            "fma_items": 3 * s["num_fma_items"], "mma_items": 3 * s["num_mma_items"],
+            "fallback_items": 3 * s["num_fallback_items"],
+            "naive_chunk_seg_off": s["naive_num_chunks"] + 1,
+            "naive_chunk_q": s["naive_num_slots"], "naive_seg_node": s["naive_num_segments"],
+            "naive_seg_tok_begin": s["naive_num_segments"],
+            "naive_seg_tok_len": s["naive_num_segments"],
+            "naive_q_slot_off": s["num_queries"] + 1, "naive_q_slot": s["naive_num_slots"],
+        }
+        return counts[name]
+
+    def get(self, name: str) -> np.ndarray:
+        """Host copy of one plan array (deft_plan_get)."""
+        which, dt = ARRAYS[name]
+        out = np.zeros(max(self._count(name), 1), dtype=dt)
+        _check("deft_plan_get", load().deft_plan_get(self.handle, which, _ptr(out), out.nbytes))
+        return out[: self._count(name)]
+
+    def upload(self, stream=None):
+        _check("deft_plan_upload", load().deft_plan_upload(self.handle, _stream(stream)))
+
+    def workspace_bytes(self, num_q_heads: int, head_dim: int) -> int:
+        return int(load().deft_workspace_bytes(self.handle, int(num_q_heads), int(head_dim)))
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+@dataclass
+class StepBuffers:
+    out: "object"
+    lse: "object"
+    workspace: "object"
+
+
+def alloc_buffers(plan: Plan, num_queries: int, num_q_heads: int, head_dim: int, device="cuda",
+                  out_dtype: int = DEFT_OUT_BF16) -> StepBuffers:
+    """Device output, lse and workspace tensors for one step (torch memory)."""
+    import torch
+    odt = torch.bfloat16 if out_dtype == DEFT_OUT_BF16 else torch.float32
+    ws = plan.workspace_bytes(num_q_heads, head_dim)
+    return StepBuffers(torch.empty((num_queries, num_q_heads, head_dim), dtype=odt, device=device),
+                       torch.empty((num_queries, num_q_heads), dtype=torch.float32, device=device),
+                       torch.empty(ws, dtype=torch.uint8, device=device))
+
+
+def _attn(fn_name: str, q, k_pages, v_pages, node_page_off, page_id, plan: Plan,
+          bufs: Optional[StepBuffers] = None, scale: Optional[float] = None,
+          out_dtype: int = DEFT_OUT_BF16, stream=None):
+    import torch
+    lib = load()
+    Q, Hq, d = q.shape
+    Hkv, P = k_pages.shape[1], k_pages.shape[2]
+    if bufs is None:
+        bufs = alloc_buffers(plan, Q, Hq, d, q.device, out_dtype)
+    for t in (q, k_pages, v_pages):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k_pages and v_pages must be contiguous bf16 CUDA tensors")
+    for t in (node_page_off, page_id):
+        if t.dtype != torch.int32 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("node_page_off and page_id must be contiguous int32 CUDA tensors")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    odt = DEFT_OUT_BF16 if bufs.out.dtype == torch.bfloat16 else DEFT_OUT_F32
+    rc = getattr(lib, fn_name)(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pages.data_ptr()),
+        ctypes.c_void_p(v_pages.data_ptr()), ctypes.c_void_p(node_page_off.data_ptr()),
+        ctypes.c_void_p(page_id.data_ptr()), int(k_pages.shape[0]), int(Hq), int(Hkv), int(d),
+        int(P), float(scale), plan.handle, ctypes.c_void_p(bufs.out.data_ptr()), odt,
+        ctypes.c_void_p(bufs.lse.data_ptr()), ctypes.c_void_p(bufs.workspace.data_ptr()),
+        int(bufs.workspace.numel()), _stream(stream))
+    _check(fn_name, rc)
+    return bufs.out, bufs.lse
+
+
+def deft_tree_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs=None,
+                   scale=None, out_dtype=DEFT_OUT_BF16, stream=None):
+    """One DeFT tree-attention step; returns (out, lse) device tensors."""
+    return _attn("deft_tree_attn", q, k_pages, v_pages, node_page_off, page_id, plan, bufs,
+                 scale, out_dtype, stream)
+
+
+def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs=None,
+                    scale=None, out_dtype=DEFT_OUT_BF16, stream=None):
+    """The per-query flash-decoding form of the same step (IO comparison)."""
+    return _attn("deft_naive_attn", q, k_pages, v_pages, node_page_off, page_id, plan, bufs,
+                 scale, out_dtype, stream)
+
+
+def deft_plan(parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1) -> Plan:
+    return Plan(parent, node_len, query_node, chunk_target, gqa_group)
+
+
+def version() -> int:
+    return int(load().deft_version())

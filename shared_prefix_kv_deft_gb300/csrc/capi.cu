@@ -1,0 +1,350 @@
+// capi.cu -- the extern "C" entry points declared in include/deft.h.
+//
+// Plan calls are host-only; deft_plan_upload copies the plan's arrays into
+// one device allocation owned by the plan; deft_tree_attn / deft_naive_attn
+// validate their arguments and enqueue phase 1 (tensor-core and CUDA-core
+// kernels) and phase 2 on the caller's stream without allocating or
+// synchronising.
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include <cuda_runtime.h>
+
+#include "deft_internal.h"
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+template <typename T>
+size_t vbytes(const std::vector<T> &v) { return v.size() * sizeof(T); }
+
+int copy_out(const void *src, size_t n, void *dst, size_t bytes)
+{
+    if (bytes < n)
+        return DEFT_EINVAL;
+    if (n)
+        std::memcpy(dst, src, n);
+    return DEFT_OK;
+}
+
+// Layout of one partition inside the device blob.
+struct Layout {
+    size_t off[14];
+};
+
+void plan_partition_layout(const deft::Partition &p, size_t &cursor, Layout &L)
+{
+    const size_t sizes[14] = {vbytes(p.chunk_seg_off), vbytes(p.chunk_q_off), vbytes(p.chunk_tokens),
+                              vbytes(p.chunk_q),       vbytes(p.seg_node),    vbytes(p.seg_tok_begin),
+                              vbytes(p.seg_tok_len),   vbytes(p.seg_chunk_pos), vbytes(p.seg_mask),
+                              vbytes(p.q_slot_off),    vbytes(p.q_slot),      vbytes(p.fma_items),
+                              vbytes(p.mma_items),     vbytes(p.fallback_items)};
+    for (int i = 0; i < 14; ++i) {
+        L.off[i] = cursor;
+        cursor = align_up(cursor + (sizes[i] ? sizes[i] : 4));
+    }
+}
+
+void fill_partition(const deft::Partition &p, const Layout &L, uint8_t *host,
+                    uint8_t *dev, int32_t num_queries, int32_t mask_words, deft::DevPartition &d)
+{
+    auto put = [&](int i, const void *src, size_t n) {
+        if (n)
+            std::memcpy(host + L.off[i], src, n);
+    };
+    put(0, p.chunk_seg_off.data(), vbytes(p.chunk_seg_off));
+    put(1, p.chunk_q_off.data(), vbytes(p.chunk_q_off));
+    put(2, p.chunk_tokens.data(), vbytes(p.chunk_tokens));
+    put(3, p.chunk_q.data(), vbytes(p.chunk_q));
+    put(4, p.seg_node.data(), vbytes(p.seg_node));
+    put(5, p.seg_tok_begin.data(), vbytes(p.seg_tok_begin));
+    put(6, p.seg_tok_len.data(), vbytes(p.seg_tok_len));
+    put(7, p.seg_chunk_pos.data(), vbytes(p.seg_chunk_pos));
+    put(8, p.seg_mask.data(), vbytes(p.seg_mask));
+    put(9, p.q_slot_off.data(), vbytes(p.q_slot_off));
+    put(10, p.q_slot.data(), vbytes(p.q_slot));
+    put(11, p.fma_items.data(), vbytes(p.fma_items));
+    put(12, p.mma_items.data(), vbytes(p.mma_items));
+    put(13, p.fallback_items.data(), vbytes(p.fallback_items));
+    auto i32 = [&](int i) { return reinterpret_cast<const int32_t *>(dev + L.off[i]); };
+    d.chunk_seg_off = i32(0);
+    d.chunk_q_off = i32(1);
+    d.chunk_tokens = i32(2);
+    d.chunk_q = i32(3);
+    d.seg_node = i32(4);
+    d.seg_tok_begin = i32(5);
+    d.seg_tok_len = i32(6);
+    d.seg_chunk_pos = i32(7);
+    d.seg_mask = reinterpret_cast<const uint64_t *>(dev + L.off[8]);
+    d.q_slot_off = i32(9);
+    d.q_slot = i32(10);
+    d.fma_items = i32(11);
+    d.mma_items = i32(12);
+    d.fallback_items = i32(13);
+    d.num_fma_items = (int32_t)(p.fma_items.size() / 3);
+    d.num_mma_items = (int32_t)(p.mma_items.size() / 3);
+    d.num_fallback_items = (int32_t)(p.fallback_items.size() / 3);
+    d.num_slots = p.num_slots();
+    d.num_queries = num_queries;
+    d.mask_words = mask_words;
+}
+
+size_t partial_bytes(int64_t slots, int32_t num_q_heads, int32_t head_dim)
+{
+    const size_t o = align_up((size_t)slots * num_q_heads * head_dim * sizeof(float));
+    const size_t l = align_up((size_t)slots * num_q_heads * sizeof(float));
+    return o + l;
+}
+
+bool env_flag(const char *name)
+{
+    const char *v = std::getenv(name);
+    return v && v[0] && v[0] != '0';
+}
+
+int run_step(const void *q, const void *k_pages, const void *v_pages, const int32_t *node_page_off,
+             const int32_t *page_id, int32_t num_pages, int32_t num_q_heads, int32_t num_kv_heads,
+             int32_t head_dim, int32_t page_size, float scale, const deft_plan_t *plan, void *out,
+             int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes, void *stream,
+             bool naive)
+{
+    if (!plan || !q || !k_pages || !v_pages || !node_page_off || !page_id || !out || !lse)
+        return DEFT_EINVAL;
+    if (out_dtype != DEFT_OUT_BF16 && out_dtype != DEFT_OUT_F32)
+        return DEFT_EINVAL;
+    if (!(scale > 0.f) || !std::isfinite(scale) || num_pages < 1)
+        return DEFT_EINVAL;
+    if (num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
+        return DEFT_EINVAL;
+    if ((head_dim != 64 && head_dim != 128) || page_size != deft::kPageSize)
+        return DEFT_EUNSUPPORTED;
+    if (num_q_heads / num_kv_heads != plan->gqa_group || !plan->uploaded)
+        return DEFT_ESTATE;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DEFT_ECUDA;
+    if (dev != plan->dev_device)
+        return DEFT_ESTATE;
+    const deft::Partition &hp = naive ? plan->naive : plan->tree;
+    const deft::DevPartition &dp = naive ? plan->dev_naive : plan->dev_tree;
+    const size_t need = deft_workspace_bytes(plan, num_q_heads, head_dim);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 || workspace_bytes < need)
+        return DEFT_EWORKSPACE;
+    if (plan->num_queries == 0)
+        return DEFT_OK;
+
+    deft::AttnArgs a{};
+    a.q = q;
+    a.k_pages = k_pages;
+    a.v_pages = v_pages;
+    a.node_page_off = node_page_off;
+    a.page_id = page_id;
+    a.num_pages = num_pages;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.gqa_group = plan->gqa_group;
+    a.scale_log2 = scale * 1.44269504088896340736f;
+    const size_t slots = (size_t)std::max(plan->tree.num_slots(), plan->naive.num_slots());
+    a.o_part = reinterpret_cast<float *>(workspace);
+    a.lse_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) +
+                                           align_up(slots * num_q_heads * head_dim * sizeof(float)));
+
+    const bool use_mma = deft::mma_supported(head_dim) && !env_flag("DEFT_DISABLE_MMA");
+    // The CUDA-core kernel holds at most kFmaMaxRows rows per item; one query
+    // of a larger GQA group needs the tensor-core path.
+    if (plan->gqa_group > deft::kFmaMaxRows && !use_mma)
+        return DEFT_EUNSUPPORTED;
+    int rc = 0;
+    if (dp.num_mma_items > 0) {
+        // The tensor-core path covers head_dim 128; other head sizes, or a run
+        // with DEFT_DISABLE_MMA set, take the same chunks on CUDA cores in
+        // items of at most 16 rows.
+        if (use_mma)
+            rc = deft::launch_phase1_mma(a, dp, stream);
+        else
+            rc = deft::launch_phase1_fma(a, dp, dp.fallback_items, hp.fallback_bucket_off.data(), stream);
+        if (rc)
+            return DEFT_ECUDA;
+    }
+    if (dp.num_fma_items > 0) {
+        rc = deft::launch_phase1_fma(a, dp, dp.fma_items, hp.fma_bucket_off.data(), stream);
+        if (rc)
+            return DEFT_ECUDA;
+    }
+    rc = deft::launch_phase2(a, dp, out, out_dtype, lse, stream);
+    return rc ? DEFT_ECUDA : DEFT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+              const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
+              int32_t gqa_group, deft_plan_t **out)
+{
+    if (!out)
+        return DEFT_EINVAL;
+    *out = nullptr;
+    deft_plan_t *p = new (std::nothrow) deft_plan_t();
+    if (!p)
+        return DEFT_ENOMEM;
+    int rc;
+    try {
+        rc = deft::build_plan(parent, node_len, num_nodes, query_node, num_queries, chunk_target,
+                              gqa_group, p);
+    } catch (const std::bad_alloc &) {
+        rc = DEFT_ENOMEM;
+    }
+    if (rc != DEFT_OK) {
+        delete p;
+        return rc;
+    }
+    *out = p;
+    return DEFT_OK;
+}
+
+int deft_plan_stats_get(const deft_plan_t *plan, deft_plan_stats *out)
+{
+    if (!plan || !out)
+        return DEFT_EINVAL;
+    *out = plan->stats;
+    return DEFT_OK;
+}
+
+int deft_plan_get(const deft_plan_t *plan, int32_t which, void *dst, size_t bytes)
+{
+    if (!plan || (!dst && bytes))
+        return DEFT_EINVAL;
+    const deft::Partition &t = plan->tree, &n = plan->naive;
+    auto cp = [&](const auto &v) { return copy_out(v.data(), vbytes(v), dst, bytes); };
+    switch (which) {
+    case DEFT_A_CHUNK_SEG_OFF: return cp(t.chunk_seg_off);
+    case DEFT_A_CHUNK_Q_OFF: return cp(t.chunk_q_off);
+    case DEFT_A_CHUNK_Q: return cp(t.chunk_q);
+    case DEFT_A_SEG_NODE: return cp(t.seg_node);
+    case DEFT_A_SEG_TOK_BEGIN: return cp(t.seg_tok_begin);
+    case DEFT_A_SEG_TOK_LEN: return cp(t.seg_tok_len);
+    case DEFT_A_SEG_MASK: return cp(t.seg_mask);
+    case DEFT_A_CHUNK_MASK: return cp(t.chunk_mask);
+    case DEFT_A_Q_SLOT_OFF: return cp(t.q_slot_off);
+    case DEFT_A_Q_SLOT: return cp(t.q_slot);
+    case DEFT_A_NODE_COVER: return cp(plan->cover);
+    case DEFT_A_NODE_ORDER: return cp(plan->order);
+    case DEFT_A_FMA_ITEMS: return cp(t.fma_items);
+    case DEFT_A_MMA_ITEMS: return cp(t.mma_items);
+    case DEFT_A_FALLBACK_ITEMS: return cp(t.fallback_items);
+    case DEFT_A_NAIVE_CHUNK_SEG_OFF: return cp(n.chunk_seg_off);
+    case DEFT_A_NAIVE_CHUNK_Q: return cp(n.chunk_q);
+    case DEFT_A_NAIVE_SEG_NODE: return cp(n.seg_node);
+    case DEFT_A_NAIVE_SEG_TOK_BEGIN: return cp(n.seg_tok_begin);
+    case DEFT_A_NAIVE_SEG_TOK_LEN: return cp(n.seg_tok_len);
+    case DEFT_A_NAIVE_Q_SLOT_OFF: return cp(n.q_slot_off);
+    case DEFT_A_NAIVE_Q_SLOT: return cp(n.q_slot);
+    default: return DEFT_EINVAL;
+    }
+}
+
+int deft_plan_upload(deft_plan_t *plan, void *stream)
+{
+    if (!plan)
+        return DEFT_EINVAL;
+    size_t cursor = 0;
+    Layout lt, ln;
+    plan_partition_layout(plan->tree, cursor, lt);
+    plan_partition_layout(plan->naive, cursor, ln);
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return DEFT_ECUDA;
+    if (plan->dev_blob && (plan->dev_bytes < cursor || plan->dev_device != dev)) {
+        cudaFree(plan->dev_blob);
+        plan->dev_blob = nullptr;
+        plan->uploaded = false;
+    }
+    if (!plan->dev_blob) {
+        if (cudaMalloc(&plan->dev_blob, cursor) != cudaSuccess) {
+            plan->dev_blob = nullptr;
+            return DEFT_ENOMEM;
+        }
+        plan->dev_bytes = cursor;
+        plan->dev_device = dev;
+    }
+    std::vector<uint8_t> host(cursor, 0);
+    uint8_t *dev_base = reinterpret_cast<uint8_t *>(plan->dev_blob);
+    fill_partition(plan->tree, lt, host.data(), dev_base, plan->num_queries, plan->mask_words,
+                   plan->dev_tree);
+    fill_partition(plan->naive, ln, host.data(), dev_base, plan->num_queries, plan->mask_words,
+                   plan->dev_naive);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // Pageable source: the runtime has staged it by the time the call
+    // returns, so the local buffer may be released afterwards.
+    if (cudaMemcpyAsync(plan->dev_blob, host.data(), cursor, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return DEFT_ECUDA;
+    plan->uploaded = true;
+    return DEFT_OK;
+}
+
+size_t deft_workspace_bytes(const deft_plan_t *plan, int32_t num_q_heads, int32_t head_dim)
+{
+    if (!plan || num_q_heads < 1 || head_dim < 1)
+        return 0;
+    const int64_t slots = std::max(plan->tree.num_slots(), plan->naive.num_slots());
+    return partial_bytes(slots > 0 ? slots : 1, num_q_heads, head_dim);
+}
+
+int deft_tree_attn(const void *q, const void *k_pages, const void *v_pages,
+                   const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
+                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                   float scale, const deft_plan_t *plan, void *out, int32_t out_dtype, float *lse,
+                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    return run_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads,
+                    num_kv_heads, head_dim, page_size, scale, plan, out, out_dtype, lse, workspace,
+                    workspace_bytes, stream, false);
+}
+
+int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
+                    const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
+                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                    float scale, const deft_plan_t *plan, void *out, int32_t out_dtype, float *lse,
+                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    return run_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads,
+                    num_kv_heads, head_dim, page_size, scale, plan, out, out_dtype, lse, workspace,
+                    workspace_bytes, stream, true);
+}
+
+void deft_plan_free(deft_plan_t *plan)
+{
+    if (!plan)
+        return;
+    if (plan->dev_blob)
+        cudaFree(plan->dev_blob);
+    delete plan;
+}
+
+const char *deft_status_str(int status)
+{
+    switch (status) {
+    case DEFT_OK: return "ok";
+    case DEFT_EINVAL: return "invalid argument";
+    case DEFT_ECYCLE: return "parent array has a cycle";
+    case DEFT_ERANGE: return "index out of range";
+    case DEFT_ENOMEM: return "out of memory";
+    case DEFT_EUNSUPPORTED: return "unsupported head_dim, page_size or GQA shape";
+    case DEFT_ECUDA: return "CUDA runtime or launch error";
+    case DEFT_EWORKSPACE: return "workspace missing, too small or misaligned";
+    case DEFT_ESTATE: return "plan not uploaded on this device or built for another GQA group";
+    default: return "unknown status";
+    }
+}
+
+int deft_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,139 @@
+// deft_internal.h -- library-internal plan structures and kernel launchers.
+//
+// The host plan (built by planner.cpp) is a set of flat arrays describing two
+// partitions of the tree's KV:
+//   * the DeFT partition: chunks of the DFS-preorder flattened tree (Flattened
+//     Tree KV Splitting), each shared by the queries whose paths cover it
+//     (KV-Guided Grouping; DeFT abstract, DeFT Guide "The DeFT Architecture");
+//   * the naive partition: every query's own path cut into pieces, the
+//     per-query flash-decoding baseline (DeFT Guide, "The Tree-Attention
+//     Bottleneck").
+// Both have the same shape, so one set of kernels runs either.
+#pragma once
+
+#include <array>
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include "deft.h"
+
+namespace deft {
+
+constexpr int kPageSize = 16;          // tokens per KV page
+constexpr int kMaxChunkTarget = 8192;  // bound on the chunk_target argument
+constexpr int kMaxSegsPerChunk = 256;  // packed chunks close at this many segments
+constexpr int kFmaMaxRows = 16;        // rows (queries x GQA group) per CUDA-core item
+constexpr int kMmaMaxRows = 128;       // rows per tensor-core item (one MMA N extent)
+constexpr int kMmaMinRows = 16;        // a chunk with this many rows goes to the tensor path
+constexpr int kSharedTokensPerRow = 16;  // long-chunk rule for shared nodes (see planner.cpp)
+
+// One partition, host side.  Items are (chunk, q_begin, q_end) triples where
+// [q_begin, q_end) indexes the chunk's query list.
+struct Partition {
+    std::vector<int32_t> chunk_seg_off;   // [C+1]
+    std::vector<int32_t> chunk_q_off;     // [C+1]
+    std::vector<int32_t> chunk_tokens;    // [C]
+    std::vector<int32_t> chunk_q;         // [slots]
+    std::vector<int32_t> seg_node;        // [S]
+    std::vector<int32_t> seg_tok_begin;   // [S]
+    std::vector<int32_t> seg_tok_len;     // [S]
+    std::vector<int32_t> seg_chunk_pos;   // [S] token offset of the segment in its chunk
+    std::vector<uint64_t> seg_mask;       // [S * W]
+    std::vector<uint64_t> chunk_mask;     // [C * W]
+    std::vector<int32_t> q_slot_off;      // [Q+1]
+    std::vector<int32_t> q_slot;          // [slots]
+    std::vector<int32_t> fma_items;       // [3 * n]
+    std::vector<int32_t> mma_items;       // [3 * n]
+    std::vector<int32_t> fallback_items;  // [3 * n]
+    // fma_items and fallback_items are sorted by row bucket b (rows <= 2^b,
+    // b = 0..4); bucket b is items [off[b], off[b+1]).
+    std::array<int32_t, 6> fma_bucket_off{};
+    std::array<int32_t, 6> fallback_bucket_off{};
+    int32_t num_chunks() const { return (int32_t)chunk_tokens.size(); }
+    int32_t num_segments() const { return (int32_t)seg_node.size(); }
+    int32_t num_slots() const { return (int32_t)chunk_q.size(); }
+};
+
+// Device view of one partition: plain pointers into the plan's device blob,
+// passed to kernels by value.
+struct DevPartition {
+    const int32_t *chunk_seg_off;
+    const int32_t *chunk_q_off;
+    const int32_t *chunk_tokens;
+    const int32_t *chunk_q;
+    const int32_t *seg_node;
+    const int32_t *seg_tok_begin;
+    const int32_t *seg_tok_len;
+    const int32_t *seg_chunk_pos;
+    const uint64_t *seg_mask;
+    const int32_t *q_slot_off;
+    const int32_t *q_slot;
+    const int32_t *fma_items;
+    const int32_t *mma_items;
+    const int32_t *fallback_items;
+    int32_t num_fma_items;
+    int32_t num_mma_items;
+    int32_t num_fallback_items;
+    int32_t num_slots;
+    int32_t num_queries;
+    int32_t mask_words;
+};
+
+}  // namespace deft
+
+struct deft_plan_t {
+    int32_t num_nodes = 0;
+    int32_t num_queries = 0;
+    int32_t gqa_group = 1;
+    int32_t chunk_target = 0;
+    int32_t mask_words = 0;
+    std::vector<uint64_t> cover;   // [N * W]
+    std::vector<int32_t> order;    // DFS preorder of all nodes
+    deft::Partition tree;
+    deft::Partition naive;
+    deft_plan_stats stats{};
+    // Device copy (deft_plan_upload).
+    void *dev_blob = nullptr;
+    size_t dev_bytes = 0;
+    int dev_device = -1;
+    bool uploaded = false;
+    deft::DevPartition dev_tree{};
+    deft::DevPartition dev_naive{};
+};
+
+namespace deft {
+
+// planner.cpp
+int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+               const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
+               int32_t gqa_group, deft_plan_t *plan);
+
+// Arguments every phase-1 kernel receives.
+struct AttnArgs {
+    const void *q;            // bf16 [Q][Hq][d]
+    const void *k_pages;      // bf16 [pages][Hkv][P][d]
+    const void *v_pages;
+    const int32_t *node_page_off;
+    const int32_t *page_id;
+    int32_t num_pages;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t gqa_group;
+    float scale_log2;         // scale * log2(e): logits are kept in base 2 on device
+    float *o_part;            // fp32 [slots][Hq][d]
+    float *lse_part;          // fp32 [slots][Hq], base-2 log-sum-exp of the base-2 logits
+};
+
+// Launchers (return a cudaError_t cast to int; 0 = success).
+int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items,
+                      const int32_t *bucket_off, void *stream);
+int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, void *stream);
+// Row bucket of an item with `rows` rows: smallest b with rows <= 2^b.
+inline int row_bucket(int rows) { return rows <= 1 ? 0 : rows <= 2 ? 1 : rows <= 4 ? 2 : rows <= 8 ? 3 : 4; }
+int launch_phase2(const AttnArgs &a, const DevPartition &p, void *out, int32_t out_dtype,
+                  float *lse, void *stream);
+bool mma_supported(int32_t head_dim);
+
+}  // namespace deft

@@ -1,0 +1,347 @@
+// planner.cpp -- host tree planner: validation, coverage bitsets, DFS
+// flattening, segment/chunk construction and work items.
+//
+// KV-Guided Grouping (DeFT abstract; DeFT Guide, "The DeFT Architecture",
+// item 1): work is grouped by KV, not by query.  A node's KV is read once
+// for every query whose root-to-node path contains it; the set of those
+// queries is the node's coverage bitset, and a chunk lists the union of its
+// segments' sets.
+//
+// Flattened Tree KV Splitting (DeFT abstract; Guide, item 2, where chunks of
+// B_KV = 128 tokens are the example): the tree is flattened into one token
+// sequence (DFS preorder) and cut into chunks of roughly equal size.  Here a
+// chunk is made of segments, each a token range of a single node, so that the
+// per-segment query set is exact.  Readings taken where the pages are silent:
+//   * Order: roots by ascending id, each subtree in preorder with children by
+//     ascending id.  The order changes only the partition, never a result.
+//   * Short nodes (at most chunk_target / 2 tokens) are packed, in preorder,
+//     into chunks of at most chunk_target tokens and at most
+//     kMaxSegsPerChunk segments.
+//   * A longer node is cut into equal page-aligned pieces of about
+//     T = max(chunk_target, kSharedTokensPerRow * rows) tokens, rows being
+//     |cover| * gqa_group.  Each (chunk, query, head) writes one fp32
+//     partial of head_dim + 1 values, so keeping T >= 16 rows bounds the
+//     partial-result write plus read to about 1/8 of the chunk's KV bytes.
+//     (The Guide's claim that partials vanish entirely, section "Fused
+//     In-SRAM Online Softmax Merging", is read as "made small", which is what
+//     the abstract's "nearly 100% IO reduction for partial results" says.)
+//   * Nodes with no token or no query on them produce no segment.
+#include <algorithm>
+#include <cstring>
+#include <numeric>
+
+#include "deft_internal.h"
+
+namespace deft {
+namespace {
+
+int popcount_words(const uint64_t *w, int32_t words)
+{
+    int c = 0;
+    for (int32_t i = 0; i < words; ++i)
+        c += __builtin_popcountll(w[i]);
+    return c;
+}
+
+struct Builder {
+    Partition &p;
+    int32_t W;
+    int32_t cur_chunk_tokens = 0;
+    int32_t cur_chunk_segs = 0;
+    bool open = false;
+    std::vector<uint64_t> cur_mask;
+
+    Builder(Partition &part, int32_t words) : p(part), W(words), cur_mask(words, 0)
+    {
+        p.chunk_seg_off.push_back(0);
+    }
+    void close()
+    {
+        if (!open)
+            return;
+        p.chunk_seg_off.push_back((int32_t)p.seg_node.size());
+        p.chunk_tokens.push_back(cur_chunk_tokens);
+        p.chunk_mask.insert(p.chunk_mask.end(), cur_mask.begin(), cur_mask.end());
+        std::fill(cur_mask.begin(), cur_mask.end(), 0);
+        cur_chunk_tokens = 0;
+        cur_chunk_segs = 0;
+        open = false;
+    }
+    void add_segment(int32_t node, int32_t begin, int32_t len, const uint64_t *mask)
+    {
+        open = true;
+        p.seg_node.push_back(node);
+        p.seg_tok_begin.push_back(begin);
+        p.seg_tok_len.push_back(len);
+        p.seg_chunk_pos.push_back(cur_chunk_tokens);
+        p.seg_mask.insert(p.seg_mask.end(), mask, mask + W);
+        for (int32_t i = 0; i < W; ++i)
+            cur_mask[i] |= mask[i];
+        cur_chunk_tokens += len;
+        cur_chunk_segs += 1;
+    }
+};
+
+// Query lists, slot lists and work items of a finished partition.
+void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
+{
+    const int32_t C = p.num_chunks();
+    p.chunk_q_off.assign(1, 0);
+    p.chunk_q.clear();
+    for (int32_t c = 0; c < C; ++c) {
+        const uint64_t *m = &p.chunk_mask[(size_t)c * W];
+        for (int32_t q = 0; q < num_queries; ++q)
+            if ((m[q / 64] >> (q % 64)) & 1ull)
+                p.chunk_q.push_back(q);
+        p.chunk_q_off.push_back((int32_t)p.chunk_q.size());
+    }
+    // Per-query slot CSR, slots in chunk order.
+    std::vector<int32_t> cnt(num_queries + 1, 0);
+    for (int32_t s = 0; s < p.num_slots(); ++s)
+        cnt[p.chunk_q[s] + 1] += 1;
+    p.q_slot_off.assign(num_queries + 1, 0);
+    for (int32_t q = 0; q < num_queries; ++q)
+        p.q_slot_off[q + 1] = p.q_slot_off[q] + cnt[q + 1];
+    p.q_slot.assign(p.num_slots(), 0);
+    std::vector<int32_t> fill(p.q_slot_off.begin(), p.q_slot_off.end() - 1);
+    for (int32_t s = 0; s < p.num_slots(); ++s)
+        p.q_slot[fill[p.chunk_q[s]]++] = s;
+
+    // Work items.  rows = queries * G.  Chunks under kMmaMinRows rows run on
+    // the CUDA-core kernel in one item; the others run on the tensor-core
+    // kernel in row blocks of at most kMmaMaxRows rows, and are also cut into
+    // items of at most kFmaMaxRows rows for head sizes without a tensor path.
+    struct Item { int32_t c, b, e; int64_t cost; int32_t bucket = 0; };
+    std::vector<Item> fma, mma, fb;
+    const int32_t qmax_mma = std::max(1, kMmaMaxRows / G);
+    const int32_t qmax_fb = std::max(1, kFmaMaxRows / G);
+    for (int32_t c = 0; c < C; ++c) {
+        const int32_t k = p.chunk_q_off[c + 1] - p.chunk_q_off[c];
+        const int64_t tok = p.chunk_tokens[c];
+        if ((int64_t)k * G < kMmaMinRows) {
+            fma.push_back({c, 0, k, tok, row_bucket(k * G)});
+            continue;
+        }
+        const int32_t nb = (k + qmax_mma - 1) / qmax_mma;
+        const int32_t per = (k + nb - 1) / nb;
+        for (int32_t b = 0; b < k; b += per)
+            mma.push_back({c, b, std::min(k, b + per), tok * (std::min(k, b + per) - b)});
+        const int32_t nf = (k + qmax_fb - 1) / qmax_fb;
+        const int32_t perf = (k + nf - 1) / nf;
+        for (int32_t b = 0; b < k; b += perf)
+            fb.push_back({c, b, std::min(k, b + perf), tok * (std::min(k, b + perf) - b),
+                          row_bucket((std::min(k, b + perf) - b) * G)});
+    }
+    // Largest first, so the hardware block scheduler starts the long items
+    // early (a longest-processing-time order).
+    auto by_cost = [](const Item &x, const Item &y) {
+        if (x.bucket != y.bucket)
+            return x.bucket < y.bucket;
+        return x.cost != y.cost ? x.cost > y.cost : (x.c != y.c ? x.c < y.c : x.b < y.b);
+    };
+    auto bucket_offsets = [](const std::vector<Item> &v, std::array<int32_t, 6> &off) {
+        off.fill(0);
+        for (const Item &it : v)
+            off[it.bucket + 1] += 1;
+        for (int b = 0; b < 5; ++b)
+            off[b + 1] += off[b];
+    };
+    std::stable_sort(fma.begin(), fma.end(), by_cost);
+    std::stable_sort(mma.begin(), mma.end(), by_cost);
+    std::stable_sort(fb.begin(), fb.end(), by_cost);
+    auto emit = [](const std::vector<Item> &v, std::vector<int32_t> &out) {
+        out.clear();
+        for (const Item &it : v) {
+            out.push_back(it.c);
+            out.push_back(it.b);
+            out.push_back(it.e);
+        }
+    };
+    emit(fma, p.fma_items);
+    emit(mma, p.mma_items);
+    emit(fb, p.fallback_items);
+    bucket_offsets(fma, p.fma_bucket_off);
+    bucket_offsets(fb, p.fallback_bucket_off);
+}
+
+}  // namespace
+
+int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+               const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
+               int32_t gqa_group, deft_plan_t *plan)
+{
+    if (!parent || !node_len || !plan || num_nodes < 1 || num_queries < 0 ||
+        (num_queries > 0 && !query_node))
+        return DEFT_EINVAL;
+    if (chunk_target < 1 || chunk_target > kMaxChunkTarget || gqa_group < 1 || gqa_group > 128)
+        return DEFT_EINVAL;
+    const int32_t N = num_nodes, Q = num_queries;
+    for (int32_t n = 0; n < N; ++n) {
+        if (parent[n] < -1 || parent[n] >= N)
+            return DEFT_ERANGE;
+        if (node_len[n] < 0)
+            return DEFT_EINVAL;
+    }
+    for (int32_t q = 0; q < Q; ++q)
+        if (query_node[q] < 0 || query_node[q] >= N)
+            return DEFT_ERANGE;
+
+    // Forest check by colouring: 0 unseen, 1 on the current upward walk, 2 done.
+    {
+        std::vector<uint8_t> colour(N, 0);
+        std::vector<int32_t> walk;
+        for (int32_t n = 0; n < N; ++n) {
+            int32_t cur = n;
+            walk.clear();
+            while (cur != -1 && colour[cur] == 0) {
+                colour[cur] = 1;
+                walk.push_back(cur);
+                cur = parent[cur];
+            }
+            if (cur != -1 && colour[cur] == 1)
+                return DEFT_ECYCLE;
+            for (int32_t x : walk)
+                colour[x] = 2;
+        }
+    }
+
+    const int32_t W = (Q + 63) / 64;
+    plan->num_nodes = N;
+    plan->num_queries = Q;
+    plan->gqa_group = gqa_group;
+    plan->chunk_target = chunk_target;
+    plan->mask_words = W;
+
+    // Coverage bitsets: walk every query's path.
+    plan->cover.assign((size_t)N * W, 0);
+    int64_t naive_tokens = 0;
+    for (int32_t q = 0; q < Q; ++q)
+        for (int32_t cur = query_node[q]; cur != -1; cur = parent[cur]) {
+            plan->cover[(size_t)cur * W + q / 64] |= 1ull << (q % 64);
+            naive_tokens += node_len[cur];
+        }
+
+    // Children lists (ascending ids) and DFS preorder.
+    std::vector<int32_t> child_off(N + 1, 0), child(N > 0 ? N : 1);
+    for (int32_t n = 0; n < N; ++n)
+        if (parent[n] >= 0)
+            child_off[parent[n] + 1] += 1;
+    for (int32_t n = 0; n < N; ++n)
+        child_off[n + 1] += child_off[n];
+    {
+        std::vector<int32_t> fill(child_off.begin(), child_off.end() - 1);
+        for (int32_t n = 0; n < N; ++n)
+            if (parent[n] >= 0)
+                child[fill[parent[n]]++] = n;
+    }
+    plan->order.clear();
+    {
+        std::vector<int32_t> stack;
+        for (int32_t r = N - 1; r >= 0; --r)
+            if (parent[r] == -1)
+                stack.push_back(r);
+        while (!stack.empty()) {
+            int32_t n = stack.back();
+            stack.pop_back();
+            plan->order.push_back(n);
+            for (int32_t i = child_off[n + 1] - 1; i >= child_off[n]; --i)
+                stack.push_back(child[i]);
+        }
+    }
+
+    // DeFT partition.
+    plan->tree = Partition();
+    int64_t unique_tokens = 0;
+    {
+        Builder b(plan->tree, W);
+        for (int32_t n : plan->order) {
+            const int32_t L = node_len[n];
+            const uint64_t *m = &plan->cover[(size_t)n * W];
+            const int k = popcount_words(m, W);
+            if (L == 0 || k == 0)
+                continue;
+            unique_tokens += L;
+            if (2 * (int64_t)L <= chunk_target) {
+                if (b.open && (b.cur_chunk_tokens + L > chunk_target ||
+                               b.cur_chunk_segs >= kMaxSegsPerChunk))
+                    b.close();
+                b.add_segment(n, 0, L, m);
+                continue;
+            }
+            b.close();
+            int64_t T = std::max<int64_t>(chunk_target, (int64_t)kSharedTokensPerRow * k * gqa_group);
+            T = (T + kPageSize - 1) / kPageSize * kPageSize;
+            const int64_t pieces = (L + T - 1) / T;
+            int64_t piece = (L + pieces - 1) / pieces;
+            piece = (piece + kPageSize - 1) / kPageSize * kPageSize;
+            for (int64_t s = 0; s < L; s += piece) {
+                b.add_segment(n, (int32_t)s, (int32_t)std::min<int64_t>(piece, L - s), m);
+                b.close();
+            }
+        }
+        b.close();
+    }
+    finish_partition(plan->tree, Q, W, gqa_group);
+
+    // Naive partition: each query's path (root first) cut every chunk_target
+    // tokens; every chunk serves that one query.
+    plan->naive = Partition();
+    {
+        Builder b(plan->naive, W);
+        std::vector<int32_t> path;
+        std::vector<uint64_t> m(W, 0);
+        for (int32_t q = 0; q < Q; ++q) {
+            path.clear();
+            for (int32_t cur = query_node[q]; cur != -1; cur = parent[cur])
+                path.push_back(cur);
+            std::reverse(path.begin(), path.end());
+            std::fill(m.begin(), m.end(), 0);
+            m[q / 64] = 1ull << (q % 64);
+            for (int32_t n : path) {
+                int32_t t = 0;
+                while (t < node_len[n]) {
+                    if (b.open && (b.cur_chunk_tokens == chunk_target ||
+                                   b.cur_chunk_segs >= kMaxSegsPerChunk))
+                        b.close();
+                    const int32_t take = std::min(node_len[n] - t, chunk_target - b.cur_chunk_tokens);
+                    b.add_segment(n, t, take, m.data());
+                    t += take;
+                }
+            }
+            b.close();
+        }
+    }
+    finish_partition(plan->naive, Q, W, gqa_group);
+
+    // Statistics.
+    deft_plan_stats &st = plan->stats;
+    std::memset(&st, 0, sizeof st);
+    st.num_nodes = N;
+    st.num_queries = Q;
+    st.gqa_group = gqa_group;
+    st.chunk_target = chunk_target;
+    st.mask_words = W;
+    st.num_chunks = plan->tree.num_chunks();
+    st.num_segments = plan->tree.num_segments();
+    st.num_slots = plan->tree.num_slots();
+    st.num_fma_items = (int32_t)plan->tree.fma_items.size() / 3;
+    st.num_mma_items = (int32_t)plan->tree.mma_items.size() / 3;
+    st.num_fallback_items = (int32_t)plan->tree.fallback_items.size() / 3;
+    for (int32_t c = 0; c < st.num_chunks; ++c) {
+        st.max_chunk_tokens = std::max(st.max_chunk_tokens, plan->tree.chunk_tokens[c]);
+        st.planned_tokens += plan->tree.chunk_tokens[c];
+        st.pair_tokens += (int64_t)plan->tree.chunk_tokens[c] *
+                          (plan->tree.chunk_q_off[c + 1] - plan->tree.chunk_q_off[c]);
+    }
+    for (int32_t q = 0; q < Q; ++q)
+        st.max_slots_per_query = std::max(st.max_slots_per_query,
+                                          plan->tree.q_slot_off[q + 1] - plan->tree.q_slot_off[q]);
+    st.naive_num_chunks = plan->naive.num_chunks();
+    st.naive_num_slots = plan->naive.num_slots();
+    st.naive_num_segments = plan->naive.num_segments();
+    st.unique_tokens = unique_tokens;
+    st.naive_tokens = naive_tokens;
+    return DEFT_OK;
+}
+
+}  // namespace deft

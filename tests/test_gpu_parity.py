@@ -1,0 +1,199 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances (stated for bf16 inputs, fp32 accumulation): max-abs error 1e-2
+on outputs, 1e-3 on lse; bit-exact integer plan (checked without a GPU in
+test_plan.py).  Unused KV slots are NaN-poisoned, so a kernel that reads a
+slot past a node's last token fails here."""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+from helpers import dense_inputs, run_oracle
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def deft():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import shared_prefix_kv_deft_gb300 as d
+    from shared_prefix_kv_deft_gb300 import build
+    build.build()
+    d.load()
+    return d
+
+
+def bits_to_cuda(b: np.ndarray):
+    return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+class Case:
+    """Device copies of one input set plus its plan."""
+
+    def __init__(self, deft, inp, chunk_target):
+        self.inp, self.spec = inp, inp.spec
+        self.q = bits_to_cuda(inp.q_bits)
+        self.k = bits_to_cuda(inp.k_pages)
+        self.v = bits_to_cuda(inp.v_pages)
+        self.npo = torch.from_numpy(inp.layout.node_page_off).cuda()
+        self.pid = torch.from_numpy(inp.layout.page_id).cuda()
+        s = self.spec
+        self.plan = deft.Plan(s.parent, s.node_len, s.query_node, chunk_target, s.gqa_group)
+        self.plan.upload()
+        self.deft = deft
+
+    def run(self, naive=False, out_dtype=0):
+        fn = self.deft.deft_naive_attn if naive else self.deft.deft_tree_attn
+        out, lse = fn(self.q, self.k, self.v, self.npo, self.pid, self.plan, out_dtype=out_dtype)
+        torch.cuda.synchronize()
+        return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def assert_parity(out, lse, ref, ref_lse, what=""):
+    assert np.isfinite(out).all(), f"{what}: non-finite output (poisoned slot read?)"
+    err = np.abs(out - ref).max() if out.size else 0.0
+    assert err <= OUT_TOL, f"{what}: out max-abs error {err}"
+    np.testing.assert_array_equal(np.isneginf(lse), np.isneginf(ref_lse), err_msg=what)
+    fin = np.isfinite(ref_lse)
+    lerr = np.abs(lse[fin] - ref_lse[fin]).max() if fin.any() else 0.0
+    assert lerr <= LSE_TOL, f"{what}: lse max-abs error {lerr}"
+
+
+def small_shapes():
+    shapes = [W.tiny_tree()]
+    shapes += [W.random_tree(s, max_nodes=16, max_len=90, max_queries=12) for s in range(16)]
+    shapes += [W.random_tree(100 + s, max_nodes=20, max_len=200, max_queries=40, q_heads=8,
+                             kv_heads=2, head_dim=128) for s in range(8)]
+    # MHA with many queries sharing the root: chunks of >= 16 rows.
+    shapes += [W.random_tree(200 + s, max_nodes=10, max_len=300, max_queries=60, q_heads=2,
+                             kv_heads=2, head_dim=128, forest=False) for s in range(4)]
+    shapes += [
+        W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4, head_dim=128),
+        W.speculative_forest(requests=2, prefix=300, tree_nodes=64, heads=4),
+        W.reasoning_tree(levels=3, len_lo=20, len_hi=90, num_queries=24, q_heads=8, kv_heads=2),
+        W.imbalance_tree(prefix=700, leaves=24, lo=5, hi=400, q_heads=8, kv_heads=2),
+        W.imbalance_tree(leaves=12, control=True, control_len=150, q_heads=8, kv_heads=2),
+        W.chain_tree([5, 70, 1, 130], q_heads=4, kv_heads=4, head_dim=128),
+    ]
+    return shapes
+
+
+SMALL = small_shapes()
+
+
+@pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [16, 100, 256])
+def test_tree_and_naive_match_oracle(deft, spec, ct):
+    inp = dense_inputs(spec, seed=ct + spec.num_nodes)
+    ref, ref_lse = run_oracle(inp)
+    case = Case(deft, inp, ct)
+    out, lse = case.run()
+    assert_parity(out, lse, ref, ref_lse, f"tree ct={ct}")
+    out, lse = case.run(naive=True)
+    assert_parity(out, lse, ref, ref_lse, f"naive ct={ct}")
+
+
+def test_fp32_output(deft):
+    spec = W.reasoning_tree(levels=3, len_lo=20, len_hi=90, num_queries=24, q_heads=8, kv_heads=2)
+    inp = dense_inputs(spec, seed=5)
+    ref, ref_lse = run_oracle(inp)
+    out, lse = Case(deft, inp, 64).run(out_dtype=1)
+    assert_parity(out, lse, ref, ref_lse, "fp32 out")
+    assert np.abs(out - ref).max() < 2e-3
+
+
+def test_empty_paths_give_zero_and_minus_inf(deft):
+    spec = W.TreeSpec("empty", np.array([-1, 0, 0, -1], np.int32), np.array([0, 0, 37, 0], np.int32),
+                      np.array([0, 1, 2, 3, 2], np.int32), 4, 2, 128)
+    inp = dense_inputs(spec, seed=1)
+    ref, ref_lse = run_oracle(inp)
+    for naive in (False, True):
+        out, lse = Case(deft, inp, 16).run(naive=naive)
+        assert np.all(out[[0, 1, 3]] == 0) and np.all(np.isneginf(lse[[0, 1, 3]]))
+        assert_parity(out, lse, ref, ref_lse, "empty paths")
+
+
+def test_results_are_bitwise_repeatable(deft):
+    spec = W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4, head_dim=128)
+    case = Case(deft, dense_inputs(spec, seed=3), 64)
+    a = case.run()
+    b = case.run()
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_abi_rejects_bad_calls(deft):
+    spec = W.tiny_tree()
+    case = Case(deft, dense_inputs(spec, seed=2), 64)
+    lib = deft.load()
+    Q, Hq, d = case.q.shape
+    out = torch.empty((Q, Hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((Q, Hq), dtype=torch.float32, device="cuda")
+    ws_bytes = case.plan.workspace_bytes(Hq, d)
+    ws = torch.empty(ws_bytes + 512, dtype=torch.uint8, device="cuda")
+    P = ctypes.c_void_p
+
+    def call(plan=case.plan.handle, hq=Hq, hkv=4, hd=d, ps=16, wsp=ws.data_ptr(), wsb=ws_bytes,
+             scale=0.125, odt=0):
+        return lib.deft_tree_attn(P(case.q.data_ptr()), P(case.k.data_ptr()), P(case.v.data_ptr()),
+                                  P(case.npo.data_ptr()), P(case.pid.data_ptr()), case.k.shape[0],
+                                  hq, hkv, hd, ps, scale, plan, P(out.data_ptr()), odt,
+                                  P(lse.data_ptr()), P(wsp), wsb,
+                                  P(torch.cuda.current_stream().cuda_stream))
+    assert call() == 0
+    assert call(hkv=2) == -8           # GQA group differs from the plan's
+    assert call(hkv=3) == -1           # heads not a multiple
+    assert call(hd=96) == -5           # head_dim not compiled
+    assert call(ps=8) == -5            # page size
+    assert call(wsb=ws_bytes - 1) == -7
+    assert call(wsp=ws.data_ptr() + 16) == -7
+    assert call(scale=0.0) == -1
+    assert call(odt=7) == -1
+    unuploaded = deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, 1)
+    assert call(plan=unuploaded.handle) == -8
+    torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the benchmark times, with
+# the oracle evaluated on a sample of queries.
+# ---------------------------------------------------------------------------
+
+FULL = {2: 256, 3: 256, 4: 256, 5: 256, 6: 256, 1: 64}
+
+
+@pytest.mark.parametrize("cfg", sorted(FULL))
+def test_full_size_workloads_sampled(deft, cfg):
+    spec = W.config(cfg)
+    layout = W.paged_layout(spec)
+    t = W.make_tensors(spec, layout, device="cuda")
+    npo = torch.from_numpy(layout.node_page_off).cuda()
+    pid = torch.from_numpy(layout.page_id).cuda()
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, FULL[cfg], spec.gqa_group)
+    plan.upload()
+    out, lse = deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
+    nout, nlse = deft.deft_naive_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(cfg)
+    sample = np.unique(np.concatenate([[0, spec.num_queries - 1],
+                                       rng.choice(spec.num_queries, size=min(6, spec.num_queries),
+                                                  replace=False)]))
+    ref, ref_lse = oracle.tree_attn(W.bf16_bits(t.q), W.bf16_bits(t.k_pages), W.bf16_bits(t.v_pages),
+                                    layout.node_page_off, layout.page_id, layout.page_size,
+                                    spec.parent, spec.node_len, spec.query_node, spec.num_q_heads,
+                                    spec.num_kv_heads, spec.head_dim, 1.0 / math.sqrt(spec.head_dim),
+                                    query_subset=sample)
+    for o, l, what in ((out, lse, "tree"), (nout, nlse, "naive")):
+        o = o.float().cpu().numpy().astype(np.float64)
+        l = l.cpu().numpy().astype(np.float64)
+        assert np.isfinite(o).all() and np.isfinite(l).all(), what
+        assert_parity(o[sample], l[sample], ref, ref_lse, f"config {cfg} {what}")

@@ -1,0 +1,233 @@
+"""Host planner and C-ABI checks (no GPU).
+
+The planner's integer outputs are compared bit-exactly with the oracle's
+independent coverage bitsets and token counts, and its chunks are expanded
+into (query, node, token) triples that must cover every query's path exactly
+once (KV-Guided Grouping + Flattened Tree KV Splitting: DeFT abstract; DeFT
+Guide, "The DeFT Architecture")."""
+import ctypes
+import os
+import re
+from collections import defaultdict
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+deft = pytest.importorskip("shared_prefix_kv_deft_gb300")
+from shared_prefix_kv_deft_gb300 import build as deft_build  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    deft_build.build()
+    deft.load()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "deft.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|void|const char \*)\s*(deft_\w+)\s*\(", src, re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = deft.load()
+    names = header_functions()
+    assert set(names) == set(deft.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), f"libdeft.so does not export {n}"
+    assert deft.version() == 100
+
+
+@pytest.mark.parametrize("parent,node_len,query,ct,g,status", [
+    ([1, 0], [3, 3], [0], 64, 1, -2),            # cycle
+    ([-1, 0, 1, 2, 1], [1, 1, 1, 1, 1], [4], 64, 1, 0),
+    ([-1, 5], [3, 3], [0], 64, 1, -3),           # parent out of range
+    ([-1, -2], [3, 3], [0], 64, 1, -3),          # parent below -1
+    ([-1, 0], [3, -1], [0], 64, 1, -1),          # negative length
+    ([-1, 0], [3, 3], [2], 64, 1, -3),           # query node out of range
+    ([-1, 0], [3, 3], [1], 0, 1, -1),            # chunk_target 0
+    ([-1, 0], [3, 3], [1], 9000, 1, -1),         # chunk_target too large
+    ([-1, 0], [3, 3], [1], 64, 0, -1),           # GQA group 0
+    ([0], [3], [0], 64, 1, -2),                  # self loop
+])
+def test_plan_validation(parent, node_len, query, ct, g, status):
+    lib = deft.load()
+    p = np.array(parent, np.int32)
+    L = np.array(node_len, np.int32)
+    qn = np.array(query, np.int32)
+    h = ctypes.c_void_p()
+    rc = lib.deft_plan(p.ctypes.data_as(ctypes.c_void_p), L.ctypes.data_as(ctypes.c_void_p),
+                       len(parent), qn.ctypes.data_as(ctypes.c_void_p), len(query), ct, g,
+                       ctypes.byref(h))
+    assert rc == status
+    if rc == 0:
+        lib.deft_plan_free(h)
+    else:
+        assert not h.value
+
+
+def check_plan(spec: W.TreeSpec, chunk_target: int, G: int):
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, chunk_target, G)
+    st = plan.stats
+    Q, N = spec.num_queries, spec.num_nodes
+    Wd = (Q + 63) // 64
+    cover = oracle.cover(spec.parent, spec.query_node)
+    uniq, naive = oracle.token_counts(spec.parent, spec.node_len, spec.query_node)
+    paths = oracle.paths(spec.parent, spec.query_node)
+
+    # Bit-exact coverage bitsets and token counts.
+    np.testing.assert_array_equal(plan.get("node_cover").reshape(N, Wd), cover)
+    assert st["unique_tokens"] == uniq and st["planned_tokens"] == uniq
+    assert st["naive_tokens"] == naive
+    order = plan.get("node_order")
+    assert sorted(order.tolist()) == list(range(N))
+
+    def bits(words):
+        return [q for q in range(Q) if (int(words[q // 64]) >> (q % 64)) & 1]
+
+    def check_partition(prefix, chunk_limit, naive_part):
+        seg_off = plan.get(prefix + "chunk_seg_off")
+        chunk_q = plan.get(prefix + "chunk_q")
+        seg_node = plan.get(prefix + "seg_node")
+        seg_b = plan.get(prefix + "seg_tok_begin")
+        seg_l = plan.get(prefix + "seg_tok_len")
+        q_off = plan.get(prefix + "q_slot_off")
+        q_slot = plan.get(prefix + "q_slot")
+        C = len(seg_off) - 1
+        if naive_part:
+            chunk_q_off = np.arange(C + 1)
+            seg_mask = None
+        else:
+            chunk_q_off = plan.get("chunk_q_off")
+            seg_mask = plan.get("seg_mask").reshape(-1, Wd)
+            chunk_mask = plan.get("chunk_mask").reshape(-1, Wd)
+        assert len(chunk_q) == chunk_q_off[-1]
+        intervals = defaultdict(list)
+        for c in range(C):
+            qs = chunk_q[chunk_q_off[c]:chunk_q_off[c + 1]].tolist()
+            assert qs == sorted(set(qs)) and len(qs) > 0
+            if naive_part:
+                assert len(qs) == 1
+            tok = 0
+            union = set()
+            nseg = seg_off[c + 1] - seg_off[c]
+            assert nseg >= 1
+            for s in range(seg_off[c], seg_off[c + 1]):
+                n, b, L = int(seg_node[s]), int(seg_b[s]), int(seg_l[s])
+                assert L > 0 and 0 <= b and b + L <= spec.node_len[n]
+                tok += L
+                if naive_part:
+                    sq = qs
+                else:
+                    # A segment's bitmask is exactly its node's coverage set.
+                    np.testing.assert_array_equal(seg_mask[s], cover[n])
+                    sq = bits(seg_mask[s])
+                union |= set(sq)
+                for q in sq:
+                    intervals[(q, n)].append((b, L))
+            assert union == set(qs)
+            if not naive_part:
+                assert bits(chunk_mask[c]) == qs
+                if nseg > 1:
+                    assert tok <= chunk_limit and nseg <= 256
+            else:
+                assert tok <= chunk_limit
+        # Exactly once: every (query, node on its path, token) in one chunk.
+        expected = {(q, n) for q in range(Q) for n in paths[q] if spec.node_len[n] > 0}
+        assert set(intervals) == expected
+        for (q, n), iv in intervals.items():
+            iv.sort()
+            pos = 0
+            for b, L in iv:
+                assert b == pos, f"gap/overlap at query {q} node {n}"
+                pos = b + L
+            assert pos == spec.node_len[n]
+        # Slot CSR: slot s of chunk_q belongs to query chunk_q[s].
+        for q in range(Q):
+            sl = q_slot[q_off[q]:q_off[q + 1]].tolist()
+            assert sl == [s for s in range(len(chunk_q)) if chunk_q[s] == q]
+        return C, chunk_q_off, chunk_q
+
+    C, cqo, _ = check_partition("", chunk_target, False)
+    check_partition("naive_", chunk_target, True)
+    assert st["num_chunks"] == C
+
+    # Work items: each chunk's query list covered once per family.
+    def item_cover(name):
+        it = plan.get(name).reshape(-1, 3)
+        cov = defaultdict(list)
+        for c, b, e in it:
+            assert 0 <= b < e <= cqo[c + 1] - cqo[c]
+            cov[int(c)].append((int(b), int(e)))
+        return it, cov
+
+    fma, fcov = item_cover("fma_items")
+    mma, mcov = item_cover("mma_items")
+    fb, bcov = item_cover("fallback_items")
+    for c in range(C):
+        k = cqo[c + 1] - cqo[c]
+        if k * G < 16:
+            assert fcov[c] == [(0, k)] and c not in mcov and c not in bcov
+        else:
+            for fam, cap in ((mcov, 128), (bcov, 16)):
+                iv = sorted(fam[c])
+                pos = 0
+                for b, e in iv:
+                    assert b == pos and (e - b) * G <= max(cap, G)
+                    pos = e
+                assert pos == k
+    for it in (fma, fb):   # sorted by row bucket
+        rows = [(e - b) * G for _, b, e in it]
+        buckets = [0 if r <= 1 else 1 if r <= 2 else 2 if r <= 4 else 3 if r <= 8 else 4 for r in rows]
+        assert buckets == sorted(buckets)
+    return plan
+
+
+RANDOM = [W.random_tree(s, max_nodes=40, max_len=300, max_queries=90) for s in range(40)]
+
+
+@pytest.mark.parametrize("spec", RANDOM, ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [1, 16, 100, 512])
+def test_plan_random_trees(spec, ct):
+    check_plan(spec, ct, spec.gqa_group)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6])
+def test_plan_workload_shapes(cfg):
+    spec = W.config(cfg)
+    plan = check_plan(spec, 256, spec.gqa_group)
+    st = plan.stats
+    if cfg == 2:
+        assert st["unique_tokens"] == 4096 + 32 * 256
+        assert st["naive_tokens"] == 32 * (4096 + 256)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_plan_relabelled_tree_has_the_same_coverage(seed):
+    spec = W.random_tree(900 + seed, max_nodes=30, max_queries=40)
+    perm = np.random.default_rng(seed).permutation(spec.num_nodes)
+    check_plan(W.relabel(spec, perm), 64, 2)
+
+
+def test_plan_worked_example_counts():
+    spec = W.heap_example_tree()
+    plan = check_plan(spec, 64, 1)
+    assert plan.stats["unique_tokens"] == 1040
+    assert plan.stats["naive_tokens"] == 16 * 1024 + 54
+
+
+def test_plan_is_deterministic():
+    spec = W.config(4)
+    a = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, 4)
+    b = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, 4)
+    for name in deft.ARRAYS:
+        np.testing.assert_array_equal(a.get(name), b.get(name))
+
+
+def test_empty_query_list_plans():
+    plan = deft.Plan([-1, 0], [5, 5], [], 64, 1)
+    assert plan.stats["num_chunks"] == 0 and plan.stats["num_slots"] == 0

@@ -1,0 +1,487 @@
+#!/usr/bin/env python
+"""Benchmark of one DeFT tree-attention decode step on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl deft|reference]
+
+A step is one pass of the whole hot path (phase-1 partial attention over all
+chunks + phase-2 LSE merge) on one synthetic tree whose KV cache and queries
+are already resident in HBM.  The default workload is the shared-prefix
+few-shot decode tree (4096-token prefix, 32 branches of 256 tokens, one
+query per branch tip, 32 query / 32 KV heads, head_dim 128, bf16); other
+shapes via --config 1..6.  The L2 cache is flushed (a 2 x L2 memset)
+between timed steps, outside the timed events.
+
+Prints one JSON line (rank 0).  `value` is microseconds per step (lower is
+better); for N > 1 the ranks run independent replicas and `value` is the
+whole job's time per step (max over ranks of the timed region / (K * N)).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "tree-attention µs/step; achieved HBM GB/s vs unique-KV-bytes roofline"
+SPEC_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--chunk-target", type=int, default=256)
+    ap.add_argument("--impl", choices=["deft", "reference"], default="deft")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the naive, e2e and CPU-baseline legs")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", FALLBACK_HBM_GBS)), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic bytes (no re-reads counted): what one launch must move at least.
+# ---------------------------------------------------------------------------
+
+def algorithmic_bytes(plan, spec, family="tree"):
+    """Per-launch algorithmic bytes, keyed like the trace records."""
+    d, Hq, Hkv = spec.head_dim, spec.num_q_heads, spec.num_kv_heads
+    kv_tok = 2 * Hkv * d * 2                      # K + V bytes of one token, all KV heads
+    part_row = (d + 1) * 4                        # one fp32 partial (o and lse)
+    pre = "" if family == "tree" else "naive_"
+    seg_off = plan.get(pre + "chunk_seg_off")
+    seg_len = plan.get(pre + "seg_tok_len")
+    tok = np.add.reduceat(seg_len, seg_off[:-1]) if len(seg_len) else np.zeros(0, np.int64)
+    G = spec.gqa_group
+    out = {}
+    if family == "tree":
+        fams = {(0, 0): plan.get("fma_items").reshape(-1, 3),
+                (1, 0): plan.get("mma_items").reshape(-1, 3),
+                (0, 1): plan.get("fallback_items").reshape(-1, 3)}
+    else:
+        fams = {(0, 0): np.zeros((0, 3), np.int32)}
+    for (kern, fb), items in fams.items():
+        if len(items) == 0:
+            continue
+        rows = (items[:, 2] - items[:, 1]) * G
+        if kern == 1:
+            groups = {0: np.ones(len(items), bool)}
+        else:
+            b = np.select([rows <= 1, rows <= 2, rows <= 4, rows <= 8], [0, 1, 2, 3], 4)
+            groups = {int(x): b == x for x in np.unique(b)}
+        for bucket, sel in groups.items():
+            chunks = np.unique(items[sel, 0])
+            kv = int(tok[chunks].sum()) * kv_tok
+            q = int(rows[sel].sum()) * Hkv * d * 2
+            part = int(rows[sel].sum()) * Hkv * part_row
+            out[(kern, bucket, fb)] = {"kv": kv, "q": q, "partials": part, "total": kv + q + part}
+    return out
+
+
+def phase2_bytes(plan, spec, family="tree"):
+    d, Hq = spec.head_dim, spec.num_q_heads
+    slots = plan.stats["num_slots" if family == "tree" else "naive_num_slots"]
+    Q = spec.num_queries
+    return slots * Hq * (d + 1) * 4 + Q * Hq * (d * 2 + 4) + (Q + 1 + slots) * 4
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        sel = []
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            sel = ["-i", vis.split(",")[device_index] if vis else str(device_index)]
+        self.sel = sel
+        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                    "-lms", "50"]
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(self.cmd, stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2].split()[0]), float(parts[3].split()[0]),
+                             parts[4], parts[6:10]))
+            except (ValueError, IndexError):
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "whole run (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[4]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window, "gpu": " ".join(self.sel)}
+
+
+# ---------------------------------------------------------------------------
+# ncu summary (committed under profiles/) for the roofline's traffic figure
+# ---------------------------------------------------------------------------
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "shared_prefix_kv_deft_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, cfg: int):
+    """DRAM bytes per launch from profiles/ncu_traffic.json, or None when no
+    capture exists for this kernel/workload or the sources changed since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    ent = d.get(f"config{cfg}", {}).get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the fp64 CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def host_inputs(spec, layout, t):
+    return (W.bf16_bits(t.q), W.bf16_bits(t.k_pages), W.bf16_bits(t.v_pages))
+
+
+def oracle_step(oracle, spec, layout, bits, subset):
+    return oracle.tree_attn(bits[0], bits[1], bits[2], layout.node_page_off, layout.page_id,
+                            layout.page_size, spec.parent, spec.node_len, spec.query_node,
+                            spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
+                            1.0 / math.sqrt(spec.head_dim), query_subset=subset)
+
+
+def cpu_baseline(spec, layout, bits, budget_s=12.0):
+    """Time the oracle, as it stands, on a bounded sample of the workload."""
+    import oracle
+    oracle.load()
+    Q = spec.num_queries
+    # Calibrate on one query, then size the sample to the budget.
+    t0 = time.perf_counter()
+    oracle_step(oracle, spec, layout, bits, [0])
+    per_q = max(time.perf_counter() - t0, 1e-6)
+    nq = int(max(1, min(Q, budget_s / 2 / per_q)))
+    subset = np.linspace(0, Q - 1, nq).astype(np.int32)
+    reps, spent = 0, 0.0
+    while spent < budget_s / 2 and reps < 50:
+        t0 = time.perf_counter()
+        oracle_step(oracle, spec, layout, bits, subset)
+        spent += time.perf_counter() - t0
+        reps += 1
+    us_per_step = spent / reps * (Q / nq) * 1e6
+    return {"value": us_per_step, "unit": "us/step", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": f"{nq} of {Q} queries x all {spec.num_q_heads} heads, {reps} run(s), "
+                      f"scaled to the full step"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    spec = W.config(args.config)
+    layout = W.paged_layout(spec)
+    t = W.make_tensors(spec, layout, device="cpu")
+    bits = host_inputs(spec, layout, t)
+    import oracle
+    oracle.load()
+    Q = spec.num_queries
+    t0 = time.perf_counter()
+    oracle_step(oracle, spec, layout, bits, [0])
+    per_q = max(time.perf_counter() - t0, 1e-6)
+    # Each step is a bounded sample sized so that the whole run takes a few minutes.
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    nq = int(max(1, min(Q, per_step / per_q)))
+    subset = np.linspace(0, Q - 1, nq).astype(np.int32)
+    for _ in range(args.warmup):
+        oracle_step(oracle, spec, layout, bits, subset)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(oracle, spec, layout, bits, subset)
+        times.append(time.perf_counter() - t0)
+    us = statistics.mean(times) * (Q / nq) * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/step",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec.name, "global_batch": Q, "parallelism": "host cores"},
+            "cpu_baseline": {"value": us, "unit": "us/step", "cores": oracle.max_threads(),
+                             "kind": "oracle",
+                             "sample": f"{nq} of {Q} queries x all heads per step, scaled"},
+            "e2e": {"value": us, "unit": "us/step", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import shared_prefix_kv_deft_gb300 as deft
+    deft.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    spec = W.config(args.config)
+    layout = W.paged_layout(spec)
+    t = W.make_tensors(spec, layout, device=dev)
+    npo = torch.from_numpy(layout.node_page_off).to(dev)
+    pid = torch.from_numpy(layout.page_id).to(dev)
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group)
+    plan.upload()
+    bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if pg is not None:
+            pg.barrier()
+
+    def timed(fn, n, trace=False):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        if trace:
+            deft.trace_read()
+            deft.trace_enable(True)
+        barrier()
+        w0 = time.time()
+        for i in range(n):
+            flush.zero_()
+            starts[i].record(stream)
+            fn()
+            ends[i].record(stream)
+        barrier()
+        w1 = time.time()
+        recs = []
+        if trace:
+            deft.trace_enable(False)
+            recs = deft.trace_read()
+        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+        return ms, recs, w0, w1
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    ms, _, w0, w1 = timed(step, args.steps)                # timed region: the value
+    clocks = sampler.summary(w0, w1)
+    sampler.stop()
+    tms, recs, _, _ = timed(step, args.steps, trace=True)  # per-kernel durations
+    elapsed = sum(ms)
+    if pg is not None:
+        tt = torch.tensor([elapsed], dtype=torch.float64, device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        elapsed = float(tt.item())
+    ms_per_step = elapsed / args.steps
+    value_us = ms_per_step * 1e3 / world
+
+    st = plan.stats
+    d, Hq, Hkv, Q = spec.head_dim, spec.num_q_heads, spec.num_kv_heads, spec.num_queries
+    unique_kv = st["unique_tokens"] * 2 * Hkv * d * 2
+    naive_kv = st["naive_tokens"] * 2 * Hkv * d * 2
+    hbm_peak, peak_kind = measured_peaks()
+
+    # Per-kernel durations and algorithmic bytes.
+    alg = algorithmic_bytes(plan, spec)
+    p2 = phase2_bytes(plan, spec)
+    per_step = len(recs) // max(1, args.steps)
+    kernels = {}
+    for r in recs:
+        if r["kernel"] == "phase2_merge":
+            key, ab = "phase2_merge", p2
+        else:
+            kk = 1 if r["kernel"] == "phase1_mma" else 0
+            key = f'{r["kernel"]}[bucket={r["bucket"]}{",fallback" if r["fallback"] else ""}]'
+            ab = alg.get((kk, r["bucket"] if kk == 0 else 0, r["fallback"]), {}).get("total", 0)
+        k = kernels.setdefault(key, {"launches": 0, "total_ms": 0.0, "alg_bytes": ab,
+                                     "items": r["items"]})
+        k["launches"] += 1
+        k["total_ms"] += r["ms"]
+    tot_ms = sum(k["total_ms"] for k in kernels.values()) or 1.0
+    for k in kernels.values():
+        k["avg_us"] = k["total_ms"] / k["launches"] * 1e3
+        k["share"] = k["total_ms"] / tot_ms
+        k["achieved_gbs"] = k["alg_bytes"] / (k["avg_us"] * 1e-6) / 1e9 if k["avg_us"] else None
+    dom_name = max(kernels, key=lambda n: kernels[n]["total_ms"]) if kernels else None
+    dom = kernels.get(dom_name, {})
+    traffic = ncu_traffic(dom_name, args.config) if dom_name else None
+    roofline = {"bound": "hbm", "kernel": dom_name,
+                "achieved": dom.get("achieved_gbs"), "peak": hbm_peak, "unit": "GB/s",
+                "frac": (dom.get("achieved_gbs") or 0) / hbm_peak, "traffic": traffic,
+                "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "alg_bytes_per_launch": dom.get("alg_bytes"),
+                "avg_launch_us": dom.get("avg_us")}
+    step_gbs = unique_kv / (ms_per_step * 1e-3) / 1e9
+
+    line = {
+        "metric": METRIC, "value": value_us, "unit": "us/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 Q/K/V, random-init; no dataset)",
+        "config": {"workload": spec.name, "config_index": args.config, "global_batch": Q * world,
+                   "seq_len": int(max(1, st["naive_tokens"] // max(1, Q))),
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "chunk_target": args.chunk_target, "l2": "flushed (2 x L2 memset) between timed steps",
+                   "q_heads": Hq, "kv_heads": Hkv, "head_dim": d},
+        "us_per_step_median": statistics.median(ms) * 1e3,
+        "us_per_step_p10": float(np.percentile(ms, 10)) * 1e3,
+        "us_per_step_p90": float(np.percentile(ms, 90)) * 1e3,
+        "unique_kv_bytes": unique_kv, "naive_kv_bytes": naive_kv,
+        "achieved_gbs_vs_unique_kv": step_gbs,
+        "frac_of_measured_hbm": step_gbs / hbm_peak, "frac_of_spec_8tbs": step_gbs / SPEC_HBM_GBS,
+        "roofline": roofline, "kernels": kernels,
+        "gpu_launches": per_step * args.steps,
+        "clocks": clocks,
+        "plan": {k: st[k] for k in ("num_chunks", "num_segments", "num_slots", "num_fma_items",
+                                    "num_mma_items", "num_fallback_items", "max_chunk_tokens")},
+    }
+
+    if not args.no_extras:
+        # In-run IO comparison: the per-query flash-decoding form.
+        def naive_step():
+            deft.deft_naive_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)
+        nk = max(3, min(args.steps, 200))
+        for _ in range(3):
+            naive_step()
+        nms, _, _, _ = timed(naive_step, nk)
+        line["naive"] = {"us_per_step": statistics.mean(nms) * 1e3, "steps": nk,
+                         "kv_bytes": naive_kv,
+                         "speedup_of_tree": statistics.mean(nms) / ms_per_step}
+        # End to end through the public API: host planning, plan upload, Q from
+        # pinned host memory, the step, out + lse back to pinned host memory.
+        q_host = t.q.cpu().pin_memory()
+        out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+        lse_host = torch.empty(bufs.lse.shape, dtype=bufs.lse.dtype).pin_memory()
+        q_dev = torch.empty_like(t.q)
+        ek = max(3, min(args.steps, 200))
+        e2e_t = []
+        for i in range(ek + 3):
+            barrier()
+            t0 = time.perf_counter()
+            p = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target,
+                          spec.gqa_group)
+            p.upload()
+            q_dev.copy_(q_host, non_blocking=True)
+            deft.deft_tree_attn(q_dev, t.k_pages, t.v_pages, npo, pid, p, bufs=bufs)
+            out_host.copy_(bufs.out, non_blocking=True)
+            lse_host.copy_(bufs.lse, non_blocking=True)
+            torch.cuda.synchronize(dev)
+            if i >= 3:
+                e2e_t.append(time.perf_counter() - t0)
+            del p
+        e2e_us = statistics.mean(e2e_t) * 1e6
+        if pg is not None:
+            tt = torch.tensor([e2e_us], dtype=torch.float64, device=dev)
+            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+            e2e_us = float(tt.item())
+        line["e2e"] = {"value": e2e_us / world, "unit": "us/step",
+                       "h2d_bytes_per_step": int(q_host.numel() * 2 + st["device_bytes"]),
+                       "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()
+                                                 + lse_host.numel() * 4),
+                       "includes": "host planning + plan upload + Q H2D + step + out/lse D2H",
+                       "steps": ek}
+        if rank == 0 and world == 1:
+            line["cpu_baseline"] = cpu_baseline(spec, layout, host_inputs(spec, layout, t))
+    if rank == 0:
+        print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -77,6 +77,7 @@ typedef struct deft_plan_stats {
     int64_t naive_tokens;        /* sum over queries of their path tokens               */
     int64_t planned_tokens;      /* sum of chunk lengths; equals unique_tokens          */
     int64_t pair_tokens;         /* sum over chunks of tokens * |Q_c| (incl. masked)    */
+    int64_t device_bytes;        /* size of the device copy deft_plan_upload makes      */
 } deft_plan_stats;
 
 /* Arrays a plan exposes through deft_plan_get (host copies, for tests and
@@ -191,6 +192,29 @@ int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
                     int32_t page_size, float scale, const deft_plan_t *plan, void *out,
                     int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes,
                     void *stream);
+
+/*
+ * Per-launch kernel timing, for measurement tools (no counterpart on the
+ * pages).  While enabled, every kernel launch made by deft_tree_attn and
+ * deft_naive_attn is bracketed by two CUDA events recorded on the launch
+ * stream.  deft_trace_read waits for those events, writes up to `cap`
+ * records (in launch order) to `out`, sets *count to the number written and
+ * forgets all pending records.  Events are created on first use and reused;
+ * the library is not thread-safe while tracing is on.
+ */
+typedef struct deft_trace_record {
+    int32_t kernel;   /* DEFT_K_* */
+    int32_t family;   /* 0 tree partition, 1 naive partition                  */
+    int32_t bucket;   /* row bucket b (rows <= 2^b) of a CUDA-core launch     */
+    int32_t fallback; /* 1 if the launch ran >= 16-row chunks on CUDA cores   */
+    int32_t items;    /* work items (grid = items * num_kv_heads for phase 1) */
+    float ms;         /* event-measured duration                              */
+} deft_trace_record;
+
+enum { DEFT_K_PHASE1_FMA = 0, DEFT_K_PHASE1_MMA = 1, DEFT_K_PHASE2 = 2 };
+
+int deft_trace_enable(int32_t on);
+int deft_trace_read(deft_trace_record *out, int32_t cap, int32_t *count);
 
 /* Free a plan and its device copy (the caller must ensure no kernel using it
  * is still running).  NULL is a no-op. */

@@ -39,7 +39,9 @@ ARRAYS = {
 # Symbols the header declares (checked by the tests).
 EXPORTS = ["deft_plan", "deft_plan_stats_get", "deft_plan_get", "deft_plan_upload",
            "deft_workspace_bytes", "deft_tree_attn", "deft_naive_attn", "deft_plan_free",
-           "deft_status_str", "deft_version"]
+           "deft_status_str", "deft_version", "deft_trace_enable", "deft_trace_read"]
+
+KERNEL_NAMES = {0: "phase1_fma", 1: "phase1_mma", 2: "phase2_merge"}
 
 
 class DeftError(RuntimeError):
@@ -48,13 +50,19 @@ class DeftError(RuntimeError):
         self.status = status
 
 
+class TraceRecord(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("family", ctypes.c_int32),
+                ("bucket", ctypes.c_int32), ("fallback", ctypes.c_int32),
+                ("items", ctypes.c_int32), ("ms", ctypes.c_float)]
+
+
 class PlanStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_nodes", "num_queries", "gqa_group", "chunk_target", "mask_words", "num_chunks",
         "num_segments", "num_slots", "num_fma_items", "num_mma_items", "num_fallback_items",
         "max_chunk_tokens", "max_slots_per_query", "naive_num_chunks", "naive_num_slots",
         "naive_num_segments")] + [(n, ctypes.c_int64) for n in (
-        "unique_tokens", "naive_tokens", "planned_tokens", "pair_tokens")]
+        "unique_tokens", "naive_tokens", "planned_tokens", "pair_tokens", "device_bytes")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -87,8 +95,11 @@ def load(path: str = LIB_PATH):
     lib.deft_status_str.argtypes = [ctypes.c_int]
     lib.deft_status_str.restype = ctypes.c_char_p
     lib.deft_version.argtypes = []
+    lib.deft_trace_enable.argtypes = [i32]
+    lib.deft_trace_read.argtypes = [ctypes.POINTER(TraceRecord), i32, ctypes.POINTER(i32)]
     for fn in ("deft_plan", "deft_plan_stats_get", "deft_plan_get", "deft_plan_upload",
-               "deft_tree_attn", "deft_naive_attn", "deft_version"):
+               "deft_tree_attn", "deft_naive_attn", "deft_version", "deft_trace_enable",
+               "deft_trace_read"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -236,6 +247,20 @@ def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, buf
 
 def deft_plan(parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1) -> Plan:
     return Plan(parent, node_len, query_node, chunk_target, gqa_group)
+
+
+def trace_enable(on: bool = True):
+    _check("deft_trace_enable", load().deft_trace_enable(1 if on else 0))
+
+
+def trace_read(cap: int = 1 << 16):
+    """Per-launch records since the last read: list of dicts (waits for the events)."""
+    recs = (TraceRecord * cap)()
+    n = ctypes.c_int32()
+    _check("deft_trace_read", load().deft_trace_read(recs, cap, ctypes.byref(n)))
+    return [{"kernel": KERNEL_NAMES.get(r.kernel, str(r.kernel)), "family": r.family,
+             "bucket": r.bucket, "fallback": r.fallback, "items": r.items, "ms": r.ms}
+            for r in recs[: n.value]]
 
 
 def version() -> int:

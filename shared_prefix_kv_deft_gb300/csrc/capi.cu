@@ -101,6 +101,45 @@ size_t partial_bytes(int64_t slots, int32_t num_q_heads, int32_t head_dim)
     return o + l;
 }
 
+// ---- launch tracing (deft_trace_enable / deft_trace_read) ----
+struct TraceEntry {
+    deft_trace_record rec;
+    cudaEvent_t start, stop;
+};
+bool g_trace_on = false;
+std::vector<TraceEntry> g_trace;          // pending records
+std::vector<cudaEvent_t> g_event_pool;    // reusable events
+
+cudaEvent_t take_event()
+{
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
+// Runs `launch` (returns a cudaError_t as int), bracketed by events when
+// tracing is on.
+template <typename F>
+int traced(const deft_trace_record &rec, void *stream, F &&launch)
+{
+    if (!g_trace_on)
+        return launch();
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    TraceEntry t{rec, take_event(), take_event()};
+    if (!t.start || !t.stop)
+        return (int)cudaErrorMemoryAllocation;
+    cudaEventRecord(t.start, st);
+    const int rc = launch();
+    cudaEventRecord(t.stop, st);
+    g_trace.push_back(t);
+    return rc;
+}
+
 bool env_flag(const char *name)
 {
     const char *v = std::getenv(name);
@@ -161,23 +200,41 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
     if (plan->gqa_group > deft::kFmaMaxRows && !use_mma)
         return DEFT_EUNSUPPORTED;
     int rc = 0;
+    const int32_t fam = naive ? 1 : 0;
+    // CUDA-core launches, one per row bucket.
+    auto fma_launches = [&](const int32_t *items, const std::array<int32_t, 6> &off, int fb) {
+        for (int b = 0; b < 5; ++b) {
+            const int32_t n = off[b + 1] - off[b];
+            if (n <= 0)
+                continue;
+            const int32_t *it = items + 3 * (size_t)off[b];
+            const int r = traced({DEFT_K_PHASE1_FMA, fam, b, fb, n, 0.f}, stream, [&] {
+                return deft::launch_phase1_fma(a, dp, it, n, b, stream);
+            });
+            if (r)
+                return r;
+        }
+        return 0;
+    };
     if (dp.num_mma_items > 0) {
         // The tensor-core path covers head_dim 128; other head sizes, or a run
         // with DEFT_DISABLE_MMA set, take the same chunks on CUDA cores in
         // items of at most 16 rows.
         if (use_mma)
-            rc = deft::launch_phase1_mma(a, dp, stream);
+            rc = traced({DEFT_K_PHASE1_MMA, fam, 0, 0, dp.num_mma_items, 0.f}, stream,
+                        [&] { return deft::launch_phase1_mma(a, dp, stream); });
         else
-            rc = deft::launch_phase1_fma(a, dp, dp.fallback_items, hp.fallback_bucket_off.data(), stream);
+            rc = fma_launches(dp.fallback_items, hp.fallback_bucket_off, 1);
         if (rc)
             return DEFT_ECUDA;
     }
     if (dp.num_fma_items > 0) {
-        rc = deft::launch_phase1_fma(a, dp, dp.fma_items, hp.fma_bucket_off.data(), stream);
+        rc = fma_launches(dp.fma_items, hp.fma_bucket_off, 0);
         if (rc)
             return DEFT_ECUDA;
     }
-    rc = deft::launch_phase2(a, dp, out, out_dtype, lse, stream);
+    rc = traced({DEFT_K_PHASE2, fam, 0, 0, dp.num_queries, 0.f}, stream,
+                [&] { return deft::launch_phase2(a, dp, out, out_dtype, lse, stream); });
     return rc ? DEFT_ECUDA : DEFT_OK;
 }
 
@@ -206,6 +263,11 @@ int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
         delete p;
         return rc;
     }
+    size_t cursor = 0;
+    Layout lt, ln;
+    plan_partition_layout(p->tree, cursor, lt);
+    plan_partition_layout(p->naive, cursor, ln);
+    p->stats.device_bytes = (int64_t)cursor;
     *out = p;
     return DEFT_OK;
 }
@@ -346,5 +408,35 @@ const char *deft_status_str(int status)
 }
 
 int deft_version(void) { return 100; }
+
+int deft_trace_enable(int32_t on)
+{
+    g_trace_on = on != 0;
+    return DEFT_OK;
+}
+
+int deft_trace_read(deft_trace_record *out, int32_t cap, int32_t *count)
+{
+    if (!count || (cap > 0 && !out) || cap < 0)
+        return DEFT_EINVAL;
+    int rc = DEFT_OK;
+    int32_t n = 0;
+    for (TraceEntry &t : g_trace) {
+        float ms = 0.f;
+        if (cudaEventSynchronize(t.stop) != cudaSuccess ||
+            cudaEventElapsedTime(&ms, t.start, t.stop) != cudaSuccess)
+            rc = DEFT_ECUDA;
+        if (n < cap) {
+            out[n] = t.rec;
+            out[n].ms = ms;
+            ++n;
+        }
+        g_event_pool.push_back(t.start);
+        g_event_pool.push_back(t.stop);
+    }
+    g_trace.clear();
+    *count = n;
+    return rc;
+}
 
 }  // extern "C"

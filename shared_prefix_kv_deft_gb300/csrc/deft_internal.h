@@ -127,8 +127,10 @@ struct AttnArgs {
 };
 
 // Launchers (return a cudaError_t cast to int; 0 = success).
-int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items,
-                      const int32_t *bucket_off, void *stream);
+// One CUDA-core launch over `n` items (device triples at `items`), all of row
+// bucket `bucket` (rows <= 2^bucket).
+int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
+                      int bucket, void *stream);
 int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, void *stream);
 // Row bucket of an item with `rows` rows: smallest b with rows <= 2^b.
 inline int row_bucket(int rows) { return rows <= 1 ? 0 : rows <= 2 ? 1 : rows <= 4 ? 2 : rows <= 8 ? 3 : 4; }

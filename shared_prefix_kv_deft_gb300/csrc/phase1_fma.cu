@@ -359,24 +359,14 @@ int launch_bucket(int bucket, const AttnArgs &a, const DevPartition &p, const in
 
 }  // namespace
 
-// items: device pointer to (chunk, q_begin, q_end) triples sorted by row
-// bucket; bucket_off (host, 6 entries): items of bucket b (rows <= 2^b) are
-// [bucket_off[b], bucket_off[b+1]).
-int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items,
-                      const int32_t *bucket_off, void *stream)
+int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
+                      int bucket, void *stream)
 {
+    if (n <= 0)
+        return 0;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    for (int b = 0; b < 5; ++b) {
-        const int32_t n = bucket_off[b + 1] - bucket_off[b];
-        if (n <= 0)
-            continue;
-        const int32_t *it = items + 3 * (size_t)bucket_off[b];
-        const int rc = a.head_dim == 128 ? launch_bucket<128>(b, a, p, it, n, st)
-                                         : launch_bucket<64>(b, a, p, it, n, st);
-        if (rc != 0)
-            return rc;
-    }
-    return 0;
+    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, n, st)
+                             : launch_bucket<64>(bucket, a, p, items, n, st);
 }
 
 }  // namespace deft

@@ -194,6 +194,41 @@ int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
                     void *stream);
 
 /*
+ * deft_tree_attn_noalloc -- deft_tree_attn for callers that cannot allocate
+ * device memory.  The paper has no counterpart; this is a library service.
+ *
+ * deft_tree_attn needs a workspace and an uploaded plan, and uploading calls
+ * cudaMalloc.  Some callers cannot do either: code running while a CUDA
+ * graph is captured (cudaMalloc is not allowed there), frameworks whose
+ * device memory belongs to a pool allocator that must not be bypassed, and
+ * latency-critical loops that cannot pay for an allocation or its implicit
+ * synchronisation.  This call takes the same inputs and outputs as
+ * deft_tree_attn but no workspace, and the plan need not be uploaded: the
+ * plan's tree arrays are copied from its host memory on `stream`, and the
+ * partials are kept, in one static device array of
+ * DEFT_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU loading the library
+ * holds until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *   - A plan whose arrays plus partials (slots * num_q_heads * (head_dim + 1)
+ *     fp32 values, 256-byte aligned pieces) exceed the array is rejected with
+ *     DEFT_EWORKSPACE before anything is enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents;
+ *     nothing in it has to start at zero.  Calls that may overlap on the GPU
+ *     (other streams, unsynchronised host threads) race and must not be made.
+ * Results are those of deft_tree_attn; other arguments and errors as there.
+ */
+#define DEFT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+int deft_tree_attn_noalloc(const void *q, const void *k_pages, const void *v_pages,
+                           const int32_t *node_page_off, const int32_t *page_id,
+                           int32_t num_pages, int32_t num_q_heads, int32_t num_kv_heads,
+                           int32_t head_dim, int32_t page_size, float scale,
+                           const deft_plan_t *plan, void *out, int32_t out_dtype, float *lse,
+                           void *stream);
+
+/*
  * Per-launch kernel timing, for measurement tools (no counterpart on the
  * pages).  While enabled, every kernel launch made by deft_tree_attn and
  * deft_naive_attn is bracketed by two CUDA events recorded on the launch

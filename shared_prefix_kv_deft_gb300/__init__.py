@@ -39,7 +39,8 @@ ARRAYS = {
 # Symbols the header declares (checked by the tests).
 EXPORTS = ["deft_plan", "deft_plan_stats_get", "deft_plan_get", "deft_plan_upload",
            "deft_workspace_bytes", "deft_tree_attn", "deft_naive_attn", "deft_plan_free",
-           "deft_status_str", "deft_version", "deft_trace_enable", "deft_trace_read"]
+           "deft_status_str", "deft_version", "deft_trace_enable", "deft_trace_read",
+           "deft_tree_attn_noalloc"]
 
 KERNEL_NAMES = {0: "phase1_fma", 1: "phase1_mma", 2: "phase2_merge"}
 
@@ -90,6 +91,8 @@ def load(path: str = LIB_PATH):
     attn = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, i32, P, P, sz, P]
     lib.deft_tree_attn.argtypes = attn
     lib.deft_naive_attn.argtypes = attn
+    lib.deft_tree_attn_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P,
+                                           i32, P, P]
     lib.deft_plan_free.argtypes = [P]
     lib.deft_plan_free.restype = None
     lib.deft_status_str.argtypes = [ctypes.c_int]
@@ -99,7 +102,7 @@ def load(path: str = LIB_PATH):
     lib.deft_trace_read.argtypes = [ctypes.POINTER(TraceRecord), i32, ctypes.POINTER(i32)]
     for fn in ("deft_plan", "deft_plan_stats_get", "deft_plan_get", "deft_plan_upload",
                "deft_tree_attn", "deft_naive_attn", "deft_version", "deft_trace_enable",
-               "deft_trace_read"):
+               "deft_trace_read", "deft_tree_attn_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib

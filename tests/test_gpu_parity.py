@@ -197,3 +197,32 @@ def test_full_size_workloads_sampled(deft, cfg):
         l = l.cpu().numpy().astype(np.float64)
         assert np.isfinite(o).all() and np.isfinite(l).all(), what
         assert_parity(o[sample], l[sample], ref, ref_lse, f"config {cfg} {what}")
+
+
+MMA_SHAPES = [
+    W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4, head_dim=128),
+    W.speculative_forest(requests=2, prefix=300, tree_nodes=64, heads=4),
+    W.random_tree(203, max_nodes=10, max_len=300, max_queries=60, q_heads=2, kv_heads=2,
+                  head_dim=128, forest=False),
+    W.reasoning_tree(levels=3, len_lo=20, len_hi=90, num_queries=40, q_heads=8, kv_heads=2),
+    W.few_shot_tree(prefix=1000, branches=140, branch_len=20, heads=2, head_dim=128),
+]
+
+
+@pytest.mark.parametrize("spec", MMA_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [64, 256])
+def test_tensor_core_and_cuda_core_paths_agree_with_oracle(deft, spec, ct, monkeypatch):
+    inp = dense_inputs(spec, seed=11 + ct)
+    ref, ref_lse = run_oracle(inp)
+    case = Case(deft, inp, ct)
+    assert case.plan.stats["num_mma_items"] > 0, "shape has no >= 16-row chunk"
+    deft.trace_read()
+    deft.trace_enable(True)
+    out, lse = case.run()
+    deft.trace_enable(False)
+    kinds = {r["kernel"] for r in deft.trace_read()}
+    assert "phase1_mma" in kinds
+    assert_parity(out, lse, ref, ref_lse, "tcgen05 path")
+    monkeypatch.setenv("DEFT_DISABLE_MMA", "1")
+    out2, lse2 = case.run()
+    assert_parity(out2, lse2, ref, ref_lse, "CUDA-core fallback")

@@ -290,8 +290,10 @@ __global__ void __launch_bounds__(kMThreads, 1) phase1_mma_kernel(AttnArgs a, De
                     const int r = g + i;
                     float pr = 0.f;
                     if (((w >> i) & 1u) && r < R) {
-                        const __nv_bfloat16 b = __float2bfloat16_rn(exp2f(fmaf(v[i], sc, -m_s[r])));
-                        pr = __bfloat162float(b);
+                        // The normaliser sums the fp32 probabilities; only the
+                        // P.V operand is rounded to bf16.
+                        pr = exp2f(fmaf(v[i], sc, -m_s[r]));
+                        const __nv_bfloat16 b = __float2bfloat16_rn(pr);
                         uint8_t *dst = smem + (prow - base) + r * 128 + ((pch ^ (r & 7)) << 4);
                         *reinterpret_cast<__nv_bfloat16 *>(dst) = b;
                     } else if (r < NP) {

@@ -4,30 +4,35 @@
 //
 // Same result as phase1_fma.cu (DeFT Guide, "Deep Dive": tree-constrained
 // attention, online-softmax tile accumulation; DeFT abstract: KV-Guided
-// Grouping), for chunks shared by enough queries that the two products
-// S = q.K^T and O = P.V are dense contractions worth the tensor cores.
+// Grouping), for chunks shared by enough queries that S = q.K^T and O = P.V
+// are dense contractions worth the tensor cores.
 //
 // Formulation: KV tokens on the MMA M dimension (128-token tiles), query
-// rows on N (R rounded up to 16):
-//     S^T[128 tok x N]  = K_tile[128 x 128] . Q^T[128 x N]       (TMEM, fp32)
-//     O^T[128 d   x N] += V_tile^T[128 x 128] . P^T[128 tok x N]   (TMEM, fp32)
-// so one thread owns one token of S^T (and one output dimension of O^T),
-// and the softmax work of a tile is spread over all 128 threads whatever
-// the row count.  Column maxima and sums are warp butterflies
-// (reduce-scatter: lane l ends with column l) plus a 4-way exchange in
-// shared memory.  Logits are kept in base 2; phase 2 converts.
+// rows on N.  The rows are split into two halves of NPH columns (NPH = R/2
+// rounded up to 16), one per softmax warpgroup:
+//     S_w^T[128 tok x NPH]  = K_tile . Q_w^T            (TMEM, fp32, 2 buffers)
+//     O_w^T[128 d   x NPH] += V_tile^T . P_w^T          (TMEM, fp32)
+// so a thread owns one token of S^T (one output dimension of O^T).  Column
+// maxima and sums are warp butterflies (reduce-scatter: lane l ends with
+// column l) plus a 4-warp exchange in shared memory.  Logits are base 2.
 //
-// Operands in shared memory use the canonical 128-byte-swizzled layouts:
-// K tile, Q^T and P^T K-major (rows of 64 bf16 = 128 B, 16-byte chunk c of
-// row r stored at chunk c ^ (r % 8), 8-row atoms 1024 B apart), V tile the
-// same bytes read MN-major for V^T.  KV rows are fetched through the page
-// table with 16-byte cp.async copies, one token row at a time, so ragged
-// node tails and 1-token nodes cost nothing extra; one CTA runs one
-// (chunk, KV head, row block) and prefetches tile t+1 while computing t.
-//
-// Every wait on an mbarrier is bounded; a CTA whose MMA never completes
-// writes NaN partials (so the step's output shows the failure), waits for
-// its own copies, frees its TMEM and returns.
+// Roles (10 warps):
+//   warps 0-3, 4-7  softmax warpgroups 0 and 1 (row halves);
+//   warp 8          producer: resolves every token row through the page
+//                   table one tile ahead, loads full pages with TMA (four
+//                   2 KB boxes of the 128-byte-swizzled layout) and ragged
+//                   rows (node tails, packed one-token nodes) with 16-byte
+//                   cp.async at the exact token count;
+//   warp 9          allocates TMEM; lane 0 issues the MMAs: S(t) for both
+//                   halves, then P.V of tile t-1, so the tensor core works
+//                   on the next tile while the warpgroups do softmax.
+// Two KV stages; every hand-off is an mbarrier, every wait on one is
+// bounded.  A CTA whose wait runs out writes NaN partials (the step's
+// output then shows the failure), waits for its own copies, frees TMEM and
+// returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "deft_internal.h"
 #include "tcgen05.cuh"
@@ -37,27 +42,35 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTileTok = 128;
-constexpr int kMStages = 2;
-constexpr int kMThreads = 128;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kThreadsMma = 320;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kHalf = 128 * 128;       // one 64-wide half of a 128-row operand (16 KB)
 constexpr uint32_t kTileBytes = 2 * kHalf;  // one 128 x 128 bf16 operand (32 KB)
+constexpr uint32_t kPHalf = 64 * 128;       // one token half of a warpgroup's P^T (64 rows)
+constexpr uint32_t kPageBytes = 4 * 2048;   // K + V of one 16-token page, four TMA boxes
 
-struct MmaSmem {
-    static constexpr uint32_t kv_off = 0;  // [stage][K, V]
-    static constexpr uint32_t q_off = kv_off + kMStages * 2 * kTileBytes;
-    static constexpr uint32_t p_off = q_off + kTileBytes;
-    static constexpr uint32_t meta_off = p_off + kTileBytes;                  // [stage][128] uint4
-    static constexpr uint32_t seg_off = meta_off + kMStages * kTileTok * 16;  // pos/node/tb + uint4 masks
-    static constexpr uint32_t red_off = seg_off + kMaxSegsPerChunk * 12 + kMaxSegsPerChunk * 16;
-    static constexpr uint32_t stat_off = red_off + 4 * 128 * 4;               // m, alpha, l
-    static constexpr uint32_t misc_off = stat_off + 3 * 128 * 4;
-    static constexpr uint32_t total = misc_off + 64;
-    static constexpr uint32_t alloc = total + 1024;  // room to align the base to 1024 bytes
+struct Smem {
+    static constexpr uint32_t kv_off = 0;                       // [stage][K,V] operands
+    static constexpr uint32_t q_off = kv_off + 4 * kTileBytes;  // Q^T, 128 rows
+    static constexpr uint32_t p_off = q_off + kTileBytes;       // P^T per warpgroup (16 KB each)
+    static constexpr uint32_t meta_off = p_off + 2 * 2 * kPHalf;        // [stage][128] uint4
+    static constexpr uint32_t seg_off = meta_off + 2 * kTileTok * 16;   // pos, node, tb, masks
+    static constexpr uint32_t red_off = seg_off + kMaxSegsPerChunk * (12 + 16);  // [wg][warp][64]
+    static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;     // [wg][m, alpha, l][64]
+    static constexpr uint32_t bar_off = stat_off + 2 * 3 * 64 * 4;     // 16 mbarriers
+    static constexpr uint32_t misc_off = bar_off + 16 * 8;             // tmem base, error flag
+    static constexpr uint32_t total = misc_off + 16;
+    static constexpr uint32_t alloc = total + 1024;
 };
 
-// Warp butterfly that leaves in every lane l the reduction over the warp of
-// column l of v (32 columns).  v is destroyed.
+// mbarrier slots
+constexpr int kBarFull = 0;     // [2] stage loaded (producer)
+constexpr int kBarEmpty = 2;    // [2] stage consumed (MMA commit)
+constexpr int kBarSFull = 4;    // [wg*2 + buf] S ready (MMA commit)
+constexpr int kBarSFree = 8;    // [wg*2 + buf] S read (warpgroup)
+constexpr int kBarPFull = 12;   // [wg] P written (warpgroup)
+constexpr int kBarPvDone = 14;  // [wg] P.V finished (MMA commit)
+
 template <bool kMax>
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
 {
@@ -75,28 +88,24 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
-__device__ __forceinline__ uint32_t mask_word(const uint4 &m, int w)
-{
-    return w == 0 ? m.x : w == 1 ? m.y : w == 2 ? m.z : m.w;
-}
-
-__global__ void __launch_bounds__(kMThreads, 1) phase1_mma_kernel(AttnArgs a, DevPartition p)
+__global__ void __launch_bounds__(kThreadsMma, 1)
+phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
-    uint4 *meta = reinterpret_cast<uint4 *>(smem + MmaSmem::meta_off);
-    int32_t *s_pos = reinterpret_cast<int32_t *>(smem + MmaSmem::seg_off);
+    uint4 *meta = reinterpret_cast<uint4 *>(smem + Smem::meta_off);
+    int32_t *s_pos = reinterpret_cast<int32_t *>(smem + Smem::seg_off);
     int32_t *s_node = s_pos + kMaxSegsPerChunk;
     int32_t *s_tb = s_node + kMaxSegsPerChunk;
-    uint4 *s_rmask = reinterpret_cast<uint4 *>(smem + MmaSmem::seg_off + kMaxSegsPerChunk * 12);
-    float *red = reinterpret_cast<float *>(smem + MmaSmem::red_off);
-    float *m_s = reinterpret_cast<float *>(smem + MmaSmem::stat_off);
-    float *alpha_s = m_s + 128;
-    float *l_fin = alpha_s + 128;
-    const uint32_t bar = base + MmaSmem::misc_off;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + MmaSmem::misc_off + 8);
+    uint4 *s_rmask = reinterpret_cast<uint4 *>(smem + Smem::seg_off + kMaxSegsPerChunk * 12);
+    float *red = reinterpret_cast<float *>(smem + Smem::red_off);
+    float *stat = reinterpret_cast<float *>(smem + Smem::stat_off);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::misc_off);
+    volatile int *err = reinterpret_cast<volatile int *>(smem + Smem::misc_off + 4);
+    auto bar = [&](int i) { return base + Smem::bar_off + 8u * (uint32_t)i; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
@@ -104,266 +113,436 @@ __global__ void __launch_bounds__(kMThreads, 1) phase1_mma_kernel(AttnArgs a, De
     const int h = blockIdx.x - item * Hkv;
     const int c = p.mma_items[3 * item], qb = p.mma_items[3 * item + 1], qe = p.mma_items[3 * item + 2];
     const int R = (qe - qb) * G;
-    const int NP = (R + 15) & ~15;
+    const int NPH = ((R + 1) / 2 + 15) & ~15;  // columns per warpgroup
+    const int rows_w1 = R > NPH ? R - NPH : 0;
     const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
     const int cq0 = p.chunk_q_off[c] + qb;
     const int T = p.chunk_tokens[c];
     const int ntiles = (T + kTileTok - 1) / kTileTok;
     const int W = p.mask_words;
+    const int nwg = rows_w1 > 0 ? 2 : 1;
 
-    if (warp == 0) {
+    // ---------------- set-up ----------------
+    if (warp == 9) {
         tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(bar, 1);
+        tc::mbar_init(bar(kBarFull + 0), 33);
+        tc::mbar_init(bar(kBarFull + 1), 33);
+        for (int i = kBarEmpty; i < 16; ++i)
+            tc::mbar_init(bar(i), 1);
+        *err = 0;
         tc::fence_mbar_init();
     }
-    // Zero the operand buffers once: rows no token fills (chunk tails) and
-    // padded query rows must hold finite values.
-    for (uint32_t i = tid; i < MmaSmem::meta_off / 16; i += kMThreads)
+    for (uint32_t i = tid; i < Smem::meta_off / 16; i += kThreadsMma)
         reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
-    for (int s = tid; s < nseg; s += kMThreads) {
+    for (int s = tid; s < nseg; s += kThreadsMma) {
         s_pos[s] = p.seg_chunk_pos[sb + s];
         s_node[s] = p.seg_node[sb + s];
         s_tb[s] = p.seg_tok_begin[sb + s];
         const uint64_t *m = p.seg_mask + (size_t)(sb + s) * W;
-        uint32_t rm[4] = {0, 0, 0, 0};
+        uint32_t rm[4] = {0, 0, 0, 0};  // warpgroup 0 bits 0-63, warpgroup 1 bits 64-127
         for (int r = 0; r < R; ++r) {
             const int qid = p.chunk_q[cq0 + r / G];
-            rm[r >> 5] |= (uint32_t)((m[qid >> 6] >> (qid & 63)) & 1ull) << (r & 31);
+            const uint32_t bit = (uint32_t)((m[qid >> 6] >> (qid & 63)) & 1ull);
+            const int col = r < NPH ? r : 64 + (r - NPH);
+            rm[col >> 5] |= bit << (col & 31);
         }
         s_rmask[s] = make_uint4(rm[0], rm[1], rm[2], rm[3]);
     }
-    m_s[tid] = -INFINITY;
-    alpha_s[tid] = 1.f;
+    if (tid < 128) {
+        stat[(tid >> 6) * 192 + (tid & 63)] = -INFINITY;    // m
+        stat[(tid >> 6) * 192 + 64 + (tid & 63)] = 1.f;     // alpha
+    }
     __syncthreads();
-    // Q^T operand: row r = (query, group member), K-major, swizzled.
     const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-    for (int i = tid; i < R * 16; i += kMThreads) {
+    for (int i = tid; i < R * 16; i += kThreadsMma) {
         const int r = i >> 4, ch = i & 15;
         const int qid = p.chunk_q[cq0 + r / G];
         const int hq = h * G + (r % G);
         const uint4 v = *reinterpret_cast<const uint4 *>(qg + ((size_t)qid * Hq + hq) * kD + ch * 8);
-        *reinterpret_cast<uint4 *>(smem + MmaSmem::q_off + (ch >> 3) * kHalf + r * 128 +
+        *reinterpret_cast<uint4 *>(smem + Smem::q_off + (ch >> 3) * kHalf + r * 128 +
                                    (((ch & 7) ^ (r & 7)) << 4)) = v;
     }
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem_base = *tmem_slot;
-    const uint32_t tmem_S = tmem_base;
-    const uint32_t tmem_O = tmem_base + 128;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tmem = *tmem_slot;
 
-    auto find_seg = [&](int pos) {
-        int lo = 0, hi = nseg - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_pos[mid] <= pos)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        return lo;
-    };
-    const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
-    const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
-
-    // Copies of tile `tile` into stage `st`: warp w moves rows w, w+4, ...;
-    // lane l resolves row w + 4l through the page table once, then the warp
-    // copies one row per step (lanes 0-15 the K row, 16-31 the V row).
-    auto issue_tile = [&](int tile, int st) {
-        const int rl = warp + 4 * lane;
-        const int pos = tile * kTileTok + rl;
-        long long off = -1;
-        uint4 rm = make_uint4(0, 0, 0, 0);
-        if (pos < T) {
-            const int s = find_seg(pos);
-            const int t = s_tb[s] + pos - s_pos[s];
-            const int page = a.page_id[a.node_page_off[s_node[s]] + t / kPageSize];
-            off = (((long long)page * Hkv + h) * kPageSize + (t % kPageSize)) * kD;
-            rm = s_rmask[s];
-        }
-        meta[st * kTileTok + rl] = rm;
-        const int kv = lane >> 4, ch = lane & 15;
-        const uint32_t dst0 = base + MmaSmem::kv_off + (uint32_t)(st * 2 + kv) * kTileBytes +
-                              (ch >> 3) * kHalf;
-        const __nv_bfloat16 *src0 = (kv ? vg : kg) + ch * 8;
-#pragma unroll 4
-        for (int k = 0; k < 32; ++k) {
-            const int row = warp + 4 * k;
-            const long long o = __shfl_sync(0xffffffffu, off, k);
-            if (o >= 0)
-                cp_async_16(dst0 + row * 128 + (((ch & 7) ^ (row & 7)) << 4), src0 + o);
-        }
-    };
-
-    const uint32_t idesc_s = tc::idesc_bf16(128, NP, 0, 0);
-    const uint32_t idesc_o = tc::idesc_bf16(128, NP, 1, 0);
-    const float sc = a.scale_log2;
-    float l_own[4] = {0.f, 0.f, 0.f, 0.f};  // column sums of columns 32*g + lane
-    uint32_t phase = 0;
-    bool ok = true;
-
+    if (warp == 8) {
+        // ---------------- producer ----------------
+        const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
+        const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
+        int last_tile[2] = {-1, -1};
+        for (int t = 0; t < ntiles; ++t) {
+            const int st = t & 1;
+            long long off[4];
+            uint4 rmk[4];
+            int segk[4], tokk[4];
 #pragma unroll
-    for (int st = 0; st < kMStages - 1; ++st) {
-        if (st < ntiles)
-            issue_tile(st, st);
-        cp_async_commit();
-    }
-    for (int t = 0; t < ntiles && ok; ++t) {
-        const int st = t % kMStages;
-        if (t + kMStages - 1 < ntiles)
-            issue_tile(t + kMStages - 1, (t + kMStages - 1) % kMStages);
-        cp_async_commit();
-        cp_async_wait<kMStages - 1>();
-        tc::fence_proxy_async();
-        __syncthreads();
-
-        // S^T = K_t . Q^T
-        if (tid == 0) {
-            tc::fence_after_sync();
-            const uint32_t kb = base + MmaSmem::kv_off + (uint32_t)(st * 2) * kTileBytes;
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = tc::smem_desc(kb + (s >> 2) * kHalf + (s & 3) * 32, 16, 1024);
-                const uint64_t bd =
-                    tc::smem_desc(base + MmaSmem::q_off + (s >> 2) * kHalf + (s & 3) * 32, 16, 1024);
-                tc::mma_bf16(tmem_S, ad, bd, idesc_s, s > 0 ? 1u : 0u);
-            }
-            tc::mma_commit(bar);
-        }
-        ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1));
-        ++phase;
-        if (!ok)
-            break;
-        tc::fence_after_sync();
-
-        // Column maxima of the tile.
-        const uint4 rm = meta[st * kTileTok + tid];
-        for (int g = 0; g < NP; g += 32) {
-            float v[32];
-            tc::tmem_ld32(tmem_S + lane_off + g, v);
-            const uint32_t w = mask_word(rm, g >> 5);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                v[i] = ((w >> i) & 1u) && (g + i < R) ? v[i] * sc : -INFINITY;
-            red[warp * 128 + g + lane] = reduce_scatter32<true>(v, lane);
-        }
-        __syncthreads();
-        bool need = false;
-        if (tid < NP) {
-            const float mt = fmaxf(fmaxf(red[tid], red[128 + tid]), fmaxf(red[256 + tid], red[384 + tid]));
-            const float mo = m_s[tid];
-            const float mn = fmaxf(mo, mt);
-            const float al = mn == -INFINITY ? 1.f : exp2f(mo - mn);
-            m_s[tid] = mn;
-            alpha_s[tid] = al;
-            need = al != 1.f;
-        }
-        const bool rescale = __syncthreads_or(need && t > 0) != 0;
-        if (rescale) {
-            for (int g = 0; g < NP; g += 32) {
-                float v[32];
-                tc::tmem_ld32(tmem_O + lane_off + g, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    v[i] *= alpha_s[g + i];
-                tc::tmem_st32(tmem_O + lane_off + g, v);
-                l_own[g >> 5] *= alpha_s[g + lane];
-            }
-        }
-
-        // Probabilities -> P^T (bf16, K-major over tokens) and column sums.
-        {
-            const int j = tid;
-            const uint32_t prow = base + MmaSmem::p_off + (j >> 6) * kHalf + ((j & 63) & 7) * 2;
-            const int pch = (j & 63) >> 3;
-            for (int g = 0; g < NP; g += 32) {
-                float v[32];
-                tc::tmem_ld32(tmem_S + lane_off + g, v);
-                const uint32_t w = mask_word(rm, g >> 5);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int r = g + i;
-                    float pr = 0.f;
-                    if (((w >> i) & 1u) && r < R) {
-                        // The normaliser sums the fp32 probabilities; only the
-                        // P.V operand is rounded to bf16.
-                        pr = exp2f(fmaf(v[i], sc, -m_s[r]));
-                        const __nv_bfloat16 b = __float2bfloat16_rn(pr);
-                        uint8_t *dst = smem + (prow - base) + r * 128 + ((pch ^ (r & 7)) << 4);
-                        *reinterpret_cast<__nv_bfloat16 *>(dst) = b;
-                    } else if (r < NP) {
-                        uint8_t *dst = smem + (prow - base) + r * 128 + ((pch ^ (r & 7)) << 4);
-                        *reinterpret_cast<__nv_bfloat16 *>(dst) = __float2bfloat16_rn(0.f);
+            for (int k = 0; k < 4; ++k) {
+                const int pos = t * kTileTok + lane + 32 * k;
+                off[k] = -1;
+                segk[k] = -1;
+                tokk[k] = 1;
+                rmk[k] = make_uint4(0, 0, 0, 0);
+                if (pos < T) {
+                    int lo = 0, hi = nseg - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (s_pos[mid] <= pos)
+                            lo = mid;
+                        else
+                            hi = mid - 1;
                     }
-                    v[i] = pr;
-                }
-                l_own[g >> 5] += reduce_scatter32<false>(v, lane);
-            }
-        }
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
-        __syncthreads();
-
-        // O^T += V_t^T . P^T
-        if (tid == 0) {
-            tc::fence_after_sync();
-            const uint32_t vb = base + MmaSmem::kv_off + (uint32_t)(st * 2 + 1) * kTileBytes;
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint64_t ad = tc::smem_desc(vb + s * 2048, kHalf, 1024);
-                const uint64_t bd =
-                    tc::smem_desc(base + MmaSmem::p_off + (s >> 2) * kHalf + (s & 3) * 32, 16, 1024);
-                tc::mma_bf16(tmem_O, ad, bd, idesc_o, (t > 0 || s > 0) ? 1u : 0u);
-            }
-            tc::mma_commit(bar);
-        }
-        ok = __syncthreads_and(tc::mbar_wait(bar, phase & 1));
-        ++phase;
-        tc::fence_after_sync();
-    }
-    cp_async_wait<0>();
-
-    if (ok) {
-        // Normalisers, then O^T / l written as fp32 partials (lane = dimension).
-        for (int g = 0; g < NP; g += 32)
-            red[warp * 128 + g + lane] = l_own[g >> 5];
-        __syncthreads();
-        if (tid < NP)
-            l_fin[tid] = red[tid] + red[128 + tid] + red[256 + tid] + red[384 + tid];
-        __syncthreads();
-        for (int g = 0; g < NP; g += 32) {
-            float v[32];
-            tc::tmem_ld32(tmem_O + lane_off + g, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = g + i;
-                if (r < R) {
-                    const size_t prow = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
-                    a.o_part[prow * kD + tid] = v[i] / l_fin[r];
+                    const int tk = s_tb[lo] + pos - s_pos[lo];
+                    const int page = a.page_id[a.node_page_off[s_node[lo]] + tk / kPageSize];
+                    off[k] = (((long long)page * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
+                    segk[k] = lo;
+                    tokk[k] = tk;
+                    rmk[k] = s_rmask[lo];
                 }
             }
+            // Page p of the tile (rows 16p..16p+15) goes by TMA when its 16
+            // rows are one aligned page of one segment.
+            uint32_t tma_pages = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int s_first = __shfl_sync(0xffffffffu, segk[k], lane & 16);
+                const int t_first = __shfl_sync(0xffffffffu, tokk[k], lane & 16);
+                const bool ok = off[k] >= 0 && segk[k] == s_first && (t_first % kPageSize) == 0;
+                const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+                if ((bal & 0xffffu) == 0xffffu)
+                    tma_pages |= 1u << (2 * k);
+                if ((bal >> 16) == 0xffffu)
+                    tma_pages |= 1u << (2 * k + 1);
+            }
+            long long page_off = -1;
+#pragma unroll
+            for (int pg = 0; pg < 8; ++pg) {
+                const long long o = __shfl_sync(0xffffffffu, off[pg >> 1], 16 * (pg & 1));
+                if (lane == pg)
+                    page_off = o;
+            }
+            if (t >= 2) {
+                const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(kBarEmpty + st), ((t - 2) >> 1) & 1));
+                if (!ok) {
+                    *err = 1;
+                    break;
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                meta[st * kTileTok + lane + 32 * k] = rmk[k];
+            const uint32_t kst = base + Smem::kv_off + (uint32_t)(st * 2) * kTileBytes;
+            const uint32_t vst = kst + kTileBytes;
+            if (lane == 0)
+                tc::mbar_arrive_expect_tx(bar(kBarFull + st), __popc(tma_pages) * kPageBytes);
+            __syncwarp();
+            if (lane < 8 && ((tma_pages >> lane) & 1u)) {
+                const int y = (int)(page_off >> 7);
+                const uint32_t row_b = (uint32_t)(16 * lane) * 128;
+                tc::tma_load_2d(kst + row_b, &tmap_k, 0, y, bar(kBarFull + st));
+                tc::tma_load_2d(kst + kHalf + row_b, &tmap_k, 64, y, bar(kBarFull + st));
+                tc::tma_load_2d(vst + row_b, &tmap_v, 0, y, bar(kBarFull + st));
+                tc::tma_load_2d(vst + kHalf + row_b, &tmap_v, 64, y, bar(kBarFull + st));
+            }
+            // Remaining valid rows, one row per warp step.
+            bool any_cp = false;
+            const int kv = lane >> 4, ch = lane & 15;
+            const uint32_t dst0 = (kv ? vst : kst) + (ch >> 3) * kHalf;
+            const __nv_bfloat16 *src0 = (kv ? vg : kg) + ch * 8;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const bool need = off[k] >= 0 && !((tma_pages >> ((lane + 32 * k) >> 4)) & 1u);
+                uint32_t nb = __ballot_sync(0xffffffffu, need);
+                any_cp |= nb != 0;
+                while (nb) {
+                    const int src_lane = __ffs(nb) - 1;
+                    nb &= nb - 1;
+                    const int row = src_lane + 32 * k;
+                    const long long o = __shfl_sync(0xffffffffu, off[k], src_lane);
+                    cp_async_16(dst0 + row * 128 + (((ch & 7) ^ (row & 7)) << 4), src0 + o);
+                }
+            }
+            if (any_cp) {
+                cp_async_commit();
+                cp_async_wait<0>();
+                tc::fence_proxy_async();
+            }
+            tc::mbar_arrive(bar(kBarFull + st));
+            last_tile[st] = t;
         }
-        if (tid < R) {
-            const size_t prow = (size_t)(cq0 + tid / G) * Hq + h * G + (tid % G);
-            a.lse_part[prow] = m_s[tid] + log2f(l_fin[tid]);
+        cp_async_wait<0>();
+        // Do not leave while a TMA copy of ours may still be landing.
+        for (int s2 = 0; s2 < 2; ++s2)
+            if (last_tile[s2] >= 0)
+                tc::mbar_wait(bar(kBarFull + s2), (last_tile[s2] >> 1) & 1);
+    } else if (warp == 9) {
+        // ---------------- MMA issue ----------------
+        if (lane == 0) {
+            const uint32_t idesc_s = tc::idesc_bf16(128, NPH, 0, 0);
+            const uint32_t idesc_o = tc::idesc_bf16(128, NPH, 1, 0);
+            bool ok = true;
+            for (int t = 0; t <= ntiles && ok; ++t) {
+                if (t < ntiles) {
+                    const int st = t & 1, b = t & 1;
+                    ok = tc::mbar_wait(bar(kBarFull + st), (t >> 1) & 1);
+                    tc::fence_after_sync();
+                    const uint32_t kb = base + Smem::kv_off + (uint32_t)(st * 2) * kTileBytes;
+                    for (int w = 0; w < nwg && ok; ++w) {
+                        if (t >= 2) {
+                            ok = tc::mbar_wait(bar(kBarSFree + w * 2 + b), ((t - 2) >> 1) & 1);
+                            tc::fence_after_sync();
+                        }
+                        const uint32_t qb_addr = base + Smem::q_off + (uint32_t)(w * NPH) * 128;
+                        const uint32_t d_s = tmem + (uint32_t)(w * 128 + b * 64);
+#pragma unroll
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t ad = tc::smem_desc(kb + (s >> 2) * kHalf + (s & 3) * 32, 16, 1024);
+                            const uint64_t bd = tc::smem_desc(qb_addr + (s >> 2) * kHalf + (s & 3) * 32, 16, 1024);
+                            tc::mma_bf16(d_s, ad, bd, idesc_s, s > 0 ? 1u : 0u);
+                        }
+                        tc::mma_commit(bar(kBarSFull + w * 2 + b));
+                    }
+                }
+                if (t >= 1 && ok) {
+                    const int tp = t - 1, stp = tp & 1;
+                    const uint32_t vb = base + Smem::kv_off + (uint32_t)(stp * 2 + 1) * kTileBytes;
+                    for (int w = 0; w < nwg && ok; ++w) {
+                        ok = tc::mbar_wait(bar(kBarPFull + w), tp & 1);
+                        tc::fence_after_sync();
+                        const uint32_t pb = base + Smem::p_off + (uint32_t)w * 2 * kPHalf;
+                        const uint32_t d_o = tmem + 256 + (uint32_t)(w * 64);
+#pragma unroll
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t ad = tc::smem_desc(vb + s * 2048, kHalf, 1024);
+                            const uint64_t bd = tc::smem_desc(pb + (s >> 2) * kPHalf + (s & 3) * 32, 16, 1024);
+                            tc::mma_bf16(d_o, ad, bd, idesc_o, (tp > 0 || s > 0) ? 1u : 0u);
+                        }
+                        tc::mma_commit(bar(kBarPvDone + w));
+                    }
+                    tc::mma_commit(bar(kBarEmpty + stp));
+                }
+            }
+            if (!ok)
+                *err = 1;
         }
     } else {
-        for (int r = 0; r < R; ++r) {
-            const size_t prow = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
-            a.o_part[prow * kD + tid] = __int_as_float(0x7fc00000);
-            if (tid == 0)
-                a.lse_part[prow] = __int_as_float(0x7fc00000);
+        // ---------------- softmax warpgroups ----------------
+        const int w = warp >> 2, wt = warp & 3, j = tid & 127;
+        const int rows_w = w == 0 ? (R < NPH ? R : NPH) : rows_w1;
+        const uint32_t nb_id = 1 + (uint32_t)w;
+        float *m_s = stat + w * 192, *alpha_s = m_s + 64, *l_fin = m_s + 128;
+        float *redw = red + w * 256;
+        const uint32_t lane_off = (uint32_t)(wt * 32) << 16;
+        const uint32_t tmem_o = tmem + 256 + (uint32_t)(w * 64) + lane_off;
+        const uint32_t prow = base + Smem::p_off + (uint32_t)w * 2 * kPHalf + (j >> 6) * kPHalf;
+        const int pch = (j & 63) >> 3, pin = (j & 7) * 2;
+        const float sc = a.scale_log2;
+        float l_own[2] = {0.f, 0.f};
+        bool ok = true;
+        if (rows_w > 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int st = t & 1, b = t & 1;
+                ok = tc::mbar_wait(bar(kBarSFull + w * 2 + b), (t >> 1) & 1);
+                tc::fence_after_sync();
+                float v[64];
+                {
+                    float tmp[32];
+                    const uint32_t sa = tmem + (uint32_t)(w * 128 + b * 64) + lane_off;
+                    tc::tmem_ld32(sa, tmp);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = tmp[i];
+                    if (NPH > 32) {
+                        tc::tmem_ld32(sa + 32, tmp);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[32 + i] = tmp[i];
+                    }
+                }
+                const uint4 mk = meta[st * kTileTok + j];
+                const uint32_t mw0 = w == 0 ? mk.x : mk.z, mw1 = w == 0 ? mk.y : mk.w;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const uint32_t mword = i < 32 ? mw0 : mw1;
+                    v[i] = ((mword >> (i & 31)) & 1u) ? v[i] * sc : -INFINITY;
+                }
+                tc::fence_before_sync();
+                // Column maxima of the tile.
+#pragma unroll
+                for (int g = 0; g < 64; g += 32) {
+                    if (g < NPH) {
+                        float tmp[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            tmp[i] = v[g + i];
+                        redw[wt * 64 + g + lane] = reduce_scatter32<true>(tmp, lane);
+                    }
+                }
+                if (tc::named_sync_or(nb_id, 128, !ok)) {
+                    ok = false;
+                    break;
+                }
+                if (j == 0)
+                    tc::mbar_arrive(bar(kBarSFree + w * 2 + b));
+                bool need = false;
+                if (j < NPH) {
+                    const float mt = fmaxf(fmaxf(redw[j], redw[64 + j]), fmaxf(redw[128 + j], redw[192 + j]));
+                    const float mo = m_s[j];
+                    const float mn = fmaxf(mo, mt);
+                    const float al = mn == -INFINITY ? 1.f : exp2f(mo - mn);
+                    m_s[j] = mn;
+                    alpha_s[j] = al;
+                    need = al != 1.f;
+                }
+                const bool rescale = tc::named_sync_or(nb_id, 128, need && t > 0);
+                if (t >= 1) {
+                    ok = tc::mbar_wait(bar(kBarPvDone + w), (t - 1) & 1);
+                    tc::fence_after_sync();
+                }
+                if (rescale) {
+#pragma unroll
+                    for (int g = 0; g < 64; g += 32) {
+                        if (g < NPH) {
+                            float o[32];
+                            tc::tmem_ld32(tmem_o + g, o);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                o[i] *= alpha_s[g + i];
+                            tc::tmem_st32(tmem_o + g, o);
+                            l_own[g >> 5] *= alpha_s[g + lane];
+                        }
+                    }
+                }
+                // Probabilities -> P^T (bf16), column sums of the fp32 values.
+#pragma unroll
+                for (int g = 0; g < 64; g += 32) {
+                    if (g < NPH) {
+                        float tmp[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int cc = g + i;
+                            const float pr = v[cc] == -INFINITY ? 0.f : exp2f(v[cc] - m_s[cc]);
+                            tmp[i] = pr;
+                            *reinterpret_cast<__nv_bfloat16 *>(smem + (prow - base) + cc * 128 +
+                                                               ((pch ^ (cc & 7)) << 4) + pin) =
+                                __float2bfloat16_rn(pr);
+                        }
+                        l_own[g >> 5] += reduce_scatter32<false>(tmp, lane);
+                    }
+                }
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                if (tc::named_sync_or(nb_id, 128, !ok)) {
+                    ok = false;
+                    break;
+                }
+                if (j == 0)
+                    tc::mbar_arrive(bar(kBarPFull + w));
+            }
+            if (ok && ntiles > 0) {
+                ok = tc::mbar_wait(bar(kBarPvDone + w), (ntiles - 1) & 1);
+                tc::fence_after_sync();
+            }
+            if (!ok)
+                *err = 1;
+            const bool failed = tc::named_sync_or(nb_id, 128, !ok || *err != 0);
+            // Normalisers and the partials of this warpgroup's rows.
+#pragma unroll
+            for (int g = 0; g < 64; g += 32)
+                if (g < NPH)
+                    redw[wt * 64 + g + lane] = l_own[g >> 5];
+            tc::named_sync(nb_id, 128);
+            if (j < NPH)
+                l_fin[j] = redw[j] + redw[64 + j] + redw[128 + j] + redw[192 + j];
+            tc::named_sync(nb_id, 128);
+            if (!failed) {
+#pragma unroll
+                for (int g = 0; g < 64; g += 32) {
+                    if (g < NPH) {
+                        float o[32];
+                        tc::tmem_ld32(tmem_o + g, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int cc = g + i;
+                            if (cc < rows_w) {
+                                const int r = w * NPH + cc;
+                                const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
+                                a.o_part[prw * kD + j] = o[i] / l_fin[cc];
+                            }
+                        }
+                    }
+                }
+                if (j < rows_w) {
+                    const int r = w * NPH + j;
+                    const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
+                    a.lse_part[prw] = m_s[j] + log2f(l_fin[j]);
+                }
+            }
         }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0)
-        tc::tmem_dealloc(tmem_base, kTmemCols);
+    if (*err && tid < 128) {
+        for (int r = 0; r < R; ++r) {
+            const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
+            a.o_part[prw * kD + tid] = __int_as_float(0x7fc00000);
+            if (tid == 0)
+                a.lse_part[prw] = __int_as_float(0x7fc00000);
+        }
+    }
+    if (warp == 9)
+        tc::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---- host: tensor maps over the paged KV, viewed as [pages*Hkv*16][128] ----
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+struct MapCache {
+    const void *ptr = nullptr;
+    uint64_t rows = 0;
+    CUtensorMap map;
+};
+
+bool kv_map(const void *ptr, uint64_t rows, MapCache &cache, CUtensorMap *out)
+{
+    if (cache.ptr == ptr && cache.rows == rows) {
+        *out = cache.map;
+        return true;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
+    if (!enc)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t estr[2] = {1, 1};
+    CUtensorMap m;
+    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    cache.ptr = ptr;
+    cache.rows = rows;
+    cache.map = m;
+    *out = m;
+    return true;
 }
 
 }  // namespace
@@ -374,16 +553,21 @@ int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, void *stream)
 {
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            phase1_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MmaSmem::alloc);
+        const cudaError_t e = cudaFuncSetAttribute(phase1_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)Smem::alloc);
         if (e != cudaSuccess)
             return (int)e;
         configured = true;
     }
     if (p.num_mma_items <= 0)
         return 0;
+    static MapCache ck, cv;
+    CUtensorMap mk, mv;
+    const uint64_t rows = (uint64_t)a.num_pages * a.num_kv_heads * kPageSize;
+    if (!kv_map(a.k_pages, rows, ck, &mk) || !kv_map(a.v_pages, rows, cv, &mv))
+        return (int)cudaErrorInvalidValue;
     const unsigned blocks = (unsigned)((int64_t)p.num_mma_items * a.num_kv_heads);
-    phase1_mma_kernel<<<blocks, kMThreads, MmaSmem::alloc, reinterpret_cast<cudaStream_t>(stream)>>>(a, p);
+    phase1_mma_kernel<<<blocks, kThreadsMma, Smem::alloc, reinterpret_cast<cudaStream_t>(stream)>>>(a, p, mk, mv);
     return (int)cudaGetLastError();
 }
 

@@ -34,17 +34,18 @@ int copy_out(const void *src, size_t n, void *dst, size_t bytes)
 
 // Layout of one partition inside the device blob.
 struct Layout {
-    size_t off[14];
+    size_t off[16];
 };
 
 void plan_partition_layout(const deft::Partition &p, size_t &cursor, Layout &L)
 {
-    const size_t sizes[14] = {vbytes(p.chunk_seg_off), vbytes(p.chunk_q_off), vbytes(p.chunk_tokens),
+    const size_t sizes[16] = {vbytes(p.chunk_seg_off), vbytes(p.chunk_q_off), vbytes(p.chunk_tokens),
                               vbytes(p.chunk_q),       vbytes(p.seg_node),    vbytes(p.seg_tok_begin),
                               vbytes(p.seg_tok_len),   vbytes(p.seg_chunk_pos), vbytes(p.seg_mask),
                               vbytes(p.q_slot_off),    vbytes(p.q_slot),      vbytes(p.fma_items),
-                              vbytes(p.mma_items),     vbytes(p.fallback_items)};
-    for (int i = 0; i < 14; ++i) {
+                              vbytes(p.mma_items),     vbytes(p.fallback_items), vbytes(p.seg_lmask_off),
+                              vbytes(p.seg_lmask)};
+    for (int i = 0; i < 16; ++i) {
         L.off[i] = cursor;
         cursor = align_up(cursor + (sizes[i] ? sizes[i] : 4));
     }
@@ -71,6 +72,8 @@ void fill_partition(const deft::Partition &p, const Layout &L, uint8_t *host,
     put(11, p.fma_items.data(), vbytes(p.fma_items));
     put(12, p.mma_items.data(), vbytes(p.mma_items));
     put(13, p.fallback_items.data(), vbytes(p.fallback_items));
+    put(14, p.seg_lmask_off.data(), vbytes(p.seg_lmask_off));
+    put(15, p.seg_lmask.data(), vbytes(p.seg_lmask));
     auto i32 = [&](int i) { return reinterpret_cast<const int32_t *>(dev + L.off[i]); };
     d.chunk_seg_off = i32(0);
     d.chunk_q_off = i32(1);
@@ -86,6 +89,8 @@ void fill_partition(const deft::Partition &p, const Layout &L, uint8_t *host,
     d.fma_items = i32(11);
     d.mma_items = i32(12);
     d.fallback_items = i32(13);
+    d.seg_lmask_off = i32(14);
+    d.seg_lmask = reinterpret_cast<const uint32_t *>(dev + L.off[15]);
     d.num_fma_items = (int32_t)(p.fma_items.size() / 3);
     d.num_mma_items = (int32_t)(p.mma_items.size() / 3);
     d.num_fallback_items = (int32_t)(p.fallback_items.size() / 3);

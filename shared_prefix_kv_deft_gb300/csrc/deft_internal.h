@@ -41,6 +41,10 @@ struct Partition {
     std::vector<int32_t> seg_chunk_pos;   // [S] token offset of the segment in its chunk
     std::vector<uint64_t> seg_mask;       // [S * W]
     std::vector<uint64_t> chunk_mask;     // [C * W]
+    // Segment s's queries as bits over its chunk's query list (bit k: the
+    // chunk's k-th query), ceil(|Q_c| / 32) words at seg_lmask_off[s].
+    std::vector<int32_t> seg_lmask_off;   // [S+1]
+    std::vector<uint32_t> seg_lmask;
     std::vector<int32_t> q_slot_off;      // [Q+1]
     std::vector<int32_t> q_slot;          // [slots]
     std::vector<int32_t> fma_items;       // [3 * n]
@@ -67,6 +71,8 @@ struct DevPartition {
     const int32_t *seg_tok_len;
     const int32_t *seg_chunk_pos;
     const uint64_t *seg_mask;
+    const int32_t *seg_lmask_off;
+    const uint32_t *seg_lmask;
     const int32_t *q_slot_off;
     const int32_t *q_slot;
     const int32_t *fma_items;

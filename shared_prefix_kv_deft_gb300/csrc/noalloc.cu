@@ -91,19 +91,21 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
 
     // Scratch layout: the tree partition's arrays, then the partials.
     const deft::Partition &p = plan->tree;
-    const void *src[14] = {p.chunk_seg_off.data(), p.chunk_q_off.data(), p.chunk_tokens.data(),
+    const void *src[16] = {p.chunk_seg_off.data(), p.chunk_q_off.data(), p.chunk_tokens.data(),
                            p.chunk_q.data(),       p.seg_node.data(),    p.seg_tok_begin.data(),
                            p.seg_tok_len.data(),   p.seg_chunk_pos.data(), p.seg_mask.data(),
                            p.q_slot_off.data(),    p.q_slot.data(),      p.fma_items.data(),
-                           p.mma_items.data(),     p.fallback_items.data()};
-    const size_t len[14] = {vbytes(p.chunk_seg_off), vbytes(p.chunk_q_off), vbytes(p.chunk_tokens),
+                           p.mma_items.data(),     p.fallback_items.data(), p.seg_lmask_off.data(),
+                           p.seg_lmask.data()};
+    const size_t len[16] = {vbytes(p.chunk_seg_off), vbytes(p.chunk_q_off), vbytes(p.chunk_tokens),
                             vbytes(p.chunk_q),       vbytes(p.seg_node),    vbytes(p.seg_tok_begin),
                             vbytes(p.seg_tok_len),   vbytes(p.seg_chunk_pos), vbytes(p.seg_mask),
                             vbytes(p.q_slot_off),    vbytes(p.q_slot),      vbytes(p.fma_items),
-                            vbytes(p.mma_items),     vbytes(p.fallback_items)};
-    size_t off[14];
+                            vbytes(p.mma_items),     vbytes(p.fallback_items), vbytes(p.seg_lmask_off),
+                            vbytes(p.seg_lmask)};
+    size_t off[16];
     size_t cursor = 0;
-    for (int i = 0; i < 14; ++i) {
+    for (int i = 0; i < 16; ++i) {
         off[i] = cursor;
         cursor = align_up(cursor + (len[i] ? len[i] : 4));
     }
@@ -124,7 +126,7 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
     if (rc != DEFT_OK)
         return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    for (int i = 0; i < 14; ++i)
+    for (int i = 0; i < 16; ++i)
         if (len[i] && cudaMemcpyAsync(base + off[i], src[i], len[i], cudaMemcpyHostToDevice, st) !=
                           cudaSuccess)
             return DEFT_ECUDA;
@@ -145,6 +147,8 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
     d.fma_items = i32(11);
     d.mma_items = i32(12);
     d.fallback_items = i32(13);
+    d.seg_lmask_off = i32(14);
+    d.seg_lmask = reinterpret_cast<const uint32_t *>(base + off[15]);
     d.num_fma_items = (int32_t)(p.fma_items.size() / 3);
     d.num_mma_items = (int32_t)(p.mma_items.size() / 3);
     d.num_fallback_items = (int32_t)(p.fallback_items.size() / 3);

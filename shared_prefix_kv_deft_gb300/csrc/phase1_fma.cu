@@ -91,19 +91,18 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items)
     const int cq0 = p.chunk_q_off[c] + qb;
     const int T = p.chunk_tokens[c];
     const int ntiles = (T + kTile - 1) / kTile;
-    const int W = p.mask_words;
 
     // Segment table of the chunk, with each segment's row mask: bit r is set
     // iff row r's query is in the segment's query bitmask.
     for (int s = tid; s < nseg; s += kThreads) {
         s_pos[s] = p.seg_chunk_pos[sb + s];
-        s_node[s] = p.seg_node[sb + s];
+        s_node[s] = a.node_page_off[p.seg_node[sb + s]];   // first page_id index of the node
         s_tb[s] = p.seg_tok_begin[sb + s];
-        const uint64_t *m = p.seg_mask + (size_t)(sb + s) * W;
+        const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
         uint32_t rm = 0;
         for (int r = 0; r < R; ++r) {
-            const int qid = p.chunk_q[cq0 + r / G];
-            rm |= (uint32_t)((m[qid >> 6] >> (qid & 63)) & 1ull) << r;
+            const int k = qb + r / G;
+            rm |= ((lm[k >> 5] >> (k & 31)) & 1u) << r;
         }
         s_rmask[s] = rm;
     }
@@ -147,7 +146,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items)
             if (pos < T) {
                 const int s = find_seg(pos);
                 const int t = s_tb[s] + pos - s_pos[s];
-                const int page = a.page_id[a.node_page_off[s_node[s]] + t / kPageSize];
+                const int page = a.page_id[s_node[s] + t / kPageSize];
                 const size_t off =
                     (((size_t)page * Hkv + h) * kPageSize + (t % kPageSize)) * D + lc * 8;
                 cp_async_16(smem_u32(kv_stage(st, kv) + (size_t)row * D * 2 + swz(row, lc) * 16),

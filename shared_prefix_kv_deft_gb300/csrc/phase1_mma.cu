@@ -119,7 +119,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
     const int cq0 = p.chunk_q_off[c] + qb;
     const int T = p.chunk_tokens[c];
     const int ntiles = (T + kTileTok - 1) / kTileTok;
-    const int W = p.mask_words;
     const int nwg = rows_w1 > 0 ? 2 : 1;
 
     // ---------------- set-up ----------------
@@ -139,13 +138,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
         reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
     for (int s = tid; s < nseg; s += kThreadsMma) {
         s_pos[s] = p.seg_chunk_pos[sb + s];
-        s_node[s] = p.seg_node[sb + s];
+        s_node[s] = a.node_page_off[p.seg_node[sb + s]];   // first page_id index of the node
         s_tb[s] = p.seg_tok_begin[sb + s];
-        const uint64_t *m = p.seg_mask + (size_t)(sb + s) * W;
+        const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
         uint32_t rm[4] = {0, 0, 0, 0};  // warpgroup 0 bits 0-63, warpgroup 1 bits 64-127
+#pragma unroll 4
         for (int r = 0; r < R; ++r) {
-            const int qid = p.chunk_q[cq0 + r / G];
-            const uint32_t bit = (uint32_t)((m[qid >> 6] >> (qid & 63)) & 1ull);
+            const int k = qb + r / G;
+            const uint32_t bit = (lm[k >> 5] >> (k & 31)) & 1u;
             const int col = r < NPH ? r : 64 + (r - NPH);
             rm[col >> 5] |= bit << (col & 31);
         }
@@ -198,7 +198,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
                             hi = mid - 1;
                     }
                     const int tk = s_tb[lo] + pos - s_pos[lo];
-                    const int page = a.page_id[a.node_page_off[s_node[lo]] + tk / kPageSize];
+                    const int page = a.page_id[s_node[lo] + tk / kPageSize];
                     off[k] = (((long long)page * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
                     segk[k] = lo;
                     tokk[k] = tk;

@@ -95,6 +95,24 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
                 p.chunk_q.push_back(q);
         p.chunk_q_off.push_back((int32_t)p.chunk_q.size());
     }
+    // Local masks: bit k of segment s = the chunk's k-th query sees s.
+    p.seg_lmask_off.assign(1, 0);
+    p.seg_lmask.clear();
+    for (int32_t c = 0; c < C; ++c) {
+        const int32_t q0 = p.chunk_q_off[c], nq = p.chunk_q_off[c + 1] - q0;
+        const int32_t words = (nq + 31) / 32;
+        for (int32_t s = p.chunk_seg_off[c]; s < p.chunk_seg_off[c + 1]; ++s) {
+            const uint64_t *m = &p.seg_mask[(size_t)s * W];
+            const size_t at = p.seg_lmask.size();
+            p.seg_lmask.resize(at + words, 0u);
+            for (int32_t k = 0; k < nq; ++k) {
+                const int32_t q = p.chunk_q[q0 + k];
+                if ((m[q / 64] >> (q % 64)) & 1ull)
+                    p.seg_lmask[at + k / 32] |= 1u << (k % 32);
+            }
+            p.seg_lmask_off.push_back((int32_t)p.seg_lmask.size());
+        }
+    }
     // Per-query slot CSR, slots in chunk order.
     std::vector<int32_t> cnt(num_queries + 1, 0);
     for (int32_t s = 0; s < p.num_slots(); ++s)

@@ -13,6 +13,11 @@
 #include <cuda_runtime.h>
 
 #include "deft_internal.h"
+#include "kprof.cuh"
+
+#ifdef DEFT_KPROF
+unsigned long long *g_kprof_buf = nullptr;
+#endif
 
 namespace {
 
@@ -194,6 +199,11 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
     a.head_dim = head_dim;
     a.gqa_group = plan->gqa_group;
     a.scale_log2 = scale * 1.44269504088896340736f;
+#ifdef DEFT_KPROF
+    if (!g_kprof_buf && cudaMalloc(&g_kprof_buf, deft::kKprofSlots * sizeof(unsigned long long)) != cudaSuccess)
+        g_kprof_buf = nullptr;
+    a.kprof = g_kprof_buf;
+#endif
     const size_t slots = (size_t)std::max(plan->tree.num_slots(), plan->naive.num_slots());
     a.o_part = reinterpret_cast<float *>(workspace);
     a.lse_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) +
@@ -225,10 +235,17 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
         // The tensor-core path covers head_dim 128; other head sizes, or a run
         // with DEFT_DISABLE_MMA set, take the same chunks on CUDA cores in
         // items of at most 16 rows.
-        if (use_mma)
-            rc = traced({DEFT_K_PHASE1_MMA, fam, 0, 0, dp.num_mma_items, 0.f}, stream,
-                        [&] { return deft::launch_phase1_mma(a, dp, stream); });
-        else
+        if (use_mma) {
+            for (int b = 0; b < 4 && !rc; ++b) {
+                const int32_t n = hp.mma_bucket_off[b + 1] - hp.mma_bucket_off[b];
+                if (n <= 0)
+                    continue;
+                const int32_t *it = dp.mma_items + 3 * (size_t)hp.mma_bucket_off[b];
+                rc = traced({DEFT_K_PHASE1_MMA, fam, b, 0, n, 0.f}, stream, [&] {
+                    return deft::launch_phase1_mma(a, dp, it, n, b, stream);
+                });
+            }
+        } else
             rc = fma_launches(dp.fallback_items, hp.fallback_bucket_off, 1);
         if (rc)
             return DEFT_ECUDA;
@@ -413,6 +430,20 @@ const char *deft_status_str(int status)
 }
 
 int deft_version(void) { return 100; }
+
+#ifdef DEFT_KPROF
+// Development builds only: copy the kernel timestamp slots to the host.
+int deft_kprof_read(unsigned long long *dst, size_t n)
+{
+    if (!g_kprof_buf)
+        return DEFT_ESTATE;
+    if (n > (size_t)deft::kKprofSlots)
+        n = deft::kKprofSlots;
+    return cudaMemcpy(dst, g_kprof_buf, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost) == cudaSuccess
+               ? DEFT_OK
+               : DEFT_ECUDA;
+}
+#endif
 
 int deft_trace_enable(int32_t on)
 {

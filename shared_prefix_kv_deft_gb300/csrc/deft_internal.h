@@ -54,6 +54,10 @@ struct Partition {
     // b = 0..4); bucket b is items [off[b], off[b+1]).
     std::array<int32_t, 6> fma_bucket_off{};
     std::array<int32_t, 6> fallback_bucket_off{};
+    // mma_items are sorted by column bucket b: each of the two softmax
+    // warpgroups of an item holds NPH = 16 (b + 1) query rows; bucket b is
+    // items [off[b], off[b+1]).
+    std::array<int32_t, 5> mma_bucket_off{};
     int32_t num_chunks() const { return (int32_t)chunk_tokens.size(); }
     int32_t num_segments() const { return (int32_t)seg_node.size(); }
     int32_t num_slots() const { return (int32_t)chunk_q.size(); }
@@ -130,6 +134,7 @@ struct AttnArgs {
     float scale_log2;         // scale * log2(e): logits are kept in base 2 on device
     float *o_part;            // fp32 [slots][Hq][d]
     float *lse_part;          // fp32 [slots][Hq], base-2 log-sum-exp of the base-2 logits
+    unsigned long long *kprof;  // timestamp slots (development builds only; else null)
 };
 
 // Launchers (return a cudaError_t cast to int; 0 = success).
@@ -137,9 +142,15 @@ struct AttnArgs {
 // bucket `bucket` (rows <= 2^bucket).
 int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
                       int bucket, void *stream);
-int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, void *stream);
+// One tensor-core launch over `n` items of column bucket `bucket`.
+int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
+                      int bucket, void *stream);
 // Row bucket of an item with `rows` rows: smallest b with rows <= 2^b.
 inline int row_bucket(int rows) { return rows <= 1 ? 0 : rows <= 2 ? 1 : rows <= 4 ? 2 : rows <= 8 ? 3 : 4; }
+// Rows per softmax warpgroup of a tensor-core item with `rows` rows (two
+// warpgroups share the rows; each takes a multiple of 16, at most 64).
+inline int mma_half_cols(int rows) { return (((rows + 1) / 2) + 15) & ~15; }
+inline int mma_bucket(int rows) { return mma_half_cols(rows) / 16 - 1; }
 int launch_phase2(const AttnArgs &a, const DevPartition &p, void *out, int32_t out_dtype,
                   float *lse, void *stream);
 bool mma_supported(int32_t head_dim);

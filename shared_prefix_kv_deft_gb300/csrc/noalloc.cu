@@ -183,8 +183,16 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
         return 0;
     };
     if (d.num_mma_items > 0) {
-        rc = use_mma ? deft::launch_phase1_mma(a, d, stream)
-                     : fma_launches(d.fallback_items, p.fallback_bucket_off);
+        if (use_mma) {
+            for (int b = 0; b < 4 && !rc; ++b) {
+                const int32_t n = p.mma_bucket_off[b + 1] - p.mma_bucket_off[b];
+                if (n > 0)
+                    rc = deft::launch_phase1_mma(a, d, d.mma_items + 3 * (size_t)p.mma_bucket_off[b], n, b,
+                                                 stream);
+            }
+        } else {
+            rc = fma_launches(d.fallback_items, p.fallback_bucket_off);
+        }
         if (rc)
             return DEFT_ECUDA;
     }

@@ -30,6 +30,7 @@
 // states are merged through shared memory at the end.
 #include "common.cuh"
 #include "deft_internal.h"
+#include "kprof.cuh"
 
 namespace deft {
 namespace {
@@ -82,6 +83,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items)
     float *ps = reinterpret_cast<float *>(smem + S::ps_off);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0)
+        KPROF(a, 2000);
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
     const int item = blockIdx.x / Hkv;
     const int h = blockIdx.x - item * Hkv;
@@ -178,13 +181,19 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items)
             issue_tile(st, st);
         cp_async_commit();
     }
+    if (tid == 0)
+        KPROF(a, 2001);
     for (int tile = 0; tile < ntiles; ++tile) {
         const int nxt = tile + kStages - 1;
         if (nxt < ntiles)
             issue_tile(nxt, nxt % kStages);
+        if (tid == 0)
+            KPROF(a, 2100 + 4 * tile);
         cp_async_commit();
         cp_async_wait<kStages - 1>();
         __syncthreads();
+        if (tid == 0)
+            KPROF(a, 2101 + 4 * tile);
 
         const int st = tile % kStages;
         const uint8_t *Ks = kv_stage(st, 0);
@@ -278,6 +287,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items)
             }
         }
         __syncthreads();
+        if (tid == 0)
+            KPROF(a, 2102 + 4 * tile);
     }
     cp_async_wait<0>();
     __syncthreads();

@@ -35,6 +35,7 @@
 
 #include "common.cuh"
 #include "deft_internal.h"
+#include "kprof.cuh"
 #include "tcgen05.cuh"
 
 namespace deft {
@@ -46,14 +47,14 @@ constexpr int kThreadsMma = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kHalf = 128 * 128;       // one 64-wide half of a 128-row operand (16 KB)
 constexpr uint32_t kTileBytes = 2 * kHalf;  // one 128 x 128 bf16 operand (32 KB)
-constexpr uint32_t kPHalf = 64 * 128;       // one token half of a warpgroup's P^T (64 rows)
+constexpr uint32_t kPBytes = 128 * 128;     // one warpgroup's P^T: 128 tokens x 64 columns, MN-major
 constexpr uint32_t kPageBytes = 4 * 2048;   // K + V of one 16-token page, four TMA boxes
 
 struct Smem {
     static constexpr uint32_t kv_off = 0;                       // [stage][K,V] operands
     static constexpr uint32_t q_off = kv_off + 4 * kTileBytes;  // Q^T, 128 rows
     static constexpr uint32_t p_off = q_off + kTileBytes;       // P^T per warpgroup (16 KB each)
-    static constexpr uint32_t meta_off = p_off + 2 * 2 * kPHalf;        // [stage][128] uint4
+    static constexpr uint32_t meta_off = p_off + 2 * kPBytes;          // [stage][128] uint4
     static constexpr uint32_t seg_off = meta_off + 2 * kTileTok * 16;   // pos, node, tb, masks
     static constexpr uint32_t red_off = seg_off + kMaxSegsPerChunk * (12 + 16);  // [wg][warp][64]
     static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;     // [wg][m, alpha, l][64]
@@ -88,9 +89,10 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
     return v[0];
 }
 
+template <int NPH>
 __global__ void __launch_bounds__(kThreadsMma, 1)
-phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v)
+phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
+                  const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v)
 {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -111,9 +113,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
     const int item = blockIdx.x / Hkv;
     const int h = blockIdx.x - item * Hkv;
-    const int c = p.mma_items[3 * item], qb = p.mma_items[3 * item + 1], qe = p.mma_items[3 * item + 2];
-    const int R = (qe - qb) * G;
-    const int NPH = ((R + 1) / 2 + 15) & ~15;  // columns per warpgroup
+    const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
+    const int R = (qe - qb) * G;  // NPH columns per warpgroup: mma_half_cols(R) == NPH
     const int rows_w1 = R > NPH ? R - NPH : 0;
     const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
     const int cq0 = p.chunk_q_off[c] + qb;
@@ -122,6 +123,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
     const int nwg = rows_w1 > 0 ? 2 : 1;
 
     // ---------------- set-up ----------------
+    if (tid == 0)
+        KPROF(a, 0);
     if (warp == 9) {
         tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tc::tmem_relinquish();
@@ -170,6 +173,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    if (tid == 0)
+        KPROF(a, 1);
 
     if (warp == 8) {
         // ---------------- producer ----------------
@@ -219,6 +224,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
                 if ((bal >> 16) == 0xffffu)
                     tma_pages |= 1u << (2 * k + 1);
             }
+            if (lane == 0)
+                KPROF(a, 100 + 4 * t);
             long long page_off = -1;
 #pragma unroll
             for (int pg = 0; pg < 8; ++pg) {
@@ -233,6 +240,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
                     break;
                 }
             }
+            if (lane == 0)
+                KPROF(a, 101 + 4 * t);
 #pragma unroll
             for (int k = 0; k < 4; ++k)
                 meta[st * kTileTok + lane + 32 * k] = rmk[k];
@@ -273,6 +282,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
                 tc::fence_proxy_async();
             }
             tc::mbar_arrive(bar(kBarFull + st));
+            if (lane == 0)
+                KPROF(a, 102 + 4 * t);
             last_tile[st] = t;
         }
         cp_async_wait<0>();
@@ -284,12 +295,13 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
         // ---------------- MMA issue ----------------
         if (lane == 0) {
             const uint32_t idesc_s = tc::idesc_bf16(128, NPH, 0, 0);
-            const uint32_t idesc_o = tc::idesc_bf16(128, NPH, 1, 0);
+            const uint32_t idesc_o = tc::idesc_bf16(128, NPH, 1, 1);
             bool ok = true;
             for (int t = 0; t <= ntiles && ok; ++t) {
                 if (t < ntiles) {
                     const int st = t & 1, b = t & 1;
                     ok = tc::mbar_wait(bar(kBarFull + st), (t >> 1) & 1);
+                    KPROF(a, 400 + 4 * t);
                     tc::fence_after_sync();
                     const uint32_t kb = base + Smem::kv_off + (uint32_t)(st * 2) * kTileBytes;
                     for (int w = 0; w < nwg && ok; ++w) {
@@ -307,6 +319,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
                         }
                         tc::mma_commit(bar(kBarSFull + w * 2 + b));
                     }
+                    KPROF(a, 401 + 4 * t);
                 }
                 if (t >= 1 && ok) {
                     const int tp = t - 1, stp = tp & 1;
@@ -314,17 +327,18 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
                     for (int w = 0; w < nwg && ok; ++w) {
                         ok = tc::mbar_wait(bar(kBarPFull + w), tp & 1);
                         tc::fence_after_sync();
-                        const uint32_t pb = base + Smem::p_off + (uint32_t)w * 2 * kPHalf;
+                        const uint32_t pb = base + Smem::p_off + (uint32_t)w * kPBytes;
                         const uint32_t d_o = tmem + 256 + (uint32_t)(w * 64);
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
                             const uint64_t ad = tc::smem_desc(vb + s * 2048, kHalf, 1024);
-                            const uint64_t bd = tc::smem_desc(pb + (s >> 2) * kPHalf + (s & 3) * 32, 16, 1024);
+                            const uint64_t bd = tc::smem_desc(pb + s * 2048, kPBytes, 1024);
                             tc::mma_bf16(d_o, ad, bd, idesc_o, (tp > 0 || s > 0) ? 1u : 0u);
                         }
                         tc::mma_commit(bar(kBarPvDone + w));
                     }
                     tc::mma_commit(bar(kBarEmpty + stp));
+                    KPROF(a, 402 + 4 * tp);
                 }
             }
             if (!ok)
@@ -332,6 +346,11 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
         }
     } else {
         // ---------------- softmax warpgroups ----------------
+        // Thread j owns token j of every tile (TMEM lane j) and, at the end,
+        // output dimension j.  The column maximum m_c is exact after the
+        // first tile and is only raised, with a rescale of O and l, when a
+        // later logit exceeds it by more than 2^8; in between each thread
+        // keeps its own partial column sums l_c, combined once at the end.
         const int w = warp >> 2, wt = warp & 3, j = tid & 127;
         const int rows_w = w == 0 ? (R < NPH ? R : NPH) : rows_w1;
         const uint32_t nb_id = 1 + (uint32_t)w;
@@ -339,110 +358,140 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
         float *redw = red + w * 256;
         const uint32_t lane_off = (uint32_t)(wt * 32) << 16;
         const uint32_t tmem_o = tmem + 256 + (uint32_t)(w * 64) + lane_off;
-        const uint32_t prow = base + Smem::p_off + (uint32_t)w * 2 * kPHalf + (j >> 6) * kPHalf;
-        const int pch = (j & 63) >> 3, pin = (j & 7) * 2;
+        uint8_t *prow_ptr = smem + Smem::p_off + (uint32_t)w * kPBytes + (j >> 3) * 1024 + (j & 7) * 128;
         const float sc = a.scale_log2;
-        float l_own[2] = {0.f, 0.f};
+        constexpr float kSlack = 8.f;   // rescale only when 2^(s - m) would exceed 2^8
+        float l[NPH];
+#pragma unroll
+        for (int c2 = 0; c2 < NPH; ++c2)
+            l[c2] = 0.f;
         bool ok = true;
+        auto load_cols = [&](uint32_t taddr, float *v) {
+#pragma unroll
+            for (int g = 0; g + 32 <= NPH; g += 32) {
+                float tmp[32];
+                tc::tmem_ld32(taddr + g, tmp);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    v[g + i] = tmp[i];
+            }
+            if constexpr (NPH % 32 != 0)
+                tc::tmem_ld16(taddr + (NPH & ~31), v + (NPH & ~31));
+        };
+        // Exact column maxima of s over the warpgroup's 128 tokens -> redw,
+        // reduced by the caller after a barrier.
+        auto tile_max_to_smem = [&](const float *v) {
+#pragma unroll
+            for (int g = 0; g < NPH; g += 32) {
+                float tmp[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    tmp[i] = (g + i < NPH) ? v[g + i] : -INFINITY;
+                redw[wt * 64 + g + lane] = reduce_scatter32<true>(tmp, lane);
+            }
+        };
         if (rows_w > 0) {
             for (int t = 0; t < ntiles; ++t) {
                 const int st = t & 1, b = t & 1;
                 ok = tc::mbar_wait(bar(kBarSFull + w * 2 + b), (t >> 1) & 1);
+                if (tid == 0)
+                    KPROF(a, 700 + 4 * t);
                 tc::fence_after_sync();
-                float v[64];
-                {
-                    float tmp[32];
-                    const uint32_t sa = tmem + (uint32_t)(w * 128 + b * 64) + lane_off;
-                    tc::tmem_ld32(sa, tmp);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        v[i] = tmp[i];
-                    if (NPH > 32) {
-                        tc::tmem_ld32(sa + 32, tmp);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[32 + i] = tmp[i];
-                    }
-                }
+                float s[NPH];
+                load_cols(tmem + (uint32_t)(w * 128 + b * 64) + lane_off, s);
                 const uint4 mk = meta[st * kTileTok + j];
                 const uint32_t mw0 = w == 0 ? mk.x : mk.z, mw1 = w == 0 ? mk.y : mk.w;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
+                for (int i = 0; i < NPH; ++i) {
                     const uint32_t mword = i < 32 ? mw0 : mw1;
-                    v[i] = ((mword >> (i & 31)) & 1u) ? v[i] * sc : -INFINITY;
+                    s[i] = ((mword >> (i & 31)) & 1u) ? s[i] * sc : -INFINITY;
                 }
                 tc::fence_before_sync();
-                // Column maxima of the tile.
+                bool slow = t == 0;
+                if (t > 0) {
+                    bool flag = false;
 #pragma unroll
-                for (int g = 0; g < 64; g += 32) {
-                    if (g < NPH) {
-                        float tmp[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            tmp[i] = v[g + i];
-                        redw[wt * 64 + g + lane] = reduce_scatter32<true>(tmp, lane);
+                    for (int i = 0; i < NPH; i += 4) {
+                        const float4 m4 = *reinterpret_cast<const float4 *>(m_s + i);
+                        flag |= (s[i] > m4.x + kSlack) | (s[i + 1] > m4.y + kSlack) |
+                                (s[i + 2] > m4.z + kSlack) | (s[i + 3] > m4.w + kSlack);
+                    }
+                    if (tc::named_sync_or(nb_id, 128, flag || !ok)) {
+                        if (tc::named_sync_or(nb_id, 128, !ok)) {
+                            ok = false;
+                            break;
+                        }
+                        slow = true;
                     }
                 }
-                if (tc::named_sync_or(nb_id, 128, !ok)) {
-                    ok = false;
-                    break;
+                if (slow) {
+                    tile_max_to_smem(s);
+                    if (tc::named_sync_or(nb_id, 128, !ok)) {
+                        ok = false;
+                        break;
+                    }
+                    if (j < NPH) {
+                        const float mt = fmaxf(fmaxf(redw[j], redw[64 + j]), fmaxf(redw[128 + j], redw[192 + j]));
+                        const float mo = t == 0 ? -INFINITY : m_s[j];
+                        const float mn = fmaxf(mo, mt);
+                        alpha_s[j] = mn == -INFINITY ? 1.f : tc::ex2(mo - mn);
+                        m_s[j] = mn;
+                    }
+                    tc::named_sync(nb_id, 128);
                 }
                 if (j == 0)
                     tc::mbar_arrive(bar(kBarSFree + w * 2 + b));
-                bool need = false;
-                if (j < NPH) {
-                    const float mt = fmaxf(fmaxf(redw[j], redw[64 + j]), fmaxf(redw[128 + j], redw[192 + j]));
-                    const float mo = m_s[j];
-                    const float mn = fmaxf(mo, mt);
-                    const float al = mn == -INFINITY ? 1.f : exp2f(mo - mn);
-                    m_s[j] = mn;
-                    alpha_s[j] = al;
-                    need = al != 1.f;
-                }
-                const bool rescale = tc::named_sync_or(nb_id, 128, need && t > 0);
+                bool ok2 = true;
                 if (t >= 1) {
-                    ok = tc::mbar_wait(bar(kBarPvDone + w), (t - 1) & 1);
+                    ok2 = tc::mbar_wait(bar(kBarPvDone + w), (t - 1) & 1);
                     tc::fence_after_sync();
                 }
-                if (rescale) {
+                if (slow && t >= 1) {
 #pragma unroll
-                    for (int g = 0; g < 64; g += 32) {
-                        if (g < NPH) {
-                            float o[32];
-                            tc::tmem_ld32(tmem_o + g, o);
+                    for (int g = 0; g < NPH; g += 16) {
+                        float o[16];
+                        tc::tmem_ld16(tmem_o + g, o);
 #pragma unroll
-                            for (int i = 0; i < 32; ++i)
-                                o[i] *= alpha_s[g + i];
-                            tc::tmem_st32(tmem_o + g, o);
-                            l_own[g >> 5] *= alpha_s[g + lane];
+                        for (int i = 0; i < 16; ++i) {
+                            o[i] *= alpha_s[g + i];
+                            l[g + i] *= alpha_s[g + i];
                         }
+                        tc::tmem_st16(tmem_o + g, o);
                     }
                 }
-                // Probabilities -> P^T (bf16), column sums of the fp32 values.
+                if (tid == 0)
+                    KPROF(a, 702 + 4 * t);
+                // Probabilities: fp32 column sums, bf16 P^T row (MN-major,
+                // 16-byte chunks swizzled by token).
 #pragma unroll
-                for (int g = 0; g < 64; g += 32) {
-                    if (g < NPH) {
-                        float tmp[32];
+                for (int ch = 0; ch < NPH / 8; ++ch) {
+                    const float4 ma = *reinterpret_cast<const float4 *>(m_s + 8 * ch);
+                    const float4 mb = *reinterpret_cast<const float4 *>(m_s + 8 * ch + 4);
+                    const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+                    float pv[8];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int cc = g + i;
-                            const float pr = v[cc] == -INFINITY ? 0.f : exp2f(v[cc] - m_s[cc]);
-                            tmp[i] = pr;
-                            *reinterpret_cast<__nv_bfloat16 *>(smem + (prow - base) + cc * 128 +
-                                                               ((pch ^ (cc & 7)) << 4) + pin) =
-                                __float2bfloat16_rn(pr);
-                        }
-                        l_own[g >> 5] += reduce_scatter32<false>(tmp, lane);
+                    for (int i = 0; i < 8; ++i) {
+                        const float x = s[8 * ch + i];
+                        pv[i] = x == -INFINITY ? 0.f : tc::ex2(x - mm[i]);
+                        l[8 * ch + i] += pv[i];
                     }
+                    uint4 packed;
+                    packed.x = tc::pack_bf16x2(pv[0], pv[1]);
+                    packed.y = tc::pack_bf16x2(pv[2], pv[3]);
+                    packed.z = tc::pack_bf16x2(pv[4], pv[5]);
+                    packed.w = tc::pack_bf16x2(pv[6], pv[7]);
+                    *reinterpret_cast<uint4 *>(prow_ptr + ((ch ^ (j & 7)) << 4)) = packed;
                 }
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
-                if (tc::named_sync_or(nb_id, 128, !ok)) {
+                if (tc::named_sync_or(nb_id, 128, !ok2)) {
                     ok = false;
                     break;
                 }
                 if (j == 0)
                     tc::mbar_arrive(bar(kBarPFull + w));
+                if (tid == 0)
+                    KPROF(a, 703 + 4 * t);
             }
             if (ok && ntiles > 0) {
                 ok = tc::mbar_wait(bar(kBarPvDone + w), (ntiles - 1) & 1);
@@ -451,36 +500,38 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
             if (!ok)
                 *err = 1;
             const bool failed = tc::named_sync_or(nb_id, 128, !ok || *err != 0);
-            // Normalisers and the partials of this warpgroup's rows.
+            // Column sums over the warpgroup, then O / l for this warpgroup's rows.
 #pragma unroll
-            for (int g = 0; g < 64; g += 32)
-                if (g < NPH)
-                    redw[wt * 64 + g + lane] = l_own[g >> 5];
+            for (int g = 0; g < NPH; g += 32) {
+                float tmp[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    tmp[i] = (g + i < NPH) ? l[g + i] : 0.f;
+                redw[wt * 64 + g + lane] = reduce_scatter32<false>(tmp, lane);
+            }
             tc::named_sync(nb_id, 128);
             if (j < NPH)
-                l_fin[j] = redw[j] + redw[64 + j] + redw[128 + j] + redw[192 + j];
+                l_fin[j] = 1.f / (redw[j] + redw[64 + j] + redw[128 + j] + redw[192 + j]);
             tc::named_sync(nb_id, 128);
             if (!failed) {
 #pragma unroll
-                for (int g = 0; g < 64; g += 32) {
-                    if (g < NPH) {
-                        float o[32];
-                        tc::tmem_ld32(tmem_o + g, o);
+                for (int g = 0; g < NPH; g += 16) {
+                    float o[16];
+                    tc::tmem_ld16(tmem_o + g, o);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int cc = g + i;
-                            if (cc < rows_w) {
-                                const int r = w * NPH + cc;
-                                const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
-                                a.o_part[prw * kD + j] = o[i] / l_fin[cc];
-                            }
+                    for (int i = 0; i < 16; ++i) {
+                        const int cc = g + i;
+                        if (cc < rows_w) {
+                            const int r = w * NPH + cc;
+                            const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
+                            a.o_part[prw * kD + j] = o[i] * l_fin[cc];
                         }
                     }
                 }
                 if (j < rows_w) {
                     const int r = w * NPH + j;
                     const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
-                    a.lse_part[prw] = m_s[j] + log2f(l_fin[j]);
+                    a.lse_part[prw] = m_s[j] - log2f(l_fin[j]);
                 }
             }
         }
@@ -497,6 +548,23 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const __grid_constant__ CUtensorMa
     }
     if (warp == 9)
         tc::tmem_dealloc(tmem, kTmemCols);
+    if (tid == 0)
+        KPROF(a, 1000);
+#ifdef DEFT_KPROF
+    if (blockIdx.x == 0 && tid == 0 && a.kprof) {
+        unsigned long long g0, g1;
+        long long c0 = clock64();
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g0));
+        for (int i = 0; i < 200000; ++i)
+            asm volatile("" ::: "memory");
+        long long c1 = clock64();
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g1));
+        a.kprof[3000] = g0;
+        a.kprof[3001] = (unsigned long long)c0;
+        a.kprof[3002] = g1;
+        a.kprof[3003] = (unsigned long long)c1;
+    }
+#endif
 }
 
 // ---- host: tensor maps over the paged KV, viewed as [pages*Hkv*16][128] ----
@@ -545,30 +613,44 @@ bool kv_map(const void *ptr, uint64_t rows, MapCache &cache, CUtensorMap *out)
     return true;
 }
 
-}  // namespace
-
-bool mma_supported(int32_t head_dim) { return head_dim == kD; }
-
-int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, void *stream)
+template <int NPH>
+int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
+                const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st)
 {
     static bool configured = false;
     if (!configured) {
-        const cudaError_t e = cudaFuncSetAttribute(phase1_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)Smem::alloc);
+        const cudaError_t e = cudaFuncSetAttribute(phase1_mma_kernel<NPH>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::alloc);
         if (e != cudaSuccess)
             return (int)e;
         configured = true;
     }
-    if (p.num_mma_items <= 0)
+    const unsigned blocks = (unsigned)((int64_t)n * a.num_kv_heads);
+    phase1_mma_kernel<NPH><<<blocks, kThreadsMma, Smem::alloc, st>>>(a, p, items, mk, mv);
+    return (int)cudaGetLastError();
+}
+
+}  // namespace
+
+bool mma_supported(int32_t head_dim) { return head_dim == kD; }
+
+int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
+                      int bucket, void *stream)
+{
+    if (n <= 0)
         return 0;
     static MapCache ck, cv;
     CUtensorMap mk, mv;
     const uint64_t rows = (uint64_t)a.num_pages * a.num_kv_heads * kPageSize;
     if (!kv_map(a.k_pages, rows, ck, &mk) || !kv_map(a.v_pages, rows, cv, &mv))
         return (int)cudaErrorInvalidValue;
-    const unsigned blocks = (unsigned)((int64_t)p.num_mma_items * a.num_kv_heads);
-    phase1_mma_kernel<<<blocks, kThreadsMma, Smem::alloc, reinterpret_cast<cudaStream_t>(stream)>>>(a, p, mk, mv);
-    return (int)cudaGetLastError();
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    switch (bucket) {
+    case 0: return launch_cols<16>(a, p, items, n, mk, mv, st);
+    case 1: return launch_cols<32>(a, p, items, n, mk, mv, st);
+    case 2: return launch_cols<48>(a, p, items, n, mk, mv, st);
+    default: return launch_cols<64>(a, p, items, n, mk, mv, st);
+    }
 }
 
 }  // namespace deft

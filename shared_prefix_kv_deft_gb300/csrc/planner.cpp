@@ -143,7 +143,8 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
         const int32_t nb = (k + qmax_mma - 1) / qmax_mma;
         const int32_t per = (k + nb - 1) / nb;
         for (int32_t b = 0; b < k; b += per)
-            mma.push_back({c, b, std::min(k, b + per), tok * (std::min(k, b + per) - b)});
+            mma.push_back({c, b, std::min(k, b + per), tok * (std::min(k, b + per) - b),
+                           mma_bucket((std::min(k, b + per) - b) * G)});
         const int32_t nf = (k + qmax_fb - 1) / qmax_fb;
         const int32_t perf = (k + nf - 1) / nf;
         for (int32_t b = 0; b < k; b += perf)
@@ -157,11 +158,11 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
             return x.bucket < y.bucket;
         return x.cost != y.cost ? x.cost > y.cost : (x.c != y.c ? x.c < y.c : x.b < y.b);
     };
-    auto bucket_offsets = [](const std::vector<Item> &v, std::array<int32_t, 6> &off) {
+    auto bucket_offsets = [](const std::vector<Item> &v, auto &off) {
         off.fill(0);
         for (const Item &it : v)
             off[it.bucket + 1] += 1;
-        for (int b = 0; b < 5; ++b)
+        for (size_t b = 0; b + 1 < off.size(); ++b)
             off[b + 1] += off[b];
     };
     std::stable_sort(fma.begin(), fma.end(), by_cost);
@@ -180,6 +181,7 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     emit(fb, p.fallback_items);
     bucket_offsets(fma, p.fma_bucket_off);
     bucket_offsets(fb, p.fallback_bucket_off);
+    bucket_offsets(mma, p.mma_bucket_off);
 }
 
 }  // namespace

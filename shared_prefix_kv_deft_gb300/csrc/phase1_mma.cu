@@ -7,25 +7,28 @@
 // Grouping), for chunks shared by enough queries that S = q.K^T and O = P.V
 // are dense contractions worth the tensor cores.
 //
-// Formulation: KV tokens on the MMA M dimension (128-token tiles), query
-// rows on N.  The rows are split into two halves of NPH columns (NPH = R/2
-// rounded up to 16), one per softmax warpgroup:
-//     S_w^T[128 tok x NPH]  = K_tile . Q_w^T            (TMEM, fp32, 2 buffers)
-//     O_w^T[128 d   x NPH] += V_tile^T . P_w^T          (TMEM, fp32)
-// so a thread owns one token of S^T (one output dimension of O^T).  Column
-// maxima and sums are warp butterflies (reduce-scatter: lane l ends with
-// column l) plus a 4-warp exchange in shared memory.  Logits are base 2.
+// Formulation: KV tokens on the MMA M dimension (128-token tiles), the
+// item's query rows on N (RP = rows rounded to 16, at most 128):
+//     S^T[128 tok x RP]  = K_tile . Q^T            (TMEM, fp32, 2 buffers)
+//     O^T[128 d   x RP] += V_tile^T . P^T          (TMEM, fp32)
+// Eight MMAs (K = 16 each) per product and tile.  Two softmax warpgroups
+// split the RP columns (NPH each, a template parameter); a thread owns one
+// token of S^T and, at the end, one output dimension of O^T.  The column
+// maximum is exact after the first tile and afterwards only raised (with a
+// rescale of O and of the per-thread column sums) when a logit exceeds it
+// by more than 2^8, decided by a warpgroup vote.  Logits are base 2.
 //
 // Roles (10 warps):
 //   warps 0-3, 4-7  softmax warpgroups 0 and 1 (row halves);
-//   warp 8          producer: resolves every token row through the page
-//                   table one tile ahead, loads full pages with TMA (four
-//                   2 KB boxes of the 128-byte-swizzled layout) and ragged
-//                   rows (node tails, packed one-token nodes) with 16-byte
-//                   cp.async at the exact token count;
-//   warp 9          allocates TMEM; lane 0 issues the MMAs: S(t) for both
-//                   halves, then P.V of tile t-1, so the tensor core works
-//                   on the next tile while the warpgroups do softmax.
+//   warps 8, 10     K and V producers: resolve the tile's pages through the
+//                   page table one tile ahead, load full aligned pages with
+//                   TMA (2 KB boxes of the 128-byte-swizzled layout) and
+//                   ragged rows (node tails, packed one-token nodes) with
+//                   16-byte cp.async at the exact token count; K of a stage
+//                   is refilled as soon as S of the tile two back is done,
+//                   V once its P.V is done;
+//   warp 9          allocates TMEM; lane 0 issues the MMAs, S(t) and P.V(t-1)
+//                   in whichever order their inputs become ready.
 // Two KV stages; every hand-off is an mbarrier, every wait on one is
 // bounded.  A CTA whose wait runs out writes NaN partials (the step's
 // output then shows the failure), waits for its own copies, frees TMEM and
@@ -43,34 +46,35 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTileTok = 128;
-constexpr int kThreadsMma = 320;
+constexpr int kThreadsMma = 352;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kHalf = 128 * 128;       // one 64-wide half of a 128-row operand (16 KB)
 constexpr uint32_t kTileBytes = 2 * kHalf;  // one 128 x 128 bf16 operand (32 KB)
-constexpr uint32_t kPBytes = 128 * 128;     // one warpgroup's P^T: 128 tokens x 64 columns, MN-major
-constexpr uint32_t kPageBytes = 4 * 2048;   // K + V of one 16-token page, four TMA boxes
+constexpr uint32_t kHalfPage = 2 * 2048;    // K (or V) of one 16-token page: two TMA boxes
 
 struct Smem {
-    static constexpr uint32_t kv_off = 0;                       // [stage][K,V] operands
-    static constexpr uint32_t q_off = kv_off + 4 * kTileBytes;  // Q^T, 128 rows
-    static constexpr uint32_t p_off = q_off + kTileBytes;       // P^T per warpgroup (16 KB each)
-    static constexpr uint32_t meta_off = p_off + 2 * kPBytes;          // [stage][128] uint4
-    static constexpr uint32_t seg_off = meta_off + 2 * kTileTok * 16;   // pos, node, tb, masks
+    static constexpr uint32_t kv_off = 0;                            // [stage][K,V] operands
+    static constexpr uint32_t q_off = kv_off + 4 * kTileBytes;       // Q^T: [d half][128 rows][128 B]
+    static constexpr uint32_t p_off = q_off + kTileBytes;            // P^T: [col block][128 tok][128 B]
+    static constexpr uint32_t meta_off = p_off + kTileBytes;         // [4 slots][128] uint4 row masks
+    static constexpr uint32_t seg_off = meta_off + 4 * kTileTok * 16;  // pos, page base, tb, masks
     static constexpr uint32_t red_off = seg_off + kMaxSegsPerChunk * (12 + 16);  // [wg][warp][64]
-    static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;     // [wg][m, alpha, l][64]
-    static constexpr uint32_t bar_off = stat_off + 2 * 3 * 64 * 4;     // 16 mbarriers
-    static constexpr uint32_t misc_off = bar_off + 16 * 8;             // tmem base, error flag
+    static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;  // [wg][m, alpha, 1/l][64]
+    static constexpr uint32_t bar_off = stat_off + 2 * 3 * 64 * 4;  // mbarriers
+    static constexpr uint32_t misc_off = bar_off + 16 * 8;          // tmem base, error flag
     static constexpr uint32_t total = misc_off + 16;
     static constexpr uint32_t alloc = total + 1024;
 };
 
 // mbarrier slots
-constexpr int kBarFull = 0;     // [2] stage loaded (producer)
-constexpr int kBarEmpty = 2;    // [2] stage consumed (MMA commit)
-constexpr int kBarSFull = 4;    // [wg*2 + buf] S ready (MMA commit)
-constexpr int kBarSFree = 8;    // [wg*2 + buf] S read (warpgroup)
-constexpr int kBarPFull = 12;   // [wg] P written (warpgroup)
-constexpr int kBarPvDone = 14;  // [wg] P.V finished (MMA commit)
+constexpr int kBarFullK = 0;   // [2] K of a stage landed (producer: 32 lanes + tx)
+constexpr int kBarFullV = 2;   // [2] V of a stage landed
+constexpr int kBarEmptyK = 4;  // [2] S of the stage's tile finished (MMA commit)
+constexpr int kBarEmptyV = 6;  // [2] P.V of the stage's tile finished (MMA commit)
+constexpr int kBarSFull = 8;   // [2] S buffer ready (MMA commit)
+constexpr int kBarSFree = 10;  // [2] S buffer read (one arrival per warpgroup)
+constexpr int kBarPFull = 12;  // P written (one arrival per warpgroup)
+constexpr int kBarPvDone = 13; // P.V finished (MMA commit)
 
 template <bool kMax>
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
@@ -100,8 +104,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     uint8_t *smem = smem_raw + (base - raw);
     uint4 *meta = reinterpret_cast<uint4 *>(smem + Smem::meta_off);
     int32_t *s_pos = reinterpret_cast<int32_t *>(smem + Smem::seg_off);
-    int32_t *s_node = s_pos + kMaxSegsPerChunk;
-    int32_t *s_tb = s_node + kMaxSegsPerChunk;
+    int32_t *s_pgb = s_pos + kMaxSegsPerChunk;
+    int32_t *s_tb = s_pgb + kMaxSegsPerChunk;
     uint4 *s_rmask = reinterpret_cast<uint4 *>(smem + Smem::seg_off + kMaxSegsPerChunk * 12);
     float *red = reinterpret_cast<float *>(smem + Smem::red_off);
     float *stat = reinterpret_cast<float *>(smem + Smem::stat_off);
@@ -114,13 +118,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     const int item = blockIdx.x / Hkv;
     const int h = blockIdx.x - item * Hkv;
     const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
-    const int R = (qe - qb) * G;  // NPH columns per warpgroup: mma_half_cols(R) == NPH
+    const int R = (qe - qb) * G;  // mma_half_cols(R) == NPH
     const int rows_w1 = R > NPH ? R - NPH : 0;
+    const int nwg = rows_w1 > 0 ? 2 : 1;
+    const int RP = nwg * NPH;     // MMA N
     const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
     const int cq0 = p.chunk_q_off[c] + qb;
     const int T = p.chunk_tokens[c];
     const int ntiles = (T + kTileTok - 1) / kTileTok;
-    const int nwg = rows_w1 > 0 ? 2 : 1;
 
     // ---------------- set-up ----------------
     if (tid == 0)
@@ -130,18 +135,26 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(bar(kBarFull + 0), 33);
-        tc::mbar_init(bar(kBarFull + 1), 33);
-        for (int i = kBarEmpty; i < 16; ++i)
+        for (int i = kBarFullK; i < kBarEmptyK; ++i)
+            tc::mbar_init(bar(i), 33);
+        for (int i = kBarEmptyK; i < kBarSFree; ++i)
             tc::mbar_init(bar(i), 1);
+        tc::mbar_init(bar(kBarSFree + 0), nwg);
+        tc::mbar_init(bar(kBarSFree + 1), nwg);
+        tc::mbar_init(bar(kBarPFull), nwg);
+        tc::mbar_init(bar(kBarPvDone), 1);
         *err = 0;
         tc::fence_mbar_init();
+    }
+    if (warp == 8 && lane == 0) {
+        tc::prefetch_tmap(&tmap_k);
+        tc::prefetch_tmap(&tmap_v);
     }
     for (uint32_t i = tid; i < Smem::meta_off / 16; i += kThreadsMma)
         reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
     for (int s = tid; s < nseg; s += kThreadsMma) {
         s_pos[s] = p.seg_chunk_pos[sb + s];
-        s_node[s] = a.node_page_off[p.seg_node[sb + s]];   // first page_id index of the node
+        s_pgb[s] = a.node_page_off[p.seg_node[sb + s]];   // first page_id index of the node
         s_tb[s] = p.seg_tok_begin[sb + s];
         const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
         uint32_t rm[4] = {0, 0, 0, 0};  // warpgroup 0 bits 0-63, warpgroup 1 bits 64-127
@@ -153,10 +166,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             rm[col >> 5] |= bit << (col & 31);
         }
         s_rmask[s] = make_uint4(rm[0], rm[1], rm[2], rm[3]);
-    }
-    if (tid < 128) {
-        stat[(tid >> 6) * 192 + (tid & 63)] = -INFINITY;    // m
-        stat[(tid >> 6) * 192 + 64 + (tid & 63)] = 1.f;     // alpha
     }
     __syncthreads();
     const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
@@ -176,23 +185,25 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     if (tid == 0)
         KPROF(a, 1);
 
-    if (warp == 8) {
-        // ---------------- producer ----------------
-        const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
-        const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
-        int last_tile[2] = {-1, -1};
-        for (int t = 0; t < ntiles; ++t) {
-            const int st = t & 1;
-            long long off[4];
-            uint4 rmk[4];
-            int segk[4], tokk[4];
+    if (warp == 8 || warp == 10) {
+        // ---------------- producers (warp 8: K, warp 10: V) ----------------
+        const int kv = warp == 8 ? 0 : 1;
+        const __nv_bfloat16 *src_base = reinterpret_cast<const __nv_bfloat16 *>(kv ? a.v_pages : a.k_pages);
+        const CUtensorMap *tm = kv ? &tmap_v : &tmap_k;
+        if (lane == 0)
+            tc::prefetch_tmap(tm);
+        // One tile's resolution: rows lane + 32k (k < 4) and pages 0..7.
+        struct Res {
+            int seg[4], tok[4], pid[4];   // per row; pid only for ragged rows
+            int page_y;                   // lane < 8: TMA row coordinate of page `lane`
+            uint32_t tma_pages;
+        };
+        auto resolve = [&](int t, Res &r) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int pos = t * kTileTok + lane + 32 * k;
-                off[k] = -1;
-                segk[k] = -1;
-                tokk[k] = 1;
-                rmk[k] = make_uint4(0, 0, 0, 0);
+                r.seg[k] = -1;
+                r.tok[k] = 1;
                 if (pos < T) {
                     int lo = 0, hi = nseg - 1;
                     while (lo < hi) {
@@ -202,78 +213,104 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         else
                             hi = mid - 1;
                     }
-                    const int tk = s_tb[lo] + pos - s_pos[lo];
-                    const int page = a.page_id[s_node[lo] + tk / kPageSize];
-                    off[k] = (((long long)page * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
-                    segk[k] = lo;
-                    tokk[k] = tk;
-                    rmk[k] = s_rmask[lo];
+                    r.seg[k] = lo;
+                    r.tok[k] = s_tb[lo] + pos - s_pos[lo];
                 }
             }
-            // Page p of the tile (rows 16p..16p+15) goes by TMA when its 16
-            // rows are one aligned page of one segment.
-            uint32_t tma_pages = 0;
+            uint32_t tp = 0;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int s_first = __shfl_sync(0xffffffffu, segk[k], lane & 16);
-                const int t_first = __shfl_sync(0xffffffffu, tokk[k], lane & 16);
-                const bool ok = off[k] >= 0 && segk[k] == s_first && (t_first % kPageSize) == 0;
+                const int s_first = __shfl_sync(0xffffffffu, r.seg[k], lane & 16);
+                const int t_first = __shfl_sync(0xffffffffu, r.tok[k], lane & 16);
+                const bool ok = r.seg[k] >= 0 && r.seg[k] == s_first && (t_first % kPageSize) == 0;
                 const uint32_t bal = __ballot_sync(0xffffffffu, ok);
                 if ((bal & 0xffffu) == 0xffffu)
-                    tma_pages |= 1u << (2 * k);
+                    tp |= 1u << (2 * k);
                 if ((bal >> 16) == 0xffffu)
-                    tma_pages |= 1u << (2 * k + 1);
+                    tp |= 1u << (2 * k + 1);
             }
-            if (lane == 0)
-                KPROF(a, 100 + 4 * t);
-            long long page_off = -1;
+            r.tma_pages = tp;
+            // Page ids: one load per TMA page (lanes 0-7), one per ragged row.
+            int pseg = -1, ptok = 0;
 #pragma unroll
             for (int pg = 0; pg < 8; ++pg) {
-                const long long o = __shfl_sync(0xffffffffu, off[pg >> 1], 16 * (pg & 1));
-                if (lane == pg)
-                    page_off = o;
+                const int sg = __shfl_sync(0xffffffffu, r.seg[pg >> 1], 16 * (pg & 1));
+                const int tk = __shfl_sync(0xffffffffu, r.tok[pg >> 1], 16 * (pg & 1));
+                if (lane == pg) {
+                    pseg = sg;
+                    ptok = tk;
+                }
             }
+            r.page_y = -1;
+            if (lane < 8 && ((tp >> lane) & 1u))
+                r.page_y = a.page_id[s_pgb[pseg] + ptok / kPageSize];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                r.pid[k] = -1;
+                if (r.seg[k] >= 0 && !((tp >> ((lane + 32 * k) >> 4)) & 1u))
+                    r.pid[k] = a.page_id[s_pgb[r.seg[k]] + r.tok[k] / kPageSize];
+            }
+        };
+        int last_tile[2] = {-1, -1};
+        Res res;
+        if (ntiles > 0)
+            resolve(0, res);
+        for (int t = 0; t < ntiles; ++t) {
+            const int st = t & 1;
             if (t >= 2) {
-                const bool ok = __all_sync(0xffffffffu, tc::mbar_wait(bar(kBarEmpty + st), ((t - 2) >> 1) & 1));
+                const bool ok = __all_sync(
+                    0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((t - 2) >> 1) & 1));
                 if (!ok) {
                     *err = 1;
                     break;
                 }
             }
-            if (lane == 0)
-                KPROF(a, 101 + 4 * t);
+            if (kv == 0) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                meta[st * kTileTok + lane + 32 * k] = rmk[k];
-            const uint32_t kst = base + Smem::kv_off + (uint32_t)(st * 2) * kTileBytes;
-            const uint32_t vst = kst + kTileBytes;
-            if (lane == 0)
-                tc::mbar_arrive_expect_tx(bar(kBarFull + st), __popc(tma_pages) * kPageBytes);
-            __syncwarp();
-            if (lane < 8 && ((tma_pages >> lane) & 1u)) {
-                const int y = (int)(page_off >> 7);
-                const uint32_t row_b = (uint32_t)(16 * lane) * 128;
-                tc::tma_load_2d(kst + row_b, &tmap_k, 0, y, bar(kBarFull + st));
-                tc::tma_load_2d(kst + kHalf + row_b, &tmap_k, 64, y, bar(kBarFull + st));
-                tc::tma_load_2d(vst + row_b, &tmap_v, 0, y, bar(kBarFull + st));
-                tc::tma_load_2d(vst + kHalf + row_b, &tmap_v, 64, y, bar(kBarFull + st));
+                for (int k = 0; k < 4; ++k)
+                    meta[(t & 3) * kTileTok + lane + 32 * k] =
+                        res.seg[k] >= 0 ? s_rmask[res.seg[k]] : make_uint4(0, 0, 0, 0);
             }
-            // Remaining valid rows, one row per warp step.
+            const uint32_t full = bar((kv ? kBarFullV : kBarFullK) + st);
+            const uint32_t dst = base + Smem::kv_off + (uint32_t)(st * 2 + kv) * kTileBytes;
+            if (lane == 0)
+                tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
+            __syncwarp();
+            if (res.page_y >= 0) {
+                const int y = (res.page_y * Hkv + h) * kPageSize;
+                const uint32_t row_b = (uint32_t)(16 * lane) * 128;
+                tc::tma_load_2d(dst + row_b, tm, 0, y, full);
+                tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full);
+            }
+            // Ragged rows: two rows per warp step, 16 lanes (16-byte chunks) each.
             bool any_cp = false;
-            const int kv = lane >> 4, ch = lane & 15;
-            const uint32_t dst0 = (kv ? vst : kst) + (ch >> 3) * kHalf;
-            const __nv_bfloat16 *src0 = (kv ? vg : kg) + ch * 8;
+            const __nv_bfloat16 *src0 = src_base + (lane & 15) * 8;
+            const uint32_t dst0 = dst + ((lane & 15) >> 3) * kHalf;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const bool need = off[k] >= 0 && !((tma_pages >> ((lane + 32 * k) >> 4)) & 1u);
-                uint32_t nb = __ballot_sync(0xffffffffu, need);
+                uint32_t nb = __ballot_sync(0xffffffffu, res.pid[k] >= 0);
                 any_cp |= nb != 0;
                 while (nb) {
-                    const int src_lane = __ffs(nb) - 1;
+                    const int l0 = __ffs(nb) - 1;
                     nb &= nb - 1;
-                    const int row = src_lane + 32 * k;
-                    const long long o = __shfl_sync(0xffffffffu, off[k], src_lane);
-                    cp_async_16(dst0 + row * 128 + (((ch & 7) ^ (row & 7)) << 4), src0 + o);
+                    int l1 = -1;
+                    if (nb) {
+                        l1 = __ffs(nb) - 1;
+                        nb &= nb - 1;
+                    }
+                    const int mine = lane < 16 ? l0 : l1;
+                    const int p0 = __shfl_sync(0xffffffffu, res.pid[k], l0);
+                    const int t0 = __shfl_sync(0xffffffffu, res.tok[k], l0);
+                    const int p1 = __shfl_sync(0xffffffffu, res.pid[k], l1 < 0 ? l0 : l1);
+                    const int t1 = __shfl_sync(0xffffffffu, res.tok[k], l1 < 0 ? l0 : l1);
+                    if (mine >= 0) {
+                        const int row = mine + 32 * k;
+                        const int pg = lane < 16 ? p0 : p1;
+                        const int tk = lane < 16 ? t0 : t1;
+                        const long long o = (((long long)pg * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
+                        const int ch = lane & 7;
+                        cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src0 + o);
+                    }
                 }
             }
             if (any_cp) {
@@ -281,90 +318,111 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 cp_async_wait<0>();
                 tc::fence_proxy_async();
             }
-            tc::mbar_arrive(bar(kBarFull + st));
-            if (lane == 0)
+            tc::mbar_arrive(full);
+            if (lane == 0 && kv == 0)
                 KPROF(a, 102 + 4 * t);
             last_tile[st] = t;
+            if (t + 1 < ntiles)
+                resolve(t + 1, res);
+            if (lane == 0 && kv == 0)
+                KPROF(a, 100 + 4 * (t + 1));
         }
         cp_async_wait<0>();
         // Do not leave while a TMA copy of ours may still be landing.
         for (int s2 = 0; s2 < 2; ++s2)
             if (last_tile[s2] >= 0)
-                tc::mbar_wait(bar(kBarFull + s2), (last_tile[s2] >> 1) & 1);
+                tc::mbar_wait(bar((kv ? kBarFullV : kBarFullK) + s2), (last_tile[s2] >> 1) & 1);
     } else if (warp == 9) {
         // ---------------- MMA issue ----------------
         if (lane == 0) {
-            const uint32_t idesc_s = tc::idesc_bf16(128, NPH, 0, 0);
-            const uint32_t idesc_o = tc::idesc_bf16(128, NPH, 1, 1);
+            const uint32_t idesc_s = tc::idesc_bf16(128, RP, 0, 0);
+            const uint32_t idesc_o = tc::idesc_bf16(128, RP, 1, 1);
+            // Descriptors of k-step 0; step s adds an address offset (16-byte units).
+            const uint64_t dq = tc::smem_desc(base + Smem::q_off, 16, 1024);
+            const uint64_t dp = tc::smem_desc(base + Smem::p_off, kHalf, 1024);
+            uint64_t dk[2], dv[2];
+            for (int st = 0; st < 2; ++st) {
+                dk[st] = tc::smem_desc(base + Smem::kv_off + (uint32_t)(st * 2) * kTileBytes, 16, 1024);
+                dv[st] = tc::smem_desc(base + Smem::kv_off + (uint32_t)(st * 2 + 1) * kTileBytes, kHalf, 1024);
+            }
             bool ok = true;
-            for (int t = 0; t <= ntiles && ok; ++t) {
-                if (t < ntiles) {
-                    const int st = t & 1, b = t & 1;
-                    ok = tc::mbar_wait(bar(kBarFull + st), (t >> 1) & 1);
-                    KPROF(a, 400 + 4 * t);
-                    tc::fence_after_sync();
-                    const uint32_t kb = base + Smem::kv_off + (uint32_t)(st * 2) * kTileBytes;
-                    for (int w = 0; w < nwg && ok; ++w) {
-                        if (t >= 2) {
-                            ok = tc::mbar_wait(bar(kBarSFree + w * 2 + b), ((t - 2) >> 1) & 1);
-                            tc::fence_after_sync();
-                        }
-                        const uint32_t qb_addr = base + Smem::q_off + (uint32_t)(w * NPH) * 128;
-                        const uint32_t d_s = tmem + (uint32_t)(w * 128 + b * 64);
-#pragma unroll
-                        for (int s = 0; s < 8; ++s) {
-                            const uint64_t ad = tc::smem_desc(kb + (s >> 2) * kHalf + (s & 3) * 32, 16, 1024);
-                            const uint64_t bd = tc::smem_desc(qb_addr + (s >> 2) * kHalf + (s & 3) * 32, 16, 1024);
-                            tc::mma_bf16(d_s, ad, bd, idesc_s, s > 0 ? 1u : 0u);
-                        }
-                        tc::mma_commit(bar(kBarSFull + w * 2 + b));
-                    }
-                    KPROF(a, 401 + 4 * t);
-                }
-                if (t >= 1 && ok) {
-                    const int tp = t - 1, stp = tp & 1;
-                    const uint32_t vb = base + Smem::kv_off + (uint32_t)(stp * 2 + 1) * kTileBytes;
-                    for (int w = 0; w < nwg && ok; ++w) {
-                        ok = tc::mbar_wait(bar(kBarPFull + w), tp & 1);
+            int ts = 0, tpv = 0;   // next S tile, next P.V tile
+            uint32_t polls = 0;
+            while (tpv < ntiles && ok) {
+                bool progressed = false;
+                // S(ts): needs K(ts) and S buffer ts % 2 released by tile ts - 2.
+                if (ts < ntiles && ts <= tpv + 1) {
+                    const int st = ts & 1, b = ts & 1;
+                    if (tc::mbar_test(bar(kBarFullK + st), (ts >> 1) & 1) &&
+                        (ts < 2 || tc::mbar_test(bar(kBarSFree + b), ((ts - 2) >> 1) & 1))) {
+                        if (tid == 288)
+                            KPROF(a, 400 + 4 * ts);
                         tc::fence_after_sync();
-                        const uint32_t pb = base + Smem::p_off + (uint32_t)w * kPBytes;
-                        const uint32_t d_o = tmem + 256 + (uint32_t)(w * 64);
+                        const uint32_t d_s = tmem + (uint32_t)(b * 128);
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
-                            const uint64_t ad = tc::smem_desc(vb + s * 2048, kHalf, 1024);
-                            const uint64_t bd = tc::smem_desc(pb + s * 2048, kPBytes, 1024);
-                            tc::mma_bf16(d_o, ad, bd, idesc_o, (tp > 0 || s > 0) ? 1u : 0u);
+                            const uint64_t ko = (uint64_t)(((s >> 2) * kHalf + (s & 3) * 32) >> 4);
+                            tc::mma_bf16(d_s, dk[st] + ko, dq + ko, idesc_s, s > 0 ? 1u : 0u);
                         }
-                        tc::mma_commit(bar(kBarPvDone + w));
+                        tc::mma_commit(bar(kBarSFull + b));
+                        tc::mma_commit(bar(kBarEmptyK + st));
+                        if (tid == 288)
+                            KPROF(a, 401 + 4 * ts);
+                        ++ts;
+                        progressed = true;
                     }
-                    tc::mma_commit(bar(kBarEmpty + stp));
-                    KPROF(a, 402 + 4 * tp);
                 }
+                // P.V(tpv): needs V(tpv) and P(tpv).
+                if (tpv < ts) {
+                    const int stp = tpv & 1;
+                    if (tc::mbar_test(bar(kBarFullV + stp), (tpv >> 1) & 1) &&
+                        tc::mbar_test(bar(kBarPFull), tpv & 1)) {
+                        tc::fence_after_sync();
+                        const uint32_t d_o = tmem + 256;
+#pragma unroll
+                        for (int s = 0; s < 8; ++s) {
+                            const uint64_t so = (uint64_t)((s * 2048) >> 4);
+                            tc::mma_bf16(d_o, dv[stp] + so, dp + so, idesc_o, (tpv > 0 || s > 0) ? 1u : 0u);
+                        }
+                        tc::mma_commit(bar(kBarPvDone));
+                        tc::mma_commit(bar(kBarEmptyV + stp));
+                        if (tid == 288)
+                            KPROF(a, 402 + 4 * tpv);
+                        ++tpv;
+                        progressed = true;
+                    }
+                }
+                if (progressed)
+                    polls = 0;
+                else if (++polls > (1u << 24))
+                    ok = false;
             }
             if (!ok)
                 *err = 1;
         }
     } else {
         // ---------------- softmax warpgroups ----------------
-        // Thread j owns token j of every tile (TMEM lane j) and, at the end,
-        // output dimension j.  The column maximum m_c is exact after the
-        // first tile and is only raised, with a rescale of O and l, when a
-        // later logit exceeds it by more than 2^8; in between each thread
-        // keeps its own partial column sums l_c, combined once at the end.
+        // Warpgroup w owns columns [w*NPH, w*NPH + NPH) of S^T and O^T.
         const int w = warp >> 2, wt = warp & 3, j = tid & 127;
         const int rows_w = w == 0 ? (R < NPH ? R : NPH) : rows_w1;
         const uint32_t nb_id = 1 + (uint32_t)w;
-        float *m_s = stat + w * 192, *alpha_s = m_s + 64, *l_fin = m_s + 128;
+        float *m_s = stat + w * 192, *alpha_s = m_s + 64, *linv = m_s + 128;
         float *redw = red + w * 256;
         const uint32_t lane_off = (uint32_t)(wt * 32) << 16;
-        const uint32_t tmem_o = tmem + 256 + (uint32_t)(w * 64) + lane_off;
-        uint8_t *prow_ptr = smem + Smem::p_off + (uint32_t)w * kPBytes + (j >> 3) * 1024 + (j & 7) * 128;
+        const uint32_t col0 = (uint32_t)(w * NPH);
+        const uint32_t tmem_o = tmem + 256 + lane_off + col0;
+        uint8_t *prow_ptr = smem + Smem::p_off + (j >> 3) * 1024 + (j & 7) * 128;
         const float sc = a.scale_log2;
         constexpr float kSlack = 8.f;   // rescale only when 2^(s - m) would exceed 2^8
         float l[NPH];
 #pragma unroll
         for (int c2 = 0; c2 < NPH; ++c2)
             l[c2] = 0.f;
+        if (j < 64) {
+            m_s[j] = -INFINITY;
+            alpha_s[j] = 1.f;
+        }
+        tc::named_sync(nb_id, 128);
         bool ok = true;
         auto load_cols = [&](uint32_t taddr, float *v) {
 #pragma unroll
@@ -378,8 +436,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             if constexpr (NPH % 32 != 0)
                 tc::tmem_ld16(taddr + (NPH & ~31), v + (NPH & ~31));
         };
-        // Exact column maxima of s over the warpgroup's 128 tokens -> redw,
-        // reduced by the caller after a barrier.
         auto tile_max_to_smem = [&](const float *v) {
 #pragma unroll
             for (int g = 0; g < NPH; g += 32) {
@@ -392,14 +448,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         };
         if (rows_w > 0) {
             for (int t = 0; t < ntiles; ++t) {
-                const int st = t & 1, b = t & 1;
-                ok = tc::mbar_wait(bar(kBarSFull + w * 2 + b), (t >> 1) & 1);
+                const int b = t & 1;
+                ok = tc::mbar_wait(bar(kBarSFull + b), (t >> 1) & 1);
                 if (tid == 0)
                     KPROF(a, 700 + 4 * t);
                 tc::fence_after_sync();
                 float s[NPH];
-                load_cols(tmem + (uint32_t)(w * 128 + b * 64) + lane_off, s);
-                const uint4 mk = meta[st * kTileTok + j];
+                load_cols(tmem + (uint32_t)(b * 128) + lane_off + col0, s);
+                const uint4 mk = meta[(t & 3) * kTileTok + j];
                 const uint32_t mw0 = w == 0 ? mk.x : mk.z, mw1 = w == 0 ? mk.y : mk.w;
 #pragma unroll
                 for (int i = 0; i < NPH; ++i) {
@@ -432,7 +488,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     }
                     if (j < NPH) {
                         const float mt = fmaxf(fmaxf(redw[j], redw[64 + j]), fmaxf(redw[128 + j], redw[192 + j]));
-                        const float mo = t == 0 ? -INFINITY : m_s[j];
+                        const float mo = m_s[j];
                         const float mn = fmaxf(mo, mt);
                         alpha_s[j] = mn == -INFINITY ? 1.f : tc::ex2(mo - mn);
                         m_s[j] = mn;
@@ -440,10 +496,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     tc::named_sync(nb_id, 128);
                 }
                 if (j == 0)
-                    tc::mbar_arrive(bar(kBarSFree + w * 2 + b));
+                    tc::mbar_arrive(bar(kBarSFree + b));
                 bool ok2 = true;
                 if (t >= 1) {
-                    ok2 = tc::mbar_wait(bar(kBarPvDone + w), (t - 1) & 1);
+                    ok2 = tc::mbar_wait(bar(kBarPvDone), (t - 1) & 1);
                     tc::fence_after_sync();
                 }
                 if (slow && t >= 1) {
@@ -461,8 +517,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
                 if (tid == 0)
                     KPROF(a, 702 + 4 * t);
-                // Probabilities: fp32 column sums, bf16 P^T row (MN-major,
-                // 16-byte chunks swizzled by token).
+                // Probabilities: fp32 column sums, bf16 P^T (MN-major: token
+                // row j holds the columns, 16-byte chunks swizzled by j % 8).
 #pragma unroll
                 for (int ch = 0; ch < NPH / 8; ++ch) {
                     const float4 ma = *reinterpret_cast<const float4 *>(m_s + 8 * ch);
@@ -480,7 +536,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     packed.y = tc::pack_bf16x2(pv[2], pv[3]);
                     packed.z = tc::pack_bf16x2(pv[4], pv[5]);
                     packed.w = tc::pack_bf16x2(pv[6], pv[7]);
-                    *reinterpret_cast<uint4 *>(prow_ptr + ((ch ^ (j & 7)) << 4)) = packed;
+                    const int q8 = (int)(col0 >> 3) + ch;   // global 8-column chunk
+                    *reinterpret_cast<uint4 *>(prow_ptr + (q8 >> 3) * kHalf + (((q8 & 7) ^ (j & 7)) << 4)) = packed;
                 }
                 tc::fence_proxy_async();
                 tc::fence_before_sync();
@@ -489,12 +546,12 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     break;
                 }
                 if (j == 0)
-                    tc::mbar_arrive(bar(kBarPFull + w));
+                    tc::mbar_arrive(bar(kBarPFull));
                 if (tid == 0)
                     KPROF(a, 703 + 4 * t);
             }
             if (ok && ntiles > 0) {
-                ok = tc::mbar_wait(bar(kBarPvDone + w), (ntiles - 1) & 1);
+                ok = tc::mbar_wait(bar(kBarPvDone), (ntiles - 1) & 1);
                 tc::fence_after_sync();
             }
             if (!ok)
@@ -511,7 +568,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             }
             tc::named_sync(nb_id, 128);
             if (j < NPH)
-                l_fin[j] = 1.f / (redw[j] + redw[64 + j] + redw[128 + j] + redw[192 + j]);
+                linv[j] = 1.f / (redw[j] + redw[64 + j] + redw[128 + j] + redw[192 + j]);
             tc::named_sync(nb_id, 128);
             if (!failed) {
 #pragma unroll
@@ -524,14 +581,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         if (cc < rows_w) {
                             const int r = w * NPH + cc;
                             const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
-                            a.o_part[prw * kD + j] = o[i] * l_fin[cc];
+                            a.o_part[prw * kD + j] = o[i] * linv[cc];
                         }
                     }
                 }
                 if (j < rows_w) {
                     const int r = w * NPH + j;
                     const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
-                    a.lse_part[prw] = m_s[j] - log2f(l_fin[j]);
+                    a.lse_part[prw] = m_s[j] - log2f(linv[j]);
                 }
             }
         }
@@ -550,21 +607,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         tc::tmem_dealloc(tmem, kTmemCols);
     if (tid == 0)
         KPROF(a, 1000);
-#ifdef DEFT_KPROF
-    if (blockIdx.x == 0 && tid == 0 && a.kprof) {
-        unsigned long long g0, g1;
-        long long c0 = clock64();
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g0));
-        for (int i = 0; i < 200000; ++i)
-            asm volatile("" ::: "memory");
-        long long c1 = clock64();
-        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g1));
-        a.kprof[3000] = g0;
-        a.kprof[3001] = (unsigned long long)c0;
-        a.kprof[3002] = g1;
-        a.kprof[3003] = (unsigned long long)c1;
-    }
-#endif
 }
 
 // ---- host: tensor maps over the paged KV, viewed as [pages*Hkv*16][128] ----

@@ -258,3 +258,35 @@ __device__ __forceinline__ bool named_sync_or(uint32_t id, uint32_t count, bool 
 
 }  // namespace tc
 }  // namespace deft
+
+namespace deft {
+namespace tc {
+
+// Bring a TMA descriptor (kernel parameter) into the descriptor cache.
+__device__ __forceinline__ void prefetch_tmap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+}  // namespace tc
+}  // namespace deft
+
+namespace deft {
+namespace tc {
+
+// Non-blocking test of the phase with parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+}  // namespace tc
+}  // namespace deft

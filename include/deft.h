@@ -162,7 +162,8 @@ size_t deft_workspace_bytes(const deft_plan_t *plan, int32_t num_q_heads, int32_
  * and lse.  Chunks with >= 16 rows run on tcgen05 tensor cores (head_dim
  * 128), the others on CUDA-core FMA.
  *   q, k_pages, v_pages, node_page_off, page_id, out, lse, workspace: device
- *     pointers as described at the top of this file; workspace must be
+ *     pointers as described at the top of this file; q, k_pages and v_pages
+ *     must be 16-byte aligned (else DEFT_EINVAL); workspace must be
  *     256-byte aligned and hold deft_workspace_bytes(plan, num_q_heads,
  *     head_dim) bytes; its contents need not be initialised.  num_pages
  *     bounds page_id's values (checked only by a debug build).

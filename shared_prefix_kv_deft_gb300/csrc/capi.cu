@@ -6,6 +6,7 @@
 // kernels) and phase 2 on the caller's stream without allocating or
 // synchronising.
 #include <cmath>
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -170,6 +171,8 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
         return DEFT_EINVAL;
     if (num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
         return DEFT_EINVAL;
+    if (((uintptr_t)q | (uintptr_t)k_pages | (uintptr_t)v_pages) & 15u)
+        return DEFT_EINVAL;   // the kernels copy q and KV rows in 16-byte pieces
     if ((head_dim != 64 && head_dim != 128) || page_size != deft::kPageSize)
         return DEFT_EUNSUPPORTED;
     if (num_q_heads / num_kv_heads != plan->gqa_group || !plan->uploaded)
@@ -217,14 +220,15 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
     int rc = 0;
     const int32_t fam = naive ? 1 : 0;
     // CUDA-core launches, one per row bucket.
-    auto fma_launches = [&](const int32_t *items, const std::array<int32_t, 6> &off, int fb) {
+    auto fma_launches = [&](const int32_t *items, const std::vector<int64_t> &cost,
+                            const std::array<int32_t, 6> &off, int fb) {
         for (int b = 0; b < 5; ++b) {
             const int32_t n = off[b + 1] - off[b];
             if (n <= 0)
                 continue;
             const int32_t *it = items + 3 * (size_t)off[b];
             const int r = traced({DEFT_K_PHASE1_FMA, fam, b, fb, n, 0.f}, stream, [&] {
-                return deft::launch_phase1_fma(a, dp, it, n, b, stream);
+                return deft::launch_phase1_fma(a, dp, it, cost.data() + off[b], n, b, stream);
             });
             if (r)
                 return r;
@@ -246,12 +250,12 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
                 });
             }
         } else
-            rc = fma_launches(dp.fallback_items, hp.fallback_bucket_off, 1);
+            rc = fma_launches(dp.fallback_items, hp.fallback_cost, hp.fallback_bucket_off, 1);
         if (rc)
             return DEFT_ECUDA;
     }
     if (dp.num_fma_items > 0) {
-        rc = fma_launches(dp.fma_items, hp.fma_bucket_off, 0);
+        rc = fma_launches(dp.fma_items, hp.fma_cost, hp.fma_bucket_off, 0);
         if (rc)
             return DEFT_ECUDA;
     }

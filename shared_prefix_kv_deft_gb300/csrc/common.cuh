@@ -47,6 +47,13 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst_smem, const void *src)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst_smem), "l"(src));
 }
 
+// Arrive on the mbarrier at `bar` once this thread's earlier cp.async copies
+// have landed; the arrival counts toward the barrier's expected count.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;\n" ::);

@@ -27,6 +27,7 @@ constexpr int kFmaMaxRows = 16;        // rows (queries x GQA group) per CUDA-co
 constexpr int kMmaMaxRows = 128;       // rows per tensor-core item (one MMA N extent)
 constexpr int kMmaMinRows = 16;        // a chunk with this many rows goes to the tensor path
 constexpr int kSharedTokensPerRow = 16;  // long-chunk rule for shared nodes (see planner.cpp)
+constexpr int kUnitOverheadTokens = 64;  // fixed cost of a CUDA-core unit, in tokens
 
 // One partition, host side.  Items are (chunk, q_begin, q_end) triples where
 // [q_begin, q_end) indexes the chunk's query list.
@@ -54,6 +55,12 @@ struct Partition {
     // b = 0..4); bucket b is items [off[b], off[b+1]).
     std::array<int32_t, 6> fma_bucket_off{};
     std::array<int32_t, 6> fallback_bucket_off{};
+    // Host-only cost prefix sums over fma_items / fallback_items ([n+1]):
+    // entry i is the summed cost of items before i, one KV head each, an
+    // item costing its chunk's tokens plus kUnitOverheadTokens.  The
+    // CUDA-core launch cuts its units into contiguous, equal-cost CTA ranges.
+    std::vector<int64_t> fma_cost;
+    std::vector<int64_t> fallback_cost;
     // mma_items are sorted by column bucket b: each of the two softmax
     // warpgroups of an item holds NPH = 16 (b + 1) query rows; bucket b is
     // items [off[b], off[b+1]).
@@ -140,8 +147,9 @@ struct AttnArgs {
 // Launchers (return a cudaError_t cast to int; 0 = success).
 // One CUDA-core launch over `n` items (device triples at `items`), all of row
 // bucket `bucket` (rows <= 2^bucket).
-int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
-                      int bucket, void *stream);
+// `cost` points at the items' host cost prefix (n + 1 entries).
+int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
+                      int32_t n, int bucket, void *stream);
 // One tensor-core launch over `n` items of column bucket `bucket`.
 int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
                       int bucket, void *stream);

@@ -21,6 +21,7 @@
 // streams, or different host threads without ordering) race on the array.
 #include <atomic>
 #include <cmath>
+#include <cstdint>
 #include <cstdlib>
 
 #include <cuda_runtime.h>
@@ -80,6 +81,8 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
         return DEFT_EINVAL;
     if (num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
         return DEFT_EINVAL;
+    if (((uintptr_t)q | (uintptr_t)k_pages | (uintptr_t)v_pages) & 15u)
+        return DEFT_EINVAL;   // the kernels copy q and KV rows in 16-byte pieces
     if ((head_dim != 64 && head_dim != 128) || page_size != deft::kPageSize)
         return DEFT_EUNSUPPORTED;
     if (num_q_heads / num_kv_heads != plan->gqa_group)
@@ -171,11 +174,13 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
     a.o_part = reinterpret_cast<float *>(base + o_off);
     a.lse_part = reinterpret_cast<float *>(base + lse_off);
 
-    auto fma_launches = [&](const int32_t *items, const std::array<int32_t, 6> &boff) {
+    auto fma_launches = [&](const int32_t *items, const std::vector<int64_t> &cost,
+                            const std::array<int32_t, 6> &boff) {
         for (int b = 0; b < 5; ++b) {
             const int32_t n = boff[b + 1] - boff[b];
             if (n > 0) {
-                const int r = deft::launch_phase1_fma(a, d, items + 3 * (size_t)boff[b], n, b, stream);
+                const int r = deft::launch_phase1_fma(a, d, items + 3 * (size_t)boff[b], cost.data() + boff[b], n,
+                                                      b, stream);
                 if (r)
                     return r;
             }
@@ -191,12 +196,12 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
                                                  stream);
             }
         } else {
-            rc = fma_launches(d.fallback_items, p.fallback_bucket_off);
+            rc = fma_launches(d.fallback_items, p.fallback_cost, p.fallback_bucket_off);
         }
         if (rc)
             return DEFT_ECUDA;
     }
-    if (d.num_fma_items > 0 && fma_launches(d.fma_items, p.fma_bucket_off))
+    if (d.num_fma_items > 0 && fma_launches(d.fma_items, p.fma_cost, p.fma_bucket_off))
         return DEFT_ECUDA;
     return deft::launch_phase2(a, d, out, out_dtype, lse, stream) ? DEFT_ECUDA : DEFT_OK;
 }

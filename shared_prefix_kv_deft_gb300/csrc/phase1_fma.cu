@@ -1,382 +1,735 @@
 // phase1_fma.cu -- phase-1 partial attention on CUDA cores, for work items
 // with fewer than 16 rows (rows = queries of the item x GQA group).
 //
-// What one thread block computes (DeFT Guide, "Deep Dive": tree-constrained
-// attention and online-softmax tile accumulation; DeFT abstract: KV-Guided
-// Grouping): for one chunk c, one KV head h and the item's rows r (query k,
-// group member g, query head h*G+g), over the chunk's tokens j whose segment
-// bitmask contains the row's query,
-//     s_rj = (q_r . k_j) * scale,  m_r = max_j s_rj,  l_r = sum_j 2^... ,
-//     o_r = sum_j exp(s_rj - m_r) v_j / l_r,  L_r = log-sum-exp of s_r,
-// and stores o_r (fp32) and L_r (base 2) in the partial slot of (c, k).
-// Logits are carried in base 2 (q pre-scaled by scale * log2 e) so that the
-// exponentials are single exp2 instructions; phase 2 converts back.
+// What a work unit (item = chunk + query range, one KV head h) computes
+// (DeFT Guide, "Deep Dive": tree-constrained attention and online-softmax
+// tile accumulation; DeFT abstract: KV-Guided Grouping): for the unit's rows
+// r (query k, group member g, query head h*G+g), over the chunk's tokens j
+// whose segment bitmask contains the row's query,
+//     s_rj = (q_r . k_j) * scale,  o_r = softmax_j(s_r) . v,  L_r = lse(s_r)
+// stored as an fp32 partial (o_r, L_r in base 2) in the unit's slot.
+// Logits are carried in base 2 (q pre-scaled by scale * log2 e).
 //
-// Data movement: the chunk's KV rows are fetched through the page table with
-// 16-byte cp.async copies (coalesced: one token row of a page is 2*head_dim
-// contiguous bytes) into a 3-stage shared-memory ring of 64-token tiles.
-// Per-token page lookup makes ragged pages, 1-token nodes and arbitrary
-// page order cost nothing extra.  The 16-byte chunks of each row are stored
-// XOR-permuted so that both compute access patterns below are free of bank
-// conflicts.
-//
-// Compute mapping (8 warps, each owning 8 tokens of a tile):
-//   q.k   lane = 4 * token + quarter; each lane dots a quarter of head_dim
-//         for every row (q broadcast from shared memory), then two xor
-//         shuffles complete the dot;
-//   p.v   lane owns head_dim/32 output elements of every row; the warp's 8
-//         probabilities per row are broadcast through shared memory.
-// Each warp keeps its own running max / sum / output per row; the 8 warp
-// states are merged through shared memory at the end.
+// Persistent CTAs (one per SM) each take a contiguous range of units of
+// about equal cost (units are item-major, so a range holds runs of one
+// item's KV heads, which share their segment table and page list); the
+// tiles of consecutive units form one continuous stream through a ring of
+// 64-token stages, so the loads of the next unit overlap the end of the
+// current one.
+//   warp 0            metadata: runs ahead; per item it builds the segment
+//                     table (positions, page bases, row masks) and gathers
+//                     the item's page ids, per unit it stages the q rows
+//                     (cp.async, completion signalled on the unit's
+//                     mbarrier, so the warp never waits on them);
+//   warps 1, 2        copies, alternating tiles: resolve a tile's pages through the page
+//                     list, loads every 16-token slot that is one whole page
+//                     of one segment as a single contiguous bulk copy (a
+//                     page holds a head's 16 rows back to back) and ragged
+//                     rows (node tails, one-token nodes) with 16-byte
+//                     cp.async at the exact token count;
+//   warps 2..         NG groups of 8 compute warps; group g takes whole units
+//                     g, g+NG, ... of the CTA; a warp owns 8 tokens of a tile:
+//                       q.k  lane = 8 * quarter + token: each lane dots a
+//                            quarter of head_dim for every row, its 16-byte
+//                            chunks rotated by the token so that the 8
+//                            tokens of a shared-memory phase hit 8 different
+//                            bank groups; xor-shuffles finish the dot;
+//                       p.v  lane owns head_dim/32 outputs of every row.
+// Stages hold K and V rows unswizzled, [64 tokens][head_dim] bf16 each.
+// Every warp keeps its own running max / sum / output per row; at the end
+// of a unit the group's warp states are merged through shared-memory
+// atomics.
+// Every wait on an mbarrier is bounded.
 #include "common.cuh"
 #include "deft_internal.h"
 #include "kprof.cuh"
+#include "tcgen05.cuh"
 
 namespace deft {
 namespace {
 
-constexpr int kTile = 64;     // tokens per pipeline stage
-constexpr int kStages = 3;
-constexpr int kWarps = 8;
-constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 64;   // tokens per stage
+constexpr int kPageList = 1024;  // page ids staged per unit (larger units look pages up in global memory)
 
-// Physical 16-byte chunk of logical chunk lc in token row `row`.
-__device__ __forceinline__ int swz(int row, int lc)
+// Bytes of everything but the stage ring, for NG compute groups.
+template <int D, int RMAX>
+constexpr uint32_t fma_fixed_bytes(int NG)
 {
-    return lc ^ ((lc >> 3) << 1) ^ (row & 1);
+    return 2 * NG * RMAX * D * 2 + 2 * NG * 32 + NG * RMAX * D * 4 + 8 * NG * 8 * RMAX * 4 +
+           2 * 8 * NG * RMAX * 4 + NG * RMAX * D * 4 + NG * 2 * RMAX * 4 + 2 * kMaxSegsPerChunk * 20 +
+           2 * kPageList * 4 + 2 * 16 + 64 + 256 + 1024;
 }
 
 template <int D, int RMAX>
-struct FmaSmem {
-    static constexpr int CH = D / 8;           // 16-byte chunks per token row
-    static constexpr int QSTR = D / 4 + 4;     // padded quarter stride (floats)
-    static constexpr int QROW = 4 * QSTR;
-    static constexpr size_t kv_bytes = (size_t)kStages * 2 * kTile * D * 2;
-    static constexpr size_t qs_off = kv_bytes;
-    static constexpr size_t qs_bytes = (size_t)RMAX * QROW * 4;
-    static constexpr size_t meta_off = qs_off + qs_bytes;
-    static constexpr size_t meta_bytes = (size_t)kStages * kTile * 4;
-    static constexpr size_t seg_off = meta_off + meta_bytes;
-    static constexpr size_t seg_bytes = (size_t)kMaxSegsPerChunk * 4 * 4;
-    static constexpr size_t ps_off = seg_off + seg_bytes;
-    static constexpr size_t ps_bytes = (size_t)kWarps * 8 * RMAX * 4;
-    static constexpr size_t total = ps_off + ps_bytes;
-    static constexpr size_t merge_bytes = (size_t)kWarps * RMAX * (D + 2) * 4;
-    static_assert(merge_bytes <= kv_bytes, "merge scratch must fit in the KV ring");
+struct FmaCfg {
+    static constexpr int NG = RMAX <= 4 ? 2 : 1;       // compute groups
+    static constexpr int NCW = 8 * NG;                 // compute warps
+    static constexpr int THREADS = 32 * (NCW + 3);     // + metadata warp + two copy warps
+    // Stages in the ring: as many as fit next to the fixed buffers, at most 6
+    // and even (copy warp w always serves the stages of parity w).
+    static constexpr uint32_t stage_bytes = 2 * kTile * D * 2 + kTile * 4 + 16;
+    static constexpr int ST_FIT = (int)((227u * 1024u - fma_fixed_bytes<D, RMAX>(NG)) / stage_bytes);
+    static constexpr int ST = (ST_FIT < 6 ? ST_FIT : 6) & ~1;
+    static_assert(ST >= 4, "at least four stages");
+    static constexpr int UB = 2 * NG;                  // unit slots (q rows, description)
+    static constexpr uint32_t op_bytes = kTile * D * 2;           // K (or V) of one stage
+    static constexpr uint32_t stage_off = 0;                      // [stage][K,V]
+    static constexpr uint32_t meta_off = ST * 2 * op_bytes;       // [stage][64] row masks
+    static constexpr uint32_t tag_off = meta_off + ST * kTile * 4;            // [ST] tile in the stage
+    static constexpr uint32_t qst_off = tag_off + 64;                          // [UB][RMAX][D] bf16
+    static constexpr uint32_t info_off = qst_off + UB * RMAX * D * 2;         // [UB] unit info
+    static constexpr uint32_t qs_off = info_off + UB * 32;                     // [NG][RMAX][2][D/8][4] f32
+    static constexpr uint32_t ps_off = qs_off + NG * RMAX * D * 4;             // [NCW][8][RMAX]
+    static constexpr uint32_t ml_off = ps_off + NCW * 8 * RMAX * 4;            // [NCW][RMAX] m, l
+    static constexpr uint32_t oacc_off = ml_off + 2 * NCW * RMAX * 4;         // [NG][RMAX][D] f32
+    static constexpr uint32_t fin_off = oacc_off + NG * RMAX * D * 4;          // [NG][2][RMAX] M, L
+    static constexpr uint32_t seg_off = fin_off + NG * 2 * RMAX * 4;           // [2][5][256]
+    static constexpr uint32_t pl_off = seg_off + 2 * kMaxSegsPerChunk * 20;    // [2][kPageList]
+    static constexpr uint32_t iinfo_off = pl_off + 2 * kPageList * 4;          // [2] ItemInfo
+    static constexpr uint32_t bar_off = iinfo_off + 2 * 16;
+    static constexpr uint32_t nbars = 2 * ST + 2 * UB + 4;
+    static constexpr uint32_t total = bar_off + nbars * 8;
+    static constexpr uint32_t alloc = total + 1024;
+    static_assert(alloc <= 227 * 1024, "shared memory of one CTA");
+};
+
+__device__ __forceinline__ uint32_t fbar(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
+
+struct UnitInfo {
+    int32_t R;       // rows
+    int32_t cq0;     // first slot of the unit's rows
+    int32_t h;       // KV head
+    int32_t ntiles;
+    int32_t seq0;    // position of the unit's first tile in the CTA's tile stream
+    int32_t pad[3];
+};
+
+struct ItemInfo {
+    int32_t nseg;
+    int32_t T;       // chunk tokens
+    int32_t listed;  // 1: the item's page ids are in the shared page list
+    int32_t pad;
+};
+
+// Contiguous unit ranges, one per CTA: CTA b takes units [begin[b], begin[b+1]).
+constexpr int kMaxFmaGrid = 256;
+struct CtaRanges {
+    int32_t begin[kMaxFmaGrid + 1];
 };
 
 template <int D, int RMAX>
-__global__ void __launch_bounds__(kThreads, (RMAX <= 8 ? 2 : 1))
-phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items)
+__global__ void __launch_bounds__(FmaCfg<D, RMAX>::THREADS, 1)
+phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
+                  const __grid_constant__ CtaRanges ranges)
 {
-    using S = FmaSmem<D, RMAX>;
-    constexpr int CH = S::CH;
-    constexpr int E = D / 32;       // output elements per lane in p.v
-    constexpr int QCH = CH / 4;     // chunks per lane in q.k
-    extern __shared__ __align__(128) uint8_t smem[];
-    float *qs = reinterpret_cast<float *>(smem + S::qs_off);
-    uint32_t *meta = reinterpret_cast<uint32_t *>(smem + S::meta_off);
-    int32_t *s_pos = reinterpret_cast<int32_t *>(smem + S::seg_off);
-    int32_t *s_node = s_pos + kMaxSegsPerChunk;
-    int32_t *s_tb = s_node + kMaxSegsPerChunk;
-    uint32_t *s_rmask = reinterpret_cast<uint32_t *>(s_tb + kMaxSegsPerChunk);
-    float *ps = reinterpret_cast<float *>(smem + S::ps_off);
+    using C = FmaCfg<D, RMAX>;
+    constexpr int NG = C::NG, NCW = C::NCW, ST = C::ST, UB = C::UB;
+    constexpr int E = D / 32;       // p.v outputs per lane
+    constexpr int QCH = D / 32;     // 16-byte chunks per lane in q.k (a quarter of the row)
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    uint32_t *meta = reinterpret_cast<uint32_t *>(smem + C::meta_off);
+    UnitInfo *info = reinterpret_cast<UnitInfo *>(smem + C::info_off);
+    const uint32_t bars = base + C::bar_off;
+    // mbarriers: full[ST], empty[ST], unit_full[UB], unit_empty[UB], seg_full[2], seg_empty[2]
+    const int kFull = 0, kEmpty = ST, kUFull = 2 * ST, kUEmpty = 2 * ST + UB;
+    const int kSFull = 2 * ST + 2 * UB, kSEmpty = kSFull + 2;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0)
-        KPROF(a, 2000);
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
-    const int item = blockIdx.x / Hkv;
-    const int h = blockIdx.x - item * Hkv;
-    const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
-    const int R = (qe - qb) * G;
-    const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
-    const int cq0 = p.chunk_q_off[c] + qb;
-    const int T = p.chunk_tokens[c];
-    const int ntiles = (T + kTile - 1) / kTile;
+    const int u0 = ranges.begin[blockIdx.x], u1 = ranges.begin[blockIdx.x + 1];
+    ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + C::iinfo_off);
+    // stag[s]: sequence number of the tile last placed in stage s.  The two
+    // compute groups share the ring, so a group may come to a stage one use
+    // early; it waits for the tag before the stage's mbarrier, whose phase
+    // parity alone cannot tell one use from the one before.
+    volatile int32_t *stag = reinterpret_cast<volatile int32_t *>(smem + C::tag_off);
 
-    // Segment table of the chunk, with each segment's row mask: bit r is set
-    // iff row r's query is in the segment's query bitmask.
-    for (int s = tid; s < nseg; s += kThreads) {
-        s_pos[s] = p.seg_chunk_pos[sb + s];
-        s_node[s] = a.node_page_off[p.seg_node[sb + s]];   // first page_id index of the node
-        s_tb[s] = p.seg_tok_begin[sb + s];
-        const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
-        uint32_t rm = 0;
-        for (int r = 0; r < R; ++r) {
-            const int k = qb + r / G;
-            rm |= ((lm[k >> 5] >> (k & 31)) & 1u) << r;
+    if (tid == 0) {
+        if (blockIdx.x < 1024)
+            KPROF_ANY(a, 3072 + blockIdx.x);
+        for (int s = 0; s < ST; ++s) {
+            stag[s] = -1;
+            tc::mbar_init(fbar(bars, kFull + s), 33);
+            tc::mbar_init(fbar(bars, kEmpty + s), 8);
         }
-        s_rmask[s] = rm;
-    }
-    // Query rows, pre-scaled into base-2 logits, stored per head_dim quarter
-    // with padding so the four quarters sit in different banks.
-    const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-    for (int i = tid; i < RMAX * D; i += kThreads) {
-        const int r = i / D, e = i - r * D;
-        float v = 0.f;
-        if (r < R) {
-            const int qid = p.chunk_q[cq0 + r / G];
-            const int hq = h * G + (r % G);
-            v = __bfloat162float(qg[((size_t)qid * Hq + hq) * D + e]) * a.scale_log2;
+        for (int u = 0; u < UB; ++u) {
+            tc::mbar_init(fbar(bars, kUFull + u), 33);   // 32 cp.async arrivals + the description
+            tc::mbar_init(fbar(bars, kUEmpty + u), 8);
         }
-        qs[r * S::QROW + (e / (D / 4)) * S::QSTR + (e % (D / 4))] = v;
+        for (int u = 0; u < 2; ++u) {
+            tc::mbar_init(fbar(bars, kSFull + u), 32);
+            tc::mbar_init(fbar(bars, kSEmpty + u), 64);
+        }
+        tc::fence_mbar_init();
     }
     __syncthreads();
 
-    auto find_seg = [&](int pos) {
-        int lo = 0, hi = nseg - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (s_pos[mid] <= pos)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        return lo;
-    };
-    const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
-    const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
-    auto kv_stage = [&](int st, int kv) { return smem + ((size_t)(st * 2 + kv) * kTile) * D * 2; };
-
-    auto issue_tile = [&](int tile, int st) {
-        const int base = tile * kTile;
-        constexpr int NCOPY = kTile * 2 * CH;
-        for (int i = tid; i < NCOPY; i += kThreads) {
-            const int row = i / (2 * CH), idx = i - row * (2 * CH);
-            const int kv = idx / CH, lc = idx - kv * CH;
-            const int pos = base + row;
-            if (pos < T) {
-                const int s = find_seg(pos);
-                const int t = s_tb[s] + pos - s_pos[s];
-                const int page = a.page_id[s_node[s] + t / kPageSize];
-                const size_t off =
-                    (((size_t)page * Hkv + h) * kPageSize + (t % kPageSize)) * D + lc * 8;
-                cp_async_16(smem_u32(kv_stage(st, kv) + (size_t)row * D * 2 + swz(row, lc) * 16),
-                            (kv ? vg : kg) + off);
+    if (warp == 0) {
+        // ------------------------------------------------- metadata (runs ahead)
+        const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+        constexpr int QJ = (RMAX * (D / 8) + 31) / 32;   // q chunks per lane
+        int qrow[QJ];   // per q chunk of this lane: query * Hq + group member, or -1
+        int seq = 0, iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
+        for (int u = u0; u < u1; ++u) {
+            const int i = u - u0;
+            const int item = u / Hkv, h = u - item * Hkv;
+            if (item != prev_item) {
+                // A new item: its segment table and page list.
+                prev_item = item;
+                ++iseq;
+                const int sbuf = iseq & 1;
+                const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
+                R = (qe - qb) * G;
+                const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
+                cq0 = p.chunk_q_off[c] + qb;
+                const int T = p.chunk_tokens[c];
+                ntiles = (T + kTile - 1) / kTile;
+#pragma unroll
+                for (int j = 0; j < QJ; ++j) {
+                    const int r = (lane + 32 * j) / (D / 8);
+                    qrow[j] = r < R ? p.chunk_q[cq0 + r / G] * Hq + r % G : -1;
+                }
+                if (iseq >= 2 &&
+                    !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kSEmpty + sbuf), ((iseq - 2) >> 1) & 1)))
+                    break;
+                int32_t *seg = reinterpret_cast<int32_t *>(smem + C::seg_off) + sbuf * 1280;
+                int32_t *plist = reinterpret_cast<int32_t *>(smem + C::pl_off) + sbuf * kPageList;
+                int npages = 0;   // page-list entries of the segments handled so far
+                for (int s0 = 0; s0 < nseg; s0 += 32) {
+                    const int s = s0 + lane;
+                    int np = 0, tb = 0, pgb = 0;
+                    if (s < nseg) {
+                        const int len = p.seg_tok_len[sb + s];
+                        tb = p.seg_tok_begin[sb + s];
+                        pgb = a.node_page_off[p.seg_node[sb + s]];
+                        np = (tb + len - 1) / kPageSize - tb / kPageSize + 1;
+                        seg[s] = p.seg_chunk_pos[sb + s];
+                        seg[256 + s] = pgb;
+                        seg[512 + s] = tb;
+                        const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
+                        uint32_t rm = 0;
+                        for (int r = 0; r < R; ++r) {
+                            const int k = qb + r / G;
+                            rm |= ((lm[k >> 5] >> (k & 31)) & 1u) << r;
+                        }
+                        seg[768 + s] = (int32_t)rm;
+                    }
+                    // Exclusive prefix sum of page counts across the warp.
+                    int incl = np;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o)
+                            incl += y;
+                    }
+                    const int ex = incl - np;
+                    if (s < nseg)
+                        seg[1024 + s] = npages + ex;
+                    // Gather the batch's page ids, one entry per lane: entry j
+                    // belongs to the last segment (lane) whose first entry is <= j.
+                    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+                    const int pfirst = pgb + tb / kPageSize;
+                    for (int j0 = 0; j0 < tot && npages + j0 < kPageList; j0 += 32) {
+                        const int j = j0 + lane;
+                        int lo = 0;
+#pragma unroll
+                        for (int step = 16; step > 0; step >>= 1)
+                            if (__shfl_sync(0xffffffffu, ex, lo + step) <= j)
+                                lo += step;
+                        const int src = __shfl_sync(0xffffffffu, pfirst, lo) + j - __shfl_sync(0xffffffffu, ex, lo);
+                        if (j < tot && npages + j < kPageList)
+                            plist[npages + j] = a.page_id[src];
+                    }
+                    npages += tot;
+                }
+                if (lane == 0)
+                    iinfo[sbuf] = ItemInfo{nseg, T, npages <= kPageList ? 1 : 0, 0};
+                __syncwarp();
+                tc::mbar_arrive(fbar(bars, kSFull + sbuf));
             }
+            // The unit's q rows (bf16) and description for its compute group.
+            const int ub = i % UB;
+            if (i >= UB && !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kUEmpty + ub), ((i - UB) / UB) & 1)))
+                break;
+            const uint32_t qdst = base + C::qst_off + (uint32_t)ub * RMAX * D * 2;
+#pragma unroll
+            for (int j = 0; j < QJ; ++j) {
+                const int x = lane + 32 * j;
+                if (qrow[j] >= 0) {
+                    const int r = x / (D / 8), ch = x - r * (D / 8);
+                    cp_async_16(qdst + (uint32_t)(r * D + ch * 8) * 2, qg + (size_t)(qrow[j] + h * G) * D + ch * 8);
+                }
+            }
+            cp_async_mbar_arrive_noinc(fbar(bars, kUFull + ub));
+            if (lane == 0) {
+                info[ub] = UnitInfo{R, cq0, h, ntiles, seq, {0, 0, 0}};
+                tc::mbar_arrive(fbar(bars, kUFull + ub));
+                KPROF(a, 2000 + 8 * i + 0);
+            }
+            seq += ntiles;
         }
-        if (tid < kTile) {
-            const int pos = base + tid;
-            meta[st * kTile + tid] = pos < T ? s_rmask[find_seg(pos)] : 0u;
+        cp_async_commit();
+        cp_async_wait<0>();
+    } else if (warp <= 2) {
+        // ------------------------------------------------------- copy warps
+        // Copy warp w (0, 1) loads the tiles of sequence number = w mod 2, so
+        // one resolves its tile's pages while the other issues its copies.
+        const int cpw = warp - 1;
+        const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
+        const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
+        constexpr uint32_t kRowBytes = D * 2;
+        constexpr uint32_t kPageBytes = kPageSize * kRowBytes;   // one head's rows of a page
+        int seq = 0, iseq = -1, prev_item = -1;
+        bool ok = true;
+        for (int u = u0; u < u1 && ok; ++u) {
+            const int i = u - u0;
+            const int item = u / Hkv, h = u - item * Hkv;
+            if (item != prev_item) {
+                prev_item = item;
+                ++iseq;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kSFull + (iseq & 1)), (iseq >> 1) & 1)))
+                    break;
+            }
+            const int sbuf = iseq & 1;
+            const int32_t *seg = reinterpret_cast<const int32_t *>(smem + C::seg_off) + sbuf * 1280;
+            const int32_t *plist = reinterpret_cast<const int32_t *>(smem + C::pl_off) + sbuf * kPageList;
+            const ItemInfo ii = iinfo[sbuf];
+            (void)i;
+            if (lane == 0)
+                KPROF(a, 2000 + 8 * i + 1);
+            // Physical page of token tk of segment sg.
+            auto page_of = [&](int sg, int tk) {
+                return ii.listed ? plist[seg[1024 + sg] + tk / kPageSize - seg[512 + sg] / kPageSize]
+                                 : a.page_id[seg[256 + sg] + tk / kPageSize];
+            };
+            const int nseg = ii.nseg, T = ii.T, ntiles = (T + kTile - 1) / kTile;
+            for (int t = 0; t < ntiles; ++t, ++seq) {
+                if ((seq & 1) != cpw)
+                    continue;
+                const int st = seq % ST;
+                // Segment and token of the tile positions lane and lane + 32.
+                int sgk[2], tkk[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int pos = t * kTile + lane + 32 * k;
+                    sgk[k] = -1;
+                    tkk[k] = 1;
+                    if (pos < T) {
+                        int lo = 0, hi = nseg - 1;
+                        while (lo < hi) {
+                            const int mid = (lo + hi + 1) >> 1;
+                            if (seg[mid] <= pos)
+                                lo = mid;
+                            else
+                                hi = mid - 1;
+                        }
+                        sgk[k] = lo;
+                        tkk[k] = seg[512 + lo] + pos - seg[lo];
+                    }
+                }
+                // Slot j (tile rows 16j..16j+15) goes by bulk copy when its 16
+                // positions are one whole page of one segment.
+                uint32_t tp = 0;
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int s_first = __shfl_sync(0xffffffffu, sgk[k], lane & 16);
+                    const int t_first = __shfl_sync(0xffffffffu, tkk[k], lane & 16);
+                    const bool okp = sgk[k] >= 0 && sgk[k] == s_first && (t_first % kPageSize) == 0;
+                    const uint32_t bal = __ballot_sync(0xffffffffu, okp);
+                    if ((bal & 0xffffu) == 0xffffu)
+                        tp |= 1u << (2 * k);
+                    if ((bal >> 16) == 0xffffu)
+                        tp |= 1u << (2 * k + 1);
+                }
+                // Lane j < 4 resolves slot j's page (position 16j is lane
+                // 16 * (j & 1)'s entry k = j >> 1).
+                const int src = 16 * (lane & 1);
+                const int s_a = __shfl_sync(0xffffffffu, sgk[0], src), s_b = __shfl_sync(0xffffffffu, sgk[1], src);
+                const int t_a = __shfl_sync(0xffffffffu, tkk[0], src), t_b = __shfl_sync(0xffffffffu, tkk[1], src);
+                int pg_lane = -1;
+                if (lane < 4 && ((tp >> lane) & 1u))
+                    pg_lane = (lane & 2) ? page_of(s_b, t_b) : page_of(s_a, t_a);
+                int pid[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    pid[k] = -1;
+                    if (sgk[k] >= 0 && !((tp >> ((lane + 32 * k) >> 4)) & 1u))
+                        pid[k] = page_of(sgk[k], tkk[k]);
+                }
+                if (lane == 0 && seq < 16)
+                    KPROF(a, 2100 + 8 * seq + 0);
+                if (seq >= ST && !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kEmpty + st), ((seq / ST) - 1) & 1))) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0)
+                    stag[st] = seq;
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    meta[st * kTile + lane + 32 * k] = sgk[k] >= 0 ? (uint32_t)seg[768 + sgk[k]] : 0u;
+                const uint32_t full = fbar(bars, kFull + st);
+                const uint32_t kdst = base + C::stage_off + (uint32_t)(st * 2) * C::op_bytes;
+                const uint32_t vdst = kdst + C::op_bytes;
+                if (lane == 0)
+                    tc::mbar_arrive_expect_tx(full, __popc(tp) * 2 * kPageBytes);
+                __syncwarp();
+                if (pg_lane >= 0) {
+                    const size_t o = ((size_t)pg_lane * Hkv + h) * kPageSize * D;
+                    const uint32_t rb = (uint32_t)lane * kPageBytes;
+                    tc::bulk_load(kdst + rb, kg + o, kPageBytes, full);
+                    tc::bulk_load(vdst + rb, vg + o, kPageBytes, full);
+                }
+                // Ragged rows: one row per warp step; lanes cover K and V chunks.
+                bool any_cp = false;
+                constexpr int CPR = D / 8;  // 16-byte chunks per row per operand
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    uint32_t nb = __ballot_sync(0xffffffffu, pid[k] >= 0);
+                    any_cp |= nb != 0;
+                    while (nb) {
+                        const int sl = __ffs(nb) - 1;
+                        nb &= nb - 1;
+                        const int row = sl + 32 * k;
+                        const int pg = __shfl_sync(0xffffffffu, pid[k], sl);
+                        const int tk = __shfl_sync(0xffffffffu, tkk[k], sl);
+                        const long long o = (((long long)pg * Hkv + h) * kPageSize + (tk % kPageSize)) * D;
+                        for (int x = lane; x < 2 * CPR; x += 32) {
+                            const int kv = x / CPR, ch = x - kv * CPR;
+                            cp_async_16((kv ? vdst : kdst) + row * kRowBytes + ch * 16, (kv ? vg : kg) + o + ch * 8);
+                        }
+                    }
+                }
+                // Rows past the chunk's end: zero V so that p.v may run over
+                // all 64 rows (their p is 0; stale shared memory could be NaN).
+                const int nvalid = min(kTile, T - t * kTile);
+                if (nvalid < kTile) {
+                    uint4 *vz = reinterpret_cast<uint4 *>(smem + (vdst - base) + nvalid * kRowBytes);
+                    for (int x = lane; x < (kTile - nvalid) * CPR; x += 32)
+                        vz[x] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                if (any_cp) {
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                }
+                tc::mbar_arrive(full);
+                if (lane == 0 && seq < 16)
+                    KPROF(a, 2100 + 8 * seq + 1);
+            }
+            // Release the item's segment table after its last unit here.
+            if (u + 1 == u1 || (u + 1) / Hkv != item) {
+                __syncwarp();
+                tc::mbar_arrive(fbar(bars, kSEmpty + sbuf));
+            }
+            if (lane == 0)
+                KPROF(a, 2000 + 8 * i + 2);
         }
-    };
-
-    // Per-warp online-softmax state for every row.
-    float m_run[RMAX], l_run[RMAX], o_acc[RMAX][E];
-#pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-        m_run[r] = -INFINITY;
-        l_run[r] = 0.f;
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-            o_acc[r][e] = 0.f;
-    }
-    const int tok = lane >> 2, qtr = lane & 3;
-    float *psw = ps + warp * 8 * RMAX;
-
-#pragma unroll
-    for (int st = 0; st < kStages - 1; ++st) {
-        if (st < ntiles)
-            issue_tile(st, st);
-        cp_async_commit();
-    }
-    if (tid == 0)
-        KPROF(a, 2001);
-    for (int tile = 0; tile < ntiles; ++tile) {
-        const int nxt = tile + kStages - 1;
-        if (nxt < ntiles)
-            issue_tile(nxt, nxt % kStages);
-        if (tid == 0)
-            KPROF(a, 2100 + 4 * tile);
-        cp_async_commit();
-        cp_async_wait<kStages - 1>();
-        __syncthreads();
-        if (tid == 0)
-            KPROF(a, 2101 + 4 * tile);
-
-        const int st = tile % kStages;
-        const uint8_t *Ks = kv_stage(st, 0);
-        const uint8_t *Vs = kv_stage(st, 1);
-        const int row = warp * 8 + tok;
-
-        // q.k: this lane's quarter of head_dim, all rows.
-        float s[RMAX];
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r)
-            s[r] = 0.f;
-#pragma unroll
-        for (int c4 = 0; c4 < QCH; ++c4) {
-            const int lc = qtr * QCH + c4;
-            const uint4 kw = *reinterpret_cast<const uint4 *>(Ks + (size_t)row * D * 2 + swz(row, lc) * 16);
-            const float2 k01 = bf16x2_to_float2(kw.x), k23 = bf16x2_to_float2(kw.y);
-            const float2 k45 = bf16x2_to_float2(kw.z), k67 = bf16x2_to_float2(kw.w);
+        cp_async_wait<0>();
+        // Do not leave while bulk copies of ours may still be landing: wait for
+        // the last use of every stage.
+        for (int s = 0; s < ST && s < seq; ++s) {
+            const int last = seq - 1 - ((seq - 1 - s) % ST);
+            tc::mbar_wait(fbar(bars, kFull + s), (last / ST) & 1);
+        }
+    } else {
+        // ------------------------------------------------------------ compute
+        // Group g takes the CTA's units g, g + NG, ... whole.
+        const int cw = warp - 3;          // compute warp 0..NCW-1
+        const int g = cw >> 3, lw = cw & 7;
+        const int tok = lane & 7, qtr = lane >> 3;
+        float *qs = reinterpret_cast<float *>(smem + C::qs_off) + g * RMAX * D;
+        float *ps = reinterpret_cast<float *>(smem + C::ps_off) + cw * 8 * RMAX;
+        float *mw = reinterpret_cast<float *>(smem + C::ml_off) + g * 8 * RMAX;
+        float *lwb = reinterpret_cast<float *>(smem + C::ml_off) + NCW * RMAX + g * 8 * RMAX;
+        float *oacc = reinterpret_cast<float *>(smem + C::oacc_off) + g * RMAX * D;
+        float *fin = reinterpret_cast<float *>(smem + C::fin_off) + g * 2 * RMAX;
+        const uint32_t bar_id = 1 + (uint32_t)g, nthr = 256;
+        const int gtid = tid - 96 - g * 256;   // thread index within the group
+        for (int i = g; u0 + i < u1; i += NG) {
+            const int ub = i % UB;
+            const bool okw = tc::mbar_wait(fbar(bars, kUFull + ub), (i / UB) & 1);
+            if (tc::named_sync_or(bar_id, nthr, !okw))
+                break;
+            const UnitInfo ui = info[ub];
+            if (gtid == 0)
+                KPROF(a, 2000 + 8 * i + 3);
+            const int R = ui.R;
+            const __nv_bfloat16 *qst = reinterpret_cast<const __nv_bfloat16 *>(smem + C::qst_off) + ub * RMAX * D;
+            // qs[r]: the 16-byte chunks' first halves, then their second halves.
+            for (int x = gtid; x < RMAX * D; x += nthr) {
+                const int r = x / D, e = x - r * D;
+                qs[r * D + ((e >> 2) & 1) * (D / 2) + (e >> 3) * 4 + (e & 3)] =
+                    x < R * D ? __bfloat162float(qst[x]) * a.scale_log2 : 0.f;
+                oacc[x] = 0.f;
+            }
+            tc::named_sync(bar_id, nthr);
+            float m_run[RMAX], l_run[RMAX], o_acc[RMAX][E];
 #pragma unroll
             for (int r = 0; r < RMAX; ++r) {
-                if (r < R) {
-                    const float *qp = qs + r * S::QROW + qtr * S::QSTR + c4 * 8;
-                    const float4 qa = *reinterpret_cast<const float4 *>(qp);
-                    const float4 qb4 = *reinterpret_cast<const float4 *>(qp + 4);
-                    float acc = s[r];
-                    acc = fmaf(qa.x, k01.x, acc);
-                    acc = fmaf(qa.y, k01.y, acc);
-                    acc = fmaf(qa.z, k23.x, acc);
-                    acc = fmaf(qa.w, k23.y, acc);
-                    acc = fmaf(qb4.x, k45.x, acc);
-                    acc = fmaf(qb4.y, k45.y, acc);
-                    acc = fmaf(qb4.z, k67.x, acc);
-                    acc = fmaf(qb4.w, k67.y, acc);
-                    s[r] = acc;
-                }
-            }
-        }
-        const uint32_t rmask = meta[st * kTile + row];
-#pragma unroll
-        for (int r = 0; r < RMAX; ++r) {
-            if (r < R) {
-                float v = s[r];
-                v += __shfl_xor_sync(0xffffffffu, v, 1);
-                v += __shfl_xor_sync(0xffffffffu, v, 2);
-                v = ((rmask >> r) & 1u) ? v : -INFINITY;
-                float mx = v;
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mnew = fmaxf(m_run[r], mx);
-                float pr = 0.f, alpha = 1.f;
-                if (mnew != -INFINITY) {
-                    alpha = exp2f(m_run[r] - mnew);
-                    pr = exp2f(v - mnew);
-                }
-                m_run[r] = mnew;
-                l_run[r] = l_run[r] * alpha + (qtr == 0 ? pr : 0.f);
+                m_run[r] = -INFINITY;
+                l_run[r] = 0.f;
 #pragma unroll
                 for (int e = 0; e < E; ++e)
-                    o_acc[r][e] *= alpha;
-                if (qtr == (r & 3))
-                    psw[tok * RMAX + r] = pr;
+                    o_acc[r][e] = 0.f;
             }
-        }
-        __syncwarp();
-        // p.v over the warp's 8 tokens.
-#pragma unroll 2
-        for (int tt = 0; tt < 8; ++tt) {
-            const int rt = warp * 8 + tt;
-            if (meta[st * kTile + rt] == 0u)
-                continue;
-            float vf[E];
-            const uint8_t *vrow = Vs + (size_t)rt * D * 2;
-            if constexpr (E == 4) {
-                const uint2 vw = *reinterpret_cast<const uint2 *>(vrow + swz(rt, lane >> 1) * 16 + (lane & 1) * 8);
-                const float2 a01 = bf16x2_to_float2(vw.x), a23 = bf16x2_to_float2(vw.y);
-                vf[0] = a01.x; vf[1] = a01.y; vf[2] = a23.x; vf[3] = a23.y;
-            } else {
-                const uint32_t vw = *reinterpret_cast<const uint32_t *>(vrow + swz(rt, lane >> 2) * 16 + (lane & 3) * 4);
-                const float2 a01 = bf16x2_to_float2(vw);
-                vf[0] = a01.x; vf[1] = a01.y;
+            bool tile_ok = true;
+            for (int t = 0; t < ui.ntiles; ++t) {
+                const int sq = ui.seq0 + t, st = sq % ST;
+                bool got = false;
+                for (int spin = 0; spin < (1 << 22) && !got; ++spin) {
+                    got = stag[st] == sq;
+                    if (!got)
+                        __nanosleep(64);
+                }
+                got = got && tc::mbar_wait(fbar(bars, kFull + st), (sq / ST) & 1);
+                if (!__all_sync(0xffffffffu, got)) {
+                    tile_ok = false;
+                    break;
+                }
+                if (gtid == 0 && sq < 16)
+                    KPROF(a, 2100 + 8 * sq + 2);
+                const uint8_t *Ks = smem + C::stage_off + (size_t)(st * 2) * C::op_bytes;
+                const uint8_t *Vs = Ks + C::op_bytes;
+                const int row = lw * 8 + tok;
+                // q.k over this lane's quarter of head_dim, all rows.
+                float s[RMAX];
+#pragma unroll
+                for (int r = 0; r < RMAX; ++r)
+                    s[r] = 0.f;
+#pragma unroll
+                for (int c4 = 0; c4 < QCH; ++c4) {
+                    const int lc = (qtr * QCH + c4 + tok) & (D / 8 - 1);
+                    const uint4 kw = *reinterpret_cast<const uint4 *>(Ks + row * (D * 2) + lc * 16);
+                    const float2 k01 = bf16x2_to_float2(kw.x), k23 = bf16x2_to_float2(kw.y);
+                    const float2 k45 = bf16x2_to_float2(kw.z), k67 = bf16x2_to_float2(kw.w);
+#pragma unroll
+                    for (int r = 0; r < RMAX; ++r) {
+                        if (r < R) {
+                            const float *qp = qs + r * D + lc * 4;
+                            const float4 qa = *reinterpret_cast<const float4 *>(qp);
+                            const float4 qb4 = *reinterpret_cast<const float4 *>(qp + D / 2);
+                            float acc0 = fmaf(qa.x, k01.x, s[r]);
+                            float acc1 = qb4.x * k45.x;
+                            acc0 = fmaf(qa.y, k01.y, acc0);
+                            acc1 = fmaf(qb4.y, k45.y, acc1);
+                            acc0 = fmaf(qa.z, k23.x, acc0);
+                            acc1 = fmaf(qb4.z, k67.x, acc1);
+                            acc0 = fmaf(qa.w, k23.y, acc0);
+                            acc1 = fmaf(qb4.w, k67.y, acc1);
+                            s[r] = acc0 + acc1;
+                        }
+                    }
+                }
+                if (gtid == 0 && sq < 16)
+                    KPROF(a, 2100 + 8 * sq + 4);
+                const uint32_t rmask = meta[st * kTile + row];
+#pragma unroll
+                for (int r = 0; r < RMAX; ++r) {
+                    if (r < R) {
+                        float v = s[r];
+                        v += __shfl_xor_sync(0xffffffffu, v, 8);
+                        v += __shfl_xor_sync(0xffffffffu, v, 16);
+                        v = ((rmask >> r) & 1u) ? v : -INFINITY;
+                        float mx = v;
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                        const float mnew = fmaxf(m_run[r], mx);
+                        float pr = 0.f, alpha = 1.f;
+                        if (mnew != -INFINITY) {
+                            alpha = tc::ex2(m_run[r] - mnew);
+                            pr = tc::ex2(v - mnew);
+                        }
+                        m_run[r] = mnew;
+                        l_run[r] = l_run[r] * alpha + (qtr == 0 ? pr : 0.f);
+#pragma unroll
+                        for (int e = 0; e < E; ++e)
+                            o_acc[r][e] *= alpha;
+                        if (qtr == (r & 3))
+                            ps[tok * RMAX + r] = pr;
+                    }
+                }
+                __syncwarp();
+                if (gtid == 0 && sq < 16)
+                    KPROF(a, 2100 + 8 * sq + 5);
+                // p.v over the warp's 8 tokens (p = 0 for masked and absent
+                // tokens, whose V rows are finite or zero).
+#pragma unroll
+                for (int tt = 0; tt < 8; ++tt) {
+                    const int rt = lw * 8 + tt;
+                    float vf[E];
+                    const uint8_t *vp = Vs + rt * (D * 2) + lane * E * 2;
+                    if constexpr (E == 4) {
+                        const uint2 vw = *reinterpret_cast<const uint2 *>(vp);
+                        const float2 a01 = bf16x2_to_float2(vw.x), a23 = bf16x2_to_float2(vw.y);
+                        vf[0] = a01.x;
+                        vf[1] = a01.y;
+                        vf[2] = a23.x;
+                        vf[3] = a23.y;
+                    } else {
+                        const float2 a01 = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(vp));
+                        vf[0] = a01.x;
+                        vf[1] = a01.y;
+                    }
+                    const float *pp = ps + tt * RMAX;
+#pragma unroll
+                    for (int r = 0; r < RMAX; ++r) {
+                        if (r < R) {
+                            const float pr = pp[r];
+#pragma unroll
+                            for (int e = 0; e < E; ++e)
+                                o_acc[r][e] = fmaf(pr, vf[e], o_acc[r][e]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (gtid == 0 && sq < 16)
+                    KPROF(a, 2100 + 8 * sq + 3);
+                if (lane == 0)
+                    tc::mbar_arrive(fbar(bars, kEmpty + st));
             }
-            const float *pp = psw + tt * RMAX;
+            if (tc::named_sync_or(bar_id, nthr, !tile_ok))
+                break;
+            // Merge the 8 warp states of the unit's rows.
 #pragma unroll
             for (int r = 0; r < RMAX; ++r) {
                 if (r < R) {
-                    const float pr = pp[r];
-#pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        o_acc[r][e] = fmaf(pr, vf[e], o_acc[r][e]);
+                    const float lt = warp_sum(l_run[r]);
+                    if (lane == 0) {
+                        mw[lw * RMAX + r] = m_run[r];
+                        lwb[lw * RMAX + r] = lt;
+                    }
                 }
             }
-        }
-        __syncthreads();
-        if (tid == 0)
-            KPROF(a, 2102 + 4 * tile);
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-
-    // Merge the 8 warp states of every row and store the partial.
-    float *mw = reinterpret_cast<float *>(smem);          // [warps][RMAX]
-    float *lw = mw + kWarps * RMAX;                      // [warps][RMAX]
-    float *ow = lw + kWarps * RMAX;                      // [warps][RMAX][D]
+            tc::named_sync(bar_id, nthr);
+            if (gtid < R) {
+                float M = -INFINITY;
 #pragma unroll
-    for (int r = 0; r < RMAX; ++r) {
-        if (r < R) {
-            const float lt = warp_sum(l_run[r]);
-            if (lane == 0) {
-                mw[warp * RMAX + r] = m_run[r];
-                lw[warp * RMAX + r] = lt;
+                for (int w = 0; w < 8; ++w)
+                    M = fmaxf(M, mw[w * RMAX + gtid]);
+                float L = 0.f;
+                if (M != -INFINITY)
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        L += lwb[w * RMAX + gtid] * tc::ex2(mw[w * RMAX + gtid] - M);
+                fin[gtid] = M;
+                fin[RMAX + gtid] = L;
             }
+            tc::named_sync(bar_id, nthr);
 #pragma unroll
-            for (int e = 0; e < E; ++e)
-                ow[((size_t)warp * RMAX + r) * D + lane * E + e] = o_acc[r][e];
-        }
-    }
-    __syncthreads();
-    for (int i = tid; i < R * D; i += kThreads) {
-        const int r = i / D, e = i - r * D;
-        float M = -INFINITY;
+            for (int r = 0; r < RMAX; ++r) {
+                if (r < R && m_run[r] != -INFINITY) {
+                    const float scl = tc::ex2(m_run[r] - fin[r]);
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w)
-            M = fmaxf(M, mw[w * RMAX + r]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float sc = exp2f(mw[w * RMAX + r] - M);
-                L = fmaf(lw[w * RMAX + r], sc, L);
-                O = fmaf(ow[((size_t)w * RMAX + r) * D + e], sc, O);
+                    for (int e = 0; e < E; ++e)
+                        atomicAdd(oacc + r * D + lane * E + e, o_acc[r][e] * scl);
+                }
             }
+            tc::named_sync(bar_id, nthr);
+            for (int x = gtid; x < R * D; x += nthr) {
+                const int r = x / D, e = x - r * D;
+                const float L = fin[RMAX + r];
+                const size_t prow = (size_t)(ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
+                a.o_part[prow * D + e] = L > 0.f ? oacc[x] / L : 0.f;
+                if (e == 0)
+                    a.lse_part[prow] = L > 0.f ? fin[r] + log2f(L) : -INFINITY;
+            }
+            tc::named_sync(bar_id, nthr);
+            if (gtid == 0)
+                KPROF(a, 2000 + 8 * i + 4);
+            if (gtid == 0 && blockIdx.x < 512 && u0 + i + NG >= u1)
+                KPROF_ANY(a, 1024 + 2 * blockIdx.x + g);
+            if (lane == 0)
+                tc::mbar_arrive(fbar(bars, kUEmpty + ub));
         }
-        const int slot = cq0 + r / G;
-        const int hq = h * G + (r % G);
-        const size_t prow = (size_t)slot * Hq + hq;
-        a.o_part[prow * D + e] = L > 0.f ? O / L : 0.f;
-        if (e == 0)
-            a.lse_part[prow] = L > 0.f ? M + log2f(L) : -INFINITY;
     }
 }
 
+int num_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 1;
+    }
+    return n;
+}
+
+// Cuts units [0, n * hkv) (item-major) into `grid` contiguous ranges of
+// about equal cost: CTA b starts at the first unit whose cost prefix
+// reaches b / grid of the total.  `cost` is the items' cost prefix.
+void cta_ranges(const int64_t *cost, int32_t n, int32_t hkv, int grid, CtaRanges &r)
+{
+    const int64_t c0 = cost[0];
+    const int64_t total = (int64_t)hkv * (cost[n] - c0);
+    int32_t i = 0;
+    r.begin[0] = 0;
+    for (int b = 1; b < grid; ++b) {
+        const int64_t target = total * b / grid;
+        while (i < n && (int64_t)hkv * (cost[i + 1] - c0) <= target)
+            ++i;
+        if (i == n) {
+            r.begin[b] = n * hkv;
+            continue;
+        }
+        const int64_t rem = target - (int64_t)hkv * (cost[i] - c0);
+        const int64_t ci = cost[i + 1] - cost[i];
+        r.begin[b] = (int32_t)((int64_t)i * hkv + (rem + ci - 1) / ci);
+    }
+    r.begin[grid] = n * hkv;
+}
+
 template <int D, int RMAX>
-int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
+int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost, int32_t n,
                cudaStream_t st)
 {
-    using S = FmaSmem<D, RMAX>;
+    using C = FmaCfg<D, RMAX>;
     static bool configured = false;
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(phase1_fma_kernel<D, RMAX>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)S::total);
+        const cudaError_t e = cudaFuncSetAttribute(phase1_fma_kernel<D, RMAX>,
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::alloc);
         if (e != cudaSuccess)
             return (int)e;
         configured = true;
     }
-    const unsigned blocks = (unsigned)((int64_t)n * a.num_kv_heads);
-    phase1_fma_kernel<D, RMAX><<<blocks, kThreads, S::total, st>>>(a, p, items);
+    const int64_t units = (int64_t)n * a.num_kv_heads;
+    const int64_t cap = num_sms() < kMaxFmaGrid ? num_sms() : kMaxFmaGrid;
+    const int grid = (int)(units < cap ? units : cap);
+    CtaRanges r;
+    cta_ranges(cost, n, a.num_kv_heads, grid, r);
+    phase1_fma_kernel<D, RMAX><<<grid, C::THREADS, C::alloc, st>>>(a, p, items, r);
     return (int)cudaGetLastError();
 }
 
 template <int D>
-int launch_bucket(int bucket, const AttnArgs &a, const DevPartition &p, const int32_t *items,
+int launch_bucket(int bucket, const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
                   int32_t n, cudaStream_t st)
 {
     switch (bucket) {
-    case 0: return launch_one<D, 1>(a, p, items, n, st);
-    case 1: return launch_one<D, 2>(a, p, items, n, st);
-    case 2: return launch_one<D, 4>(a, p, items, n, st);
-    case 3: return launch_one<D, 8>(a, p, items, n, st);
-    default: return launch_one<D, 16>(a, p, items, n, st);
+    case 0: return launch_one<D, 1>(a, p, items, cost, n, st);
+    case 1: return launch_one<D, 2>(a, p, items, cost, n, st);
+    case 2: return launch_one<D, 4>(a, p, items, cost, n, st);
+    case 3: return launch_one<D, 8>(a, p, items, cost, n, st);
+    default: return launch_one<D, 16>(a, p, items, cost, n, st);
     }
 }
 
 }  // namespace
 
-int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
-                      int bucket, void *stream)
+int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
+                      int32_t n, int bucket, void *stream)
 {
     if (n <= 0)
         return 0;
+    if ((int64_t)n * a.num_kv_heads > INT32_MAX)
+        return (int)cudaErrorInvalidValue;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, n, st)
-                             : launch_bucket<64>(bucket, a, p, items, n, st);
+    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, cost, n, st)
+                             : launch_bucket<64>(bucket, a, p, items, cost, n, st);
 }
 
 }  // namespace deft

@@ -11,8 +11,9 @@
 //
 // One warp per (query, head); lane i owns head_dim/32 consecutive elements,
 // so each slot's partial is read with one coalesced 128-bit (or 64-bit) load
-// per lane.  The partials were written moments earlier by phase 1 and are
-// mostly still in L2.
+// per lane; the slot ids and weights are loaded one slot per lane and
+// broadcast by shuffles.  The partials were written moments earlier by
+// phase 1 and are mostly still in L2.
 #include "common.cuh"
 #include "deft_internal.h"
 
@@ -34,9 +35,15 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
     const int h = warp - q * num_q_heads;
     const int s0 = q_slot_off[q], s1 = q_slot_off[q + 1];
 
+    // Slots are taken 32 at a time: lane j loads slot j's row and lse, so the
+    // dependent loads (slot list -> lse) happen once per batch, not per slot;
+    // the batch's partial rows are then independent loads.
     float M = -INFINITY;
-    for (int i = s0 + lane; i < s1; i += 32)
-        M = fmaxf(M, lse_part[(size_t)q_slot[i] * num_q_heads + h]);
+    for (int b = s0; b < s1; b += 32) {
+        const int i = b + lane;
+        if (i < s1)
+            M = fmaxf(M, lse_part[(size_t)q_slot[i] * num_q_heads + h]);
+    }
     M = warp_max(M);
 
     float acc[E];
@@ -45,24 +52,35 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
         acc[e] = 0.f;
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int i = s0; i < s1; ++i) {
-            const int s = q_slot[i];
-            const size_t row = (size_t)s * num_q_heads + h;
-            const float w = exp2f(lse_part[row] - M);
-            const float *src = o_part + row * D + lane * E;
-            if constexpr (E == 4) {
-                const float4 v = *reinterpret_cast<const float4 *>(src);
-                acc[0] = fmaf(w, v.x, acc[0]);
-                acc[1] = fmaf(w, v.y, acc[1]);
-                acc[2] = fmaf(w, v.z, acc[2]);
-                acc[3] = fmaf(w, v.w, acc[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2 *>(src);
-                acc[0] = fmaf(w, v.x, acc[0]);
-                acc[1] = fmaf(w, v.y, acc[1]);
+        for (int b = s0; b < s1; b += 32) {
+            const int i = b + lane;
+            size_t myrow = 0;
+            float myw = 0.f;
+            if (i < s1) {
+                myrow = (size_t)q_slot[i] * num_q_heads + h;
+                myw = exp2f(lse_part[myrow] - M);
             }
-            wsum += w;
+            wsum += myw;
+            const int nb = min(32, s1 - b);
+#pragma unroll 4
+            for (int j = 0; j < nb; ++j) {
+                const size_t row = __shfl_sync(0xffffffffu, myrow, j);
+                const float w = __shfl_sync(0xffffffffu, myw, j);
+                const float *src = o_part + row * D + lane * E;
+                if constexpr (E == 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(src);
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                    acc[2] = fmaf(w, v.z, acc[2]);
+                    acc[3] = fmaf(w, v.w, acc[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2 *>(src);
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                }
+            }
         }
+        wsum = warp_sum(wsum);
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     const size_t orow = ((size_t)q * num_q_heads + h) * D + lane * E;

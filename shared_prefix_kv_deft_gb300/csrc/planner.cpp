@@ -179,6 +179,13 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     emit(fma, p.fma_items);
     emit(mma, p.mma_items);
     emit(fb, p.fallback_items);
+    auto cost_prefix = [&](const std::vector<Item> &v, std::vector<int64_t> &out) {
+        out.assign(1, 0);
+        for (const Item &it : v)
+            out.push_back(out.back() + p.chunk_tokens[it.c] + kUnitOverheadTokens);
+    };
+    cost_prefix(fma, p.fma_cost);
+    cost_prefix(fb, p.fallback_cost);
     bucket_offsets(fma, p.fma_bucket_off);
     bucket_offsets(fb, p.fallback_bucket_off);
     bucket_offsets(mma, p.mma_bucket_off);

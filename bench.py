@@ -8,8 +8,10 @@ chunks + phase-2 LSE merge) on one synthetic tree whose KV cache and queries
 are already resident in HBM.  The default workload is the shared-prefix
 few-shot decode tree (4096-token prefix, 32 branches of 256 tokens, one
 query per branch tip, 32 query / 32 KV heads, head_dim 128, bf16); other
-shapes via --config 1..6.  The L2 cache is flushed (a 2 x L2 memset)
-between timed steps, outside the timed events.
+shapes via --config 1..6.  The L2 cache is flushed between timed steps,
+outside the timed events: a 2 x L2 memset, then a read of another 2 x L2
+buffer, so that the step starts with a cold L2 that holds no dirty lines
+(their write-back would otherwise land inside the timed region).
 
 Prints one JSON line (rank 0).  `value` is microseconds per step (lower is
 better); for N > 1 the ranks run independent replicas and `value` is the
@@ -319,6 +321,11 @@ def main():
     bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim, dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_rd = torch.zeros(2 * l2 // 8, dtype=torch.int64, device=dev)
+
+    def flush_l2():
+        flush.zero_()
+        flush_rd.sum()
     stream = torch.cuda.current_stream(dev)
 
     def step():
@@ -338,7 +345,7 @@ def main():
         barrier()
         w0 = time.time()
         for i in range(n):
-            flush.zero_()
+            flush_l2()
             starts[i].record(stream)
             fn()
             ends[i].record(stream)
@@ -352,7 +359,7 @@ def main():
         return ms, recs, w0, w1
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         step()
     sampler = ClockSampler(local)
     sampler.start()
@@ -415,7 +422,7 @@ def main():
         "config": {"workload": spec.name, "config_index": args.config, "global_batch": Q * world,
                    "seq_len": int(max(1, st["naive_tokens"] // max(1, Q))),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "chunk_target": args.chunk_target, "l2": "flushed (2 x L2 memset) between timed steps",
+                   "chunk_target": args.chunk_target, "l2": "flushed between timed steps (2 x L2 memset, then 2 x L2 read: cold, clean)",
                    "q_heads": Hq, "kv_heads": Hkv, "head_dim": d},
         "us_per_step_median": statistics.median(ms) * 1e3,
         "us_per_step_p10": float(np.percentile(ms, 10)) * 1e3,

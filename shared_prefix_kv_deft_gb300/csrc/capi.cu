@@ -20,6 +20,24 @@
 unsigned long long *g_kprof_buf = nullptr;
 #endif
 
+namespace deft {
+
+int num_sms()
+{
+    static int n = 0;
+    if (n == 0) {
+        int dev = 0, v = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0)
+            n = v;
+        else
+            return 1;
+    }
+    return n;
+}
+
+}  // namespace deft
+
 namespace {
 
 constexpr size_t kAlign = 256;
@@ -202,6 +220,7 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
     a.head_dim = head_dim;
     a.gqa_group = plan->gqa_group;
     a.scale_log2 = scale * 1.44269504088896340736f;
+    a.wait_prior = 1;
 #ifdef DEFT_KPROF
     if (!g_kprof_buf && cudaMalloc(&g_kprof_buf, deft::kKprofSlots * sizeof(unsigned long long)) != cudaSuccess)
         g_kprof_buf = nullptr;
@@ -228,7 +247,10 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
                 continue;
             const int32_t *it = items + 3 * (size_t)off[b];
             const int r = traced({DEFT_K_PHASE1_FMA, fam, b, fb, n, 0.f}, stream, [&] {
-                return deft::launch_phase1_fma(a, dp, it, cost.data() + off[b], n, b, stream);
+                const int r = deft::launch_phase1_fma(a, dp, it, cost.data() + off[b], n, b, stream);
+                if (r == 0)
+                    a.wait_prior = 0;
+                return r;
             });
             if (r)
                 return r;
@@ -246,7 +268,11 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
                     continue;
                 const int32_t *it = dp.mma_items + 3 * (size_t)hp.mma_bucket_off[b];
                 rc = traced({DEFT_K_PHASE1_MMA, fam, b, 0, n, 0.f}, stream, [&] {
-                    return deft::launch_phase1_mma(a, dp, it, n, b, stream);
+                    const int r = deft::launch_phase1_mma(a, dp, it, hp.mma_cost.data() + hp.mma_bucket_off[b],
+                                                          n, b, stream);
+                    if (r == 0)
+                        a.wait_prior = 0;
+                    return r;
                 });
             }
         } else

@@ -54,6 +54,18 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their writes are visible / let the next grid launch.
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;\n" ::);
@@ -63,6 +75,26 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait()
 {
     asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Host: launch `kernel` as a programmatic dependent of the stream's previous
+// kernel (it may be scheduled once that kernel's CTAs have all signalled
+// grid_dep_launch or exited; its own grid_dep_wait orders what must wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args &&...args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }
 
 }  // namespace deft

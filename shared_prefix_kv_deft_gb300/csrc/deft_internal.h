@@ -61,6 +61,7 @@ struct Partition {
     // CUDA-core launch cuts its units into contiguous, equal-cost CTA ranges.
     std::vector<int64_t> fma_cost;
     std::vector<int64_t> fallback_cost;
+    std::vector<int64_t> mma_cost;        // the same over mma_items
     // mma_items are sorted by column bucket b: each of the two softmax
     // warpgroups of an item holds NPH = 16 (b + 1) query rows; bucket b is
     // items [off[b], off[b+1]).
@@ -142,6 +143,13 @@ struct AttnArgs {
     float *o_part;            // fp32 [slots][Hq][d]
     float *lse_part;          // fp32 [slots][Hq], base-2 log-sum-exp of the base-2 logits
     unsigned long long *kprof;  // timestamp slots (development builds only; else null)
+    // 1 for the step's first launch: it waits for the stream's earlier work
+    // before reading anything.  Every launch of a step is a programmatic
+    // dependent of the one before (it may start while that one finishes);
+    // later phase-1 launches read only what the first one's wait already
+    // covered and write disjoint partials, and each waits for its
+    // predecessor before it exits, so the merge's single wait covers them all.
+    int32_t wait_prior;
 };
 
 // Launchers (return a cudaError_t cast to int; 0 = success).
@@ -150,8 +158,23 @@ struct AttnArgs {
 // `cost` points at the items' host cost prefix (n + 1 entries).
 int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
                       int32_t n, int bucket, void *stream);
+
+// Persistent phase-1 launches split their units (item-major: unit = item *
+// num_kv_heads + head) into contiguous per-CTA ranges of about equal cost:
+// CTA b takes units [begin[b], begin[b + 1]).
+constexpr int kMaxGrid = 256;
+struct CtaRanges {
+    int32_t begin[kMaxGrid + 1];
+};
+// Fills r for `grid` CTAs (grid <= kMaxGrid, <= n * hkv) from the items'
+// cost prefix; CTA b starts at the first unit whose cost prefix reaches
+// b / grid of the total.
+void cta_ranges(const int64_t *cost, int32_t n, int32_t hkv, int grid, CtaRanges &r);
+// Streaming multiprocessors of the current device.
+int num_sms();
 // One tensor-core launch over `n` items of column bucket `bucket`.
-int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
+int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
+                      int32_t n,
                       int bucket, void *stream);
 // Row bucket of an item with `rows` rows: smallest b with rows <= 2^b.
 inline int row_bucket(int rows) { return rows <= 1 ? 0 : rows <= 2 ? 1 : rows <= 4 ? 2 : rows <= 8 ? 3 : 4; }

@@ -171,6 +171,7 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
     a.head_dim = head_dim;
     a.gqa_group = plan->gqa_group;
     a.scale_log2 = scale * 1.44269504088896340736f;
+    a.wait_prior = 1;
     a.o_part = reinterpret_cast<float *>(base + o_off);
     a.lse_part = reinterpret_cast<float *>(base + lse_off);
 
@@ -183,6 +184,7 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
                                                       b, stream);
                 if (r)
                     return r;
+                a.wait_prior = 0;
             }
         }
         return 0;
@@ -192,8 +194,11 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
             for (int b = 0; b < 4 && !rc; ++b) {
                 const int32_t n = p.mma_bucket_off[b + 1] - p.mma_bucket_off[b];
                 if (n > 0)
-                    rc = deft::launch_phase1_mma(a, d, d.mma_items + 3 * (size_t)p.mma_bucket_off[b], n, b,
+                    rc = deft::launch_phase1_mma(a, d, d.mma_items + 3 * (size_t)p.mma_bucket_off[b],
+                                                 p.mma_cost.data() + p.mma_bucket_off[b], n, b,
                                                  stream);
+                if (n > 0 && rc == 0)
+                    a.wait_prior = 0;
             }
         } else {
             rc = fma_launches(d.fallback_items, p.fallback_cost, p.fallback_bucket_off);

@@ -111,12 +111,6 @@ struct ItemInfo {
     int32_t pad;
 };
 
-// Contiguous unit ranges, one per CTA: CTA b takes units [begin[b], begin[b+1]).
-constexpr int kMaxFmaGrid = 256;
-struct CtaRanges {
-    int32_t begin[kMaxFmaGrid + 1];
-};
-
 template <int D, int RMAX>
 __global__ void __launch_bounds__(FmaCfg<D, RMAX>::THREADS, 1)
 phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
@@ -147,9 +141,10 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     // parity alone cannot tell one use from the one before.
     volatile int32_t *stag = reinterpret_cast<volatile int32_t *>(smem + C::tag_off);
 
+    if (a.wait_prior)
+        grid_dep_wait();
     if (tid == 0) {
-        if (blockIdx.x < 1024)
-            KPROF_ANY(a, 3072 + blockIdx.x);
+        grid_dep_launch();
         for (int s = 0; s < ST; ++s) {
             stag[s] = -1;
             tc::mbar_init(fbar(bars, kFull + s), 33);
@@ -639,49 +634,15 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::named_sync(bar_id, nthr);
             if (gtid == 0)
                 KPROF(a, 2000 + 8 * i + 4);
-            if (gtid == 0 && blockIdx.x < 512 && u0 + i + NG >= u1)
-                KPROF_ANY(a, 1024 + 2 * blockIdx.x + g);
             if (lane == 0)
                 tc::mbar_arrive(fbar(bars, kUEmpty + ub));
         }
     }
+    // This grid completes only after the launch before it has.
+    if (tid == 0)
+        grid_dep_wait();
 }
 
-int num_sms()
-{
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 1;
-    }
-    return n;
-}
-
-// Cuts units [0, n * hkv) (item-major) into `grid` contiguous ranges of
-// about equal cost: CTA b starts at the first unit whose cost prefix
-// reaches b / grid of the total.  `cost` is the items' cost prefix.
-void cta_ranges(const int64_t *cost, int32_t n, int32_t hkv, int grid, CtaRanges &r)
-{
-    const int64_t c0 = cost[0];
-    const int64_t total = (int64_t)hkv * (cost[n] - c0);
-    int32_t i = 0;
-    r.begin[0] = 0;
-    for (int b = 1; b < grid; ++b) {
-        const int64_t target = total * b / grid;
-        while (i < n && (int64_t)hkv * (cost[i + 1] - c0) <= target)
-            ++i;
-        if (i == n) {
-            r.begin[b] = n * hkv;
-            continue;
-        }
-        const int64_t rem = target - (int64_t)hkv * (cost[i] - c0);
-        const int64_t ci = cost[i + 1] - cost[i];
-        r.begin[b] = (int32_t)((int64_t)i * hkv + (rem + ci - 1) / ci);
-    }
-    r.begin[grid] = n * hkv;
-}
 
 template <int D, int RMAX>
 int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost, int32_t n,
@@ -697,12 +658,12 @@ int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, c
         configured = true;
     }
     const int64_t units = (int64_t)n * a.num_kv_heads;
-    const int64_t cap = num_sms() < kMaxFmaGrid ? num_sms() : kMaxFmaGrid;
+    const int64_t cap = num_sms() < kMaxGrid ? num_sms() : kMaxGrid;
     const int grid = (int)(units < cap ? units : cap);
     CtaRanges r;
     cta_ranges(cost, n, a.num_kv_heads, grid, r);
-    phase1_fma_kernel<D, RMAX><<<grid, C::THREADS, C::alloc, st>>>(a, p, items, r);
-    return (int)cudaGetLastError();
+    return (int)launch_dependent(phase1_fma_kernel<D, RMAX>, dim3(grid), dim3(C::THREADS), C::alloc, st, a, p,
+                                 items, r);
 }
 
 template <int D>

@@ -8,19 +8,24 @@
 // are dense contractions worth the tensor cores.
 //
 // Formulation: KV tokens on the MMA M dimension (128-token tiles), the
-// item's query rows on N (RP = rows rounded to 16, at most 128):
+// item's query rows on N (RP = 2 NPH columns, NPH a template parameter;
+// columns past the item's rows are masked):
 //     S^T[128 tok x RP]  = K_tile . Q^T            (TMEM, fp32, 2 buffers)
-//     O^T[128 d   x RP] += V_tile^T . P^T          (TMEM, fp32)
+//     O^T[128 d   x RP] += V_tile^T . P^T          (TMEM, fp32, 2 buffers)
 // Eight MMAs (K = 16 each) per product and tile.  Two softmax warpgroups
-// split the RP columns (NPH each, a template parameter); a thread owns one
-// token of S^T and, at the end, one output dimension of O^T.  The column
-// maximum is exact after the first tile and afterwards only raised (with a
-// rescale of O and of the per-thread column sums) when a logit exceeds it
-// by more than 2^8, decided by a warpgroup vote.  Logits are base 2.
+// split the RP columns (NPH each); a thread owns one token of S^T and, at
+// the end, one output dimension of O^T.  The column maximum is exact after
+// a unit's first tile and afterwards only raised (with a rescale of O and
+// of the per-thread column sums) when a logit exceeds it by more than 2^8,
+// decided by a warpgroup vote.  Logits are base 2.
 //
-// Roles (10 warps):
-//   warps 0-3, 4-7  softmax warpgroups 0 and 1 (row halves);
-//   warps 8, 10     K and V producers: resolve the tile's pages through the
+// Persistent CTAs (one per SM) take contiguous, equal-cost ranges of units
+// (unit = item x KV head, item-major); all roles walk the range in order and
+// the CTA's tiles form one sequence through the stages, so the next unit's
+// loads and its first S overlap the end of the current one.
+// Roles (12 warps):
+//   warps 0-3, 4-7  softmax warpgroups 0 and 1 (column halves);
+//   warps 8, 10     K and V producers: resolve a tile's pages through the
 //                   page table one tile ahead, load full aligned pages with
 //                   TMA (2 KB boxes of the 128-byte-swizzled layout) and
 //                   ragged rows (node tails, packed one-token nodes) with
@@ -28,11 +33,14 @@
 //                   is refilled as soon as S of the tile two back is done,
 //                   V once its P.V is done;
 //   warp 9          allocates TMEM; lane 0 issues the MMAs, S(t) and P.V(t-1)
-//                   in whichever order their inputs become ready.
+//                   in whichever order their inputs become ready;
+//   warp 11         per item, the segment table (positions, page bases,
+//                   row masks); per unit, Q^T once the previous unit's last
+//                   S has read the buffer.
 // Two KV stages; every hand-off is an mbarrier, every wait on one is
-// bounded.  A CTA whose wait runs out writes NaN partials (the step's
-// output then shows the failure), waits for its own copies, frees TMEM and
-// returns.
+// bounded.  A CTA whose wait runs out writes NaN partials for its units
+// (the step's output then shows the failure), waits for its own copies,
+// frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,35 +54,61 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTileTok = 128;
-constexpr int kThreadsMma = 352;
+constexpr int kThreadsMma = 384;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kHalf = 128 * 128;       // one 64-wide half of a 128-row operand (16 KB)
 constexpr uint32_t kTileBytes = 2 * kHalf;  // one 128 x 128 bf16 operand (32 KB)
 constexpr uint32_t kHalfPage = 2 * 2048;    // K (or V) of one 16-token page: two TMA boxes
+constexpr int kSegInts = 7 * kMaxSegsPerChunk;  // pos, page base, token begin, row mask (4)
+
+struct UnitInfo {
+    int32_t R;       // rows
+    int32_t cq0;     // first slot of the unit's rows
+    int32_t h;       // KV head
+    int32_t ntiles;
+    int32_t pad[4];
+};
+
+struct ItemInfo {
+    int32_t nseg;
+    int32_t T;       // chunk tokens
+    int32_t pad[2];
+};
 
 struct Smem {
     static constexpr uint32_t kv_off = 0;                            // [stage][K,V] operands
     static constexpr uint32_t q_off = kv_off + 4 * kTileBytes;       // Q^T: [d half][128 rows][128 B]
     static constexpr uint32_t p_off = q_off + kTileBytes;            // P^T: [col block][128 tok][128 B]
     static constexpr uint32_t meta_off = p_off + kTileBytes;         // [4 slots][128] uint4 row masks
-    static constexpr uint32_t seg_off = meta_off + 4 * kTileTok * 16;  // pos, page base, tb, masks
-    static constexpr uint32_t red_off = seg_off + kMaxSegsPerChunk * (12 + 16);  // [wg][warp][64]
+    static constexpr uint32_t seg_off = meta_off + 4 * kTileTok * 16;  // [2][kSegInts]
+    static constexpr uint32_t red_off = seg_off + 2 * kSegInts * 4;  // [wg][warp][64]
     static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;  // [wg][m, alpha, 1/l][64]
-    static constexpr uint32_t bar_off = stat_off + 2 * 3 * 64 * 4;  // mbarriers
-    static constexpr uint32_t misc_off = bar_off + 16 * 8;          // tmem base, error flag
+    static constexpr uint32_t uinfo_off = stat_off + 2 * 3 * 64 * 4;  // [2] UnitInfo
+    static constexpr uint32_t iinfo_off = uinfo_off + 2 * 32;         // [2] ItemInfo
+    static constexpr uint32_t bar_off = iinfo_off + 2 * 16;          // mbarriers
+    static constexpr uint32_t misc_off = bar_off + 32 * 8;          // tmem base, error flag
     static constexpr uint32_t total = misc_off + 16;
     static constexpr uint32_t alloc = total + 1024;
+    static_assert(alloc <= 227 * 1024, "shared memory of one CTA");
 };
 
 // mbarrier slots
-constexpr int kBarFullK = 0;   // [2] K of a stage landed (producer: 32 lanes + tx)
-constexpr int kBarFullV = 2;   // [2] V of a stage landed
-constexpr int kBarEmptyK = 4;  // [2] S of the stage's tile finished (MMA commit)
-constexpr int kBarEmptyV = 6;  // [2] P.V of the stage's tile finished (MMA commit)
-constexpr int kBarSFull = 8;   // [2] S buffer ready (MMA commit)
-constexpr int kBarSFree = 10;  // [2] S buffer read (one arrival per warpgroup)
-constexpr int kBarPFull = 12;  // P written (one arrival per warpgroup)
-constexpr int kBarPvDone = 13; // P.V finished (MMA commit)
+constexpr int kBarFullK = 0;     // [2] K of a stage landed (producer: 32 lanes + tx)
+constexpr int kBarFullV = 2;     // [2] V of a stage landed
+constexpr int kBarEmptyK = 4;    // [2] S of the stage's tile finished (MMA commit)
+constexpr int kBarEmptyV = 6;    // [2] P.V of the stage's tile finished (MMA commit)
+constexpr int kBarSFull = 8;     // [2] S buffer ready (MMA commit)
+constexpr int kBarSFree = 10;    // [2] S buffer read (one arrival per warpgroup)
+constexpr int kBarPFull = 12;    // P written (one arrival per warpgroup)
+constexpr int kBarPvDone = 13;   // P.V finished (MMA commit)
+constexpr int kBarSegFull = 14;  // [2] an item's segment table written (32 lanes)
+constexpr int kBarSegEmpty = 16; // [2] ... no longer read (both producers, 32 lanes each)
+constexpr int kBarUFull = 18;    // [2] a unit's description and Q^T written (32 lanes)
+constexpr int kBarUEmpty = 20;   // [2] ... description read (MMA issuer + 2 warpgroups)
+constexpr int kBarQFree = 22;    // the unit's last S finished: Q^T may be replaced (MMA commit)
+constexpr int kBarOFree = 23;    // [2] O buffer read out by the epilogue (one per warpgroup)
+constexpr int kNumBars = 25;
+static_assert(kNumBars * 8 <= Smem::misc_off - Smem::bar_off, "mbarrier space");
 
 template <bool kMax>
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
@@ -96,40 +130,40 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
 template <int NPH>
 __global__ void __launch_bounds__(kThreadsMma, 1)
 phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
-                  const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v)
+                  const __grid_constant__ CtaRanges ranges, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v)
 {
+    constexpr int RP = 2 * NPH;   // MMA N: both warpgroups' columns
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
     uint4 *meta = reinterpret_cast<uint4 *>(smem + Smem::meta_off);
-    int32_t *s_pos = reinterpret_cast<int32_t *>(smem + Smem::seg_off);
-    int32_t *s_pgb = s_pos + kMaxSegsPerChunk;
-    int32_t *s_tb = s_pgb + kMaxSegsPerChunk;
-    uint4 *s_rmask = reinterpret_cast<uint4 *>(smem + Smem::seg_off + kMaxSegsPerChunk * 12);
     float *red = reinterpret_cast<float *>(smem + Smem::red_off);
     float *stat = reinterpret_cast<float *>(smem + Smem::stat_off);
+    UnitInfo *uinfo = reinterpret_cast<UnitInfo *>(smem + Smem::uinfo_off);
+    ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + Smem::iinfo_off);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::misc_off);
     volatile int *err = reinterpret_cast<volatile int *>(smem + Smem::misc_off + 4);
     auto bar = [&](int i) { return base + Smem::bar_off + 8u * (uint32_t)i; };
+    // Segment table of buffer sb: s_pos, s_pgb (first page_id index of the
+    // node), s_tb (token begin in the node), s_rmask (columns of warpgroup 0
+    // in bits 0-63, of warpgroup 1 in bits 64-127).
+    auto seg_tab = [&](int sbuf) { return reinterpret_cast<int32_t *>(smem + Smem::seg_off) + sbuf * kSegInts; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
-    const int item = blockIdx.x / Hkv;
-    const int h = blockIdx.x - item * Hkv;
-    const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
-    const int R = (qe - qb) * G;  // mma_half_cols(R) == NPH
-    const int rows_w1 = R > NPH ? R - NPH : 0;
-    const int nwg = rows_w1 > 0 ? 2 : 1;
-    const int RP = nwg * NPH;     // MMA N
-    const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
-    const int cq0 = p.chunk_q_off[c] + qb;
-    const int T = p.chunk_tokens[c];
-    const int ntiles = (T + kTileTok - 1) / kTileTok;
+    const int u0 = ranges.begin[blockIdx.x], u1 = ranges.begin[blockIdx.x + 1];
 
     // ---------------- set-up ----------------
-    if (tid == 0)
+    if (a.wait_prior)
+        grid_dep_wait();
+    if (tid == 0) {
+        grid_dep_launch();
         KPROF(a, 0);
+        if (blockIdx.x < 1024)
+            KPROF_ANY(a, 3072 + blockIdx.x);
+    }
     if (warp == 9) {
         tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tc::tmem_relinquish();
@@ -139,44 +173,25 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_init(bar(i), 33);
         for (int i = kBarEmptyK; i < kBarSFree; ++i)
             tc::mbar_init(bar(i), 1);
-        tc::mbar_init(bar(kBarSFree + 0), nwg);
-        tc::mbar_init(bar(kBarSFree + 1), nwg);
-        tc::mbar_init(bar(kBarPFull), nwg);
+        tc::mbar_init(bar(kBarSFree + 0), 2);
+        tc::mbar_init(bar(kBarSFree + 1), 2);
+        tc::mbar_init(bar(kBarPFull), 2);
         tc::mbar_init(bar(kBarPvDone), 1);
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(kBarSegFull + i), 32);
+            tc::mbar_init(bar(kBarSegEmpty + i), 64);
+            tc::mbar_init(bar(kBarUFull + i), 32);
+            tc::mbar_init(bar(kBarUEmpty + i), 3);
+            tc::mbar_init(bar(kBarOFree + i), 2);
+        }
+        tc::mbar_init(bar(kBarQFree), 1);
         *err = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 8 && lane == 0) {
-        tc::prefetch_tmap(&tmap_k);
-        tc::prefetch_tmap(&tmap_v);
-    }
+    // Operands start finite: rows past a chunk's end are never loaded and
+    // their P is 0, which must not meet a NaN.
     for (uint32_t i = tid; i < Smem::meta_off / 16; i += kThreadsMma)
         reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
-    for (int s = tid; s < nseg; s += kThreadsMma) {
-        s_pos[s] = p.seg_chunk_pos[sb + s];
-        s_pgb[s] = a.node_page_off[p.seg_node[sb + s]];   // first page_id index of the node
-        s_tb[s] = p.seg_tok_begin[sb + s];
-        const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
-        uint32_t rm[4] = {0, 0, 0, 0};  // warpgroup 0 bits 0-63, warpgroup 1 bits 64-127
-#pragma unroll 4
-        for (int r = 0; r < R; ++r) {
-            const int k = qb + r / G;
-            const uint32_t bit = (lm[k >> 5] >> (k & 31)) & 1u;
-            const int col = r < NPH ? r : 64 + (r - NPH);
-            rm[col >> 5] |= bit << (col & 31);
-        }
-        s_rmask[s] = make_uint4(rm[0], rm[1], rm[2], rm[3]);
-    }
-    __syncthreads();
-    const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-    for (int i = tid; i < R * 16; i += kThreadsMma) {
-        const int r = i >> 4, ch = i & 15;
-        const int qid = p.chunk_q[cq0 + r / G];
-        const int hq = h * G + (r % G);
-        const uint4 v = *reinterpret_cast<const uint4 *>(qg + ((size_t)qid * Hq + hq) * kD + ch * 8);
-        *reinterpret_cast<uint4 *>(smem + Smem::q_off + (ch >> 3) * kHalf + r * 128 +
-                                   (((ch & 7) ^ (r & 7)) << 4)) = v;
-    }
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -185,7 +200,110 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     if (tid == 0)
         KPROF(a, 1);
 
-    if (warp == 8 || warp == 10) {
+    if (warp == 11) {
+        // ---------------- metadata: segment tables and Q^T ----------------
+        // Per unit, Q^T is copied once the previous unit's last S has read
+        // the buffer; the rows of the unit after it are prefetched into L2
+        // meanwhile.  A new item's Q^T copy is issued before its segment
+        // table is built, so the two chains of dependent loads overlap.
+        const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+        int iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
+        auto issue_q = [&](int h) {
+            for (int x = lane; x < R * 16; x += 32) {
+                const int r = x >> 4, ch = x & 15;
+                const int qid = p.chunk_q[cq0 + r / G];
+                cp_async_16(base + Smem::q_off + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
+                            qg + ((size_t)qid * Hq + h * G + (r % G)) * kD + ch * 8);
+            }
+            cp_async_commit();
+        };
+        auto prefetch_q = [&](int h) {
+            for (int x = lane; x < R * 2; x += 32) {
+                const int r = x >> 1;
+                const int qid = p.chunk_q[cq0 + r / G];
+                const char *addr = reinterpret_cast<const char *>(qg + ((size_t)qid * Hq + h * G + (r % G)) * kD) +
+                                   (x & 1) * 128;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+            }
+        };
+        for (int u = u0; u < u1; ++u) {
+            const int i = u - u0;
+            const int item = u / Hkv, h = u - item * Hkv;
+            const int ub = i & 1;
+            bool q_issued = false;
+            if (item != prev_item) {
+                prev_item = item;
+                ++iseq;
+                const int sbuf = iseq & 1;
+                const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
+                if (lane == 0 && i == 0)
+                    KPROF(a, 30);
+                R = (qe - qb) * G;
+                const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
+                cq0 = p.chunk_q_off[c] + qb;
+                const int T = p.chunk_tokens[c];
+                ntiles = (T + kTileTok - 1) / kTileTok;
+                if (lane == 0 && i == 0)
+                    KPROF(a, 31 + 0 * (sb + nseg + cq0 + T));
+                if (i == 0) {
+                    issue_q(h);
+                    q_issued = true;
+                }
+                if (lane == 0 && i == 0)
+                    KPROF(a, 32);
+                if (iseq >= 2 &&
+                    !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegEmpty + sbuf), ((iseq - 2) >> 1) & 1))) {
+                    *err = 1;
+                    break;
+                }
+                int32_t *tab = seg_tab(sbuf);
+                uint4 *s_rmask = reinterpret_cast<uint4 *>(tab + 3 * kMaxSegsPerChunk);
+                for (int s = lane; s < nseg; s += 32) {
+                    tab[s] = p.seg_chunk_pos[sb + s];
+                    tab[kMaxSegsPerChunk + s] = a.node_page_off[p.seg_node[sb + s]];
+                    tab[2 * kMaxSegsPerChunk + s] = p.seg_tok_begin[sb + s];
+                    const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
+                    uint32_t rm[4] = {0, 0, 0, 0};
+#pragma unroll 4
+                    for (int r = 0; r < R; ++r) {
+                        const int k = qb + r / G;
+                        const uint32_t bit = (lm[k >> 5] >> (k & 31)) & 1u;
+                        const int col = r < NPH ? r : 64 + (r - NPH);
+                        rm[col >> 5] |= bit << (col & 31);
+                    }
+                    s_rmask[s] = make_uint4(rm[0], rm[1], rm[2], rm[3]);
+                }
+                if (lane == 0 && i == 0)
+                    KPROF(a, 33);
+                if (lane == 0)
+                    iinfo[sbuf] = ItemInfo{nseg, T, {0, 0}};
+                __syncwarp();
+                tc::mbar_arrive(bar(kBarSegFull + sbuf));
+                if (lane == 0 && i < 8)
+                    KPROF(a, 10 + i);
+            }
+            if (!q_issued) {
+                bool okw = i < 2 || tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1);
+                okw = okw && tc::mbar_wait(bar(kBarQFree), (i - 1) & 1);
+                if (!__all_sync(0xffffffffu, okw)) {
+                    *err = 1;
+                    break;
+                }
+                issue_q(h);
+            }
+            cp_async_wait<0>();
+            tc::fence_proxy_async();
+            if (lane == 0)
+                uinfo[ub] = UnitInfo{R, cq0, h, ntiles, {0, 0, 0, 0}};
+            __syncwarp();
+            tc::mbar_arrive(bar(kBarUFull + ub));
+            if (lane == 0 && i < 8)
+                KPROF(a, 20 + i);
+            // Warm L2 with the next unit's rows when it is the same item.
+            if (u + 1 < u1 && (u + 1) / Hkv == item)
+                prefetch_q(h + 1);
+        }
+    } else if (warp == 8 || warp == 10) {
         // ---------------- producers (warp 8: K, warp 10: V) ----------------
         const int kv = warp == 8 ? 0 : 1;
         const __nv_bfloat16 *src_base = reinterpret_cast<const __nv_bfloat16 *>(kv ? a.v_pages : a.k_pages);
@@ -195,9 +313,12 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         // One tile's resolution: rows lane + 32k (k < 4) and pages 0..7.
         struct Res {
             int seg[4], tok[4], pid[4];   // per row; pid only for ragged rows
-            int page_y;                   // lane < 8: TMA row coordinate of page `lane`
+            int page_y;                   // lane < 8: page id of page `lane` when it goes by TMA
             uint32_t tma_pages;
         };
+        const int32_t *s_pos = nullptr, *s_pgb = nullptr, *s_tb = nullptr;
+        const uint4 *s_rmask = nullptr;
+        int T = 0, nseg = 0;
         auto resolve = [&](int t, Res &r) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -251,87 +372,123 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     r.pid[k] = a.page_id[s_pgb[r.seg[k]] + r.tok[k] / kPageSize];
             }
         };
-        int last_tile[2] = {-1, -1};
-        Res res;
-        if (ntiles > 0)
-            resolve(0, res);
-        for (int t = 0; t < ntiles; ++t) {
-            const int st = t & 1;
-            if (t >= 2) {
-                const bool ok = __all_sync(
-                    0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((t - 2) >> 1) & 1));
-                if (!ok) {
+        int last0 = -1, last1 = -1;   // last tile placed in stage 0 / 1
+        int iseq = -1, prev_item = -1, gseq = 0;
+        bool ok = true;
+        for (int u = u0; u < u1 && ok; ++u) {
+            const int item = u / Hkv, h = u - item * Hkv;
+            if (item != prev_item) {
+                prev_item = item;
+                ++iseq;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegFull + (iseq & 1)), (iseq >> 1) & 1))) {
                     *err = 1;
                     break;
                 }
             }
-            if (kv == 0) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    meta[(t & 3) * kTileTok + lane + 32 * k] =
-                        res.seg[k] >= 0 ? s_rmask[res.seg[k]] : make_uint4(0, 0, 0, 0);
-            }
-            const uint32_t full = bar((kv ? kBarFullV : kBarFullK) + st);
-            const uint32_t dst = base + Smem::kv_off + (uint32_t)(st * 2 + kv) * kTileBytes;
-            if (lane == 0)
-                tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
-            __syncwarp();
-            if (res.page_y >= 0) {
-                const int y = (res.page_y * Hkv + h) * kPageSize;
-                const uint32_t row_b = (uint32_t)(16 * lane) * 128;
-                tc::tma_load_2d(dst + row_b, tm, 0, y, full);
-                tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full);
-            }
-            // Ragged rows: two rows per warp step, 16 lanes (16-byte chunks) each.
-            bool any_cp = false;
-            const __nv_bfloat16 *src0 = src_base + (lane & 15) * 8;
-            const uint32_t dst0 = dst + ((lane & 15) >> 3) * kHalf;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint32_t nb = __ballot_sync(0xffffffffu, res.pid[k] >= 0);
-                any_cp |= nb != 0;
-                while (nb) {
-                    const int l0 = __ffs(nb) - 1;
-                    nb &= nb - 1;
-                    int l1 = -1;
-                    if (nb) {
-                        l1 = __ffs(nb) - 1;
-                        nb &= nb - 1;
-                    }
-                    const int mine = lane < 16 ? l0 : l1;
-                    const int p0 = __shfl_sync(0xffffffffu, res.pid[k], l0);
-                    const int t0 = __shfl_sync(0xffffffffu, res.tok[k], l0);
-                    const int p1 = __shfl_sync(0xffffffffu, res.pid[k], l1 < 0 ? l0 : l1);
-                    const int t1 = __shfl_sync(0xffffffffu, res.tok[k], l1 < 0 ? l0 : l1);
-                    if (mine >= 0) {
-                        const int row = mine + 32 * k;
-                        const int pg = lane < 16 ? p0 : p1;
-                        const int tk = lane < 16 ? t0 : t1;
-                        const long long o = (((long long)pg * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
-                        const int ch = lane & 7;
-                        cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src0 + o);
+            const int sbuf = iseq & 1;
+            const int32_t *tab = seg_tab(sbuf);
+            s_pos = tab;
+            s_pgb = tab + kMaxSegsPerChunk;
+            s_tb = tab + 2 * kMaxSegsPerChunk;
+            s_rmask = reinterpret_cast<const uint4 *>(tab + 3 * kMaxSegsPerChunk);
+            const ItemInfo ii = iinfo[sbuf];
+            T = ii.T;
+            nseg = ii.nseg;
+            const int ntiles = (T + kTileTok - 1) / kTileTok;
+            if (lane == 0 && kv == 0 && gseq == 0)
+                KPROF(a, 40);
+            Res res;
+            resolve(0, res);
+            if (lane == 0 && kv == 0 && gseq == 0)
+                KPROF(a, 41 + 0 * res.page_y);
+            for (int t = 0; t < ntiles; ++t, ++gseq) {
+                const int st = gseq & 1;
+                if (gseq >= 2) {
+                    const bool okw = __all_sync(
+                        0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((gseq - 2) >> 1) & 1));
+                    if (!okw) {
+                        *err = 1;
+                        ok = false;
+                        break;
                     }
                 }
+                if (kv == 0) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        meta[(gseq & 3) * kTileTok + lane + 32 * k] =
+                            res.seg[k] >= 0 ? s_rmask[res.seg[k]] : make_uint4(0, 0, 0, 0);
+                }
+                const uint32_t full = bar((kv ? kBarFullV : kBarFullK) + st);
+                const uint32_t dst = base + Smem::kv_off + (uint32_t)(st * 2 + kv) * kTileBytes;
+                if (lane == 0)
+                    tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
+                __syncwarp();
+                if (res.page_y >= 0) {
+                    const int y = (res.page_y * Hkv + h) * kPageSize;
+                    const uint32_t row_b = (uint32_t)(16 * lane) * 128;
+                    tc::tma_load_2d(dst + row_b, tm, 0, y, full);
+                    tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full);
+                }
+                // Ragged rows: two rows per warp step, 16 lanes (16-byte chunks) each.
+                bool any_cp = false;
+                const __nv_bfloat16 *src0 = src_base + (lane & 15) * 8;
+                const uint32_t dst0 = dst + ((lane & 15) >> 3) * kHalf;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t nb = __ballot_sync(0xffffffffu, res.pid[k] >= 0);
+                    any_cp |= nb != 0;
+                    while (nb) {
+                        const int l0 = __ffs(nb) - 1;
+                        nb &= nb - 1;
+                        int l1 = -1;
+                        if (nb) {
+                            l1 = __ffs(nb) - 1;
+                            nb &= nb - 1;
+                        }
+                        const int mine = lane < 16 ? l0 : l1;
+                        const int p0 = __shfl_sync(0xffffffffu, res.pid[k], l0);
+                        const int t0 = __shfl_sync(0xffffffffu, res.tok[k], l0);
+                        const int p1 = __shfl_sync(0xffffffffu, res.pid[k], l1 < 0 ? l0 : l1);
+                        const int t1 = __shfl_sync(0xffffffffu, res.tok[k], l1 < 0 ? l0 : l1);
+                        if (mine >= 0) {
+                            const int row = mine + 32 * k;
+                            const int pg = lane < 16 ? p0 : p1;
+                            const int tk = lane < 16 ? t0 : t1;
+                            const long long o = (((long long)pg * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
+                            const int ch = lane & 7;
+                            cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src0 + o);
+                        }
+                    }
+                }
+                if (any_cp) {
+                    cp_async_commit();
+                    cp_async_wait<0>();
+                    tc::fence_proxy_async();
+                }
+                tc::mbar_arrive(full);
+                if (lane == 0 && gseq < 64)
+                    KPROF(a, 100 + 100 * kv + gseq);
+                if (st)
+                    last1 = gseq;
+                else
+                    last0 = gseq;
+                if (t + 1 < ntiles)
+                    resolve(t + 1, res);
             }
-            if (any_cp) {
-                cp_async_commit();
-                cp_async_wait<0>();
-                tc::fence_proxy_async();
+            if (!ok)
+                break;
+            // Release the item's segment table after its last unit here.
+            if (u + 1 == u1 || (u + 1) / Hkv != item) {
+                __syncwarp();
+                tc::mbar_arrive(bar(kBarSegEmpty + sbuf));
             }
-            tc::mbar_arrive(full);
-            if (lane == 0 && kv == 0)
-                KPROF(a, 102 + 4 * t);
-            last_tile[st] = t;
-            if (t + 1 < ntiles)
-                resolve(t + 1, res);
-            if (lane == 0 && kv == 0)
-                KPROF(a, 100 + 4 * (t + 1));
         }
         cp_async_wait<0>();
         // Do not leave while a TMA copy of ours may still be landing.
-        for (int s2 = 0; s2 < 2; ++s2)
-            if (last_tile[s2] >= 0)
-                tc::mbar_wait(bar((kv ? kBarFullV : kBarFullK) + s2), (last_tile[s2] >> 1) & 1);
+        if (last0 >= 0)
+            tc::mbar_wait(bar(kv ? kBarFullV : kBarFullK), (last0 >> 1) & 1);
+        if (last1 >= 0)
+            tc::mbar_wait(bar((kv ? kBarFullV : kBarFullK) + 1), (last1 >> 1) & 1);
     } else if (warp == 9) {
         // ---------------- MMA issue ----------------
         if (lane == 0) {
@@ -345,18 +502,30 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 dk[st] = tc::smem_desc(base + Smem::kv_off + (uint32_t)(st * 2) * kTileBytes, 16, 1024);
                 dv[st] = tc::smem_desc(base + Smem::kv_off + (uint32_t)(st * 2 + 1) * kTileBytes, kHalf, 1024);
             }
+            const int nunits = u1 - u0;
+            // S cursor: unit is, its tile ts (nts tiles, -1 before its
+            // description is read), CTA tile gs.  P.V cursor: ip, tp, gp.
+            int is = 0, ts = 0, nts = -1, gs = 0;
+            int ip = 0, tp = 0, gp = 0;
+            int ntq0 = 0, ntq1 = 0;   // tiles of the units in flight, by unit parity
             bool ok = true;
-            int ts = 0, tpv = 0;   // next S tile, next P.V tile
             uint32_t polls = 0;
-            while (tpv < ntiles && ok) {
+            while (ip < nunits && ok) {
                 bool progressed = false;
-                // S(ts): needs K(ts) and S buffer ts % 2 released by tile ts - 2.
-                if (ts < ntiles && ts <= tpv + 1) {
-                    const int st = ts & 1, b = ts & 1;
-                    if (tc::mbar_test(bar(kBarFullK + st), (ts >> 1) & 1) &&
-                        (ts < 2 || tc::mbar_test(bar(kBarSFree + b), ((ts - 2) >> 1) & 1))) {
-                        if (tid == 288)
-                            KPROF(a, 400 + 4 * ts);
+                // S(gs): needs the unit's Q^T, K(gs) and S buffer gs % 2
+                // released by tile gs - 2; at most one tile ahead of P.V.
+                if (is < nunits && gs <= gp + 1) {
+                    if (nts < 0 && tc::mbar_test(bar(kBarUFull + (is & 1)), (is >> 1) & 1)) {
+                        nts = uinfo[is & 1].ntiles;
+                        if (is & 1)
+                            ntq1 = nts;
+                        else
+                            ntq0 = nts;
+                        tc::mbar_arrive(bar(kBarUEmpty + (is & 1)));
+                    }
+                    const int st = gs & 1, b = gs & 1;
+                    if (nts > 0 && tc::mbar_test(bar(kBarFullK + st), (gs >> 1) & 1) &&
+                        (gs < 2 || tc::mbar_test(bar(kBarSFree + b), ((gs - 2) >> 1) & 1))) {
                         tc::fence_after_sync();
                         const uint32_t d_s = tmem + (uint32_t)(b * 128);
 #pragma unroll
@@ -366,29 +535,41 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         }
                         tc::mma_commit(bar(kBarSFull + b));
                         tc::mma_commit(bar(kBarEmptyK + st));
-                        if (tid == 288)
-                            KPROF(a, 401 + 4 * ts);
-                        ++ts;
+                        if (gs < 64)
+                            KPROF(a, 300 + gs);
+                        ++gs;
+                        if (++ts == nts) {
+                            tc::mma_commit(bar(kBarQFree));
+                            ++is;
+                            ts = 0;
+                            nts = -1;
+                        }
                         progressed = true;
                     }
                 }
-                // P.V(tpv): needs V(tpv) and P(tpv).
-                if (tpv < ts) {
-                    const int stp = tpv & 1;
-                    if (tc::mbar_test(bar(kBarFullV + stp), (tpv >> 1) & 1) &&
-                        tc::mbar_test(bar(kBarPFull), tpv & 1)) {
+                // P.V(gp): needs V(gp), P(gp) and, for a unit's first tile,
+                // its O buffer read out by the epilogue of the unit two back.
+                if (gp < gs) {
+                    const int stp = gp & 1, ob = ip & 1;
+                    if (tc::mbar_test(bar(kBarFullV + stp), (gp >> 1) & 1) &&
+                        tc::mbar_test(bar(kBarPFull), gp & 1) &&
+                        (tp > 0 || ip < 2 || tc::mbar_test(bar(kBarOFree + ob), ((ip - 2) >> 1) & 1))) {
                         tc::fence_after_sync();
-                        const uint32_t d_o = tmem + 256;
+                        const uint32_t d_o = tmem + 256 + (uint32_t)(ob * 128);
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
                             const uint64_t so = (uint64_t)((s * 2048) >> 4);
-                            tc::mma_bf16(d_o, dv[stp] + so, dp + so, idesc_o, (tpv > 0 || s > 0) ? 1u : 0u);
+                            tc::mma_bf16(d_o, dv[stp] + so, dp + so, idesc_o, (tp > 0 || s > 0) ? 1u : 0u);
                         }
                         tc::mma_commit(bar(kBarPvDone));
                         tc::mma_commit(bar(kBarEmptyV + stp));
-                        if (tid == 288)
-                            KPROF(a, 402 + 4 * tpv);
-                        ++tpv;
+                        if (gp < 64)
+                            KPROF(a, 400 + gp);
+                        ++gp;
+                        if (++tp == ((ip & 1) ? ntq1 : ntq0)) {
+                            ++ip;
+                            tp = 0;
+                        }
                         progressed = true;
                     }
                 }
@@ -404,26 +585,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         // ---------------- softmax warpgroups ----------------
         // Warpgroup w owns columns [w*NPH, w*NPH + NPH) of S^T and O^T.
         const int w = warp >> 2, wt = warp & 3, j = tid & 127;
-        const int rows_w = w == 0 ? (R < NPH ? R : NPH) : rows_w1;
         const uint32_t nb_id = 1 + (uint32_t)w;
         float *m_s = stat + w * 192, *alpha_s = m_s + 64, *linv = m_s + 128;
         float *redw = red + w * 256;
         const uint32_t lane_off = (uint32_t)(wt * 32) << 16;
         const uint32_t col0 = (uint32_t)(w * NPH);
-        const uint32_t tmem_o = tmem + 256 + lane_off + col0;
         uint8_t *prow_ptr = smem + Smem::p_off + (j >> 3) * 1024 + (j & 7) * 128;
         const float sc = a.scale_log2;
         constexpr float kSlack = 8.f;   // rescale only when 2^(s - m) would exceed 2^8
-        float l[NPH];
-#pragma unroll
-        for (int c2 = 0; c2 < NPH; ++c2)
-            l[c2] = 0.f;
-        if (j < 64) {
-            m_s[j] = -INFINITY;
-            alpha_s[j] = 1.f;
-        }
-        tc::named_sync(nb_id, 128);
-        bool ok = true;
         auto load_cols = [&](uint32_t taddr, float *v) {
 #pragma unroll
             for (int g = 0; g + 32 <= NPH; g += 32) {
@@ -446,31 +615,55 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 redw[wt * 64 + g + lane] = reduce_scatter32<true>(tmp, lane);
             }
         };
-        if (rows_w > 0) {
-            for (int t = 0; t < ntiles; ++t) {
-                const int b = t & 1;
-                ok = tc::mbar_wait(bar(kBarSFull + b), (t >> 1) & 1);
-                if (tid == 0)
-                    KPROF(a, 700 + 4 * t);
+        int gseq = 0;
+        for (int i = 0; u0 + i < u1; ++i) {
+            const int ub = i & 1, ob = i & 1;
+            const bool okw = tc::mbar_wait(bar(kBarUFull + ub), (i >> 1) & 1);
+            if (tc::named_sync_or(nb_id, 128, !okw)) {
+                *err = 1;
+                break;
+            }
+            const UnitInfo ui = uinfo[ub];
+            tc::named_sync(nb_id, 128);
+            if (j == 0)
+                tc::mbar_arrive(bar(kBarUEmpty + ub));
+            const int R = ui.R, ntiles = ui.ntiles;
+            const int rows_w = w == 0 ? (R < NPH ? R : NPH) : (R > NPH ? R - NPH : 0);
+            const uint32_t tmem_o = tmem + 256 + (uint32_t)(ob * 128) + lane_off + col0;
+            float l[NPH];
+#pragma unroll
+            for (int c2 = 0; c2 < NPH; ++c2)
+                l[c2] = 0.f;
+            if (j < 64) {
+                m_s[j] = -INFINITY;
+                alpha_s[j] = 1.f;
+            }
+            tc::named_sync(nb_id, 128);
+            bool ok = true;
+            for (int t = 0; t < ntiles; ++t, ++gseq) {
+                const int b = gseq & 1;
+                ok = tc::mbar_wait(bar(kBarSFull + b), (gseq >> 1) & 1);
                 tc::fence_after_sync();
+                if (tid == 0 && gseq < 64)
+                    KPROF(a, 500 + gseq);
                 float s[NPH];
                 load_cols(tmem + (uint32_t)(b * 128) + lane_off + col0, s);
-                const uint4 mk = meta[(t & 3) * kTileTok + j];
+                const uint4 mk = meta[(gseq & 3) * kTileTok + j];
                 const uint32_t mw0 = w == 0 ? mk.x : mk.z, mw1 = w == 0 ? mk.y : mk.w;
 #pragma unroll
-                for (int i = 0; i < NPH; ++i) {
-                    const uint32_t mword = i < 32 ? mw0 : mw1;
-                    s[i] = ((mword >> (i & 31)) & 1u) ? s[i] * sc : -INFINITY;
+                for (int c2 = 0; c2 < NPH; ++c2) {
+                    const uint32_t mword = c2 < 32 ? mw0 : mw1;
+                    s[c2] = ((mword >> (c2 & 31)) & 1u) ? s[c2] * sc : -INFINITY;
                 }
                 tc::fence_before_sync();
                 bool slow = t == 0;
                 if (t > 0) {
                     bool flag = false;
 #pragma unroll
-                    for (int i = 0; i < NPH; i += 4) {
-                        const float4 m4 = *reinterpret_cast<const float4 *>(m_s + i);
-                        flag |= (s[i] > m4.x + kSlack) | (s[i + 1] > m4.y + kSlack) |
-                                (s[i + 2] > m4.z + kSlack) | (s[i + 3] > m4.w + kSlack);
+                    for (int c2 = 0; c2 < NPH; c2 += 4) {
+                        const float4 m4 = *reinterpret_cast<const float4 *>(m_s + c2);
+                        flag |= (s[c2] > m4.x + kSlack) | (s[c2 + 1] > m4.y + kSlack) |
+                                (s[c2 + 2] > m4.z + kSlack) | (s[c2 + 3] > m4.w + kSlack);
                     }
                     if (tc::named_sync_or(nb_id, 128, flag || !ok)) {
                         if (tc::named_sync_or(nb_id, 128, !ok)) {
@@ -497,9 +690,11 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
                 if (j == 0)
                     tc::mbar_arrive(bar(kBarSFree + b));
+                // P (one buffer) may be rewritten once the previous tile's
+                // P.V is done; that P.V also finishes O before a rescale.
                 bool ok2 = true;
-                if (t >= 1) {
-                    ok2 = tc::mbar_wait(bar(kBarPvDone), (t - 1) & 1);
+                if (gseq >= 1) {
+                    ok2 = tc::mbar_wait(bar(kBarPvDone), (gseq - 1) & 1);
                     tc::fence_after_sync();
                 }
                 if (slow && t >= 1) {
@@ -508,15 +703,13 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         float o[16];
                         tc::tmem_ld16(tmem_o + g, o);
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            o[i] *= alpha_s[g + i];
-                            l[g + i] *= alpha_s[g + i];
+                        for (int c2 = 0; c2 < 16; ++c2) {
+                            o[c2] *= alpha_s[g + c2];
+                            l[g + c2] *= alpha_s[g + c2];
                         }
                         tc::tmem_st16(tmem_o + g, o);
                     }
                 }
-                if (tid == 0)
-                    KPROF(a, 702 + 4 * t);
                 // Probabilities: fp32 column sums, bf16 P^T (MN-major: token
                 // row j holds the columns, 16-byte chunks swizzled by j % 8).
 #pragma unroll
@@ -526,10 +719,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     const float mm[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
                     float pv[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float x = s[8 * ch + i];
-                        pv[i] = x == -INFINITY ? 0.f : tc::ex2(x - mm[i]);
-                        l[8 * ch + i] += pv[i];
+                    for (int c2 = 0; c2 < 8; ++c2) {
+                        const float x = s[8 * ch + c2];
+                        pv[c2] = x == -INFINITY ? 0.f : tc::ex2(x - mm[c2]);
+                        l[8 * ch + c2] += pv[c2];
                     }
                     uint4 packed;
                     packed.x = tc::pack_bf16x2(pv[0], pv[1]);
@@ -547,23 +740,23 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
                 if (j == 0)
                     tc::mbar_arrive(bar(kBarPFull));
-                if (tid == 0)
-                    KPROF(a, 703 + 4 * t);
+                if (tid == 0 && gseq < 64)
+                    KPROF(a, 600 + gseq);
             }
-            if (ok && ntiles > 0) {
-                ok = tc::mbar_wait(bar(kBarPvDone), (ntiles - 1) & 1);
+            // The unit's last P.V, then O / l for this warpgroup's rows.
+            if (ok) {
+                ok = tc::mbar_wait(bar(kBarPvDone), (gseq - 1) & 1);
                 tc::fence_after_sync();
             }
             if (!ok)
                 *err = 1;
             const bool failed = tc::named_sync_or(nb_id, 128, !ok || *err != 0);
-            // Column sums over the warpgroup, then O / l for this warpgroup's rows.
 #pragma unroll
             for (int g = 0; g < NPH; g += 32) {
                 float tmp[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    tmp[i] = (g + i < NPH) ? l[g + i] : 0.f;
+                for (int c2 = 0; c2 < 32; ++c2)
+                    tmp[c2] = (g + c2 < NPH) ? l[g + c2] : 0.f;
                 redw[wt * 64 + g + lane] = reduce_scatter32<false>(tmp, lane);
             }
             tc::named_sync(nb_id, 128);
@@ -576,37 +769,55 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     float o[16];
                     tc::tmem_ld16(tmem_o + g, o);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int cc = g + i;
+                    for (int c2 = 0; c2 < 16; ++c2) {
+                        const int cc = g + c2;
                         if (cc < rows_w) {
                             const int r = w * NPH + cc;
-                            const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
-                            a.o_part[prw * kD + j] = o[i] * linv[cc];
+                            const size_t prw = (size_t)(ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
+                            a.o_part[prw * kD + j] = o[c2] * linv[cc];
                         }
                     }
                 }
                 if (j < rows_w) {
                     const int r = w * NPH + j;
-                    const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
+                    const size_t prw = (size_t)(ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
                     a.lse_part[prw] = m_s[j] - log2f(linv[j]);
                 }
             }
+            // O buffer ob and the statistics are free for the unit two on.
+            tc::fence_before_sync();
+            tc::named_sync(nb_id, 128);
+            if (j == 0)
+                tc::mbar_arrive(bar(kBarOFree + ob));
+            if (tid == 0 && i < 8)
+                KPROF(a, 700 + i);
+            if (tid == 0 && u0 + i + 1 == u1 && blockIdx.x < 1024)
+                KPROF_ANY(a, 1024 + blockIdx.x);
+            if (failed)
+                break;
         }
     }
     tc::fence_before_sync();
     __syncthreads();
     if (*err && tid < 128) {
-        for (int r = 0; r < R; ++r) {
-            const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
-            a.o_part[prw * kD + tid] = __int_as_float(0x7fc00000);
-            if (tid == 0)
-                a.lse_part[prw] = __int_as_float(0x7fc00000);
+        // Mark every partial of the CTA's units as failed.
+        for (int u = u0; u < u1; ++u) {
+            const int item = u / Hkv, h = u - item * Hkv;
+            const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
+            const int cq0 = p.chunk_q_off[c] + qb;
+            for (int r = 0; r < (qe - qb) * G; ++r) {
+                const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
+                a.o_part[prw * kD + tid] = __int_as_float(0x7fc00000);
+                if (tid == 0)
+                    a.lse_part[prw] = __int_as_float(0x7fc00000);
+            }
         }
     }
     if (warp == 9)
         tc::tmem_dealloc(tmem, kTmemCols);
+    // This grid completes only after the launch before it has.
     if (tid == 0)
-        KPROF(a, 1000);
+        grid_dep_wait();
 }
 
 // ---- host: tensor maps over the paged KV, viewed as [pages*Hkv*16][128] ----
@@ -656,7 +867,7 @@ bool kv_map(const void *ptr, uint64_t rows, MapCache &cache, CUtensorMap *out)
 }
 
 template <int NPH>
-int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
+int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost, int32_t n,
                 const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st)
 {
     static bool configured = false;
@@ -667,20 +878,26 @@ int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, 
             return (int)e;
         configured = true;
     }
-    const unsigned blocks = (unsigned)((int64_t)n * a.num_kv_heads);
-    phase1_mma_kernel<NPH><<<blocks, kThreadsMma, Smem::alloc, st>>>(a, p, items, mk, mv);
-    return (int)cudaGetLastError();
+    const int64_t units = (int64_t)n * a.num_kv_heads;
+    const int64_t cap = num_sms() < kMaxGrid ? num_sms() : kMaxGrid;
+    const int grid = (int)(units < cap ? units : cap);
+    CtaRanges r;
+    cta_ranges(cost, n, a.num_kv_heads, grid, r);
+    return (int)launch_dependent(phase1_mma_kernel<NPH>, dim3(grid), dim3(kThreadsMma), Smem::alloc, st, a, p,
+                                 items, r, mk, mv);
 }
 
 }  // namespace
 
 bool mma_supported(int32_t head_dim) { return head_dim == kD; }
 
-int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, int32_t n,
-                      int bucket, void *stream)
+int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
+                      int32_t n, int bucket, void *stream)
 {
     if (n <= 0)
         return 0;
+    if ((int64_t)n * a.num_kv_heads > INT32_MAX)
+        return (int)cudaErrorInvalidValue;
     static MapCache ck, cv;
     CUtensorMap mk, mv;
     const uint64_t rows = (uint64_t)a.num_pages * a.num_kv_heads * kPageSize;
@@ -688,10 +905,10 @@ int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *i
         return (int)cudaErrorInvalidValue;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (bucket) {
-    case 0: return launch_cols<16>(a, p, items, n, mk, mv, st);
-    case 1: return launch_cols<32>(a, p, items, n, mk, mv, st);
-    case 2: return launch_cols<48>(a, p, items, n, mk, mv, st);
-    default: return launch_cols<64>(a, p, items, n, mk, mv, st);
+    case 0: return launch_cols<16>(a, p, items, cost, n, mk, mv, st);
+    case 1: return launch_cols<32>(a, p, items, cost, n, mk, mv, st);
+    case 2: return launch_cols<48>(a, p, items, cost, n, mk, mv, st);
+    default: return launch_cols<64>(a, p, items, cost, n, mk, mv, st);
     }
 }
 

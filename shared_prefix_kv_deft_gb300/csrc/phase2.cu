@@ -12,8 +12,11 @@
 // One warp per (query, head); lane i owns head_dim/32 consecutive elements,
 // so each slot's partial is read with one coalesced 128-bit (or 64-bit) load
 // per lane; the slot ids and weights are loaded one slot per lane and
-// broadcast by shuffles.  The partials were written moments earlier by
-// phase 1 and are mostly still in L2.
+// broadcast by shuffles.  The kernel is a programmatic dependent of the last
+// phase-1 launch: it reads its slot lists while phase 1 finishes, waits for
+// the grid dependency, then issues the partials' loads of up to 16 slots
+// before the first arithmetic.  The partials were written moments earlier
+// and are mostly still in L2.
 #include "common.cuh"
 #include "deft_internal.h"
 
@@ -27,22 +30,52 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
     int32_t num_q_heads, void *__restrict__ out, int32_t out_dtype, float *__restrict__ lse_out)
 {
     constexpr int E = D / 32;  // elements per lane
+    constexpr int KP = 16;     // slots whose partial rows are loaded before any arithmetic
+    if (threadIdx.x == 0)
+        grid_dep_launch();
     const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (warp >= num_queries * num_q_heads)
         return;
     const int q = warp / num_q_heads;
     const int h = warp - q * num_q_heads;
-    const int s0 = q_slot_off[q], s1 = q_slot_off[q + 1];
+    // Slot rows come from the plan, so they are read before the partials are
+    // ready (lane j: the query's slot j, for the first 32).
+    const int s0 = q_slot_off[q], n = q_slot_off[q + 1] - s0;
+    size_t row = 0;
+    if (lane < n)
+        row = (size_t)q_slot[s0 + lane] * num_q_heads + h;
+    grid_dep_wait();   // the phase-1 launches have completed
 
-    // Slots are taken 32 at a time: lane j loads slot j's row and lse, so the
-    // dependent loads (slot list -> lse) happen once per batch, not per slot;
-    // the batch's partial rows are then independent loads.
-    float M = -INFINITY;
-    for (int b = s0; b < s1; b += 32) {
+    // Every load of the first KP slots goes out before the first use.
+    const float l = lane < n ? lse_part[row] : -INFINITY;
+    float ov[KP][E];
+#pragma unroll
+    for (int j = 0; j < KP; ++j) {
+        const size_t rj = __shfl_sync(0xffffffffu, row, j);
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            ov[j][e] = 0.f;
+        if (j < n) {
+            const float *src = o_part + rj * D + lane * E;
+            if constexpr (E == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                ov[j][0] = v.x;
+                ov[j][1] = v.y;
+                ov[j][2] = v.z;
+                ov[j][3] = v.w;
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                ov[j][0] = v.x;
+                ov[j][1] = v.y;
+            }
+        }
+    }
+    float M = l;
+    for (int b = 32; b < n; b += 32) {
         const int i = b + lane;
-        if (i < s1)
-            M = fmaxf(M, lse_part[(size_t)q_slot[i] * num_q_heads + h]);
+        if (i < n)
+            M = fmaxf(M, lse_part[(size_t)q_slot[s0 + i] * num_q_heads + h]);
     }
     M = warp_max(M);
 
@@ -52,33 +85,44 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
         acc[e] = 0.f;
     float wsum = 0.f;
     if (M != -INFINITY) {
-        for (int b = s0; b < s1; b += 32) {
+        auto add_row = [&](size_t rj, float wj) {
+            const float *src = o_part + rj * D + lane * E;
+            if constexpr (E == 4) {
+                const float4 v = *reinterpret_cast<const float4 *>(src);
+                acc[0] = fmaf(wj, v.x, acc[0]);
+                acc[1] = fmaf(wj, v.y, acc[1]);
+                acc[2] = fmaf(wj, v.z, acc[2]);
+                acc[3] = fmaf(wj, v.w, acc[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2 *>(src);
+                acc[0] = fmaf(wj, v.x, acc[0]);
+                acc[1] = fmaf(wj, v.y, acc[1]);
+            }
+        };
+        const float w = lane < n ? exp2f(l - M) : 0.f;   // weights of the first 32 slots
+        wsum = w;
+#pragma unroll
+        for (int j = 0; j < KP; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                acc[e] = fmaf(wj, ov[j][e], acc[e]);
+        }
+        const int n32 = n < 32 ? n : 32;
+        for (int j = KP; j < n32; ++j)
+            add_row(__shfl_sync(0xffffffffu, row, j), __shfl_sync(0xffffffffu, w, j));
+        for (int b = 32; b < n; b += 32) {
             const int i = b + lane;
-            size_t myrow = 0;
-            float myw = 0.f;
-            if (i < s1) {
-                myrow = (size_t)q_slot[i] * num_q_heads + h;
-                myw = exp2f(lse_part[myrow] - M);
+            size_t rb = 0;
+            float wb = 0.f;
+            if (i < n) {
+                rb = (size_t)q_slot[s0 + i] * num_q_heads + h;
+                wb = exp2f(lse_part[rb] - M);
             }
-            wsum += myw;
-            const int nb = min(32, s1 - b);
-#pragma unroll 4
-            for (int j = 0; j < nb; ++j) {
-                const size_t row = __shfl_sync(0xffffffffu, myrow, j);
-                const float w = __shfl_sync(0xffffffffu, myw, j);
-                const float *src = o_part + row * D + lane * E;
-                if constexpr (E == 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(src);
-                    acc[0] = fmaf(w, v.x, acc[0]);
-                    acc[1] = fmaf(w, v.y, acc[1]);
-                    acc[2] = fmaf(w, v.z, acc[2]);
-                    acc[3] = fmaf(w, v.w, acc[3]);
-                } else {
-                    const float2 v = *reinterpret_cast<const float2 *>(src);
-                    acc[0] = fmaf(w, v.x, acc[0]);
-                    acc[1] = fmaf(w, v.y, acc[1]);
-                }
-            }
+            wsum += wb;
+            const int nb = n - b < 32 ? n - b : 32;
+            for (int j = 0; j < nb; ++j)
+                add_row(__shfl_sync(0xffffffffu, rb, j), __shfl_sync(0xffffffffu, wb, j));
         }
         wsum = warp_sum(wsum);
     }
@@ -112,15 +156,14 @@ int launch_phase2(const AttnArgs &a, const DevPartition &p, void *out, int32_t o
     const int threads = 256;
     const unsigned blocks = (unsigned)((warps * 32 + threads - 1) / threads);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const float *op = a.o_part, *lp = a.lse_part;
+    const int32_t *so = p.q_slot_off, *sl = p.q_slot;
+    const int32_t nq = p.num_queries, hq = a.num_q_heads;
     if (a.head_dim == 128)
-        phase2_merge_kernel<128><<<blocks, threads, 0, st>>>(
-            a.o_part, a.lse_part, p.q_slot_off, p.q_slot, p.num_queries, a.num_q_heads, out,
-            out_dtype, lse);
-    else
-        phase2_merge_kernel<64><<<blocks, threads, 0, st>>>(
-            a.o_part, a.lse_part, p.q_slot_off, p.q_slot, p.num_queries, a.num_q_heads, out,
-            out_dtype, lse);
-    return (int)cudaGetLastError();
+        return (int)launch_dependent(phase2_merge_kernel<128>, dim3(blocks), dim3(threads), 0, st, op, lp, so, sl,
+                                     nq, hq, out, out_dtype, lse);
+    return (int)launch_dependent(phase2_merge_kernel<64>, dim3(blocks), dim3(threads), 0, st, op, lp, so, sl, nq,
+                                 hq, out, out_dtype, lse);
 }
 
 }  // namespace deft

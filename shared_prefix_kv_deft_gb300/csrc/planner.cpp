@@ -186,12 +186,35 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     };
     cost_prefix(fma, p.fma_cost);
     cost_prefix(fb, p.fallback_cost);
+    cost_prefix(mma, p.mma_cost);
     bucket_offsets(fma, p.fma_bucket_off);
     bucket_offsets(fb, p.fallback_bucket_off);
     bucket_offsets(mma, p.mma_bucket_off);
 }
 
 }  // namespace
+
+void cta_ranges(const int64_t *cost, int32_t n, int32_t hkv, int grid, CtaRanges &r)
+{
+    const int64_t c0 = cost[0];
+    const int64_t total = (int64_t)hkv * (cost[n] - c0);
+    int32_t i = 0;
+    r.begin[0] = 0;
+    for (int b = 1; b < grid; ++b) {
+        const int64_t target = total * b / grid;
+        while (i < n && (int64_t)hkv * (cost[i + 1] - c0) <= target)
+            ++i;
+        if (i == n) {
+            r.begin[b] = n * hkv;
+            continue;
+        }
+        // Item i holds the target: its first head whose start is at or past it.
+        const int64_t rem = target - (int64_t)hkv * (cost[i] - c0);
+        const int64_t ci = cost[i + 1] - cost[i];
+        r.begin[b] = (int32_t)((int64_t)i * hkv + (rem + ci - 1) / ci);
+    }
+    r.begin[grid] = n * hkv;
+}
 
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                const int32_t *query_node, int32_t num_queries, int32_t chunk_target,

@@ -58,69 +58,28 @@ int copy_out(const void *src, size_t n, void *dst, size_t bytes)
 
 // Layout of one partition inside the device blob.
 struct Layout {
-    size_t off[16];
+    size_t off[deft::kPartArrays];
+    size_t end;
 };
 
 void plan_partition_layout(const deft::Partition &p, size_t &cursor, Layout &L)
 {
-    const size_t sizes[16] = {vbytes(p.chunk_seg_off), vbytes(p.chunk_q_off), vbytes(p.chunk_tokens),
-                              vbytes(p.chunk_q),       vbytes(p.seg_node),    vbytes(p.seg_tok_begin),
-                              vbytes(p.seg_tok_len),   vbytes(p.seg_chunk_pos), vbytes(p.seg_mask),
-                              vbytes(p.q_slot_off),    vbytes(p.q_slot),      vbytes(p.fma_items),
-                              vbytes(p.mma_items),     vbytes(p.fallback_items), vbytes(p.seg_lmask_off),
-                              vbytes(p.seg_lmask)};
-    for (int i = 0; i < 16; ++i) {
+    const auto arrays = deft::partition_arrays(p);
+    for (int i = 0; i < deft::kPartArrays; ++i) {
         L.off[i] = cursor;
-        cursor = align_up(cursor + (sizes[i] ? sizes[i] : 4));
+        cursor = align_up(cursor + (arrays[i].bytes ? arrays[i].bytes : 4));
     }
+    L.end = cursor;
 }
 
-void fill_partition(const deft::Partition &p, const Layout &L, uint8_t *host,
-                    uint8_t *dev, int32_t num_queries, int32_t mask_words, deft::DevPartition &d)
+void fill_partition(const deft::Partition &p, const Layout &L, uint8_t *host, uint8_t *dev, int32_t num_nodes,
+                    int32_t num_queries, int32_t mask_words, deft::DevPartition &d)
 {
-    auto put = [&](int i, const void *src, size_t n) {
-        if (n)
-            std::memcpy(host + L.off[i], src, n);
-    };
-    put(0, p.chunk_seg_off.data(), vbytes(p.chunk_seg_off));
-    put(1, p.chunk_q_off.data(), vbytes(p.chunk_q_off));
-    put(2, p.chunk_tokens.data(), vbytes(p.chunk_tokens));
-    put(3, p.chunk_q.data(), vbytes(p.chunk_q));
-    put(4, p.seg_node.data(), vbytes(p.seg_node));
-    put(5, p.seg_tok_begin.data(), vbytes(p.seg_tok_begin));
-    put(6, p.seg_tok_len.data(), vbytes(p.seg_tok_len));
-    put(7, p.seg_chunk_pos.data(), vbytes(p.seg_chunk_pos));
-    put(8, p.seg_mask.data(), vbytes(p.seg_mask));
-    put(9, p.q_slot_off.data(), vbytes(p.q_slot_off));
-    put(10, p.q_slot.data(), vbytes(p.q_slot));
-    put(11, p.fma_items.data(), vbytes(p.fma_items));
-    put(12, p.mma_items.data(), vbytes(p.mma_items));
-    put(13, p.fallback_items.data(), vbytes(p.fallback_items));
-    put(14, p.seg_lmask_off.data(), vbytes(p.seg_lmask_off));
-    put(15, p.seg_lmask.data(), vbytes(p.seg_lmask));
-    auto i32 = [&](int i) { return reinterpret_cast<const int32_t *>(dev + L.off[i]); };
-    d.chunk_seg_off = i32(0);
-    d.chunk_q_off = i32(1);
-    d.chunk_tokens = i32(2);
-    d.chunk_q = i32(3);
-    d.seg_node = i32(4);
-    d.seg_tok_begin = i32(5);
-    d.seg_tok_len = i32(6);
-    d.seg_chunk_pos = i32(7);
-    d.seg_mask = reinterpret_cast<const uint64_t *>(dev + L.off[8]);
-    d.q_slot_off = i32(9);
-    d.q_slot = i32(10);
-    d.fma_items = i32(11);
-    d.mma_items = i32(12);
-    d.fallback_items = i32(13);
-    d.seg_lmask_off = i32(14);
-    d.seg_lmask = reinterpret_cast<const uint32_t *>(dev + L.off[15]);
-    d.num_fma_items = (int32_t)(p.fma_items.size() / 3);
-    d.num_mma_items = (int32_t)(p.mma_items.size() / 3);
-    d.num_fallback_items = (int32_t)(p.fallback_items.size() / 3);
-    d.num_slots = p.num_slots();
-    d.num_queries = num_queries;
-    d.mask_words = mask_words;
+    const auto arrays = deft::partition_arrays(p);
+    for (int i = 0; i < deft::kPartArrays; ++i)
+        if (arrays[i].bytes)
+            std::memcpy(host + L.off[i], arrays[i].ptr, arrays[i].bytes);
+    deft::bind_partition(p, dev, L.off, L.end, num_nodes, num_queries, mask_words, d);
 }
 
 size_t partial_bytes(int64_t slots, int32_t num_q_heads, int32_t head_dim)
@@ -236,58 +195,11 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
     // of a larger GQA group needs the tensor-core path.
     if (plan->gqa_group > deft::kFmaMaxRows && !use_mma)
         return DEFT_EUNSUPPORTED;
-    int rc = 0;
-    const int32_t fam = naive ? 1 : 0;
-    // CUDA-core launches, one per row bucket.
-    auto fma_launches = [&](const int32_t *items, const std::vector<int64_t> &cost,
-                            const std::array<int32_t, 6> &off, int fb) {
-        for (int b = 0; b < 5; ++b) {
-            const int32_t n = off[b + 1] - off[b];
-            if (n <= 0)
-                continue;
-            const int32_t *it = items + 3 * (size_t)off[b];
-            const int r = traced({DEFT_K_PHASE1_FMA, fam, b, fb, n, 0.f}, stream, [&] {
-                const int r = deft::launch_phase1_fma(a, dp, it, cost.data() + off[b], n, b, stream);
-                if (r == 0)
-                    a.wait_prior = 0;
-                return r;
-            });
-            if (r)
-                return r;
-        }
-        return 0;
+    const deft::LaunchTracer trace = [](const deft_trace_record &rec, void *st, const std::function<int()> &launch) {
+        return traced(rec, st, launch);
     };
-    if (dp.num_mma_items > 0) {
-        // The tensor-core path covers head_dim 128; other head sizes, or a run
-        // with DEFT_DISABLE_MMA set, take the same chunks on CUDA cores in
-        // items of at most 16 rows.
-        if (use_mma) {
-            for (int b = 0; b < 4 && !rc; ++b) {
-                const int32_t n = hp.mma_bucket_off[b + 1] - hp.mma_bucket_off[b];
-                if (n <= 0)
-                    continue;
-                const int32_t *it = dp.mma_items + 3 * (size_t)hp.mma_bucket_off[b];
-                rc = traced({DEFT_K_PHASE1_MMA, fam, b, 0, n, 0.f}, stream, [&] {
-                    const int r = deft::launch_phase1_mma(a, dp, it, hp.mma_cost.data() + hp.mma_bucket_off[b],
-                                                          n, b, stream);
-                    if (r == 0)
-                        a.wait_prior = 0;
-                    return r;
-                });
-            }
-        } else
-            rc = fma_launches(dp.fallback_items, hp.fallback_cost, hp.fallback_bucket_off, 1);
-        if (rc)
-            return DEFT_ECUDA;
-    }
-    if (dp.num_fma_items > 0) {
-        rc = fma_launches(dp.fma_items, hp.fma_cost, hp.fma_bucket_off, 0);
-        if (rc)
-            return DEFT_ECUDA;
-    }
-    rc = traced({DEFT_K_PHASE2, fam, 0, 0, dp.num_queries, 0.f}, stream,
-                [&] { return deft::launch_phase2(a, dp, out, out_dtype, lse, stream); });
-    return rc ? DEFT_ECUDA : DEFT_OK;
+    return deft::dispatch_step(a, dp, hp, use_mma, naive ? 1 : 0, out, out_dtype, lse, stream, trace) ? DEFT_ECUDA
+                                                                                                       : DEFT_OK;
 }
 
 }  // namespace
@@ -391,10 +303,10 @@ int deft_plan_upload(deft_plan_t *plan, void *stream)
     }
     std::vector<uint8_t> host(cursor, 0);
     uint8_t *dev_base = reinterpret_cast<uint8_t *>(plan->dev_blob);
-    fill_partition(plan->tree, lt, host.data(), dev_base, plan->num_queries, plan->mask_words,
+    fill_partition(plan->tree, lt, host.data(), dev_base, plan->num_nodes, plan->num_queries, plan->mask_words,
                    plan->dev_tree);
-    fill_partition(plan->naive, ln, host.data(), dev_base, plan->num_queries, plan->mask_words,
-                   plan->dev_naive);
+    fill_partition(plan->naive, ln, host.data(), dev_base, plan->num_nodes, plan->num_queries,
+                   plan->mask_words, plan->dev_naive);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // Pageable source: the runtime has staged it by the time the call
     // returns, so the local buffer may be released afterwards.

@@ -54,6 +54,21 @@ __device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
 
+// Prefetch into L2 this CTA's share (part `part` of `parts`) of the 128-byte
+// lines that lie wholly inside [p, p + bytes), spread over `nthr` threads.
+__device__ __forceinline__ void prefetch_l2_share(const void *p, size_t bytes, int part, int parts, int tid,
+                                                  int nthr)
+{
+    const uintptr_t a0 = (reinterpret_cast<uintptr_t>(p) + 127) & ~(uintptr_t)127;
+    const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + bytes;
+    if (a1 < a0 + 128)
+        return;
+    const size_t lines = (a1 - a0) / 128;
+    const size_t l0 = lines * part / parts, l1 = lines * (part + 1) / parts;
+    for (size_t l = l0 + tid; l < l1; l += nthr)
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a0 + l * 128));
+}
+
 // Programmatic dependent launch: wait until the grids this one depends on
 // have completed and their writes are visible / let the next grid launch.
 __device__ __forceinline__ void grid_dep_wait()

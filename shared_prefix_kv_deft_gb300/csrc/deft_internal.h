@@ -14,6 +14,7 @@
 #include <array>
 #include <cstddef>
 #include <cstdint>
+#include <functional>
 #include <vector>
 
 #include "deft.h"
@@ -62,6 +63,15 @@ struct Partition {
     std::vector<int64_t> fma_cost;
     std::vector<int64_t> fallback_cost;
     std::vector<int64_t> mma_cost;        // the same over mma_items
+    // Row masks of each item over its chunk's segments, so kernels need not
+    // expand the segments' query masks: for item i, entries
+    // [*_rmask_off[i], *_rmask_off[i + 1]) are its chunk's segments in order.
+    // CUDA-core items: bit r = item row r.  Tensor-core items: four words
+    // per segment, the first warpgroup's columns (rows 0 .. NPH-1) in bits
+    // 0-63, the second's (rows NPH ..) in bits 64-127, NPH =
+    // mma_half_cols(rows).
+    std::vector<uint32_t> fma_rmask, fallback_rmask, mma_rmask;
+    std::vector<int32_t> fma_rmask_off, fallback_rmask_off, mma_rmask_off;   // [n+1]
     // mma_items are sorted by column bucket b: each of the two softmax
     // warpgroups of an item holds NPH = 16 (b + 1) query rows; bucket b is
     // items [off[b], off[b+1]).
@@ -90,13 +100,81 @@ struct DevPartition {
     const int32_t *fma_items;
     const int32_t *mma_items;
     const int32_t *fallback_items;
+    const uint32_t *fma_rmask;
+    const int32_t *fma_rmask_off;
+    const uint32_t *fallback_rmask;
+    const int32_t *fallback_rmask_off;
+    const uint32_t *mma_rmask;          // uint4 per (item, segment)
+    const int32_t *mma_rmask_off;       // in uint4 units
     int32_t num_fma_items;
     int32_t num_mma_items;
     int32_t num_fallback_items;
     int32_t num_slots;
     int32_t num_queries;
     int32_t mask_words;
+    int32_t num_nodes;
+    // All of the partition's arrays lie in [arrays, arrays + array_bytes)
+    // (kernels prefetch them into L2 at start-up).
+    const uint8_t *arrays;
+    uint32_t array_bytes;
 };
+
+// The partition's device arrays in blob order, and how a blob placed at
+// `base` with offsets `off` binds to a DevPartition (shared by the uploaded
+// plan and the allocation-free entry point).
+constexpr int kPartArrays = 22;
+struct ArrayRef {
+    const void *ptr;
+    size_t bytes;
+};
+template <typename T>
+inline ArrayRef aref(const std::vector<T> &v) { return ArrayRef{v.data(), v.size() * sizeof(T)}; }
+inline std::array<ArrayRef, kPartArrays> partition_arrays(const Partition &p)
+{
+    return {{aref(p.chunk_seg_off), aref(p.chunk_q_off), aref(p.chunk_tokens), aref(p.chunk_q),
+             aref(p.seg_node), aref(p.seg_tok_begin), aref(p.seg_tok_len), aref(p.seg_chunk_pos),
+             aref(p.seg_mask), aref(p.q_slot_off), aref(p.q_slot), aref(p.fma_items), aref(p.mma_items),
+             aref(p.fallback_items), aref(p.seg_lmask_off), aref(p.seg_lmask), aref(p.fma_rmask),
+             aref(p.fma_rmask_off), aref(p.fallback_rmask), aref(p.fallback_rmask_off), aref(p.mma_rmask),
+             aref(p.mma_rmask_off)}};
+}
+inline void bind_partition(const Partition &p, const uint8_t *base, const size_t *off, size_t end,
+                           int32_t num_nodes, int32_t num_queries, int32_t mask_words, DevPartition &d)
+{
+    auto i32 = [&](int i) { return reinterpret_cast<const int32_t *>(base + off[i]); };
+    auto u32 = [&](int i) { return reinterpret_cast<const uint32_t *>(base + off[i]); };
+    d.chunk_seg_off = i32(0);
+    d.chunk_q_off = i32(1);
+    d.chunk_tokens = i32(2);
+    d.chunk_q = i32(3);
+    d.seg_node = i32(4);
+    d.seg_tok_begin = i32(5);
+    d.seg_tok_len = i32(6);
+    d.seg_chunk_pos = i32(7);
+    d.seg_mask = reinterpret_cast<const uint64_t *>(base + off[8]);
+    d.q_slot_off = i32(9);
+    d.q_slot = i32(10);
+    d.fma_items = i32(11);
+    d.mma_items = i32(12);
+    d.fallback_items = i32(13);
+    d.seg_lmask_off = i32(14);
+    d.seg_lmask = u32(15);
+    d.fma_rmask = u32(16);
+    d.fma_rmask_off = i32(17);
+    d.fallback_rmask = u32(18);
+    d.fallback_rmask_off = i32(19);
+    d.mma_rmask = u32(20);
+    d.mma_rmask_off = i32(21);
+    d.num_fma_items = (int32_t)(p.fma_items.size() / 3);
+    d.num_mma_items = (int32_t)(p.mma_items.size() / 3);
+    d.num_fallback_items = (int32_t)(p.fallback_items.size() / 3);
+    d.num_slots = p.num_slots();
+    d.num_queries = num_queries;
+    d.mask_words = mask_words;
+    d.num_nodes = num_nodes;
+    d.arrays = base + off[0];
+    d.array_bytes = (uint32_t)(end - off[0]);
+}
 
 }  // namespace deft
 
@@ -155,9 +233,12 @@ struct AttnArgs {
 // Launchers (return a cudaError_t cast to int; 0 = success).
 // One CUDA-core launch over `n` items (device triples at `items`), all of row
 // bucket `bucket` (rows <= 2^bucket).
-// `cost` points at the items' host cost prefix (n + 1 entries).
-int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
-                      int32_t n, int bucket, void *stream);
+// `rmask` / `rmask_off`: the items' row masks (device; rmask_off indexed
+// like items), `cost`: their host cost prefix (n + 1 entries), `max_ctas`:
+// the most CTAs the launch may use.
+int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
+                      const int32_t *rmask_off, const int64_t *cost, int32_t n, int bucket, int max_ctas,
+                      void *stream);
 
 // Persistent phase-1 launches split their units (item-major: unit = item *
 // num_kv_heads + head) into contiguous per-CTA ranges of about equal cost:
@@ -173,9 +254,17 @@ void cta_ranges(const int64_t *cost, int32_t n, int32_t hkv, int grid, CtaRanges
 // Streaming multiprocessors of the current device.
 int num_sms();
 // One tensor-core launch over `n` items of column bucket `bucket`.
-int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
-                      int32_t n,
-                      int bucket, void *stream);
+int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
+                      const int32_t *rmask_off, const int64_t *cost, int32_t n, int bucket, int max_ctas,
+                      void *stream);
+// Runs `launch` (returns a cudaError_t as int) on `stream`, recording it
+// under `rec` when tracing is on.
+using LaunchTracer = std::function<int(const deft_trace_record &rec, void *stream, const std::function<int()> &launch)>;
+// Enqueues one step on `stream`: the phase-1 launches of partition dp (the
+// two families concurrently when both are present) and the merge into
+// out / lse.  `hp` is dp's host copy.  Returns a cudaError_t as int.
+int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool use_mma, int32_t family,
+                  void *out, int32_t out_dtype, float *lse, void *stream, const LaunchTracer &trace);
 // Row bucket of an item with `rows` rows: smallest b with rows <= 2^b.
 inline int row_bucket(int rows) { return rows <= 1 ? 0 : rows <= 2 ? 1 : rows <= 4 ? 2 : rows <= 8 ? 3 : 4; }
 // Rows per softmax warpgroup of a tensor-core item with `rows` rows (two

@@ -61,8 +61,6 @@ int scratch_address(int dev, unsigned char **out)
     return DEFT_OK;
 }
 
-template <typename T>
-size_t vbytes(const std::vector<T> &v) { return v.size() * sizeof(T); }
 
 }  // namespace
 
@@ -94,23 +92,12 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
 
     // Scratch layout: the tree partition's arrays, then the partials.
     const deft::Partition &p = plan->tree;
-    const void *src[16] = {p.chunk_seg_off.data(), p.chunk_q_off.data(), p.chunk_tokens.data(),
-                           p.chunk_q.data(),       p.seg_node.data(),    p.seg_tok_begin.data(),
-                           p.seg_tok_len.data(),   p.seg_chunk_pos.data(), p.seg_mask.data(),
-                           p.q_slot_off.data(),    p.q_slot.data(),      p.fma_items.data(),
-                           p.mma_items.data(),     p.fallback_items.data(), p.seg_lmask_off.data(),
-                           p.seg_lmask.data()};
-    const size_t len[16] = {vbytes(p.chunk_seg_off), vbytes(p.chunk_q_off), vbytes(p.chunk_tokens),
-                            vbytes(p.chunk_q),       vbytes(p.seg_node),    vbytes(p.seg_tok_begin),
-                            vbytes(p.seg_tok_len),   vbytes(p.seg_chunk_pos), vbytes(p.seg_mask),
-                            vbytes(p.q_slot_off),    vbytes(p.q_slot),      vbytes(p.fma_items),
-                            vbytes(p.mma_items),     vbytes(p.fallback_items), vbytes(p.seg_lmask_off),
-                            vbytes(p.seg_lmask)};
-    size_t off[16];
+    const auto arrays = deft::partition_arrays(p);
+    size_t off[deft::kPartArrays];
     size_t cursor = 0;
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < deft::kPartArrays; ++i) {
         off[i] = cursor;
-        cursor = align_up(cursor + (len[i] ? len[i] : 4));
+        cursor = align_up(cursor + (arrays[i].bytes ? arrays[i].bytes : 4));
     }
     const size_t slots = (size_t)p.num_slots();
     const size_t o_off = cursor;
@@ -129,35 +116,14 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
     if (rc != DEFT_OK)
         return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    for (int i = 0; i < 16; ++i)
-        if (len[i] && cudaMemcpyAsync(base + off[i], src[i], len[i], cudaMemcpyHostToDevice, st) !=
-                          cudaSuccess)
+    for (int i = 0; i < deft::kPartArrays; ++i)
+        if (arrays[i].bytes &&
+            cudaMemcpyAsync(base + off[i], arrays[i].ptr, arrays[i].bytes, cudaMemcpyHostToDevice, st) !=
+                cudaSuccess)
             return DEFT_ECUDA;
 
     deft::DevPartition d{};
-    auto i32 = [&](int i) { return reinterpret_cast<const int32_t *>(base + off[i]); };
-    d.chunk_seg_off = i32(0);
-    d.chunk_q_off = i32(1);
-    d.chunk_tokens = i32(2);
-    d.chunk_q = i32(3);
-    d.seg_node = i32(4);
-    d.seg_tok_begin = i32(5);
-    d.seg_tok_len = i32(6);
-    d.seg_chunk_pos = i32(7);
-    d.seg_mask = reinterpret_cast<const uint64_t *>(base + off[8]);
-    d.q_slot_off = i32(9);
-    d.q_slot = i32(10);
-    d.fma_items = i32(11);
-    d.mma_items = i32(12);
-    d.fallback_items = i32(13);
-    d.seg_lmask_off = i32(14);
-    d.seg_lmask = reinterpret_cast<const uint32_t *>(base + off[15]);
-    d.num_fma_items = (int32_t)(p.fma_items.size() / 3);
-    d.num_mma_items = (int32_t)(p.mma_items.size() / 3);
-    d.num_fallback_items = (int32_t)(p.fallback_items.size() / 3);
-    d.num_slots = p.num_slots();
-    d.num_queries = plan->num_queries;
-    d.mask_words = plan->mask_words;
+    deft::bind_partition(p, base, off, cursor, plan->num_nodes, plan->num_queries, plan->mask_words, d);
 
     deft::AttnArgs a{};
     a.q = q;
@@ -175,38 +141,8 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
     a.o_part = reinterpret_cast<float *>(base + o_off);
     a.lse_part = reinterpret_cast<float *>(base + lse_off);
 
-    auto fma_launches = [&](const int32_t *items, const std::vector<int64_t> &cost,
-                            const std::array<int32_t, 6> &boff) {
-        for (int b = 0; b < 5; ++b) {
-            const int32_t n = boff[b + 1] - boff[b];
-            if (n > 0) {
-                const int r = deft::launch_phase1_fma(a, d, items + 3 * (size_t)boff[b], cost.data() + boff[b], n,
-                                                      b, stream);
-                if (r)
-                    return r;
-                a.wait_prior = 0;
-            }
-        }
-        return 0;
+    const deft::LaunchTracer untraced = [](const deft_trace_record &, void *, const std::function<int()> &launch) {
+        return launch();
     };
-    if (d.num_mma_items > 0) {
-        if (use_mma) {
-            for (int b = 0; b < 4 && !rc; ++b) {
-                const int32_t n = p.mma_bucket_off[b + 1] - p.mma_bucket_off[b];
-                if (n > 0)
-                    rc = deft::launch_phase1_mma(a, d, d.mma_items + 3 * (size_t)p.mma_bucket_off[b],
-                                                 p.mma_cost.data() + p.mma_bucket_off[b], n, b,
-                                                 stream);
-                if (n > 0 && rc == 0)
-                    a.wait_prior = 0;
-            }
-        } else {
-            rc = fma_launches(d.fallback_items, p.fallback_cost, p.fallback_bucket_off);
-        }
-        if (rc)
-            return DEFT_ECUDA;
-    }
-    if (d.num_fma_items > 0 && fma_launches(d.fma_items, p.fma_cost, p.fma_bucket_off))
-        return DEFT_ECUDA;
-    return deft::launch_phase2(a, d, out, out_dtype, lse, stream) ? DEFT_ECUDA : DEFT_OK;
+    return deft::dispatch_step(a, d, p, use_mma, 0, out, out_dtype, lse, stream, untraced) ? DEFT_ECUDA : DEFT_OK;
 }

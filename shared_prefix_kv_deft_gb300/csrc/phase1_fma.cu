@@ -12,22 +12,26 @@
 //
 // Persistent CTAs (one per SM) each take a contiguous range of units of
 // about equal cost (units are item-major, so a range holds runs of one
-// item's KV heads, which share their segment table and page list); the
-// tiles of consecutive units form one continuous stream through a ring of
-// 64-token stages, so the loads of the next unit overlap the end of the
-// current one.
+// item's KV heads, which share their segment table and page list).  Each
+// compute group has its own ring of 64-token stages through which the
+// tiles of its units stream continuously, so the loads of its next unit
+// overlap the end of the current one and the groups never wait on each
+// other's tiles.
 //   warp 0            metadata: runs ahead; per item it builds the segment
 //                     table (positions, page bases, row masks) and gathers
 //                     the item's page ids, per unit it stages the q rows
 //                     (cp.async, completion signalled on the unit's
 //                     mbarrier, so the warp never waits on them);
-//   warps 1, 2        copies, alternating tiles: resolve a tile's pages through the page
-//                     list, loads every 16-token slot that is one whole page
+//   warps 1, 2        copies: with two groups, warp 1 + g fills group g's
+//                     ring; with one, the two alternate tiles.  A copy warp
+//                     resolves a tile's pages through the page list (a
+//                     fast path when the tile is four whole pages of one
+//                     segment), loads every 16-token slot that is one whole page
 //                     of one segment as a single contiguous bulk copy (a
 //                     page holds a head's 16 rows back to back) and ragged
 //                     rows (node tails, one-token nodes) with 16-byte
 //                     cp.async at the exact token count;
-//   warps 2..         NG groups of 8 compute warps; group g takes whole units
+//   warps 3..         NG groups of 8 compute warps; group g takes whole units
 //                     g, g+NG, ... of the CTA; a warp owns 8 tokens of a tile:
 //                       q.k  lane = 8 * quarter + token: each lane dots a
 //                            quarter of head_dim for every row, its 16-byte
@@ -56,8 +60,8 @@ template <int D, int RMAX>
 constexpr uint32_t fma_fixed_bytes(int NG)
 {
     return 2 * NG * RMAX * D * 2 + 2 * NG * 32 + NG * RMAX * D * 4 + 8 * NG * 8 * RMAX * 4 +
-           2 * 8 * NG * RMAX * 4 + NG * RMAX * D * 4 + NG * 2 * RMAX * 4 + 2 * kMaxSegsPerChunk * 20 +
-           2 * kPageList * 4 + 2 * 16 + 64 + 256 + 1024;
+           2 * 8 * NG * RMAX * 4 + NG * RMAX * D * 4 + NG * 4 * RMAX * 4 + 2 * kMaxSegsPerChunk * 20 +
+           2 * kPageList * 4 + 2 * 16 + 256 + 1024;
 }
 
 template <int D, int RMAX>
@@ -66,24 +70,25 @@ struct FmaCfg {
     static constexpr int NCW = 8 * NG;                 // compute warps
     static constexpr int THREADS = 32 * (NCW + 3);     // + metadata warp + two copy warps
     // Stages in the ring: as many as fit next to the fixed buffers, at most 6
-    // and even (copy warp w always serves the stages of parity w).
+    // and even: two groups get half each; one group's ring is filled by the two
+    // copy warps alternately (copy warp w always serves the stages of parity w).
     static constexpr uint32_t stage_bytes = 2 * kTile * D * 2 + kTile * 4 + 16;
     static constexpr int ST_FIT = (int)((227u * 1024u - fma_fixed_bytes<D, RMAX>(NG)) / stage_bytes);
     static constexpr int ST = (ST_FIT < 6 ? ST_FIT : 6) & ~1;
     static_assert(ST >= 4, "at least four stages");
+    static constexpr int RST = ST / NG;                // stages per group ring
     static constexpr int UB = 2 * NG;                  // unit slots (q rows, description)
     static constexpr uint32_t op_bytes = kTile * D * 2;           // K (or V) of one stage
     static constexpr uint32_t stage_off = 0;                      // [stage][K,V]
     static constexpr uint32_t meta_off = ST * 2 * op_bytes;       // [stage][64] row masks
-    static constexpr uint32_t tag_off = meta_off + ST * kTile * 4;            // [ST] tile in the stage
-    static constexpr uint32_t qst_off = tag_off + 64;                          // [UB][RMAX][D] bf16
+    static constexpr uint32_t qst_off = meta_off + ST * kTile * 4;            // [UB][RMAX][D] bf16
     static constexpr uint32_t info_off = qst_off + UB * RMAX * D * 2;         // [UB] unit info
     static constexpr uint32_t qs_off = info_off + UB * 32;                     // [NG][RMAX][2][D/8][4] f32
     static constexpr uint32_t ps_off = qs_off + NG * RMAX * D * 4;             // [NCW][8][RMAX]
     static constexpr uint32_t ml_off = ps_off + NCW * 8 * RMAX * 4;            // [NCW][RMAX] m, l
     static constexpr uint32_t oacc_off = ml_off + 2 * NCW * RMAX * 4;         // [NG][RMAX][D] f32
-    static constexpr uint32_t fin_off = oacc_off + NG * RMAX * D * 4;          // [NG][2][RMAX] M, L
-    static constexpr uint32_t seg_off = fin_off + NG * 2 * RMAX * 4;           // [2][5][256]
+    static constexpr uint32_t fin_off = oacc_off + NG * RMAX * D * 4;          // [NG][4][RMAX] M, L, 1/L, row
+    static constexpr uint32_t seg_off = fin_off + NG * 4 * RMAX * 4;           // [2][5][256]
     static constexpr uint32_t pl_off = seg_off + 2 * kMaxSegsPerChunk * 20;    // [2][kPageList]
     static constexpr uint32_t iinfo_off = pl_off + 2 * kPageList * 4;          // [2] ItemInfo
     static constexpr uint32_t bar_off = iinfo_off + 2 * 16;
@@ -114,10 +119,11 @@ struct ItemInfo {
 template <int D, int RMAX>
 __global__ void __launch_bounds__(FmaCfg<D, RMAX>::THREADS, 1)
 phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
+                  const uint32_t *__restrict__ rmask, const int32_t *__restrict__ rmask_off,
                   const __grid_constant__ CtaRanges ranges)
 {
     using C = FmaCfg<D, RMAX>;
-    constexpr int NG = C::NG, NCW = C::NCW, ST = C::ST, UB = C::UB;
+    constexpr int NG = C::NG, NCW = C::NCW, ST = C::ST, RST = C::RST, UB = C::UB;
     constexpr int E = D / 32;       // p.v outputs per lane
     constexpr int QCH = D / 32;     // 16-byte chunks per lane in q.k (a quarter of the row)
     extern __shared__ uint8_t smem_raw[];
@@ -135,18 +141,14 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
     const int u0 = ranges.begin[blockIdx.x], u1 = ranges.begin[blockIdx.x + 1];
     ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + C::iinfo_off);
-    // stag[s]: sequence number of the tile last placed in stage s.  The two
-    // compute groups share the ring, so a group may come to a stage one use
-    // early; it waits for the tag before the stage's mbarrier, whose phase
-    // parity alone cannot tell one use from the one before.
-    volatile int32_t *stag = reinterpret_cast<volatile int32_t *>(smem + C::tag_off);
 
     if (a.wait_prior)
         grid_dep_wait();
     if (tid == 0) {
+        if (blockIdx.x < 256)
+            KPROF_ANY(a, 3300 + blockIdx.x);
         grid_dep_launch();
         for (int s = 0; s < ST; ++s) {
-            stag[s] = -1;
             tc::mbar_init(fbar(bars, kFull + s), 33);
             tc::mbar_init(fbar(bars, kEmpty + s), 8);
         }
@@ -160,6 +162,10 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         }
         tc::fence_mbar_init();
     }
+    // Warm L2 with the plan's arrays, the node page offsets and q.
+    prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid, C::THREADS);
+    prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid, C::THREADS);
+    prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * D * 2, blockIdx.x, gridDim.x, tid, C::THREADS);
     __syncthreads();
 
     if (warp == 0) {
@@ -167,7 +173,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
         constexpr int QJ = (RMAX * (D / 8) + 31) / 32;   // q chunks per lane
         int qrow[QJ];   // per q chunk of this lane: query * Hq + group member, or -1
-        int seq = 0, iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
+        int rseq0 = 0, rseq1 = 0;   // next tile of each group's ring
+        int iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
         for (int u = u0; u < u1; ++u) {
             const int i = u - u0;
             const int item = u / Hkv, h = u - item * Hkv;
@@ -191,6 +198,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kSEmpty + sbuf), ((iseq - 2) >> 1) & 1)))
                     break;
                 int32_t *seg = reinterpret_cast<int32_t *>(smem + C::seg_off) + sbuf * 1280;
+                const uint32_t *item_rm = rmask + rmask_off[item];
                 int32_t *plist = reinterpret_cast<int32_t *>(smem + C::pl_off) + sbuf * kPageList;
                 int npages = 0;   // page-list entries of the segments handled so far
                 for (int s0 = 0; s0 < nseg; s0 += 32) {
@@ -204,13 +212,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         seg[s] = p.seg_chunk_pos[sb + s];
                         seg[256 + s] = pgb;
                         seg[512 + s] = tb;
-                        const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
-                        uint32_t rm = 0;
-                        for (int r = 0; r < R; ++r) {
-                            const int k = qb + r / G;
-                            rm |= ((lm[k >> 5] >> (k & 31)) & 1u) << r;
-                        }
-                        seg[768 + s] = (int32_t)rm;
+                        seg[768 + s] = (int32_t)item_rm[s];
                     }
                     // Exclusive prefix sum of page counts across the warp.
                     int incl = np;
@@ -260,11 +262,14 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             }
             cp_async_mbar_arrive_noinc(fbar(bars, kUFull + ub));
             if (lane == 0) {
-                info[ub] = UnitInfo{R, cq0, h, ntiles, seq, {0, 0, 0}};
+                info[ub] = UnitInfo{R, cq0, h, ntiles, (i % NG) ? rseq1 : rseq0, {0, 0, 0}};
                 tc::mbar_arrive(fbar(bars, kUFull + ub));
                 KPROF(a, 2000 + 8 * i + 0);
             }
-            seq += ntiles;
+            if (i % NG)
+                rseq1 += ntiles;
+            else
+                rseq0 += ntiles;
         }
         cp_async_commit();
         cp_async_wait<0>();
@@ -273,6 +278,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         // Copy warp w (0, 1) loads the tiles of sequence number = w mod 2, so
         // one resolves its tile's pages while the other issues its copies.
         const int cpw = warp - 1;
+        const int ring = NG == 2 ? cpw : 0;
         const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
         const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
         constexpr uint32_t kRowBytes = D * 2;
@@ -301,15 +307,59 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                                  : a.page_id[seg[256 + sg] + tk / kPageSize];
             };
             const int nseg = ii.nseg, T = ii.T, ntiles = (T + kTile - 1) / kTile;
-            for (int t = 0; t < ntiles; ++t, ++seq) {
-                if ((seq & 1) != cpw)
+            const bool mine = NG == 1 || (i % NG) == cpw;   // the unit goes through this warp's ring
+            for (int t = 0; t < (mine ? ntiles : 0); ++t, ++seq) {
+                if (NG == 1 && (seq & 1) != cpw)
                     continue;
-                const int st = seq % ST;
-                // Segment and token of the tile positions lane and lane + 32.
+                const int st = ring * RST + seq % RST;
+                const uint32_t full = fbar(bars, kFull + st);
+                const uint32_t kdst = base + C::stage_off + (uint32_t)(st * 2) * C::op_bytes;
+                const uint32_t vdst = kdst + C::op_bytes;
+                // Segment holding position pos (warp-uniform: broadcast reads).
+                auto seg_at = [&](int pos) {
+                    int lo = 0, hi = nseg - 1;
+                    while (lo < hi) {
+                        const int mid = (lo + hi + 1) >> 1;
+                        if (seg[mid] <= pos)
+                            lo = mid;
+                        else
+                            hi = mid - 1;
+                    }
+                    return lo;
+                };
+                const int p0 = t * kTile, nvalid = min(kTile, T - p0);
+                const int sga = seg_at(p0);
+                const int tka = seg[512 + sga] + p0 - seg[sga];
+                if (nvalid == kTile && (tka % kPageSize) == 0 && seg_at(p0 + kTile - 1) == sga) {
+                    // Fast path: four whole pages of one segment.
+                    const int pg = lane < 4 ? page_of(sga, tka + kPageSize * lane) : -1;
+                    if (seq >= RST &&
+                        !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kEmpty + st), ((seq / RST) - 1) & 1))) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t mrow = (uint32_t)seg[768 + sga];
+                    meta[st * kTile + lane] = mrow;
+                    meta[st * kTile + lane + 32] = mrow;
+                    if (lane == 0)
+                        tc::mbar_arrive_expect_tx(full, 4 * 2 * kPageBytes);
+                    __syncwarp();
+                    if (lane < 4) {
+                        const size_t o = ((size_t)pg * Hkv + h) * kPageSize * D;
+                        const uint32_t rb = (uint32_t)lane * kPageBytes;
+                        tc::bulk_load(kdst + rb, kg + o, kPageBytes, full);
+                        tc::bulk_load(vdst + rb, vg + o, kPageBytes, full);
+                    }
+                    tc::mbar_arrive(full);
+                    if (lane == 0 && seq < 16)
+                        KPROF(a, 2100 + 8 * seq + 1);
+                    continue;
+                }
+                // General path: segment and token of the tile positions lane and lane + 32.
                 int sgk[2], tkk[2];
 #pragma unroll
                 for (int k = 0; k < 2; ++k) {
-                    const int pos = t * kTile + lane + 32 * k;
+                    const int pos = p0 + lane + 32 * k;
                     sgk[k] = -1;
                     tkk[k] = 1;
                     if (pos < T) {
@@ -354,20 +404,14 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     if (sgk[k] >= 0 && !((tp >> ((lane + 32 * k) >> 4)) & 1u))
                         pid[k] = page_of(sgk[k], tkk[k]);
                 }
-                if (lane == 0 && seq < 16)
-                    KPROF(a, 2100 + 8 * seq + 0);
-                if (seq >= ST && !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kEmpty + st), ((seq / ST) - 1) & 1))) {
+                if (seq >= RST &&
+                    !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kEmpty + st), ((seq / RST) - 1) & 1))) {
                     ok = false;
                     break;
                 }
-                if (lane == 0)
-                    stag[st] = seq;
 #pragma unroll
                 for (int k = 0; k < 2; ++k)
                     meta[st * kTile + lane + 32 * k] = sgk[k] >= 0 ? (uint32_t)seg[768 + sgk[k]] : 0u;
-                const uint32_t full = fbar(bars, kFull + st);
-                const uint32_t kdst = base + C::stage_off + (uint32_t)(st * 2) * C::op_bytes;
-                const uint32_t vdst = kdst + C::op_bytes;
                 if (lane == 0)
                     tc::mbar_arrive_expect_tx(full, __popc(tp) * 2 * kPageBytes);
                 __syncwarp();
@@ -388,9 +432,9 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         const int sl = __ffs(nb) - 1;
                         nb &= nb - 1;
                         const int row = sl + 32 * k;
-                        const int pg = __shfl_sync(0xffffffffu, pid[k], sl);
+                        const int pgr = __shfl_sync(0xffffffffu, pid[k], sl);
                         const int tk = __shfl_sync(0xffffffffu, tkk[k], sl);
-                        const long long o = (((long long)pg * Hkv + h) * kPageSize + (tk % kPageSize)) * D;
+                        const long long o = (((long long)pgr * Hkv + h) * kPageSize + (tk % kPageSize)) * D;
                         for (int x = lane; x < 2 * CPR; x += 32) {
                             const int kv = x / CPR, ch = x - kv * CPR;
                             cp_async_16((kv ? vdst : kdst) + row * kRowBytes + ch * 16, (kv ? vg : kg) + o + ch * 8);
@@ -399,7 +443,6 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
                 // Rows past the chunk's end: zero V so that p.v may run over
                 // all 64 rows (their p is 0; stale shared memory could be NaN).
-                const int nvalid = min(kTile, T - t * kTile);
                 if (nvalid < kTile) {
                     uint4 *vz = reinterpret_cast<uint4 *>(smem + (vdst - base) + nvalid * kRowBytes);
                     for (int x = lane; x < (kTile - nvalid) * CPR; x += 32)
@@ -424,9 +467,9 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         cp_async_wait<0>();
         // Do not leave while bulk copies of ours may still be landing: wait for
         // the last use of every stage.
-        for (int s = 0; s < ST && s < seq; ++s) {
-            const int last = seq - 1 - ((seq - 1 - s) % ST);
-            tc::mbar_wait(fbar(bars, kFull + s), (last / ST) & 1);
+        for (int s = 0; s < RST && s < seq; ++s) {
+            const int last = seq - 1 - ((seq - 1 - s) % RST);
+            tc::mbar_wait(fbar(bars, kFull + ring * RST + s), (last / RST) & 1);
         }
     } else {
         // ------------------------------------------------------------ compute
@@ -439,7 +482,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         float *mw = reinterpret_cast<float *>(smem + C::ml_off) + g * 8 * RMAX;
         float *lwb = reinterpret_cast<float *>(smem + C::ml_off) + NCW * RMAX + g * 8 * RMAX;
         float *oacc = reinterpret_cast<float *>(smem + C::oacc_off) + g * RMAX * D;
-        float *fin = reinterpret_cast<float *>(smem + C::fin_off) + g * 2 * RMAX;
+        float *fin = reinterpret_cast<float *>(smem + C::fin_off) + g * 4 * RMAX;   // M, L, 1/L, row
+        int32_t *fin_row = reinterpret_cast<int32_t *>(fin + 3 * RMAX);
         const uint32_t bar_id = 1 + (uint32_t)g, nthr = 256;
         const int gtid = tid - 96 - g * 256;   // thread index within the group
         for (int i = g; u0 + i < u1; i += NG) {
@@ -471,14 +515,9 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             }
             bool tile_ok = true;
             for (int t = 0; t < ui.ntiles; ++t) {
-                const int sq = ui.seq0 + t, st = sq % ST;
-                bool got = false;
-                for (int spin = 0; spin < (1 << 22) && !got; ++spin) {
-                    got = stag[st] == sq;
-                    if (!got)
-                        __nanosleep(64);
-                }
-                got = got && tc::mbar_wait(fbar(bars, kFull + st), (sq / ST) & 1);
+                const int sq = ui.seq0 + t, st = g * RST + sq % RST;
+                // One consumer per ring, in order: the parity names the use.
+                const bool got = tc::mbar_wait(fbar(bars, kFull + st), (sq / RST) & 1);
                 if (!__all_sync(0xffffffffu, got)) {
                     tile_ok = false;
                     break;
@@ -611,6 +650,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         L += lwb[w * RMAX + gtid] * tc::ex2(mw[w * RMAX + gtid] - M);
                 fin[gtid] = M;
                 fin[RMAX + gtid] = L;
+                fin[2 * RMAX + gtid] = L > 0.f ? 1.f / L : 0.f;
+                fin_row[gtid] = (ui.cq0 + gtid / G) * Hq + ui.h * G + (gtid % G);
             }
             tc::named_sync(bar_id, nthr);
 #pragma unroll
@@ -625,11 +666,12 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::named_sync(bar_id, nthr);
             for (int x = gtid; x < R * D; x += nthr) {
                 const int r = x / D, e = x - r * D;
-                const float L = fin[RMAX + r];
-                const size_t prow = (size_t)(ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
-                a.o_part[prow * D + e] = L > 0.f ? oacc[x] / L : 0.f;
-                if (e == 0)
+                const size_t prow = (size_t)fin_row[r];
+                a.o_part[prow * D + e] = oacc[x] * fin[2 * RMAX + r];
+                if (e == 0) {
+                    const float L = fin[RMAX + r];
                     a.lse_part[prow] = L > 0.f ? fin[r] + log2f(L) : -INFINITY;
+                }
             }
             tc::named_sync(bar_id, nthr);
             if (gtid == 0)
@@ -638,6 +680,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 tc::mbar_arrive(fbar(bars, kUEmpty + ub));
         }
     }
+    if (tid == 96 && blockIdx.x < 256)
+        KPROF_ANY(a, 3600 + blockIdx.x);
     // This grid completes only after the launch before it has.
     if (tid == 0)
         grid_dep_wait();
@@ -645,8 +689,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 
 
 template <int D, int RMAX>
-int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost, int32_t n,
-               cudaStream_t st)
+int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
+               const int32_t *rmask_off, const int64_t *cost, int32_t n, int max_ctas, cudaStream_t st)
 {
     using C = FmaCfg<D, RMAX>;
     static bool configured = false;
@@ -658,39 +702,41 @@ int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, c
         configured = true;
     }
     const int64_t units = (int64_t)n * a.num_kv_heads;
-    const int64_t cap = num_sms() < kMaxGrid ? num_sms() : kMaxGrid;
+    const int64_t cap = max_ctas < kMaxGrid ? max_ctas : kMaxGrid;
     const int grid = (int)(units < cap ? units : cap);
     CtaRanges r;
     cta_ranges(cost, n, a.num_kv_heads, grid, r);
     return (int)launch_dependent(phase1_fma_kernel<D, RMAX>, dim3(grid), dim3(C::THREADS), C::alloc, st, a, p,
-                                 items, r);
+                                 items, rmask, rmask_off, r);
 }
 
 template <int D>
-int launch_bucket(int bucket, const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
-                  int32_t n, cudaStream_t st)
+int launch_bucket(int bucket, const AttnArgs &a, const DevPartition &p, const int32_t *items,
+                  const uint32_t *rmask, const int32_t *rmask_off, const int64_t *cost, int32_t n, int max_ctas,
+                  cudaStream_t st)
 {
     switch (bucket) {
-    case 0: return launch_one<D, 1>(a, p, items, cost, n, st);
-    case 1: return launch_one<D, 2>(a, p, items, cost, n, st);
-    case 2: return launch_one<D, 4>(a, p, items, cost, n, st);
-    case 3: return launch_one<D, 8>(a, p, items, cost, n, st);
-    default: return launch_one<D, 16>(a, p, items, cost, n, st);
+    case 0: return launch_one<D, 1>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
+    case 1: return launch_one<D, 2>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
+    case 2: return launch_one<D, 4>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
+    case 3: return launch_one<D, 8>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
+    default: return launch_one<D, 16>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
     }
 }
 
 }  // namespace
 
-int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
-                      int32_t n, int bucket, void *stream)
+int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
+                      const int32_t *rmask_off, const int64_t *cost, int32_t n, int bucket, int max_ctas,
+                      void *stream)
 {
     if (n <= 0)
         return 0;
-    if ((int64_t)n * a.num_kv_heads > INT32_MAX)
+    if ((int64_t)n * a.num_kv_heads > INT32_MAX || max_ctas < 1)
         return (int)cudaErrorInvalidValue;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, cost, n, st)
-                             : launch_bucket<64>(bucket, a, p, items, cost, n, st);
+    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, rmask, rmask_off, cost, n, max_ctas, st)
+                             : launch_bucket<64>(bucket, a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
 }
 
 }  // namespace deft

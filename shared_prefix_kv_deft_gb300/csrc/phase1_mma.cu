@@ -75,40 +75,57 @@ struct ItemInfo {
     int32_t pad[2];
 };
 
+// Shared-memory layout for NPH columns per warpgroup (RP = 2 NPH).  Q^T
+// and P^T are sized by RP, which leaves room for a third V stage when
+// NPH <= 32: a V stage is held through its tile's softmax, K only until S.
+template <int NPH>
 struct Smem {
-    static constexpr uint32_t kv_off = 0;                            // [stage][K,V] operands
-    static constexpr uint32_t q_off = kv_off + 4 * kTileBytes;       // Q^T: [d half][128 rows][128 B]
-    static constexpr uint32_t p_off = q_off + kTileBytes;            // P^T: [col block][128 tok][128 B]
-    static constexpr uint32_t meta_off = p_off + kTileBytes;         // [4 slots][128] uint4 row masks
+    static constexpr int RP = 2 * NPH;
+    static constexpr int VST = NPH <= 32 ? 3 : 2;                    // V stages (K has 2)
+    static constexpr uint32_t q_half = RP * 128;                     // one 64-wide half of Q^T
+    static constexpr uint32_t k_off = 0;                             // [2] K operands
+    static constexpr uint32_t v_off = k_off + 2 * kTileBytes;       // [VST] V operands
+    static constexpr uint32_t q_off = v_off + VST * kTileBytes;     // Q^T: [d half][RP rows][128 B]
+    static constexpr uint32_t p_off = q_off + 2 * q_half;           // P^T: [col block][128 tok][128 B]
+    static constexpr uint32_t meta_off = p_off + (RP > 64 ? 2 : 1) * kHalf;  // [4 slots][128] uint4 row masks
     static constexpr uint32_t seg_off = meta_off + 4 * kTileTok * 16;  // [2][kSegInts]
     static constexpr uint32_t red_off = seg_off + 2 * kSegInts * 4;  // [wg][warp][64]
-    static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;  // [wg][m, alpha, 1/l][64]
-    static constexpr uint32_t uinfo_off = stat_off + 2 * 3 * 64 * 4;  // [2] UnitInfo
+    static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;  // [wg][m, alpha, 1/l, out row][64]
+    static constexpr uint32_t uinfo_off = stat_off + 2 * 4 * 64 * 4;  // [2] UnitInfo
     static constexpr uint32_t iinfo_off = uinfo_off + 2 * 32;         // [2] ItemInfo
     static constexpr uint32_t bar_off = iinfo_off + 2 * 16;          // mbarriers
     static constexpr uint32_t misc_off = bar_off + 32 * 8;          // tmem base, error flag
     static constexpr uint32_t total = misc_off + 16;
     static constexpr uint32_t alloc = total + 1024;
     static_assert(alloc <= 227 * 1024, "shared memory of one CTA");
+    static_assert(q_off % 1024 == 0 && p_off % 1024 == 0, "128-byte-swizzle atoms");
 };
 
 // mbarrier slots
 constexpr int kBarFullK = 0;     // [2] K of a stage landed (producer: 32 lanes + tx)
-constexpr int kBarFullV = 2;     // [2] V of a stage landed
-constexpr int kBarEmptyK = 4;    // [2] S of the stage's tile finished (MMA commit)
-constexpr int kBarEmptyV = 6;    // [2] P.V of the stage's tile finished (MMA commit)
-constexpr int kBarSFull = 8;     // [2] S buffer ready (MMA commit)
-constexpr int kBarSFree = 10;    // [2] S buffer read (one arrival per warpgroup)
-constexpr int kBarPFull = 12;    // P written (one arrival per warpgroup)
-constexpr int kBarPvDone = 13;   // P.V finished (MMA commit)
-constexpr int kBarSegFull = 14;  // [2] an item's segment table written (32 lanes)
-constexpr int kBarSegEmpty = 16; // [2] ... no longer read (both producers, 32 lanes each)
-constexpr int kBarUFull = 18;    // [2] a unit's description and Q^T written (32 lanes)
-constexpr int kBarUEmpty = 20;   // [2] ... description read (MMA issuer + 2 warpgroups)
-constexpr int kBarQFree = 22;    // the unit's last S finished: Q^T may be replaced (MMA commit)
-constexpr int kBarOFree = 23;    // [2] O buffer read out by the epilogue (one per warpgroup)
-constexpr int kNumBars = 25;
-static_assert(kNumBars * 8 <= Smem::misc_off - Smem::bar_off, "mbarrier space");
+constexpr int kBarFullV = 2;     // [3] V of a stage landed
+constexpr int kBarEmptyK = 5;    // [2] S of the stage's tile finished (MMA commit)
+constexpr int kBarEmptyV = 7;    // [3] P.V of the stage's tile finished (MMA commit)
+constexpr int kBarSFull = 10;    // [2] S buffer ready (MMA commit)
+constexpr int kBarSFree = 12;    // [2] S buffer read (one arrival per warpgroup)
+constexpr int kBarPFull = 14;    // P written (one arrival per warpgroup)
+constexpr int kBarPvDone = 15;   // P.V finished (MMA commit)
+constexpr int kBarSegFull = 16;  // [2] an item's segment table written (32 lanes)
+constexpr int kBarSegEmpty = 18; // [2] ... no longer read (both producers, 32 lanes each)
+constexpr int kBarUFull = 20;    // [2] a unit's description and Q^T written (32 lanes)
+constexpr int kBarUEmpty = 22;   // [2] ... description read (MMA issuer + 2 warpgroups)
+constexpr int kBarQFree = 24;    // the unit's last S finished: Q^T may be replaced (MMA commit)
+constexpr int kBarOFree = 25;    // [2] O buffer read out by the epilogue (one per warpgroup)
+constexpr int kNumBars = 27;
+static_assert(kNumBars * 8 <= Smem<16>::misc_off - Smem<16>::bar_off, "mbarrier space");
+
+// Tensor maps over the paged K and V.  *1: the pool as [pages*Hkv*16 rows]
+// [128], boxes of one page's 16 rows x 64 columns; *8: the pool as
+// [pages][Hkv][16][128], boxes of eight consecutive pages of one head x 64
+// columns (a tile whose pages were allocated back to back in one copy).
+struct KvMaps {
+    CUtensorMap k1, v1, k8, v8;
+};
 
 template <bool kMax>
 __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
@@ -130,26 +147,28 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
 template <int NPH>
 __global__ void __launch_bounds__(kThreadsMma, 1)
 phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
-                  const __grid_constant__ CtaRanges ranges, const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v)
+                  const uint4 *__restrict__ rmask, const int32_t *__restrict__ rmask_off,
+                  const __grid_constant__ CtaRanges ranges, const __grid_constant__ KvMaps maps)
 {
-    constexpr int RP = 2 * NPH;   // MMA N: both warpgroups' columns
+    using L = Smem<NPH>;
+    constexpr int RP = L::RP;     // MMA N: both warpgroups' columns
+    constexpr int VST = L::VST;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t *smem = smem_raw + (base - raw);
-    uint4 *meta = reinterpret_cast<uint4 *>(smem + Smem::meta_off);
-    float *red = reinterpret_cast<float *>(smem + Smem::red_off);
-    float *stat = reinterpret_cast<float *>(smem + Smem::stat_off);
-    UnitInfo *uinfo = reinterpret_cast<UnitInfo *>(smem + Smem::uinfo_off);
-    ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + Smem::iinfo_off);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::misc_off);
-    volatile int *err = reinterpret_cast<volatile int *>(smem + Smem::misc_off + 4);
-    auto bar = [&](int i) { return base + Smem::bar_off + 8u * (uint32_t)i; };
+    uint4 *meta = reinterpret_cast<uint4 *>(smem + L::meta_off);
+    float *red = reinterpret_cast<float *>(smem + L::red_off);
+    float *stat = reinterpret_cast<float *>(smem + L::stat_off);
+    UnitInfo *uinfo = reinterpret_cast<UnitInfo *>(smem + L::uinfo_off);
+    ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + L::iinfo_off);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
+    volatile int *err = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
+    auto bar = [&](int i) { return base + L::bar_off + 8u * (uint32_t)i; };
     // Segment table of buffer sb: s_pos, s_pgb (first page_id index of the
     // node), s_tb (token begin in the node), s_rmask (columns of warpgroup 0
     // in bits 0-63, of warpgroup 1 in bits 64-127).
-    auto seg_tab = [&](int sbuf) { return reinterpret_cast<int32_t *>(smem + Smem::seg_off) + sbuf * kSegInts; };
+    auto seg_tab = [&](int sbuf) { return reinterpret_cast<int32_t *>(smem + L::seg_off) + sbuf * kSegInts; };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
@@ -188,9 +207,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         *err = 0;
         tc::fence_mbar_init();
     }
+    // Warm L2 with the plan's arrays, the node page offsets and q: the
+    // start-up is a chain of dependent loads through them.
+    prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid, kThreadsMma);
+    prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid, kThreadsMma);
+    prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * kD * 2, blockIdx.x, gridDim.x, tid, kThreadsMma);
     // Operands start finite: rows past a chunk's end are never loaded and
     // their P is 0, which must not meet a NaN.
-    for (uint32_t i = tid; i < Smem::meta_off / 16; i += kThreadsMma)
+    for (uint32_t i = tid; i < L::meta_off / 16; i += kThreadsMma)
         reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
     tc::fence_proxy_async();
     tc::fence_before_sync();
@@ -208,22 +232,33 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         // table is built, so the two chains of dependent loads overlap.
         const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
         int iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
+        // qrow[k]: q row of item row lane + 32 k without the head term
+        // (query * Hq + group member), loaded once per item in parallel.
+        int qrow[4] = {0, 0, 0, 0};
         auto issue_q = [&](int h) {
-            for (int x = lane; x < R * 16; x += 32) {
-                const int r = x >> 4, ch = x & 15;
-                const int qid = p.chunk_q[cq0 + r / G];
-                cp_async_16(base + Smem::q_off + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
-                            qg + ((size_t)qid * Hq + h * G + (r % G)) * kD + ch * 8);
+            // Row r's 16 chunks go to lanes 16 (r & 1) ... + 15 in step r / 2.
+#pragma unroll 4
+            for (int x0 = 0; x0 < R * 16; x0 += 32) {
+                const int x = x0 + lane, r = x >> 4, ch = x & 15;
+                const int src = r & 31;
+                const int qr0 = __shfl_sync(0xffffffffu, qrow[0], src), qr1 = __shfl_sync(0xffffffffu, qrow[1], src);
+                const int qr2 = __shfl_sync(0xffffffffu, qrow[2], src), qr3 = __shfl_sync(0xffffffffu, qrow[3], src);
+                const int k = r >> 5;
+                const int qr = k == 0 ? qr0 : k == 1 ? qr1 : k == 2 ? qr2 : qr3;
+                if (x < R * 16)
+                    cp_async_16(base + L::q_off + (ch >> 3) * L::q_half + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
+                                qg + (size_t)(qr + h * G) * kD + ch * 8);
             }
             cp_async_commit();
         };
         auto prefetch_q = [&](int h) {
-            for (int x = lane; x < R * 2; x += 32) {
-                const int r = x >> 1;
-                const int qid = p.chunk_q[cq0 + r / G];
-                const char *addr = reinterpret_cast<const char *>(qg + ((size_t)qid * Hq + h * G + (r % G)) * kD) +
-                                   (x & 1) * 128;
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (lane + 32 * k < R) {
+                    const char *addr = reinterpret_cast<const char *>(qg + (size_t)(qrow[k] + h * G) * kD);
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr + 128));
+                }
             }
         };
         for (int u = u0; u < u1; ++u) {
@@ -243,6 +278,11 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 cq0 = p.chunk_q_off[c] + qb;
                 const int T = p.chunk_tokens[c];
                 ntiles = (T + kTileTok - 1) / kTileTok;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int r = lane + 32 * k;
+                    qrow[k] = r < R ? p.chunk_q[cq0 + r / G] * Hq + r % G : 0;
+                }
                 if (lane == 0 && i == 0)
                     KPROF(a, 31 + 0 * (sb + nseg + cq0 + T));
                 if (i == 0) {
@@ -258,20 +298,16 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
                 int32_t *tab = seg_tab(sbuf);
                 uint4 *s_rmask = reinterpret_cast<uint4 *>(tab + 3 * kMaxSegsPerChunk);
+                const uint4 *item_rm = rmask + rmask_off[item];
                 for (int s = lane; s < nseg; s += 32) {
+                    const int pgb = a.node_page_off[p.seg_node[sb + s]];
+                    const int tb = p.seg_tok_begin[sb + s];
                     tab[s] = p.seg_chunk_pos[sb + s];
-                    tab[kMaxSegsPerChunk + s] = a.node_page_off[p.seg_node[sb + s]];
-                    tab[2 * kMaxSegsPerChunk + s] = p.seg_tok_begin[sb + s];
-                    const uint32_t *lm = p.seg_lmask + p.seg_lmask_off[sb + s];
-                    uint32_t rm[4] = {0, 0, 0, 0};
-#pragma unroll 4
-                    for (int r = 0; r < R; ++r) {
-                        const int k = qb + r / G;
-                        const uint32_t bit = (lm[k >> 5] >> (k & 31)) & 1u;
-                        const int col = r < NPH ? r : 64 + (r - NPH);
-                        rm[col >> 5] |= bit << (col & 31);
-                    }
-                    s_rmask[s] = make_uint4(rm[0], rm[1], rm[2], rm[3]);
+                    tab[kMaxSegsPerChunk + s] = pgb;
+                    tab[2 * kMaxSegsPerChunk + s] = tb;
+                    // The producers' first page-table reads for this segment.
+                    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.page_id + pgb + tb / kPageSize));
+                    s_rmask[s] = item_rm[s];
                 }
                 if (lane == 0 && i == 0)
                     KPROF(a, 33);
@@ -306,10 +342,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     } else if (warp == 8 || warp == 10) {
         // ---------------- producers (warp 8: K, warp 10: V) ----------------
         const int kv = warp == 8 ? 0 : 1;
+        const int NS = kv ? VST : 2;   // stages of this operand
         const __nv_bfloat16 *src_base = reinterpret_cast<const __nv_bfloat16 *>(kv ? a.v_pages : a.k_pages);
-        const CUtensorMap *tm = kv ? &tmap_v : &tmap_k;
-        if (lane == 0)
+        const CUtensorMap *tm = kv ? &maps.v1 : &maps.k1;
+        const CUtensorMap *tm8 = kv ? &maps.v8 : &maps.k8;
+        if (lane == 0) {
             tc::prefetch_tmap(tm);
+            tc::prefetch_tmap(tm8);
+        }
         // One tile's resolution: rows lane + 32k (k < 4) and pages 0..7.
         struct Res {
             int seg[4], tok[4], pid[4];   // per row; pid only for ragged rows
@@ -319,7 +359,34 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         const int32_t *s_pos = nullptr, *s_pgb = nullptr, *s_tb = nullptr;
         const uint4 *s_rmask = nullptr;
         int T = 0, nseg = 0;
+        // Segment holding position pos (warp-uniform: broadcast reads).
+        auto seg_at = [&](int pos) {
+            int lo = 0, hi = nseg - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (s_pos[mid] <= pos)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            return lo;
+        };
         auto resolve = [&](int t, Res &r) {
+            const int p0 = t * kTileTok;
+            const int sga = seg_at(p0);
+            const int tka = s_tb[sga] + p0 - s_pos[sga];
+            if (T - p0 >= kTileTok && (tka % kPageSize) == 0 && seg_at(p0 + kTileTok - 1) == sga) {
+                // Fast path: eight whole pages of one segment.
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    r.seg[k] = sga;
+                    r.tok[k] = tka + lane + 32 * k;
+                    r.pid[k] = -1;
+                }
+                r.tma_pages = 0xffu;
+                r.page_y = lane < 8 ? a.page_id[s_pgb[sga] + tka / kPageSize + lane] : -1;
+                return;
+            }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int pos = t * kTileTok + lane + 32 * k;
@@ -372,7 +439,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     r.pid[k] = a.page_id[s_pgb[r.seg[k]] + r.tok[k] / kPageSize];
             }
         };
-        int last0 = -1, last1 = -1;   // last tile placed in stage 0 / 1
         int iseq = -1, prev_item = -1, gseq = 0;
         bool ok = true;
         for (int u = u0; u < u1 && ok; ++u) {
@@ -402,16 +468,18 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             if (lane == 0 && kv == 0 && gseq == 0)
                 KPROF(a, 41 + 0 * res.page_y);
             for (int t = 0; t < ntiles; ++t, ++gseq) {
-                const int st = gseq & 1;
-                if (gseq >= 2) {
+                const int st = gseq % NS;
+                if (gseq >= NS) {
                     const bool okw = __all_sync(
-                        0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((gseq - 2) >> 1) & 1));
+                        0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((gseq / NS) - 1) & 1));
                     if (!okw) {
                         *err = 1;
                         ok = false;
                         break;
                     }
                 }
+                if (lane == 0 && kv == 0 && gseq < 16)
+                    KPROF(a, 800 + 4 * gseq);
                 if (kv == 0) {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -419,16 +487,32 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             res.seg[k] >= 0 ? s_rmask[res.seg[k]] : make_uint4(0, 0, 0, 0);
                 }
                 const uint32_t full = bar((kv ? kBarFullV : kBarFullK) + st);
-                const uint32_t dst = base + Smem::kv_off + (uint32_t)(st * 2 + kv) * kTileBytes;
+                const uint32_t dst = base + (kv ? L::v_off : L::k_off) + (uint32_t)st * kTileBytes;
                 if (lane == 0)
                     tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
                 __syncwarp();
-                if (res.page_y >= 0) {
+                if (lane == 0 && kv == 0 && gseq == 0)
+                    KPROF(a, 42);
+                // Eight whole, consecutive pages: one box per column half.
+                bool run8 = false;
+                const int pg0 = __shfl_sync(0xffffffffu, res.page_y, 0);
+                if (res.tma_pages == 0xffu)
+                    run8 = __all_sync(0xffffffffu, lane >= 8 || res.page_y == pg0 + lane);
+                if (run8) {
+                    if (lane == 0) {
+                        tc::tma_load_4d(dst, tm8, 0, 0, h, pg0, full);
+                        tc::tma_load_4d(dst + kHalf, tm8, 64, 0, h, pg0, full);
+                    }
+                } else if (res.page_y >= 0) {
                     const int y = (res.page_y * Hkv + h) * kPageSize;
+                    if (lane == 0 && kv == 0 && gseq == 0)
+                        KPROF(a, 43);
                     const uint32_t row_b = (uint32_t)(16 * lane) * 128;
                     tc::tma_load_2d(dst + row_b, tm, 0, y, full);
                     tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full);
                 }
+                if (lane == 0 && kv == 0 && gseq < 16)
+                    KPROF(a, 801 + 4 * gseq);
                 // Ragged rows: two rows per warp step, 16 lanes (16-byte chunks) each.
                 bool any_cp = false;
                 const __nv_bfloat16 *src0 = src_base + (lane & 15) * 8;
@@ -468,12 +552,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 tc::mbar_arrive(full);
                 if (lane == 0 && gseq < 64)
                     KPROF(a, 100 + 100 * kv + gseq);
-                if (st)
-                    last1 = gseq;
-                else
-                    last0 = gseq;
                 if (t + 1 < ntiles)
                     resolve(t + 1, res);
+                if (lane == 0 && kv == 0 && gseq < 16)
+                    KPROF(a, 802 + 4 * gseq);
             }
             if (!ok)
                 break;
@@ -485,23 +567,21 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         }
         cp_async_wait<0>();
         // Do not leave while a TMA copy of ours may still be landing.
-        if (last0 >= 0)
-            tc::mbar_wait(bar(kv ? kBarFullV : kBarFullK), (last0 >> 1) & 1);
-        if (last1 >= 0)
-            tc::mbar_wait(bar((kv ? kBarFullV : kBarFullK) + 1), (last1 >> 1) & 1);
+        for (int s2 = 0; s2 < NS && s2 < gseq; ++s2) {
+            const int last = gseq - 1 - ((gseq - 1 - s2) % NS);
+            tc::mbar_wait(bar((kv ? kBarFullV : kBarFullK) + s2), (last / NS) & 1);
+        }
     } else if (warp == 9) {
         // ---------------- MMA issue ----------------
         if (lane == 0) {
             const uint32_t idesc_s = tc::idesc_bf16(128, RP, 0, 0);
             const uint32_t idesc_o = tc::idesc_bf16(128, RP, 1, 1);
             // Descriptors of k-step 0; step s adds an address offset (16-byte units).
-            const uint64_t dq = tc::smem_desc(base + Smem::q_off, 16, 1024);
-            const uint64_t dp = tc::smem_desc(base + Smem::p_off, kHalf, 1024);
-            uint64_t dk[2], dv[2];
-            for (int st = 0; st < 2; ++st) {
-                dk[st] = tc::smem_desc(base + Smem::kv_off + (uint32_t)(st * 2) * kTileBytes, 16, 1024);
-                dv[st] = tc::smem_desc(base + Smem::kv_off + (uint32_t)(st * 2 + 1) * kTileBytes, kHalf, 1024);
-            }
+            const uint64_t dq = tc::smem_desc(base + L::q_off, 16, 1024);
+            const uint64_t dp = tc::smem_desc(base + L::p_off, kHalf, 1024);
+            const uint64_t dk0 = tc::smem_desc(base + L::k_off, 16, 1024);
+            const uint64_t dv0 = tc::smem_desc(base + L::v_off, kHalf, 1024);
+            constexpr uint64_t kStageStep = kTileBytes >> 4;   // descriptor address units
             const int nunits = u1 - u0;
             // S cursor: unit is, its tile ts (nts tiles, -1 before its
             // description is read), CTA tile gs.  P.V cursor: ip, tp, gp.
@@ -531,7 +611,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
                             const uint64_t ko = (uint64_t)(((s >> 2) * kHalf + (s & 3) * 32) >> 4);
-                            tc::mma_bf16(d_s, dk[st] + ko, dq + ko, idesc_s, s > 0 ? 1u : 0u);
+                            const uint64_t qo = (uint64_t)(((s >> 2) * L::q_half + (s & 3) * 32) >> 4);
+                            tc::mma_bf16(d_s, dk0 + (uint64_t)st * kStageStep + ko, dq + qo, idesc_s, s > 0 ? 1u : 0u);
                         }
                         tc::mma_commit(bar(kBarSFull + b));
                         tc::mma_commit(bar(kBarEmptyK + st));
@@ -550,8 +631,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 // P.V(gp): needs V(gp), P(gp) and, for a unit's first tile,
                 // its O buffer read out by the epilogue of the unit two back.
                 if (gp < gs) {
-                    const int stp = gp & 1, ob = ip & 1;
-                    if (tc::mbar_test(bar(kBarFullV + stp), (gp >> 1) & 1) &&
+                    const int stp = gp % VST, ob = ip & 1;
+                    if (tc::mbar_test(bar(kBarFullV + stp), (gp / VST) & 1) &&
                         tc::mbar_test(bar(kBarPFull), gp & 1) &&
                         (tp > 0 || ip < 2 || tc::mbar_test(bar(kBarOFree + ob), ((ip - 2) >> 1) & 1))) {
                         tc::fence_after_sync();
@@ -559,7 +640,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
                             const uint64_t so = (uint64_t)((s * 2048) >> 4);
-                            tc::mma_bf16(d_o, dv[stp] + so, dp + so, idesc_o, (tp > 0 || s > 0) ? 1u : 0u);
+                            tc::mma_bf16(d_o, dv0 + (uint64_t)stp * kStageStep + so, dp + so, idesc_o,
+                                         (tp > 0 || s > 0) ? 1u : 0u);
                         }
                         tc::mma_commit(bar(kBarPvDone));
                         tc::mma_commit(bar(kBarEmptyV + stp));
@@ -586,11 +668,12 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         // Warpgroup w owns columns [w*NPH, w*NPH + NPH) of S^T and O^T.
         const int w = warp >> 2, wt = warp & 3, j = tid & 127;
         const uint32_t nb_id = 1 + (uint32_t)w;
-        float *m_s = stat + w * 192, *alpha_s = m_s + 64, *linv = m_s + 128;
+        float *m_s = stat + w * 256, *alpha_s = m_s + 64, *linv = m_s + 128;
+        int32_t *orow_s = reinterpret_cast<int32_t *>(m_s + 192);   // partial row of each column
         float *redw = red + w * 256;
         const uint32_t lane_off = (uint32_t)(wt * 32) << 16;
         const uint32_t col0 = (uint32_t)(w * NPH);
-        uint8_t *prow_ptr = smem + Smem::p_off + (j >> 3) * 1024 + (j & 7) * 128;
+        uint8_t *prow_ptr = smem + L::p_off + (j >> 3) * 1024 + (j & 7) * 128;
         const float sc = a.scale_log2;
         constexpr float kSlack = 8.f;   // rescale only when 2^(s - m) would exceed 2^8
         auto load_cols = [&](uint32_t taddr, float *v) {
@@ -748,6 +831,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 ok = tc::mbar_wait(bar(kBarPvDone), (gseq - 1) & 1);
                 tc::fence_after_sync();
             }
+            if (tid == 0 && i < 8)
+                KPROF(a, 710 + 4 * i);
             if (!ok)
                 *err = 1;
             const bool failed = tc::named_sync_or(nb_id, 128, !ok || *err != 0);
@@ -760,9 +845,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 redw[wt * 64 + g + lane] = reduce_scatter32<false>(tmp, lane);
             }
             tc::named_sync(nb_id, 128);
-            if (j < NPH)
+            if (j < NPH) {
                 linv[j] = 1.f / (redw[j] + redw[64 + j] + redw[128 + j] + redw[192 + j]);
+                const int r = w * NPH + j;
+                orow_s[j] = (ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
+            }
             tc::named_sync(nb_id, 128);
+            if (tid == 0 && i < 8)
+                KPROF(a, 711 + 4 * i);
             if (!failed) {
 #pragma unroll
                 for (int g = 0; g < NPH; g += 16) {
@@ -771,19 +861,15 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                     for (int c2 = 0; c2 < 16; ++c2) {
                         const int cc = g + c2;
-                        if (cc < rows_w) {
-                            const int r = w * NPH + cc;
-                            const size_t prw = (size_t)(ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
-                            a.o_part[prw * kD + j] = o[c2] * linv[cc];
-                        }
+                        if (cc < rows_w)
+                            a.o_part[(size_t)orow_s[cc] * kD + j] = o[c2] * linv[cc];
                     }
                 }
-                if (j < rows_w) {
-                    const int r = w * NPH + j;
-                    const size_t prw = (size_t)(ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
-                    a.lse_part[prw] = m_s[j] - log2f(linv[j]);
-                }
+                if (j < rows_w)
+                    a.lse_part[orow_s[j]] = m_s[j] - log2f(linv[j]);
             }
+            if (tid == 0 && i < 8)
+                KPROF(a, 712 + 4 * i);
             // O buffer ob and the statistics are free for the unit two on.
             tc::fence_before_sync();
             tc::named_sync(nb_id, 128);
@@ -820,7 +906,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         grid_dep_wait();
 }
 
-// ---- host: tensor maps over the paged KV, viewed as [pages*Hkv*16][128] ----
+// ---- host: tensor maps over the paged KV ----
 PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -835,80 +921,101 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder()
     return fn;
 }
 
-struct MapCache {
-    const void *ptr = nullptr;
-    uint64_t rows = 0;
-    CUtensorMap map;
-};
-
-bool kv_map(const void *ptr, uint64_t rows, MapCache &cache, CUtensorMap *out)
+// Encodes the *1 (run8 = false) or *8 view of a page pool.
+bool encode_pool_map(const void *ptr, int32_t pages, int32_t hkv, bool run8, CUtensorMap *m)
 {
-    if (cache.ptr == ptr && cache.rows == rows) {
-        *out = cache.map;
-        return true;
-    }
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
     if (!enc)
         return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    const cuuint32_t box[2] = {64, 16};
-    const cuuint32_t estr[2] = {1, 1};
-    CUtensorMap m;
-    if (enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return false;
-    cache.ptr = ptr;
-    cache.rows = rows;
-    cache.map = m;
-    *out = m;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r;
+    if (!run8) {
+        const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)pages * hkv * kPageSize};
+        const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+        const cuuint32_t box[2] = {64, 16};
+        r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)pages};
+        const cuuint64_t row = (cuuint64_t)kD * 2;
+        const cuuint64_t strides[3] = {row, row * kPageSize, row * kPageSize * hkv};
+        const cuuint32_t box[4] = {64, (cuuint32_t)kPageSize, 1, 8};
+        r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    return r == CUDA_SUCCESS;
+}
+
+// The four maps of (k, v, pages, hkv), cached per host thread for the last
+// pools seen.
+bool kv_maps(const void *k, const void *v, int32_t pages, int32_t hkv, KvMaps *out)
+{
+    struct Cache {
+        const void *k = nullptr, *v = nullptr;
+        int32_t pages = 0, hkv = 0;
+        KvMaps maps;
+    };
+    thread_local Cache c;
+    if (c.k != k || c.v != v || c.pages != pages || c.hkv != hkv) {
+        KvMaps m;
+        if (!encode_pool_map(k, pages, hkv, false, &m.k1) || !encode_pool_map(v, pages, hkv, false, &m.v1) ||
+            !encode_pool_map(k, pages, hkv, true, &m.k8) || !encode_pool_map(v, pages, hkv, true, &m.v8))
+            return false;
+        c.k = k;
+        c.v = v;
+        c.pages = pages;
+        c.hkv = hkv;
+        c.maps = m;
+    }
+    *out = c.maps;
     return true;
 }
 
 template <int NPH>
-int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost, int32_t n,
-                const CUtensorMap &mk, const CUtensorMap &mv, cudaStream_t st)
+int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
+                const int32_t *rmask_off, const int64_t *cost, int32_t n, int max_ctas, const KvMaps &maps,
+                cudaStream_t st)
 {
     static bool configured = false;
     if (!configured) {
         const cudaError_t e = cudaFuncSetAttribute(phase1_mma_kernel<NPH>,
-                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem::alloc);
+                                                   cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Smem<NPH>::alloc);
         if (e != cudaSuccess)
             return (int)e;
         configured = true;
     }
     const int64_t units = (int64_t)n * a.num_kv_heads;
-    const int64_t cap = num_sms() < kMaxGrid ? num_sms() : kMaxGrid;
+    const int64_t cap = max_ctas < kMaxGrid ? max_ctas : kMaxGrid;
     const int grid = (int)(units < cap ? units : cap);
     CtaRanges r;
     cta_ranges(cost, n, a.num_kv_heads, grid, r);
-    return (int)launch_dependent(phase1_mma_kernel<NPH>, dim3(grid), dim3(kThreadsMma), Smem::alloc, st, a, p,
-                                 items, r, mk, mv);
+    return (int)launch_dependent(phase1_mma_kernel<NPH>, dim3(grid), dim3(kThreadsMma), Smem<NPH>::alloc, st, a, p,
+                                 items, reinterpret_cast<const uint4 *>(rmask), rmask_off, r, maps);
 }
 
 }  // namespace
 
 bool mma_supported(int32_t head_dim) { return head_dim == kD; }
 
-int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const int64_t *cost,
-                      int32_t n, int bucket, void *stream)
+int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
+                      const int32_t *rmask_off, const int64_t *cost, int32_t n, int bucket, int max_ctas,
+                      void *stream)
 {
     if (n <= 0)
         return 0;
-    if ((int64_t)n * a.num_kv_heads > INT32_MAX)
+    if ((int64_t)n * a.num_kv_heads > INT32_MAX || max_ctas < 1)
         return (int)cudaErrorInvalidValue;
-    static MapCache ck, cv;
-    CUtensorMap mk, mv;
-    const uint64_t rows = (uint64_t)a.num_pages * a.num_kv_heads * kPageSize;
-    if (!kv_map(a.k_pages, rows, ck, &mk) || !kv_map(a.v_pages, rows, cv, &mv))
+    KvMaps maps;
+    if (!kv_maps(a.k_pages, a.v_pages, a.num_pages, a.num_kv_heads, &maps))
         return (int)cudaErrorInvalidValue;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (bucket) {
-    case 0: return launch_cols<16>(a, p, items, cost, n, mk, mv, st);
-    case 1: return launch_cols<32>(a, p, items, cost, n, mk, mv, st);
-    case 2: return launch_cols<48>(a, p, items, cost, n, mk, mv, st);
-    default: return launch_cols<64>(a, p, items, cost, n, mk, mv, st);
+    case 0: return launch_cols<16>(a, p, items, rmask, rmask_off, cost, n, max_ctas, maps, st);
+    case 1: return launch_cols<32>(a, p, items, rmask, rmask_off, cost, n, max_ctas, maps, st);
+    case 2: return launch_cols<48>(a, p, items, rmask, rmask_off, cost, n, max_ctas, maps, st);
+    default: return launch_cols<64>(a, p, items, rmask, rmask_off, cost, n, max_ctas, maps, st);
     }
 }
 

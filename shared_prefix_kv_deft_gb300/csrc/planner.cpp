@@ -187,6 +187,42 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     cost_prefix(fma, p.fma_cost);
     cost_prefix(fb, p.fallback_cost);
     cost_prefix(mma, p.mma_cost);
+
+    // Row masks per (item, segment): row r of an item is its query
+    // b + r / G, present in segment s when s's query mask has that bit.
+    auto qbit = [&](int32_t s, int32_t k) -> uint32_t {
+        return (p.seg_lmask[p.seg_lmask_off[s] + k / 32] >> (k % 32)) & 1u;
+    };
+    auto row_masks = [&](const std::vector<Item> &v, std::vector<uint32_t> &mask, std::vector<int32_t> &off) {
+        mask.clear();
+        off.assign(1, 0);
+        for (const Item &it : v) {
+            const int32_t rows = (it.e - it.b) * G;
+            for (int32_t s = p.chunk_seg_off[it.c]; s < p.chunk_seg_off[it.c + 1]; ++s) {
+                uint32_t m = 0;
+                for (int32_t r = 0; r < rows; ++r)
+                    m |= qbit(s, it.b + r / G) << r;
+                mask.push_back(m);
+            }
+            off.push_back((int32_t)mask.size());
+        }
+    };
+    row_masks(fma, p.fma_rmask, p.fma_rmask_off);
+    row_masks(fb, p.fallback_rmask, p.fallback_rmask_off);
+    p.mma_rmask.clear();
+    p.mma_rmask_off.assign(1, 0);
+    for (const Item &it : mma) {
+        const int32_t rows = (it.e - it.b) * G, nph = mma_half_cols(rows);
+        for (int32_t s = p.chunk_seg_off[it.c]; s < p.chunk_seg_off[it.c + 1]; ++s) {
+            uint32_t w[4] = {0, 0, 0, 0};
+            for (int32_t r = 0; r < rows; ++r) {
+                const int32_t col = r < nph ? r : 64 + (r - nph);
+                w[col / 32] |= qbit(s, it.b + r / G) << (col % 32);
+            }
+            p.mma_rmask.insert(p.mma_rmask.end(), w, w + 4);
+        }
+        p.mma_rmask_off.push_back((int32_t)(p.mma_rmask.size() / 4));
+    }
     bucket_offsets(fma, p.fma_bucket_off);
     bucket_offsets(fb, p.fallback_bucket_off);
     bucket_offsets(mma, p.mma_bucket_off);

@@ -170,14 +170,11 @@ size_t deft_workspace_bytes(const deft_plan_t *plan, int32_t num_q_heads, int32_
  *   head_dim in {64, 128}; page_size 16; num_q_heads a multiple of
  *     num_kv_heads whose quotient equals the plan's gqa_group (else
  *     DEFT_ESTATE); scale > 0 multiplies q.k (pass 1/sqrt(head_dim)).
- * Never allocates device memory, never synchronises the host; stream-ordered
- * on `stream`.  When a step has both tensor-core and CUDA-core chunks, the
- * tensor-core launches run concurrently on a side stream that the call
- * orders after `stream`'s earlier work and before the merge with two events
- * (so the whole step stays ordered on `stream` and can be captured in a
- * CUDA graph); the side stream and events are created by the first such
- * call on each host thread and device, so make that call before any stream
- * capture.  Launch failures return DEFT_ECUDA.
+ * Never allocates, never synchronises the host; stream-ordered on `stream`.
+ * The plan's device copy holds the phase-1 launches' work queues, so one
+ * plan serves one step at a time: steps that use the same plan must be
+ * ordered (one stream, or synchronised streams).  Launch failures return
+ * DEFT_ECUDA.
  */
 int deft_tree_attn(const void *q, const void *k_pages, const void *v_pages,
                    const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
@@ -220,9 +217,8 @@ int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
  *     fp32 values, 256-byte aligned pieces) exceed the array is rejected with
  *     DEFT_EWORKSPACE before anything is enqueued.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current, and the first call
- *     on a host thread may create deft_tree_attn's side stream and events;
- *     make a first call before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
  *   - All calls share the array and it keeps the last call's contents;
  *     nothing in it has to start at zero.  Calls that may overlap on the GPU
  *     (other streams, unsynchronised host threads) race and must not be made.

@@ -181,8 +181,12 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
     a.scale_log2 = scale * 1.44269504088896340736f;
     a.wait_prior = 1;
 #ifdef DEFT_KPROF
-    if (!g_kprof_buf && cudaMalloc(&g_kprof_buf, deft::kKprofSlots * sizeof(unsigned long long)) != cudaSuccess)
-        g_kprof_buf = nullptr;
+    if (!g_kprof_buf) {
+        if (cudaMalloc(&g_kprof_buf, deft::kKprofSlots * sizeof(unsigned long long)) != cudaSuccess)
+            g_kprof_buf = nullptr;
+        else
+            cudaMemset(g_kprof_buf, 0, deft::kKprofSlots * sizeof(unsigned long long));
+    }
     a.kprof = g_kprof_buf;
 #endif
     const size_t slots = (size_t)std::max(plan->tree.num_slots(), plan->naive.num_slots());

@@ -28,7 +28,10 @@ constexpr int kFmaMaxRows = 16;        // rows (queries x GQA group) per CUDA-co
 constexpr int kMmaMaxRows = 128;       // rows per tensor-core item (one MMA N extent)
 constexpr int kMmaMinRows = 16;        // a chunk with this many rows goes to the tensor path
 constexpr int kSharedTokensPerRow = 16;  // long-chunk rule for shared nodes (see planner.cpp)
-constexpr int kUnitOverheadTokens = 64;  // fixed cost of a CUDA-core unit, in tokens
+// Work-queue slots: tensor-core buckets 0-3, CUDA-core buckets 4-8, the
+// CUDA-core fallback for tensor-core chunks 9-13.
+constexpr int kQueueSlots = 14;
+inline int queue_slot(int family, int bucket) { return family == 0 ? bucket : family == 1 ? 4 + bucket : 9 + bucket; }
 
 // One partition, host side.  Items are (chunk, q_begin, q_end) triples where
 // [q_begin, q_end) indexes the chunk's query list.
@@ -56,13 +59,6 @@ struct Partition {
     // b = 0..4); bucket b is items [off[b], off[b+1]).
     std::array<int32_t, 6> fma_bucket_off{};
     std::array<int32_t, 6> fallback_bucket_off{};
-    // Host-only cost prefix sums over fma_items / fallback_items ([n+1]):
-    // entry i is the summed cost of items before i, one KV head each, an
-    // item costing its chunk's tokens plus kUnitOverheadTokens.  The
-    // CUDA-core launch cuts its units into contiguous, equal-cost CTA ranges.
-    std::vector<int64_t> fma_cost;
-    std::vector<int64_t> fallback_cost;
-    std::vector<int64_t> mma_cost;        // the same over mma_items
     // Row masks of each item over its chunk's segments, so kernels need not
     // expand the segments' query masks: for item i, entries
     // [*_rmask_off[i], *_rmask_off[i + 1]) are its chunk's segments in order.
@@ -72,10 +68,17 @@ struct Partition {
     // mma_half_cols(rows).
     std::vector<uint32_t> fma_rmask, fallback_rmask, mma_rmask;
     std::vector<int32_t> fma_rmask_off, fallback_rmask_off, mma_rmask_off;   // [n+1]
+    // Work queues of the phase-1 launches (two words each: next unit, CTAs
+    // finished), zero between launches: uploaded as zeros, reset by each
+    // launch's last CTA.  Slot of a launch: queue_slot().
+    std::vector<uint32_t> queue_words = std::vector<uint32_t>(2 * kQueueSlots, 0u);
     // mma_items are sorted by column bucket b: each of the two softmax
     // warpgroups of an item holds NPH = 16 (b + 1) query rows; bucket b is
     // items [off[b], off[b+1]).
     std::array<int32_t, 5> mma_bucket_off{};
+    // KV tokens of each bucket's items (chunk tokens summed over the items).
+    std::array<int64_t, 5> fma_bucket_tok{}, fallback_bucket_tok{};
+    std::array<int64_t, 4> mma_bucket_tok{};
     int32_t num_chunks() const { return (int32_t)chunk_tokens.size(); }
     int32_t num_segments() const { return (int32_t)seg_node.size(); }
     int32_t num_slots() const { return (int32_t)chunk_q.size(); }
@@ -106,6 +109,7 @@ struct DevPartition {
     const int32_t *fallback_rmask_off;
     const uint32_t *mma_rmask;          // uint4 per (item, segment)
     const int32_t *mma_rmask_off;       // in uint4 units
+    uint32_t *queues;                   // [kQueueSlots][2]
     int32_t num_fma_items;
     int32_t num_mma_items;
     int32_t num_fallback_items;
@@ -122,7 +126,7 @@ struct DevPartition {
 // The partition's device arrays in blob order, and how a blob placed at
 // `base` with offsets `off` binds to a DevPartition (shared by the uploaded
 // plan and the allocation-free entry point).
-constexpr int kPartArrays = 22;
+constexpr int kPartArrays = 23;
 struct ArrayRef {
     const void *ptr;
     size_t bytes;
@@ -136,7 +140,7 @@ inline std::array<ArrayRef, kPartArrays> partition_arrays(const Partition &p)
              aref(p.seg_mask), aref(p.q_slot_off), aref(p.q_slot), aref(p.fma_items), aref(p.mma_items),
              aref(p.fallback_items), aref(p.seg_lmask_off), aref(p.seg_lmask), aref(p.fma_rmask),
              aref(p.fma_rmask_off), aref(p.fallback_rmask), aref(p.fallback_rmask_off), aref(p.mma_rmask),
-             aref(p.mma_rmask_off)}};
+             aref(p.mma_rmask_off), aref(p.queue_words)}};
 }
 inline void bind_partition(const Partition &p, const uint8_t *base, const size_t *off, size_t end,
                            int32_t num_nodes, int32_t num_queries, int32_t mask_words, DevPartition &d)
@@ -165,6 +169,7 @@ inline void bind_partition(const Partition &p, const uint8_t *base, const size_t
     d.fallback_rmask_off = i32(19);
     d.mma_rmask = u32(20);
     d.mma_rmask_off = i32(21);
+    d.queues = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(base) + off[22]);
     d.num_fma_items = (int32_t)(p.fma_items.size() / 3);
     d.num_mma_items = (int32_t)(p.mma_items.size() / 3);
     d.num_fallback_items = (int32_t)(p.fallback_items.size() / 3);
@@ -231,38 +236,43 @@ struct AttnArgs {
 };
 
 // Launchers (return a cudaError_t cast to int; 0 = success).
+//
+// A phase-1 launch is persistent: `grid` CTAs, one per SM, take the launch's
+// units (item x KV head).  The step's launches run concurrently, so the
+// first `early` CTAs of a launch start at once and the rest only on SMs that
+// earlier launches leave; each early CTA first takes a contiguous block of
+// about 3/4 of an even share of the units (static_block), and every CTA
+// then takes single units from the launch's work queue.
+struct LaunchShape {
+    int32_t grid;
+    int32_t early;   // 1 <= early <= grid
+};
+inline int32_t static_block(int32_t units, int32_t early)
+{
+    return early > 0 ? (int32_t)((int64_t)units * 3 / (4 * (int64_t)early)) : 0;
+}
 // One CUDA-core launch over `n` items (device triples at `items`), all of row
 // bucket `bucket` (rows <= 2^bucket).
 // `rmask` / `rmask_off`: the items' row masks (device; rmask_off indexed
-// like items), `cost`: their host cost prefix (n + 1 entries), `max_ctas`:
-// the most CTAs the launch may use.
+// like items); `queue`: the launch's work queue (two device words, zero).
 int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-                      const int32_t *rmask_off, const int64_t *cost, int32_t n, int bucket, int max_ctas,
+                      const int32_t *rmask_off, int32_t n, int bucket, uint32_t *queue, LaunchShape shape,
                       void *stream);
-
-// Persistent phase-1 launches split their units (item-major: unit = item *
-// num_kv_heads + head) into contiguous per-CTA ranges of about equal cost:
-// CTA b takes units [begin[b], begin[b + 1]).
-constexpr int kMaxGrid = 256;
-struct CtaRanges {
-    int32_t begin[kMaxGrid + 1];
-};
-// Fills r for `grid` CTAs (grid <= kMaxGrid, <= n * hkv) from the items'
-// cost prefix; CTA b starts at the first unit whose cost prefix reaches
-// b / grid of the total.
-void cta_ranges(const int64_t *cost, int32_t n, int32_t hkv, int grid, CtaRanges &r);
 // Streaming multiprocessors of the current device.
 int num_sms();
+// Shares `sms` SMs among n concurrent launches of estimated costs cost[i]
+// and units[i] units each (dispatch.cu).
+void shape_launches(const double *cost, const int32_t *units, int n, int sms, LaunchShape *out);
 // One tensor-core launch over `n` items of column bucket `bucket`.
 int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-                      const int32_t *rmask_off, const int64_t *cost, int32_t n, int bucket, int max_ctas,
+                      const int32_t *rmask_off, int32_t n, int bucket, uint32_t *queue, LaunchShape shape,
                       void *stream);
 // Runs `launch` (returns a cudaError_t as int) on `stream`, recording it
 // under `rec` when tracing is on.
 using LaunchTracer = std::function<int(const deft_trace_record &rec, void *stream, const std::function<int()> &launch)>;
-// Enqueues one step on `stream`: the phase-1 launches of partition dp (the
-// two families concurrently when both are present) and the merge into
-// out / lse.  `hp` is dp's host copy.  Returns a cudaError_t as int.
+// Enqueues one step on `stream`: the phase-1 launches of partition dp and
+// the merge into out / lse.  `hp` is dp's host copy.  Returns a cudaError_t
+// as int.
 int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool use_mma, int32_t family,
                   void *out, int32_t out_dtype, float *lse, void *stream, const LaunchTracer &trace);
 // Row bucket of an item with `rows` rows: smallest b with rows <= 2^b.

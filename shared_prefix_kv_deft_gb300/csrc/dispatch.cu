@@ -1,151 +1,148 @@
 // dispatch.cu -- the launches of one step: phase 1 (tensor-core and
-// CUDA-core families) and the phase-2 merge.
+// CUDA-core launches, one per bucket) and the phase-2 merge, on the
+// caller's stream.
 //
-// Both phase-1 families are persistent, memory-bound kernels over disjoint
-// partial slots.  When a step has both, the tensor-core launches run on a
-// side stream concurrently with the CUDA-core launches on the caller's
-// stream, each family on a share of the SMs proportional to its cost (KV
-// tokens plus a per-unit overhead, per KV head, tensor-core tokens weighted
-// by kMmaCostNum / kMmaCostDen), so that the two finish together; a fork event orders the side stream after the caller's earlier
-// work and a join event orders the merge after both.  The side stream and
-// its events are created once per host thread and device and reused.
+// Every launch is a programmatic dependent of the one before and starts its
+// CTAs as soon as that one's CTAs are all running, so the phase-1 launches
+// run concurrently.  They share the SMs (one persistent CTA per SM): every
+// launch but the last gets a share of the SMs in proportion to its estimated
+// cost, and the last, the costliest, gets the rest plus one CTA for each SM
+// the others will leave; those extra CTAs start as the others finish and
+// take units from the last launch's work queue.  Each launch has its own
+// queue (two words in the plan's device memory, zero between launches).
 #include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
 
 #include "deft_internal.h"
 
 namespace deft {
+
 namespace {
 
-// Relative cost of a tensor-core token against a CUDA-core one when both
-// families stream at once: the tensor-core kernel holds its stages longer
-// (a V stage through the tile's softmax) and so draws less bandwidth per SM
-// (measured about 1.6x slower per byte on the few-shot tree).
-constexpr int64_t kMmaCostNum = 8, kMmaCostDen = 5;
-
-struct SideStream {
-    int dev = -1;
-    cudaStream_t s = nullptr;
-    cudaEvent_t fork = nullptr, join = nullptr;
+struct Launch {
+    int kind;      // 0 tensor core, 1 CUDA core, 2 CUDA core on tensor-core chunks
+    int bucket;
+    int32_t off;   // first item of the bucket
+    int32_t n;     // items
+    double cost;   // estimated SM time (KV tokens x KV heads x relative cost per token)
 };
 
-int side_stream(SideStream **out)
-{
-    thread_local SideStream cache[8];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return (int)cudaErrorInvalidDevice;
-    SideStream &c = cache[dev & 7];
-    if (c.dev != dev) {
-        if (c.s) {   // another device took this slot: make room
-            cudaStreamDestroy(c.s);
-            cudaEventDestroy(c.fork);
-            cudaEventDestroy(c.join);
-            c = SideStream{};
-        }
-        cudaError_t e = cudaStreamCreateWithFlags(&c.s, cudaStreamNonBlocking);
-        if (e == cudaSuccess)
-            e = cudaEventCreateWithFlags(&c.fork, cudaEventDisableTiming);
-        if (e == cudaSuccess)
-            e = cudaEventCreateWithFlags(&c.join, cudaEventDisableTiming);
-        if (e != cudaSuccess)
-            return (int)e;
-        c.dev = dev;
-    }
-    *out = &c;
-    return 0;
-}
+// Relative SM time per KV token of a CUDA-core item by row bucket: up to 4
+// rows the kernel streams at the memory rate; above, the per-row FMA work
+// outgrows it (16 rows x 2 d FMAs per 4 d bytes).
+double fma_weight(int bucket) { return bucket <= 2 ? 1.0 : bucket == 3 ? 2.5 : 5.0; }
 
 }  // namespace
+
+// SM shares of the step's phase-1 launches, in launch order (the costliest
+// last): grid and early CTAs of each.
+void shape_launches(const double *cost, const int32_t *units, int n, int sms, LaunchShape *out)
+{
+    if (n <= 0)
+        return;
+    double total = 0.0;
+    for (int i = 0; i < n; ++i)
+        total += cost[i];
+    int used = 0;
+    for (int i = 0; i + 1 < n; ++i) {
+        // A quarter over the proportional share: a launch that finishes
+        // early hands its SMs to the last launch, one that finishes late
+        // is the step's tail.
+        const double share = total > 0.0 ? 1.25 * sms * cost[i] / total : 1.0;
+        int g = (int)std::ceil(share);
+        g = std::max(1, std::min({g, (int)units[i], sms}));
+        out[i] = LaunchShape{g, g};
+        used += g;
+    }
+    // Leave the last launch at least a quarter of the SMs at the start.
+    const int cap = std::max(n - 1, sms - std::max(1, sms / 4));
+    while (used > cap) {
+        int j = 0;
+        for (int i = 1; i + 1 < n; ++i)
+            if (out[i].grid > out[j].grid)
+                j = i;
+        if (out[j].grid <= 1)
+            break;
+        --out[j].grid;
+        out[j].early = out[j].grid;
+        --used;
+    }
+    const int g = std::max(1, std::min((int)units[n - 1], sms));
+    out[n - 1] = LaunchShape{g, std::max(1, std::min(g, sms - used))};
+}
 
 int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool use_mma, int32_t family,
                   void *out, int32_t out_dtype, float *lse, void *stream, const LaunchTracer &trace)
 {
-    const int64_t hkv = a.num_kv_heads;
-    const bool mma_on = use_mma && dp.num_mma_items > 0;
-    // Cost of each family (the cost prefixes' totals, per KV head).
-    const int64_t c_mma = mma_on ? hkv * (hp.mma_cost.back() - hp.mma_cost.front()) * kMmaCostNum / kMmaCostDen : 0;
-    const int64_t c_fma = hkv * ((dp.num_fma_items ? hp.fma_cost.back() : 0) +
-                                 (!use_mma && dp.num_mma_items ? hp.fallback_cost.back() : 0));
-    const int sms = num_sms();
-    int cta_mma = sms, cta_fma = sms;
-    const bool split = c_mma > 0 && c_fma > 0 && sms >= 2;
-    if (split) {
-        cta_mma = (int)((c_mma * sms + (c_mma + c_fma) / 2) / (c_mma + c_fma));
-        cta_mma = cta_mma < 1 ? 1 : cta_mma > sms - 1 ? sms - 1 : cta_mma;
-        cta_fma = sms - cta_mma;
+    const int32_t hkv = a.num_kv_heads;
+    Launch ls[14];
+    int n = 0;
+    if (dp.num_mma_items > 0 && use_mma) {
+        for (int b = 0; b < 4; ++b) {
+            const int32_t c = hp.mma_bucket_off[b + 1] - hp.mma_bucket_off[b];
+            if (c > 0)
+                ls[n++] = Launch{0, b, hp.mma_bucket_off[b], c, (double)hp.mma_bucket_tok[b] * hkv};
+        }
     }
-    SideStream *side = nullptr;
-    void *mma_stream = stream;
-    if (split) {
-        int e = side_stream(&side);
-        if (e)
-            return e;
-        cudaStream_t main = reinterpret_cast<cudaStream_t>(stream);
-        if ((e = (int)cudaEventRecord(side->fork, main)) || (e = (int)cudaStreamWaitEvent(side->s, side->fork, 0)))
-            return e;
-        mma_stream = side->s;
-    }
-
-    // CUDA-core launches, one per row bucket; each family's first launch
-    // waits for the work before it (wait_prior).
-    AttnArgs af = a;
-    auto fma_launches = [&](const int32_t *items, const uint32_t *rmask, const int32_t *rmask_off,
-                            const std::vector<int64_t> &cost, const std::array<int32_t, 6> &off, int fb) {
+    auto add_fma = [&](int kind, const std::array<int32_t, 6> &off, const std::array<int64_t, 5> &tok) {
         for (int b = 0; b < 5; ++b) {
-            const int32_t n = off[b + 1] - off[b];
-            if (n <= 0)
-                continue;
-            const int32_t *it = items + 3 * (size_t)off[b];
-            const int r = trace({DEFT_K_PHASE1_FMA, family, b, fb, n, 0.f}, stream, [&] {
-                const int r2 = launch_phase1_fma(af, dp, it, rmask, rmask_off + off[b], cost.data() + off[b], n, b,
-                                                 cta_fma, stream);
-                if (r2 == 0)
-                    af.wait_prior = 0;
-                return r2;
-            });
-            if (r)
-                return r;
+            const int32_t c = off[b + 1] - off[b];
+            if (c > 0)
+                ls[n++] = Launch{kind, b, off[b], c, (double)tok[b] * hkv * fma_weight(b)};
         }
-        return 0;
     };
-    int rc = 0;
-    if (mma_on) {
-        AttnArgs am = a;
-        for (int b = 0; b < 4 && !rc; ++b) {
-            const int32_t n = hp.mma_bucket_off[b + 1] - hp.mma_bucket_off[b];
-            if (n <= 0)
-                continue;
-            const int32_t *it = dp.mma_items + 3 * (size_t)hp.mma_bucket_off[b];
-            rc = trace({DEFT_K_PHASE1_MMA, family, b, 0, n, 0.f}, mma_stream, [&] {
-                const int r2 = launch_phase1_mma(am, dp, it, dp.mma_rmask, dp.mma_rmask_off + hp.mma_bucket_off[b],
-                                                 hp.mma_cost.data() + hp.mma_bucket_off[b], n, b, cta_mma,
-                                                 mma_stream);
-                if (r2 == 0)
-                    am.wait_prior = 0;
-                return r2;
+    // The tensor-core path covers head_dim 128; other head sizes, or a run
+    // with DEFT_DISABLE_MMA set, take the same chunks on CUDA cores in items
+    // of at most 16 rows.
+    if (dp.num_mma_items > 0 && !use_mma)
+        add_fma(2, hp.fallback_bucket_off, hp.fallback_bucket_tok);
+    if (dp.num_fma_items > 0)
+        add_fma(1, hp.fma_bucket_off, hp.fma_bucket_tok);
+    // The costliest launch goes last: its CTAs fill the SMs the others leave.
+    if (n > 1) {
+        int j = 0;
+        for (int i = 1; i < n; ++i)
+            if (ls[i].cost > ls[j].cost)
+                j = i;
+        std::rotate(ls + j, ls + j + 1, ls + n);
+    }
+    double cost[14];
+    int32_t units[14];
+    LaunchShape shape[14];
+    for (int i = 0; i < n; ++i) {
+        cost[i] = ls[i].cost;
+        units[i] = ls[i].n * hkv;
+    }
+    shape_launches(cost, units, n, num_sms(), shape);
+
+    // Only the step's first launch waits for the stream's earlier work
+    // before reading inputs (wait_prior); the rest follow it.
+    for (int i = 0; i < n; ++i) {
+        const Launch &l = ls[i];
+        int r;
+        if (l.kind == 0) {
+            const int32_t *it = dp.mma_items + 3 * (size_t)l.off;
+            uint32_t *queue = dp.queues + 2 * queue_slot(0, l.bucket);
+            r = trace({DEFT_K_PHASE1_MMA, family, l.bucket, 0, l.n, 0.f}, stream, [&] {
+                return launch_phase1_mma(a, dp, it, dp.mma_rmask, dp.mma_rmask_off + l.off, l.n, l.bucket, queue,
+                                         shape[i], stream);
+            });
+        } else {
+            const bool fb = l.kind == 2;
+            const int32_t *it = (fb ? dp.fallback_items : dp.fma_items) + 3 * (size_t)l.off;
+            const uint32_t *rm = fb ? dp.fallback_rmask : dp.fma_rmask;
+            const int32_t *rmo = (fb ? dp.fallback_rmask_off : dp.fma_rmask_off) + l.off;
+            uint32_t *queue = dp.queues + 2 * queue_slot(fb ? 2 : 1, l.bucket);
+            r = trace({DEFT_K_PHASE1_FMA, family, l.bucket, fb ? 1 : 0, l.n, 0.f}, stream, [&] {
+                return launch_phase1_fma(a, dp, it, rm, rmo, l.n, l.bucket, queue, shape[i], stream);
             });
         }
-        if (!split && rc == 0)
-            af.wait_prior = 0;   // the CUDA-core launches follow on the same stream
-    } else if (dp.num_mma_items > 0) {
-        // The tensor-core path covers head_dim 128; other head sizes, or a
-        // run with DEFT_DISABLE_MMA set, take the same chunks on CUDA cores
-        // in items of at most 16 rows.
-        rc = fma_launches(dp.fallback_items, dp.fallback_rmask, dp.fallback_rmask_off, hp.fallback_cost,
-                          hp.fallback_bucket_off, 1);
+        if (r)
+            return r;
+        a.wait_prior = 0;
     }
-    if (rc == 0 && dp.num_fma_items > 0)
-        rc = fma_launches(dp.fma_items, dp.fma_rmask, dp.fma_rmask_off, hp.fma_cost, hp.fma_bucket_off, 0);
-    if (split) {
-        // Join even after a failed launch, so the caller's stream never runs
-        // ahead of work already queued on the side stream.
-        const int e1 = (int)cudaEventRecord(side->join, side->s);
-        const int e2 = (int)cudaStreamWaitEvent(reinterpret_cast<cudaStream_t>(stream), side->join, 0);
-        if (!rc)
-            rc = e1 ? e1 : e2;
-    }
-    if (rc)
-        return rc;
     return trace({DEFT_K_PHASE2, family, 0, 0, dp.num_queries, 0.f}, stream,
                  [&] { return launch_phase2(a, dp, out, out_dtype, lse, stream); });
 }

@@ -9,6 +9,10 @@
 
 namespace deft {
 constexpr int kKprofSlots = 4096;
+// The timestamp buffer alone, for kernels that take no AttnArgs.
+struct KprofArg {
+    unsigned long long *kprof;
+};
 }
 
 #ifdef DEFT_KPROF

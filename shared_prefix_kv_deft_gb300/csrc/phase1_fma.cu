@@ -10,14 +10,19 @@
 // stored as an fp32 partial (o_r, L_r in base 2) in the unit's slot.
 // Logits are carried in base 2 (q pre-scaled by scale * log2 e).
 //
-// Persistent CTAs (one per SM) each take a contiguous range of units of
-// about equal cost (units are item-major, so a range holds runs of one
-// item's KV heads, which share their segment table and page list).  Each
-// compute group has its own ring of 64-token stages through which the
-// tiles of its units stream continuously, so the loads of its next unit
-// overlap the end of the current one and the groups never wait on each
-// other's tiles.
-//   warp 0            metadata: runs ahead; per item it builds the segment
+// Persistent CTAs (one per SM): the launch's early CTAs, those that start
+// with the step, first take a contiguous block of units (about 3/4 of an
+// even share among them; units are item-major, so the block holds runs of
+// one item's KV heads, which share the item's segment table and page list);
+// then every CTA takes units one at a time from the launch's work queue (an
+// atomic counter), so a CTA that starts late or runs fast takes more.  Each
+// compute group has its own ring of 64-token stages through which the tiles
+// of its units stream continuously, so the loads of its next unit overlap
+// the end of the current one and the groups never wait on each other's
+// tiles.
+//   warp 0            metadata: runs ahead; takes the next unit from the
+//                     queue and passes its number to the copy warps through a
+//                     shared-memory ring; per item it builds the segment
 //                     table (positions, page bases, row masks) and gathers
 //                     the item's page ids, per unit it stages the q rows
 //                     (cp.async, completion signalled on the unit's
@@ -53,15 +58,16 @@ namespace deft {
 namespace {
 
 constexpr int kTile = 64;   // tokens per stage
-constexpr int kPageList = 1024;  // page ids staged per unit (larger units look pages up in global memory)
+constexpr int kPageList = 512;  // page ids staged per item (larger items look pages up in global memory)
 
 // Bytes of everything but the stage ring, for NG compute groups.
 template <int D, int RMAX>
 constexpr uint32_t fma_fixed_bytes(int NG)
 {
     return 2 * NG * RMAX * D * 2 + 2 * NG * 32 + NG * RMAX * D * 4 + 8 * NG * 8 * RMAX * 4 +
-           2 * 8 * NG * RMAX * 4 + NG * RMAX * D * 4 + NG * 4 * RMAX * 4 + 2 * kMaxSegsPerChunk * 20 +
-           2 * kPageList * 4 + 2 * 16 + 256 + 1024;
+           3 * 8 * NG * RMAX * 4 + NG * 8 * (RMAX < 8 ? RMAX : 8) * D * 4 + NG * 4 * RMAX * 4 +
+           2 * kMaxSegsPerChunk * 20 +
+           2 * kPageList * 4 + 2 * 16 + 64 + 384 + 1024;
 }
 
 template <int D, int RMAX>
@@ -85,14 +91,16 @@ struct FmaCfg {
     static constexpr uint32_t info_off = qst_off + UB * RMAX * D * 2;         // [UB] unit info
     static constexpr uint32_t qs_off = info_off + UB * 32;                     // [NG][RMAX][2][D/8][4] f32
     static constexpr uint32_t ps_off = qs_off + NG * RMAX * D * 4;             // [NCW][8][RMAX]
-    static constexpr uint32_t ml_off = ps_off + NCW * 8 * RMAX * 4;            // [NCW][RMAX] m, l
-    static constexpr uint32_t oacc_off = ml_off + 2 * NCW * RMAX * 4;         // [NG][RMAX][D] f32
-    static constexpr uint32_t fin_off = oacc_off + NG * RMAX * D * 4;          // [NG][4][RMAX] M, L, 1/L, row
+    static constexpr uint32_t ml_off = ps_off + NCW * 8 * RMAX * 4;            // [3][NCW][RMAX] m, l, weight
+    static constexpr int MRB = RMAX < 8 ? RMAX : 8;                            // rows per merge round
+    static constexpr uint32_t obuf_off = ml_off + 3 * NCW * RMAX * 4;         // [NG][8 warps][MRB][D] f32
+    static constexpr uint32_t fin_off = obuf_off + NG * 8 * MRB * D * 4;       // [NG][4][RMAX] M, L, 1/L, row
     static constexpr uint32_t seg_off = fin_off + NG * 4 * RMAX * 4;           // [2][5][256]
     static constexpr uint32_t pl_off = seg_off + 2 * kMaxSegsPerChunk * 20;    // [2][kPageList]
     static constexpr uint32_t iinfo_off = pl_off + 2 * kPageList * 4;          // [2] ItemInfo
-    static constexpr uint32_t bar_off = iinfo_off + 2 * 16;
-    static constexpr uint32_t nbars = 2 * ST + 2 * UB + 4;
+    static constexpr uint32_t useq_off = iinfo_off + 2 * 16;                    // [UQ] unit numbers, error flag
+    static constexpr uint32_t bar_off = useq_off + 16 * 4;
+    static constexpr uint32_t nbars = 2 * ST + 2 * UB + 4 + 2 * 8;
     static constexpr uint32_t total = bar_off + nbars * 8;
     static constexpr uint32_t alloc = total + 1024;
     static_assert(alloc <= 227 * 1024, "shared memory of one CTA");
@@ -100,8 +108,10 @@ struct FmaCfg {
 
 __device__ __forceinline__ uint32_t fbar(uint32_t base, int i) { return base + 8u * (uint32_t)i; }
 
+constexpr int kUnitQueue = 8;   // unit numbers passed from the metadata warp to the copy warps
+
 struct UnitInfo {
-    int32_t R;       // rows
+    int32_t R;       // rows (-1: no more units)
     int32_t cq0;     // first slot of the unit's rows
     int32_t h;       // KV head
     int32_t ntiles;
@@ -113,14 +123,14 @@ struct ItemInfo {
     int32_t nseg;
     int32_t T;       // chunk tokens
     int32_t listed;  // 1: the item's page ids are in the shared page list
-    int32_t pad;
+    int32_t npages;  // page-list entries of the item
 };
 
 template <int D, int RMAX>
 __global__ void __launch_bounds__(FmaCfg<D, RMAX>::THREADS, 1)
 phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
-                  const uint32_t *__restrict__ rmask, const int32_t *__restrict__ rmask_off,
-                  const __grid_constant__ CtaRanges ranges)
+                  const uint32_t *__restrict__ rmask, const int32_t *__restrict__ rmask_off, int32_t n_units,
+                  int32_t static_units, int32_t early, uint32_t *__restrict__ queue)
 {
     using C = FmaCfg<D, RMAX>;
     constexpr int NG = C::NG, NCW = C::NCW, ST = C::ST, RST = C::RST, UB = C::UB;
@@ -133,14 +143,18 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     uint32_t *meta = reinterpret_cast<uint32_t *>(smem + C::meta_off);
     UnitInfo *info = reinterpret_cast<UnitInfo *>(smem + C::info_off);
     const uint32_t bars = base + C::bar_off;
-    // mbarriers: full[ST], empty[ST], unit_full[UB], unit_empty[UB], seg_full[2], seg_empty[2]
+    // mbarriers: full[ST], empty[ST], unit_full[UB], unit_empty[UB], seg_full[2], seg_empty[2],
+    // queue_full[UQ], queue_empty[UQ]
+    constexpr int UQ = kUnitQueue;
     const int kFull = 0, kEmpty = ST, kUFull = 2 * ST, kUEmpty = 2 * ST + UB;
     const int kSFull = 2 * ST + 2 * UB, kSEmpty = kSFull + 2;
+    const int kQFull = kSEmpty + 2, kQEmpty = kQFull + UQ;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
-    const int u0 = ranges.begin[blockIdx.x], u1 = ranges.begin[blockIdx.x + 1];
     ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + C::iinfo_off);
+    volatile int32_t *useq = reinterpret_cast<volatile int32_t *>(smem + C::useq_off);
+    volatile int32_t *err = useq + UQ;
 
     if (a.wait_prior)
         grid_dep_wait();
@@ -160,6 +174,11 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_init(fbar(bars, kSFull + u), 32);
             tc::mbar_init(fbar(bars, kSEmpty + u), 64);
         }
+        for (int u = 0; u < UQ; ++u) {
+            tc::mbar_init(fbar(bars, kQFull + u), 1);
+            tc::mbar_init(fbar(bars, kQEmpty + u), 2);   // lane 0 of each copy warp
+        }
+        *err = 0;
         tc::fence_mbar_init();
     }
     // Warm L2 with the plan's arrays, the node page offsets and q.
@@ -175,8 +194,49 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         int qrow[QJ];   // per q chunk of this lane: query * Hq + group member, or -1
         int rseq0 = 0, rseq1 = 0;   // next tile of each group's ring
         int iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
-        for (int u = u0; u < u1; ++u) {
-            const int i = u - u0;
+        // Only the launch's early CTAs own a block: the others start when
+        // the step's earlier launches leave their SMs.
+        const int own_units = (int)blockIdx.x < early ? static_units : 0;
+        for (int i = 0;; ++i) {
+            // The next unit: first the CTA's own contiguous block (runs of
+            // one item's heads share its tables), then the launch's queue.
+            int u = (int)blockIdx.x * static_units + i;
+            if (i >= own_units) {
+                if (lane == 0)
+                    u = early * static_units + (int)atomicAdd(queue, 1u);
+                u = __shfl_sync(0xffffffffu, u, 0);
+            }
+            const bool last = u >= n_units;
+            // Pass it (or the end, -1) to the copy warps.
+            const int qslot = i % UQ;
+            if (i >= UQ &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kQEmpty + qslot), ((i / UQ) - 1) & 1))) {
+                if (!*err) *err = 101;
+                break;
+            }
+            if (lane == 0) {
+                useq[qslot] = last ? -1 : u;
+                tc::mbar_arrive(fbar(bars, kQFull + qslot));
+            }
+            if (last) {
+                // One end mark for each compute group (local units i .. i + NG - 1).
+                for (int k = 0; k < NG; ++k) {
+                    const int ub = (i + k) % UB;
+                    if (i + k >= UB &&
+                        !__all_sync(0xffffffffu,
+                                    tc::mbar_wait(fbar(bars, kUEmpty + ub), (((i + k) - UB) / UB) & 1))) {
+                        if (!*err) *err = 102;
+                        break;
+                    }
+                    if (lane == 0)
+                        info[ub].R = -1;
+                    __syncwarp();
+                    tc::mbar_arrive(fbar(bars, kUFull + ub));
+                    if (lane == 0)
+                        tc::mbar_arrive(fbar(bars, kUFull + ub));
+                }
+                break;
+            }
             const int item = u / Hkv, h = u - item * Hkv;
             if (item != prev_item) {
                 // A new item: its segment table and page list.
@@ -195,8 +255,10 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     qrow[j] = r < R ? p.chunk_q[cq0 + r / G] * Hq + r % G : -1;
                 }
                 if (iseq >= 2 &&
-                    !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kSEmpty + sbuf), ((iseq - 2) >> 1) & 1)))
+                    !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kSEmpty + sbuf), ((iseq - 2) >> 1) & 1))) {
+                    if (!*err) *err = 103;
                     break;
+                }
                 int32_t *seg = reinterpret_cast<int32_t *>(smem + C::seg_off) + sbuf * 1280;
                 const uint32_t *item_rm = rmask + rmask_off[item];
                 int32_t *plist = reinterpret_cast<int32_t *>(smem + C::pl_off) + sbuf * kPageList;
@@ -243,14 +305,16 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     npages += tot;
                 }
                 if (lane == 0)
-                    iinfo[sbuf] = ItemInfo{nseg, T, npages <= kPageList ? 1 : 0, 0};
+                    iinfo[sbuf] = ItemInfo{nseg, T, npages <= kPageList ? 1 : 0, npages};
                 __syncwarp();
                 tc::mbar_arrive(fbar(bars, kSFull + sbuf));
             }
             // The unit's q rows (bf16) and description for its compute group.
             const int ub = i % UB;
-            if (i >= UB && !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kUEmpty + ub), ((i - UB) / UB) & 1)))
+            if (i >= UB && !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kUEmpty + ub), ((i - UB) / UB) & 1))) {
+                if (!*err) *err = 104;
                 break;
+            }
             const uint32_t qdst = base + C::qst_off + (uint32_t)ub * RMAX * D * 2;
 #pragma unroll
             for (int j = 0; j < QJ; ++j) {
@@ -283,18 +347,37 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
         constexpr uint32_t kRowBytes = D * 2;
         constexpr uint32_t kPageBytes = kPageSize * kRowBytes;   // one head's rows of a page
-        int seq = 0, iseq = -1, prev_item = -1;
+        int seq = 0, iseq = -1, prev_item = -1, sbuf = 0;
         bool ok = true;
-        for (int u = u0; u < u1 && ok; ++u) {
-            const int i = u - u0;
-            const int item = u / Hkv, h = u - item * Hkv;
-            if (item != prev_item) {
+        for (int i = 0; ok; ++i) {
+            // The next unit number from the metadata warp (-1: no more).
+            const int qslot = i % UQ;
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kQFull + qslot), (i / UQ) & 1))) {
+                if (!*err) *err = 105;
+                break;
+            }
+            const int u = useq[qslot];
+            __syncwarp();
+            if (lane == 0)
+                tc::mbar_arrive(fbar(bars, kQEmpty + qslot));
+            const int item = u < 0 ? -1 : u / Hkv;
+            if (u < 0 || item != prev_item) {
+                // Release the previous item's segment table, then wait for this one's.
+                if (prev_item >= 0) {
+                    __syncwarp();
+                    tc::mbar_arrive(fbar(bars, kSEmpty + sbuf));
+                }
+                if (u < 0)
+                    break;
                 prev_item = item;
                 ++iseq;
-                if (!__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kSFull + (iseq & 1)), (iseq >> 1) & 1)))
+                sbuf = iseq & 1;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kSFull + sbuf), (iseq >> 1) & 1))) {
+                    if (!*err) *err = 106;
                     break;
+                }
             }
-            const int sbuf = iseq & 1;
+            const int h = u - item * Hkv;
             const int32_t *seg = reinterpret_cast<const int32_t *>(smem + C::seg_off) + sbuf * 1280;
             const int32_t *plist = reinterpret_cast<const int32_t *>(smem + C::pl_off) + sbuf * kPageList;
             const ItemInfo ii = iinfo[sbuf];
@@ -351,7 +434,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         tc::bulk_load(vdst + rb, vg + o, kPageBytes, full);
                     }
                     tc::mbar_arrive(full);
-                    if (lane == 0 && seq < 16)
+                    if (lane == 0 && ring == 0 && seq < 16)
                         KPROF(a, 2100 + 8 * seq + 1);
                     continue;
                 }
@@ -453,14 +536,11 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     cp_async_wait<0>();
                 }
                 tc::mbar_arrive(full);
-                if (lane == 0 && seq < 16)
+                if (lane == 0 && ring == 0 && seq < 16)
                     KPROF(a, 2100 + 8 * seq + 1);
             }
-            // Release the item's segment table after its last unit here.
-            if (u + 1 == u1 || (u + 1) / Hkv != item) {
-                __syncwarp();
-                tc::mbar_arrive(fbar(bars, kSEmpty + sbuf));
-            }
+            if (!ok)
+                if (!*err) *err = 107;
             if (lane == 0)
                 KPROF(a, 2000 + 8 * i + 2);
         }
@@ -481,17 +561,22 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         float *ps = reinterpret_cast<float *>(smem + C::ps_off) + cw * 8 * RMAX;
         float *mw = reinterpret_cast<float *>(smem + C::ml_off) + g * 8 * RMAX;
         float *lwb = reinterpret_cast<float *>(smem + C::ml_off) + NCW * RMAX + g * 8 * RMAX;
-        float *oacc = reinterpret_cast<float *>(smem + C::oacc_off) + g * RMAX * D;
+        float *wts = reinterpret_cast<float *>(smem + C::ml_off) + 2 * NCW * RMAX + g * 8 * RMAX;
+        float *obuf = reinterpret_cast<float *>(smem + C::obuf_off) + g * 8 * C::MRB * D;
         float *fin = reinterpret_cast<float *>(smem + C::fin_off) + g * 4 * RMAX;   // M, L, 1/L, row
         int32_t *fin_row = reinterpret_cast<int32_t *>(fin + 3 * RMAX);
         const uint32_t bar_id = 1 + (uint32_t)g, nthr = 256;
         const int gtid = tid - 96 - g * 256;   // thread index within the group
-        for (int i = g; u0 + i < u1; i += NG) {
+        for (int i = g;; i += NG) {
             const int ub = i % UB;
             const bool okw = tc::mbar_wait(fbar(bars, kUFull + ub), (i / UB) & 1);
-            if (tc::named_sync_or(bar_id, nthr, !okw))
+            if (tc::named_sync_or(bar_id, nthr, !okw)) {
+                if (!*err) *err = 108;
                 break;
+            }
             const UnitInfo ui = info[ub];
+            if (ui.R < 0)
+                break;   // no more units
             if (gtid == 0)
                 KPROF(a, 2000 + 8 * i + 3);
             const int R = ui.R;
@@ -501,7 +586,6 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 const int r = x / D, e = x - r * D;
                 qs[r * D + ((e >> 2) & 1) * (D / 2) + (e >> 3) * 4 + (e & 3)] =
                     x < R * D ? __bfloat162float(qst[x]) * a.scale_log2 : 0.f;
-                oacc[x] = 0.f;
             }
             tc::named_sync(bar_id, nthr);
             float m_run[RMAX], l_run[RMAX], o_acc[RMAX][E];
@@ -522,7 +606,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     tile_ok = false;
                     break;
                 }
-                if (gtid == 0 && sq < 16)
+                if (gtid == 0 && g == 0 && sq < 16)
                     KPROF(a, 2100 + 8 * sq + 2);
                 const uint8_t *Ks = smem + C::stage_off + (size_t)(st * 2) * C::op_bytes;
                 const uint8_t *Vs = Ks + C::op_bytes;
@@ -556,7 +640,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         }
                     }
                 }
-                if (gtid == 0 && sq < 16)
+                if (gtid == 0 && g == 0 && sq < 16)
                     KPROF(a, 2100 + 8 * sq + 4);
                 const uint32_t rmask = meta[st * kTile + row];
 #pragma unroll
@@ -586,7 +670,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     }
                 }
                 __syncwarp();
-                if (gtid == 0 && sq < 16)
+                if (gtid == 0 && g == 0 && sq < 16)
                     KPROF(a, 2100 + 8 * sq + 5);
                 // p.v over the warp's 8 tokens (p = 0 for masked and absent
                 // tokens, whose V rows are finite or zero).
@@ -619,14 +703,19 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     }
                 }
                 __syncwarp();
-                if (gtid == 0 && sq < 16)
+                if (gtid == 0 && g == 0 && sq < 16)
                     KPROF(a, 2100 + 8 * sq + 3);
                 if (lane == 0)
                     tc::mbar_arrive(fbar(bars, kEmpty + st));
             }
-            if (tc::named_sync_or(bar_id, nthr, !tile_ok))
+            if (tc::named_sync_or(bar_id, nthr, !tile_ok)) {
+                if (!*err) *err = 109;
                 break;
-            // Merge the 8 warp states of the unit's rows.
+            }
+            // Merge the 8 warp states of the unit's rows, in a fixed order (the
+            // step is bitwise repeatable): per row the max M over the warps,
+            // each warp's weight 2^(m_w - M) / L, then each output element as
+            // the weighted sum of the 8 warps' values, in rounds of MRB rows.
 #pragma unroll
             for (int r = 0; r < RMAX; ++r) {
                 if (r < R) {
@@ -643,34 +732,51 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                 for (int w = 0; w < 8; ++w)
                     M = fmaxf(M, mw[w * RMAX + gtid]);
-                float L = 0.f;
-                if (M != -INFINITY)
+                float L = 0.f, c[8];
 #pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        L += lwb[w * RMAX + gtid] * tc::ex2(mw[w * RMAX + gtid] - M);
+                for (int w = 0; w < 8; ++w) {
+                    const float mwv = mw[w * RMAX + gtid];
+                    c[w] = (M == -INFINITY || mwv == -INFINITY) ? 0.f : tc::ex2(mwv - M);
+                    L += lwb[w * RMAX + gtid] * c[w];
+                }
+                const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    wts[w * RMAX + gtid] = c[w] * inv;
                 fin[gtid] = M;
                 fin[RMAX + gtid] = L;
-                fin[2 * RMAX + gtid] = L > 0.f ? 1.f / L : 0.f;
                 fin_row[gtid] = (ui.cq0 + gtid / G) * Hq + ui.h * G + (gtid % G);
+                if (L > 0.f)
+                    a.lse_part[fin_row[gtid]] = M + log2f(L);
+                else
+                    a.lse_part[fin_row[gtid]] = -INFINITY;
             }
-            tc::named_sync(bar_id, nthr);
 #pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                if (r < R && m_run[r] != -INFINITY) {
-                    const float scl = tc::ex2(m_run[r] - fin[r]);
+            for (int rb = 0; rb < RMAX; rb += C::MRB) {
+                if (rb >= R)
+                    break;
+                if (rb > 0)
+                    tc::named_sync(bar_id, nthr);   // the previous round's reads are done
 #pragma unroll
-                    for (int e = 0; e < E; ++e)
-                        atomicAdd(oacc + r * D + lane * E + e, o_acc[r][e] * scl);
+                for (int r = 0; r < C::MRB; ++r) {
+                    if (rb + r < R) {
+                        float *dst = obuf + (lw * C::MRB + r) * D + lane * E;
+                        if constexpr (E == 4)
+                            *reinterpret_cast<float4 *>(dst) =
+                                make_float4(o_acc[rb + r][0], o_acc[rb + r][1], o_acc[rb + r][2], o_acc[rb + r][3]);
+                        else
+                            *reinterpret_cast<float2 *>(dst) = make_float2(o_acc[rb + r][0], o_acc[rb + r][1]);
+                    }
                 }
-            }
-            tc::named_sync(bar_id, nthr);
-            for (int x = gtid; x < R * D; x += nthr) {
-                const int r = x / D, e = x - r * D;
-                const size_t prow = (size_t)fin_row[r];
-                a.o_part[prow * D + e] = oacc[x] * fin[2 * RMAX + r];
-                if (e == 0) {
-                    const float L = fin[RMAX + r];
-                    a.lse_part[prow] = L > 0.f ? fin[r] + log2f(L) : -INFINITY;
+                tc::named_sync(bar_id, nthr);
+                const int rows = R - rb < C::MRB ? R - rb : C::MRB;
+                for (int x = gtid; x < rows * D; x += nthr) {
+                    const int r = x / D, e = x - r * D;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        acc = fmaf(obuf[(w * C::MRB + r) * D + e], wts[w * RMAX + rb + r], acc);
+                    a.o_part[(size_t)fin_row[rb + r] * D + e] = acc;
                 }
             }
             tc::named_sync(bar_id, nthr);
@@ -682,15 +788,42 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     }
     if (tid == 96 && blockIdx.x < 256)
         KPROF_ANY(a, 3600 + blockIdx.x);
-    // This grid completes only after the launch before it has.
-    if (tid == 0)
-        grid_dep_wait();
+    __syncthreads();
+    if (*err) {
+        // A wait ran out: mark every partial of the launch as failed (the
+        // step's output then shows it); the units are not tracked per CTA.
+        for (int u = 0; u < n_units; ++u) {
+            const int item = u / Hkv, h = u - item * Hkv;
+            const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
+            const int cq0 = p.chunk_q_off[c] + qb;
+            for (int x = tid; x < (qe - qb) * G * D; x += C::THREADS) {
+                const int r = x / D, e = x - r * D;
+                const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
+                a.o_part[prw * D + e] = __int_as_float(0x7fc00000);
+                if (e == 0)
+                    a.lse_part[prw] = __int_as_float(0x7fc00000);
+            }
+        }
+    }
+    if (tid == 0) {
+        // The launch's last CTA to finish resets its queue for the next
+        // launch and, before it exits, waits for the launch before this one:
+        // the grid completes only after that one has, while the other CTAs
+        // leave their SMs at once.
+        __threadfence();
+        if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {
+            queue[0] = 0u;
+            queue[1] = 0u;
+            __threadfence();
+            grid_dep_wait();
+        }
+    }
 }
 
 
 template <int D, int RMAX>
 int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-               const int32_t *rmask_off, const int64_t *cost, int32_t n, int max_ctas, cudaStream_t st)
+               const int32_t *rmask_off, int32_t n, uint32_t *queue, LaunchShape sh, cudaStream_t st)
 {
     using C = FmaCfg<D, RMAX>;
     static bool configured = false;
@@ -701,42 +834,40 @@ int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, c
             return (int)e;
         configured = true;
     }
-    const int64_t units = (int64_t)n * a.num_kv_heads;
-    const int64_t cap = max_ctas < kMaxGrid ? max_ctas : kMaxGrid;
-    const int grid = (int)(units < cap ? units : cap);
-    CtaRanges r;
-    cta_ranges(cost, n, a.num_kv_heads, grid, r);
+    const int32_t units = n * a.num_kv_heads;
+    const int32_t grid = sh.grid < units ? sh.grid : units;
+    const int32_t early = sh.early < grid ? sh.early : grid;
     return (int)launch_dependent(phase1_fma_kernel<D, RMAX>, dim3(grid), dim3(C::THREADS), C::alloc, st, a, p,
-                                 items, rmask, rmask_off, r);
+                                 items, rmask, rmask_off, units, static_block(units, early), early, queue);
 }
 
 template <int D>
 int launch_bucket(int bucket, const AttnArgs &a, const DevPartition &p, const int32_t *items,
-                  const uint32_t *rmask, const int32_t *rmask_off, const int64_t *cost, int32_t n, int max_ctas,
+                  const uint32_t *rmask, const int32_t *rmask_off, int32_t n, uint32_t *queue, LaunchShape sh,
                   cudaStream_t st)
 {
     switch (bucket) {
-    case 0: return launch_one<D, 1>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
-    case 1: return launch_one<D, 2>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
-    case 2: return launch_one<D, 4>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
-    case 3: return launch_one<D, 8>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
-    default: return launch_one<D, 16>(a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
+    case 0: return launch_one<D, 1>(a, p, items, rmask, rmask_off, n, queue, sh, st);
+    case 1: return launch_one<D, 2>(a, p, items, rmask, rmask_off, n, queue, sh, st);
+    case 2: return launch_one<D, 4>(a, p, items, rmask, rmask_off, n, queue, sh, st);
+    case 3: return launch_one<D, 8>(a, p, items, rmask, rmask_off, n, queue, sh, st);
+    default: return launch_one<D, 16>(a, p, items, rmask, rmask_off, n, queue, sh, st);
     }
 }
 
 }  // namespace
 
 int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-                      const int32_t *rmask_off, const int64_t *cost, int32_t n, int bucket, int max_ctas,
+                      const int32_t *rmask_off, int32_t n, int bucket, uint32_t *queue, LaunchShape shape,
                       void *stream)
 {
     if (n <= 0)
         return 0;
-    if ((int64_t)n * a.num_kv_heads > INT32_MAX || max_ctas < 1)
+    if ((int64_t)n * a.num_kv_heads > INT32_MAX || !queue || shape.grid < 1 || shape.early < 1)
         return (int)cudaErrorInvalidValue;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, rmask, rmask_off, cost, n, max_ctas, st)
-                             : launch_bucket<64>(bucket, a, p, items, rmask, rmask_off, cost, n, max_ctas, st);
+    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, rmask, rmask_off, n, queue, shape, st)
+                             : launch_bucket<64>(bucket, a, p, items, rmask, rmask_off, n, queue, shape, st);
 }
 
 }  // namespace deft

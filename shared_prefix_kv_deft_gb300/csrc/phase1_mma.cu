@@ -19,10 +19,15 @@
 // of the per-thread column sums) when a logit exceeds it by more than 2^8,
 // decided by a warpgroup vote.  Logits are base 2.
 //
-// Persistent CTAs (one per SM) take contiguous, equal-cost ranges of units
-// (unit = item x KV head, item-major); all roles walk the range in order and
-// the CTA's tiles form one sequence through the stages, so the next unit's
-// loads and its first S overlap the end of the current one.
+// Persistent CTAs (one per SM): the launch's early CTAs, those that start
+// with the step, first take a contiguous block of units (unit = item x KV
+// head, item-major, largest items first; about 3/4 of an even share among
+// them); then every CTA takes units one at a time from the launch's work
+// queue (an atomic counter), so a CTA that starts late or runs fast takes
+// more;
+// all roles walk the CTA's units in order and its tiles form one sequence
+// through the stages, so the next unit's loads and its first S overlap the
+// end of the current one.
 // Roles (12 warps):
 //   warps 0-3, 4-7  softmax warpgroups 0 and 1 (column halves);
 //   warps 8, 10     K and V producers: resolve a tile's pages through the
@@ -34,9 +39,11 @@
 //                   V once its P.V is done;
 //   warp 9          allocates TMEM; lane 0 issues the MMAs, S(t) and P.V(t-1)
 //                   in whichever order their inputs become ready;
-//   warp 11         per item, the segment table (positions, page bases,
-//                   row masks); per unit, Q^T once the previous unit's last
-//                   S has read the buffer.
+//   warp 11         takes the next unit from the queue and passes its number
+//                   to the producers through a shared-memory ring; per
+//                   item, the segment table (positions, page bases, row
+//                   masks); per unit, Q^T once the previous unit's last S has
+//                   read the buffer.
 // Two KV stages; every hand-off is an mbarrier, every wait on one is
 // bounded.  A CTA whose wait runs out writes NaN partials for its units
 // (the step's output then shows the failure), waits for its own copies,
@@ -61,11 +68,13 @@ constexpr uint32_t kTileBytes = 2 * kHalf;  // one 128 x 128 bf16 operand (32 KB
 constexpr uint32_t kHalfPage = 2 * 2048;    // K (or V) of one 16-token page: two TMA boxes
 constexpr int kSegInts = 7 * kMaxSegsPerChunk;  // pos, page base, token begin, row mask (4)
 
+constexpr int kUnitQueue = 8;   // unit numbers passed from the metadata warp to the producers
+
 struct UnitInfo {
     int32_t R;       // rows
     int32_t cq0;     // first slot of the unit's rows
     int32_t h;       // KV head
-    int32_t ntiles;
+    int32_t ntiles;  // -1: no more units
     int32_t pad[4];
 };
 
@@ -93,8 +102,9 @@ struct Smem {
     static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;  // [wg][m, alpha, 1/l, out row][64]
     static constexpr uint32_t uinfo_off = stat_off + 2 * 4 * 64 * 4;  // [2] UnitInfo
     static constexpr uint32_t iinfo_off = uinfo_off + 2 * 32;         // [2] ItemInfo
-    static constexpr uint32_t bar_off = iinfo_off + 2 * 16;          // mbarriers
-    static constexpr uint32_t misc_off = bar_off + 32 * 8;          // tmem base, error flag
+    static constexpr uint32_t useq_off = iinfo_off + 2 * 16;         // [kUnitQueue] unit numbers
+    static constexpr uint32_t bar_off = useq_off + kUnitQueue * 4;   // mbarriers
+    static constexpr uint32_t misc_off = bar_off + 48 * 8;          // tmem base, error flag
     static constexpr uint32_t total = misc_off + 16;
     static constexpr uint32_t alloc = total + 1024;
     static_assert(alloc <= 227 * 1024, "shared memory of one CTA");
@@ -116,7 +126,9 @@ constexpr int kBarUFull = 20;    // [2] a unit's description and Q^T written (32
 constexpr int kBarUEmpty = 22;   // [2] ... description read (MMA issuer + 2 warpgroups)
 constexpr int kBarQFree = 24;    // the unit's last S finished: Q^T may be replaced (MMA commit)
 constexpr int kBarOFree = 25;    // [2] O buffer read out by the epilogue (one per warpgroup)
-constexpr int kNumBars = 27;
+constexpr int kBarQFull = 27;    // [kUnitQueue] a unit number written (metadata lane 0)
+constexpr int kBarQEmpty = 35;   // [kUnitQueue] ... read (lane 0 of each producer)
+constexpr int kNumBars = 43;
 static_assert(kNumBars * 8 <= Smem<16>::misc_off - Smem<16>::bar_off, "mbarrier space");
 
 // Tensor maps over the paged K and V.  *1: the pool as [pages*Hkv*16 rows]
@@ -148,7 +160,8 @@ template <int NPH>
 __global__ void __launch_bounds__(kThreadsMma, 1)
 phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                   const uint4 *__restrict__ rmask, const int32_t *__restrict__ rmask_off,
-                  const __grid_constant__ CtaRanges ranges, const __grid_constant__ KvMaps maps)
+                  int32_t n_units, int32_t static_units, int32_t early, uint32_t *__restrict__ queue,
+                  const __grid_constant__ KvMaps maps)
 {
     using L = Smem<NPH>;
     constexpr int RP = L::RP;     // MMA N: both warpgroups' columns
@@ -172,7 +185,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
-    const int u0 = ranges.begin[blockIdx.x], u1 = ranges.begin[blockIdx.x + 1];
+    constexpr int UQ = kUnitQueue;
+    volatile int32_t *useq = reinterpret_cast<volatile int32_t *>(smem + L::useq_off);
 
     // ---------------- set-up ----------------
     if (a.wait_prior)
@@ -204,6 +218,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_init(bar(kBarOFree + i), 2);
         }
         tc::mbar_init(bar(kBarQFree), 1);
+        for (int i = 0; i < UQ; ++i) {
+            tc::mbar_init(bar(kBarQFull + i), 1);
+            tc::mbar_init(bar(kBarQEmpty + i), 2);
+        }
         *err = 0;
         tc::fence_mbar_init();
     }
@@ -261,10 +279,44 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
             }
         };
-        for (int u = u0; u < u1; ++u) {
-            const int i = u - u0;
-            const int item = u / Hkv, h = u - item * Hkv;
+        // Only the launch's early CTAs own a block: the others start when
+        // the step's earlier launches leave their SMs.
+        const int own_units = (int)blockIdx.x < early ? static_units : 0;
+        for (int i = 0;; ++i) {
+            // The next unit: first the CTA's own contiguous block (runs of
+            // one item's heads share its tables), then the launch's queue.
+            int u = (int)blockIdx.x * static_units + i;
+            if (i >= own_units) {
+                if (lane == 0)
+                    u = early * static_units + (int)atomicAdd(queue, 1u);
+                u = __shfl_sync(0xffffffffu, u, 0);
+            }
+            const bool last = u >= n_units;
             const int ub = i & 1;
+            // Pass it (or the end, -1) to the producers.
+            const int qslot = i % UQ;
+            if (i >= UQ &&
+                !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarQEmpty + qslot), ((i / UQ) - 1) & 1))) {
+                if (!*err) *err = 201;
+                break;
+            }
+            if (lane == 0) {
+                useq[qslot] = last ? -1 : u;
+                tc::mbar_arrive(bar(kBarQFull + qslot));
+            }
+            if (last) {
+                // End mark for the MMA issuer and the softmax warpgroups.
+                if (i >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1))) {
+                    if (!*err) *err = 202;
+                    break;
+                }
+                if (lane == 0)
+                    uinfo[ub].ntiles = -1;
+                __syncwarp();
+                tc::mbar_arrive(bar(kBarUFull + ub));
+                break;
+            }
+            const int item = u / Hkv, h = u - item * Hkv;
             bool q_issued = false;
             if (item != prev_item) {
                 prev_item = item;
@@ -293,7 +345,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     KPROF(a, 32);
                 if (iseq >= 2 &&
                     !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegEmpty + sbuf), ((iseq - 2) >> 1) & 1))) {
-                    *err = 1;
+                    if (!*err) *err = 203;
                     break;
                 }
                 int32_t *tab = seg_tab(sbuf);
@@ -322,7 +374,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 bool okw = i < 2 || tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1);
                 okw = okw && tc::mbar_wait(bar(kBarQFree), (i - 1) & 1);
                 if (!__all_sync(0xffffffffu, okw)) {
-                    *err = 1;
+                    if (!*err) *err = 204;
                     break;
                 }
                 issue_q(h);
@@ -335,8 +387,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_arrive(bar(kBarUFull + ub));
             if (lane == 0 && i < 8)
                 KPROF(a, 20 + i);
-            // Warm L2 with the next unit's rows when it is the same item.
-            if (u + 1 < u1 && (u + 1) / Hkv == item)
+            // Warm L2 with the rows of the item's next KV head, likely this
+            // CTA's next unit (the queue hands out units in order).
+            if (h + 1 < Hkv)
                 prefetch_q(h + 1);
         }
     } else if (warp == 8 || warp == 10) {
@@ -439,19 +492,37 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     r.pid[k] = a.page_id[s_pgb[r.seg[k]] + r.tok[k] / kPageSize];
             }
         };
-        int iseq = -1, prev_item = -1, gseq = 0;
+        int iseq = -1, prev_item = -1, gseq = 0, sbuf = 0;
         bool ok = true;
-        for (int u = u0; u < u1 && ok; ++u) {
-            const int item = u / Hkv, h = u - item * Hkv;
-            if (item != prev_item) {
+        for (int i = 0; ok; ++i) {
+            // The next unit number from the metadata warp (-1: no more).
+            const int qslot = i % UQ;
+            if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarQFull + qslot), (i / UQ) & 1))) {
+                if (!*err) *err = 205;
+                break;
+            }
+            const int u = useq[qslot];
+            __syncwarp();
+            if (lane == 0)
+                tc::mbar_arrive(bar(kBarQEmpty + qslot));
+            const int item = u < 0 ? -1 : u / Hkv;
+            if (u < 0 || item != prev_item) {
+                // Release the previous item's segment table, then wait for this one's.
+                if (prev_item >= 0) {
+                    __syncwarp();
+                    tc::mbar_arrive(bar(kBarSegEmpty + sbuf));
+                }
+                if (u < 0)
+                    break;
                 prev_item = item;
                 ++iseq;
-                if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegFull + (iseq & 1)), (iseq >> 1) & 1))) {
-                    *err = 1;
+                sbuf = iseq & 1;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegFull + sbuf), (iseq >> 1) & 1))) {
+                    if (!*err) *err = 206;
                     break;
                 }
             }
-            const int sbuf = iseq & 1;
+            const int h = u - item * Hkv;
             const int32_t *tab = seg_tab(sbuf);
             s_pos = tab;
             s_pgb = tab + kMaxSegsPerChunk;
@@ -473,7 +544,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     const bool okw = __all_sync(
                         0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((gseq / NS) - 1) & 1));
                     if (!okw) {
-                        *err = 1;
+                        if (!*err) *err = 207;
                         ok = false;
                         break;
                     }
@@ -557,13 +628,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 if (lane == 0 && kv == 0 && gseq < 16)
                     KPROF(a, 802 + 4 * gseq);
             }
-            if (!ok)
-                break;
-            // Release the item's segment table after its last unit here.
-            if (u + 1 == u1 || (u + 1) / Hkv != item) {
-                __syncwarp();
-                tc::mbar_arrive(bar(kBarSegEmpty + sbuf));
-            }
         }
         cp_async_wait<0>();
         // Do not leave while a TMA copy of ours may still be landing.
@@ -582,7 +646,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             const uint64_t dk0 = tc::smem_desc(base + L::k_off, 16, 1024);
             const uint64_t dv0 = tc::smem_desc(base + L::v_off, kHalf, 1024);
             constexpr uint64_t kStageStep = kTileBytes >> 4;   // descriptor address units
-            const int nunits = u1 - u0;
+            int nunits = 0x7fffffff;   // known once the end mark is read
             // S cursor: unit is, its tile ts (nts tiles, -1 before its
             // description is read), CTA tile gs.  P.V cursor: ip, tp, gp.
             int is = 0, ts = 0, nts = -1, gs = 0;
@@ -597,6 +661,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 if (is < nunits && gs <= gp + 1) {
                     if (nts < 0 && tc::mbar_test(bar(kBarUFull + (is & 1)), (is >> 1) & 1)) {
                         nts = uinfo[is & 1].ntiles;
+                        if (nts < 0)
+                            nunits = is;   // no more units
                         if (is & 1)
                             ntq1 = nts;
                         else
@@ -661,7 +727,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     ok = false;
             }
             if (!ok)
-                *err = 1;
+                if (!*err) *err = 208;
         }
     } else {
         // ---------------- softmax warpgroups ----------------
@@ -699,15 +765,17 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             }
         };
         int gseq = 0;
-        for (int i = 0; u0 + i < u1; ++i) {
+        for (int i = 0;; ++i) {
             const int ub = i & 1, ob = i & 1;
             const bool okw = tc::mbar_wait(bar(kBarUFull + ub), (i >> 1) & 1);
             if (tc::named_sync_or(nb_id, 128, !okw)) {
-                *err = 1;
+                if (!*err) *err = 209;
                 break;
             }
             const UnitInfo ui = uinfo[ub];
             tc::named_sync(nb_id, 128);
+            if (ui.ntiles < 0)
+                break;   // no more units
             if (j == 0)
                 tc::mbar_arrive(bar(kBarUEmpty + ub));
             const int R = ui.R, ntiles = ui.ntiles;
@@ -834,7 +902,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             if (tid == 0 && i < 8)
                 KPROF(a, 710 + 4 * i);
             if (!ok)
-                *err = 1;
+                if (!*err) *err = 210;
             const bool failed = tc::named_sync_or(nb_id, 128, !ok || *err != 0);
 #pragma unroll
             for (int g = 0; g < NPH; g += 32) {
@@ -877,7 +945,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 tc::mbar_arrive(bar(kBarOFree + ob));
             if (tid == 0 && i < 8)
                 KPROF(a, 700 + i);
-            if (tid == 0 && u0 + i + 1 == u1 && blockIdx.x < 1024)
+            if (tid == 0 && blockIdx.x < 1024)
                 KPROF_ANY(a, 1024 + blockIdx.x);
             if (failed)
                 break;
@@ -886,8 +954,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     tc::fence_before_sync();
     __syncthreads();
     if (*err && tid < 128) {
-        // Mark every partial of the CTA's units as failed.
-        for (int u = u0; u < u1; ++u) {
+        // A wait ran out: mark every partial of the launch as failed (the
+        // step's output then shows it); the units are not tracked per CTA.
+        for (int u = 0; u < n_units; ++u) {
             const int item = u / Hkv, h = u - item * Hkv;
             const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
             const int cq0 = p.chunk_q_off[c] + qb;
@@ -901,9 +970,19 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     }
     if (warp == 9)
         tc::tmem_dealloc(tmem, kTmemCols);
-    // This grid completes only after the launch before it has.
-    if (tid == 0)
-        grid_dep_wait();
+    if (tid == 0) {
+        // The launch's last CTA to finish resets its queue for the next
+        // launch and, before it exits, waits for the launch before this one:
+        // the grid completes only after that one has, while the other CTAs
+        // leave their SMs at once.
+        __threadfence();
+        if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {
+            queue[0] = 0u;
+            queue[1] = 0u;
+            __threadfence();
+            grid_dep_wait();
+        }
+    }
 }
 
 // ---- host: tensor maps over the paged KV ----
@@ -975,7 +1054,7 @@ bool kv_maps(const void *k, const void *v, int32_t pages, int32_t hkv, KvMaps *o
 
 template <int NPH>
 int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-                const int32_t *rmask_off, const int64_t *cost, int32_t n, int max_ctas, const KvMaps &maps,
+                const int32_t *rmask_off, int32_t n, uint32_t *queue, LaunchShape sh, const KvMaps &maps,
                 cudaStream_t st)
 {
     static bool configured = false;
@@ -986,13 +1065,12 @@ int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, 
             return (int)e;
         configured = true;
     }
-    const int64_t units = (int64_t)n * a.num_kv_heads;
-    const int64_t cap = max_ctas < kMaxGrid ? max_ctas : kMaxGrid;
-    const int grid = (int)(units < cap ? units : cap);
-    CtaRanges r;
-    cta_ranges(cost, n, a.num_kv_heads, grid, r);
+    const int32_t units = n * a.num_kv_heads;
+    const int32_t grid = sh.grid < units ? sh.grid : units;
+    const int32_t early = sh.early < grid ? sh.early : grid;
     return (int)launch_dependent(phase1_mma_kernel<NPH>, dim3(grid), dim3(kThreadsMma), Smem<NPH>::alloc, st, a, p,
-                                 items, reinterpret_cast<const uint4 *>(rmask), rmask_off, r, maps);
+                                 items, reinterpret_cast<const uint4 *>(rmask), rmask_off, units,
+                                 static_block(units, early), early, queue, maps);
 }
 
 }  // namespace
@@ -1000,22 +1078,22 @@ int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, 
 bool mma_supported(int32_t head_dim) { return head_dim == kD; }
 
 int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-                      const int32_t *rmask_off, const int64_t *cost, int32_t n, int bucket, int max_ctas,
+                      const int32_t *rmask_off, int32_t n, int bucket, uint32_t *queue, LaunchShape shape,
                       void *stream)
 {
     if (n <= 0)
         return 0;
-    if ((int64_t)n * a.num_kv_heads > INT32_MAX || max_ctas < 1)
+    if ((int64_t)n * a.num_kv_heads > INT32_MAX || !queue || shape.grid < 1 || shape.early < 1)
         return (int)cudaErrorInvalidValue;
     KvMaps maps;
     if (!kv_maps(a.k_pages, a.v_pages, a.num_pages, a.num_kv_heads, &maps))
         return (int)cudaErrorInvalidValue;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (bucket) {
-    case 0: return launch_cols<16>(a, p, items, rmask, rmask_off, cost, n, max_ctas, maps, st);
-    case 1: return launch_cols<32>(a, p, items, rmask, rmask_off, cost, n, max_ctas, maps, st);
-    case 2: return launch_cols<48>(a, p, items, rmask, rmask_off, cost, n, max_ctas, maps, st);
-    default: return launch_cols<64>(a, p, items, rmask, rmask_off, cost, n, max_ctas, maps, st);
+    case 0: return launch_cols<16>(a, p, items, rmask, rmask_off, n, queue, shape, maps, st);
+    case 1: return launch_cols<32>(a, p, items, rmask, rmask_off, n, queue, shape, maps, st);
+    case 2: return launch_cols<48>(a, p, items, rmask, rmask_off, n, queue, shape, maps, st);
+    default: return launch_cols<64>(a, p, items, rmask, rmask_off, n, queue, shape, maps, st);
     }
 }
 

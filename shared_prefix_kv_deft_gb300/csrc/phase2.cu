@@ -19,6 +19,7 @@
 // and are mostly still in L2.
 #include "common.cuh"
 #include "deft_internal.h"
+#include "kprof.cuh"
 
 namespace deft {
 namespace {
@@ -27,12 +28,16 @@ template <int D>
 __global__ void __launch_bounds__(256) phase2_merge_kernel(
     const float *__restrict__ o_part, const float *__restrict__ lse_part,
     const int32_t *__restrict__ q_slot_off, const int32_t *__restrict__ q_slot, int32_t num_queries,
-    int32_t num_q_heads, void *__restrict__ out, int32_t out_dtype, float *__restrict__ lse_out)
+    int32_t num_q_heads, void *__restrict__ out, int32_t out_dtype, float *__restrict__ lse_out,
+    KprofArg kp)
 {
     constexpr int E = D / 32;  // elements per lane
     constexpr int KP = 16;     // slots whose partial rows are loaded before any arithmetic
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0) {
         grid_dep_launch();
+        if (blockIdx.x < 96)
+            KPROF_ANY(kp, 3760 + blockIdx.x);
+    }
     const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (warp >= num_queries * num_q_heads)
@@ -46,6 +51,8 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
     if (lane < n)
         row = (size_t)q_slot[s0 + lane] * num_q_heads + h;
     grid_dep_wait();   // the phase-1 launches have completed
+    if ((threadIdx.x & 255) == 0 && blockIdx.x < 96)
+        KPROF_ANY(kp, 3856 + blockIdx.x);
 
     // Every load of the first KP slots goes out before the first use.
     const float l = lane < n ? lse_part[row] : -INFINITY;
@@ -143,6 +150,8 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
     if (lane == 0)
         lse_out[(size_t)q * num_q_heads + h] =
             wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
+    if (threadIdx.x == 0 && blockIdx.x < 96)
+        KPROF_ANY(kp, 3952 + blockIdx.x);
 }
 
 }  // namespace
@@ -161,9 +170,9 @@ int launch_phase2(const AttnArgs &a, const DevPartition &p, void *out, int32_t o
     const int32_t nq = p.num_queries, hq = a.num_q_heads;
     if (a.head_dim == 128)
         return (int)launch_dependent(phase2_merge_kernel<128>, dim3(blocks), dim3(threads), 0, st, op, lp, so, sl,
-                                     nq, hq, out, out_dtype, lse);
+                                     nq, hq, out, out_dtype, lse, KprofArg{a.kprof});
     return (int)launch_dependent(phase2_merge_kernel<64>, dim3(blocks), dim3(threads), 0, st, op, lp, so, sl, nq,
-                                 hq, out, out_dtype, lse);
+                                 hq, out, out_dtype, lse, KprofArg{a.kprof});
 }
 
 }  // namespace deft

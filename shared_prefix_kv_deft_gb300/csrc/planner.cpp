@@ -179,14 +179,6 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     emit(fma, p.fma_items);
     emit(mma, p.mma_items);
     emit(fb, p.fallback_items);
-    auto cost_prefix = [&](const std::vector<Item> &v, std::vector<int64_t> &out) {
-        out.assign(1, 0);
-        for (const Item &it : v)
-            out.push_back(out.back() + p.chunk_tokens[it.c] + kUnitOverheadTokens);
-    };
-    cost_prefix(fma, p.fma_cost);
-    cost_prefix(fb, p.fallback_cost);
-    cost_prefix(mma, p.mma_cost);
 
     // Row masks per (item, segment): row r of an item is its query
     // b + r / G, present in segment s when s's query mask has that bit.
@@ -226,31 +218,19 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     bucket_offsets(fma, p.fma_bucket_off);
     bucket_offsets(fb, p.fallback_bucket_off);
     bucket_offsets(mma, p.mma_bucket_off);
+    // KV tokens each bucket's launch reads (per KV head): the dispatcher
+    // shares the SMs among concurrent launches in proportion.
+    auto bucket_tokens = [&](const std::vector<Item> &v, auto &tok) {
+        tok.fill(0);
+        for (const Item &it : v)
+            tok[it.bucket] += p.chunk_tokens[it.c];
+    };
+    bucket_tokens(fma, p.fma_bucket_tok);
+    bucket_tokens(fb, p.fallback_bucket_tok);
+    bucket_tokens(mma, p.mma_bucket_tok);
 }
 
 }  // namespace
-
-void cta_ranges(const int64_t *cost, int32_t n, int32_t hkv, int grid, CtaRanges &r)
-{
-    const int64_t c0 = cost[0];
-    const int64_t total = (int64_t)hkv * (cost[n] - c0);
-    int32_t i = 0;
-    r.begin[0] = 0;
-    for (int b = 1; b < grid; ++b) {
-        const int64_t target = total * b / grid;
-        while (i < n && (int64_t)hkv * (cost[i + 1] - c0) <= target)
-            ++i;
-        if (i == n) {
-            r.begin[b] = n * hkv;
-            continue;
-        }
-        // Item i holds the target: its first head whose start is at or past it.
-        const int64_t rem = target - (int64_t)hkv * (cost[i] - c0);
-        const int64_t ci = cost[i + 1] - cost[i];
-        r.begin[b] = (int32_t)((int64_t)i * hkv + (rem + ci - 1) / ci);
-    }
-    r.begin[grid] = n * hkv;
-}
 
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                const int32_t *query_node, int32_t num_queries, int32_t chunk_target,

@@ -18,6 +18,20 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// A persistent CTA is done with its launch's work queue (queue[0]: next
+// unit, queue[1]: CTAs done).  The launch's last CTA to get here resets the
+// queue to zero for the next launch (every CTA has made its last queue[0]
+// access by then) and records that in done[1]; done[0] marks the call.
+__device__ __forceinline__ void queue_done(uint32_t *queue, volatile int32_t *done)
+{
+    done[0] = 1;
+    if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {
+        queue[0] = 0u;
+        queue[1] = 0u;
+        done[1] = 1;
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll

@@ -98,7 +98,7 @@ struct FmaCfg {
     static constexpr uint32_t seg_off = fin_off + NG * 4 * RMAX * 4;           // [2][5][256]
     static constexpr uint32_t pl_off = seg_off + 2 * kMaxSegsPerChunk * 20;    // [2][kPageList]
     static constexpr uint32_t iinfo_off = pl_off + 2 * kPageList * 4;          // [2] ItemInfo
-    static constexpr uint32_t useq_off = iinfo_off + 2 * 16;                    // [UQ] unit numbers, error flag
+    static constexpr uint32_t useq_off = iinfo_off + 2 * 16;                    // [UQ] unit numbers, error and queue flags
     static constexpr uint32_t bar_off = useq_off + 16 * 4;
     static constexpr uint32_t nbars = 2 * ST + 2 * UB + 4 + 2 * 8;
     static constexpr uint32_t total = bar_off + nbars * 8;
@@ -155,6 +155,9 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + C::iinfo_off);
     volatile int32_t *useq = reinterpret_cast<volatile int32_t *>(smem + C::useq_off);
     volatile int32_t *err = useq + UQ;
+    // qdone[0]: this CTA has counted itself done with the queue; qdone[1]:
+    // it was the launch's last to do so.
+    volatile int32_t *qdone = useq + UQ + 1;
 
     if (a.wait_prior)
         grid_dep_wait();
@@ -179,12 +182,10 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_init(fbar(bars, kQEmpty + u), 2);   // lane 0 of each copy warp
         }
         *err = 0;
+        qdone[0] = 0;
+        qdone[1] = 0;
         tc::fence_mbar_init();
     }
-    // Warm L2 with the plan's arrays, the node page offsets and q.
-    prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid, C::THREADS);
-    prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid, C::THREADS);
-    prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * D * 2, blockIdx.x, gridDim.x, tid, C::THREADS);
     __syncthreads();
 
     if (warp == 0) {
@@ -219,6 +220,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 tc::mbar_arrive(fbar(bars, kQFull + qslot));
             }
             if (last) {
+                if (lane == 0)
+                    queue_done(queue, qdone);
                 // One end mark for each compute group (local units i .. i + NG - 1).
                 for (int k = 0; k < NG; ++k) {
                     const int ub = (i + k) % UB;
@@ -553,6 +556,13 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         }
     } else {
         // ------------------------------------------------------------ compute
+        // While the first tiles load: warm L2 with the plan's arrays, the
+        // node page offsets and q, which the metadata and copy warps walk in
+        // chains of dependent loads (prefetches hold the issuing warp, so the
+        // idle warps issue them).
+        prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
+        prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
+        prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * D * 2, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
         // Group g takes the CTA's units g, g + NG, ... whole.
         const int cw = warp - 3;          // compute warp 0..NCW-1
         const int g = cw >> 3, lw = cw & 7;
@@ -806,17 +816,13 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         }
     }
     if (tid == 0) {
-        // The launch's last CTA to finish resets its queue for the next
-        // launch and, before it exits, waits for the launch before this one:
-        // the grid completes only after that one has, while the other CTAs
-        // leave their SMs at once.
-        __threadfence();
-        if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {
-            queue[0] = 0u;
-            queue[1] = 0u;
-            __threadfence();
+        // The CTA that counted itself last waits, before it exits, for the
+        // launch before this one: the grid completes only after that one
+        // has, while the other CTAs leave their SMs at once.
+        if (!qdone[0])
+            queue_done(queue, qdone);
+        if (qdone[1])
             grid_dep_wait();
-        }
     }
 }
 

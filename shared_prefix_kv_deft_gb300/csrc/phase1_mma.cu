@@ -104,7 +104,7 @@ struct Smem {
     static constexpr uint32_t iinfo_off = uinfo_off + 2 * 32;         // [2] ItemInfo
     static constexpr uint32_t useq_off = iinfo_off + 2 * 16;         // [kUnitQueue] unit numbers
     static constexpr uint32_t bar_off = useq_off + kUnitQueue * 4;   // mbarriers
-    static constexpr uint32_t misc_off = bar_off + 48 * 8;          // tmem base, error flag
+    static constexpr uint32_t misc_off = bar_off + 48 * 8;          // tmem base, error flag, queue flags
     static constexpr uint32_t total = misc_off + 16;
     static constexpr uint32_t alloc = total + 1024;
     static_assert(alloc <= 227 * 1024, "shared memory of one CTA");
@@ -177,6 +177,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + L::iinfo_off);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc_off);
     volatile int *err = reinterpret_cast<volatile int *>(smem + L::misc_off + 4);
+    // qdone[0]: this CTA has counted itself done with the queue; qdone[1]:
+    // it was the launch's last to do so.
+    volatile int *qdone = reinterpret_cast<volatile int *>(smem + L::misc_off + 8);
     auto bar = [&](int i) { return base + L::bar_off + 8u * (uint32_t)i; };
     // Segment table of buffer sb: s_pos, s_pgb (first page_id index of the
     // node), s_tb (token begin in the node), s_rmask (columns of warpgroup 0
@@ -189,6 +192,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     volatile int32_t *useq = reinterpret_cast<volatile int32_t *>(smem + L::useq_off);
 
     // ---------------- set-up ----------------
+    // The tensor maps are kernel parameters: fetch them before anything else.
+    if (warp == 8 && lane < 4)
+        tc::prefetch_tmap(lane == 0 ? &maps.k1 : lane == 1 ? &maps.k8 : lane == 2 ? &maps.v1 : &maps.v8);
     if (a.wait_prior)
         grid_dep_wait();
     if (tid == 0) {
@@ -200,6 +206,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     if (warp == 9) {
         tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tc::tmem_relinquish();
+        if (lane == 0)
+            KPROF(a, 2);
     }
     if (tid == 0) {
         for (int i = kBarFullK; i < kBarEmptyK; ++i)
@@ -223,17 +231,17 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_init(bar(kBarQEmpty + i), 2);
         }
         *err = 0;
+        qdone[0] = 0;
+        qdone[1] = 0;
         tc::fence_mbar_init();
+        KPROF(a, 3);
     }
-    // Warm L2 with the plan's arrays, the node page offsets and q: the
-    // start-up is a chain of dependent loads through them.
-    prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid, kThreadsMma);
-    prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid, kThreadsMma);
-    prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * kD * 2, blockIdx.x, gridDim.x, tid, kThreadsMma);
     // Operands start finite: rows past a chunk's end are never loaded and
     // their P is 0, which must not meet a NaN.
     for (uint32_t i = tid; i < L::meta_off / 16; i += kThreadsMma)
         reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0)
+        KPROF(a, 5);
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
@@ -305,6 +313,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 tc::mbar_arrive(bar(kBarQFull + qslot));
             }
             if (last) {
+                if (lane == 0)
+                    queue_done(queue, qdone);
                 // End mark for the MMA issuer and the softmax warpgroups.
                 if (i >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1))) {
                     if (!*err) *err = 202;
@@ -399,10 +409,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         const __nv_bfloat16 *src_base = reinterpret_cast<const __nv_bfloat16 *>(kv ? a.v_pages : a.k_pages);
         const CUtensorMap *tm = kv ? &maps.v1 : &maps.k1;
         const CUtensorMap *tm8 = kv ? &maps.v8 : &maps.k8;
-        if (lane == 0) {
-            tc::prefetch_tmap(tm);
-            tc::prefetch_tmap(tm8);
-        }
         // One tile's resolution: rows lane + 32k (k < 4) and pages 0..7.
         struct Res {
             int seg[4], tok[4], pid[4];   // per row; pid only for ragged rows
@@ -731,6 +737,13 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         }
     } else {
         // ---------------- softmax warpgroups ----------------
+        // While the first tile loads: warm L2 with the plan's arrays, the
+        // node page offsets and q, which the metadata warp and the producers
+        // walk in chains of dependent loads (prefetches hold the issuing
+        // warp, so the idle warps issue them).
+        prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid, 256);
+        prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid, 256);
+        prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * kD * 2, blockIdx.x, gridDim.x, tid, 256);
         // Warpgroup w owns columns [w*NPH, w*NPH + NPH) of S^T and O^T.
         const int w = warp >> 2, wt = warp & 3, j = tid & 127;
         const uint32_t nb_id = 1 + (uint32_t)w;
@@ -971,17 +984,13 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     if (warp == 9)
         tc::tmem_dealloc(tmem, kTmemCols);
     if (tid == 0) {
-        // The launch's last CTA to finish resets its queue for the next
-        // launch and, before it exits, waits for the launch before this one:
-        // the grid completes only after that one has, while the other CTAs
-        // leave their SMs at once.
-        __threadfence();
-        if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {
-            queue[0] = 0u;
-            queue[1] = 0u;
-            __threadfence();
+        // The CTA that counted itself last waits, before it exits, for the
+        // launch before this one: the grid completes only after that one
+        // has, while the other CTAs leave their SMs at once.
+        if (!qdone[0])
+            queue_done(queue, qdone);
+        if (qdone[1])
             grid_dep_wait();
-        }
     }
 }
 

@@ -40,6 +40,19 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// Packed fp32 pair fused multiply-add (one f32x2 instruction): a * b + c
+// element-wise, each element rounded once as by fmaf.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%6, %7};\n\t"
+        "fma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
 // bf16 pair packed in a 32-bit word -> two floats (exact).
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w)
 {

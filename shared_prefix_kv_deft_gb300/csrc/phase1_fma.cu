@@ -64,15 +64,14 @@ constexpr int kPageList = 512;  // page ids staged per item (larger items look p
 template <int D, int RMAX>
 constexpr uint32_t fma_fixed_bytes(int NG)
 {
-    return 2 * NG * RMAX * D * 2 + 2 * NG * 32 + NG * RMAX * D * 4 + 8 * NG * 8 * RMAX * 4 +
-           3 * 8 * NG * RMAX * 4 + NG * 8 * (RMAX < 8 ? RMAX : 8) * D * 4 + NG * 4 * RMAX * 4 +
+    return 2 * NG * RMAX * D * 2 + 2 * NG * 32 + NG * RMAX * D * 4 + 3 * 8 * NG * RMAX * 4 + NG * 8 * (RMAX < 8 ? RMAX : 8) * D * 4 + NG * 4 * RMAX * 4 +
            2 * kMaxSegsPerChunk * 20 +
            2 * kPageList * 4 + 2 * 16 + 64 + 384 + 1024;
 }
 
 template <int D, int RMAX>
 struct FmaCfg {
-    static constexpr int NG = RMAX <= 4 ? 2 : 1;       // compute groups
+    static constexpr int NG = RMAX <= 2 ? 2 : 1;       // compute groups
     static constexpr int NCW = 8 * NG;                 // compute warps
     static constexpr int THREADS = 32 * (NCW + 3);     // + metadata warp + two copy warps
     // Stages in the ring: as many as fit next to the fixed buffers, at most 6
@@ -89,9 +88,8 @@ struct FmaCfg {
     static constexpr uint32_t meta_off = ST * 2 * op_bytes;       // [stage][64] row masks
     static constexpr uint32_t qst_off = meta_off + ST * kTile * 4;            // [UB][RMAX][D] bf16
     static constexpr uint32_t info_off = qst_off + UB * RMAX * D * 2;         // [UB] unit info
-    static constexpr uint32_t qs_off = info_off + UB * 32;                     // [NG][RMAX][2][D/8][4] f32
-    static constexpr uint32_t ps_off = qs_off + NG * RMAX * D * 4;             // [NCW][8][RMAX]
-    static constexpr uint32_t ml_off = ps_off + NCW * 8 * RMAX * 4;            // [3][NCW][RMAX] m, l, weight
+    static constexpr uint32_t qs_off = info_off + UB * 32;                     // [NG][RMAX][D] f32
+    static constexpr uint32_t ml_off = qs_off + NG * RMAX * D * 4;             // [3][NCW][RMAX] m, l, weight
     static constexpr int MRB = RMAX < 8 ? RMAX : 8;                            // rows per merge round
     static constexpr uint32_t obuf_off = ml_off + 3 * NCW * RMAX * 4;         // [NG][8 warps][MRB][D] f32
     static constexpr uint32_t fin_off = obuf_off + NG * 8 * MRB * D * 4;       // [NG][4][RMAX] M, L, 1/L, row
@@ -563,12 +561,28 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
         prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
         prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * D * 2, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
-        // Group g takes the CTA's units g, g + NG, ... whole.
+        // Group g takes the CTA's units g, g + NG, ... whole; warp lw of the
+        // group takes tokens 8 lw .. 8 lw + 7 of every tile.  Lane layout:
+        //   part = lane & 7   owns the head dims of 16-byte chunks part,
+        //                     part + 8, ... (DP dims; 8 lanes read 128
+        //                     contiguous bytes of a K or V row);
+        //   rg                row group: rows rg RL .. rg RL + RL - 1;
+        //   ts                token slot: token 8 lw + step TS + ts.
+        // A lane keeps its q rows and its share of the output rows in
+        // registers and works on fp32 pairs (f32x2 FMAs).  q.k is summed over
+        // the 8 part lanes by shuffles, so each of them holds its token's
+        // logits and computes the probabilities its p.v needs.
+        constexpr int DP = D / 8;                      // dims per lane
+        constexpr int NCH = DP / 8;                    // 16-byte chunks per lane and row
+        constexpr int NRG = RMAX <= 2 ? 1 : RMAX == 4 ? 2 : 4;
+        constexpr int RL = RMAX / NRG;                 // rows per lane
+        constexpr int TS = 4 / NRG;                    // token slots per step
+        constexpr int NSTEP = 8 / TS;                  // steps per tile
+        constexpr int SUB = RL >= 4 ? 2 : NSTEP < 4 ? NSTEP : 4;   // steps per maximum update
         const int cw = warp - 3;          // compute warp 0..NCW-1
         const int g = cw >> 3, lw = cw & 7;
-        const int tok = lane & 7, qtr = lane >> 3;
+        const int part = lane & 7, rg = (lane >> 3) % NRG, ts = (lane >> 3) / NRG;
         float *qs = reinterpret_cast<float *>(smem + C::qs_off) + g * RMAX * D;
-        float *ps = reinterpret_cast<float *>(smem + C::ps_off) + cw * 8 * RMAX;
         float *mw = reinterpret_cast<float *>(smem + C::ml_off) + g * 8 * RMAX;
         float *lwb = reinterpret_cast<float *>(smem + C::ml_off) + NCW * RMAX + g * 8 * RMAX;
         float *wts = reinterpret_cast<float *>(smem + C::ml_off) + 2 * NCW * RMAX + g * 8 * RMAX;
@@ -591,21 +605,32 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 KPROF(a, 2000 + 8 * i + 3);
             const int R = ui.R;
             const __nv_bfloat16 *qst = reinterpret_cast<const __nv_bfloat16 *>(smem + C::qst_off) + ub * RMAX * D;
-            // qs[r]: the 16-byte chunks' first halves, then their second halves.
-            for (int x = gtid; x < RMAX * D; x += nthr) {
-                const int r = x / D, e = x - r * D;
-                qs[r * D + ((e >> 2) & 1) * (D / 2) + (e >> 3) * 4 + (e & 3)] =
-                    x < R * D ? __bfloat162float(qst[x]) * a.scale_log2 : 0.f;
-            }
+            // qs[r][e]: q pre-scaled by scale * log2 e; rows past R are 0.
+            for (int x = gtid; x < RMAX * D; x += nthr)
+                qs[x] = x < R * D ? __bfloat162float(qst[x]) * a.scale_log2 : 0.f;
             tc::named_sync(bar_id, nthr);
-            float m_run[RMAX], l_run[RMAX], o_acc[RMAX][E];
+            float2 qv[RL][NCH * 4];
 #pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                m_run[r] = -INFINITY;
-                l_run[r] = 0.f;
+            for (int rl = 0; rl < RL; ++rl)
 #pragma unroll
-                for (int e = 0; e < E; ++e)
-                    o_acc[r][e] = 0.f;
+                for (int c = 0; c < NCH; ++c) {
+                    const float *qp = qs + (rg * RL + rl) * D + (part + 8 * c) * 8;
+                    const float4 a0 = *reinterpret_cast<const float4 *>(qp);
+                    const float4 a1 = *reinterpret_cast<const float4 *>(qp + 4);
+                    qv[rl][4 * c + 0] = make_float2(a0.x, a0.y);
+                    qv[rl][4 * c + 1] = make_float2(a0.z, a0.w);
+                    qv[rl][4 * c + 2] = make_float2(a1.x, a1.y);
+                    qv[rl][4 * c + 3] = make_float2(a1.z, a1.w);
+                }
+            float m_run[RL], l_run[RL];
+            float2 o_acc[RL][NCH * 4];
+#pragma unroll
+            for (int rl = 0; rl < RL; ++rl) {
+                m_run[rl] = -INFINITY;
+                l_run[rl] = 0.f;
+#pragma unroll
+                for (int e = 0; e < NCH * 4; ++e)
+                    o_acc[rl][e] = make_float2(0.f, 0.f);
             }
             bool tile_ok = true;
             for (int t = 0; t < ui.ntiles; ++t) {
@@ -620,95 +645,96 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     KPROF(a, 2100 + 8 * sq + 2);
                 const uint8_t *Ks = smem + C::stage_off + (size_t)(st * 2) * C::op_bytes;
                 const uint8_t *Vs = Ks + C::op_bytes;
-                const int row = lw * 8 + tok;
-                // q.k over this lane's quarter of head_dim, all rows.
-                float s[RMAX];
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r)
-                    s[r] = 0.f;
+                for (int s0 = 0; s0 < NSTEP; s0 += SUB) {
+                    // Logits of the lane's rows for the SUB tokens of its slot.
+                    float sv[SUB][RL];
 #pragma unroll
-                for (int c4 = 0; c4 < QCH; ++c4) {
-                    const int lc = (qtr * QCH + c4 + tok) & (D / 8 - 1);
-                    const uint4 kw = *reinterpret_cast<const uint4 *>(Ks + row * (D * 2) + lc * 16);
-                    const float2 k01 = bf16x2_to_float2(kw.x), k23 = bf16x2_to_float2(kw.y);
-                    const float2 k45 = bf16x2_to_float2(kw.z), k67 = bf16x2_to_float2(kw.w);
+                    for (int s = 0; s < SUB; ++s) {
+                        const int tok = lw * 8 + (s0 + s) * TS + ts;
+                        float2 acc[RL];
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r) {
-                        if (r < R) {
-                            const float *qp = qs + r * D + lc * 4;
-                            const float4 qa = *reinterpret_cast<const float4 *>(qp);
-                            const float4 qb4 = *reinterpret_cast<const float4 *>(qp + D / 2);
-                            float acc0 = fmaf(qa.x, k01.x, s[r]);
-                            float acc1 = qb4.x * k45.x;
-                            acc0 = fmaf(qa.y, k01.y, acc0);
-                            acc1 = fmaf(qb4.y, k45.y, acc1);
-                            acc0 = fmaf(qa.z, k23.x, acc0);
-                            acc1 = fmaf(qb4.z, k67.x, acc1);
-                            acc0 = fmaf(qa.w, k23.y, acc0);
-                            acc1 = fmaf(qb4.w, k67.y, acc1);
-                            s[r] = acc0 + acc1;
+                        for (int rl = 0; rl < RL; ++rl)
+                            acc[rl] = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c) {
+                            const uint4 kw =
+                                *reinterpret_cast<const uint4 *>(Ks + tok * (D * 2) + (part + 8 * c) * 16);
+                            const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
+                            const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
+#pragma unroll
+                            for (int rl = 0; rl < RL; ++rl) {
+                                acc[rl] = ffma2(qv[rl][4 * c + 0], k0, acc[rl]);
+                                acc[rl] = ffma2(qv[rl][4 * c + 1], k1, acc[rl]);
+                                acc[rl] = ffma2(qv[rl][4 * c + 2], k2, acc[rl]);
+                                acc[rl] = ffma2(qv[rl][4 * c + 3], k3, acc[rl]);
+                            }
+                        }
+                        const uint32_t mrow = meta[st * kTile + tok];
+#pragma unroll
+                        for (int rl = 0; rl < RL; ++rl) {
+                            float v = acc[rl].x + acc[rl].y;
+                            v += __shfl_xor_sync(0xffffffffu, v, 1);
+                            v += __shfl_xor_sync(0xffffffffu, v, 2);
+                            v += __shfl_xor_sync(0xffffffffu, v, 4);
+                            sv[s][rl] = ((mrow >> (rg * RL + rl)) & 1u) ? v : -INFINITY;
                         }
                     }
-                }
-                if (gtid == 0 && g == 0 && sq < 16)
-                    KPROF(a, 2100 + 8 * sq + 4);
-                const uint32_t rmask = meta[st * kTile + row];
+                    // Running maximum over the warp's tokens (the slot lanes
+                    // differ in lane bits 3 + log2 NRG and up), rescale, and
+                    // the probabilities.
 #pragma unroll
-                for (int r = 0; r < RMAX; ++r) {
-                    if (r < R) {
-                        float v = s[r];
-                        v += __shfl_xor_sync(0xffffffffu, v, 8);
-                        v += __shfl_xor_sync(0xffffffffu, v, 16);
-                        v = ((rmask >> r) & 1u) ? v : -INFINITY;
-                        float mx = v;
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                        const float mnew = fmaxf(m_run[r], mx);
-                        float pr = 0.f, alpha = 1.f;
+                    for (int rl = 0; rl < RL; ++rl) {
+                        float mx = sv[0][rl];
+#pragma unroll
+                        for (int s = 1; s < SUB; ++s)
+                            mx = fmaxf(mx, sv[s][rl]);
+#pragma unroll
+                        for (int o = 8 * NRG; o < 32; o <<= 1)
+                            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                        const float mnew = fmaxf(m_run[rl], mx);
                         if (mnew != -INFINITY) {
-                            alpha = tc::ex2(m_run[r] - mnew);
-                            pr = tc::ex2(v - mnew);
+                            if (mnew > m_run[rl]) {
+                                const float alpha = tc::ex2(m_run[rl] - mnew);
+                                l_run[rl] *= alpha;
+#pragma unroll
+                                for (int e = 0; e < NCH * 4; ++e) {
+                                    o_acc[rl][e].x *= alpha;
+                                    o_acc[rl][e].y *= alpha;
+                                }
+                            }
+#pragma unroll
+                            for (int s = 0; s < SUB; ++s) {
+                                const float pr = tc::ex2(sv[s][rl] - mnew);
+                                sv[s][rl] = pr;
+                                l_run[rl] += pr;
+                            }
+                        } else {
+#pragma unroll
+                            for (int s = 0; s < SUB; ++s)
+                                sv[s][rl] = 0.f;
                         }
-                        m_run[r] = mnew;
-                        l_run[r] = l_run[r] * alpha + (qtr == 0 ? pr : 0.f);
-#pragma unroll
-                        for (int e = 0; e < E; ++e)
-                            o_acc[r][e] *= alpha;
-                        if (qtr == (r & 3))
-                            ps[tok * RMAX + r] = pr;
+                        m_run[rl] = mnew;
                     }
-                }
-                __syncwarp();
-                if (gtid == 0 && g == 0 && sq < 16)
-                    KPROF(a, 2100 + 8 * sq + 5);
-                // p.v over the warp's 8 tokens (p = 0 for masked and absent
-                // tokens, whose V rows are finite or zero).
+                    // p.v (p = 0 for masked and absent tokens, whose V rows
+                    // are finite or zero).
 #pragma unroll
-                for (int tt = 0; tt < 8; ++tt) {
-                    const int rt = lw * 8 + tt;
-                    float vf[E];
-                    const uint8_t *vp = Vs + rt * (D * 2) + lane * E * 2;
-                    if constexpr (E == 4) {
-                        const uint2 vw = *reinterpret_cast<const uint2 *>(vp);
-                        const float2 a01 = bf16x2_to_float2(vw.x), a23 = bf16x2_to_float2(vw.y);
-                        vf[0] = a01.x;
-                        vf[1] = a01.y;
-                        vf[2] = a23.x;
-                        vf[3] = a23.y;
-                    } else {
-                        const float2 a01 = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(vp));
-                        vf[0] = a01.x;
-                        vf[1] = a01.y;
-                    }
-                    const float *pp = ps + tt * RMAX;
+                    for (int s = 0; s < SUB; ++s) {
+                        const int tok = lw * 8 + (s0 + s) * TS + ts;
 #pragma unroll
-                    for (int r = 0; r < RMAX; ++r) {
-                        if (r < R) {
-                            const float pr = pp[r];
+                        for (int c = 0; c < NCH; ++c) {
+                            const uint4 vw =
+                                *reinterpret_cast<const uint4 *>(Vs + tok * (D * 2) + (part + 8 * c) * 16);
+                            const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
+                            const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
 #pragma unroll
-                            for (int e = 0; e < E; ++e)
-                                o_acc[r][e] = fmaf(pr, vf[e], o_acc[r][e]);
+                            for (int rl = 0; rl < RL; ++rl) {
+                                const float2 pp = make_float2(sv[s][rl], sv[s][rl]);
+                                o_acc[rl][4 * c + 0] = ffma2(pp, v0, o_acc[rl][4 * c + 0]);
+                                o_acc[rl][4 * c + 1] = ffma2(pp, v1, o_acc[rl][4 * c + 1]);
+                                o_acc[rl][4 * c + 2] = ffma2(pp, v2, o_acc[rl][4 * c + 2]);
+                                o_acc[rl][4 * c + 3] = ffma2(pp, v3, o_acc[rl][4 * c + 3]);
+                            }
                         }
                     }
                 }
@@ -722,21 +748,30 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 if (!*err) *err = 109;
                 break;
             }
+            // The warp's state per row: sums over its token slots (lanes that
+            // differ in the slot bits), the same on all part lanes.
+#pragma unroll
+            for (int rl = 0; rl < RL; ++rl) {
+#pragma unroll
+                for (int o = 8 * NRG; o < 32; o <<= 1) {
+                    l_run[rl] += __shfl_xor_sync(0xffffffffu, l_run[rl], o);
+#pragma unroll
+                    for (int e = 0; e < NCH * 4; ++e) {
+                        o_acc[rl][e].x += __shfl_xor_sync(0xffffffffu, o_acc[rl][e].x, o);
+                        o_acc[rl][e].y += __shfl_xor_sync(0xffffffffu, o_acc[rl][e].y, o);
+                    }
+                }
+                const int r = rg * RL + rl;
+                if (ts == 0 && part == 0 && r < R) {
+                    mw[lw * RMAX + r] = m_run[rl];
+                    lwb[lw * RMAX + r] = l_run[rl];
+                }
+            }
+            tc::named_sync(bar_id, nthr);
             // Merge the 8 warp states of the unit's rows, in a fixed order (the
             // step is bitwise repeatable): per row the max M over the warps,
             // each warp's weight 2^(m_w - M) / L, then each output element as
             // the weighted sum of the 8 warps' values, in rounds of MRB rows.
-#pragma unroll
-            for (int r = 0; r < RMAX; ++r) {
-                if (r < R) {
-                    const float lt = warp_sum(l_run[r]);
-                    if (lane == 0) {
-                        mw[lw * RMAX + r] = m_run[r];
-                        lwb[lw * RMAX + r] = lt;
-                    }
-                }
-            }
-            tc::named_sync(bar_id, nthr);
             if (gtid < R) {
                 float M = -INFINITY;
 #pragma unroll
@@ -767,15 +802,22 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     break;
                 if (rb > 0)
                     tc::named_sync(bar_id, nthr);   // the previous round's reads are done
+                if (ts == 0) {
 #pragma unroll
-                for (int r = 0; r < C::MRB; ++r) {
-                    if (rb + r < R) {
-                        float *dst = obuf + (lw * C::MRB + r) * D + lane * E;
-                        if constexpr (E == 4)
-                            *reinterpret_cast<float4 *>(dst) =
-                                make_float4(o_acc[rb + r][0], o_acc[rb + r][1], o_acc[rb + r][2], o_acc[rb + r][3]);
-                        else
-                            *reinterpret_cast<float2 *>(dst) = make_float2(o_acc[rb + r][0], o_acc[rb + r][1]);
+                    for (int rl = 0; rl < RL; ++rl) {
+                        const int r = rg * RL + rl;
+                        if (r >= rb && r < rb + C::MRB && r < R) {
+#pragma unroll
+                            for (int c = 0; c < NCH; ++c) {
+                                float *dst = obuf + (lw * C::MRB + (r - rb)) * D + (part + 8 * c) * 8;
+                                *reinterpret_cast<float4 *>(dst) =
+                                    make_float4(o_acc[rl][4 * c + 0].x, o_acc[rl][4 * c + 0].y,
+                                                o_acc[rl][4 * c + 1].x, o_acc[rl][4 * c + 1].y);
+                                *reinterpret_cast<float4 *>(dst + 4) =
+                                    make_float4(o_acc[rl][4 * c + 2].x, o_acc[rl][4 * c + 2].y,
+                                                o_acc[rl][4 * c + 3].x, o_acc[rl][4 * c + 3].y);
+                            }
+                        }
                     }
                 }
                 tc::named_sync(bar_id, nthr);

@@ -40,17 +40,49 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-// Packed fp32 pair fused multiply-add (one f32x2 instruction): a * b + c
-// element-wise, each element rounded once as by fmaf.
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+// Packed fp32 pairs: two floats in one 64-bit register (element 0 in the
+// low word, as in memory), operated on by the f32x2 instructions, each
+// element rounded once as by the scalar instruction.
+using f32x2 = unsigned long long;
+__device__ __forceinline__ f32x2 f2_pack(float x, float y)
 {
-    float2 d;
-    asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
-        "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%6, %7};\n\t"
-        "fma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    f32x2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(x), "f"(y));
+    return r;
+}
+__device__ __forceinline__ float2 f2_unpack(f32x2 v)
+{
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
     return d;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// bf16 pair packed in a 32-bit word -> packed fp32 pair (exact).
+__device__ __forceinline__ f32x2 bf16x2_to_f2(uint32_t w)
+{
+    f32x2 r;
+    asm("{\n\t.reg .b32 lo, hi;\n\tshl.b32 lo, %1, 16;\n\tand.b32 hi, %1, 0xffff0000;\n\t"
+        "mov.b64 %0, {lo, hi};\n\t}"
+        : "=l"(r)
+        : "r"(w));
+    return r;
 }
 
 // bf16 pair packed in a 32-bit word -> two floats (exact).

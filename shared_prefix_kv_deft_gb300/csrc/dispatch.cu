@@ -26,13 +26,23 @@ struct Launch {
     int bucket;
     int32_t off;   // first item of the bucket
     int32_t n;     // items
-    double cost;   // estimated SM time (KV tokens x KV heads x relative cost per token)
+    double cost;   // estimated SM time (KV tokens x KV heads x time per token)
 };
 
-// Relative SM time per KV token of a CUDA-core item by row bucket: up to 4
-// rows the kernel streams at the memory rate; above, the per-row FMA work
-// outgrows it (16 rows x 2 d FMAs per 4 d bytes).
-double fma_weight(int bucket) { return bucket <= 2 ? 1.0 : bucket == 3 ? 2.5 : 5.0; }
+// Estimated SM time per KV token and KV head (ns, with every SM streaming):
+// CUDA-core items by row bucket (up to 2 rows the kernel streams at the
+// memory rate; above, the per-row FMA work sets the pace), tensor-core items
+// by column bucket (the softmax over the item's columns grows with them).
+double fma_ns_per_token(int bucket)
+{
+    static const double ns[5] = {10.0, 12.0, 16.0, 32.0, 56.0};
+    return ns[bucket];
+}
+double mma_ns_per_token(int bucket)
+{
+    static const double ns[4] = {18.0, 18.0, 22.0, 28.0};
+    return ns[bucket];
+}
 
 }  // namespace
 
@@ -53,6 +63,10 @@ void shape_launches(const double *cost, const int32_t *units, int n, int sms, La
         const double share = total > 0.0 ? 1.25 * sms * cost[i] / total : 1.0;
         int g = (int)std::ceil(share);
         g = std::max(1, std::min({g, (int)units[i], sms}));
+        // No more CTAs than the rounds of units need: ceil(units / g)
+        // rounds take as long with ceil(units / rounds) CTAs.
+        const int rounds = (int)((units[i] + g - 1) / g);
+        g = (int)((units[i] + rounds - 1) / rounds);
         out[i] = LaunchShape{g, g};
         used += g;
     }
@@ -83,14 +97,15 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
         for (int b = 0; b < 4; ++b) {
             const int32_t c = hp.mma_bucket_off[b + 1] - hp.mma_bucket_off[b];
             if (c > 0)
-                ls[n++] = Launch{0, b, hp.mma_bucket_off[b], c, (double)hp.mma_bucket_tok[b] * hkv};
+                ls[n++] = Launch{0, b, hp.mma_bucket_off[b], c,
+                                 (double)hp.mma_bucket_tok[b] * hkv * mma_ns_per_token(b)};
         }
     }
     auto add_fma = [&](int kind, const std::array<int32_t, 6> &off, const std::array<int64_t, 5> &tok) {
         for (int b = 0; b < 5; ++b) {
             const int32_t c = off[b + 1] - off[b];
             if (c > 0)
-                ls[n++] = Launch{kind, b, off[b], c, (double)tok[b] * hkv * fma_weight(b)};
+                ls[n++] = Launch{kind, b, off[b], c, (double)tok[b] * hkv * fma_ns_per_token(b)};
         }
     };
     // The tensor-core path covers head_dim 128; other head sizes, or a run

@@ -71,7 +71,7 @@ constexpr uint32_t fma_fixed_bytes(int NG)
 
 template <int D, int RMAX>
 struct FmaCfg {
-    static constexpr int NG = RMAX <= 2 ? 2 : 1;       // compute groups
+    static constexpr int NG = RMAX <= 4 ? 2 : 1;       // compute groups
     static constexpr int NCW = 8 * NG;                 // compute warps
     static constexpr int THREADS = 32 * (NCW + 3);     // + metadata warp + two copy warps
     // Stages in the ring: as many as fit next to the fixed buffers, at most 6
@@ -609,28 +609,28 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             for (int x = gtid; x < RMAX * D; x += nthr)
                 qs[x] = x < R * D ? __bfloat162float(qst[x]) * a.scale_log2 : 0.f;
             tc::named_sync(bar_id, nthr);
-            float2 qv[RL][NCH * 4];
+            f32x2 qv[RL][NCH * 4];
 #pragma unroll
             for (int rl = 0; rl < RL; ++rl)
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
                     const float *qp = qs + (rg * RL + rl) * D + (part + 8 * c) * 8;
-                    const float4 a0 = *reinterpret_cast<const float4 *>(qp);
-                    const float4 a1 = *reinterpret_cast<const float4 *>(qp + 4);
-                    qv[rl][4 * c + 0] = make_float2(a0.x, a0.y);
-                    qv[rl][4 * c + 1] = make_float2(a0.z, a0.w);
-                    qv[rl][4 * c + 2] = make_float2(a1.x, a1.y);
-                    qv[rl][4 * c + 3] = make_float2(a1.z, a1.w);
+                    const ulonglong2 a0 = *reinterpret_cast<const ulonglong2 *>(qp);
+                    const ulonglong2 a1 = *reinterpret_cast<const ulonglong2 *>(qp + 4);
+                    qv[rl][4 * c + 0] = a0.x;
+                    qv[rl][4 * c + 1] = a0.y;
+                    qv[rl][4 * c + 2] = a1.x;
+                    qv[rl][4 * c + 3] = a1.y;
                 }
             float m_run[RL], l_run[RL];
-            float2 o_acc[RL][NCH * 4];
+            f32x2 o_acc[RL][NCH * 4];
 #pragma unroll
             for (int rl = 0; rl < RL; ++rl) {
                 m_run[rl] = -INFINITY;
                 l_run[rl] = 0.f;
 #pragma unroll
                 for (int e = 0; e < NCH * 4; ++e)
-                    o_acc[rl][e] = make_float2(0.f, 0.f);
+                    o_acc[rl][e] = 0ull;   // (+0, +0)
             }
             bool tile_ok = true;
             for (int t = 0; t < ui.ntiles; ++t) {
@@ -652,28 +652,29 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                     for (int s = 0; s < SUB; ++s) {
                         const int tok = lw * 8 + (s0 + s) * TS + ts;
-                        float2 acc[RL];
+                        f32x2 acc[RL];
 #pragma unroll
                         for (int rl = 0; rl < RL; ++rl)
-                            acc[rl] = make_float2(0.f, 0.f);
+                            acc[rl] = 0ull;
 #pragma unroll
                         for (int c = 0; c < NCH; ++c) {
                             const uint4 kw =
                                 *reinterpret_cast<const uint4 *>(Ks + tok * (D * 2) + (part + 8 * c) * 16);
-                            const float2 k0 = bf16x2_to_float2(kw.x), k1 = bf16x2_to_float2(kw.y);
-                            const float2 k2 = bf16x2_to_float2(kw.z), k3 = bf16x2_to_float2(kw.w);
+                            const f32x2 k0 = bf16x2_to_f2(kw.x), k1 = bf16x2_to_f2(kw.y);
+                            const f32x2 k2 = bf16x2_to_f2(kw.z), k3 = bf16x2_to_f2(kw.w);
 #pragma unroll
                             for (int rl = 0; rl < RL; ++rl) {
-                                acc[rl] = ffma2(qv[rl][4 * c + 0], k0, acc[rl]);
-                                acc[rl] = ffma2(qv[rl][4 * c + 1], k1, acc[rl]);
-                                acc[rl] = ffma2(qv[rl][4 * c + 2], k2, acc[rl]);
-                                acc[rl] = ffma2(qv[rl][4 * c + 3], k3, acc[rl]);
+                                acc[rl] = f2_fma(qv[rl][4 * c + 0], k0, acc[rl]);
+                                acc[rl] = f2_fma(qv[rl][4 * c + 1], k1, acc[rl]);
+                                acc[rl] = f2_fma(qv[rl][4 * c + 2], k2, acc[rl]);
+                                acc[rl] = f2_fma(qv[rl][4 * c + 3], k3, acc[rl]);
                             }
                         }
                         const uint32_t mrow = meta[st * kTile + tok];
 #pragma unroll
                         for (int rl = 0; rl < RL; ++rl) {
-                            float v = acc[rl].x + acc[rl].y;
+                            const float2 a2 = f2_unpack(acc[rl]);
+                            float v = a2.x + a2.y;
                             v += __shfl_xor_sync(0xffffffffu, v, 1);
                             v += __shfl_xor_sync(0xffffffffu, v, 2);
                             v += __shfl_xor_sync(0xffffffffu, v, 4);
@@ -694,15 +695,13 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                         const float mnew = fmaxf(m_run[rl], mx);
                         if (mnew != -INFINITY) {
-                            if (mnew > m_run[rl]) {
-                                const float alpha = tc::ex2(m_run[rl] - mnew);
-                                l_run[rl] *= alpha;
+                            // (m_run may be -inf: alpha = 0 then, on zero sums)
+                            const float alpha = mnew > m_run[rl] ? tc::ex2(m_run[rl] - mnew) : 1.f;
+                            l_run[rl] *= alpha;
+                            const f32x2 aa = f2_pack(alpha, alpha);
 #pragma unroll
-                                for (int e = 0; e < NCH * 4; ++e) {
-                                    o_acc[rl][e].x *= alpha;
-                                    o_acc[rl][e].y *= alpha;
-                                }
-                            }
+                            for (int e = 0; e < NCH * 4; ++e)
+                                o_acc[rl][e] = f2_mul(o_acc[rl][e], aa);
 #pragma unroll
                             for (int s = 0; s < SUB; ++s) {
                                 const float pr = tc::ex2(sv[s][rl] - mnew);
@@ -725,15 +724,15 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         for (int c = 0; c < NCH; ++c) {
                             const uint4 vw =
                                 *reinterpret_cast<const uint4 *>(Vs + tok * (D * 2) + (part + 8 * c) * 16);
-                            const float2 v0 = bf16x2_to_float2(vw.x), v1 = bf16x2_to_float2(vw.y);
-                            const float2 v2 = bf16x2_to_float2(vw.z), v3 = bf16x2_to_float2(vw.w);
+                            const f32x2 v0 = bf16x2_to_f2(vw.x), v1 = bf16x2_to_f2(vw.y);
+                            const f32x2 v2 = bf16x2_to_f2(vw.z), v3 = bf16x2_to_f2(vw.w);
 #pragma unroll
                             for (int rl = 0; rl < RL; ++rl) {
-                                const float2 pp = make_float2(sv[s][rl], sv[s][rl]);
-                                o_acc[rl][4 * c + 0] = ffma2(pp, v0, o_acc[rl][4 * c + 0]);
-                                o_acc[rl][4 * c + 1] = ffma2(pp, v1, o_acc[rl][4 * c + 1]);
-                                o_acc[rl][4 * c + 2] = ffma2(pp, v2, o_acc[rl][4 * c + 2]);
-                                o_acc[rl][4 * c + 3] = ffma2(pp, v3, o_acc[rl][4 * c + 3]);
+                                const f32x2 pp = f2_pack(sv[s][rl], sv[s][rl]);
+                                o_acc[rl][4 * c + 0] = f2_fma(pp, v0, o_acc[rl][4 * c + 0]);
+                                o_acc[rl][4 * c + 1] = f2_fma(pp, v1, o_acc[rl][4 * c + 1]);
+                                o_acc[rl][4 * c + 2] = f2_fma(pp, v2, o_acc[rl][4 * c + 2]);
+                                o_acc[rl][4 * c + 3] = f2_fma(pp, v3, o_acc[rl][4 * c + 3]);
                             }
                         }
                     }
@@ -756,10 +755,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 for (int o = 8 * NRG; o < 32; o <<= 1) {
                     l_run[rl] += __shfl_xor_sync(0xffffffffu, l_run[rl], o);
 #pragma unroll
-                    for (int e = 0; e < NCH * 4; ++e) {
-                        o_acc[rl][e].x += __shfl_xor_sync(0xffffffffu, o_acc[rl][e].x, o);
-                        o_acc[rl][e].y += __shfl_xor_sync(0xffffffffu, o_acc[rl][e].y, o);
-                    }
+                    for (int e = 0; e < NCH * 4; ++e)
+                        o_acc[rl][e] = f2_add(o_acc[rl][e], __shfl_xor_sync(0xffffffffu, o_acc[rl][e], o));
                 }
                 const int r = rg * RL + rl;
                 if (ts == 0 && part == 0 && r < R) {
@@ -810,12 +807,10 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                             for (int c = 0; c < NCH; ++c) {
                                 float *dst = obuf + (lw * C::MRB + (r - rb)) * D + (part + 8 * c) * 8;
-                                *reinterpret_cast<float4 *>(dst) =
-                                    make_float4(o_acc[rl][4 * c + 0].x, o_acc[rl][4 * c + 0].y,
-                                                o_acc[rl][4 * c + 1].x, o_acc[rl][4 * c + 1].y);
-                                *reinterpret_cast<float4 *>(dst + 4) =
-                                    make_float4(o_acc[rl][4 * c + 2].x, o_acc[rl][4 * c + 2].y,
-                                                o_acc[rl][4 * c + 3].x, o_acc[rl][4 * c + 3].y);
+                                *reinterpret_cast<ulonglong2 *>(dst) =
+                                    make_ulonglong2(o_acc[rl][4 * c + 0], o_acc[rl][4 * c + 1]);
+                                *reinterpret_cast<ulonglong2 *>(dst + 4) =
+                                    make_ulonglong2(o_acc[rl][4 * c + 2], o_acc[rl][4 * c + 3]);
                             }
                         }
                     }

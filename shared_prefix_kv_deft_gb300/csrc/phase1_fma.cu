@@ -64,16 +64,16 @@ constexpr int kPageList = 512;  // page ids staged per item (larger items look p
 template <int D, int RMAX>
 constexpr uint32_t fma_fixed_bytes(int NG)
 {
-    return 2 * NG * RMAX * D * 2 + 2 * NG * 32 + NG * RMAX * D * 4 + 3 * 8 * NG * RMAX * 4 + NG * 8 * (RMAX < 8 ? RMAX : 8) * D * 4 + NG * 4 * RMAX * 4 +
+    return 2 * NG * RMAX * D * 2 + 2 * NG * 32 + NG * RMAX * D * 4 + 3 * 8 * NG * RMAX * 4 + NG * 8 * (RMAX < 8 ? RMAX : 8) * D * 4 +
            2 * kMaxSegsPerChunk * 20 +
-           2 * kPageList * 4 + 2 * 16 + 64 + 384 + 1024;
+           2 * kPageList * 4 + 2 * 16 + 64 + 384 + 1024 + NG * 16 + 2 * NG * 8;
 }
 
 template <int D, int RMAX>
 struct FmaCfg {
     static constexpr int NG = RMAX <= 4 ? 2 : 1;       // compute groups
     static constexpr int NCW = 8 * NG;                 // compute warps
-    static constexpr int THREADS = 32 * (NCW + 3);     // + metadata warp + two copy warps
+    static constexpr int THREADS = 32 * (NCW + 4);     // + metadata, two copy and a merge warp
     // Stages in the ring: as many as fit next to the fixed buffers, at most 6
     // and even: two groups get half each; one group's ring is filled by the two
     // copy warps alternately (copy warp w always serves the stages of parity w).
@@ -92,13 +92,13 @@ struct FmaCfg {
     static constexpr uint32_t ml_off = qs_off + NG * RMAX * D * 4;             // [3][NCW][RMAX] m, l, weight
     static constexpr int MRB = RMAX < 8 ? RMAX : 8;                            // rows per merge round
     static constexpr uint32_t obuf_off = ml_off + 3 * NCW * RMAX * 4;         // [NG][8 warps][MRB][D] f32
-    static constexpr uint32_t fin_off = obuf_off + NG * 8 * MRB * D * 4;       // [NG][4][RMAX] M, L, 1/L, row
-    static constexpr uint32_t seg_off = fin_off + NG * 4 * RMAX * 4;           // [2][5][256]
+    static constexpr uint32_t mdesc_off = obuf_off + NG * 8 * MRB * D * 4;     // [NG] MergeDesc
+    static constexpr uint32_t seg_off = mdesc_off + NG * 16;                   // [2][5][256]
     static constexpr uint32_t pl_off = seg_off + 2 * kMaxSegsPerChunk * 20;    // [2][kPageList]
     static constexpr uint32_t iinfo_off = pl_off + 2 * kPageList * 4;          // [2] ItemInfo
     static constexpr uint32_t useq_off = iinfo_off + 2 * 16;                    // [UQ] unit numbers, error and queue flags
     static constexpr uint32_t bar_off = useq_off + 16 * 4;
-    static constexpr uint32_t nbars = 2 * ST + 2 * UB + 4 + 2 * 8;
+    static constexpr uint32_t nbars = 2 * ST + 2 * UB + 4 + 2 * 8 + 2 * NG;
     static constexpr uint32_t total = bar_off + nbars * 8;
     static constexpr uint32_t alloc = total + 1024;
     static_assert(alloc <= 227 * 1024, "shared memory of one CTA");
@@ -124,6 +124,13 @@ struct ItemInfo {
     int32_t npages;  // page-list entries of the item
 };
 
+// A compute group's states of one unit, handed to the merge warp: rows
+// rb .. rb + MRB - 1 of the unit (R rows, first slot cq0, KV head h); R < 0:
+// the group has finished.
+struct MergeDesc {
+    int32_t R, cq0, h, rb;
+};
+
 template <int D, int RMAX>
 __global__ void __launch_bounds__(FmaCfg<D, RMAX>::THREADS, 1)
 phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
@@ -147,10 +154,12 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     const int kFull = 0, kEmpty = ST, kUFull = 2 * ST, kUEmpty = 2 * ST + UB;
     const int kSFull = 2 * ST + 2 * UB, kSEmpty = kSFull + 2;
     const int kQFull = kSEmpty + 2, kQEmpty = kQFull + UQ;
+    const int kMFull = kQEmpty + UQ, kMEmpty = kMFull + NG;   // [NG] each: states written / read
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int Hkv = a.num_kv_heads, Hq = a.num_q_heads, G = a.gqa_group;
     ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + C::iinfo_off);
+    volatile MergeDesc *mdesc = reinterpret_cast<volatile MergeDesc *>(smem + C::mdesc_off);
     volatile int32_t *useq = reinterpret_cast<volatile int32_t *>(smem + C::useq_off);
     volatile int32_t *err = useq + UQ;
     // qdone[0]: this CTA has counted itself done with the queue; qdone[1]:
@@ -178,6 +187,10 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         for (int u = 0; u < UQ; ++u) {
             tc::mbar_init(fbar(bars, kQFull + u), 1);
             tc::mbar_init(fbar(bars, kQEmpty + u), 2);   // lane 0 of each copy warp
+        }
+        for (int g = 0; g < NG; ++g) {
+            tc::mbar_init(fbar(bars, kMFull + g), 1);
+            tc::mbar_init(fbar(bars, kMEmpty + g), 1);
         }
         *err = 0;
         qdone[0] = 0;
@@ -417,11 +430,15 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 if (nvalid == kTile && (tka % kPageSize) == 0 && seg_at(p0 + kTile - 1) == sga) {
                     // Fast path: four whole pages of one segment.
                     const int pg = lane < 4 ? page_of(sga, tka + kPageSize * lane) : -1;
+                    if (lane == 0 && ring == 0 && seq < 16)
+                        KPROF(a, 2100 + 8 * seq + 4);
                     if (seq >= RST &&
                         !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kEmpty + st), ((seq / RST) - 1) & 1))) {
                         ok = false;
                         break;
                     }
+                    if (lane == 0 && ring == 0 && seq < 16)
+                        KPROF(a, 2100 + 8 * seq + 5);
                     const uint32_t mrow = (uint32_t)seg[768 + sga];
                     meta[st * kTile + lane] = mrow;
                     meta[st * kTile + lane + 32] = mrow;
@@ -552,7 +569,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             const int last = seq - 1 - ((seq - 1 - s) % RST);
             tc::mbar_wait(fbar(bars, kFull + ring * RST + s), (last / RST) & 1);
         }
-    } else {
+    } else if (warp < 3 + NCW) {
         // ------------------------------------------------------------ compute
         // While the first tiles load: warm L2 with the plan's arrays, the
         // node page offsets and q, which the metadata and copy warps walk in
@@ -585,12 +602,10 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         float *qs = reinterpret_cast<float *>(smem + C::qs_off) + g * RMAX * D;
         float *mw = reinterpret_cast<float *>(smem + C::ml_off) + g * 8 * RMAX;
         float *lwb = reinterpret_cast<float *>(smem + C::ml_off) + NCW * RMAX + g * 8 * RMAX;
-        float *wts = reinterpret_cast<float *>(smem + C::ml_off) + 2 * NCW * RMAX + g * 8 * RMAX;
         float *obuf = reinterpret_cast<float *>(smem + C::obuf_off) + g * 8 * C::MRB * D;
-        float *fin = reinterpret_cast<float *>(smem + C::fin_off) + g * 4 * RMAX;   // M, L, 1/L, row
-        int32_t *fin_row = reinterpret_cast<int32_t *>(fin + 3 * RMAX);
         const uint32_t bar_id = 1 + (uint32_t)g, nthr = 256;
         const int gtid = tid - 96 - g * 256;   // thread index within the group
+        int mseq = 0;                          // states handed to the merge warp
         for (int i = g;; i += NG) {
             const int ub = i % UB;
             const bool okw = tc::mbar_wait(fbar(bars, kUFull + ub), (i / UB) & 1);
@@ -609,6 +624,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             for (int x = gtid; x < RMAX * D; x += nthr)
                 qs[x] = x < R * D ? __bfloat162float(qst[x]) * a.scale_log2 : 0.f;
             tc::named_sync(bar_id, nthr);
+            if (gtid == 0 && g == 0 && i < 16)
+                KPROF(a, 2300 + 4 * i + 3);
             f32x2 qv[RL][NCH * 4];
 #pragma unroll
             for (int rl = 0; rl < RL; ++rl)
@@ -740,6 +757,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 __syncwarp();
                 if (gtid == 0 && g == 0 && sq < 16)
                     KPROF(a, 2100 + 8 * sq + 3);
+                if (gtid == 7 * 32 && g == 0 && sq < 16)
+                    KPROF(a, 2100 + 8 * sq + 6);
                 if (lane == 0)
                     tc::mbar_arrive(fbar(bars, kEmpty + st));
             }
@@ -758,79 +777,142 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     for (int e = 0; e < NCH * 4; ++e)
                         o_acc[rl][e] = f2_add(o_acc[rl][e], __shfl_xor_sync(0xffffffffu, o_acc[rl][e], o));
                 }
-                const int r = rg * RL + rl;
-                if (ts == 0 && part == 0 && r < R) {
-                    mw[lw * RMAX + r] = m_run[rl];
-                    lwb[lw * RMAX + r] = l_run[rl];
-                }
             }
-            tc::named_sync(bar_id, nthr);
-            // Merge the 8 warp states of the unit's rows, in a fixed order (the
-            // step is bitwise repeatable): per row the max M over the warps,
-            // each warp's weight 2^(m_w - M) / L, then each output element as
-            // the weighted sum of the 8 warps' values, in rounds of MRB rows.
-            if (gtid < R) {
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < 8; ++w)
-                    M = fmaxf(M, mw[w * RMAX + gtid]);
-                float L = 0.f, c[8];
-#pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const float mwv = mw[w * RMAX + gtid];
-                    c[w] = (M == -INFINITY || mwv == -INFINITY) ? 0.f : tc::ex2(mwv - M);
-                    L += lwb[w * RMAX + gtid] * c[w];
-                }
-                const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-                for (int w = 0; w < 8; ++w)
-                    wts[w * RMAX + gtid] = c[w] * inv;
-                fin[gtid] = M;
-                fin[RMAX + gtid] = L;
-                fin_row[gtid] = (ui.cq0 + gtid / G) * Hq + ui.h * G + (gtid % G);
-                if (L > 0.f)
-                    a.lse_part[fin_row[gtid]] = M + log2f(L);
-                else
-                    a.lse_part[fin_row[gtid]] = -INFINITY;
-            }
-#pragma unroll
-            for (int rb = 0; rb < RMAX; rb += C::MRB) {
-                if (rb >= R)
+            // Hand the states to the merge warp, MRB rows at a time, each
+            // time after it has read the previous ones; the group goes on
+            // with its next unit meanwhile.
+            bool merr = false;
+            if (gtid == 0 && g == 0 && i < 16)
+                KPROF(a, 2300 + 4 * i + 0);
+            for (int rb = 0; rb < R; rb += C::MRB) {
+                const bool okm = mseq == 0 || tc::mbar_wait(fbar(bars, kMEmpty + g), (mseq - 1) & 1);
+                if (gtid == 0 && g == 0 && i < 16 && rb == 0)
+                    KPROF(a, 2300 + 4 * i + 1);
+                if (tc::named_sync_or(bar_id, nthr, !okm)) {
+                    if (!*err) *err = 110;
+                    merr = true;
                     break;
-                if (rb > 0)
-                    tc::named_sync(bar_id, nthr);   // the previous round's reads are done
-                if (ts == 0) {
+                }
 #pragma unroll
-                    for (int rl = 0; rl < RL; ++rl) {
-                        const int r = rg * RL + rl;
-                        if (r >= rb && r < rb + C::MRB && r < R) {
+                for (int rl = 0; rl < RL; ++rl) {
+                    const int r = rg * RL + rl;
+                    if (rb == 0 && ts == 0 && part == 0 && r < R) {
+                        mw[lw * RMAX + r] = m_run[rl];
+                        lwb[lw * RMAX + r] = l_run[rl];
+                    }
+                    if (ts == 0 && r >= rb && r < rb + C::MRB && r < R) {
 #pragma unroll
-                            for (int c = 0; c < NCH; ++c) {
-                                float *dst = obuf + (lw * C::MRB + (r - rb)) * D + (part + 8 * c) * 8;
-                                *reinterpret_cast<ulonglong2 *>(dst) =
-                                    make_ulonglong2(o_acc[rl][4 * c + 0], o_acc[rl][4 * c + 1]);
-                                *reinterpret_cast<ulonglong2 *>(dst + 4) =
-                                    make_ulonglong2(o_acc[rl][4 * c + 2], o_acc[rl][4 * c + 3]);
-                            }
+                        for (int c = 0; c < NCH; ++c) {
+                            float *dst = obuf + (lw * C::MRB + (r - rb)) * D + (part + 8 * c) * 8;
+                            *reinterpret_cast<ulonglong2 *>(dst) =
+                                make_ulonglong2(o_acc[rl][4 * c + 0], o_acc[rl][4 * c + 1]);
+                            *reinterpret_cast<ulonglong2 *>(dst + 4) =
+                                make_ulonglong2(o_acc[rl][4 * c + 2], o_acc[rl][4 * c + 3]);
                         }
                     }
                 }
-                tc::named_sync(bar_id, nthr);
-                const int rows = R - rb < C::MRB ? R - rb : C::MRB;
-                for (int x = gtid; x < rows * D; x += nthr) {
-                    const int r = x / D, e = x - r * D;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int w = 0; w < 8; ++w)
-                        acc = fmaf(obuf[(w * C::MRB + r) * D + e], wts[w * RMAX + rb + r], acc);
-                    a.o_part[(size_t)fin_row[rb + r] * D + e] = acc;
+                if (gtid == 0) {
+                    mdesc[g].R = R;
+                    mdesc[g].cq0 = ui.cq0;
+                    mdesc[g].h = ui.h;
+                    mdesc[g].rb = rb;
                 }
+                tc::named_sync(bar_id, nthr);
+                if (gtid == 0 && g == 0 && i < 16 && rb == 0)
+                    KPROF(a, 2300 + 4 * i + 2);
+                if (gtid == 0)
+                    tc::mbar_arrive(fbar(bars, kMFull + g));
+                ++mseq;
             }
-            tc::named_sync(bar_id, nthr);
+            if (merr)
+                break;
             if (gtid == 0)
                 KPROF(a, 2000 + 8 * i + 4);
             if (lane == 0)
                 tc::mbar_arrive(fbar(bars, kUEmpty + ub));
+        }
+        // The group is done: tell the merge warp, once it has read the last
+        // states.
+        if (gtid == 0) {
+            if (mseq > 0 && !tc::mbar_wait(fbar(bars, kMEmpty + g), (mseq - 1) & 1))
+                if (!*err) *err = 110;
+            mdesc[g].R = -1;
+            tc::mbar_arrive(fbar(bars, kMFull + g));
+        }
+    } else {
+        // -------------------------------------------------------------- merge
+        // Merges each unit's 8 warp states per row in a fixed order (the step
+        // is bitwise repeatable): the max M over the warps, each warp's
+        // weight 2^(m_w - M) / L with L the weighted sum of the warps' sums,
+        // the lse partial M + log2 L, then each output element as the
+        // weighted sum of the warps' values (a lane takes 4 elements).
+        int ms[2] = {0, 0};
+        bool live[2] = {true, NG == 2};
+        uint32_t idle = 0;
+        while (live[0] || live[1]) {
+            bool any = false;
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {
+                if (!live[g] || !tc::mbar_test(fbar(bars, kMFull + g), ms[g] & 1))
+                    continue;
+                any = true;
+                const MergeDesc md{mdesc[g].R, mdesc[g].cq0, mdesc[g].h, mdesc[g].rb};
+                if (md.R < 0) {
+                    live[g] = false;
+                    continue;
+                }
+                const float *mw = reinterpret_cast<const float *>(smem + C::ml_off) + g * 8 * RMAX;
+                const float *lwb = mw + NCW * RMAX;
+                float *wts = reinterpret_cast<float *>(smem + C::ml_off) + 2 * NCW * RMAX + g * 8 * RMAX;
+                const float *obuf = reinterpret_cast<const float *>(smem + C::obuf_off) + g * 8 * C::MRB * D;
+                if (md.rb == 0 && lane < md.R) {
+                    float M = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        M = fmaxf(M, mw[w * RMAX + lane]);
+                    float L = 0.f, c[8];
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const float mwv = mw[w * RMAX + lane];
+                        c[w] = (M == -INFINITY || mwv == -INFINITY) ? 0.f : tc::ex2(mwv - M);
+                        L += lwb[w * RMAX + lane] * c[w];
+                    }
+                    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+                    for (int w = 0; w < 8; ++w)
+                        wts[w * RMAX + lane] = c[w] * inv;
+                    const size_t row = (size_t)(md.cq0 + lane / G) * Hq + md.h * G + (lane % G);
+                    a.lse_part[row] = L > 0.f ? M + log2f(L) : -INFINITY;
+                }
+                __syncwarp();
+                const int rows = md.R - md.rb < C::MRB ? md.R - md.rb : C::MRB;
+                for (int x = lane; x < rows * (D / 4); x += 32) {
+                    const int r = x / (D / 4), e4 = (x - r * (D / 4)) * 4;
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int w = 0; w < 8; ++w) {
+                        const float4 v = *reinterpret_cast<const float4 *>(obuf + (w * C::MRB + r) * D + e4);
+                        const float wt = wts[w * RMAX + md.rb + r];
+                        acc.x = fmaf(v.x, wt, acc.x);
+                        acc.y = fmaf(v.y, wt, acc.y);
+                        acc.z = fmaf(v.z, wt, acc.z);
+                        acc.w = fmaf(v.w, wt, acc.w);
+                    }
+                    const int rr = md.rb + r;
+                    const size_t row = (size_t)(md.cq0 + rr / G) * Hq + md.h * G + (rr % G);
+                    *reinterpret_cast<float4 *>(a.o_part + row * D + e4) = acc;
+                }
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(fbar(bars, kMEmpty + g));
+                ++ms[g];
+            }
+            if (any)
+                idle = 0;
+            else if (++idle > (1u << 24)) {
+                if (!*err) *err = 111;
+                break;
+            }
         }
     }
     if (tid == 96 && blockIdx.x < 256)

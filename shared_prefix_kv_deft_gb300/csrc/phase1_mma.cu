@@ -90,12 +90,13 @@ struct ItemInfo {
 template <int NPH>
 struct Smem {
     static constexpr int RP = 2 * NPH;
-    static constexpr int VST = NPH <= 32 ? 3 : 2;                    // V stages (K has 2)
+    static constexpr int VST = NPH <= 16 ? 3 : 2;                    // V stages (K has 2)
+    static constexpr int QB = NPH <= 32 ? 2 : 1;                     // Q^T buffers
     static constexpr uint32_t q_half = RP * 128;                     // one 64-wide half of Q^T
     static constexpr uint32_t k_off = 0;                             // [2] K operands
     static constexpr uint32_t v_off = k_off + 2 * kTileBytes;       // [VST] V operands
-    static constexpr uint32_t q_off = v_off + VST * kTileBytes;     // Q^T: [d half][RP rows][128 B]
-    static constexpr uint32_t p_off = q_off + 2 * q_half;           // P^T: [col block][128 tok][128 B]
+    static constexpr uint32_t q_off = v_off + VST * kTileBytes;     // [QB] Q^T: [d half][RP rows][128 B]
+    static constexpr uint32_t p_off = q_off + QB * 2 * q_half;      // P^T: [col block][128 tok][128 B]
     static constexpr uint32_t meta_off = p_off + (RP > 64 ? 2 : 1) * kHalf;  // [4 slots][128] uint4 row masks
     static constexpr uint32_t seg_off = meta_off + 4 * kTileTok * 16;  // [2][kSegInts]
     static constexpr uint32_t red_off = seg_off + 2 * kSegInts * 4;  // [wg][warp][64]
@@ -124,11 +125,13 @@ constexpr int kBarSegFull = 16;  // [2] an item's segment table written (32 lane
 constexpr int kBarSegEmpty = 18; // [2] ... no longer read (both producers, 32 lanes each)
 constexpr int kBarUFull = 20;    // [2] a unit's description and Q^T written (32 lanes)
 constexpr int kBarUEmpty = 22;   // [2] ... description read (MMA issuer + 2 warpgroups)
-constexpr int kBarQFree = 24;    // the unit's last S finished: Q^T may be replaced (MMA commit)
+constexpr int kBarQFree = 24;    // the unit's last S finished: its Q^T buffer may be replaced (MMA commit)
 constexpr int kBarOFree = 25;    // [2] O buffer read out by the epilogue (one per warpgroup)
 constexpr int kBarQFull = 27;    // [kUnitQueue] a unit number written (metadata lane 0)
 constexpr int kBarQEmpty = 35;   // [kUnitQueue] ... read (lane 0 of each producer)
-constexpr int kNumBars = 43;
+constexpr int kBarQFree1 = 43;   // ... the same for Q^T buffer 1
+constexpr int kNumBars = 44;
+__device__ __forceinline__ int qfree_bar(int qb) { return qb == 0 ? kBarQFree : kBarQFree1; }
 static_assert(kNumBars * 8 <= Smem<16>::misc_off - Smem<16>::bar_off, "mbarrier space");
 
 // Tensor maps over the paged K and V.  *1: the pool as [pages*Hkv*16 rows]
@@ -226,6 +229,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_init(bar(kBarOFree + i), 2);
         }
         tc::mbar_init(bar(kBarQFree), 1);
+        tc::mbar_init(bar(kBarQFree1), 1);
         for (int i = 0; i < UQ; ++i) {
             tc::mbar_init(bar(kBarQFull + i), 1);
             tc::mbar_init(bar(kBarQEmpty + i), 2);
@@ -252,8 +256,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 
     if (warp == 11) {
         // ---------------- metadata: segment tables and Q^T ----------------
-        // Per unit, Q^T is copied once the previous unit's last S has read
-        // the buffer; the rows of the unit after it are prefetched into L2
+        // Per unit, Q^T is copied into buffer i % QB once the last S of the
+        // unit QB back has read it (with two buffers, while the previous
+        // unit runs); the rows of the unit after it are prefetched into L2
         // meanwhile.  A new item's Q^T copy is issued before its segment
         // table is built, so the two chains of dependent loads overlap.
         const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
@@ -261,7 +266,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         // qrow[k]: q row of item row lane + 32 k without the head term
         // (query * Hq + group member), loaded once per item in parallel.
         int qrow[4] = {0, 0, 0, 0};
-        auto issue_q = [&](int h) {
+        auto issue_q = [&](int h, int qb) {
             // Row r's 16 chunks go to lanes 16 (r & 1) ... + 15 in step r / 2.
 #pragma unroll 4
             for (int x0 = 0; x0 < R * 16; x0 += 32) {
@@ -272,7 +277,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 const int k = r >> 5;
                 const int qr = k == 0 ? qr0 : k == 1 ? qr1 : k == 2 ? qr2 : qr3;
                 if (x < R * 16)
-                    cp_async_16(base + L::q_off + (ch >> 3) * L::q_half + r * 128 + (((ch & 7) ^ (r & 7)) << 4),
+                    cp_async_16(base + L::q_off + (uint32_t)qb * 2 * L::q_half + (ch >> 3) * L::q_half + r * 128 +
+                                    (((ch & 7) ^ (r & 7)) << 4),
                                 qg + (size_t)(qr + h * G) * kD + ch * 8);
             }
             cp_async_commit();
@@ -348,7 +354,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 if (lane == 0 && i == 0)
                     KPROF(a, 31 + 0 * (sb + nseg + cq0 + T));
                 if (i == 0) {
-                    issue_q(h);
+                    issue_q(h, 0);
                     q_issued = true;
                 }
                 if (lane == 0 && i == 0)
@@ -381,13 +387,15 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     KPROF(a, 10 + i);
             }
             if (!q_issued) {
+                // Q^T buffer i % QB, once unit i - QB's last S has read it.
+                const int qb = i % L::QB;
                 bool okw = i < 2 || tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1);
-                okw = okw && tc::mbar_wait(bar(kBarQFree), (i - 1) & 1);
+                okw = okw && (i < L::QB || tc::mbar_wait(bar(qfree_bar(qb)), ((i - L::QB) / L::QB) & 1));
                 if (!__all_sync(0xffffffffu, okw)) {
                     if (!*err) *err = 204;
                     break;
                 }
-                issue_q(h);
+                issue_q(h, qb);
             }
             cp_async_wait<0>();
             tc::fence_proxy_async();
@@ -683,7 +691,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                         for (int s = 0; s < 8; ++s) {
                             const uint64_t ko = (uint64_t)(((s >> 2) * kHalf + (s & 3) * 32) >> 4);
-                            const uint64_t qo = (uint64_t)(((s >> 2) * L::q_half + (s & 3) * 32) >> 4);
+                            const uint64_t qo = (uint64_t)(((is % L::QB) * 2 * L::q_half + (s >> 2) * L::q_half +
+                                                            (s & 3) * 32) >> 4);
                             tc::mma_bf16(d_s, dk0 + (uint64_t)st * kStageStep + ko, dq + qo, idesc_s, s > 0 ? 1u : 0u);
                         }
                         tc::mma_commit(bar(kBarSFull + b));
@@ -692,7 +701,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             KPROF(a, 300 + gs);
                         ++gs;
                         if (++ts == nts) {
-                            tc::mma_commit(bar(kBarQFree));
+                            tc::mma_commit(bar(qfree_bar(is % L::QB)));
                             ++is;
                             ts = 0;
                             nts = -1;

@@ -16,7 +16,10 @@
 //     ascending id.  The order changes only the partition, never a result.
 //   * Short nodes (at most chunk_target / 2 tokens) are packed, in preorder,
 //     into chunks of at most chunk_target tokens and at most
-//     kMaxSegsPerChunk segments.
+//     kMaxSegsPerChunk segments; a node whose query set and the chunk's are
+//     not one within the other joins only if it is tiny (at most
+//     chunk_target / 4 tokens), since the chunk's rows, and with them the
+//     work on every token of it, grow by its queries.
 //   * A longer node is cut into equal page-aligned pieces of about
 //     T = max(chunk_target, kSharedTokensPerRow * rows) tokens, rows being
 //     |cover| * gqa_group.  Each (chunk, query, head) writes one fp32
@@ -66,6 +69,16 @@ struct Builder {
         cur_chunk_tokens = 0;
         cur_chunk_segs = 0;
         open = false;
+    }
+    // The open chunk's query set and `mask` are one within the other.
+    bool nested(const uint64_t *mask) const
+    {
+        bool sub = true, sup = true;
+        for (int32_t i = 0; i < W; ++i) {
+            sub = sub && (mask[i] & ~cur_mask[i]) == 0;
+            sup = sup && (cur_mask[i] & ~mask[i]) == 0;
+        }
+        return sub || sup;
     }
     void add_segment(int32_t node, int32_t begin, int32_t len, const uint64_t *mask)
     {
@@ -328,8 +341,11 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
                 continue;
             unique_tokens += L;
             if (2 * (int64_t)L <= chunk_target) {
+                // A segment that would add queries to the open chunk (its
+                // rows grow for every token of it) joins only when tiny.
+                const bool tiny = 4 * (int64_t)L <= chunk_target;
                 if (b.open && (b.cur_chunk_tokens + L > chunk_target ||
-                               b.cur_chunk_segs >= kMaxSegsPerChunk))
+                               b.cur_chunk_segs >= kMaxSegsPerChunk || (!tiny && !b.nested(m))))
                     b.close();
                 b.add_segment(n, 0, L, m);
                 continue;

@@ -40,7 +40,7 @@ double fma_ns_per_token(int bucket)
 }
 double mma_ns_per_token(int bucket)
 {
-    static const double ns[4] = {18.0, 18.0, 22.0, 28.0};
+    static const double ns[4] = {14.0, 18.0, 22.0, 28.0};
     return ns[bucket];
 }
 

@@ -28,26 +28,32 @@
 // all roles walk the CTA's units in order and its tiles form one sequence
 // through the stages, so the next unit's loads and its first S overlap the
 // end of the current one.
-// Roles (12 warps):
-//   warps 0-3, 4-7  softmax warpgroups 0 and 1 (column halves);
+// Roles (16 warps; the softmax warpgroups run with 168 registers a thread,
+// the other two with 88):
+//   warps 0-3, 4-7  softmax warpgroups 0 and 1 (column halves); at a unit's
+//                   end they reduce their column sums and hand them, with
+//                   the partial rows, to the epilogue warpgroup;
 //   warps 8, 10     K and V producers: resolve a tile's pages through the
 //                   page table one tile ahead, load full aligned pages with
-//                   TMA (2 KB boxes of the 128-byte-swizzled layout) and
-//                   ragged rows (node tails, packed one-token nodes) with
-//                   16-byte cp.async at the exact token count; K of a stage
-//                   is refilled as soon as S of the tile two back is done,
-//                   V once its P.V is done;
+//                   TMA (one 4-D box for eight consecutive pages, 2 KB boxes
+//                   of the 128-byte-swizzled layout otherwise) and ragged
+//                   rows (node tails, packed one-token nodes) with 16-byte
+//                   cp.async at the exact token count; K of a stage is
+//                   refilled as soon as S of the tile two back is done, V
+//                   once its P.V is done;
 //   warp 9          allocates TMEM; lane 0 issues the MMAs, S(t) and P.V(t-1)
 //                   in whichever order their inputs become ready;
 //   warp 11         takes the next unit from the queue and passes its number
 //                   to the producers through a shared-memory ring; per
 //                   item, the segment table (positions, page bases, row
-//                   masks); per unit, Q^T once the previous unit's last S has
-//                   read the buffer.
-// Two KV stages; every hand-off is an mbarrier, every wait on one is
-// bounded.  A CTA whose wait runs out writes NaN partials for its units
-// (the step's output then shows the failure), waits for its own copies,
-// frees TMEM and returns.
+//                   masks); per unit, Q^T (two buffers up to 32 columns a
+//                   warpgroup, so the next unit's Q^T loads meanwhile);
+//   warps 12-15     epilogue: O^T / l out of TMEM (two O buffers) into the
+//                   fp32 partials while the softmax warpgroups go on with
+//                   the next unit.
+// Every hand-off is an mbarrier, every wait on one is bounded.  A CTA whose
+// wait runs out writes NaN partials for its units (the step's output then
+// shows the failure), waits for its own copies, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -61,7 +67,11 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kTileTok = 128;
-constexpr int kThreadsMma = 384;
+constexpr int kThreadsMma = 512;
+// Registers per thread: the launch gives 128; the softmax warpgroups take
+// 168 and the other two 88 (2 x 128 x 168 + 2 x 128 x 88 = 512 x 128).
+constexpr uint32_t kRegsSoftmax = 168, kRegsOther = 88;
+static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther == kThreadsMma * 128, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kHalf = 128 * 128;       // one 64-wide half of a 128-row operand (16 KB)
 constexpr uint32_t kTileBytes = 2 * kHalf;  // one 128 x 128 bf16 operand (32 KB)
@@ -101,7 +111,8 @@ struct Smem {
     static constexpr uint32_t seg_off = meta_off + 4 * kTileTok * 16;  // [2][kSegInts]
     static constexpr uint32_t red_off = seg_off + 2 * kSegInts * 4;  // [wg][warp][64]
     static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;  // [wg][m, alpha, 1/l, out row][64]
-    static constexpr uint32_t uinfo_off = stat_off + 2 * 4 * 64 * 4;  // [2] UnitInfo
+    static constexpr uint32_t epi_off = stat_off + 2 * 4 * 64 * 4;   // [ob][wg][1/l 64, out row 64]; [ob][R, fail0, fail1, -]
+    static constexpr uint32_t uinfo_off = epi_off + 2 * 2 * 128 * 4 + 2 * 16;  // [2] UnitInfo
     static constexpr uint32_t iinfo_off = uinfo_off + 2 * 32;         // [2] ItemInfo
     static constexpr uint32_t useq_off = iinfo_off + 2 * 16;         // [kUnitQueue] unit numbers
     static constexpr uint32_t bar_off = useq_off + kUnitQueue * 4;   // mbarriers
@@ -126,11 +137,12 @@ constexpr int kBarSegEmpty = 18; // [2] ... no longer read (both producers, 32 l
 constexpr int kBarUFull = 20;    // [2] a unit's description and Q^T written (32 lanes)
 constexpr int kBarUEmpty = 22;   // [2] ... description read (MMA issuer + 2 warpgroups)
 constexpr int kBarQFree = 24;    // the unit's last S finished: its Q^T buffer may be replaced (MMA commit)
-constexpr int kBarOFree = 25;    // [2] O buffer read out by the epilogue (one per warpgroup)
+constexpr int kBarOFree = 25;    // [2] O buffer read out by the epilogue warpgroup
 constexpr int kBarQFull = 27;    // [kUnitQueue] a unit number written (metadata lane 0)
 constexpr int kBarQEmpty = 35;   // [kUnitQueue] ... read (lane 0 of each producer)
 constexpr int kBarQFree1 = 43;   // ... the same for Q^T buffer 1
-constexpr int kNumBars = 44;
+constexpr int kBarEpiFull = 44;  // [2] a unit's column sums and rows handed to the epilogue (one per warpgroup)
+constexpr int kNumBars = 46;
 __device__ __forceinline__ int qfree_bar(int qb) { return qb == 0 ? kBarQFree : kBarQFree1; }
 static_assert(kNumBars * 8 <= Smem<16>::misc_off - Smem<16>::bar_off, "mbarrier space");
 
@@ -226,7 +238,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_init(bar(kBarSegEmpty + i), 64);
             tc::mbar_init(bar(kBarUFull + i), 32);
             tc::mbar_init(bar(kBarUEmpty + i), 3);
-            tc::mbar_init(bar(kBarOFree + i), 2);
+            tc::mbar_init(bar(kBarOFree + i), 1);
+            tc::mbar_init(bar(kBarEpiFull + i), 2);
         }
         tc::mbar_init(bar(kBarQFree), 1);
         tc::mbar_init(bar(kBarQFree1), 1);
@@ -253,498 +266,558 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     const uint32_t tmem = *tmem_slot;
     if (tid == 0)
         KPROF(a, 1);
+    float *epi = reinterpret_cast<float *>(smem + L::epi_off);
+    volatile int32_t *epi_info = reinterpret_cast<volatile int32_t *>(smem + L::epi_off + 2 * 2 * 128 * 4);
 
-    if (warp == 11) {
-        // ---------------- metadata: segment tables and Q^T ----------------
-        // Per unit, Q^T is copied into buffer i % QB once the last S of the
-        // unit QB back has read it (with two buffers, while the previous
-        // unit runs); the rows of the unit after it are prefetched into L2
-        // meanwhile.  A new item's Q^T copy is issued before its segment
-        // table is built, so the two chains of dependent loads overlap.
-        const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
-        int iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
-        // qrow[k]: q row of item row lane + 32 k without the head term
-        // (query * Hq + group member), loaded once per item in parallel.
-        int qrow[4] = {0, 0, 0, 0};
-        auto issue_q = [&](int h, int qb) {
-            // Row r's 16 chunks go to lanes 16 (r & 1) ... + 15 in step r / 2.
-#pragma unroll 4
-            for (int x0 = 0; x0 < R * 16; x0 += 32) {
-                const int x = x0 + lane, r = x >> 4, ch = x & 15;
-                const int src = r & 31;
-                const int qr0 = __shfl_sync(0xffffffffu, qrow[0], src), qr1 = __shfl_sync(0xffffffffu, qrow[1], src);
-                const int qr2 = __shfl_sync(0xffffffffu, qrow[2], src), qr3 = __shfl_sync(0xffffffffu, qrow[3], src);
-                const int k = r >> 5;
-                const int qr = k == 0 ? qr0 : k == 1 ? qr1 : k == 2 ? qr2 : qr3;
-                if (x < R * 16)
-                    cp_async_16(base + L::q_off + (uint32_t)qb * 2 * L::q_half + (ch >> 3) * L::q_half + r * 128 +
-                                    (((ch & 7) ^ (r & 7)) << 4),
-                                qg + (size_t)(qr + h * G) * kD + ch * 8);
-            }
-            cp_async_commit();
-        };
-        auto prefetch_q = [&](int h) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (lane + 32 * k < R) {
-                    const char *addr = reinterpret_cast<const char *>(qg + (size_t)(qrow[k] + h * G) * kD);
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
-                    asm volatile("prefetch.global.L2 [%0];" ::"l"(addr + 128));
+    if (warp >= 8) {
+        // Warps 8-11 and the epilogue warpgroup give registers to the
+        // softmax warpgroups (each warpgroup as a whole, before its roles).
+        tc::setmaxnreg_dec<kRegsOther>();
+        if (warp == 11) {
+            // ---------------- metadata: segment tables and Q^T ----------------
+            // Per unit, Q^T is copied into buffer i % QB once the last S of the
+            // unit QB back has read it (with two buffers, while the previous
+            // unit runs); the rows of the unit after it are prefetched into L2
+            // meanwhile.  A new item's Q^T copy is issued before its segment
+            // table is built, so the two chains of dependent loads overlap.
+            const __nv_bfloat16 *qg = reinterpret_cast<const __nv_bfloat16 *>(a.q);
+            int iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
+            // qrow[k]: q row of item row lane + 32 k without the head term
+            // (query * Hq + group member), loaded once per item in parallel.
+            int qrow[4] = {0, 0, 0, 0};
+            auto issue_q = [&](int h, int qb) {
+                // Row r's 16 chunks go to lanes 16 (r & 1) ... + 15 in step r / 2.
+    #pragma unroll 4
+                for (int x0 = 0; x0 < R * 16; x0 += 32) {
+                    const int x = x0 + lane, r = x >> 4, ch = x & 15;
+                    const int src = r & 31;
+                    const int qr0 = __shfl_sync(0xffffffffu, qrow[0], src), qr1 = __shfl_sync(0xffffffffu, qrow[1], src);
+                    const int qr2 = __shfl_sync(0xffffffffu, qrow[2], src), qr3 = __shfl_sync(0xffffffffu, qrow[3], src);
+                    const int k = r >> 5;
+                    const int qr = k == 0 ? qr0 : k == 1 ? qr1 : k == 2 ? qr2 : qr3;
+                    if (x < R * 16)
+                        cp_async_16(base + L::q_off + (uint32_t)qb * 2 * L::q_half + (ch >> 3) * L::q_half + r * 128 +
+                                        (((ch & 7) ^ (r & 7)) << 4),
+                                    qg + (size_t)(qr + h * G) * kD + ch * 8);
                 }
-            }
-        };
-        // Only the launch's early CTAs own a block: the others start when
-        // the step's earlier launches leave their SMs.
-        const int own_units = (int)blockIdx.x < early ? static_units : 0;
-        for (int i = 0;; ++i) {
-            // The next unit: first the CTA's own contiguous block (runs of
-            // one item's heads share its tables), then the launch's queue.
-            int u = (int)blockIdx.x * static_units + i;
-            if (i >= own_units) {
-                if (lane == 0)
-                    u = early * static_units + (int)atomicAdd(queue, 1u);
-                u = __shfl_sync(0xffffffffu, u, 0);
-            }
-            const bool last = u >= n_units;
-            const int ub = i & 1;
-            // Pass it (or the end, -1) to the producers.
-            const int qslot = i % UQ;
-            if (i >= UQ &&
-                !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarQEmpty + qslot), ((i / UQ) - 1) & 1))) {
-                if (!*err) *err = 201;
-                break;
-            }
-            if (lane == 0) {
-                useq[qslot] = last ? -1 : u;
-                tc::mbar_arrive(bar(kBarQFull + qslot));
-            }
-            if (last) {
-                if (lane == 0)
-                    queue_done(queue, qdone);
-                // End mark for the MMA issuer and the softmax warpgroups.
-                if (i >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1))) {
-                    if (!*err) *err = 202;
+                cp_async_commit();
+            };
+            auto prefetch_q = [&](int h) {
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (lane + 32 * k < R) {
+                        const char *addr = reinterpret_cast<const char *>(qg + (size_t)(qrow[k] + h * G) * kD);
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(addr + 128));
+                    }
+                }
+            };
+            // Only the launch's early CTAs own a block: the others start when
+            // the step's earlier launches leave their SMs.
+            const int own_units = (int)blockIdx.x < early ? static_units : 0;
+            for (int i = 0;; ++i) {
+                // The next unit: first the CTA's own contiguous block (runs of
+                // one item's heads share its tables), then the launch's queue.
+                int u = (int)blockIdx.x * static_units + i;
+                if (i >= own_units) {
+                    if (lane == 0)
+                        u = early * static_units + (int)atomicAdd(queue, 1u);
+                    u = __shfl_sync(0xffffffffu, u, 0);
+                }
+                const bool last = u >= n_units;
+                const int ub = i & 1;
+                // Pass it (or the end, -1) to the producers.
+                const int qslot = i % UQ;
+                if (i >= UQ &&
+                    !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarQEmpty + qslot), ((i / UQ) - 1) & 1))) {
+                    if (!*err) *err = 201;
                     break;
                 }
+                if (lane == 0) {
+                    useq[qslot] = last ? -1 : u;
+                    tc::mbar_arrive(bar(kBarQFull + qslot));
+                }
+                if (last) {
+                    if (lane == 0)
+                        queue_done(queue, qdone);
+                    // End mark for the MMA issuer and the softmax warpgroups.
+                    if (i >= 2 && !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1))) {
+                        if (!*err) *err = 202;
+                        break;
+                    }
+                    if (lane == 0)
+                        uinfo[ub].ntiles = -1;
+                    __syncwarp();
+                    tc::mbar_arrive(bar(kBarUFull + ub));
+                    break;
+                }
+                const int item = u / Hkv, h = u - item * Hkv;
+                bool q_issued = false;
+                if (item != prev_item) {
+                    prev_item = item;
+                    ++iseq;
+                    const int sbuf = iseq & 1;
+                    const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
+                    if (lane == 0 && i == 0)
+                        KPROF(a, 30);
+                    R = (qe - qb) * G;
+                    const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
+                    cq0 = p.chunk_q_off[c] + qb;
+                    const int T = p.chunk_tokens[c];
+                    ntiles = (T + kTileTok - 1) / kTileTok;
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int r = lane + 32 * k;
+                        qrow[k] = r < R ? p.chunk_q[cq0 + r / G] * Hq + r % G : 0;
+                    }
+                    if (lane == 0 && i == 0)
+                        KPROF(a, 31 + 0 * (sb + nseg + cq0 + T));
+                    if (i == 0) {
+                        issue_q(h, 0);
+                        q_issued = true;
+                    }
+                    if (lane == 0 && i == 0)
+                        KPROF(a, 32);
+                    if (iseq >= 2 &&
+                        !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegEmpty + sbuf), ((iseq - 2) >> 1) & 1))) {
+                        if (!*err) *err = 203;
+                        break;
+                    }
+                    int32_t *tab = seg_tab(sbuf);
+                    uint4 *s_rmask = reinterpret_cast<uint4 *>(tab + 3 * kMaxSegsPerChunk);
+                    const uint4 *item_rm = rmask + rmask_off[item];
+                    for (int s = lane; s < nseg; s += 32) {
+                        const int pgb = a.node_page_off[p.seg_node[sb + s]];
+                        const int tb = p.seg_tok_begin[sb + s];
+                        tab[s] = p.seg_chunk_pos[sb + s];
+                        tab[kMaxSegsPerChunk + s] = pgb;
+                        tab[2 * kMaxSegsPerChunk + s] = tb;
+                        // The producers' first page-table reads for this segment.
+                        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.page_id + pgb + tb / kPageSize));
+                        s_rmask[s] = item_rm[s];
+                    }
+                    if (lane == 0 && i == 0)
+                        KPROF(a, 33);
+                    if (lane == 0)
+                        iinfo[sbuf] = ItemInfo{nseg, T, {0, 0}};
+                    __syncwarp();
+                    tc::mbar_arrive(bar(kBarSegFull + sbuf));
+                    if (lane == 0 && i < 8)
+                        KPROF(a, 10 + i);
+                }
+                if (!q_issued) {
+                    // Q^T buffer i % QB, once unit i - QB's last S has read it.
+                    const int qb = i % L::QB;
+                    bool okw = i < 2 || tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1);
+                    okw = okw && (i < L::QB || tc::mbar_wait(bar(qfree_bar(qb)), ((i - L::QB) / L::QB) & 1));
+                    if (!__all_sync(0xffffffffu, okw)) {
+                        if (!*err) *err = 204;
+                        break;
+                    }
+                    issue_q(h, qb);
+                }
+                cp_async_wait<0>();
+                tc::fence_proxy_async();
                 if (lane == 0)
-                    uinfo[ub].ntiles = -1;
+                    uinfo[ub] = UnitInfo{R, cq0, h, ntiles, {0, 0, 0, 0}};
                 __syncwarp();
                 tc::mbar_arrive(bar(kBarUFull + ub));
-                break;
-            }
-            const int item = u / Hkv, h = u - item * Hkv;
-            bool q_issued = false;
-            if (item != prev_item) {
-                prev_item = item;
-                ++iseq;
-                const int sbuf = iseq & 1;
-                const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
-                if (lane == 0 && i == 0)
-                    KPROF(a, 30);
-                R = (qe - qb) * G;
-                const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
-                cq0 = p.chunk_q_off[c] + qb;
-                const int T = p.chunk_tokens[c];
-                ntiles = (T + kTileTok - 1) / kTileTok;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int r = lane + 32 * k;
-                    qrow[k] = r < R ? p.chunk_q[cq0 + r / G] * Hq + r % G : 0;
-                }
-                if (lane == 0 && i == 0)
-                    KPROF(a, 31 + 0 * (sb + nseg + cq0 + T));
-                if (i == 0) {
-                    issue_q(h, 0);
-                    q_issued = true;
-                }
-                if (lane == 0 && i == 0)
-                    KPROF(a, 32);
-                if (iseq >= 2 &&
-                    !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegEmpty + sbuf), ((iseq - 2) >> 1) & 1))) {
-                    if (!*err) *err = 203;
-                    break;
-                }
-                int32_t *tab = seg_tab(sbuf);
-                uint4 *s_rmask = reinterpret_cast<uint4 *>(tab + 3 * kMaxSegsPerChunk);
-                const uint4 *item_rm = rmask + rmask_off[item];
-                for (int s = lane; s < nseg; s += 32) {
-                    const int pgb = a.node_page_off[p.seg_node[sb + s]];
-                    const int tb = p.seg_tok_begin[sb + s];
-                    tab[s] = p.seg_chunk_pos[sb + s];
-                    tab[kMaxSegsPerChunk + s] = pgb;
-                    tab[2 * kMaxSegsPerChunk + s] = tb;
-                    // The producers' first page-table reads for this segment.
-                    asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.page_id + pgb + tb / kPageSize));
-                    s_rmask[s] = item_rm[s];
-                }
-                if (lane == 0 && i == 0)
-                    KPROF(a, 33);
-                if (lane == 0)
-                    iinfo[sbuf] = ItemInfo{nseg, T, {0, 0}};
-                __syncwarp();
-                tc::mbar_arrive(bar(kBarSegFull + sbuf));
                 if (lane == 0 && i < 8)
-                    KPROF(a, 10 + i);
+                    KPROF(a, 20 + i);
+                // Warm L2 with the rows of the item's next KV head, likely this
+                // CTA's next unit (the queue hands out units in order).
+                if (h + 1 < Hkv)
+                    prefetch_q(h + 1);
             }
-            if (!q_issued) {
-                // Q^T buffer i % QB, once unit i - QB's last S has read it.
-                const int qb = i % L::QB;
-                bool okw = i < 2 || tc::mbar_wait(bar(kBarUEmpty + ub), ((i - 2) >> 1) & 1);
-                okw = okw && (i < L::QB || tc::mbar_wait(bar(qfree_bar(qb)), ((i - L::QB) / L::QB) & 1));
-                if (!__all_sync(0xffffffffu, okw)) {
-                    if (!*err) *err = 204;
-                    break;
+        } else if (warp == 8 || warp == 10) {
+            // ---------------- producers (warp 8: K, warp 10: V) ----------------
+            const int kv = warp == 8 ? 0 : 1;
+            const int NS = kv ? VST : 2;   // stages of this operand
+            const __nv_bfloat16 *src_base = reinterpret_cast<const __nv_bfloat16 *>(kv ? a.v_pages : a.k_pages);
+            const CUtensorMap *tm = kv ? &maps.v1 : &maps.k1;
+            const CUtensorMap *tm8 = kv ? &maps.v8 : &maps.k8;
+            // One tile's resolution: rows lane + 32k (k < 4) and pages 0..7.
+            struct Res {
+                int seg[4], tok[4], pid[4];   // per row; pid only for ragged rows
+                int page_y;                   // lane < 8: page id of page `lane` when it goes by TMA
+                uint32_t tma_pages;
+            };
+            const int32_t *s_pos = nullptr, *s_pgb = nullptr, *s_tb = nullptr;
+            const uint4 *s_rmask = nullptr;
+            int T = 0, nseg = 0;
+            // Segment holding position pos (warp-uniform: broadcast reads).
+            auto seg_at = [&](int pos) {
+                int lo = 0, hi = nseg - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (s_pos[mid] <= pos)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
                 }
-                issue_q(h, qb);
-            }
-            cp_async_wait<0>();
-            tc::fence_proxy_async();
-            if (lane == 0)
-                uinfo[ub] = UnitInfo{R, cq0, h, ntiles, {0, 0, 0, 0}};
-            __syncwarp();
-            tc::mbar_arrive(bar(kBarUFull + ub));
-            if (lane == 0 && i < 8)
-                KPROF(a, 20 + i);
-            // Warm L2 with the rows of the item's next KV head, likely this
-            // CTA's next unit (the queue hands out units in order).
-            if (h + 1 < Hkv)
-                prefetch_q(h + 1);
-        }
-    } else if (warp == 8 || warp == 10) {
-        // ---------------- producers (warp 8: K, warp 10: V) ----------------
-        const int kv = warp == 8 ? 0 : 1;
-        const int NS = kv ? VST : 2;   // stages of this operand
-        const __nv_bfloat16 *src_base = reinterpret_cast<const __nv_bfloat16 *>(kv ? a.v_pages : a.k_pages);
-        const CUtensorMap *tm = kv ? &maps.v1 : &maps.k1;
-        const CUtensorMap *tm8 = kv ? &maps.v8 : &maps.k8;
-        // One tile's resolution: rows lane + 32k (k < 4) and pages 0..7.
-        struct Res {
-            int seg[4], tok[4], pid[4];   // per row; pid only for ragged rows
-            int page_y;                   // lane < 8: page id of page `lane` when it goes by TMA
-            uint32_t tma_pages;
-        };
-        const int32_t *s_pos = nullptr, *s_pgb = nullptr, *s_tb = nullptr;
-        const uint4 *s_rmask = nullptr;
-        int T = 0, nseg = 0;
-        // Segment holding position pos (warp-uniform: broadcast reads).
-        auto seg_at = [&](int pos) {
-            int lo = 0, hi = nseg - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (s_pos[mid] <= pos)
-                    lo = mid;
-                else
-                    hi = mid - 1;
-            }
-            return lo;
-        };
-        auto resolve = [&](int t, Res &r) {
-            const int p0 = t * kTileTok;
-            const int sga = seg_at(p0);
-            const int tka = s_tb[sga] + p0 - s_pos[sga];
-            if (T - p0 >= kTileTok && (tka % kPageSize) == 0 && seg_at(p0 + kTileTok - 1) == sga) {
-                // Fast path: eight whole pages of one segment.
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    r.seg[k] = sga;
-                    r.tok[k] = tka + lane + 32 * k;
-                    r.pid[k] = -1;
-                }
-                r.tma_pages = 0xffu;
-                r.page_y = lane < 8 ? a.page_id[s_pgb[sga] + tka / kPageSize + lane] : -1;
-                return;
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int pos = t * kTileTok + lane + 32 * k;
-                r.seg[k] = -1;
-                r.tok[k] = 1;
-                if (pos < T) {
-                    int lo = 0, hi = nseg - 1;
-                    while (lo < hi) {
-                        const int mid = (lo + hi + 1) >> 1;
-                        if (s_pos[mid] <= pos)
-                            lo = mid;
-                        else
-                            hi = mid - 1;
+                return lo;
+            };
+            auto resolve = [&](int t, Res &r) {
+                const int p0 = t * kTileTok;
+                const int sga = seg_at(p0);
+                const int tka = s_tb[sga] + p0 - s_pos[sga];
+                if (T - p0 >= kTileTok && (tka % kPageSize) == 0 && seg_at(p0 + kTileTok - 1) == sga) {
+                    // Fast path: eight whole pages of one segment.
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        r.seg[k] = sga;
+                        r.tok[k] = tka + lane + 32 * k;
+                        r.pid[k] = -1;
                     }
-                    r.seg[k] = lo;
-                    r.tok[k] = s_tb[lo] + pos - s_pos[lo];
+                    r.tma_pages = 0xffu;
+                    r.page_y = lane < 8 ? a.page_id[s_pgb[sga] + tka / kPageSize + lane] : -1;
+                    return;
                 }
-            }
-            uint32_t tp = 0;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int s_first = __shfl_sync(0xffffffffu, r.seg[k], lane & 16);
-                const int t_first = __shfl_sync(0xffffffffu, r.tok[k], lane & 16);
-                const bool ok = r.seg[k] >= 0 && r.seg[k] == s_first && (t_first % kPageSize) == 0;
-                const uint32_t bal = __ballot_sync(0xffffffffu, ok);
-                if ((bal & 0xffffu) == 0xffffu)
-                    tp |= 1u << (2 * k);
-                if ((bal >> 16) == 0xffffu)
-                    tp |= 1u << (2 * k + 1);
-            }
-            r.tma_pages = tp;
-            // Page ids: one load per TMA page (lanes 0-7), one per ragged row.
-            int pseg = -1, ptok = 0;
-#pragma unroll
-            for (int pg = 0; pg < 8; ++pg) {
-                const int sg = __shfl_sync(0xffffffffu, r.seg[pg >> 1], 16 * (pg & 1));
-                const int tk = __shfl_sync(0xffffffffu, r.tok[pg >> 1], 16 * (pg & 1));
-                if (lane == pg) {
-                    pseg = sg;
-                    ptok = tk;
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int pos = t * kTileTok + lane + 32 * k;
+                    r.seg[k] = -1;
+                    r.tok[k] = 1;
+                    if (pos < T) {
+                        int lo = 0, hi = nseg - 1;
+                        while (lo < hi) {
+                            const int mid = (lo + hi + 1) >> 1;
+                            if (s_pos[mid] <= pos)
+                                lo = mid;
+                            else
+                                hi = mid - 1;
+                        }
+                        r.seg[k] = lo;
+                        r.tok[k] = s_tb[lo] + pos - s_pos[lo];
+                    }
                 }
-            }
-            r.page_y = -1;
-            if (lane < 8 && ((tp >> lane) & 1u))
-                r.page_y = a.page_id[s_pgb[pseg] + ptok / kPageSize];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                r.pid[k] = -1;
-                if (r.seg[k] >= 0 && !((tp >> ((lane + 32 * k) >> 4)) & 1u))
-                    r.pid[k] = a.page_id[s_pgb[r.seg[k]] + r.tok[k] / kPageSize];
-            }
-        };
-        int iseq = -1, prev_item = -1, gseq = 0, sbuf = 0;
-        bool ok = true;
-        for (int i = 0; ok; ++i) {
-            // The next unit number from the metadata warp (-1: no more).
-            const int qslot = i % UQ;
-            if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarQFull + qslot), (i / UQ) & 1))) {
-                if (!*err) *err = 205;
-                break;
-            }
-            const int u = useq[qslot];
-            __syncwarp();
-            if (lane == 0)
-                tc::mbar_arrive(bar(kBarQEmpty + qslot));
-            const int item = u < 0 ? -1 : u / Hkv;
-            if (u < 0 || item != prev_item) {
-                // Release the previous item's segment table, then wait for this one's.
-                if (prev_item >= 0) {
-                    __syncwarp();
-                    tc::mbar_arrive(bar(kBarSegEmpty + sbuf));
+                uint32_t tp = 0;
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int s_first = __shfl_sync(0xffffffffu, r.seg[k], lane & 16);
+                    const int t_first = __shfl_sync(0xffffffffu, r.tok[k], lane & 16);
+                    const bool ok = r.seg[k] >= 0 && r.seg[k] == s_first && (t_first % kPageSize) == 0;
+                    const uint32_t bal = __ballot_sync(0xffffffffu, ok);
+                    if ((bal & 0xffffu) == 0xffffu)
+                        tp |= 1u << (2 * k);
+                    if ((bal >> 16) == 0xffffu)
+                        tp |= 1u << (2 * k + 1);
                 }
-                if (u < 0)
-                    break;
-                prev_item = item;
-                ++iseq;
-                sbuf = iseq & 1;
-                if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegFull + sbuf), (iseq >> 1) & 1))) {
-                    if (!*err) *err = 206;
+                r.tma_pages = tp;
+                // Page ids: one load per TMA page (lanes 0-7), one per ragged row.
+                int pseg = -1, ptok = 0;
+    #pragma unroll
+                for (int pg = 0; pg < 8; ++pg) {
+                    const int sg = __shfl_sync(0xffffffffu, r.seg[pg >> 1], 16 * (pg & 1));
+                    const int tk = __shfl_sync(0xffffffffu, r.tok[pg >> 1], 16 * (pg & 1));
+                    if (lane == pg) {
+                        pseg = sg;
+                        ptok = tk;
+                    }
+                }
+                r.page_y = -1;
+                if (lane < 8 && ((tp >> lane) & 1u))
+                    r.page_y = a.page_id[s_pgb[pseg] + ptok / kPageSize];
+    #pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    r.pid[k] = -1;
+                    if (r.seg[k] >= 0 && !((tp >> ((lane + 32 * k) >> 4)) & 1u))
+                        r.pid[k] = a.page_id[s_pgb[r.seg[k]] + r.tok[k] / kPageSize];
+                }
+            };
+            int iseq = -1, prev_item = -1, gseq = 0, sbuf = 0;
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                // The next unit number from the metadata warp (-1: no more).
+                const int qslot = i % UQ;
+                if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarQFull + qslot), (i / UQ) & 1))) {
+                    if (!*err) *err = 205;
                     break;
                 }
-            }
-            const int h = u - item * Hkv;
-            const int32_t *tab = seg_tab(sbuf);
-            s_pos = tab;
-            s_pgb = tab + kMaxSegsPerChunk;
-            s_tb = tab + 2 * kMaxSegsPerChunk;
-            s_rmask = reinterpret_cast<const uint4 *>(tab + 3 * kMaxSegsPerChunk);
-            const ItemInfo ii = iinfo[sbuf];
-            T = ii.T;
-            nseg = ii.nseg;
-            const int ntiles = (T + kTileTok - 1) / kTileTok;
-            if (lane == 0 && kv == 0 && gseq == 0)
-                KPROF(a, 40);
-            Res res;
-            resolve(0, res);
-            if (lane == 0 && kv == 0 && gseq == 0)
-                KPROF(a, 41 + 0 * res.page_y);
-            for (int t = 0; t < ntiles; ++t, ++gseq) {
-                const int st = gseq % NS;
-                if (gseq >= NS) {
-                    const bool okw = __all_sync(
-                        0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((gseq / NS) - 1) & 1));
-                    if (!okw) {
-                        if (!*err) *err = 207;
-                        ok = false;
+                const int u = useq[qslot];
+                __syncwarp();
+                if (lane == 0)
+                    tc::mbar_arrive(bar(kBarQEmpty + qslot));
+                const int item = u < 0 ? -1 : u / Hkv;
+                if (u < 0 || item != prev_item) {
+                    // Release the previous item's segment table, then wait for this one's.
+                    if (prev_item >= 0) {
+                        __syncwarp();
+                        tc::mbar_arrive(bar(kBarSegEmpty + sbuf));
+                    }
+                    if (u < 0)
+                        break;
+                    prev_item = item;
+                    ++iseq;
+                    sbuf = iseq & 1;
+                    if (!__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegFull + sbuf), (iseq >> 1) & 1))) {
+                        if (!*err) *err = 206;
                         break;
                     }
                 }
-                if (lane == 0 && kv == 0 && gseq < 16)
-                    KPROF(a, 800 + 4 * gseq);
-                if (kv == 0) {
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        meta[(gseq & 3) * kTileTok + lane + 32 * k] =
-                            res.seg[k] >= 0 ? s_rmask[res.seg[k]] : make_uint4(0, 0, 0, 0);
-                }
-                const uint32_t full = bar((kv ? kBarFullV : kBarFullK) + st);
-                const uint32_t dst = base + (kv ? L::v_off : L::k_off) + (uint32_t)st * kTileBytes;
-                if (lane == 0)
-                    tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
-                __syncwarp();
+                const int h = u - item * Hkv;
+                const int32_t *tab = seg_tab(sbuf);
+                s_pos = tab;
+                s_pgb = tab + kMaxSegsPerChunk;
+                s_tb = tab + 2 * kMaxSegsPerChunk;
+                s_rmask = reinterpret_cast<const uint4 *>(tab + 3 * kMaxSegsPerChunk);
+                const ItemInfo ii = iinfo[sbuf];
+                T = ii.T;
+                nseg = ii.nseg;
+                const int ntiles = (T + kTileTok - 1) / kTileTok;
                 if (lane == 0 && kv == 0 && gseq == 0)
-                    KPROF(a, 42);
-                // Eight whole, consecutive pages: one box per column half.
-                bool run8 = false;
-                const int pg0 = __shfl_sync(0xffffffffu, res.page_y, 0);
-                if (res.tma_pages == 0xffu)
-                    run8 = __all_sync(0xffffffffu, lane >= 8 || res.page_y == pg0 + lane);
-                if (run8) {
-                    if (lane == 0) {
-                        tc::tma_load_4d(dst, tm8, 0, 0, h, pg0, full);
-                        tc::tma_load_4d(dst + kHalf, tm8, 64, 0, h, pg0, full);
+                    KPROF(a, 40);
+                Res res;
+                resolve(0, res);
+                if (lane == 0 && kv == 0 && gseq == 0)
+                    KPROF(a, 41 + 0 * res.page_y);
+                for (int t = 0; t < ntiles; ++t, ++gseq) {
+                    const int st = gseq % NS;
+                    if (gseq >= NS) {
+                        const bool okw = __all_sync(
+                            0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((gseq / NS) - 1) & 1));
+                        if (!okw) {
+                            if (!*err) *err = 207;
+                            ok = false;
+                            break;
+                        }
                     }
-                } else if (res.page_y >= 0) {
-                    const int y = (res.page_y * Hkv + h) * kPageSize;
+                    if (lane == 0 && kv == 0 && gseq < 16)
+                        KPROF(a, 800 + 4 * gseq);
+                    if (kv == 0) {
+    #pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            meta[(gseq & 3) * kTileTok + lane + 32 * k] =
+                                res.seg[k] >= 0 ? s_rmask[res.seg[k]] : make_uint4(0, 0, 0, 0);
+                    }
+                    const uint32_t full = bar((kv ? kBarFullV : kBarFullK) + st);
+                    const uint32_t dst = base + (kv ? L::v_off : L::k_off) + (uint32_t)st * kTileBytes;
+                    if (lane == 0)
+                        tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
+                    __syncwarp();
                     if (lane == 0 && kv == 0 && gseq == 0)
-                        KPROF(a, 43);
-                    const uint32_t row_b = (uint32_t)(16 * lane) * 128;
-                    tc::tma_load_2d(dst + row_b, tm, 0, y, full);
-                    tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full);
-                }
-                if (lane == 0 && kv == 0 && gseq < 16)
-                    KPROF(a, 801 + 4 * gseq);
-                // Ragged rows: two rows per warp step, 16 lanes (16-byte chunks) each.
-                bool any_cp = false;
-                const __nv_bfloat16 *src0 = src_base + (lane & 15) * 8;
-                const uint32_t dst0 = dst + ((lane & 15) >> 3) * kHalf;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t nb = __ballot_sync(0xffffffffu, res.pid[k] >= 0);
-                    any_cp |= nb != 0;
-                    while (nb) {
-                        const int l0 = __ffs(nb) - 1;
-                        nb &= nb - 1;
-                        int l1 = -1;
-                        if (nb) {
-                            l1 = __ffs(nb) - 1;
+                        KPROF(a, 42);
+                    // Eight whole, consecutive pages: one box per column half.
+                    bool run8 = false;
+                    const int pg0 = __shfl_sync(0xffffffffu, res.page_y, 0);
+                    if (res.tma_pages == 0xffu)
+                        run8 = __all_sync(0xffffffffu, lane >= 8 || res.page_y == pg0 + lane);
+                    if (run8) {
+                        if (lane == 0) {
+                            tc::tma_load_4d(dst, tm8, 0, 0, h, pg0, full);
+                            tc::tma_load_4d(dst + kHalf, tm8, 64, 0, h, pg0, full);
+                        }
+                    } else if (res.page_y >= 0) {
+                        const int y = (res.page_y * Hkv + h) * kPageSize;
+                        if (lane == 0 && kv == 0 && gseq == 0)
+                            KPROF(a, 43);
+                        const uint32_t row_b = (uint32_t)(16 * lane) * 128;
+                        tc::tma_load_2d(dst + row_b, tm, 0, y, full);
+                        tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full);
+                    }
+                    if (lane == 0 && kv == 0 && gseq < 16)
+                        KPROF(a, 801 + 4 * gseq);
+                    // Ragged rows: two rows per warp step, 16 lanes (16-byte chunks) each.
+                    bool any_cp = false;
+                    const __nv_bfloat16 *src0 = src_base + (lane & 15) * 8;
+                    const uint32_t dst0 = dst + ((lane & 15) >> 3) * kHalf;
+    #pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t nb = __ballot_sync(0xffffffffu, res.pid[k] >= 0);
+                        any_cp |= nb != 0;
+                        while (nb) {
+                            const int l0 = __ffs(nb) - 1;
                             nb &= nb - 1;
-                        }
-                        const int mine = lane < 16 ? l0 : l1;
-                        const int p0 = __shfl_sync(0xffffffffu, res.pid[k], l0);
-                        const int t0 = __shfl_sync(0xffffffffu, res.tok[k], l0);
-                        const int p1 = __shfl_sync(0xffffffffu, res.pid[k], l1 < 0 ? l0 : l1);
-                        const int t1 = __shfl_sync(0xffffffffu, res.tok[k], l1 < 0 ? l0 : l1);
-                        if (mine >= 0) {
-                            const int row = mine + 32 * k;
-                            const int pg = lane < 16 ? p0 : p1;
-                            const int tk = lane < 16 ? t0 : t1;
-                            const long long o = (((long long)pg * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
-                            const int ch = lane & 7;
-                            cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src0 + o);
+                            int l1 = -1;
+                            if (nb) {
+                                l1 = __ffs(nb) - 1;
+                                nb &= nb - 1;
+                            }
+                            const int mine = lane < 16 ? l0 : l1;
+                            const int p0 = __shfl_sync(0xffffffffu, res.pid[k], l0);
+                            const int t0 = __shfl_sync(0xffffffffu, res.tok[k], l0);
+                            const int p1 = __shfl_sync(0xffffffffu, res.pid[k], l1 < 0 ? l0 : l1);
+                            const int t1 = __shfl_sync(0xffffffffu, res.tok[k], l1 < 0 ? l0 : l1);
+                            if (mine >= 0) {
+                                const int row = mine + 32 * k;
+                                const int pg = lane < 16 ? p0 : p1;
+                                const int tk = lane < 16 ? t0 : t1;
+                                const long long o = (((long long)pg * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
+                                const int ch = lane & 7;
+                                cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src0 + o);
+                            }
                         }
                     }
+                    if (any_cp) {
+                        cp_async_commit();
+                        cp_async_wait<0>();
+                        tc::fence_proxy_async();
+                    }
+                    tc::mbar_arrive(full);
+                    if (lane == 0 && gseq < 64)
+                        KPROF(a, 100 + 100 * kv + gseq);
+                    if (t + 1 < ntiles)
+                        resolve(t + 1, res);
+                    if (lane == 0 && kv == 0 && gseq < 16)
+                        KPROF(a, 802 + 4 * gseq);
                 }
-                if (any_cp) {
-                    cp_async_commit();
-                    cp_async_wait<0>();
-                    tc::fence_proxy_async();
-                }
-                tc::mbar_arrive(full);
-                if (lane == 0 && gseq < 64)
-                    KPROF(a, 100 + 100 * kv + gseq);
-                if (t + 1 < ntiles)
-                    resolve(t + 1, res);
-                if (lane == 0 && kv == 0 && gseq < 16)
-                    KPROF(a, 802 + 4 * gseq);
             }
-        }
-        cp_async_wait<0>();
-        // Do not leave while a TMA copy of ours may still be landing.
-        for (int s2 = 0; s2 < NS && s2 < gseq; ++s2) {
-            const int last = gseq - 1 - ((gseq - 1 - s2) % NS);
-            tc::mbar_wait(bar((kv ? kBarFullV : kBarFullK) + s2), (last / NS) & 1);
-        }
-    } else if (warp == 9) {
-        // ---------------- MMA issue ----------------
-        if (lane == 0) {
-            const uint32_t idesc_s = tc::idesc_bf16(128, RP, 0, 0);
-            const uint32_t idesc_o = tc::idesc_bf16(128, RP, 1, 1);
-            // Descriptors of k-step 0; step s adds an address offset (16-byte units).
-            const uint64_t dq = tc::smem_desc(base + L::q_off, 16, 1024);
-            const uint64_t dp = tc::smem_desc(base + L::p_off, kHalf, 1024);
-            const uint64_t dk0 = tc::smem_desc(base + L::k_off, 16, 1024);
-            const uint64_t dv0 = tc::smem_desc(base + L::v_off, kHalf, 1024);
-            constexpr uint64_t kStageStep = kTileBytes >> 4;   // descriptor address units
-            int nunits = 0x7fffffff;   // known once the end mark is read
-            // S cursor: unit is, its tile ts (nts tiles, -1 before its
-            // description is read), CTA tile gs.  P.V cursor: ip, tp, gp.
-            int is = 0, ts = 0, nts = -1, gs = 0;
-            int ip = 0, tp = 0, gp = 0;
-            int ntq0 = 0, ntq1 = 0;   // tiles of the units in flight, by unit parity
-            bool ok = true;
-            uint32_t polls = 0;
-            while (ip < nunits && ok) {
-                bool progressed = false;
-                // S(gs): needs the unit's Q^T, K(gs) and S buffer gs % 2
-                // released by tile gs - 2; at most one tile ahead of P.V.
-                if (is < nunits && gs <= gp + 1) {
-                    if (nts < 0 && tc::mbar_test(bar(kBarUFull + (is & 1)), (is >> 1) & 1)) {
-                        nts = uinfo[is & 1].ntiles;
-                        if (nts < 0)
-                            nunits = is;   // no more units
-                        if (is & 1)
-                            ntq1 = nts;
-                        else
-                            ntq0 = nts;
-                        tc::mbar_arrive(bar(kBarUEmpty + (is & 1)));
-                    }
-                    const int st = gs & 1, b = gs & 1;
-                    if (nts > 0 && tc::mbar_test(bar(kBarFullK + st), (gs >> 1) & 1) &&
-                        (gs < 2 || tc::mbar_test(bar(kBarSFree + b), ((gs - 2) >> 1) & 1))) {
-                        tc::fence_after_sync();
-                        const uint32_t d_s = tmem + (uint32_t)(b * 128);
-#pragma unroll
-                        for (int s = 0; s < 8; ++s) {
-                            const uint64_t ko = (uint64_t)(((s >> 2) * kHalf + (s & 3) * 32) >> 4);
-                            const uint64_t qo = (uint64_t)(((is % L::QB) * 2 * L::q_half + (s >> 2) * L::q_half +
-                                                            (s & 3) * 32) >> 4);
-                            tc::mma_bf16(d_s, dk0 + (uint64_t)st * kStageStep + ko, dq + qo, idesc_s, s > 0 ? 1u : 0u);
-                        }
-                        tc::mma_commit(bar(kBarSFull + b));
-                        tc::mma_commit(bar(kBarEmptyK + st));
-                        if (gs < 64)
-                            KPROF(a, 300 + gs);
-                        ++gs;
-                        if (++ts == nts) {
-                            tc::mma_commit(bar(qfree_bar(is % L::QB)));
-                            ++is;
-                            ts = 0;
-                            nts = -1;
-                        }
-                        progressed = true;
-                    }
-                }
-                // P.V(gp): needs V(gp), P(gp) and, for a unit's first tile,
-                // its O buffer read out by the epilogue of the unit two back.
-                if (gp < gs) {
-                    const int stp = gp % VST, ob = ip & 1;
-                    if (tc::mbar_test(bar(kBarFullV + stp), (gp / VST) & 1) &&
-                        tc::mbar_test(bar(kBarPFull), gp & 1) &&
-                        (tp > 0 || ip < 2 || tc::mbar_test(bar(kBarOFree + ob), ((ip - 2) >> 1) & 1))) {
-                        tc::fence_after_sync();
-                        const uint32_t d_o = tmem + 256 + (uint32_t)(ob * 128);
-#pragma unroll
-                        for (int s = 0; s < 8; ++s) {
-                            const uint64_t so = (uint64_t)((s * 2048) >> 4);
-                            tc::mma_bf16(d_o, dv0 + (uint64_t)stp * kStageStep + so, dp + so, idesc_o,
-                                         (tp > 0 || s > 0) ? 1u : 0u);
-                        }
-                        tc::mma_commit(bar(kBarPvDone));
-                        tc::mma_commit(bar(kBarEmptyV + stp));
-                        if (gp < 64)
-                            KPROF(a, 400 + gp);
-                        ++gp;
-                        if (++tp == ((ip & 1) ? ntq1 : ntq0)) {
-                            ++ip;
-                            tp = 0;
-                        }
-                        progressed = true;
-                    }
-                }
-                if (progressed)
-                    polls = 0;
-                else if (++polls > (1u << 24))
-                    ok = false;
+            cp_async_wait<0>();
+            // Do not leave while a TMA copy of ours may still be landing.
+            for (int s2 = 0; s2 < NS && s2 < gseq; ++s2) {
+                const int last = gseq - 1 - ((gseq - 1 - s2) % NS);
+                tc::mbar_wait(bar((kv ? kBarFullV : kBarFullK) + s2), (last / NS) & 1);
             }
-            if (!ok)
-                if (!*err) *err = 208;
-        }
+        } else if (warp == 9) {
+            // ---------------- MMA issue ----------------
+            if (lane == 0) {
+                const uint32_t idesc_s = tc::idesc_bf16(128, RP, 0, 0);
+                const uint32_t idesc_o = tc::idesc_bf16(128, RP, 1, 1);
+                // Descriptors of k-step 0; step s adds an address offset (16-byte units).
+                const uint64_t dq = tc::smem_desc(base + L::q_off, 16, 1024);
+                const uint64_t dp = tc::smem_desc(base + L::p_off, kHalf, 1024);
+                const uint64_t dk0 = tc::smem_desc(base + L::k_off, 16, 1024);
+                const uint64_t dv0 = tc::smem_desc(base + L::v_off, kHalf, 1024);
+                constexpr uint64_t kStageStep = kTileBytes >> 4;   // descriptor address units
+                int nunits = 0x7fffffff;   // known once the end mark is read
+                // S cursor: unit is, its tile ts (nts tiles, -1 before its
+                // description is read), CTA tile gs.  P.V cursor: ip, tp, gp.
+                int is = 0, ts = 0, nts = -1, gs = 0;
+                int ip = 0, tp = 0, gp = 0;
+                int ntq0 = 0, ntq1 = 0;   // tiles of the units in flight, by unit parity
+                bool ok = true;
+                uint32_t polls = 0;
+                while (ip < nunits && ok) {
+                    bool progressed = false;
+                    // S(gs): needs the unit's Q^T, K(gs) and S buffer gs % 2
+                    // released by tile gs - 2; at most one tile ahead of P.V.
+                    if (is < nunits && gs <= gp + 1) {
+                        if (nts < 0 && tc::mbar_test(bar(kBarUFull + (is & 1)), (is >> 1) & 1)) {
+                            nts = uinfo[is & 1].ntiles;
+                            if (nts < 0)
+                                nunits = is;   // no more units
+                            if (is & 1)
+                                ntq1 = nts;
+                            else
+                                ntq0 = nts;
+                            tc::mbar_arrive(bar(kBarUEmpty + (is & 1)));
+                        }
+                        const int st = gs & 1, b = gs & 1;
+                        if (nts > 0 && tc::mbar_test(bar(kBarFullK + st), (gs >> 1) & 1) &&
+                            (gs < 2 || tc::mbar_test(bar(kBarSFree + b), ((gs - 2) >> 1) & 1))) {
+                            tc::fence_after_sync();
+                            const uint32_t d_s = tmem + (uint32_t)(b * 128);
+    #pragma unroll
+                            for (int s = 0; s < 8; ++s) {
+                                const uint64_t ko = (uint64_t)(((s >> 2) * kHalf + (s & 3) * 32) >> 4);
+                                const uint64_t qo = (uint64_t)(((is % L::QB) * 2 * L::q_half + (s >> 2) * L::q_half +
+                                                                (s & 3) * 32) >> 4);
+                                tc::mma_bf16(d_s, dk0 + (uint64_t)st * kStageStep + ko, dq + qo, idesc_s, s > 0 ? 1u : 0u);
+                            }
+                            tc::mma_commit(bar(kBarSFull + b));
+                            tc::mma_commit(bar(kBarEmptyK + st));
+                            if (gs < 64)
+                                KPROF(a, 300 + gs);
+                            ++gs;
+                            if (++ts == nts) {
+                                tc::mma_commit(bar(qfree_bar(is % L::QB)));
+                                ++is;
+                                ts = 0;
+                                nts = -1;
+                            }
+                            progressed = true;
+                        }
+                    }
+                    // P.V(gp): needs V(gp), P(gp) and, for a unit's first tile,
+                    // its O buffer read out by the epilogue of the unit two back.
+                    if (gp < gs) {
+                        const int stp = gp % VST, ob = ip & 1;
+                        if (tc::mbar_test(bar(kBarFullV + stp), (gp / VST) & 1) &&
+                            tc::mbar_test(bar(kBarPFull), gp & 1) &&
+                            (tp > 0 || ip < 2 || tc::mbar_test(bar(kBarOFree + ob), ((ip - 2) >> 1) & 1))) {
+                            tc::fence_after_sync();
+                            const uint32_t d_o = tmem + 256 + (uint32_t)(ob * 128);
+    #pragma unroll
+                            for (int s = 0; s < 8; ++s) {
+                                const uint64_t so = (uint64_t)((s * 2048) >> 4);
+                                tc::mma_bf16(d_o, dv0 + (uint64_t)stp * kStageStep + so, dp + so, idesc_o,
+                                             (tp > 0 || s > 0) ? 1u : 0u);
+                            }
+                            tc::mma_commit(bar(kBarPvDone));
+                            tc::mma_commit(bar(kBarEmptyV + stp));
+                            if (gp < 64)
+                                KPROF(a, 400 + gp);
+                            ++gp;
+                            if (++tp == ((ip & 1) ? ntq1 : ntq0)) {
+                                ++ip;
+                                tp = 0;
+                            }
+                            progressed = true;
+                        }
+                    }
+                    if (progressed)
+                        polls = 0;
+                    else if (++polls > (1u << 24))
+                        ok = false;
+                }
+                if (!ok)
+                    if (!*err) *err = 208;
+            }
+        } else if (warp >= 12) {
+            // ---------------- epilogue warpgroup ----------------
+            // Per unit, once both softmax warpgroups have handed over their
+            // column sums: O^T / l from TMEM buffer ob into the fp32 partials
+            // (thread je owns head dim je, the TMEM lane of its warp quarter),
+            // then the buffer is free for the unit two on.
+            const int je = tid - 384;
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            for (int i = 0;; ++i) {
+                const int ob = i & 1;
+                const bool okw = tc::mbar_wait(bar(kBarEpiFull + ob), (i >> 1) & 1);
+                if (tc::named_sync_or(3, 128, !okw)) {
+                    if (!*err) *err = 211;
+                    break;
+                }
+                tc::fence_after_sync();
+                const int R = epi_info[ob * 4];
+                if (R == -1)
+                    break;
+                if (R >= 0) {
+                    const uint32_t tmem_ob = tmem + 256 + (uint32_t)(ob * 128) + lane_off;
+    #pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int rows_w = w == 0 ? (R < NPH ? R : NPH) : (R > NPH ? R - NPH : 0);
+                        if (epi_info[ob * 4 + 1 + w])
+                            continue;
+                        const float *linv_e = epi + (ob * 2 + w) * 128;
+                        const int32_t *orow_e = reinterpret_cast<const int32_t *>(linv_e + 64);
+    #pragma unroll
+                        for (int g = 0; g < NPH; g += 16) {
+                            if (g >= rows_w)
+                                break;
+                            float o[16];
+                            tc::tmem_ld16(tmem_ob + (uint32_t)(w * NPH + g), o);
+    #pragma unroll
+                            for (int c2 = 0; c2 < 16; ++c2) {
+                                const int cc = g + c2;
+                                if (cc < rows_w)
+                                    a.o_part[(size_t)orow_e[cc] * kD + je] = o[c2] * linv_e[cc];
+                            }
+                        }
+                    }
+                }
+                tc::fence_before_sync();
+                tc::named_sync(3, 128);
+                if (je == 0)
+                    tc::mbar_arrive(bar(kBarOFree + ob));
+                if (je == 0 && i < 8)
+                    KPROF(a, 700 + i);
+                if (R < 0)
+                    break;
+            }
+    }
     } else {
+        tc::setmaxnreg_inc<kRegsSoftmax>();
         // ---------------- softmax warpgroups ----------------
         // While the first tile loads: warm L2 with the plan's arrays, the
         // node page offsets and q, which the metadata warp and the producers
@@ -756,8 +829,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         // Warpgroup w owns columns [w*NPH, w*NPH + NPH) of S^T and O^T.
         const int w = warp >> 2, wt = warp & 3, j = tid & 127;
         const uint32_t nb_id = 1 + (uint32_t)w;
-        float *m_s = stat + w * 256, *alpha_s = m_s + 64, *linv = m_s + 128;
-        int32_t *orow_s = reinterpret_cast<int32_t *>(m_s + 192);   // partial row of each column
+        float *m_s = stat + w * 256, *alpha_s = m_s + 64;
         float *redw = red + w * 256;
         const uint32_t lane_off = (uint32_t)(wt * 32) << 16;
         const uint32_t col0 = (uint32_t)(w * NPH);
@@ -786,18 +858,30 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 redw[wt * 64 + g + lane] = reduce_scatter32<true>(tmp, lane);
             }
         };
+        // Tells the epilogue warpgroup that no unit follows (R = -1) or that
+        // this one failed and none follows (R = -2).
+        auto end_epilogue = [&](int ob, int code) {
+            if (j == 0) {
+                if (w == 0)
+                    epi_info[ob * 4] = code;
+                tc::mbar_arrive(bar(kBarEpiFull + ob));
+            }
+        };
         int gseq = 0;
         for (int i = 0;; ++i) {
             const int ub = i & 1, ob = i & 1;
             const bool okw = tc::mbar_wait(bar(kBarUFull + ub), (i >> 1) & 1);
             if (tc::named_sync_or(nb_id, 128, !okw)) {
                 if (!*err) *err = 209;
+                end_epilogue(ob, -2);
                 break;
             }
             const UnitInfo ui = uinfo[ub];
             tc::named_sync(nb_id, 128);
-            if (ui.ntiles < 0)
-                break;   // no more units
+            if (ui.ntiles < 0) {
+                end_epilogue(ob, -1);   // no more units
+                break;
+            }
             if (j == 0)
                 tc::mbar_arrive(bar(kBarUEmpty + ub));
             const int R = ui.R, ntiles = ui.ntiles;
@@ -935,38 +1019,31 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 redw[wt * 64 + g + lane] = reduce_scatter32<false>(tmp, lane);
             }
             tc::named_sync(nb_id, 128);
-            if (j < NPH) {
-                linv[j] = 1.f / (redw[j] + redw[64 + j] + redw[128 + j] + redw[192 + j]);
-                const int r = w * NPH + j;
-                orow_s[j] = (ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
-            }
-            tc::named_sync(nb_id, 128);
-            if (tid == 0 && i < 8)
-                KPROF(a, 711 + 4 * i);
-            if (!failed) {
-#pragma unroll
-                for (int g = 0; g < NPH; g += 16) {
-                    float o[16];
-                    tc::tmem_ld16(tmem_o + g, o);
-#pragma unroll
-                    for (int c2 = 0; c2 < 16; ++c2) {
-                        const int cc = g + c2;
-                        if (cc < rows_w)
-                            a.o_part[(size_t)orow_s[cc] * kD + j] = o[c2] * linv[cc];
-                    }
-                }
-                if (j < rows_w)
-                    a.lse_part[orow_s[j]] = m_s[j] - log2f(linv[j]);
-            }
             if (tid == 0 && i < 8)
                 KPROF(a, 712 + 4 * i);
-            // O buffer ob and the statistics are free for the unit two on.
-            tc::fence_before_sync();
+            // Column sums and partial rows for the epilogue warpgroup, which
+            // reads O (buffer ob) out of TMEM; the lse partials go out here.
+            float *linv_e = epi + (ob * 2 + w) * 128;
+            int32_t *orow_e = reinterpret_cast<int32_t *>(linv_e + 64);
+            if (j < NPH) {
+                const float li = 1.f / (redw[j] + redw[64 + j] + redw[128 + j] + redw[192 + j]);
+                const int r = w * NPH + j;
+                const int orow = (ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
+                linv_e[j] = li;
+                orow_e[j] = orow;
+                if (j < rows_w && !failed)
+                    a.lse_part[orow] = m_s[j] - log2f(li);
+            }
+            if (j == 0) {
+                epi_info[ob * 4 + 1 + w] = failed ? 1 : 0;
+                if (w == 0)
+                    epi_info[ob * 4] = failed ? -2 : R;
+            }
             tc::named_sync(nb_id, 128);
             if (j == 0)
-                tc::mbar_arrive(bar(kBarOFree + ob));
+                tc::mbar_arrive(bar(kBarEpiFull + ob));
             if (tid == 0 && i < 8)
-                KPROF(a, 700 + i);
+                KPROF(a, 711 + 4 * i);
             if (tid == 0 && blockIdx.x < 1024)
                 KPROF_ANY(a, 1024 + blockIdx.x);
             if (failed)

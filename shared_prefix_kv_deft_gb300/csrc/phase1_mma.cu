@@ -771,6 +771,13 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             // then the buffer is free for the unit two on.
             const int je = tid - 384;
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            // While the first unit runs: warm L2 with the plan's arrays, the
+            // node page offsets and q, which the metadata warp and the
+            // producers walk in chains of dependent loads (prefetches hold
+            // the issuing warp, so this otherwise idle warpgroup issues them).
+            prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, je, 128);
+            prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, je, 128);
+            prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * kD * 2, blockIdx.x, gridDim.x, je, 128);
             for (int i = 0;; ++i) {
                 const int ob = i & 1;
                 const bool okw = tc::mbar_wait(bar(kBarEpiFull + ob), (i >> 1) & 1);
@@ -818,14 +825,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     }
     } else {
         tc::setmaxnreg_inc<kRegsSoftmax>();
+        if (tid == 0)
+            KPROF(a, 6);
         // ---------------- softmax warpgroups ----------------
-        // While the first tile loads: warm L2 with the plan's arrays, the
-        // node page offsets and q, which the metadata warp and the producers
-        // walk in chains of dependent loads (prefetches hold the issuing
-        // warp, so the idle warps issue them).
-        prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid, 256);
-        prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid, 256);
-        prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * kD * 2, blockIdx.x, gridDim.x, tid, 256);
         // Warpgroup w owns columns [w*NPH, w*NPH + NPH) of S^T and O^T.
         const int w = warp >> 2, wt = warp & 3, j = tid & 127;
         const uint32_t nb_id = 1 + (uint32_t)w;
@@ -868,21 +870,27 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             }
         };
         int gseq = 0;
-        for (int i = 0;; ++i) {
+        // Unit -1 is a dry run of one tile and a unit's end, made while the
+        // first tile loads: it runs the same instructions on whatever TMEM
+        // and shared memory hold, with no waits, signals or global stores,
+        // so that the instruction fetches of this code are not paid again
+        // on the real first tile.
+        for (int i = -1;; ++i) {
+            const bool dry = i < 0;
             const int ub = i & 1, ob = i & 1;
-            const bool okw = tc::mbar_wait(bar(kBarUFull + ub), (i >> 1) & 1);
+            const bool okw = dry || tc::mbar_wait(bar(kBarUFull + ub), (i >> 1) & 1);
             if (tc::named_sync_or(nb_id, 128, !okw)) {
                 if (!*err) *err = 209;
                 end_epilogue(ob, -2);
                 break;
             }
-            const UnitInfo ui = uinfo[ub];
+            const UnitInfo ui = dry ? UnitInfo{2 * NPH, 0, 0, 1, {0, 0, 0, 0}} : uinfo[ub];
             tc::named_sync(nb_id, 128);
             if (ui.ntiles < 0) {
                 end_epilogue(ob, -1);   // no more units
                 break;
             }
-            if (j == 0)
+            if (j == 0 && !dry)
                 tc::mbar_arrive(bar(kBarUEmpty + ub));
             const int R = ui.R, ntiles = ui.ntiles;
             const int rows_w = w == 0 ? (R < NPH ? R : NPH) : (R > NPH ? R - NPH : 0);
@@ -899,7 +907,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             bool ok = true;
             for (int t = 0; t < ntiles; ++t, ++gseq) {
                 const int b = gseq & 1;
-                ok = tc::mbar_wait(bar(kBarSFull + b), (gseq >> 1) & 1);
+                ok = dry || tc::mbar_wait(bar(kBarSFull + b), (gseq >> 1) & 1);
                 tc::fence_after_sync();
                 if (tid == 0 && gseq < 64)
                     KPROF(a, 500 + gseq);
@@ -945,7 +953,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     }
                     tc::named_sync(nb_id, 128);
                 }
-                if (j == 0)
+                if (j == 0 && !dry)
                     tc::mbar_arrive(bar(kBarSFree + b));
                 // P (one buffer) may be rewritten once the previous tile's
                 // P.V is done; that P.V also finishes O before a rescale.
@@ -995,17 +1003,17 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     ok = false;
                     break;
                 }
-                if (j == 0)
+                if (j == 0 && !dry)
                     tc::mbar_arrive(bar(kBarPFull));
                 if (tid == 0 && gseq < 64)
                     KPROF(a, 600 + gseq);
             }
             // The unit's last P.V, then O / l for this warpgroup's rows.
-            if (ok) {
+            if (ok && !dry) {
                 ok = tc::mbar_wait(bar(kBarPvDone), (gseq - 1) & 1);
                 tc::fence_after_sync();
             }
-            if (tid == 0 && i < 8)
+            if (tid == 0 && i >= 0 && i < 8)
                 KPROF(a, 710 + 4 * i);
             if (!ok)
                 if (!*err) *err = 210;
@@ -1019,7 +1027,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 redw[wt * 64 + g + lane] = reduce_scatter32<false>(tmp, lane);
             }
             tc::named_sync(nb_id, 128);
-            if (tid == 0 && i < 8)
+            if (tid == 0 && i >= 0 && i < 8)
                 KPROF(a, 712 + 4 * i);
             // Column sums and partial rows for the epilogue warpgroup, which
             // reads O (buffer ob) out of TMEM; the lse partials go out here.
@@ -1031,18 +1039,23 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 const int orow = (ui.cq0 + r / G) * Hq + ui.h * G + (r % G);
                 linv_e[j] = li;
                 orow_e[j] = orow;
-                if (j < rows_w && !failed)
+                if (j < rows_w && !failed && !dry)
                     a.lse_part[orow] = m_s[j] - log2f(li);
             }
-            if (j == 0) {
+            if (j == 0 && !dry) {
                 epi_info[ob * 4 + 1 + w] = failed ? 1 : 0;
                 if (w == 0)
                     epi_info[ob * 4] = failed ? -2 : R;
             }
             tc::named_sync(nb_id, 128);
-            if (j == 0)
+            if (j == 0 && !dry)
                 tc::mbar_arrive(bar(kBarEpiFull + ob));
-            if (tid == 0 && i < 8)
+            if (dry) {
+                gseq = 0;
+                if (tid == 0)
+                    KPROF(a, 8);
+            }
+            if (tid == 0 && i >= 0 && i < 8)
                 KPROF(a, 711 + 4 * i);
             if (tid == 0 && blockIdx.x < 1024)
                 KPROF_ANY(a, 1024 + blockIdx.x);

@@ -1,0 +1,45 @@
+"""Runs a few tree-attention steps of a named, seeded workload on cuda:0, for
+profiling captures that must stay small (a few hundred MB on the device):
+
+    python -m shared_prefix_kv_deft_gb300.profile_case <case> [steps]
+
+Cases (synthetic, seeded; the shapes of the benchmark workloads, fewer
+requests):
+    speculative_3req   3 requests x (4000-token prefix + 64-node token tree),
+                       32/32 heads, d 128 (tensor-core launch, 64 rows)
+    control_32x2048    32 independent 2048-token sequences, GQA 32/8, d 128
+                       (CUDA-core launch, 4 rows)
+    few_shot           the few-shot tree (4096-token prefix + 32 x 256)
+"""
+import sys
+
+import torch
+
+import workloads as W
+import shared_prefix_kv_deft_gb300 as deft
+
+CASES = {
+    "speculative_3req": lambda: W.speculative_forest(requests=3),
+    "control_32x2048": lambda: W.imbalance_tree(control=True, leaves=32),
+    "few_shot": lambda: W.config(2),
+}
+
+
+def main(argv):
+    spec = CASES[argv[1]]()
+    steps = int(argv[2]) if len(argv) > 2 else 4
+    lay = W.paged_layout(spec)
+    t = W.make_tensors(spec, lay, device="cuda")
+    npo = torch.from_numpy(lay.node_page_off).cuda()
+    pid = torch.from_numpy(lay.page_id).cuda()
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, spec.gqa_group)
+    plan.upload()
+    bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim)
+    for _ in range(steps):
+        deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)
+    torch.cuda.synchronize()
+    print("ok", spec.name)
+
+
+if __name__ == "__main__":
+    main(sys.argv)

@@ -438,6 +438,27 @@ def main():
     }
 
     if not args.no_extras:
+        # The same step captured once into a CUDA graph and replayed (launch
+        # overhead of the host call removed; the kernels are the same).
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                step()   # warm the side stream
+            stream.wait_stream(side)
+            torch.cuda.synchronize(dev)
+            with torch.cuda.graph(g):
+                step()
+            for _ in range(3):
+                flush_l2()
+                g.replay()
+            gms, _, _, _ = timed(g.replay, args.steps)
+            line["cuda_graph"] = {"us_per_step": statistics.mean(gms) * 1e3,
+                                  "us_per_step_median": statistics.median(gms) * 1e3,
+                                  "steps": args.steps}
+        except Exception as e:   # report, do not fail the bench line
+            line["cuda_graph"] = {"error": str(e).splitlines()[0][:200]}
         # In-run IO comparison: the per-query flash-decoding form.
         def naive_step():
             deft.deft_naive_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)

@@ -131,6 +131,30 @@ def test_results_are_bitwise_repeatable(deft):
     np.testing.assert_array_equal(a[1], b[1])
 
 
+def test_step_captured_in_a_cuda_graph(deft):
+    """The step is graph-capturable: a captured step, replayed several times
+    (the work queues reset themselves between launches), gives the eager
+    step's results bit for bit, on a tree with both kernel families."""
+    spec = W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4, head_dim=128)
+    case = Case(deft, dense_inputs(spec, seed=5), 64)
+    ref_out, ref_lse = case.run()
+    s = case.spec
+    bufs = deft.alloc_buffers(case.plan, s.num_queries, s.num_q_heads, s.head_dim)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        deft.deft_tree_attn(case.q, case.k, case.v, case.npo, case.pid, case.plan, bufs=bufs)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        deft.deft_tree_attn(case.q, case.k, case.v, case.npo, case.pid, case.plan, bufs=bufs)
+    for _ in range(3):
+        bufs.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(bufs.out.float().cpu().numpy().astype(np.float64), ref_out)
+        np.testing.assert_array_equal(bufs.lse.cpu().numpy().astype(np.float64), ref_lse)
+
+
 def test_abi_rejects_bad_calls(deft):
     spec = W.tiny_tree()
     case = Case(deft, dense_inputs(spec, seed=2), 64)

@@ -51,12 +51,12 @@ def load(path: Optional[str] = None):
     lib.oracle_paths.restype = i64
     lib.oracle_cover.argtypes = [P, i32, P, i32, P]
     lib.oracle_cover.restype = ctypes.c_int
-    lib.oracle_token_counts.argtypes = [P, P, i32, P, i32, P, P]
+    lib.oracle_token_counts.argtypes = [P, P, i32, P, P, i32, P, P]
     lib.oracle_token_counts.restype = ctypes.c_int
-    lib.oracle_tree_attn_f64.argtypes = [P, P, P, P, P, i32, P, P, i32, P, i32, P, i32,
+    lib.oracle_tree_attn_f64.argtypes = [P, P, P, P, P, i32, P, P, i32, P, P, i32, P, i32,
                                          i32, i32, i32, f64, P, P, i32]
     lib.oracle_tree_attn_f64.restype = ctypes.c_int
-    lib.oracle_tree_attn_pieces_f64.argtypes = [P, P, P, P, P, i32, P, P, i32, P, i32,
+    lib.oracle_tree_attn_pieces_f64.argtypes = [P, P, P, P, P, i32, P, P, i32, P, P, i32,
                                                 i32, i32, i32, f64, P, i64, P, P]
     lib.oracle_tree_attn_pieces_f64.restype = ctypes.c_int
     lib.oracle_max_threads.argtypes = []
@@ -101,14 +101,20 @@ def cover(parent, query_node, lib=None) -> np.ndarray:
     return out[:, :words]
 
 
-def token_counts(parent, node_len, query_node, lib=None):
-    """(unique tokens on any path, sum over queries of path tokens)."""
+def _pos(query_pos):
+    return None if query_pos is None else _i32(query_pos)
+
+
+def token_counts(parent, node_len, query_node, query_pos=None, lib=None):
+    """(unique tokens on any path, sum over queries of path tokens); a query
+    with query_pos[q] >= 0 attends tokens 0..query_pos[q] of its own node."""
     lib = lib or load()
     parent, node_len, query_node = _i32(parent), _i32(node_len), _i32(query_node)
+    pos = _pos(query_pos)
     u = np.zeros(1, dtype=np.int64)
     v = np.zeros(1, dtype=np.int64)
     rc = lib.oracle_token_counts(_p(parent), _p(node_len), int(parent.shape[0]), _p(query_node),
-                                 int(query_node.shape[0]), _p(u), _p(v))
+                                 _p(pos), int(query_node.shape[0]), _p(u), _p(v))
     if rc != 0:
         raise ValueError("oracle_token_counts failed")
     return int(u[0]), int(v[0])
@@ -117,10 +123,12 @@ def token_counts(parent, node_len, query_node, lib=None):
 def tree_attn(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, node_page_off,
               page_id, page_size: int, parent, node_len, query_node, num_q_heads: int,
               num_kv_heads: int, head_dim: int, scale: float,
-              query_subset: Optional[Sequence[int]] = None, threads: int = 0, lib=None):
+              query_subset: Optional[Sequence[int]] = None, threads: int = 0, lib=None,
+              query_pos=None):
     """fp64 tree attention.  q_bits/k_bits/v_bits are uint16 bf16 bit arrays
     in the library's layouts.  Returns (out [n, Hq, d], lse [n, Hq]) where n
-    is the number of queries (or of `query_subset`)."""
+    is the number of queries (or of `query_subset`).  query_pos: per query,
+    the token of its node it sits at (-1 or None: the node's last)."""
     lib = lib or load()
     q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
     k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
@@ -132,9 +140,10 @@ def tree_attn(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, node_p
     nsel = nq if sub is None else int(sub.shape[0])
     out = np.zeros((nsel, num_q_heads, head_dim), dtype=np.float64)
     lse = np.zeros((nsel, num_q_heads), dtype=np.float64)
+    pos = _pos(query_pos)
     rc = lib.oracle_tree_attn_f64(_p(q_bits), _p(k_bits), _p(v_bits), _p(node_page_off),
                                   _p(page_id), page_size, _p(parent), _p(node_len),
-                                  int(parent.shape[0]), _p(query_node), nq, _p(sub), nsel,
+                                  int(parent.shape[0]), _p(query_node), _p(pos), nq, _p(sub), nsel,
                                   num_q_heads, num_kv_heads, head_dim, float(scale), _p(out),
                                   _p(lse), int(threads))
     if rc != 0:
@@ -144,7 +153,7 @@ def tree_attn(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, node_p
 
 def tree_attn_pieces(q_bits, k_bits, v_bits, node_page_off, page_id, page_size: int, parent,
                      node_len, query_node, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                     scale: float, cut: np.ndarray, lib=None):
+                     scale: float, cut: np.ndarray, lib=None, query_pos=None):
     """The split-and-merge form: every query's token sequence is cut before
     each position i with cut[i] != 0, pieces are merged by lse weight."""
     lib = lib or load()
@@ -157,9 +166,10 @@ def tree_attn_pieces(q_bits, k_bits, v_bits, node_page_off, page_id, page_size: 
     nq = int(query_node.shape[0])
     out = np.zeros((nq, num_q_heads, head_dim), dtype=np.float64)
     lse = np.zeros((nq, num_q_heads), dtype=np.float64)
+    pos = _pos(query_pos)
     rc = lib.oracle_tree_attn_pieces_f64(_p(q_bits), _p(k_bits), _p(v_bits), _p(node_page_off),
                                          _p(page_id), page_size, _p(parent), _p(node_len),
-                                         int(parent.shape[0]), _p(query_node), nq, num_q_heads,
+                                         int(parent.shape[0]), _p(query_node), _p(pos), nq, num_q_heads,
                                          num_kv_heads, head_dim, float(scale), _p(cut),
                                          int(cut.shape[0]), _p(out), _p(lse))
     if rc != 0:

@@ -14,7 +14,12 @@
  *   of every node on the root-to-n path, n itself included (the Guide's
  *   ancestor map starts each node's list with the node itself, section
  *   "End-to-End Implementation", TreeTopologyManager).  Tokens outside that
- *   path are masked to -inf.  For query head h (KV head h / G):
+ *   path are masked to -inf.  A query may instead sit at token position
+ *   p = query_pos[q] of its node (tree verification with multi-token
+ *   nodes): the node's tokens are a chain, so it attends tokens 0..p of its
+ *   own node and every token of the nodes above (the Guide's causal tree
+ *   mask, section "Deep Dive", taken at token granularity); query_pos NULL
+ *   or p < 0 means the node's last token.  For query head h (KV head h / G):
  *       s_j   = (q . k_j) * scale
  *       m     = max_j s_j,  l = sum_j exp(s_j - m)
  *       out   = sum_j exp(s_j - m) v_j / l
@@ -123,32 +128,45 @@ int oracle_cover(const int32_t *parent, int32_t num_nodes, const int32_t *query_
     return 0;
 }
 
+/* Tokens of `node` (on the path of a query at node qnode) that the query
+ * attends: all of them, or 0..pos of its own node when it sits at pos. */
+static int32_t tokens_taken(const int32_t *node_len, int32_t node, int32_t qnode, int32_t pos)
+{
+    if (node == qnode && pos >= 0)
+        return pos + 1;
+    return node_len[node];
+}
+
 /* Tokens on at least one query path (each counted once) and the sum over
- * queries of their path token counts.  Returns 0 or -1. */
+ * queries of their path token counts.  query_pos may be NULL.  Returns 0 or
+ * -1 (bad tree, or a position outside its node). */
 int oracle_token_counts(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-                        const int32_t *query_node, int32_t num_queries,
+                        const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
                         int64_t *unique_tokens, int64_t *naive_tokens)
 {
     int32_t *buf = (int32_t *)malloc(sizeof(int32_t) * (size_t)(num_nodes > 0 ? num_nodes : 1));
-    char *seen = (char *)calloc((size_t)(num_nodes > 0 ? num_nodes : 1), 1);
+    /* taken[n]: how many leading tokens of node n some query attends */
+    int32_t *taken = (int32_t *)calloc((size_t)(num_nodes > 0 ? num_nodes : 1), sizeof(int32_t));
     int64_t uniq = 0, naive = 0;
     for (int32_t q = 0; q < num_queries; ++q) {
         int32_t len = path_of(parent, num_nodes, query_node[q], buf);
-        if (len < 0) {
+        int32_t pos = query_pos ? query_pos[q] : -1;
+        if (len < 0 || pos >= node_len[query_node[q]]) {
             free(buf);
-            free(seen);
+            free(taken);
             return -1;
         }
         for (int32_t i = 0; i < len; ++i) {
-            naive += node_len[buf[i]];
-            if (!seen[buf[i]]) {
-                seen[buf[i]] = 1;
-                uniq += node_len[buf[i]];
-            }
+            int32_t take = tokens_taken(node_len, buf[i], query_node[q], pos);
+            naive += take;
+            if (take > taken[buf[i]])
+                taken[buf[i]] = take;
         }
     }
+    for (int32_t n = 0; n < num_nodes; ++n)
+        uniq += taken[n];
     free(buf);
-    free(seen);
+    free(taken);
     *unique_tokens = uniq;
     *naive_tokens = naive;
     return 0;
@@ -200,16 +218,18 @@ static double attend(const uint16_t *qv, const uint16_t *k_pages, const uint16_t
     return m + log(l);
 }
 
-/* Expand query q's path into its token list (root first, tokens in order). */
+/* Expand query q's path into its token list (root first, tokens in order);
+ * qpos >= 0: the query sits at that token of its node. */
 static int64_t path_tokens(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-                           int32_t qnode, int32_t *pathbuf, int32_t *tok_node, int32_t *tok_idx)
+                           int32_t qnode, int32_t qpos, int32_t *pathbuf, int32_t *tok_node,
+                           int32_t *tok_idx)
 {
     int32_t len = path_of(parent, num_nodes, qnode, pathbuf);
-    if (len < 0)
+    if (len < 0 || qpos >= node_len[qnode])
         return -1;
     int64_t nt = 0;
     for (int32_t i = 0; i < len; ++i)
-        for (int32_t t = 0; t < node_len[pathbuf[i]]; ++t) {
+        for (int32_t t = 0; t < tokens_taken(node_len, pathbuf[i], qnode, qpos); ++t) {
             tok_node[nt] = pathbuf[i];
             tok_idx[nt] = t;
             ++nt;
@@ -245,7 +265,7 @@ static int64_t longest_path_tokens(const int32_t *parent, const int32_t *node_le
 int oracle_tree_attn_f64(const uint16_t *q, const uint16_t *k_pages, const uint16_t *v_pages,
                          const int32_t *node_page_off, const int32_t *page_id, int32_t page_size,
                          const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-                         const int32_t *query_node, int32_t num_queries,
+                         const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
                          const int32_t *query_subset, int32_t n_subset,
                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                          double scale, double *out, double *lse, int32_t threads)
@@ -281,8 +301,8 @@ int oracle_tree_attn_f64(const uint16_t *q, const uint16_t *k_pages, const uint1
             int32_t i = (int32_t)(w / num_q_heads);
             int32_t h = (int32_t)(w % num_q_heads);
             int32_t qi = query_subset ? query_subset[i] : i;
-            int64_t nt = path_tokens(parent, node_len, num_nodes, query_node[qi], pathbuf,
-                                     tok_node, tok_idx);
+            int64_t nt = path_tokens(parent, node_len, num_nodes, query_node[qi],
+                                     query_pos ? query_pos[qi] : -1, pathbuf, tok_node, tok_idx);
             if (nt < 0) {
                 bad = 1;
                 continue;
@@ -316,9 +336,9 @@ int oracle_tree_attn_pieces_f64(const uint16_t *q, const uint16_t *k_pages,
                                 const uint16_t *v_pages, const int32_t *node_page_off,
                                 const int32_t *page_id, int32_t page_size,
                                 const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-                                const int32_t *query_node, int32_t num_queries,
-                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                double scale, const uint8_t *cut, int64_t cut_len,
+                                const int32_t *query_node, const int32_t *query_pos,
+                                int32_t num_queries, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, double scale, const uint8_t *cut, int64_t cut_len,
                                 double *out, double *lse)
 {
     if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || page_size <= 0)
@@ -337,8 +357,17 @@ int oracle_tree_attn_pieces_f64(const uint16_t *q, const uint16_t *k_pages,
     double *piece_out = (double *)malloc(sizeof(double) * (size_t)head_dim * cap);
     double *piece_lse = (double *)malloc(sizeof(double) * cap);
     for (int32_t qi = 0; qi < num_queries; ++qi) {
-        int64_t nt = path_tokens(parent, node_len, num_nodes, query_node[qi], pathbuf,
-                                 tok_node, tok_idx);
+        int64_t nt = path_tokens(parent, node_len, num_nodes, query_node[qi],
+                                 query_pos ? query_pos[qi] : -1, pathbuf, tok_node, tok_idx);
+        if (nt < 0) {
+            free(pathbuf);
+            free(tok_node);
+            free(tok_idx);
+            free(scores);
+            free(piece_out);
+            free(piece_lse);
+            return -1;
+        }
         for (int32_t h = 0; h < num_q_heads; ++h) {
             const uint16_t *qv = q + ((size_t)qi * num_q_heads + h) * head_dim;
             int64_t npieces = 0;

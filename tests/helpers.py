@@ -96,8 +96,9 @@ def subtree_sets(parent: np.ndarray):
 
 def dense_reference(inp: DenseInputs):
     """Textbook masked softmax attention over ALL tokens with the tree mask
-    M[q, j] = 0 if token j's node has query q's node in its subtree, else
-    -inf.  fp64, numpy."""
+    M[q, j] = 0 if token j's node has query q's node in its subtree (and, in
+    q's own node, j's position is at most q's position when it has one),
+    else -inf.  fp64, numpy."""
     spec = inp.spec
     sub = subtree_sets(spec.parent)
     Q, Hq, Hkv, d = spec.num_queries, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
@@ -105,9 +106,12 @@ def dense_reference(inp: DenseInputs):
     T = inp.k_tok.shape[0]
     mask = np.full((Q, T), -np.inf)
     for qi in range(Q):
+        pos = -1 if spec.query_pos is None else int(spec.query_pos[qi])
         for j in range(T):
             if spec.query_node[qi] in sub[inp.tok_node[j]]:
-                mask[qi, j] = 0.0
+                own = inp.tok_node[j] == spec.query_node[qi]
+                if not (own and pos >= 0 and inp.tok_pos[j] > pos):
+                    mask[qi, j] = 0.0
     qf = bits_to_f64(inp.q_bits)
     out = np.zeros((Q, Hq, d))
     lse = np.full((Q, Hq), -np.inf)
@@ -132,4 +136,5 @@ def run_oracle(inp: DenseInputs, query_subset=None, threads=0, lib=None):
     return oracle.tree_attn(inp.q_bits, inp.k_pages, inp.v_pages, inp.layout.node_page_off,
                             inp.layout.page_id, inp.layout.page_size, s.parent, s.node_len,
                             s.query_node, s.num_q_heads, s.num_kv_heads, s.head_dim, inp.scale,
-                            query_subset=query_subset, threads=threads, lib=lib)
+                            query_subset=query_subset, threads=threads, lib=lib,
+                            query_pos=s.query_pos)

@@ -32,11 +32,13 @@ MUTATIONS = {
         "const uint16_t *qv = q + ((size_t)qi * num_q_heads + h) * head_dim;\n            double *o = out + ((size_t)i",
         "const uint16_t *qv = q + ((size_t)h * num_queries + qi) * head_dim;\n            double *o = out + ((size_t)i"),
     "cover_bit_uses_word_index": ("|= (uint64_t)1 << (q % 64);", "|= (uint64_t)1 << (q / 64);"),
-    "unique_tokens_not_deduplicated": ("if (!seen[buf[i]]) {", "if (1) {"),
+    "unique_tokens_not_deduplicated": ("if (take > taken[buf[i]])\n                taken[buf[i]] = take;",
+                                       "uniq += take;"),
     "path_not_reversed": ("for (int32_t i = 0; i < len / 2; ++i) {", "for (int32_t i = 0; i < 0; ++i) {"),
     "merge_weight_sign_flipped": ("double w = exp(piece_lse[p] - M);", "double w = exp(M - piece_lse[p]);"),
-    "last_token_of_node_dropped": ("for (int32_t t = 0; t < node_len[pathbuf[i]]; ++t) {",
-                                   "for (int32_t t = 0; t + 1 < node_len[pathbuf[i]]; ++t) {"),
+    "last_token_of_node_dropped": ("for (int32_t t = 0; t < tokens_taken(node_len, pathbuf[i], qnode, qpos); ++t) {",
+                                   "for (int32_t t = 0; t + 1 < tokens_taken(node_len, pathbuf[i], qnode, qpos); ++t) {"),
+    "own_node_position_off_by_one": ("        return pos + 1;\n", "        return pos;\n"),
 }
 
 
@@ -72,6 +74,18 @@ def pins_pass(lib) -> bool:
                 scale=inp.scale)[0, 0]
             if not _close(out[i, 0], ref[e].numpy()):
                 return False
+        # a node with a query at every position == causal self-attention
+        spec = W.causal_node_tree(9, parent_len=5)
+        inp = dense_inputs(spec, seed=6)
+        out, _ = run_oracle(inp, lib=lib)
+        K = torch.from_numpy(inp.k_tok[:, 0]); V = torch.from_numpy(inp.v_tok[:, 0])
+        qf = torch.from_numpy(bits_to_f64(inp.q_bits))
+        qfull = torch.zeros((14, spec.head_dim), dtype=torch.float64)
+        qfull[5:] = qf[:, 0]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qfull[None, None], K[None, None], V[None, None], is_causal=True, scale=inp.scale)[0, 0]
+        if not _close(out[:, 0], ref[5:].numpy()):
+            return False
         # closed form: q = 0 -> mean, ln count
         spec = W.random_tree(101, zero_len_prob=0.0)
         inp = dense_inputs(spec, seed=2, zero_q=True)

@@ -223,3 +223,88 @@ def test_worked_io_example_of_the_guide():
     uniq, naive = oracle.token_counts(spec.parent, spec.node_len, spec.query_node)
     assert uniq == prefix + nq
     assert naive == nq * prefix + anc
+
+
+# ---------------------------------------------------------------------------
+# Queries at token positions of multi-token nodes (tree verification / node
+# prefill: the Guide's causal tree mask, section "Deep Dive", at token level)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("seed", range(12))
+def test_positions_match_dense_masked_attention(seed):
+    """Random trees with queries at random positions of their nodes against
+    the brute-force masked softmax (mask built from subtree sets and the
+    token positions)."""
+    spec = W.positions_tree(seed, q_heads=4, kv_heads=2)
+    inp = dense_inputs(spec, seed=seed)
+    out, lse = run_oracle(inp)
+    ref, ref_lse = dense_reference(inp)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("length,parent_len", [(9, 0), (33, 5), (1, 16), (70, 17)])
+def test_node_with_a_query_at_every_position_is_causal_attention(length, parent_len):
+    """Queries at positions 0..L-1 of one node (under a root of parent_len
+    tokens) equal causal self-attention over root + node, computed by torch's
+    scaled_dot_product_attention."""
+    spec = W.causal_node_tree(length, q_heads=2, kv_heads=1, parent_len=parent_len)
+    inp = dense_inputs(spec, seed=length)
+    out, _ = run_oracle(inp)
+    T = parent_len + length
+    K = torch.from_numpy(inp.k_tok[:, 0]); V = torch.from_numpy(inp.v_tok[:, 0])
+    qf = torch.from_numpy(bits_to_f64(inp.q_bits))
+    for h in range(spec.num_q_heads):
+        qfull = torch.zeros((T, spec.head_dim), dtype=torch.float64)
+        qfull[parent_len:] = qf[:, h]
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            qfull[None, None], K[None, None], V[None, None], is_causal=True,
+            scale=inp.scale)[0, 0]
+        np.testing.assert_allclose(out[:, h], ref[parent_len:].numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("length", [1, 6, 19])
+def test_positions_equal_a_chain_of_one_token_nodes(length):
+    """A node of L tokens with a query at each position gives bit for bit
+    the results of a chain of L one-token nodes with a query at each node
+    (the same tokens, attended in the same order)."""
+    a = W.causal_node_tree(length, parent_len=4)
+    b = W.chain_tree([4] + [1] * length, q_heads=a.num_q_heads, kv_heads=a.num_kv_heads,
+                     head_dim=a.head_dim)
+    b.query_node = np.arange(1, length + 1, dtype=np.int32)
+    ia, ib = dense_inputs(a, seed=9), dense_inputs(b, seed=9)
+    np.testing.assert_array_equal(ia.q_bits, ib.q_bits)
+    oa, la = run_oracle(ia)
+    ob, lb = run_oracle(ib)
+    np.testing.assert_array_equal(oa, ob)
+    np.testing.assert_array_equal(la, lb)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_last_position_is_the_whole_node(seed):
+    spec = W.positions_tree(seed)
+    tip = spec.node_len[spec.query_node] - 1
+    spec.query_pos = np.where(spec.node_len[spec.query_node] > 0, tip, -1).astype(np.int32)
+    inp = dense_inputs(spec, seed=seed)
+    out, lse = run_oracle(inp)
+    spec.query_pos = None
+    out2, lse2 = run_oracle(inp)
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(lse, lse2)
+
+
+def test_position_token_counts_closed_form():
+    L, P = 23, 7
+    spec = W.causal_node_tree(L, parent_len=P)
+    uniq, naive = oracle.token_counts(spec.parent, spec.node_len, spec.query_node,
+                                      query_pos=spec.query_pos)
+    assert uniq == P + L
+    assert naive == sum(P + i + 1 for i in range(L))
+    # only the first 3 tokens of the node attended by anyone
+    pos = np.array([0, 2, 1], dtype=np.int32)
+    uniq, naive = oracle.token_counts(spec.parent, spec.node_len, np.array([1, 1, 1], np.int32),
+                                      query_pos=pos)
+    assert uniq == P + 3 and naive == 3 * P + 1 + 3 + 2
+    with pytest.raises(ValueError):
+        oracle.token_counts(spec.parent, spec.node_len, np.array([1], np.int32),
+                            query_pos=np.array([L], np.int32))

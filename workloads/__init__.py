@@ -48,6 +48,10 @@ class TreeSpec:
     shuffle_pages: bool = False
     seed: int = 0
     notes: dict = field(default_factory=dict)
+    # Per query, the token of its node it sits at (tree verification with
+    # multi-token nodes: it attends tokens 0..p of its own node); None: every
+    # query sits at its node's last token.
+    query_pos: Optional[np.ndarray] = None
 
     @property
     def num_nodes(self) -> int:
@@ -245,6 +249,37 @@ def chain_tree(lengths: List[int], q_heads: int = 2, kv_heads: int = 1,
                     q_heads, kv_heads, head_dim, seed=31337)
 
 
+def causal_node_tree(length: int, q_heads: int = 2, kv_heads: int = 1, head_dim: int = 64,
+                     parent_len: int = 0) -> TreeSpec:
+    """Prefill of one node: a `length`-token node (under an optional
+    `parent_len`-token root) with a query at every one of its positions, so
+    that query i attends the root and tokens 0..i: causal self-attention."""
+    if parent_len:
+        parent, node_len, node = [-1, 0], [parent_len, length], 1
+    else:
+        parent, node_len, node = [-1], [length], 0
+    spec = TreeSpec(f"causal_node_{parent_len}+{length}", _arr(parent), _arr(node_len),
+                    _arr([node] * length), q_heads, kv_heads, head_dim, seed=3000 + length)
+    spec.query_pos = _arr(list(range(length)))
+    return spec
+
+
+def positions_tree(seed: int, max_nodes: int = 12, max_len: int = 40, max_queries: int = 16,
+                   q_heads: int = 2, kv_heads: int = 1, head_dim: int = 64) -> TreeSpec:
+    """A random tree whose queries sit at random token positions of their
+    nodes (-1 for some: the node's last token), several per node."""
+    spec = random_tree(seed, max_nodes=max_nodes, max_len=max_len, max_queries=max_queries,
+                       q_heads=q_heads, kv_heads=kv_heads, head_dim=head_dim, zero_len_prob=0.0)
+    rng = random.Random(7000 + seed)
+    pos = []
+    for n in spec.query_node:
+        L = int(spec.node_len[n])
+        pos.append(-1 if L == 0 or rng.random() < 0.25 else rng.randrange(L))
+    spec.query_pos = _arr(pos)
+    spec.name = f"positions_{seed}"
+    return spec
+
+
 def heap_example_tree(prefix: int = 1024, tree_nodes: int = 16, head_dim: int = 64) -> TreeSpec:
     """The simulator example of the aifetchly "DeFT Guide" (section "End-to-End
     Implementation"): a 1024-token prefix and 16 one-token candidate nodes in
@@ -268,9 +303,11 @@ def relabel(spec: TreeSpec, perm: np.ndarray) -> TreeSpec:
         parent[perm[old]] = -1 if p < 0 else perm[p]
         node_len[perm[old]] = spec.node_len[old]
     query = perm[spec.query_node].astype(np.int32)
-    return TreeSpec(spec.name + "_relabelled", parent, node_len, query, spec.num_q_heads,
-                    spec.num_kv_heads, spec.head_dim, spec.k_scale, spec.shuffle_pages,
-                    spec.seed)
+    out = TreeSpec(spec.name + "_relabelled", parent, node_len, query, spec.num_q_heads,
+                   spec.num_kv_heads, spec.head_dim, spec.k_scale, spec.shuffle_pages,
+                   spec.seed)
+    out.query_pos = None if spec.query_pos is None else spec.query_pos.copy()
+    return out
 
 
 # ---------------------------------------------------------------------------

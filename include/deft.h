@@ -133,6 +133,22 @@ int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
               const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
               int32_t gqa_group, deft_plan_t **out);
 
+/*
+ * deft_plan_at -- deft_plan for queries that sit at token positions of their
+ * nodes (tree verification or prefill with multi-token nodes; the Guide's
+ * causal tree mask, section "Deep Dive", taken at token granularity).
+ *   query_pos[q] in [-1, node_len[query_node[q]]): the query attends tokens
+ *   0..query_pos[q] of its own node and every token of the nodes above it;
+ *   -1 means the node's last token, as in deft_plan.  query_pos NULL: all
+ *   -1 (exactly deft_plan).  A position outside its node: DEFT_ERANGE.
+ * A node holding queries at several positions is cut where each query's
+ * part ends, so that every segment keeps one query set; the kernels run the
+ * plan unchanged.  Other arguments, results and errors as deft_plan.
+ */
+int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+                 const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+                 int32_t chunk_target, int32_t gqa_group, deft_plan_t **out);
+
 /* Plan statistics (host).  DEFT_EINVAL on null arguments. */
 int deft_plan_stats_get(const deft_plan_t *plan, deft_plan_stats *out);
 

@@ -210,9 +210,9 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
 
 extern "C" {
 
-int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-              const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
-              int32_t gqa_group, deft_plan_t **out)
+int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+                 const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+                 int32_t chunk_target, int32_t gqa_group, deft_plan_t **out)
 {
     if (!out)
         return DEFT_EINVAL;
@@ -222,8 +222,8 @@ int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
         return DEFT_ENOMEM;
     int rc;
     try {
-        rc = deft::build_plan(parent, node_len, num_nodes, query_node, num_queries, chunk_target,
-                              gqa_group, p);
+        rc = deft::build_plan(parent, node_len, num_nodes, query_node, query_pos, num_queries,
+                              chunk_target, gqa_group, p);
     } catch (const std::bad_alloc &) {
         rc = DEFT_ENOMEM;
     }
@@ -238,6 +238,14 @@ int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
     p->stats.device_bytes = (int64_t)cursor;
     *out = p;
     return DEFT_OK;
+}
+
+int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+              const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
+              int32_t gqa_group, deft_plan_t **out)
+{
+    return deft_plan_at(parent, node_len, num_nodes, query_node, nullptr, num_queries, chunk_target,
+                        gqa_group, out);
 }
 
 int deft_plan_stats_get(const deft_plan_t *plan, deft_plan_stats *out)

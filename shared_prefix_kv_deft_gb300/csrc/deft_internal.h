@@ -207,8 +207,8 @@ namespace deft {
 
 // planner.cpp
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-               const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
-               int32_t gqa_group, deft_plan_t *plan);
+               const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+               int32_t chunk_target, int32_t gqa_group, deft_plan_t *plan);
 
 // Arguments every phase-1 kernel receives.
 struct AttnArgs {

@@ -246,8 +246,8 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
 }  // namespace
 
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-               const int32_t *query_node, int32_t num_queries, int32_t chunk_target,
-               int32_t gqa_group, deft_plan_t *plan)
+               const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+               int32_t chunk_target, int32_t gqa_group, deft_plan_t *plan)
 {
     if (!parent || !node_len || !plan || num_nodes < 1 || num_queries < 0 ||
         (num_queries > 0 && !query_node))
@@ -264,6 +264,13 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
     for (int32_t q = 0; q < Q; ++q)
         if (query_node[q] < 0 || query_node[q] >= N)
             return DEFT_ERANGE;
+    // A query at position p of its node attends tokens 0..p of it (-1: all).
+    for (int32_t q = 0; q < Q && query_pos; ++q)
+        if (query_pos[q] < -1 || query_pos[q] >= node_len[query_node[q]])
+            return DEFT_ERANGE;
+    auto taken = [&](int32_t q, int32_t n) {
+        return (query_pos && n == query_node[q] && query_pos[q] >= 0) ? query_pos[q] + 1 : node_len[n];
+    };
 
     // Forest check by colouring: 0 unseen, 1 on the current upward walk, 2 done.
     {
@@ -297,8 +304,23 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
     for (int32_t q = 0; q < Q; ++q)
         for (int32_t cur = query_node[q]; cur != -1; cur = parent[cur]) {
             plan->cover[(size_t)cur * W + q / 64] |= 1ull << (q % 64);
-            naive_tokens += node_len[cur];
+            naive_tokens += taken(q, cur);
         }
+    // Per node, the queries that sit at a position before its last token
+    // (their part of the node ends there), as CSR.
+    std::vector<int32_t> own_off(N + 1, 0), own_q;
+    if (query_pos) {
+        for (int32_t q = 0; q < Q; ++q)
+            if (query_pos[q] >= 0 && query_pos[q] + 1 < node_len[query_node[q]])
+                own_off[query_node[q] + 1] += 1;
+        for (int32_t n = 0; n < N; ++n)
+            own_off[n + 1] += own_off[n];
+        own_q.resize(own_off[N]);
+        std::vector<int32_t> fill(own_off.begin(), own_off.end() - 1);
+        for (int32_t q = 0; q < Q; ++q)
+            if (query_pos[q] >= 0 && query_pos[q] + 1 < node_len[query_node[q]])
+                own_q[fill[query_node[q]]++] = q;
+    }
 
     // Children lists (ascending ids) and DFS preorder.
     std::vector<int32_t> child_off(N + 1, 0), child(N > 0 ? N : 1);
@@ -333,12 +355,8 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
     int64_t unique_tokens = 0;
     {
         Builder b(plan->tree, W);
-        for (int32_t n : plan->order) {
-            const int32_t L = node_len[n];
-            const uint64_t *m = &plan->cover[(size_t)n * W];
-            const int k = popcount_words(m, W);
-            if (L == 0 || k == 0)
-                continue;
+        // Tokens [b0, b0 + L) of node n, attended by the queries in m (k of them).
+        auto emit = [&](int32_t n, int32_t b0, int32_t L, const uint64_t *m, int k) {
             unique_tokens += L;
             if (2 * (int64_t)L <= chunk_target) {
                 // A segment that would add queries to the open chunk (its
@@ -347,8 +365,8 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
                 if (b.open && (b.cur_chunk_tokens + L > chunk_target ||
                                b.cur_chunk_segs >= kMaxSegsPerChunk || (!tiny && !b.nested(m))))
                     b.close();
-                b.add_segment(n, 0, L, m);
-                continue;
+                b.add_segment(n, b0, L, m);
+                return;
             }
             b.close();
             int64_t T = std::max<int64_t>(chunk_target, (int64_t)kSharedTokensPerRow * k * gqa_group);
@@ -357,8 +375,43 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
             int64_t piece = (L + pieces - 1) / pieces;
             piece = (piece + kPageSize - 1) / kPageSize * kPageSize;
             for (int64_t s = 0; s < L; s += piece) {
-                b.add_segment(n, (int32_t)s, (int32_t)std::min<int64_t>(piece, L - s), m);
+                b.add_segment(n, (int32_t)(b0 + s), (int32_t)std::min<int64_t>(piece, L - s), m);
                 b.close();
+            }
+        };
+        std::vector<int32_t> cuts;
+        std::vector<uint64_t> pm(W, 0);
+        for (int32_t n : plan->order) {
+            const int32_t L = node_len[n];
+            const uint64_t *m = &plan->cover[(size_t)n * W];
+            const int k = popcount_words(m, W);
+            if (L == 0 || k == 0)
+                continue;
+            if (own_off[n] == own_off[n + 1]) {
+                emit(n, 0, L, m, k);
+                continue;
+            }
+            // Queries sitting inside the node cut it where their part ends:
+            // every piece has one query set (the node's, less the queries
+            // whose position lies before the piece).
+            cuts.clear();
+            for (int32_t i = own_off[n]; i < own_off[n + 1]; ++i)
+                cuts.push_back(query_pos[own_q[i]] + 1);
+            std::sort(cuts.begin(), cuts.end());
+            cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
+            cuts.push_back(L);
+            int32_t b0 = 0;
+            for (int32_t e : cuts) {
+                std::copy(m, m + W, pm.begin());
+                for (int32_t i = own_off[n]; i < own_off[n + 1]; ++i) {
+                    const int32_t q = own_q[i];
+                    if (query_pos[q] < b0)
+                        pm[q / 64] &= ~(1ull << (q % 64));
+                }
+                const int kp = popcount_words(pm.data(), W);
+                if (kp > 0)
+                    emit(n, b0, e - b0, pm.data(), kp);
+                b0 = e;
             }
         }
         b.close();
@@ -380,12 +433,13 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
             std::fill(m.begin(), m.end(), 0);
             m[q / 64] = 1ull << (q % 64);
             for (int32_t n : path) {
+                const int32_t len = taken(q, n);
                 int32_t t = 0;
-                while (t < node_len[n]) {
+                while (t < len) {
                     if (b.open && (b.cur_chunk_tokens == chunk_target ||
                                    b.cur_chunk_segs >= kMaxSegsPerChunk))
                         b.close();
-                    const int32_t take = std::min(node_len[n] - t, chunk_target - b.cur_chunk_tokens);
+                    const int32_t take = std::min(len - t, chunk_target - b.cur_chunk_tokens);
                     b.add_segment(n, t, take, m.data());
                     t += take;
                 }

@@ -47,7 +47,8 @@ class Case:
         self.npo = torch.from_numpy(inp.layout.node_page_off).cuda()
         self.pid = torch.from_numpy(inp.layout.page_id).cuda()
         s = self.spec
-        self.plan = deft.Plan(s.parent, s.node_len, s.query_node, chunk_target, s.gqa_group)
+        self.plan = deft.Plan(s.parent, s.node_len, s.query_node, chunk_target, s.gqa_group,
+                              query_pos=s.query_pos)
         self.plan.upload()
         self.deft = deft
 
@@ -250,3 +251,28 @@ def test_tensor_core_and_cuda_core_paths_agree_with_oracle(deft, spec, ct, monke
     monkeypatch.setenv("DEFT_DISABLE_MMA", "1")
     out2, lse2 = case.run()
     assert_parity(out2, lse2, ref, ref_lse, "CUDA-core fallback")
+
+
+POSITION_SHAPES = [W.positions_tree(s, max_nodes=14, max_len=120, max_queries=24, q_heads=8,
+                                    kv_heads=2, head_dim=128) for s in range(6)]
+POSITION_SHAPES += [W.positions_tree(50 + s, max_nodes=10, max_len=60, max_queries=12)
+                    for s in range(4)]
+POSITION_SHAPES += [
+    # node prefill: a query at every token of a 96-token node under a
+    # 200-token root (GQA 4: the early pieces of the node have >= 16 rows)
+    W.causal_node_tree(96, q_heads=8, kv_heads=2, head_dim=128, parent_len=200),
+    W.causal_node_tree(40, q_heads=4, kv_heads=4, head_dim=64),
+]
+
+
+@pytest.mark.parametrize("spec", POSITION_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [16, 128])
+def test_queries_at_token_positions_match_oracle(deft, spec, ct):
+    """Tree verification / node prefill: queries at token positions of
+    multi-token nodes, tree and naive forms, against the fp64 oracle."""
+    inp = dense_inputs(spec, seed=11)
+    ref, ref_lse = run_oracle(inp)
+    case = Case(deft, inp, ct)
+    for naive in (False, True):
+        out, lse = case.run(naive=naive)
+        assert_parity(out, lse, ref, ref_lse, f"{spec.name} ct={ct} naive={naive}")

@@ -71,13 +71,21 @@ def test_plan_validation(parent, node_len, query, ct, g, status):
 
 
 def check_plan(spec: W.TreeSpec, chunk_target: int, G: int):
-    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, chunk_target, G)
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, chunk_target, G,
+                     query_pos=spec.query_pos)
     st = plan.stats
     Q, N = spec.num_queries, spec.num_nodes
     Wd = (Q + 63) // 64
     cover = oracle.cover(spec.parent, spec.query_node)
-    uniq, naive = oracle.token_counts(spec.parent, spec.node_len, spec.query_node)
+    uniq, naive = oracle.token_counts(spec.parent, spec.node_len, spec.query_node,
+                                      query_pos=spec.query_pos)
     paths = oracle.paths(spec.parent, spec.query_node)
+
+    def taken(q, n):
+        """Tokens of node n (on q's path) that query q attends."""
+        if spec.query_pos is not None and n == spec.query_node[q] and spec.query_pos[q] >= 0:
+            return int(spec.query_pos[q]) + 1
+        return int(spec.node_len[n])
 
     # Bit-exact coverage bitsets and token counts.
     np.testing.assert_array_equal(plan.get("node_cover").reshape(N, Wd), cover)
@@ -123,9 +131,13 @@ def check_plan(spec: W.TreeSpec, chunk_target: int, G: int):
                 if naive_part:
                     sq = qs
                 else:
-                    # A segment's bitmask is exactly its node's coverage set.
-                    np.testing.assert_array_equal(seg_mask[s], cover[n])
+                    # A segment's bitmask is exactly the set of queries that
+                    # attend its tokens: its node's coverage set, less the
+                    # queries sitting in the node before the segment.
                     sq = bits(seg_mask[s])
+                    want = [q for q in bits(cover[n]) if taken(q, n) > b]
+                    assert sq == want
+                    assert all(taken(q, n) >= b + L for q in sq)
                 union |= set(sq)
                 for q in sq:
                     intervals[(q, n)].append((b, L))
@@ -137,7 +149,7 @@ def check_plan(spec: W.TreeSpec, chunk_target: int, G: int):
             else:
                 assert tok <= chunk_limit
         # Exactly once: every (query, node on its path, token) in one chunk.
-        expected = {(q, n) for q in range(Q) for n in paths[q] if spec.node_len[n] > 0}
+        expected = {(q, n) for q in range(Q) for n in paths[q] if taken(q, n) > 0}
         assert set(intervals) == expected
         for (q, n), iv in intervals.items():
             iv.sort()
@@ -145,7 +157,7 @@ def check_plan(spec: W.TreeSpec, chunk_target: int, G: int):
             for b, L in iv:
                 assert b == pos, f"gap/overlap at query {q} node {n}"
                 pos = b + L
-            assert pos == spec.node_len[n]
+            assert pos == taken(q, n)
         # Slot CSR: slot s of chunk_q belongs to query chunk_q[s].
         for q in range(Q):
             sl = q_slot[q_off[q]:q_off[q + 1]].tolist()
@@ -231,3 +243,35 @@ def test_plan_is_deterministic():
 def test_empty_query_list_plans():
     plan = deft.Plan([-1, 0], [5, 5], [], 64, 1)
     assert plan.stats["num_chunks"] == 0 and plan.stats["num_slots"] == 0
+
+
+POSITIONS = [W.positions_tree(s, max_nodes=30, max_len=200, max_queries=70) for s in range(30)]
+POSITIONS += [W.causal_node_tree(L, parent_len=P) for L, P in ((40, 0), (300, 1000), (17, 33))]
+
+
+@pytest.mark.parametrize("spec", POSITIONS, ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [1, 16, 100, 512])
+def test_plan_with_query_positions(spec, ct):
+    """Queries at token positions: the same exactly-once coverage of every
+    (query, node, token) the query attends, segment masks equal to the
+    attending query sets, and the oracle's token counts."""
+    check_plan(spec, ct, 4)
+
+
+def test_plan_rejects_positions_outside_the_node():
+    spec = W.causal_node_tree(8)
+    for bad in (8, -2):
+        pos = spec.query_pos.copy()
+        pos[3] = bad
+        with pytest.raises(deft.DeftError):
+            deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, 1, query_pos=pos)
+
+
+def test_positions_at_the_last_token_plan_like_no_positions():
+    spec = W.random_tree(7, max_nodes=20, max_len=120, max_queries=40, zero_len_prob=0.0)
+    a = deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, 2)
+    b = deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, 2,
+                  query_pos=spec.node_len[spec.query_node] - 1)
+    for name in ("chunk_seg_off", "chunk_q", "seg_node", "seg_tok_begin", "seg_tok_len",
+                 "seg_mask", "q_slot", "mma_items", "fma_items"):
+        np.testing.assert_array_equal(a.get(name), b.get(name))

@@ -224,7 +224,8 @@ def oracle_step(oracle, spec, layout, bits, subset):
     return oracle.tree_attn(bits[0], bits[1], bits[2], layout.node_page_off, layout.page_id,
                             layout.page_size, spec.parent, spec.node_len, spec.query_node,
                             spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
-                            1.0 / math.sqrt(spec.head_dim), query_subset=subset)
+                            1.0 / math.sqrt(spec.head_dim), query_subset=subset,
+                            query_pos=spec.query_pos)
 
 
 def cpu_baseline(spec, layout, bits, budget_s=12.0):
@@ -316,7 +317,8 @@ def main():
     t = W.make_tensors(spec, layout, device=dev)
     npo = torch.from_numpy(layout.node_page_off).to(dev)
     pid = torch.from_numpy(layout.page_id).to(dev)
-    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group)
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
+                     query_pos=spec.query_pos)
     plan.upload()
     bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim, dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -481,7 +483,7 @@ def main():
             barrier()
             t0 = time.perf_counter()
             p = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target,
-                          spec.gqa_group)
+                          spec.gqa_group, query_pos=spec.query_pos)
             p.upload()
             q_dev.copy_(q_host, non_blocking=True)
             deft.deft_tree_attn(q_dev, t.k_pages, t.v_pages, npo, pid, p, bufs=bufs)

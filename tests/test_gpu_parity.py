@@ -193,7 +193,7 @@ def test_abi_rejects_bad_calls(deft):
 # the oracle evaluated on a sample of queries.
 # ---------------------------------------------------------------------------
 
-FULL = {2: 256, 3: 256, 4: 256, 5: 256, 6: 256, 1: 64}
+FULL = {2: 256, 3: 256, 4: 256, 5: 256, 6: 256, 1: 64, 7: 256}
 
 
 @pytest.mark.parametrize("cfg", sorted(FULL))
@@ -203,7 +203,8 @@ def test_full_size_workloads_sampled(deft, cfg):
     t = W.make_tensors(spec, layout, device="cuda")
     npo = torch.from_numpy(layout.node_page_off).cuda()
     pid = torch.from_numpy(layout.page_id).cuda()
-    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, FULL[cfg], spec.gqa_group)
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, FULL[cfg], spec.gqa_group,
+                     query_pos=spec.query_pos)
     plan.upload()
     out, lse = deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
     nout, nlse = deft.deft_naive_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
@@ -216,7 +217,7 @@ def test_full_size_workloads_sampled(deft, cfg):
                                     layout.node_page_off, layout.page_id, layout.page_size,
                                     spec.parent, spec.node_len, spec.query_node, spec.num_q_heads,
                                     spec.num_kv_heads, spec.head_dim, 1.0 / math.sqrt(spec.head_dim),
-                                    query_subset=sample)
+                                    query_subset=sample, query_pos=spec.query_pos)
     for o, l, what in ((out, lse, "tree"), (nout, nlse, "naive")):
         o = o.float().cpu().numpy().astype(np.float64)
         l = l.cpu().numpy().astype(np.float64)

@@ -156,6 +156,41 @@ def speculative_forest(requests: int = 8, prefix: int = 4000, tree_nodes: int = 
                     head_dim, seed=1003, notes={"resampled_subseeds": resampled})
 
 
+def multitoken_speculative_forest(requests: int = 8, prefix: int = 4000, tree_nodes: int = 16,
+                                  node_tokens: int = 4, max_depth: int = 6, heads: int = 32,
+                                  head_dim: int = 128, seed: int = 7) -> TreeSpec:
+    """Tree verification with multi-token nodes: like speculative_forest, but
+    each tree node holds `node_tokens` candidate tokens and every token is a
+    query that sits at its position (attending the prefix, its ancestors and
+    its own node up to itself)."""
+    parent: List[int] = []
+    node_len: List[int] = []
+    query: List[int] = []
+    pos: List[int] = []
+    for r in range(requests):
+        sub = 0
+        while True:
+            rng = random.Random(seed * 1000003 + r * 7919 + sub)
+            local = _grow_token_tree(rng, tree_nodes, max_depth, 1, 4)
+            if local is not None:
+                break
+            sub += 1
+        root = len(parent)
+        parent.append(-1)
+        node_len.append(prefix)
+        base = len(parent)
+        for p in local:
+            parent.append(root if p < 0 else base + p)
+            node_len.append(node_tokens)
+        for n in range(base, base + tree_nodes):
+            query.extend([n] * node_tokens)
+            pos.extend(range(node_tokens))
+    spec = TreeSpec(f"verify_{requests}x({prefix}p+{tree_nodes}n x{node_tokens}t)_h{heads}_d{head_dim}",
+                    _arr(parent), _arr(node_len), _arr(query), heads, heads, head_dim, seed=1007)
+    spec.query_pos = _arr(pos)
+    return spec
+
+
 def reasoning_tree(levels: int = 4, branch_lo: int = 3, branch_hi: int = 5,
                    len_lo: int = 100, len_hi: int = 600, num_queries: int = 128,
                    q_heads: int = 32, kv_heads: int = 8, head_dim: int = 128,
@@ -207,10 +242,12 @@ def imbalance_tree(prefix: int = 32768, leaves: int = 256, lo: int = 64, hi: int
 
 def config(i: int) -> TreeSpec:
     """The five workload shapes, numbered 1..5 in the order the task lists
-    them (6 = the no-sharing control of shape 5)."""
+    them (6 = the no-sharing control of shape 5; 7 = tree verification with
+    multi-token nodes, every token a query)."""
     return {1: tiny_tree, 2: few_shot_tree, 3: speculative_forest,
             4: reasoning_tree, 5: imbalance_tree,
-            6: lambda: imbalance_tree(control=True)}[i]()
+            6: lambda: imbalance_tree(control=True),
+            7: multitoken_speculative_forest}[i]()
 
 
 # ---------------------------------------------------------------------------

@@ -471,7 +471,8 @@ def main():
         line["naive"] = {"us_per_step": statistics.mean(nms) * 1e3, "steps": nk,
                          "kv_bytes": naive_kv,
                          "speedup_of_tree": statistics.mean(nms) / ms_per_step}
-        # End to end through the public API: host planning, plan upload, Q from
+        # End to end through the public API: host planning (a tree-only plan:
+        # the naive partition is the comparison leg's), plan upload, Q from
         # pinned host memory, the step, out + lse back to pinned host memory.
         q_host = t.q.cpu().pin_memory()
         out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
@@ -483,7 +484,7 @@ def main():
             barrier()
             t0 = time.perf_counter()
             p = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target,
-                          spec.gqa_group, query_pos=spec.query_pos)
+                          spec.gqa_group, query_pos=spec.query_pos, naive=False)
             p.upload()
             q_dev.copy_(q_host, non_blocking=True)
             deft.deft_tree_attn(q_dev, t.k_pages, t.v_pages, npo, pid, p, bufs=bufs)
@@ -492,6 +493,7 @@ def main():
             torch.cuda.synchronize(dev)
             if i >= 3:
                 e2e_t.append(time.perf_counter() - t0)
+            plan_bytes = p.stats["device_bytes"]
             del p
         e2e_us = statistics.mean(e2e_t) * 1e6
         if pg is not None:
@@ -499,7 +501,7 @@ def main():
             pg.all_reduce(tt, op=pg.ReduceOp.MAX)
             e2e_us = float(tt.item())
         line["e2e"] = {"value": e2e_us / world, "unit": "us/step",
-                       "h2d_bytes_per_step": int(q_host.numel() * 2 + st["device_bytes"]),
+                       "h2d_bytes_per_step": int(q_host.numel() * 2 + plan_bytes),
                        "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()
                                                  + lse_host.numel() * 4),
                        "includes": "host planning + plan upload + Q H2D + step + out/lse D2H",

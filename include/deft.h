@@ -47,10 +47,14 @@ typedef enum deft_status {
     DEFT_EUNSUPPORTED = -5,  /* head_dim / page_size / GQA group not compiled in    */
     DEFT_ECUDA = -6,         /* a CUDA runtime call or kernel launch failed          */
     DEFT_EWORKSPACE = -7,    /* workspace null, too small or not 256-byte aligned   */
-    DEFT_ESTATE = -8         /* plan not uploaded, or built for another GQA group   */
+    DEFT_ESTATE = -8         /* plan not uploaded, built for another GQA group, or  */
+                             /* (deft_naive_attn) built without the naive partition */
 } deft_status;
 
 enum { DEFT_OUT_BF16 = 0, DEFT_OUT_F32 = 1 };
+
+/* deft_plan_ex flags. */
+enum { DEFT_PLAN_TREE_ONLY = 1 };
 
 /* Opaque plan: the flattened chunk list, segment bitmasks and per-query
  * partial-slot lists of one tree.  Library-owned; free with deft_plan_free. */
@@ -70,7 +74,7 @@ typedef struct deft_plan_stats {
     int32_t num_fallback_items;  /* the >= 16-row chunks cut into <= 16-row items       */
     int32_t max_chunk_tokens;
     int32_t max_slots_per_query;
-    int32_t naive_num_chunks;    /* per-query flash-decoding partition                  */
+    int32_t naive_num_chunks;    /* per-query flash-decoding partition (0 if tree-only) */
     int32_t naive_num_slots;
     int32_t naive_num_segments;
     int64_t unique_tokens;       /* tokens on at least one query path                   */
@@ -149,6 +153,21 @@ int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nod
                  const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
                  int32_t chunk_target, int32_t gqa_group, deft_plan_t **out);
 
+/*
+ * deft_plan_ex -- deft_plan_at with option flags (0 = exactly deft_plan_at).
+ *   DEFT_PLAN_TREE_ONLY: skip the naive per-query partition (a plan for
+ *   deft_tree_attn alone: about half the planning time and a smaller device
+ *   copy).  Its naive partition is empty (naive_num_* = 0, the naive arrays
+ *   have no element but naive_q_slot_off's num_queries + 1 zeros) and
+ *   deft_naive_attn on it returns DEFT_ESTATE.  naive_tokens is still
+ *   counted.
+ * Unknown flag bits: DEFT_EINVAL.  Other arguments, results and errors as
+ * deft_plan_at.
+ */
+int deft_plan_ex(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+                 const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+                 int32_t chunk_target, int32_t gqa_group, int32_t flags, deft_plan_t **out);
+
 /* Plan statistics (host).  DEFT_EINVAL on null arguments. */
 int deft_plan_stats_get(const deft_plan_t *plan, deft_plan_stats *out);
 
@@ -205,6 +224,7 @@ int deft_tree_attn(const void *q, const void *k_pages, const void *v_pages,
  * shared prefix): each query's path is split into pieces of chunk_target
  * tokens, each piece read for that query alone, then the same merge.  Same
  * arguments, results and rules as deft_tree_attn; the in-run IO comparison.
+ * A plan made with DEFT_PLAN_TREE_ONLY: DEFT_ESTATE.
  */
 int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
                     const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,

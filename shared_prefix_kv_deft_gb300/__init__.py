@@ -37,12 +37,13 @@ ARRAYS = {
 }
 
 # Symbols the header declares (checked by the tests).
-EXPORTS = ["deft_plan", "deft_plan_at", "deft_plan_stats_get", "deft_plan_get", "deft_plan_upload",
-           "deft_workspace_bytes", "deft_tree_attn", "deft_naive_attn", "deft_plan_free",
-           "deft_status_str", "deft_version", "deft_trace_enable", "deft_trace_read",
+EXPORTS = ["deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_stats_get", "deft_plan_get",
+           "deft_plan_upload", "deft_workspace_bytes", "deft_tree_attn", "deft_naive_attn",
+           "deft_plan_free", "deft_status_str", "deft_version", "deft_trace_enable", "deft_trace_read",
            "deft_tree_attn_noalloc"]
 
 KERNEL_NAMES = {0: "phase1_fma", 1: "phase1_mma", 2: "phase2_merge"}
+PLAN_TREE_ONLY = 1   # deft_plan_ex flag
 
 
 class DeftError(RuntimeError):
@@ -84,6 +85,7 @@ def load(path: str = LIB_PATH):
     P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_float
     lib.deft_plan.argtypes = [P, P, i32, P, i32, i32, i32, ctypes.POINTER(P)]
     lib.deft_plan_at.argtypes = [P, P, i32, P, P, i32, i32, i32, ctypes.POINTER(P)]
+    lib.deft_plan_ex.argtypes = [P, P, i32, P, P, i32, i32, i32, i32, ctypes.POINTER(P)]
     lib.deft_plan_stats_get.argtypes = [P, ctypes.POINTER(PlanStats)]
     lib.deft_plan_get.argtypes = [P, i32, P, sz]
     lib.deft_plan_upload.argtypes = [P, P]
@@ -101,7 +103,8 @@ def load(path: str = LIB_PATH):
     lib.deft_version.argtypes = []
     lib.deft_trace_enable.argtypes = [i32]
     lib.deft_trace_read.argtypes = [ctypes.POINTER(TraceRecord), i32, ctypes.POINTER(i32)]
-    for fn in ("deft_plan", "deft_plan_at", "deft_plan_stats_get", "deft_plan_get", "deft_plan_upload",
+    for fn in ("deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_stats_get", "deft_plan_get",
+               "deft_plan_upload",
                "deft_tree_attn", "deft_naive_attn", "deft_version", "deft_trace_enable",
                "deft_trace_read", "deft_tree_attn_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
@@ -127,21 +130,23 @@ def _ptr(a: np.ndarray):
 
 
 class Plan:
-    """Owner of a deft_plan_t handle (deft_plan / deft_plan_at ... deft_plan_free).
+    """Owner of a deft_plan_t handle (deft_plan_ex ... deft_plan_free).
     query_pos: per query, the token of its node it sits at (-1: the last);
-    None: every query at its node's last token."""
+    None: every query at its node's last token.  naive=False: tree-only plan
+    (DEFT_PLAN_TREE_ONLY; deft_naive_attn refuses it)."""
 
     def __init__(self, parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
-                 query_pos=None):
+                 query_pos=None, naive: bool = True):
         lib = load()
         self._parent, self._len, self._qn = _i32(parent), _i32(node_len), _i32(query_node)
         self._pos = None if query_pos is None else _i32(query_pos)
         h = ctypes.c_void_p()
-        _check("deft_plan_at", lib.deft_plan_at(_ptr(self._parent), _ptr(self._len),
+        _check("deft_plan_ex", lib.deft_plan_ex(_ptr(self._parent), _ptr(self._len),
                                                 int(self._parent.shape[0]), _ptr(self._qn),
                                                 None if self._pos is None else _ptr(self._pos),
                                                 int(self._qn.shape[0]), int(chunk_target),
-                                                int(gqa_group), ctypes.byref(h)))
+                                                int(gqa_group), 0 if naive else PLAN_TREE_ONLY,
+                                                ctypes.byref(h)))
         self.handle = h
         st = PlanStats()
         _check("deft_plan_stats_get", lib.deft_plan_stats_get(self.handle, ctypes.byref(st)))
@@ -255,8 +260,8 @@ def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, buf
 
 
 def deft_plan(parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
-              query_pos=None) -> Plan:
-    return Plan(parent, node_len, query_node, chunk_target, gqa_group, query_pos)
+              query_pos=None, naive: bool = True) -> Plan:
+    return Plan(parent, node_len, query_node, chunk_target, gqa_group, query_pos, naive)
 
 
 def trace_enable(on: bool = True):

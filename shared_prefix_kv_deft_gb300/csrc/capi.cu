@@ -152,7 +152,7 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
         return DEFT_EINVAL;   // the kernels copy q and KV rows in 16-byte pieces
     if ((head_dim != 64 && head_dim != 128) || page_size != deft::kPageSize)
         return DEFT_EUNSUPPORTED;
-    if (num_q_heads / num_kv_heads != plan->gqa_group || !plan->uploaded)
+    if (num_q_heads / num_kv_heads != plan->gqa_group || !plan->uploaded || (naive && !plan->has_naive))
         return DEFT_ESTATE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess)
@@ -210,12 +210,16 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
 
 extern "C" {
 
-int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+int deft_plan_ex(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                  const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
-                 int32_t chunk_target, int32_t gqa_group, deft_plan_t **out)
+                 int32_t chunk_target, int32_t gqa_group, int32_t flags, deft_plan_t **out)
 {
     if (!out)
         return DEFT_EINVAL;
+    if (flags & ~(int32_t)DEFT_PLAN_TREE_ONLY) {
+        *out = nullptr;
+        return DEFT_EINVAL;
+    }
     *out = nullptr;
     deft_plan_t *p = new (std::nothrow) deft_plan_t();
     if (!p)
@@ -223,7 +227,7 @@ int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nod
     int rc;
     try {
         rc = deft::build_plan(parent, node_len, num_nodes, query_node, query_pos, num_queries,
-                              chunk_target, gqa_group, p);
+                              chunk_target, gqa_group, (flags & DEFT_PLAN_TREE_ONLY) == 0, p);
     } catch (const std::bad_alloc &) {
         rc = DEFT_ENOMEM;
     }
@@ -238,6 +242,14 @@ int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nod
     p->stats.device_bytes = (int64_t)cursor;
     *out = p;
     return DEFT_OK;
+}
+
+int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+                 const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+                 int32_t chunk_target, int32_t gqa_group, deft_plan_t **out)
+{
+    return deft_plan_ex(parent, node_len, num_nodes, query_node, query_pos, num_queries, chunk_target,
+                        gqa_group, 0, out);
 }
 
 int deft_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
@@ -378,7 +390,7 @@ const char *deft_status_str(int status)
     case DEFT_EUNSUPPORTED: return "unsupported head_dim, page_size or GQA shape";
     case DEFT_ECUDA: return "CUDA runtime or launch error";
     case DEFT_EWORKSPACE: return "workspace missing, too small or misaligned";
-    case DEFT_ESTATE: return "plan not uploaded on this device or built for another GQA group";
+    case DEFT_ESTATE: return "plan not uploaded on this device, built for another GQA group, or without the naive partition";
     default: return "unknown status";
     }
 }

@@ -192,7 +192,8 @@ struct deft_plan_t {
     std::vector<uint64_t> cover;   // [N * W]
     std::vector<int32_t> order;    // DFS preorder of all nodes
     deft::Partition tree;
-    deft::Partition naive;
+    deft::Partition naive;         // empty unless has_naive
+    bool has_naive = true;
     deft_plan_stats stats{};
     // Device copy (deft_plan_upload).
     void *dev_blob = nullptr;
@@ -208,7 +209,7 @@ namespace deft {
 // planner.cpp
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
-               int32_t chunk_target, int32_t gqa_group, deft_plan_t *plan);
+               int32_t chunk_target, int32_t gqa_group, bool with_naive, deft_plan_t *plan);
 
 // Arguments every phase-1 kernel receives.
 struct AttnArgs {

@@ -54,8 +54,18 @@ struct Builder {
     bool open = false;
     std::vector<uint64_t> cur_mask;
 
-    Builder(Partition &part, int32_t words) : p(part), W(words), cur_mask(words, 0)
+    // Capacity for about `chunks` chunks of `segs` segments in all.
+    Builder(Partition &part, int32_t words, int64_t chunks, int64_t segs)
+        : p(part), W(words), cur_mask(words, 0)
     {
+        p.chunk_seg_off.reserve(chunks + 1);
+        p.chunk_tokens.reserve(chunks);
+        p.chunk_mask.reserve(chunks * W);
+        p.seg_node.reserve(segs);
+        p.seg_tok_begin.reserve(segs);
+        p.seg_tok_len.reserve(segs);
+        p.seg_chunk_pos.reserve(segs);
+        p.seg_mask.reserve(segs * W);
         p.chunk_seg_off.push_back(0);
     }
     void close()
@@ -103,9 +113,9 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     p.chunk_q.clear();
     for (int32_t c = 0; c < C; ++c) {
         const uint64_t *m = &p.chunk_mask[(size_t)c * W];
-        for (int32_t q = 0; q < num_queries; ++q)
-            if ((m[q / 64] >> (q % 64)) & 1ull)
-                p.chunk_q.push_back(q);
+        for (int32_t w = 0; w < W; ++w)
+            for (uint64_t bits = m[w]; bits; bits &= bits - 1)
+                p.chunk_q.push_back(w * 64 + __builtin_ctzll(bits));
         p.chunk_q_off.push_back((int32_t)p.chunk_q.size());
     }
     // Local masks: bit k of segment s = the chunk's k-th query sees s.
@@ -247,7 +257,7 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
 
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
-               int32_t chunk_target, int32_t gqa_group, deft_plan_t *plan)
+               int32_t chunk_target, int32_t gqa_group, bool with_naive, deft_plan_t *plan)
 {
     if (!parent || !node_len || !plan || num_nodes < 1 || num_queries < 0 ||
         (num_queries > 0 && !query_node))
@@ -300,11 +310,12 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
 
     // Coverage bitsets: walk every query's path.
     plan->cover.assign((size_t)N * W, 0);
-    int64_t naive_tokens = 0;
+    int64_t naive_tokens = 0, path_nodes = 0;
     for (int32_t q = 0; q < Q; ++q)
         for (int32_t cur = query_node[q]; cur != -1; cur = parent[cur]) {
             plan->cover[(size_t)cur * W + q / 64] |= 1ull << (q % 64);
             naive_tokens += taken(q, cur);
+            path_nodes += 1;
         }
     // Per node, the queries that sit at a position before its last token
     // (their part of the node ends there), as CSR.
@@ -354,7 +365,10 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
     plan->tree = Partition();
     int64_t unique_tokens = 0;
     {
-        Builder b(plan->tree, W);
+        int64_t tokens = 0;
+        for (int32_t n = 0; n < N; ++n)
+            tokens += node_len[n];
+        Builder b(plan->tree, W, tokens / chunk_target + N, tokens / chunk_target + 2 * (int64_t)N);
         // Tokens [b0, b0 + L) of node n, attended by the queries in m (k of them).
         auto emit = [&](int32_t n, int32_t b0, int32_t L, const uint64_t *m, int k) {
             unique_tokens += L;
@@ -419,10 +433,14 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
     finish_partition(plan->tree, Q, W, gqa_group);
 
     // Naive partition: each query's path (root first) cut every chunk_target
-    // tokens; every chunk serves that one query.
+    // tokens; every chunk serves that one query.  Left empty (no chunk) when
+    // the caller will not run it.
     plan->naive = Partition();
-    {
-        Builder b(plan->naive, W);
+    plan->has_naive = with_naive;
+    if (!with_naive) {
+        Builder b(plan->naive, W, 0, 0);
+    } else {
+        Builder b(plan->naive, W, naive_tokens / chunk_target + Q, naive_tokens / chunk_target + Q + path_nodes);
         std::vector<int32_t> path;
         std::vector<uint64_t> m(W, 0);
         for (int32_t q = 0; q < Q; ++q) {

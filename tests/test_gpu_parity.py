@@ -168,8 +168,8 @@ def test_abi_rejects_bad_calls(deft):
     P = ctypes.c_void_p
 
     def call(plan=case.plan.handle, hq=Hq, hkv=4, hd=d, ps=16, wsp=ws.data_ptr(), wsb=ws_bytes,
-             scale=0.125, odt=0):
-        return lib.deft_tree_attn(P(case.q.data_ptr()), P(case.k.data_ptr()), P(case.v.data_ptr()),
+             scale=0.125, odt=0, fn=lib.deft_tree_attn):
+        return fn(P(case.q.data_ptr()), P(case.k.data_ptr()), P(case.v.data_ptr()),
                                   P(case.npo.data_ptr()), P(case.pid.data_ptr()), case.k.shape[0],
                                   hq, hkv, hd, ps, scale, plan, P(out.data_ptr()), odt,
                                   P(lse.data_ptr()), P(wsp), wsb,
@@ -185,7 +185,33 @@ def test_abi_rejects_bad_calls(deft):
     assert call(odt=7) == -1
     unuploaded = deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, 1)
     assert call(plan=unuploaded.handle) == -8
+    tree_only = deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, 1, naive=False)
+    tree_only.upload()
+    assert call(plan=tree_only.handle) == 0
+    assert call(plan=tree_only.handle, fn=lib.deft_naive_attn) == -8   # no naive partition
+    assert call(fn=lib.deft_naive_attn) == 0
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("cfg", [2, 7])
+def test_tree_only_plan_gives_the_same_step(deft, cfg):
+    """A plan without the naive partition runs the tree step bit for bit as
+    the full plan does (same partition, same launches)."""
+    spec = W.config(cfg)
+    layout = W.paged_layout(spec)
+    t = W.make_tensors(spec, layout, device="cuda")
+    npo = torch.from_numpy(layout.node_page_off).cuda()
+    pid = torch.from_numpy(layout.page_id).cuda()
+    res = []
+    for naive in (True, False):
+        plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, spec.gqa_group,
+                         query_pos=spec.query_pos, naive=naive)
+        plan.upload()
+        out, lse = deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
+        torch.cuda.synchronize()
+        res.append((out.float().cpu().numpy(), lse.cpu().numpy()))
+    np.testing.assert_array_equal(res[0][0], res[1][0])
+    np.testing.assert_array_equal(res[0][1], res[1][1])
 
 
 # ---------------------------------------------------------------------------

@@ -275,3 +275,44 @@ def test_positions_at_the_last_token_plan_like_no_positions():
     for name in ("chunk_seg_off", "chunk_q", "seg_node", "seg_tok_begin", "seg_tok_len",
                  "seg_mask", "q_slot", "mma_items", "fma_items"):
         np.testing.assert_array_equal(a.get(name), b.get(name))
+
+
+@pytest.mark.parametrize("cfg", [2, 4, 7])
+def test_tree_only_plan_matches_the_full_plan(cfg):
+    """DEFT_PLAN_TREE_ONLY leaves the tree partition as it is and the naive
+    one empty (no chunk, no slot; every query's slot list empty)."""
+    spec = W.config(cfg)
+    full = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, spec.gqa_group,
+                     query_pos=spec.query_pos)
+    tree = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, spec.gqa_group,
+                     query_pos=spec.query_pos, naive=False)
+    for name in deft.ARRAYS:
+        if name.startswith("naive_"):
+            continue
+        np.testing.assert_array_equal(full.get(name), tree.get(name))
+    for key, v in tree.stats.items():
+        if key.startswith("naive_num_"):
+            assert v == 0
+        elif key != "device_bytes":
+            assert v == full.stats[key], key
+    assert tree.stats["device_bytes"] < full.stats["device_bytes"]
+    assert tree.get("naive_chunk_seg_off").tolist() == [0]
+    assert tree.get("naive_q_slot_off").tolist() == [0] * (spec.num_queries + 1)
+    for name in ("naive_chunk_q", "naive_seg_node", "naive_q_slot"):
+        assert tree.get(name).size == 0
+
+
+def test_plan_ex_rejects_unknown_flags():
+    lib = deft.load()
+    p = np.array([-1, 0], np.int32)
+    L = np.array([5, 5], np.int32)
+    qn = np.array([1], np.int32)
+    h = ctypes.c_void_p()
+    vp = ctypes.c_void_p
+    rc = lib.deft_plan_ex(p.ctypes.data_as(vp), L.ctypes.data_as(vp), 2, qn.ctypes.data_as(vp), None, 1,
+                          64, 1, 2, ctypes.byref(h))
+    assert rc == -1 and not h.value
+    rc = lib.deft_plan_ex(p.ctypes.data_as(vp), L.ctypes.data_as(vp), 2, qn.ctypes.data_as(vp), None, 1,
+                          64, 1, deft.PLAN_TREE_ONLY, ctypes.byref(h))
+    assert rc == 0 and h.value
+    lib.deft_plan_free(h)

@@ -595,7 +595,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         constexpr int RL = RMAX / NRG;                 // rows per lane
         constexpr int TS = 4 / NRG;                    // token slots per step
         constexpr int NSTEP = 8 / TS;                  // steps per tile
-        constexpr int SUB = RL >= 4 ? 2 : NSTEP < 4 ? NSTEP : 4;   // steps per maximum update
+        constexpr int SUB = NSTEP < 4 ? NSTEP : 4;   // steps per maximum update
         const int cw = warp - 3;          // compute warp 0..NCW-1
         const int g = cw >> 3, lw = cw & 7;
         const int part = lane & 7, rg = (lane >> 3) % NRG, ts = (lane >> 3) / NRG;
@@ -711,14 +711,19 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         for (int o = 8 * NRG; o < 32; o <<= 1)
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                         const float mnew = fmaxf(m_run[rl], mx);
-                        if (mnew != -INFINITY) {
-                            // (m_run may be -inf: alpha = 0 then, on zero sums)
-                            const float alpha = mnew > m_run[rl] ? tc::ex2(m_run[rl] - mnew) : 1.f;
+                        // Rescale the sums where the maximum grew (m_run may
+                        // be -inf: alpha = 0 then, on zero sums); the warp
+                        // skips it when no lane's maximum moved.
+                        const bool grew = mnew > m_run[rl];
+                        if (__any_sync(0xffffffffu, grew)) {
+                            const float alpha = grew ? tc::ex2(m_run[rl] - mnew) : 1.f;
                             l_run[rl] *= alpha;
                             const f32x2 aa = f2_pack(alpha, alpha);
 #pragma unroll
                             for (int e = 0; e < NCH * 4; ++e)
                                 o_acc[rl][e] = f2_mul(o_acc[rl][e], aa);
+                        }
+                        if (mnew != -INFINITY) {
 #pragma unroll
                             for (int s = 0; s < SUB; ++s) {
                                 const float pr = tc::ex2(sv[s][rl] - mnew);

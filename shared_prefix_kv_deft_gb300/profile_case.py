@@ -10,6 +10,8 @@ requests):
     control_32x2048    32 independent 2048-token sequences, GQA 32/8, d 128
                        (CUDA-core launch, 4 rows)
     few_shot           the few-shot tree (4096-token prefix + 32 x 256)
+    reasoning          the reasoning tree (4 levels, 128 queries, GQA 32/8):
+                       CUDA-core launches with 8 and 12 rows
 """
 import sys
 
@@ -22,6 +24,7 @@ CASES = {
     "speculative_3req": lambda: W.speculative_forest(requests=3),
     "control_32x2048": lambda: W.imbalance_tree(control=True, leaves=32),
     "few_shot": lambda: W.config(2),
+    "reasoning": lambda: W.config(4),
 }
 
 

@@ -149,9 +149,12 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
         p.q_slot[fill[p.chunk_q[s]]++] = s;
 
     // Work items.  rows = queries * G.  Chunks under kMmaMinRows rows run on
-    // the CUDA-core kernel in one item; the others run on the tensor-core
-    // kernel in row blocks of at most kMmaMaxRows rows, and are also cut into
-    // items of at most kFmaMaxRows rows for head sizes without a tensor path.
+    // the CUDA-core kernel in row blocks of at most kFmaItemRows rows (whole
+    // queries): above 8 rows the kernel's per-token work outgrows what one
+    // SM streams, and two blocks run on two SMs at once, the second reading
+    // the chunk from L2.  The others run on the tensor-core kernel in row
+    // blocks of at most kMmaMaxRows rows, and are also cut into items of at
+    // most kFmaMaxRows rows for head sizes without a tensor path.
     struct Item { int32_t c, b, e; int64_t cost; int32_t bucket = 0; };
     std::vector<Item> fma, mma, fb;
     const int32_t qmax_mma = std::max(1, kMmaMaxRows / G);
@@ -160,7 +163,10 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
         const int32_t k = p.chunk_q_off[c + 1] - p.chunk_q_off[c];
         const int64_t tok = p.chunk_tokens[c];
         if ((int64_t)k * G < kMmaMinRows) {
-            fma.push_back({c, 0, k, tok, row_bucket(k * G)});
+            const int32_t qmax = std::max(1, kFmaItemRows / G);
+            const int32_t nb = (k + qmax - 1) / qmax, per = (k + nb - 1) / nb;
+            for (int32_t b = 0; b < k; b += per)
+                fma.push_back({c, b, std::min(k, b + per), tok, row_bucket((std::min(k, b + per) - b) * G)});
             continue;
         }
         const int32_t nb = (k + qmax_mma - 1) / qmax_mma;

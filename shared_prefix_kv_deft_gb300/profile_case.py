@@ -1,7 +1,12 @@
 """Runs a few tree-attention steps of a named, seeded workload on cuda:0, for
 profiling captures that must stay small (a few hundred MB on the device):
 
-    python -m shared_prefix_kv_deft_gb300.profile_case <case> [steps]
+    python -m shared_prefix_kv_deft_gb300.profile_case <case> [steps] [--range]
+
+--range brackets one more step, after the others, with cudaProfilerStart /
+cudaProfilerStop, so that ncu's range replay (--replay-mode range
+--profile-from-start off) measures the whole step, its launches running
+concurrently as they do in the benchmark.
 
 Cases (synthetic, seeded; the shapes of the benchmark workloads, fewer
 requests):
@@ -29,6 +34,8 @@ CASES = {
 
 
 def main(argv):
+    ranged = "--range" in argv
+    argv = [x for x in argv if x != "--range"]
     spec = CASES[argv[1]]()
     steps = int(argv[2]) if len(argv) > 2 else 4
     lay = W.paged_layout(spec)
@@ -41,6 +48,11 @@ def main(argv):
     for _ in range(steps):
         deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)
     torch.cuda.synchronize()
+    if ranged:
+        torch.cuda.profiler.start()
+        deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
     print("ok", spec.name)
 
 

@@ -183,7 +183,13 @@ def check_plan(spec: W.TreeSpec, chunk_target: int, G: int):
     for c in range(C):
         k = cqo[c + 1] - cqo[c]
         if k * G < 16:
-            assert fcov[c] == [(0, k)] and c not in mcov and c not in bcov
+            assert c not in mcov and c not in bcov
+            iv = sorted(fcov[c])
+            pos = 0
+            for b, e in iv:   # row blocks of at most 8 rows (whole queries)
+                assert b == pos and (e - b) * G <= max(8, G)
+                pos = e
+            assert pos == k and len(iv) == -(-k // max(1, 8 // G))
         else:
             for fam, cap in ((mcov, 128), (bcov, 16)):
                 iv = sorted(fam[c])

@@ -599,6 +599,16 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         const int cw = warp - 3;          // compute warp 0..NCW-1
         const int g = cw >> 3, lw = cw & 7;
         const int part = lane & 7, rg = (lane >> 3) % NRG, ts = (lane >> 3) / NRG;
+        // Rows whose softmax state a lane keeps.  With two rows per lane the
+        // part lanes split the last steps of the dot-product sums between
+        // the rows: a lane finishes row rg RL + hi (hi = bit 2 of part) and
+        // keeps only that row's logits, maximum and sum, so each part lane
+        // does half the exponentials; it fetches the other row's
+        // probabilities from lane ^ 4 for p.v.  Otherwise every part lane
+        // keeps all RL rows.
+        constexpr bool SPLIT = RL == 2;
+        constexpr int RS = SPLIT ? 1 : RL;
+        const int hi = SPLIT ? (part >> 2) & 1 : 0;
         float *qs = reinterpret_cast<float *>(smem + C::qs_off) + g * RMAX * D;
         float *mw = reinterpret_cast<float *>(smem + C::ml_off) + g * 8 * RMAX;
         float *lwb = reinterpret_cast<float *>(smem + C::ml_off) + NCW * RMAX + g * 8 * RMAX;
@@ -639,16 +649,18 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     qv[rl][4 * c + 2] = a1.x;
                     qv[rl][4 * c + 3] = a1.y;
                 }
-            float m_run[RL], l_run[RL];
+            float m_run[RS], l_run[RS];
             f32x2 o_acc[RL][NCH * 4];
 #pragma unroll
-            for (int rl = 0; rl < RL; ++rl) {
-                m_run[rl] = -INFINITY;
-                l_run[rl] = 0.f;
+            for (int k = 0; k < RS; ++k) {
+                m_run[k] = -INFINITY;
+                l_run[k] = 0.f;
+            }
+#pragma unroll
+            for (int rl = 0; rl < RL; ++rl)
 #pragma unroll
                 for (int e = 0; e < NCH * 4; ++e)
                     o_acc[rl][e] = 0ull;   // (+0, +0)
-            }
             bool tile_ok = true;
             for (int t = 0; t < ui.ntiles; ++t) {
                 const int sq = ui.seq0 + t, st = g * RST + sq % RST;
@@ -664,8 +676,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 const uint8_t *Vs = Ks + C::op_bytes;
 #pragma unroll
                 for (int s0 = 0; s0 < NSTEP; s0 += SUB) {
-                    // Logits of the lane's rows for the SUB tokens of its slot.
-                    float sv[SUB][RL];
+                    // Logits of the lane's state rows for the SUB tokens of its slot.
+                    float sv[SUB][RS];
 #pragma unroll
                     for (int s = 0; s < SUB; ++s) {
                         const int tok = lw * 8 + (s0 + s) * TS + ts;
@@ -688,60 +700,93 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             }
                         }
                         const uint32_t mrow = meta[st * kTile + tok];
-#pragma unroll
-                        for (int rl = 0; rl < RL; ++rl) {
-                            const float2 a2 = f2_unpack(acc[rl]);
-                            float v = a2.x + a2.y;
-                            v += __shfl_xor_sync(0xffffffffu, v, 1);
+                        if constexpr (SPLIT) {
+                            // Lane and lane ^ 4 swap halves: each adds the
+                            // partner's part of the row it finishes.
+                            const float2 a0 = f2_unpack(acc[0]), a1 = f2_unpack(acc[1]);
+                            const float v0 = a0.x + a0.y, v1 = a1.x + a1.y;
+                            float v = hi ? v1 : v0;
+                            v += __shfl_xor_sync(0xffffffffu, hi ? v0 : v1, 4);
                             v += __shfl_xor_sync(0xffffffffu, v, 2);
-                            v += __shfl_xor_sync(0xffffffffu, v, 4);
-                            sv[s][rl] = ((mrow >> (rg * RL + rl)) & 1u) ? v : -INFINITY;
+                            v += __shfl_xor_sync(0xffffffffu, v, 1);
+                            sv[s][0] = ((mrow >> (rg * RL + hi)) & 1u) ? v : -INFINITY;
+                        } else {
+#pragma unroll
+                            for (int rl = 0; rl < RL; ++rl) {
+                                const float2 a2 = f2_unpack(acc[rl]);
+                                float v = a2.x + a2.y;
+                                v += __shfl_xor_sync(0xffffffffu, v, 1);
+                                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                                sv[s][rl] = ((mrow >> (rg * RL + rl)) & 1u) ? v : -INFINITY;
+                            }
                         }
                     }
                     // Running maximum over the warp's tokens (the slot lanes
                     // differ in lane bits 3 + log2 NRG and up), rescale, and
                     // the probabilities.
 #pragma unroll
-                    for (int rl = 0; rl < RL; ++rl) {
-                        float mx = sv[0][rl];
+                    for (int k = 0; k < RS; ++k) {
+                        float mx = sv[0][k];
 #pragma unroll
                         for (int s = 1; s < SUB; ++s)
-                            mx = fmaxf(mx, sv[s][rl]);
+                            mx = fmaxf(mx, sv[s][k]);
 #pragma unroll
                         for (int o = 8 * NRG; o < 32; o <<= 1)
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                        const float mnew = fmaxf(m_run[rl], mx);
+                        const float mnew = fmaxf(m_run[k], mx);
                         // Rescale the sums where the maximum grew (m_run may
                         // be -inf: alpha = 0 then, on zero sums); the warp
                         // skips it when no lane's maximum moved.
-                        const bool grew = mnew > m_run[rl];
+                        const bool grew = mnew > m_run[k];
                         if (__any_sync(0xffffffffu, grew)) {
-                            const float alpha = grew ? tc::ex2(m_run[rl] - mnew) : 1.f;
-                            l_run[rl] *= alpha;
-                            const f32x2 aa = f2_pack(alpha, alpha);
+                            const float alpha = grew ? tc::ex2(m_run[k] - mnew) : 1.f;
+                            l_run[k] *= alpha;
+                            if constexpr (SPLIT) {
+                                const float ao = __shfl_xor_sync(0xffffffffu, alpha, 4);
+                                const f32x2 a0 = f2_pack(hi ? ao : alpha, hi ? ao : alpha);
+                                const f32x2 a1 = f2_pack(hi ? alpha : ao, hi ? alpha : ao);
 #pragma unroll
-                            for (int e = 0; e < NCH * 4; ++e)
-                                o_acc[rl][e] = f2_mul(o_acc[rl][e], aa);
+                                for (int e = 0; e < NCH * 4; ++e) {
+                                    o_acc[0][e] = f2_mul(o_acc[0][e], a0);
+                                    o_acc[1][e] = f2_mul(o_acc[1][e], a1);
+                                }
+                            } else {
+                                const f32x2 aa = f2_pack(alpha, alpha);
+#pragma unroll
+                                for (int e = 0; e < NCH * 4; ++e)
+                                    o_acc[k][e] = f2_mul(o_acc[k][e], aa);
+                            }
                         }
                         if (mnew != -INFINITY) {
 #pragma unroll
                             for (int s = 0; s < SUB; ++s) {
-                                const float pr = tc::ex2(sv[s][rl] - mnew);
-                                sv[s][rl] = pr;
-                                l_run[rl] += pr;
+                                const float pr = tc::ex2(sv[s][k] - mnew);
+                                sv[s][k] = pr;
+                                l_run[k] += pr;
                             }
                         } else {
 #pragma unroll
                             for (int s = 0; s < SUB; ++s)
-                                sv[s][rl] = 0.f;
+                                sv[s][k] = 0.f;
                         }
-                        m_run[rl] = mnew;
+                        m_run[k] = mnew;
                     }
                     // p.v (p = 0 for masked and absent tokens, whose V rows
                     // are finite or zero).
 #pragma unroll
                     for (int s = 0; s < SUB; ++s) {
                         const int tok = lw * 8 + (s0 + s) * TS + ts;
+                        float pr[RL];
+                        if constexpr (SPLIT) {
+                            const float po = __shfl_xor_sync(0xffffffffu, sv[s][0], 4);
+                            pr[0] = hi ? po : sv[s][0];
+                            pr[1] = hi ? sv[s][0] : po;
+                        } else {
+#pragma unroll
+                            for (int rl = 0; rl < RL; ++rl)
+                                pr[rl] = sv[s][rl];
+                        }
 #pragma unroll
                         for (int c = 0; c < NCH; ++c) {
                             const uint4 vw =
@@ -750,7 +795,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             const f32x2 v2 = bf16x2_to_f2(vw.z), v3 = bf16x2_to_f2(vw.w);
 #pragma unroll
                             for (int rl = 0; rl < RL; ++rl) {
-                                const f32x2 pp = f2_pack(sv[s][rl], sv[s][rl]);
+                                const f32x2 pp = f2_pack(pr[rl], pr[rl]);
                                 o_acc[rl][4 * c + 0] = f2_fma(pp, v0, o_acc[rl][4 * c + 0]);
                                 o_acc[rl][4 * c + 1] = f2_fma(pp, v1, o_acc[rl][4 * c + 1]);
                                 o_acc[rl][4 * c + 2] = f2_fma(pp, v2, o_acc[rl][4 * c + 2]);
@@ -774,10 +819,14 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             // The warp's state per row: sums over its token slots (lanes that
             // differ in the slot bits), the same on all part lanes.
 #pragma unroll
+            for (int k = 0; k < RS; ++k)
+#pragma unroll
+                for (int o = 8 * NRG; o < 32; o <<= 1)
+                    l_run[k] += __shfl_xor_sync(0xffffffffu, l_run[k], o);
+#pragma unroll
             for (int rl = 0; rl < RL; ++rl) {
 #pragma unroll
                 for (int o = 8 * NRG; o < 32; o <<= 1) {
-                    l_run[rl] += __shfl_xor_sync(0xffffffffu, l_run[rl], o);
 #pragma unroll
                     for (int e = 0; e < NCH * 4; ++e)
                         o_acc[rl][e] = f2_add(o_acc[rl][e], __shfl_xor_sync(0xffffffffu, o_acc[rl][e], o));
@@ -799,12 +848,16 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     break;
                 }
 #pragma unroll
+                for (int k = 0; k < RS; ++k) {
+                    const int r = rg * RL + (SPLIT ? hi : k);
+                    if (rb == 0 && ts == 0 && (part & (SPLIT ? 3 : 7)) == 0 && r < R) {
+                        mw[lw * RMAX + r] = m_run[k];
+                        lwb[lw * RMAX + r] = l_run[k];
+                    }
+                }
+#pragma unroll
                 for (int rl = 0; rl < RL; ++rl) {
                     const int r = rg * RL + rl;
-                    if (rb == 0 && ts == 0 && part == 0 && r < R) {
-                        mw[lw * RMAX + r] = m_run[rl];
-                        lwb[lw * RMAX + r] = l_run[rl];
-                    }
                     if (ts == 0 && r >= rb && r < rb + C::MRB && r < R) {
 #pragma unroll
                         for (int c = 0; c < NCH; ++c) {

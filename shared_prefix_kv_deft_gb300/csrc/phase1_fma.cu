@@ -580,35 +580,41 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * D * 2, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
         // Group g takes the CTA's units g, g + NG, ... whole; warp lw of the
         // group takes tokens 8 lw .. 8 lw + 7 of every tile.  Lane layout:
-        //   part = lane & 7   owns the head dims of 16-byte chunks part,
-        //                     part + 8, ... (DP dims; 8 lanes read 128
-        //                     contiguous bytes of a K or V row);
-        //   rg                row group: rows rg RL .. rg RL + RL - 1;
-        //   ts                token slot: token 8 lw + step TS + ts.
+        //   part = lane % NPART   owns the head dims of 16-byte chunks part,
+        //                         part + NPART, ... (DP dims; the part lanes
+        //                         read contiguous bytes of a K or V row);
+        //   rg                    row group: rows rg RL .. rg RL + RL - 1;
+        //   ts                    token slot: token 8 lw + step TS + ts.
         // A lane keeps its q rows and its share of the output rows in
-        // registers and works on fp32 pairs (f32x2 FMAs).  q.k is summed over
-        // the 8 part lanes by shuffles, so each of them holds its token's
-        // logits and computes the probabilities its p.v needs.
-        constexpr int DP = D / 8;                      // dims per lane
+        // registers and works on fp32 pairs (f32x2 FMAs).  NPART is 16 at
+        // head_dim 128 with 3-8 rows (one row group holds all rows, so each
+        // K and V element is widened from bf16 once), else 8.
+        constexpr int NPART = (D == 128 && (RMAX == 4 || RMAX == 8)) ? 16 : 8;
+        constexpr int LP = NPART == 16 ? 4 : 3;        // log2 NPART
+        constexpr int DP = D / NPART;                  // dims per lane
         constexpr int NCH = DP / 8;                    // 16-byte chunks per lane and row
-        constexpr int NRG = RMAX <= 2 ? 1 : RMAX == 4 ? 2 : 4;
+        constexpr int NRG = NPART == 16 ? (RMAX == 8 ? 2 : 1) : (RMAX <= 2 ? 1 : RMAX == 4 ? 2 : 4);
         constexpr int RL = RMAX / NRG;                 // rows per lane
-        constexpr int TS = 4 / NRG;                    // token slots per step
+        constexpr int TS = 32 / (NPART * NRG);         // token slots per step
         constexpr int NSTEP = 8 / TS;                  // steps per tile
         constexpr int SUB = NSTEP < 4 ? NSTEP : 4;   // steps per maximum update
+        static_assert(NCH >= 1 && TS >= 1 && NPART * NRG * TS == 32, "lane layout");
         const int cw = warp - 3;          // compute warp 0..NCW-1
         const int g = cw >> 3, lw = cw & 7;
-        const int part = lane & 7, rg = (lane >> 3) % NRG, ts = (lane >> 3) / NRG;
-        // Rows whose softmax state a lane keeps.  With two rows per lane the
-        // part lanes split the last steps of the dot-product sums between
-        // the rows: a lane finishes row rg RL + hi (hi = bit 2 of part) and
-        // keeps only that row's logits, maximum and sum, so each part lane
-        // does half the exponentials; it fetches the other row's
-        // probabilities from lane ^ 4 for p.v.  Otherwise every part lane
-        // keeps all RL rows.
-        constexpr bool SPLIT = RL == 2;
+        const int part = lane & (NPART - 1), rg = (lane >> LP) % NRG, ts = (lane >> LP) / NRG;
+        // Rows whose softmax state a lane keeps.  With RL = 2 or 4 rows per
+        // lane the part lanes split the first log2 RL steps of the
+        // dot-product sums between the rows (a reduce-scatter over the part
+        // bits RS_SH .. LP - 1) and finish one row each, hr: a lane keeps
+        // only that row's logits, maximum and sum (1/RL of the
+        // exponentials) and fetches the other rows' probabilities for p.v
+        // from the lanes that finished them.  With one row per lane every
+        // part lane keeps the row.
+        constexpr bool SPLIT = RL >= 2;
         constexpr int RS = SPLIT ? 1 : RL;
-        const int hi = SPLIT ? (part >> 2) & 1 : 0;
+        constexpr int RS_SH = LP - (RL == 4 ? 2 : RL == 2 ? 1 : 0);   // lowest row bit of part
+        constexpr int ROWBITS = (RL - 1) << RS_SH;                    // part bits naming hr
+        const int hr = SPLIT ? (part >> RS_SH) & (RL - 1) : 0;
         float *qs = reinterpret_cast<float *>(smem + C::qs_off) + g * RMAX * D;
         float *mw = reinterpret_cast<float *>(smem + C::ml_off) + g * 8 * RMAX;
         float *lwb = reinterpret_cast<float *>(smem + C::ml_off) + NCW * RMAX + g * 8 * RMAX;
@@ -641,7 +647,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             for (int rl = 0; rl < RL; ++rl)
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
-                    const float *qp = qs + (rg * RL + rl) * D + (part + 8 * c) * 8;
+                    const float *qp = qs + (rg * RL + rl) * D + (part + NPART * c) * 8;
                     const ulonglong2 a0 = *reinterpret_cast<const ulonglong2 *>(qp);
                     const ulonglong2 a1 = *reinterpret_cast<const ulonglong2 *>(qp + 4);
                     qv[rl][4 * c + 0] = a0.x;
@@ -688,7 +694,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                         for (int c = 0; c < NCH; ++c) {
                             const uint4 kw =
-                                *reinterpret_cast<const uint4 *>(Ks + tok * (D * 2) + (part + 8 * c) * 16);
+                                *reinterpret_cast<const uint4 *>(Ks + tok * (D * 2) + (part + NPART * c) * 16);
                             const f32x2 k0 = bf16x2_to_f2(kw.x), k1 = bf16x2_to_f2(kw.y);
                             const f32x2 k2 = bf16x2_to_f2(kw.z), k3 = bf16x2_to_f2(kw.w);
 #pragma unroll
@@ -701,15 +707,36 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         }
                         const uint32_t mrow = meta[st * kTile + tok];
                         if constexpr (SPLIT) {
-                            // Lane and lane ^ 4 swap halves: each adds the
-                            // partner's part of the row it finishes.
-                            const float2 a0 = f2_unpack(acc[0]), a1 = f2_unpack(acc[1]);
-                            const float v0 = a0.x + a0.y, v1 = a1.x + a1.y;
-                            float v = hi ? v1 : v0;
-                            v += __shfl_xor_sync(0xffffffffu, hi ? v0 : v1, 4);
-                            v += __shfl_xor_sync(0xffffffffu, v, 2);
-                            v += __shfl_xor_sync(0xffffffffu, v, 1);
-                            sv[s][0] = ((mrow >> (rg * RL + hi)) & 1u) ? v : -INFINITY;
+                            float v[RL];
+#pragma unroll
+                            for (int rl = 0; rl < RL; ++rl) {
+                                const float2 a2 = f2_unpack(acc[rl]);
+                                v[rl] = a2.x + a2.y;
+                            }
+                            // Lane and lane ^ NPART/2 swap halves of their
+                            // rows: each adds the partner's share of the
+                            // half it keeps (upper half if the bit is set).
+                            {
+                                constexpr int o1 = NPART / 2;
+                                const bool up = (part & o1) != 0;
+#pragma unroll
+                                for (int j = 0; j < RL / 2; ++j) {
+                                    const float keep = up ? v[j + RL / 2] : v[j];
+                                    const float send = up ? v[j] : v[j + RL / 2];
+                                    v[j] = keep + __shfl_xor_sync(0xffffffffu, send, o1);
+                                }
+                            }
+                            if constexpr (RL == 4) {
+                                constexpr int o2 = NPART / 4;
+                                const bool up = (part & o2) != 0;
+                                const float keep = up ? v[1] : v[0];
+                                const float send = up ? v[0] : v[1];
+                                v[0] = keep + __shfl_xor_sync(0xffffffffu, send, o2);
+                            }
+#pragma unroll
+                            for (int o = NPART / (2 * RL); o >= 1; o >>= 1)
+                                v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+                            sv[s][0] = ((mrow >> (rg * RL + hr)) & 1u) ? v[0] : -INFINITY;
                         } else {
 #pragma unroll
                             for (int rl = 0; rl < RL; ++rl) {
@@ -732,7 +759,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         for (int s = 1; s < SUB; ++s)
                             mx = fmaxf(mx, sv[s][k]);
 #pragma unroll
-                        for (int o = 8 * NRG; o < 32; o <<= 1)
+                        for (int o = NPART * NRG; o < 32; o <<= 1)
                             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
                         const float mnew = fmaxf(m_run[k], mx);
                         // Rescale the sums where the maximum grew (m_run may
@@ -743,13 +770,14 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             const float alpha = grew ? tc::ex2(m_run[k] - mnew) : 1.f;
                             l_run[k] *= alpha;
                             if constexpr (SPLIT) {
-                                const float ao = __shfl_xor_sync(0xffffffffu, alpha, 4);
-                                const f32x2 a0 = f2_pack(hi ? ao : alpha, hi ? ao : alpha);
-                                const f32x2 a1 = f2_pack(hi ? alpha : ao, hi ? alpha : ao);
 #pragma unroll
-                                for (int e = 0; e < NCH * 4; ++e) {
-                                    o_acc[0][e] = f2_mul(o_acc[0][e], a0);
-                                    o_acc[1][e] = f2_mul(o_acc[1][e], a1);
+                                for (int j = 0; j < RL; ++j) {
+                                    const float aj =
+                                        __shfl_sync(0xffffffffu, alpha, (lane & ~ROWBITS) | (j << RS_SH));
+                                    const f32x2 aa = f2_pack(aj, aj);
+#pragma unroll
+                                    for (int e = 0; e < NCH * 4; ++e)
+                                        o_acc[j][e] = f2_mul(o_acc[j][e], aa);
                                 }
                             } else {
                                 const f32x2 aa = f2_pack(alpha, alpha);
@@ -779,9 +807,9 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         const int tok = lw * 8 + (s0 + s) * TS + ts;
                         float pr[RL];
                         if constexpr (SPLIT) {
-                            const float po = __shfl_xor_sync(0xffffffffu, sv[s][0], 4);
-                            pr[0] = hi ? po : sv[s][0];
-                            pr[1] = hi ? sv[s][0] : po;
+#pragma unroll
+                            for (int j = 0; j < RL; ++j)
+                                pr[j] = __shfl_sync(0xffffffffu, sv[s][0], (lane & ~ROWBITS) | (j << RS_SH));
                         } else {
 #pragma unroll
                             for (int rl = 0; rl < RL; ++rl)
@@ -790,7 +818,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                         for (int c = 0; c < NCH; ++c) {
                             const uint4 vw =
-                                *reinterpret_cast<const uint4 *>(Vs + tok * (D * 2) + (part + 8 * c) * 16);
+                                *reinterpret_cast<const uint4 *>(Vs + tok * (D * 2) + (part + NPART * c) * 16);
                             const f32x2 v0 = bf16x2_to_f2(vw.x), v1 = bf16x2_to_f2(vw.y);
                             const f32x2 v2 = bf16x2_to_f2(vw.z), v3 = bf16x2_to_f2(vw.w);
 #pragma unroll
@@ -821,12 +849,12 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
             for (int k = 0; k < RS; ++k)
 #pragma unroll
-                for (int o = 8 * NRG; o < 32; o <<= 1)
+                for (int o = NPART * NRG; o < 32; o <<= 1)
                     l_run[k] += __shfl_xor_sync(0xffffffffu, l_run[k], o);
 #pragma unroll
             for (int rl = 0; rl < RL; ++rl) {
 #pragma unroll
-                for (int o = 8 * NRG; o < 32; o <<= 1) {
+                for (int o = NPART * NRG; o < 32; o <<= 1) {
 #pragma unroll
                     for (int e = 0; e < NCH * 4; ++e)
                         o_acc[rl][e] = f2_add(o_acc[rl][e], __shfl_xor_sync(0xffffffffu, o_acc[rl][e], o));
@@ -849,8 +877,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
 #pragma unroll
                 for (int k = 0; k < RS; ++k) {
-                    const int r = rg * RL + (SPLIT ? hi : k);
-                    if (rb == 0 && ts == 0 && (part & (SPLIT ? 3 : 7)) == 0 && r < R) {
+                    const int r = rg * RL + (SPLIT ? hr : k);
+                    if (rb == 0 && ts == 0 && (part & ~ROWBITS) == 0 && r < R) {
                         mw[lw * RMAX + r] = m_run[k];
                         lwb[lw * RMAX + r] = l_run[k];
                     }
@@ -861,7 +889,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     if (ts == 0 && r >= rb && r < rb + C::MRB && r < R) {
 #pragma unroll
                         for (int c = 0; c < NCH; ++c) {
-                            float *dst = obuf + (lw * C::MRB + (r - rb)) * D + (part + 8 * c) * 8;
+                            float *dst = obuf + (lw * C::MRB + (r - rb)) * D + (part + NPART * c) * 8;
                             *reinterpret_cast<ulonglong2 *>(dst) =
                                 make_ulonglong2(o_acc[rl][4 * c + 0], o_acc[rl][4 * c + 1]);
                             *reinterpret_cast<ulonglong2 *>(dst + 4) =

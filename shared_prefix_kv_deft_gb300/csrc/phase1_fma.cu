@@ -359,6 +359,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         const int ring = NG == 2 ? cpw : 0;
         const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
         const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
+        const uint64_t kv_pol = tc::l2_evict_first_policy();   // KV is read once per step
         constexpr uint32_t kRowBytes = D * 2;
         constexpr uint32_t kPageBytes = kPageSize * kRowBytes;   // one head's rows of a page
         int seq = 0, iseq = -1, prev_item = -1, sbuf = 0;
@@ -448,8 +449,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     if (lane < 4) {
                         const size_t o = ((size_t)pg * Hkv + h) * kPageSize * D;
                         const uint32_t rb = (uint32_t)lane * kPageBytes;
-                        tc::bulk_load(kdst + rb, kg + o, kPageBytes, full);
-                        tc::bulk_load(vdst + rb, vg + o, kPageBytes, full);
+                        tc::bulk_load(kdst + rb, kg + o, kPageBytes, full, kv_pol);
+                        tc::bulk_load(vdst + rb, vg + o, kPageBytes, full, kv_pol);
                     }
                     tc::mbar_arrive(full);
                     if (lane == 0 && ring == 0 && seq < 16)
@@ -519,8 +520,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 if (pg_lane >= 0) {
                     const size_t o = ((size_t)pg_lane * Hkv + h) * kPageSize * D;
                     const uint32_t rb = (uint32_t)lane * kPageBytes;
-                    tc::bulk_load(kdst + rb, kg + o, kPageBytes, full);
-                    tc::bulk_load(vdst + rb, vg + o, kPageBytes, full);
+                    tc::bulk_load(kdst + rb, kg + o, kPageBytes, full, kv_pol);
+                    tc::bulk_load(vdst + rb, vg + o, kPageBytes, full, kv_pol);
                 }
                 // Ragged rows: one row per warp step; lanes cover K and V chunks.
                 bool any_cp = false;

@@ -436,6 +436,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             const __nv_bfloat16 *src_base = reinterpret_cast<const __nv_bfloat16 *>(kv ? a.v_pages : a.k_pages);
             const CUtensorMap *tm = kv ? &maps.v1 : &maps.k1;
             const CUtensorMap *tm8 = kv ? &maps.v8 : &maps.k8;
+            const uint64_t kv_pol = tc::l2_evict_first_policy();   // KV is read once per step
             // One tile's resolution: rows lane + 32k (k < 4) and pages 0..7.
             struct Res {
                 int seg[4], tok[4], pid[4];   // per row; pid only for ragged rows
@@ -604,16 +605,16 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         run8 = __all_sync(0xffffffffu, lane >= 8 || res.page_y == pg0 + lane);
                     if (run8) {
                         if (lane == 0) {
-                            tc::tma_load_4d(dst, tm8, 0, 0, h, pg0, full);
-                            tc::tma_load_4d(dst + kHalf, tm8, 64, 0, h, pg0, full);
+                            tc::tma_load_4d(dst, tm8, 0, 0, h, pg0, full, kv_pol);
+                            tc::tma_load_4d(dst + kHalf, tm8, 64, 0, h, pg0, full, kv_pol);
                         }
                     } else if (res.page_y >= 0) {
                         const int y = (res.page_y * Hkv + h) * kPageSize;
                         if (lane == 0 && kv == 0 && gseq == 0)
                             KPROF(a, 43);
                         const uint32_t row_b = (uint32_t)(16 * lane) * 128;
-                        tc::tma_load_2d(dst + row_b, tm, 0, y, full);
-                        tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full);
+                        tc::tma_load_2d(dst + row_b, tm, 0, y, full, kv_pol);
+                        tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full, kv_pol);
                     }
                     if (lane == 0 && kv == 0 && gseq < 16)
                         KPROF(a, 801 + 4 * gseq);

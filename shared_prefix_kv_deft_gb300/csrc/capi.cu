@@ -180,6 +180,7 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
     a.gqa_group = plan->gqa_group;
     a.scale_log2 = scale * 1.44269504088896340736f;
     a.wait_prior = 1;
+    a.kv_once = naive ? 0 : 1;
 #ifdef DEFT_KPROF
     if (!g_kprof_buf) {
         if (cudaMalloc(&g_kprof_buf, deft::kKprofSlots * sizeof(unsigned long long)) != cudaSuccess)

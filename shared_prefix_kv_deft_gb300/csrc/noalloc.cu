@@ -138,6 +138,7 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
     a.gqa_group = plan->gqa_group;
     a.scale_log2 = scale * 1.44269504088896340736f;
     a.wait_prior = 1;
+    a.kv_once = 1;
     a.o_part = reinterpret_cast<float *>(base + o_off);
     a.lse_part = reinterpret_cast<float *>(base + lse_off);
 

@@ -359,7 +359,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         const int ring = NG == 2 ? cpw : 0;
         const __nv_bfloat16 *kg = reinterpret_cast<const __nv_bfloat16 *>(a.k_pages);
         const __nv_bfloat16 *vg = reinterpret_cast<const __nv_bfloat16 *>(a.v_pages);
-        const uint64_t kv_pol = tc::l2_evict_first_policy();   // KV is read once per step
+        const uint64_t kv_pol = tc::l2_kv_policy(a.kv_once != 0);
         constexpr uint32_t kRowBytes = D * 2;
         constexpr uint32_t kPageBytes = kPageSize * kRowBytes;   // one head's rows of a page
         int seq = 0, iseq = -1, prev_item = -1, sbuf = 0;

@@ -436,7 +436,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             const __nv_bfloat16 *src_base = reinterpret_cast<const __nv_bfloat16 *>(kv ? a.v_pages : a.k_pages);
             const CUtensorMap *tm = kv ? &maps.v1 : &maps.k1;
             const CUtensorMap *tm8 = kv ? &maps.v8 : &maps.k8;
-            const uint64_t kv_pol = tc::l2_evict_first_policy();   // KV is read once per step
+            const uint64_t kv_pol = tc::l2_kv_policy(a.kv_once != 0);
             // One tile's resolution: rows lane + 32k (k < 4) and pages 0..7.
             struct Res {
                 int seg[4], tok[4], pid[4];   // per row; pid only for ragged rows

@@ -225,13 +225,16 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// L2 cache policy for data a step reads once (the KV stream): its lines are
-// evicted first, so that what the step writes and reads back later (the
-// fp32 partials the merge reads) stays in L2.
-__device__ __forceinline__ uint64_t l2_evict_first_policy()
+// L2 cache policy for the KV stream.  Read once (once = true): its lines
+// are evicted first, so that what the step writes and reads back later (the
+// fp32 partials the merge reads) stays in L2.  Otherwise the normal policy.
+__device__ __forceinline__ uint64_t l2_kv_policy(bool once)
 {
     uint64_t pol;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    if (once)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;\n" : "=l"(pol));
     return pol;
 }
 

@@ -303,3 +303,29 @@ def test_queries_at_token_positions_match_oracle(deft, spec, ct):
     for naive in (False, True):
         out, lse = case.run(naive=naive)
         assert_parity(out, lse, ref, ref_lse, f"{spec.name} ct={ct} naive={naive}")
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_kv_head_shards_give_the_same_step(deft, cfg):
+    """The step splits by KV head with no exchange: a device holding half the
+    KV heads (and their query heads) computes exactly the full step's rows
+    for those heads, bit for bit (same units, same merge order)."""
+    spec = W.config(cfg)
+    layout = W.paged_layout(spec)
+    t = W.make_tensors(spec, layout, device="cuda")
+    npo = torch.from_numpy(layout.node_page_off).cuda()
+    pid = torch.from_numpy(layout.page_id).cuda()
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, spec.gqa_group, naive=False)
+    plan.upload()
+    out, lse = deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
+    torch.cuda.synchronize()
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    Hkv, G = spec.num_kv_heads, spec.gqa_group
+    for shard in range(2):
+        kv = slice(shard * Hkv // 2, (shard + 1) * Hkv // 2)
+        qh = slice(kv.start * G, kv.stop * G)
+        o_s, l_s = deft.deft_tree_attn(t.q[:, qh].contiguous(), t.k_pages[:, kv].contiguous(),
+                                       t.v_pages[:, kv].contiguous(), npo, pid, plan)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(o_s.float().cpu().numpy(), out[:, qh])
+        np.testing.assert_array_equal(l_s.cpu().numpy(), lse[:, qh])

@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -127,8 +128,8 @@ class ClockSampler:
 
     def __init__(self, device_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        fd, self.path = tempfile.mkstemp(prefix=f"deft_clocks_rank{device_index}_", suffix=".csv")
+        os.close(fd)
         sel = []
         try:
             import torch
@@ -156,6 +157,10 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
             self.fh.close()
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
 
     def summary(self, t0: float, t1: float):
         if self.proc is None or not os.path.exists(self.path):

@@ -241,9 +241,10 @@ def imbalance_tree(prefix: int = 32768, leaves: int = 256, lo: int = 64, hi: int
 
 
 def config(i: int) -> TreeSpec:
-    """The five workload shapes, numbered 1..5 in the order the task lists
-    them (6 = the no-sharing control of shape 5; 7 = tree verification with
-    multi-token nodes, every token a query)."""
+    """The benchmark workloads by number: 1 tiny tree, 2 few-shot prefix,
+    3 speculative-decoding forest, 4 multi-step reasoning tree, 5 length
+    imbalance under a long prefix, 6 the no-sharing control of 5, 7 tree
+    verification with multi-token nodes (every token a query)."""
     return {1: tiny_tree, 2: few_shot_tree, 3: speculative_forest,
             4: reasoning_tree, 5: imbalance_tree,
             6: lambda: imbalance_tree(control=True),

@@ -168,6 +168,22 @@ int deft_plan_ex(const int32_t *parent, const int32_t *node_len, int32_t num_nod
                  const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
                  int32_t chunk_target, int32_t gqa_group, int32_t flags, deft_plan_t **out);
 
+/*
+ * deft_plan_rebuild -- re-plan a new tree into an existing plan (a decode
+ * loop, whose tree changes every step): the same arguments, checks and
+ * results as deft_plan_ex, but the plan keeps its device allocation (grown
+ * only when the new plan needs more) and its pinned staging buffer, so the
+ * next deft_plan_upload allocates nothing.  On success the plan is marked
+ * not uploaded (deft_tree_attn returns DEFT_ESTATE until deft_plan_upload);
+ * on error the plan is left exactly as it was.  The device copy of the old
+ * plan stays valid until the next upload, which is stream-ordered: a step
+ * still reading it must be ordered before that upload (same stream, or
+ * synchronised streams).  DEFT_EINVAL for a null plan.
+ */
+int deft_plan_rebuild(deft_plan_t *plan, const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+                      const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+                      int32_t chunk_target, int32_t gqa_group, int32_t flags);
+
 /* Plan statistics (host).  DEFT_EINVAL on null arguments. */
 int deft_plan_stats_get(const deft_plan_t *plan, deft_plan_stats *out);
 
@@ -177,10 +193,14 @@ int deft_plan_stats_get(const deft_plan_t *plan, deft_plan_stats *out);
 int deft_plan_get(const deft_plan_t *plan, int32_t which, void *dst, size_t bytes);
 
 /* Copy the plan to device memory owned by the plan (allocated on the first
- * call, on the current device).  Enqueued on `stream` (a cudaStream_t, NULL =
- * legacy default stream); the plan's host copy stays alive, so the call may
- * return before the copy ends.  Call before deft_tree_attn / deft_naive_attn
- * on the same device. */
+ * call, on the current device, and re-allocated only when a rebuilt plan
+ * needs more or the device changes).  The copy goes through a pinned host
+ * staging buffer owned by the plan (allocated on the first call, grown when
+ * needed) and is enqueued on `stream` (a cudaStream_t, NULL = legacy
+ * default stream); the call returns before it ends, after waiting for the
+ * plan's previous upload copy, if any, to finish.  Call before
+ * deft_tree_attn / deft_naive_attn on the same device.  DEFT_ENOMEM when an
+ * allocation fails, DEFT_ECUDA when a copy or event call fails. */
 int deft_plan_upload(deft_plan_t *plan, void *stream);
 
 /* Bytes of device workspace deft_tree_attn and deft_naive_attn need for this

@@ -37,10 +37,10 @@ ARRAYS = {
 }
 
 # Symbols the header declares (checked by the tests).
-EXPORTS = ["deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_stats_get", "deft_plan_get",
-           "deft_plan_upload", "deft_workspace_bytes", "deft_tree_attn", "deft_naive_attn",
-           "deft_plan_free", "deft_status_str", "deft_version", "deft_trace_enable", "deft_trace_read",
-           "deft_tree_attn_noalloc"]
+EXPORTS = ["deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_rebuild", "deft_plan_stats_get",
+           "deft_plan_get", "deft_plan_upload", "deft_workspace_bytes", "deft_tree_attn",
+           "deft_naive_attn", "deft_plan_free", "deft_status_str", "deft_version", "deft_trace_enable",
+           "deft_trace_read", "deft_tree_attn_noalloc"]
 
 KERNEL_NAMES = {0: "phase1_fma", 1: "phase1_mma", 2: "phase2_merge"}
 PLAN_TREE_ONLY = 1   # deft_plan_ex flag
@@ -86,6 +86,7 @@ def load(path: str = LIB_PATH):
     lib.deft_plan.argtypes = [P, P, i32, P, i32, i32, i32, ctypes.POINTER(P)]
     lib.deft_plan_at.argtypes = [P, P, i32, P, P, i32, i32, i32, ctypes.POINTER(P)]
     lib.deft_plan_ex.argtypes = [P, P, i32, P, P, i32, i32, i32, i32, ctypes.POINTER(P)]
+    lib.deft_plan_rebuild.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32]
     lib.deft_plan_stats_get.argtypes = [P, ctypes.POINTER(PlanStats)]
     lib.deft_plan_get.argtypes = [P, i32, P, sz]
     lib.deft_plan_upload.argtypes = [P, P]
@@ -103,10 +104,9 @@ def load(path: str = LIB_PATH):
     lib.deft_version.argtypes = []
     lib.deft_trace_enable.argtypes = [i32]
     lib.deft_trace_read.argtypes = [ctypes.POINTER(TraceRecord), i32, ctypes.POINTER(i32)]
-    for fn in ("deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_stats_get", "deft_plan_get",
-               "deft_plan_upload",
-               "deft_tree_attn", "deft_naive_attn", "deft_version", "deft_trace_enable",
-               "deft_trace_read", "deft_tree_attn_noalloc"):
+    for fn in ("deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_rebuild", "deft_plan_stats_get",
+               "deft_plan_get", "deft_plan_upload", "deft_tree_attn", "deft_naive_attn", "deft_version",
+               "deft_trace_enable", "deft_trace_read", "deft_tree_attn_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -148,9 +148,26 @@ class Plan:
                                                 int(gqa_group), 0 if naive else PLAN_TREE_ONLY,
                                                 ctypes.byref(h)))
         self.handle = h
+        self._read_stats()
+
+    def _read_stats(self):
         st = PlanStats()
-        _check("deft_plan_stats_get", lib.deft_plan_stats_get(self.handle, ctypes.byref(st)))
+        _check("deft_plan_stats_get", load().deft_plan_stats_get(self.handle, ctypes.byref(st)))
         self.stats = st.as_dict()
+
+    def rebuild(self, parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
+                query_pos=None, naive: bool = True):
+        """deft_plan_rebuild: plan a new tree into this plan, keeping its device
+        allocation and staging buffer; upload() again before the next step.
+        On error (DeftError) the plan is unchanged."""
+        par, ln, qn = _i32(parent), _i32(node_len), _i32(query_node)
+        pos = None if query_pos is None else _i32(query_pos)
+        _check("deft_plan_rebuild", load().deft_plan_rebuild(
+            self.handle, _ptr(par), _ptr(ln), int(par.shape[0]), _ptr(qn),
+            None if pos is None else _ptr(pos), int(qn.shape[0]), int(chunk_target), int(gqa_group),
+            0 if naive else PLAN_TREE_ONLY))
+        self._parent, self._len, self._qn, self._pos = par, ln, qn, pos
+        self._read_stats()
 
     def __del__(self):
         h = getattr(self, "handle", None)

@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <new>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -211,20 +212,15 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
 
 extern "C" {
 
-int deft_plan_ex(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-                 const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
-                 int32_t chunk_target, int32_t gqa_group, int32_t flags, deft_plan_t **out)
+namespace {
+
+// Builds the host side of a plan into `p` (its device state untouched).
+int build_host(const int32_t *parent, const int32_t *node_len, int32_t num_nodes, const int32_t *query_node,
+               const int32_t *query_pos, int32_t num_queries, int32_t chunk_target, int32_t gqa_group,
+               int32_t flags, deft_plan_t *p)
 {
-    if (!out)
+    if (flags & ~(int32_t)DEFT_PLAN_TREE_ONLY)
         return DEFT_EINVAL;
-    if (flags & ~(int32_t)DEFT_PLAN_TREE_ONLY) {
-        *out = nullptr;
-        return DEFT_EINVAL;
-    }
-    *out = nullptr;
-    deft_plan_t *p = new (std::nothrow) deft_plan_t();
-    if (!p)
-        return DEFT_ENOMEM;
     int rc;
     try {
         rc = deft::build_plan(parent, node_len, num_nodes, query_node, query_pos, num_queries,
@@ -232,16 +228,62 @@ int deft_plan_ex(const int32_t *parent, const int32_t *node_len, int32_t num_nod
     } catch (const std::bad_alloc &) {
         rc = DEFT_ENOMEM;
     }
-    if (rc != DEFT_OK) {
-        delete p;
+    if (rc != DEFT_OK)
         return rc;
-    }
     size_t cursor = 0;
     Layout lt, ln;
     plan_partition_layout(p->tree, cursor, lt);
     plan_partition_layout(p->naive, cursor, ln);
     p->stats.device_bytes = (int64_t)cursor;
+    return DEFT_OK;
+}
+
+}  // namespace
+
+int deft_plan_ex(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+                 const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+                 int32_t chunk_target, int32_t gqa_group, int32_t flags, deft_plan_t **out)
+{
+    if (!out)
+        return DEFT_EINVAL;
+    *out = nullptr;
+    deft_plan_t *p = new (std::nothrow) deft_plan_t();
+    if (!p)
+        return DEFT_ENOMEM;
+    const int rc = build_host(parent, node_len, num_nodes, query_node, query_pos, num_queries, chunk_target,
+                              gqa_group, flags, p);
+    if (rc != DEFT_OK) {
+        delete p;
+        return rc;
+    }
     *out = p;
+    return DEFT_OK;
+}
+
+int deft_plan_rebuild(deft_plan_t *plan, const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+                      const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+                      int32_t chunk_target, int32_t gqa_group, int32_t flags)
+{
+    if (!plan)
+        return DEFT_EINVAL;
+    deft_plan_t fresh;
+    const int rc = build_host(parent, node_len, num_nodes, query_node, query_pos, num_queries, chunk_target,
+                              gqa_group, flags, &fresh);
+    if (rc != DEFT_OK)
+        return rc;   // the plan is left as it was
+    // The host side moves in; the device copy, staging buffer and event stay.
+    plan->num_nodes = fresh.num_nodes;
+    plan->num_queries = fresh.num_queries;
+    plan->gqa_group = fresh.gqa_group;
+    plan->chunk_target = fresh.chunk_target;
+    plan->mask_words = fresh.mask_words;
+    plan->cover = std::move(fresh.cover);
+    plan->order = std::move(fresh.order);
+    plan->tree = std::move(fresh.tree);
+    plan->naive = std::move(fresh.naive);
+    plan->has_naive = fresh.has_naive;
+    plan->stats = fresh.stats;
+    plan->uploaded = false;
     return DEFT_OK;
 }
 
@@ -326,16 +368,43 @@ int deft_plan_upload(deft_plan_t *plan, void *stream)
         plan->dev_bytes = cursor;
         plan->dev_device = dev;
     }
-    std::vector<uint8_t> host(cursor, 0);
+    // The pinned staging buffer: wait for its previous copy, grow it if
+    // needed (the only host allocation, kept across uploads and rebuilds).
+    cudaEvent_t done = reinterpret_cast<cudaEvent_t>(plan->stage_done);
+    if (done && cudaEventSynchronize(done) != cudaSuccess)
+        return DEFT_ECUDA;
+    if (done && plan->stage_device != dev) {
+        cudaEventDestroy(done);
+        done = nullptr;
+        plan->stage_done = nullptr;
+    }
+    if (!done) {
+        if (cudaEventCreateWithFlags(&done, cudaEventDisableTiming) != cudaSuccess)
+            return DEFT_ECUDA;
+        plan->stage_done = done;
+        plan->stage_device = dev;
+    }
+    if (plan->host_stage_bytes < cursor) {
+        if (plan->host_stage)
+            cudaFreeHost(plan->host_stage);
+        plan->host_stage = nullptr;
+        plan->host_stage_bytes = 0;
+        if (cudaHostAlloc(&plan->host_stage, cursor, cudaHostAllocPortable) != cudaSuccess) {
+            plan->host_stage = nullptr;
+            return DEFT_ENOMEM;
+        }
+        plan->host_stage_bytes = cursor;
+    }
+    uint8_t *host = reinterpret_cast<uint8_t *>(plan->host_stage);
+    std::memset(host, 0, cursor);
     uint8_t *dev_base = reinterpret_cast<uint8_t *>(plan->dev_blob);
-    fill_partition(plan->tree, lt, host.data(), dev_base, plan->num_nodes, plan->num_queries, plan->mask_words,
+    fill_partition(plan->tree, lt, host, dev_base, plan->num_nodes, plan->num_queries, plan->mask_words,
                    plan->dev_tree);
-    fill_partition(plan->naive, ln, host.data(), dev_base, plan->num_nodes, plan->num_queries,
-                   plan->mask_words, plan->dev_naive);
+    fill_partition(plan->naive, ln, host, dev_base, plan->num_nodes, plan->num_queries, plan->mask_words,
+                   plan->dev_naive);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // Pageable source: the runtime has staged it by the time the call
-    // returns, so the local buffer may be released afterwards.
-    if (cudaMemcpyAsync(plan->dev_blob, host.data(), cursor, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    if (cudaMemcpyAsync(plan->dev_blob, host, cursor, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaEventRecord(done, st) != cudaSuccess)
         return DEFT_ECUDA;
     plan->uploaded = true;
     return DEFT_OK;
@@ -375,6 +444,12 @@ void deft_plan_free(deft_plan_t *plan)
 {
     if (!plan)
         return;
+    if (plan->stage_done) {
+        cudaEventSynchronize(reinterpret_cast<cudaEvent_t>(plan->stage_done));
+        cudaEventDestroy(reinterpret_cast<cudaEvent_t>(plan->stage_done));
+    }
+    if (plan->host_stage)
+        cudaFreeHost(plan->host_stage);
     if (plan->dev_blob)
         cudaFree(plan->dev_blob);
     delete plan;

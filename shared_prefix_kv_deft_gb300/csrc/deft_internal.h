@@ -203,6 +203,13 @@ struct deft_plan_t {
     bool uploaded = false;
     deft::DevPartition dev_tree{};
     deft::DevPartition dev_naive{};
+    // Pinned host staging buffer of deft_plan_upload, kept across uploads and
+    // rebuilds, and the event (a cudaEvent_t, created on device stage_device)
+    // recorded after its last copy.
+    void *host_stage = nullptr;
+    size_t host_stage_bytes = 0;
+    void *stage_done = nullptr;
+    int stage_device = -1;
 };
 
 namespace deft {

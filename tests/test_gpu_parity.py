@@ -329,3 +329,36 @@ def test_kv_head_shards_give_the_same_step(deft, cfg):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(o_s.float().cpu().numpy(), out[:, qh])
         np.testing.assert_array_equal(l_s.cpu().numpy(), lse[:, qh])
+
+
+def test_rebuilt_plan_runs_like_a_fresh_one(deft):
+    """A decode loop's plan reuse: rebuild into the same plan (smaller tree,
+    then a larger one that grows the device copy), upload, step: bit for bit
+    the step of a fresh plan; a rebuilt plan not yet uploaded is refused."""
+    lib = deft.load()
+    P = ctypes.c_void_p
+    big, small = W.config(2), W.config(1)
+    plan = deft.Plan(small.parent, small.node_len, small.query_node, 64, small.gqa_group, naive=False)
+    plan.upload()
+    for spec, ct in ((big, 256), (small, 64), (big, 128)):
+        layout = W.paged_layout(spec)
+        t = W.make_tensors(spec, layout, device="cuda")
+        npo = torch.from_numpy(layout.node_page_off).cuda()
+        pid = torch.from_numpy(layout.page_id).cuda()
+        plan.rebuild(spec.parent, spec.node_len, spec.query_node, ct, spec.gqa_group, naive=False)
+        bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim)
+        rc = lib.deft_tree_attn(P(t.q.data_ptr()), P(t.k_pages.data_ptr()), P(t.v_pages.data_ptr()),
+                                P(npo.data_ptr()), P(pid.data_ptr()), t.k_pages.shape[0], spec.num_q_heads,
+                                spec.num_kv_heads, spec.head_dim, 16, 0.1, plan.handle,
+                                P(bufs.out.data_ptr()), 0, P(bufs.lse.data_ptr()),
+                                P(bufs.workspace.data_ptr()), bufs.workspace.numel(),
+                                P(torch.cuda.current_stream().cuda_stream))
+        assert rc == -8   # rebuilt, not uploaded
+        plan.upload()
+        out, lse = deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)
+        fresh = deft.Plan(spec.parent, spec.node_len, spec.query_node, ct, spec.gqa_group, naive=False)
+        fresh.upload()
+        out2, lse2 = deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, fresh)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.float().cpu().numpy(), out2.float().cpu().numpy())
+        np.testing.assert_array_equal(lse.cpu().numpy(), lse2.cpu().numpy())

@@ -322,3 +322,38 @@ def test_plan_ex_rejects_unknown_flags():
                           64, 1, deft.PLAN_TREE_ONLY, ctypes.byref(h))
     assert rc == 0 and h.value
     lib.deft_plan_free(h)
+
+
+REBUILDS = [(2, 4), (4, 7), (7, 1), (1, 3)]
+
+
+@pytest.mark.parametrize("first,second", REBUILDS)
+@pytest.mark.parametrize("naive", [True, False])
+def test_rebuild_matches_a_fresh_plan(first, second, naive):
+    """deft_plan_rebuild leaves exactly what deft_plan_ex builds for the new
+    tree (every array and statistic)."""
+    a, b = W.config(first), W.config(second)
+    p = deft.Plan(a.parent, a.node_len, a.query_node, 256, a.gqa_group, query_pos=a.query_pos)
+    p.rebuild(b.parent, b.node_len, b.query_node, 128, b.gqa_group, query_pos=b.query_pos, naive=naive)
+    f = deft.Plan(b.parent, b.node_len, b.query_node, 128, b.gqa_group, query_pos=b.query_pos, naive=naive)
+    assert p.stats == f.stats
+    for name in deft.ARRAYS:
+        np.testing.assert_array_equal(p.get(name), f.get(name))
+
+
+def test_failed_rebuild_leaves_the_plan_unchanged():
+    a = W.config(4)
+    p = deft.Plan(a.parent, a.node_len, a.query_node, 256, a.gqa_group)
+    before = {name: p.get(name).copy() for name in deft.ARRAYS}
+    stats = dict(p.stats)
+    bad_parent = a.parent.copy()
+    bad_parent[3] = 3   # a self-loop: not a forest
+    for kwargs in ({"parent": bad_parent}, {"chunk_target": 0}, {"query_node": a.query_node + 10 ** 6}):
+        args = dict(parent=a.parent, node_len=a.node_len, query_node=a.query_node, chunk_target=256,
+                    gqa_group=a.gqa_group)
+        args.update(kwargs)
+        with pytest.raises(deft.DeftError):
+            p.rebuild(**args)
+        assert p.stats == stats
+        for name in deft.ARRAYS:
+            np.testing.assert_array_equal(p.get(name), before[name])

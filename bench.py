@@ -194,11 +194,16 @@ class ClockSampler:
 # ncu summary (committed under profiles/) for the roofline's traffic figure
 # ---------------------------------------------------------------------------
 
+# Sources that decide what the phase-1 kernels read and write: the kernels,
+# their launch shapes and the planner (not the C-ABI glue).
+HOST_GLUE = ("capi.cu", "noalloc.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shared_prefix_kv_deft_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")) and f not in HOST_GLUE:
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

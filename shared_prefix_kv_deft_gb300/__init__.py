@@ -125,8 +125,10 @@ def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
-def _ptr(a: np.ndarray):
-    return a.ctypes.data_as(ctypes.c_void_p)
+def _ptr(a: np.ndarray) -> int:
+    # The address as an int (ctypes converts it for c_void_p parameters);
+    # cheaper than building a ctypes pointer object.
+    return a.ctypes.data
 
 
 class Plan:
@@ -148,12 +150,16 @@ class Plan:
                                                 int(gqa_group), 0 if naive else PLAN_TREE_ONLY,
                                                 ctypes.byref(h)))
         self.handle = h
-        self._read_stats()
+        self._stats = None
 
-    def _read_stats(self):
-        st = PlanStats()
-        _check("deft_plan_stats_get", load().deft_plan_stats_get(self.handle, ctypes.byref(st)))
-        self.stats = st.as_dict()
+    @property
+    def stats(self) -> dict:
+        """deft_plan_stats_get, read once per build."""
+        if self._stats is None:
+            st = PlanStats()
+            _check("deft_plan_stats_get", load().deft_plan_stats_get(self.handle, ctypes.byref(st)))
+            self._stats = st.as_dict()
+        return self._stats
 
     def rebuild(self, parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
                 query_pos=None, naive: bool = True):
@@ -167,7 +173,7 @@ class Plan:
             None if pos is None else _ptr(pos), int(qn.shape[0]), int(chunk_target), int(gqa_group),
             0 if naive else PLAN_TREE_ONLY))
         self._parent, self._len, self._qn, self._pos = par, ln, qn, pos
-        self._read_stats()
+        self._stats = None
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -252,11 +258,10 @@ def _attn(fn_name: str, q, k_pages, v_pages, node_page_off, page_id, plan: Plan,
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     odt = DEFT_OUT_BF16 if bufs.out.dtype == torch.bfloat16 else DEFT_OUT_F32
     rc = getattr(lib, fn_name)(
-        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k_pages.data_ptr()),
-        ctypes.c_void_p(v_pages.data_ptr()), ctypes.c_void_p(node_page_off.data_ptr()),
-        ctypes.c_void_p(page_id.data_ptr()), int(k_pages.shape[0]), int(Hq), int(Hkv), int(d),
-        int(P), float(scale), plan.handle, ctypes.c_void_p(bufs.out.data_ptr()), odt,
-        ctypes.c_void_p(bufs.lse.data_ptr()), ctypes.c_void_p(bufs.workspace.data_ptr()),
+        q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), node_page_off.data_ptr(),
+        page_id.data_ptr(), int(k_pages.shape[0]), int(Hq), int(Hkv), int(d),
+        int(P), float(scale), plan.handle, bufs.out.data_ptr(), odt,
+        bufs.lse.data_ptr(), bufs.workspace.data_ptr(),
         int(bufs.workspace.numel()), _stream(stream))
     _check(fn_name, rc)
     return bufs.out, bufs.lse

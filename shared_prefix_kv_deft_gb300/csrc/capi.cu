@@ -395,8 +395,9 @@ int deft_plan_upload(deft_plan_t *plan, void *stream)
         }
         plan->host_stage_bytes = cursor;
     }
+    // Every array is written in full; the alignment padding between arrays
+    // is never read.
     uint8_t *host = reinterpret_cast<uint8_t *>(plan->host_stage);
-    std::memset(host, 0, cursor);
     uint8_t *dev_base = reinterpret_cast<uint8_t *>(plan->dev_blob);
     fill_partition(plan->tree, lt, host, dev_base, plan->num_nodes, plan->num_queries, plan->mask_words,
                    plan->dev_tree);

@@ -261,6 +261,22 @@ def cpu_baseline(spec, layout, bits, budget_s=12.0):
                       f"scaled to the full step"}
 
 
+def max_over_ranks(x: float, pg, device) -> float:
+    """The largest of every rank's x (x itself without a process group)."""
+    if pg is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_step(slowest_ms_per_step: float, world: int) -> float:
+    """Whole-job time per step: `world` replicas each finish a step in the
+    slowest rank's time, so the job completes `world` steps in that time."""
+    return slowest_ms_per_step * 1e3 / world
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
@@ -380,13 +396,9 @@ def main():
     clocks = sampler.summary(w0, w1)
     sampler.stop()
     tms, recs, _, _ = timed(step, args.steps, trace=True)  # per-kernel durations
-    elapsed = sum(ms)
-    if pg is not None:
-        tt = torch.tensor([elapsed], dtype=torch.float64, device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        elapsed = float(tt.item())
+    elapsed = max_over_ranks(sum(ms), pg, dev)
     ms_per_step = elapsed / args.steps
-    value_us = ms_per_step * 1e3 / world
+    value_us = job_us_per_step(ms_per_step, world)
 
     st = plan.stats
     d, Hq, Hkv, Q = spec.head_dim, spec.num_q_heads, spec.num_kv_heads, spec.num_queries
@@ -509,12 +521,8 @@ def main():
                 e2e_t.append(time.perf_counter() - t0)
         plan_bytes = p.stats["device_bytes"]
         del p
-        e2e_us = statistics.mean(e2e_t) * 1e6
-        if pg is not None:
-            tt = torch.tensor([e2e_us], dtype=torch.float64, device=dev)
-            pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-            e2e_us = float(tt.item())
-        line["e2e"] = {"value": e2e_us / world, "unit": "us/step",
+        e2e_us = max_over_ranks(statistics.mean(e2e_t) * 1e6, pg, dev)
+        line["e2e"] = {"value": job_us_per_step(e2e_us * 1e-3, world), "unit": "us/step",
                        "h2d_bytes_per_step": int(q_host.numel() * 2 + plan_bytes),
                        "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()
                                                  + lse_host.numel() * 4),

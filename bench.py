@@ -230,35 +230,44 @@ def host_inputs(spec, layout, t):
     return (W.bf16_bits(t.q), W.bf16_bits(t.k_pages), W.bf16_bits(t.v_pages))
 
 
-def oracle_step(oracle, spec, layout, bits, subset):
+def oracle_step(oracle, spec, layout, bits, subset, threads=0):
     return oracle.tree_attn(bits[0], bits[1], bits[2], layout.node_page_off, layout.page_id,
                             layout.page_size, spec.parent, spec.node_len, spec.query_node,
                             spec.num_q_heads, spec.num_kv_heads, spec.head_dim,
                             1.0 / math.sqrt(spec.head_dim), query_subset=subset,
-                            query_pos=spec.query_pos)
+                            query_pos=spec.query_pos, threads=threads)
 
 
-def cpu_baseline(spec, layout, bits, budget_s=12.0):
-    """Time the oracle, as it stands, on a bounded sample of the workload."""
-    import oracle
-    oracle.load()
+def time_oracle(oracle, spec, layout, bits, budget_s, threads=0):
+    """us per full step of the oracle on `threads` host threads (0: all),
+    timed on a sample of queries sized to about `budget_s` seconds."""
     Q = spec.num_queries
     # Calibrate on one query, then size the sample to the budget.
     t0 = time.perf_counter()
-    oracle_step(oracle, spec, layout, bits, [0])
+    oracle_step(oracle, spec, layout, bits, [0], threads)
     per_q = max(time.perf_counter() - t0, 1e-6)
     nq = int(max(1, min(Q, budget_s / 2 / per_q)))
     subset = np.linspace(0, Q - 1, nq).astype(np.int32)
     reps, spent = 0, 0.0
     while spent < budget_s / 2 and reps < 50:
         t0 = time.perf_counter()
-        oracle_step(oracle, spec, layout, bits, subset)
+        oracle_step(oracle, spec, layout, bits, subset, threads)
         spent += time.perf_counter() - t0
         reps += 1
-    us_per_step = spent / reps * (Q / nq) * 1e6
-    return {"value": us_per_step, "unit": "us/step", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{nq} of {Q} queries x all {spec.num_q_heads} heads, {reps} run(s), "
-                      f"scaled to the full step"}
+    return spent / reps * (Q / nq) * 1e6, f"{nq} of {Q} queries x all {spec.num_q_heads} heads, " \
+                                           f"{reps} run(s), scaled to the full step"
+
+
+def cpu_baseline(spec, layout, bits, budget_s=12.0):
+    """Time the oracle, as it stands, on a bounded sample of the workload: on
+    all host threads (the value) and on one thread."""
+    import oracle
+    oracle.load()
+    us, sample = time_oracle(oracle, spec, layout, bits, budget_s)
+    us1, sample1 = time_oracle(oracle, spec, layout, bits, budget_s / 2, threads=1)
+    return {"value": us, "unit": "us/step", "cores": oracle.max_threads(), "kind": "oracle",
+            "sample": sample,
+            "single_thread": {"value": us1, "unit": "us/step", "cores": 1, "sample": sample1}}
 
 
 def max_over_ranks(x: float, pg, device) -> float:

@@ -178,7 +178,9 @@ int deft_plan_ex(const int32_t *parent, const int32_t *node_len, int32_t num_nod
  * on error the plan is left exactly as it was.  The device copy of the old
  * plan stays valid until the next upload, which is stream-ordered: a step
  * still reading it must be ordered before that upload (same stream, or
- * synchronised streams).  DEFT_EINVAL for a null plan.
+ * synchronised streams).  A CUDA graph that captured a step of this plan
+ * holds the old launch shapes and device addresses: capture it again after
+ * a rebuild.  DEFT_EINVAL for a null plan.
  */
 int deft_plan_rebuild(deft_plan_t *plan, const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                       const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,

@@ -103,6 +103,27 @@ def test_tree_and_naive_match_oracle(deft, spec, ct):
     assert_parity(out, lse, ref, ref_lse, f"naive ct={ct}")
 
 
+EXTREME = [W.tiny_tree(),
+           W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4, head_dim=128),
+           W.reasoning_tree(levels=3, len_lo=20, len_hi=90, num_queries=24, q_heads=8, kv_heads=2),
+           W.random_tree(7, max_nodes=16, max_len=90, max_queries=12),
+           W.chain_tree([5, 70, 1, 130], q_heads=4, kv_heads=4, head_dim=128)]
+
+
+@pytest.mark.parametrize("spec", EXTREME, ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [1, 8192])
+def test_extreme_chunk_targets_match_oracle(deft, spec, ct):
+    """chunk_target at its bounds: 1 (every node its own run of pieces) and
+    8192 (the largest chunks the plan allows, page lists at their limit)."""
+    inp = dense_inputs(spec, seed=ct + 3)
+    ref, ref_lse = run_oracle(inp)
+    case = Case(deft, inp, ct)
+    out, lse = case.run()
+    assert_parity(out, lse, ref, ref_lse, f"tree ct={ct}")
+    out, lse = case.run(naive=True)
+    assert_parity(out, lse, ref, ref_lse, f"naive ct={ct}")
+
+
 def test_fp32_output(deft):
     spec = W.reasoning_tree(levels=3, len_lo=20, len_hi=90, num_queries=24, q_heads=8, kv_heads=2)
     inp = dense_inputs(spec, seed=5)

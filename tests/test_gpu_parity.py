@@ -383,3 +383,45 @@ def test_rebuilt_plan_runs_like_a_fresh_one(deft):
         torch.cuda.synchronize()
         np.testing.assert_array_equal(out.float().cpu().numpy(), out2.float().cpu().numpy())
         np.testing.assert_array_equal(lse.cpu().numpy(), lse2.cpu().numpy())
+
+
+def path_token_counts(spec):
+    """|T(q)| per query from the oracle's own path walk: the tokens query q
+    attends (its own node up to its position)."""
+    counts = []
+    for q, path in enumerate(oracle.paths(spec.parent, spec.query_node)):
+        n_own = int(spec.query_node[q])
+        c = 0
+        for n in path:
+            if n == n_own and spec.query_pos is not None and spec.query_pos[q] >= 0:
+                c += int(spec.query_pos[q]) + 1
+            else:
+                c += int(spec.node_len[n])
+        counts.append(c)
+    return np.array(counts, dtype=np.int64)
+
+
+@pytest.mark.parametrize("cfg", sorted(FULL))
+def test_every_query_attends_each_of_its_tokens_once(deft, cfg):
+    """An exact count of the (query, token) pairs the kernels process, for
+    every query and head, at full size: with K = 0 every logit is 0, each
+    attended token adds exactly 1 to its chunk's sum, and the merged lse is
+    ln(number of tokens attended).  It must be |T(q)| (each pair once, none
+    missed), in the tree and the naive forms."""
+    spec = W.config(cfg)
+    layout = W.paged_layout(spec)
+    t = W.make_tensors(spec, layout, device="cuda")
+    t.k_pages.zero_()
+    npo = torch.from_numpy(layout.node_page_off).cuda()
+    pid = torch.from_numpy(layout.page_id).cuda()
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, FULL[cfg], spec.gqa_group,
+                     query_pos=spec.query_pos)
+    plan.upload()
+    want = path_token_counts(spec)
+    for fn in (deft.deft_tree_attn, deft.deft_naive_attn):
+        _, lse = fn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
+        torch.cuda.synchronize()
+        got = np.rint(np.exp(lse.cpu().numpy().astype(np.float64))).astype(np.int64)
+        bad = np.argwhere(got != want[:, None])
+        assert bad.size == 0, f"{fn.__name__}: query {bad[0][0]} head {bad[0][1]} attends " \
+                              f"{got[tuple(bad[0])]} tokens, expected {want[bad[0][0]]}"

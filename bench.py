@@ -52,7 +52,60 @@ def parse():
     ap.add_argument("--impl", choices=["deft", "reference"], default="deft")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the naive, e2e and CPU-baseline legs")
+    ap.add_argument("--step-flags", type=int, default=0,
+                    help="deft_tree_attn_ex flags for the timed step (4: merge in a separate launch)")
+    ap.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
+                    help="run a few steps of a small named case for an ncu capture, print nothing else")
+    ap.add_argument("--range", action="store_true",
+                    help="with --profile-case: bracket one more step with cudaProfilerStart/Stop "
+                         "(ncu --replay-mode range --profile-from-start off)")
     return ap.parse_args()
+
+
+# Small seeded cases of the benchmark workloads' shapes, for ncu captures that
+# must stay small (a few hundred MB on the device).
+PROFILE_CASES = {
+    # 3 requests x (4000-token prefix + 64-node token tree), 32/32 heads: tensor-core launch, 64 rows
+    "speculative_3req": lambda: W.speculative_forest(requests=3),
+    # 32 independent 2048-token sequences, GQA 32/8: CUDA-core launch, 4 rows
+    "control_32x2048": lambda: W.imbalance_tree(control=True, leaves=32),
+    # the few-shot tree (4096-token prefix + 32 x 256)
+    "few_shot": lambda: W.config(2),
+    # the reasoning tree (4 levels, 128 queries, GQA 32/8)
+    "reasoning": lambda: W.config(4),
+    # the imbalance shape with 16 leaves: the 32768-token prefix at 64 rows, split over CTAs
+    "imbalance_16leaves": lambda: W.imbalance_tree(leaves=16),
+}
+
+
+def run_profile_case(args):
+    """A few steps of a named case on cuda:0 (the capture target); with
+    --range one more step bracketed for ncu's range replay."""
+    import torch
+    import shared_prefix_kv_deft_gb300 as deft
+    spec = PROFILE_CASES[args.profile_case]()
+    lay = W.paged_layout(spec)
+    t = W.make_tensors(spec, lay, device="cuda")
+    npo = torch.from_numpy(lay.node_page_off).cuda()
+    pid = torch.from_numpy(lay.page_id).cuda()
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group)
+    plan.upload()
+    bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim)
+
+    def step():
+        deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs, flags=args.step_flags)
+    for _ in range(max(1, args.steps)):
+        step()
+    torch.cuda.synchronize()
+    if args.range:
+        torch.cuda.profiler.start()
+        step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+    if plan.step_status() != 0:
+        raise RuntimeError("a kernel reported a failed wait")
+    print("ok", spec.name)
+    return 0
 
 
 def dist_env():
@@ -335,6 +388,8 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.profile_case:
+        return run_profile_case(args)
 
     import torch
     import shared_prefix_kv_deft_gb300 as deft
@@ -366,7 +421,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)
+        deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs, flags=args.step_flags)
 
     def barrier():
         torch.cuda.synchronize(dev)

@@ -10,7 +10,10 @@
  * Splitting), reads each chunk once for all queries whose path covers it
  * (KV-Guided Grouping, recorded as a per-segment query bitmask), computes a
  * partial softmax attention with its log-sum-exp per (chunk, query, head)
- * and merges the partials per query by lse weight.
+ * and merges the partials per query by lse weight (a query whose path lies
+ * in one CUDA-core chunk needs no merge: its rows are written by the kernel
+ * that reads the chunk, the Guide's "Fused In-SRAM Online Softmax
+ * Merging").
  *
  * Conventions shared by every call:
  *   - Tree: parent[n] (int32, -1 = root; forests allowed), node_len[n] (int32
@@ -47,14 +50,23 @@ typedef enum deft_status {
     DEFT_EUNSUPPORTED = -5,  /* head_dim / page_size / GQA group not compiled in    */
     DEFT_ECUDA = -6,         /* a CUDA runtime call or kernel launch failed          */
     DEFT_EWORKSPACE = -7,    /* workspace null, too small or not 256-byte aligned   */
-    DEFT_ESTATE = -8         /* plan not uploaded, built for another GQA group, or  */
+    DEFT_ESTATE = -8,        /* plan not uploaded, built for another GQA group, or  */
                              /* (deft_naive_attn) built without the naive partition */
+    DEFT_EDEVICE = -9        /* deft_step_status: a kernel reported a failed wait   */
 } deft_status;
 
 enum { DEFT_OUT_BF16 = 0, DEFT_OUT_F32 = 1 };
 
 /* deft_plan_ex flags. */
 enum { DEFT_PLAN_TREE_ONLY = 1 };
+
+/* deft_tree_attn_ex flags. */
+enum {
+    DEFT_STEP_NAIVE = 1,          /* run the naive per-query partition (deft_naive_attn)          */
+    DEFT_STEP_CUDA_CORES = 2,     /* run >= 16-row chunks on the CUDA-core kernel too, in items   */
+                                  /* of at most 16 rows (same results; a comparison of the paths) */
+    DEFT_STEP_SEPARATE_MERGE = 4  /* every query through the partials and the merge launch        */
+};
 
 /* Opaque plan: the flattened chunk list, segment bitmasks and per-query
  * partial-slot lists of one tree.  Library-owned; free with deft_plan_free. */
@@ -77,6 +89,8 @@ typedef struct deft_plan_stats {
     int32_t naive_num_chunks;    /* per-query flash-decoding partition (0 if tree-only) */
     int32_t naive_num_slots;
     int32_t naive_num_segments;
+    int32_t num_merge_queries;   /* queries of the tree plan the merge launch handles     */
+    int32_t reserved0;
     int64_t unique_tokens;       /* tokens on at least one query path                   */
     int64_t naive_tokens;        /* sum over queries of their path tokens               */
     int64_t planned_tokens;      /* sum of chunk lengths; equals unique_tokens          */
@@ -109,7 +123,10 @@ typedef enum deft_plan_array {
     DEFT_A_NAIVE_SEG_TOK_LEN = 19,   /* int32 [naive_num_segments]                            */
     DEFT_A_NAIVE_Q_SLOT_OFF = 20,    /* int32 [num_queries + 1]                               */
     DEFT_A_NAIVE_Q_SLOT = 21,        /* int32 [naive_num_slots]                               */
-    DEFT_A_COUNT = 22
+    DEFT_A_FMA_DIRECT = 22,     /* uint32 [num_fma_items]   bit r: row r goes to out directly */
+    DEFT_A_FALLBACK_DIRECT = 23,/* uint32 [num_fallback_items]  (always 0)                    */
+    DEFT_A_MERGE_Q = 24,        /* int32  [num_merge_queries]  queries the merge launch takes */
+    DEFT_A_COUNT = 25
 } deft_plan_array;
 
 /*
@@ -216,14 +233,19 @@ size_t deft_workspace_bytes(const deft_plan_t *plan, int32_t num_q_heads, int32_
  * per query).  Phase 1 reads every chunk's KV once per KV head and writes
  * (o, lse) partials for each (chunk, query, query head) into the
  * workspace; phase 2 merges each query's partials by lse weight into out
- * and lse.  Chunks with >= 16 rows run on tcgen05 tensor cores (head_dim
- * 128), the others on CUDA-core FMA.
+ * and lse.  A query whose whole path lies in one chunk of fewer than 16 rows
+ * has a single partial: the CUDA-core kernel writes its rows to out / lse
+ * directly, and phase 2 runs only over the other queries (and not at all
+ * when there are none).  Chunks with >= 16 rows run on tcgen05 tensor cores
+ * (head_dim 128), the others on CUDA-core FMA.
  *   q, k_pages, v_pages, node_page_off, page_id, out, lse, workspace: device
  *     pointers as described at the top of this file; q, k_pages and v_pages
  *     must be 16-byte aligned (else DEFT_EINVAL); workspace must be
  *     256-byte aligned and hold deft_workspace_bytes(plan, num_q_heads,
- *     head_dim) bytes; its contents need not be initialised.  num_pages
- *     bounds page_id's values (checked only by a debug build).
+ *     head_dim) bytes; its contents need not be initialised.  num_pages is the
+ *     number of pages of k_pages / v_pages (it sizes the tensor maps); the
+ *     kernels do not check page_id's values or node_page_off against it:
+ *     deft_check_pages checks a layout on the host, once per change.
  *   head_dim in {64, 128}; page_size 16; num_q_heads a multiple of
  *     num_kv_heads whose quotient equals the plan's gqa_group (else
  *     DEFT_ESTATE); scale > 0 multiplies q.k (pass 1/sqrt(head_dim)).
@@ -256,30 +278,79 @@ int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
                     void *stream);
 
 /*
+ * deft_tree_attn_ex -- deft_tree_attn / deft_naive_attn with option flags
+ * (DEFT_STEP_*; 0 = deft_tree_attn).  DEFT_STEP_CUDA_CORES runs the
+ * tensor-core chunks on the CUDA-core kernel (head_dim 128 only needs it to
+ * compare the two paths; a GQA group above 16 returns DEFT_EUNSUPPORTED),
+ * DEFT_STEP_SEPARATE_MERGE sends every query, single-chunk ones included,
+ * through the partials and the merge launch.  Results equal those without
+ * flags within the tolerances of floating point (SEPARATE_MERGE gives the
+ * same values: a single partial merges to itself).  Unknown flag bits: DEFT_EINVAL.  Other arguments and errors as
+ * deft_tree_attn.
+ */
+int deft_tree_attn_ex(const void *q, const void *k_pages, const void *v_pages,
+                      const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                      float scale, const deft_plan_t *plan, void *out, int32_t out_dtype, float *lse,
+                      void *workspace, size_t workspace_bytes, int32_t flags, void *stream);
+
+/*
+ * deft_step_status -- device-side failures of earlier steps of this plan (no
+ * counterpart on the pages).  Every wait of a kernel on another part of its
+ * CTA is bounded; one that runs out writes NaN into the rows of its launch
+ * and records a code in the plan's device memory.  This call copies the
+ * codes of both partitions back on `stream`, waits for that copy (it
+ * synchronises the host with the stream) and clears them.  *code = 0 and
+ * DEFT_OK when no step failed; otherwise *code = the first failing wait's
+ * code and DEFT_EDEVICE: out / lse of the failed steps are not valid.
+ * Steps of deft_tree_attn_noalloc are not covered (see there).
+ * DEFT_ESTATE if the plan was never uploaded, DEFT_ECUDA if a copy fails.
+ */
+int deft_step_status(deft_plan_t *plan, void *stream, int32_t *code);
+
+/*
+ * deft_check_pages -- host check of a paged KV layout (DeFT Guide,
+ * "Production Engineering", paged KV-cache compatibility): for every node
+ * with tokens, its ceil(node_len / page_size) page-table entries
+ * node_page_off[n] .. lie inside page_id[0 .. num_page_ids) and each names a
+ * page in [0, num_pages).  All arrays are host memory (node_len and
+ * node_page_off have num_nodes entries at least).  DEFT_OK, DEFT_ERANGE at
+ * the first violation, DEFT_EINVAL on bad arguments.  The kernels read
+ * page_id without checking it: run this once whenever the layout changes.
+ */
+int deft_check_pages(const int32_t *node_len, int32_t num_nodes, const int32_t *node_page_off,
+                     const int32_t *page_id, int64_t num_page_ids, int32_t num_pages, int32_t page_size);
+
+/*
  * deft_tree_attn_noalloc -- deft_tree_attn for callers that cannot allocate
  * device memory.  The paper has no counterpart; this is a library service.
  *
  * deft_tree_attn needs a workspace and an uploaded plan, and uploading calls
- * cudaMalloc.  Some callers cannot do either: code running while a CUDA
- * graph is captured (cudaMalloc is not allowed there), frameworks whose
- * device memory belongs to a pool allocator that must not be bypassed, and
- * latency-critical loops that cannot pay for an allocation or its implicit
- * synchronisation.  This call takes the same inputs and outputs as
- * deft_tree_attn but no workspace, and the plan need not be uploaded: the
- * plan's tree arrays are copied from its host memory on `stream`, and the
- * partials are kept, in one static device array of
- * DEFT_NOALLOC_SCRATCH_BYTES (64 MiB) that every GPU loading the library
- * holds until the process exits.  It calls no cudaMalloc, cudaFree or other
- * allocating routine.
+ * cudaMalloc.  Some callers may not do either: a runtime that reserves all
+ * device memory for its own pool allocator and gives its kernels no way to
+ * take more (a cudaMalloc there fails, or takes memory the pool counts on),
+ * a plugin interface that hands the plugin its buffers and forbids it to
+ * allocate during execution, and a serving loop that cannot afford the
+ * device-wide synchronisation a cudaMalloc or cudaFree may cause.  This call
+ * takes the same inputs and outputs as deft_tree_attn but no workspace, and
+ * the plan need not be uploaded: the plan's tree arrays are copied, with one
+ * cudaMemcpyAsync on `stream` from a host image the plan keeps (pageable
+ * memory: CUDA returns from that copy once it has staged the bytes), into
+ * one static device array of DEFT_NOALLOC_SCRATCH_BYTES (64 MiB) that every
+ * GPU loading the library holds until the process exits; the partials live
+ * there too.  It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - A plan whose arrays plus partials (slots * num_q_heads * (head_dim + 1)
- *     fp32 values, 256-byte aligned pieces) exceed the array is rejected with
- *     DEFT_EWORKSPACE before anything is enqueued.
+ *     fp32 values), in 256-byte aligned pieces, exceed the array is rejected
+ *     with DEFT_EWORKSPACE before anything is enqueued.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
- *   - All calls share the array and it keeps the last call's contents;
- *     nothing in it has to start at zero.  Calls that may overlap on the GPU
- *     (other streams, unsynchronised host threads) race and must not be made.
+ *     (cudaGetSymbolAddress) with that device current.
+ *   - All calls share the array and it keeps the last call's contents: each
+ *     call rewrites the plan arrays (work queues included) before its
+ *     kernels run, and nothing else in it has to start at zero.  Calls that
+ *     may overlap on the GPU (other streams, unsynchronised host threads)
+ *     race and must not be made.
+ *   - A failed wait inside a kernel shows only as NaN in out / lse (the
+ *     status words live in the array; deft_step_status does not see them).
  * Results are those of deft_tree_attn; other arguments and errors as there.
  */
 #define DEFT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)

@@ -33,17 +33,23 @@ ARRAYS = {
     "naive_chunk_seg_off": (15, np.int32), "naive_chunk_q": (16, np.int32),
     "naive_seg_node": (17, np.int32), "naive_seg_tok_begin": (18, np.int32),
     "naive_seg_tok_len": (19, np.int32), "naive_q_slot_off": (20, np.int32),
-    "naive_q_slot": (21, np.int32),
+    "naive_q_slot": (21, np.int32), "fma_direct": (22, np.uint32),
+    "fallback_direct": (23, np.uint32), "merge_q": (24, np.int32),
 }
 
 # Symbols the header declares (checked by the tests).
 EXPORTS = ["deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_rebuild", "deft_plan_stats_get",
            "deft_plan_get", "deft_plan_upload", "deft_workspace_bytes", "deft_tree_attn",
-           "deft_naive_attn", "deft_plan_free", "deft_status_str", "deft_version", "deft_trace_enable",
+           "deft_naive_attn", "deft_tree_attn_ex", "deft_step_status", "deft_check_pages",
+           "deft_plan_free", "deft_status_str", "deft_version", "deft_trace_enable",
            "deft_trace_read", "deft_tree_attn_noalloc"]
 
 KERNEL_NAMES = {0: "phase1_fma", 1: "phase1_mma", 2: "phase2_merge"}
 PLAN_TREE_ONLY = 1   # deft_plan_ex flag
+# deft_tree_attn_ex flags
+STEP_NAIVE = 1
+STEP_CUDA_CORES = 2
+STEP_SEPARATE_MERGE = 4
 
 
 class DeftError(RuntimeError):
@@ -63,7 +69,7 @@ class PlanStats(ctypes.Structure):
         "num_nodes", "num_queries", "gqa_group", "chunk_target", "mask_words", "num_chunks",
         "num_segments", "num_slots", "num_fma_items", "num_mma_items", "num_fallback_items",
         "max_chunk_tokens", "max_slots_per_query", "naive_num_chunks", "naive_num_slots",
-        "naive_num_segments")] + [(n, ctypes.c_int64) for n in (
+        "naive_num_segments", "num_merge_queries", "reserved0")] + [(n, ctypes.c_int64) for n in (
         "unique_tokens", "naive_tokens", "planned_tokens", "pair_tokens", "device_bytes")]
 
     def as_dict(self):
@@ -95,6 +101,9 @@ def load(path: str = LIB_PATH):
     attn = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P, i32, P, P, sz, P]
     lib.deft_tree_attn.argtypes = attn
     lib.deft_naive_attn.argtypes = attn
+    lib.deft_tree_attn_ex.argtypes = attn[:-1] + [i32, P]
+    lib.deft_step_status.argtypes = [P, P, ctypes.POINTER(i32)]
+    lib.deft_check_pages.argtypes = [P, i32, P, P, ctypes.c_int64, i32, i32]
     lib.deft_tree_attn_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P,
                                            i32, P, P]
     lib.deft_plan_free.argtypes = [P]
@@ -106,7 +115,8 @@ def load(path: str = LIB_PATH):
     lib.deft_trace_read.argtypes = [ctypes.POINTER(TraceRecord), i32, ctypes.POINTER(i32)]
     for fn in ("deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_rebuild", "deft_plan_stats_get",
                "deft_plan_get", "deft_plan_upload", "deft_tree_attn", "deft_naive_attn", "deft_version",
-               "deft_trace_enable", "deft_trace_read", "deft_tree_attn_noalloc"):
+               "deft_trace_enable", "deft_trace_read", "deft_tree_attn_noalloc", "deft_tree_attn_ex",
+               "deft_step_status", "deft_check_pages"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -196,6 +206,8 @@ class Plan:
             "naive_seg_tok_begin": s["naive_num_segments"],
             "naive_seg_tok_len": s["naive_num_segments"],
             "naive_q_slot_off": s["num_queries"] + 1, "naive_q_slot": s["naive_num_slots"],
+            "fma_direct": s["num_fma_items"], "fallback_direct": s["num_fallback_items"],
+            "merge_q": s["num_merge_queries"],
         }
         return counts[name]
 
@@ -211,6 +223,15 @@ class Plan:
 
     def workspace_bytes(self, num_q_heads: int, head_dim: int) -> int:
         return int(load().deft_workspace_bytes(self.handle, int(num_q_heads), int(head_dim)))
+
+    def step_status(self, stream=None) -> int:
+        """deft_step_status: 0, or the code of a kernel wait that ran out in an
+        earlier step (the codes are cleared by the call)."""
+        code = ctypes.c_int32()
+        rc = load().deft_step_status(self.handle, _stream(stream), ctypes.byref(code))
+        if rc not in (0, -9):
+            _check("deft_step_status", rc)
+        return int(code.value)
 
 
 def _stream(stream):
@@ -242,7 +263,7 @@ def alloc_buffers(plan: Plan, num_queries: int, num_q_heads: int, head_dim: int,
 
 def _attn(fn_name: str, q, k_pages, v_pages, node_page_off, page_id, plan: Plan,
           bufs: Optional[StepBuffers] = None, scale: Optional[float] = None,
-          out_dtype: int = DEFT_OUT_BF16, stream=None):
+          out_dtype: int = DEFT_OUT_BF16, stream=None, flags: int = 0):
     import torch
     lib = load()
     Q, Hq, d = q.shape
@@ -257,21 +278,23 @@ def _attn(fn_name: str, q, k_pages, v_pages, node_page_off, page_id, plan: Plan,
             raise ValueError("node_page_off and page_id must be contiguous int32 CUDA tensors")
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     odt = DEFT_OUT_BF16 if bufs.out.dtype == torch.bfloat16 else DEFT_OUT_F32
-    rc = getattr(lib, fn_name)(
-        q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), node_page_off.data_ptr(),
-        page_id.data_ptr(), int(k_pages.shape[0]), int(Hq), int(Hkv), int(d),
-        int(P), float(scale), plan.handle, bufs.out.data_ptr(), odt,
-        bufs.lse.data_ptr(), bufs.workspace.data_ptr(),
-        int(bufs.workspace.numel()), _stream(stream))
+    args = [q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), node_page_off.data_ptr(),
+            page_id.data_ptr(), int(k_pages.shape[0]), int(Hq), int(Hkv), int(d),
+            int(P), float(scale), plan.handle, bufs.out.data_ptr(), odt,
+            bufs.lse.data_ptr(), bufs.workspace.data_ptr(), int(bufs.workspace.numel())]
+    if fn_name == "deft_tree_attn_ex":
+        args.append(int(flags))
+    rc = getattr(lib, fn_name)(*args, _stream(stream))
     _check(fn_name, rc)
     return bufs.out, bufs.lse
 
 
 def deft_tree_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs=None,
-                   scale=None, out_dtype=DEFT_OUT_BF16, stream=None):
-    """One DeFT tree-attention step; returns (out, lse) device tensors."""
-    return _attn("deft_tree_attn", q, k_pages, v_pages, node_page_off, page_id, plan, bufs,
-                 scale, out_dtype, stream)
+                   scale=None, out_dtype=DEFT_OUT_BF16, stream=None, flags: int = 0):
+    """One DeFT tree-attention step; returns (out, lse) device tensors.
+    flags (STEP_*): deft_tree_attn_ex's options; 0 calls deft_tree_attn."""
+    return _attn("deft_tree_attn_ex" if flags else "deft_tree_attn", q, k_pages, v_pages,
+                 node_page_off, page_id, plan, bufs, scale, out_dtype, stream, flags)
 
 
 def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs=None,
@@ -284,6 +307,14 @@ def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, buf
 def deft_plan(parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
               query_pos=None, naive: bool = True) -> Plan:
     return Plan(parent, node_len, query_node, chunk_target, gqa_group, query_pos, naive)
+
+
+def deft_check_pages(node_len, node_page_off, page_id, num_pages: int, page_size: int = 16) -> int:
+    """deft_check_pages on host arrays: 0 (DEFT_OK) or the status code."""
+    ln, npo, pid = _i32(node_len), _i32(node_page_off), _i32(page_id)
+    return int(load().deft_check_pages(_ptr(ln), int(ln.shape[0]), _ptr(npo),
+                                       _ptr(pid) if pid.size else None, int(pid.size),
+                                       int(num_pages), int(page_size)))
 
 
 def trace_enable(on: bool = True):

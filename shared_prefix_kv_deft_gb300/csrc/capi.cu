@@ -2,9 +2,9 @@
 //
 // Plan calls are host-only; deft_plan_upload copies the plan's arrays into
 // one device allocation owned by the plan; deft_tree_attn / deft_naive_attn
-// validate their arguments and enqueue phase 1 (tensor-core and CUDA-core
-// kernels) and phase 2 on the caller's stream without allocating or
-// synchronising.
+// / deft_tree_attn_ex validate their arguments and enqueue phase 1
+// (tensor-core and CUDA-core kernels, merging in phase 1) or phase 1 and the
+// phase-2 merge on the caller's stream without allocating or synchronising.
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
@@ -15,11 +15,6 @@
 #include <cuda_runtime.h>
 
 #include "deft_internal.h"
-#include "kprof.cuh"
-
-#ifdef DEFT_KPROF
-unsigned long long *g_kprof_buf = nullptr;
-#endif
 
 namespace deft {
 
@@ -37,11 +32,71 @@ int num_sms()
     return n;
 }
 
+WorkLayout work_layout(int64_t slots, int32_t num_q_heads, int32_t head_dim)
+{
+    auto up = [](size_t x) { return (x + kWorkAlign - 1) / kWorkAlign * kWorkAlign; };
+    WorkLayout w{};
+    w.o_off = 0;
+    w.lse_off = up((size_t)slots * num_q_heads * head_dim * sizeof(float));
+    w.total = w.lse_off + up((size_t)slots * num_q_heads * sizeof(float));
+    return w;
+}
+
+int prepare_step(const void *q, const void *k_pages, const void *v_pages, const int32_t *node_page_off,
+                 const int32_t *page_id, int32_t num_pages, int32_t num_q_heads, int32_t num_kv_heads,
+                 int32_t head_dim, int32_t page_size, float scale, const deft_plan_t *plan, void *out,
+                 int32_t out_dtype, float *lse, int32_t flags, AttnArgs &a, bool &use_mma)
+{
+    if (!plan || !q || !k_pages || !v_pages || !node_page_off || !page_id || !out || !lse)
+        return DEFT_EINVAL;
+    if (flags & ~(int32_t)(DEFT_STEP_NAIVE | DEFT_STEP_CUDA_CORES | DEFT_STEP_SEPARATE_MERGE))
+        return DEFT_EINVAL;
+    if (out_dtype != DEFT_OUT_BF16 && out_dtype != DEFT_OUT_F32)
+        return DEFT_EINVAL;
+    if (!(scale > 0.f) || !std::isfinite(scale) || num_pages < 1)
+        return DEFT_EINVAL;
+    if (num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
+        return DEFT_EINVAL;
+    if (((uintptr_t)q | (uintptr_t)k_pages | (uintptr_t)v_pages) & 15u)
+        return DEFT_EINVAL;   // the kernels copy q and KV rows in 16-byte pieces
+    if ((head_dim != 64 && head_dim != 128) || page_size != kPageSize)
+        return DEFT_EUNSUPPORTED;
+    const bool naive = (flags & DEFT_STEP_NAIVE) != 0;
+    if (num_q_heads / num_kv_heads != plan->gqa_group || (naive && !plan->has_naive))
+        return DEFT_ESTATE;
+    use_mma = mma_supported(head_dim) && !(flags & DEFT_STEP_CUDA_CORES);
+    // The CUDA-core kernel holds at most kFmaMaxRows rows per item; one query
+    // of a larger GQA group needs the tensor-core path.
+    if (plan->gqa_group > kFmaMaxRows && !use_mma)
+        return DEFT_EUNSUPPORTED;
+    a = AttnArgs{};
+    a.q = q;
+    a.k_pages = k_pages;
+    a.v_pages = v_pages;
+    a.node_page_off = node_page_off;
+    a.page_id = page_id;
+    a.num_pages = num_pages;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_dim = head_dim;
+    a.gqa_group = plan->gqa_group;
+    a.scale_log2 = scale * 1.44269504088896340736f;
+    a.wait_prior = 1;
+    a.kv_once = naive ? 0 : 1;
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.lse_out = lse;
+    // Rows of single-chunk queries go to out / lse from phase 1 unless every
+    // query is to be merged by the merge launch.
+    a.direct = (flags & DEFT_STEP_SEPARATE_MERGE) ? 0 : 1;
+    return DEFT_OK;
+}
+
 }  // namespace deft
 
 namespace {
 
-constexpr size_t kAlign = 256;
+constexpr size_t kAlign = deft::kWorkAlign;
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
@@ -83,13 +138,6 @@ void fill_partition(const deft::Partition &p, const Layout &L, uint8_t *host, ui
     deft::bind_partition(p, dev, L.off, L.end, num_nodes, num_queries, mask_words, d);
 }
 
-size_t partial_bytes(int64_t slots, int32_t num_q_heads, int32_t head_dim)
-{
-    const size_t o = align_up((size_t)slots * num_q_heads * head_dim * sizeof(float));
-    const size_t l = align_up((size_t)slots * num_q_heads * sizeof(float));
-    return o + l;
-}
-
 // ---- launch tracing (deft_trace_enable / deft_trace_read) ----
 struct TraceEntry {
     deft_trace_record rec;
@@ -129,37 +177,25 @@ int traced(const deft_trace_record &rec, void *stream, F &&launch)
     return rc;
 }
 
-bool env_flag(const char *name)
-{
-    const char *v = std::getenv(name);
-    return v && v[0] && v[0] != '0';
-}
-
 int run_step(const void *q, const void *k_pages, const void *v_pages, const int32_t *node_page_off,
              const int32_t *page_id, int32_t num_pages, int32_t num_q_heads, int32_t num_kv_heads,
              int32_t head_dim, int32_t page_size, float scale, const deft_plan_t *plan, void *out,
-             int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes, void *stream,
-             bool naive)
+             int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes, int32_t flags, void *stream)
 {
-    if (!plan || !q || !k_pages || !v_pages || !node_page_off || !page_id || !out || !lse)
-        return DEFT_EINVAL;
-    if (out_dtype != DEFT_OUT_BF16 && out_dtype != DEFT_OUT_F32)
-        return DEFT_EINVAL;
-    if (!(scale > 0.f) || !std::isfinite(scale) || num_pages < 1)
-        return DEFT_EINVAL;
-    if (num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
-        return DEFT_EINVAL;
-    if (((uintptr_t)q | (uintptr_t)k_pages | (uintptr_t)v_pages) & 15u)
-        return DEFT_EINVAL;   // the kernels copy q and KV rows in 16-byte pieces
-    if ((head_dim != 64 && head_dim != 128) || page_size != deft::kPageSize)
-        return DEFT_EUNSUPPORTED;
-    if (num_q_heads / num_kv_heads != plan->gqa_group || !plan->uploaded || (naive && !plan->has_naive))
+    deft::AttnArgs a;
+    bool use_mma = false;
+    int rc = deft::prepare_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads, num_kv_heads,
+                                head_dim, page_size, scale, plan, out, out_dtype, lse, flags, a, use_mma);
+    if (rc != DEFT_OK)
+        return rc;
+    if (!plan->uploaded)
         return DEFT_ESTATE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return DEFT_ECUDA;
     if (dev != plan->dev_device)
         return DEFT_ESTATE;
+    const bool naive = (flags & DEFT_STEP_NAIVE) != 0;
     const deft::Partition &hp = naive ? plan->naive : plan->tree;
     const deft::DevPartition &dp = naive ? plan->dev_naive : plan->dev_tree;
     const size_t need = deft_workspace_bytes(plan, num_q_heads, head_dim);
@@ -167,45 +203,15 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
         return DEFT_EWORKSPACE;
     if (plan->num_queries == 0)
         return DEFT_OK;
-
-    deft::AttnArgs a{};
-    a.q = q;
-    a.k_pages = k_pages;
-    a.v_pages = v_pages;
-    a.node_page_off = node_page_off;
-    a.page_id = page_id;
-    a.num_pages = num_pages;
-    a.num_q_heads = num_q_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.head_dim = head_dim;
-    a.gqa_group = plan->gqa_group;
-    a.scale_log2 = scale * 1.44269504088896340736f;
-    a.wait_prior = 1;
-    a.kv_once = naive ? 0 : 1;
-#ifdef DEFT_KPROF
-    if (!g_kprof_buf) {
-        if (cudaMalloc(&g_kprof_buf, deft::kKprofSlots * sizeof(unsigned long long)) != cudaSuccess)
-            g_kprof_buf = nullptr;
-        else
-            cudaMemset(g_kprof_buf, 0, deft::kKprofSlots * sizeof(unsigned long long));
-    }
-    a.kprof = g_kprof_buf;
-#endif
-    const size_t slots = (size_t)std::max(plan->tree.num_slots(), plan->naive.num_slots());
-    a.o_part = reinterpret_cast<float *>(workspace);
-    a.lse_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) +
-                                           align_up(slots * num_q_heads * head_dim * sizeof(float)));
-
-    const bool use_mma = deft::mma_supported(head_dim) && !env_flag("DEFT_DISABLE_MMA");
-    // The CUDA-core kernel holds at most kFmaMaxRows rows per item; one query
-    // of a larger GQA group needs the tensor-core path.
-    if (plan->gqa_group > deft::kFmaMaxRows && !use_mma)
-        return DEFT_EUNSUPPORTED;
+    const int64_t slots = std::max(plan->tree.num_slots(), plan->naive.num_slots());
+    const deft::WorkLayout wl = deft::work_layout(slots > 0 ? slots : 1, num_q_heads, head_dim);
+    uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+    a.o_part = reinterpret_cast<float *>(ws + wl.o_off);
+    a.lse_part = reinterpret_cast<float *>(ws + wl.lse_off);
     const deft::LaunchTracer trace = [](const deft_trace_record &rec, void *st, const std::function<int()> &launch) {
         return traced(rec, st, launch);
     };
-    return deft::dispatch_step(a, dp, hp, use_mma, naive ? 1 : 0, out, out_dtype, lse, stream, trace) ? DEFT_ECUDA
-                                                                                                       : DEFT_OK;
+    return deft::dispatch_step(a, dp, hp, use_mma, naive ? 1 : 0, stream, trace) ? DEFT_ECUDA : DEFT_OK;
 }
 
 }  // namespace
@@ -284,6 +290,7 @@ int deft_plan_rebuild(deft_plan_t *plan, const int32_t *parent, const int32_t *n
     plan->has_naive = fresh.has_naive;
     plan->stats = fresh.stats;
     plan->uploaded = false;
+    plan->noalloc_image_ok = false;
     return DEFT_OK;
 }
 
@@ -340,6 +347,9 @@ int deft_plan_get(const deft_plan_t *plan, int32_t which, void *dst, size_t byte
     case DEFT_A_NAIVE_SEG_TOK_LEN: return cp(n.seg_tok_len);
     case DEFT_A_NAIVE_Q_SLOT_OFF: return cp(n.q_slot_off);
     case DEFT_A_NAIVE_Q_SLOT: return cp(n.q_slot);
+    case DEFT_A_FMA_DIRECT: return cp(t.fma_direct);
+    case DEFT_A_FALLBACK_DIRECT: return cp(t.fallback_direct);
+    case DEFT_A_MERGE_Q: return cp(t.merge_q);
     default: return DEFT_EINVAL;
     }
 }
@@ -416,7 +426,7 @@ size_t deft_workspace_bytes(const deft_plan_t *plan, int32_t num_q_heads, int32_
     if (!plan || num_q_heads < 1 || head_dim < 1)
         return 0;
     const int64_t slots = std::max(plan->tree.num_slots(), plan->naive.num_slots());
-    return partial_bytes(slots > 0 ? slots : 1, num_q_heads, head_dim);
+    return deft::work_layout(slots > 0 ? slots : 1, num_q_heads, head_dim).total;
 }
 
 int deft_tree_attn(const void *q, const void *k_pages, const void *v_pages,
@@ -427,7 +437,7 @@ int deft_tree_attn(const void *q, const void *k_pages, const void *v_pages,
 {
     return run_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads,
                     num_kv_heads, head_dim, page_size, scale, plan, out, out_dtype, lse, workspace,
-                    workspace_bytes, stream, false);
+                    workspace_bytes, 0, stream);
 }
 
 int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
@@ -438,7 +448,60 @@ int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,
 {
     return run_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads,
                     num_kv_heads, head_dim, page_size, scale, plan, out, out_dtype, lse, workspace,
-                    workspace_bytes, stream, true);
+                    workspace_bytes, DEFT_STEP_NAIVE, stream);
+}
+
+int deft_tree_attn_ex(const void *q, const void *k_pages, const void *v_pages,
+                      const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
+                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                      float scale, const deft_plan_t *plan, void *out, int32_t out_dtype, float *lse,
+                      void *workspace, size_t workspace_bytes, int32_t flags, void *stream)
+{
+    return run_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads,
+                    num_kv_heads, head_dim, page_size, scale, plan, out, out_dtype, lse, workspace,
+                    workspace_bytes, flags, stream);
+}
+
+int deft_step_status(deft_plan_t *plan, void *stream, int32_t *code)
+{
+    if (!plan || !code)
+        return DEFT_EINVAL;
+    *code = 0;
+    if (!plan->uploaded)
+        return DEFT_ESTATE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint32_t words[2] = {0u, 0u};
+    if (cudaMemcpyAsync(&words[0], plan->dev_tree.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaMemcpyAsync(&words[1], plan->dev_naive.status, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return DEFT_ECUDA;
+    if ((words[0] && cudaMemsetAsync(plan->dev_tree.status, 0, 4, st) != cudaSuccess) ||
+        (words[1] && cudaMemsetAsync(plan->dev_naive.status, 0, 4, st) != cudaSuccess))
+        return DEFT_ECUDA;
+    *code = (int32_t)(words[0] ? words[0] : words[1]);
+    return *code ? DEFT_EDEVICE : DEFT_OK;
+}
+
+int deft_check_pages(const int32_t *node_len, int32_t num_nodes, const int32_t *node_page_off,
+                     const int32_t *page_id, int64_t num_page_ids, int32_t num_pages, int32_t page_size)
+{
+    if (!node_len || !node_page_off || num_nodes < 1 || num_page_ids < 0 || num_pages < 1 || page_size < 1 ||
+        (num_page_ids > 0 && !page_id))
+        return DEFT_EINVAL;
+    for (int32_t n = 0; n < num_nodes; ++n) {
+        if (node_len[n] < 0)
+            return DEFT_EINVAL;
+        if (node_len[n] == 0)
+            continue;
+        const int64_t first = node_page_off[n];
+        const int64_t pages = ((int64_t)node_len[n] + page_size - 1) / page_size;
+        if (first < 0 || first + pages > num_page_ids)
+            return DEFT_ERANGE;
+        for (int64_t i = first; i < first + pages; ++i)
+            if (page_id[i] < 0 || page_id[i] >= num_pages)
+                return DEFT_ERANGE;
+    }
+    return DEFT_OK;
 }
 
 void deft_plan_free(deft_plan_t *plan)
@@ -468,25 +531,12 @@ const char *deft_status_str(int status)
     case DEFT_ECUDA: return "CUDA runtime or launch error";
     case DEFT_EWORKSPACE: return "workspace missing, too small or misaligned";
     case DEFT_ESTATE: return "plan not uploaded on this device, built for another GQA group, or without the naive partition";
+    case DEFT_EDEVICE: return "a kernel of an earlier step reported a failed wait (see deft_step_status)";
     default: return "unknown status";
     }
 }
 
-int deft_version(void) { return 100; }
-
-#ifdef DEFT_KPROF
-// Development builds only: copy the kernel timestamp slots to the host.
-int deft_kprof_read(unsigned long long *dst, size_t n)
-{
-    if (!g_kprof_buf)
-        return DEFT_ESTATE;
-    if (n > (size_t)deft::kKprofSlots)
-        n = deft::kKprofSlots;
-    return cudaMemcpy(dst, g_kprof_buf, n * sizeof(unsigned long long), cudaMemcpyDeviceToHost) == cudaSuccess
-               ? DEFT_OK
-               : DEFT_ECUDA;
-}
-#endif
+int deft_version(void) { return 200; }
 
 int deft_trace_enable(int32_t on)
 {

@@ -32,6 +32,8 @@ constexpr int kSharedTokensPerRow = 16;  // long-chunk rule for shared nodes (se
 // Work-queue slots: tensor-core buckets 0-3, CUDA-core buckets 4-8, the
 // CUDA-core fallback for tensor-core chunks 9-13.
 constexpr int kQueueSlots = 14;
+constexpr int kStatusWord = 2 * kQueueSlots;
+constexpr int kQueueWords = 2 * kQueueSlots + 2;
 inline int queue_slot(int family, int bucket) { return family == 0 ? bucket : family == 1 ? 4 + bucket : 9 + bucket; }
 
 // One partition, host side.  Items are (chunk, q_begin, q_end) triples where
@@ -69,10 +71,20 @@ struct Partition {
     // mma_half_cols(rows).
     std::vector<uint32_t> fma_rmask, fallback_rmask, mma_rmask;
     std::vector<int32_t> fma_rmask_off, fallback_rmask_off, mma_rmask_off;   // [n+1]
+    // Rows of each CUDA-core item whose query has this one partial slot
+    // (its whole path lies in the item's chunk): phase 1 writes them to out /
+    // lse directly.  Bit r = item row r.
+    std::vector<uint32_t> fma_direct, fallback_direct;
+    // Queries the merge launch handles: all but those direct rows belong to
+    // (queries with no slot, an empty path, get out = 0 and lse = -inf).
+    std::vector<int32_t> merge_q;
     // Work queues of the phase-1 launches (two words each: next unit, CTAs
     // finished), zero between launches: uploaded as zeros, reset by each
-    // launch's last CTA.  Slot of a launch: queue_slot().
-    std::vector<uint32_t> queue_words = std::vector<uint32_t>(2 * kQueueSlots, 0u);
+    // launch's last CTA.  Slot of a launch: queue_slot().  Then the status
+    // word (kStatusWord): 0, or the code of the first bounded wait of a
+    // kernel of this partition that ran out (read and cleared by
+    // deft_step_status), and one word of padding.
+    std::vector<uint32_t> queue_words = std::vector<uint32_t>(kQueueWords, 0u);
     // mma_items are sorted by column bucket b: each of the two softmax
     // warpgroups of an item holds NPH = 16 (b + 1) query rows; bucket b is
     // items [off[b], off[b+1]).
@@ -110,12 +122,17 @@ struct DevPartition {
     const int32_t *fallback_rmask_off;
     const uint32_t *mma_rmask;          // uint4 per (item, segment)
     const int32_t *mma_rmask_off;       // in uint4 units
+    const uint32_t *fma_direct;         // [num_fma_items]
+    const uint32_t *fallback_direct;    // [num_fallback_items]
+    const int32_t *merge_q;             // [num_merge_q]
     uint32_t *queues;                   // [kQueueSlots][2]
+    uint32_t *status;                   // the partition's status word (queues + kStatusWord)
     int32_t num_fma_items;
     int32_t num_mma_items;
     int32_t num_fallback_items;
     int32_t num_slots;
     int32_t num_queries;
+    int32_t num_merge_q;
     int32_t mask_words;
     int32_t num_nodes;
     // All of the partition's arrays lie in [arrays, arrays + array_bytes)
@@ -127,7 +144,7 @@ struct DevPartition {
 // The partition's device arrays in blob order, and how a blob placed at
 // `base` with offsets `off` binds to a DevPartition (shared by the uploaded
 // plan and the allocation-free entry point).
-constexpr int kPartArrays = 23;
+constexpr int kPartArrays = 26;
 struct ArrayRef {
     const void *ptr;
     size_t bytes;
@@ -141,7 +158,8 @@ inline std::array<ArrayRef, kPartArrays> partition_arrays(const Partition &p)
              aref(p.seg_mask), aref(p.q_slot_off), aref(p.q_slot), aref(p.fma_items), aref(p.mma_items),
              aref(p.fallback_items), aref(p.seg_lmask_off), aref(p.seg_lmask), aref(p.fma_rmask),
              aref(p.fma_rmask_off), aref(p.fallback_rmask), aref(p.fallback_rmask_off), aref(p.mma_rmask),
-             aref(p.mma_rmask_off), aref(p.queue_words)}};
+             aref(p.mma_rmask_off), aref(p.queue_words), aref(p.fma_direct), aref(p.fallback_direct),
+             aref(p.merge_q)}};
 }
 inline void bind_partition(const Partition &p, const uint8_t *base, const size_t *off, size_t end,
                            int32_t num_nodes, int32_t num_queries, int32_t mask_words, DevPartition &d)
@@ -171,6 +189,11 @@ inline void bind_partition(const Partition &p, const uint8_t *base, const size_t
     d.mma_rmask = u32(20);
     d.mma_rmask_off = i32(21);
     d.queues = reinterpret_cast<uint32_t *>(const_cast<uint8_t *>(base) + off[22]);
+    d.status = d.queues + kStatusWord;
+    d.fma_direct = u32(23);
+    d.fallback_direct = u32(24);
+    d.merge_q = i32(25);
+    d.num_merge_q = (int32_t)p.merge_q.size();
     d.num_fma_items = (int32_t)(p.fma_items.size() / 3);
     d.num_mma_items = (int32_t)(p.mma_items.size() / 3);
     d.num_fallback_items = (int32_t)(p.fallback_items.size() / 3);
@@ -210,6 +233,11 @@ struct deft_plan_t {
     size_t host_stage_bytes = 0;
     void *stage_done = nullptr;
     int stage_device = -1;
+    // Host image of the tree partition's device arrays for
+    // deft_tree_attn_noalloc (built on its first call after a plan build;
+    // the capacity is kept across rebuilds).
+    std::vector<uint8_t> noalloc_image;
+    bool noalloc_image_ok = false;
 };
 
 namespace deft {
@@ -218,6 +246,15 @@ namespace deft {
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
                int32_t chunk_target, int32_t gqa_group, bool with_naive, deft_plan_t *plan);
+
+// Workspace of a step (caller memory, or the allocation-free entry point's
+// static array): fp32 partial outputs [slots][Hq][d], then fp32 partial lse
+// [slots][Hq], each piece kWorkAlign-aligned.
+constexpr size_t kWorkAlign = 256;
+struct WorkLayout {
+    size_t o_off, lse_off, total;
+};
+WorkLayout work_layout(int64_t slots, int32_t num_q_heads, int32_t head_dim);
 
 // Arguments every phase-1 kernel receives.
 struct AttnArgs {
@@ -234,7 +271,14 @@ struct AttnArgs {
     float scale_log2;         // scale * log2(e): logits are kept in base 2 on device
     float *o_part;            // fp32 [slots][Hq][d]
     float *lse_part;          // fp32 [slots][Hq], base-2 log-sum-exp of the base-2 logits
-    unsigned long long *kprof;  // timestamp slots (development builds only; else null)
+    void *out;                // [Q][Hq][d] bf16 or fp32 (out_dtype)
+    int32_t out_dtype;
+    float *lse_out;           // fp32 [Q][Hq], natural log
+    // 1: a CUDA-core row whose query has a single partial slot (the item's
+    // direct mask) is written to out / lse by phase 1 and the merge launch
+    // handles the partition's merge_q only; 0: every row goes to the
+    // partials and the merge launch handles every query.
+    int32_t direct;
     // 1 for the step's first launch: it waits for the stream's earlier work
     // before reading anything.  Every launch of a step is a programmatic
     // dependent of the one before (it may start while that one finishes);
@@ -247,6 +291,15 @@ struct AttnArgs {
     // in L2; 0 for the naive partition, whose prefix re-reads hit L2.
     int32_t kv_once;
 };
+
+// The argument checks shared by every step entry point (flags: DEFT_STEP_*).
+// On DEFT_OK, `a` holds everything but the workspace pointers (o_part,
+// lse_part) and use_mma says whether >= 16-row items run on the
+// tensor cores.  The plan's upload state is the caller's to check.
+int prepare_step(const void *q, const void *k_pages, const void *v_pages, const int32_t *node_page_off,
+                 const int32_t *page_id, int32_t num_pages, int32_t num_q_heads, int32_t num_kv_heads,
+                 int32_t head_dim, int32_t page_size, float scale, const deft_plan_t *plan, void *out,
+                 int32_t out_dtype, float *lse, int32_t flags, AttnArgs &a, bool &use_mma);
 
 // Launchers (return a cudaError_t cast to int; 0 = success).
 //
@@ -267,16 +320,18 @@ inline int32_t static_block(int32_t units, int32_t early)
 // One CUDA-core launch over `n` items (device triples at `items`), all of row
 // bucket `bucket` (rows <= 2^bucket).
 // `rmask` / `rmask_off`: the items' row masks (device; rmask_off indexed
-// like items); `queue`: the launch's work queue (two device words, zero).
+// like items); `direct`: the items' direct-row masks (indexed like items);
+// `queue`: the launch's work queue (two device words, zero).
 int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-                      const int32_t *rmask_off, int32_t n, int bucket, uint32_t *queue, LaunchShape shape,
-                      void *stream);
+                      const int32_t *rmask_off, const uint32_t *direct, int32_t n, int bucket, uint32_t *queue,
+                      LaunchShape shape, void *stream);
 // Streaming multiprocessors of the current device.
 int num_sms();
 // Shares `sms` SMs among n concurrent launches of estimated costs cost[i]
 // and units[i] units each (dispatch.cu).
 void shape_launches(const double *cost, const int32_t *units, int n, int sms, LaunchShape *out);
-// One tensor-core launch over `n` items of column bucket `bucket`.
+// One tensor-core launch over `n` items of column bucket `bucket` (its rows
+// all go to the partials).
 int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
                       const int32_t *rmask_off, int32_t n, int bucket, uint32_t *queue, LaunchShape shape,
                       void *stream);
@@ -284,18 +339,19 @@ int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *i
 // under `rec` when tracing is on.
 using LaunchTracer = std::function<int(const deft_trace_record &rec, void *stream, const std::function<int()> &launch)>;
 // Enqueues one step on `stream`: the phase-1 launches of partition dp and
-// the merge into out / lse.  `hp` is dp's host copy.  Returns a cudaError_t
-// as int.
+// the phase-2 merge into a.out / a.lse_out (of every query, or with
+// a.direct of the partition's merge_q, skipped when that is empty).  `hp` is
+// dp's host copy.  Returns a cudaError_t as int.
 int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool use_mma, int32_t family,
-                  void *out, int32_t out_dtype, float *lse, void *stream, const LaunchTracer &trace);
+                  void *stream, const LaunchTracer &trace);
 // Row bucket of an item with `rows` rows: smallest b with rows <= 2^b.
 inline int row_bucket(int rows) { return rows <= 1 ? 0 : rows <= 2 ? 1 : rows <= 4 ? 2 : rows <= 8 ? 3 : 4; }
 // Rows per softmax warpgroup of a tensor-core item with `rows` rows (two
 // warpgroups share the rows; each takes a multiple of 16, at most 64).
 inline int mma_half_cols(int rows) { return (((rows + 1) / 2) + 15) & ~15; }
 inline int mma_bucket(int rows) { return mma_half_cols(rows) / 16 - 1; }
-int launch_phase2(const AttnArgs &a, const DevPartition &p, void *out, int32_t out_dtype,
-                  float *lse, void *stream);
+// The merge launch over `nq` queries: queries[i], or i when queries is null.
+int launch_phase2(const AttnArgs &a, const DevPartition &p, const int32_t *queries, int32_t nq, void *stream);
 bool mma_supported(int32_t head_dim);
 
 }  // namespace deft

@@ -88,7 +88,7 @@ void shape_launches(const double *cost, const int32_t *units, int n, int sms, La
 }
 
 int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool use_mma, int32_t family,
-                  void *out, int32_t out_dtype, float *lse, void *stream, const LaunchTracer &trace)
+                  void *stream, const LaunchTracer &trace)
 {
     const int32_t hkv = a.num_kv_heads;
     Launch ls[14];
@@ -108,9 +108,9 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
                 ls[n++] = Launch{kind, b, off[b], c, (double)tok[b] * hkv * fma_ns_per_token(b)};
         }
     };
-    // The tensor-core path covers head_dim 128; other head sizes, or a run
-    // with DEFT_DISABLE_MMA set, take the same chunks on CUDA cores in items
-    // of at most 16 rows.
+    // The tensor-core path covers head_dim 128; other head sizes, or a step
+    // asked to run on CUDA cores only, take the same chunks on CUDA cores in
+    // items of at most 16 rows.
     if (dp.num_mma_items > 0 && !use_mma)
         add_fma(2, hp.fallback_bucket_off, hp.fallback_bucket_tok);
     if (dp.num_fma_items > 0)
@@ -149,17 +149,25 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
             const int32_t *it = (fb ? dp.fallback_items : dp.fma_items) + 3 * (size_t)l.off;
             const uint32_t *rm = fb ? dp.fallback_rmask : dp.fma_rmask;
             const int32_t *rmo = (fb ? dp.fallback_rmask_off : dp.fma_rmask_off) + l.off;
+            const uint32_t *dr = (fb ? dp.fallback_direct : dp.fma_direct) + l.off;
             uint32_t *queue = dp.queues + 2 * queue_slot(fb ? 2 : 1, l.bucket);
             r = trace({DEFT_K_PHASE1_FMA, family, l.bucket, fb ? 1 : 0, l.n, 0.f}, stream, [&] {
-                return launch_phase1_fma(a, dp, it, rm, rmo, l.n, l.bucket, queue, shape[i], stream);
+                return launch_phase1_fma(a, dp, it, rm, rmo, dr, l.n, l.bucket, queue, shape[i], stream);
             });
         }
         if (r)
             return r;
         a.wait_prior = 0;
     }
-    return trace({DEFT_K_PHASE2, family, 0, 0, dp.num_queries, 0.f}, stream,
-                 [&] { return launch_phase2(a, dp, out, out_dtype, lse, stream); });
+    // With direct rows, the merge launch takes the queries with several
+    // slots or none, and is left out when there are none.
+    const int32_t nq = a.direct ? dp.num_merge_q : dp.num_queries;
+    if (nq == 0)
+        return 0;
+    // Every query merged: no list to read.
+    const int32_t *qlist = nq < dp.num_queries ? dp.merge_q : nullptr;
+    return trace({DEFT_K_PHASE2, family, 0, 0, nq, 0.f}, stream,
+                 [&] { return launch_phase2(a, dp, qlist, nq, stream); });
 }
 
 }  // namespace deft

@@ -4,25 +4,27 @@
 // deft_tree_attn needs two pieces of device memory besides its inputs and
 // outputs: the plan's device copy (from deft_plan_upload, which calls
 // cudaMalloc) and a workspace for the phase-1 partial results.  Some callers
-// cannot provide either: code that must not call cudaMalloc while a CUDA
-// graph is being captured, runtimes whose memory is owned by a pool or
-// allocator they may not bypass, and latency-bound loops where an allocation
-// (or its implicit synchronisation) is not acceptable.  This entry point
-// serves them from one fixed, file-scope device array instead: the plan's
-// tree-partition arrays are copied into it from the plan's host memory on
-// the caller's stream, and the partials live after them.  It calls no
+// cannot provide either: a runtime that has reserved the device memory for
+// its own pool and gives kernels no way to take more, a plugin interface
+// that hands a plugin its buffers and forbids allocation while it executes,
+// a serving loop that cannot afford the device-wide synchronisation a
+// cudaMalloc or cudaFree may cause.  This entry point serves them from one
+// fixed, file-scope device array instead: the plan's tree-partition arrays
+// are copied into it from a host image the plan keeps (one cudaMemcpyAsync
+// on the caller's stream), and the partials live after them.  It calls no
 // cudaMalloc, cudaFree or other allocating routine.
 //
 // The array is kNoallocScratchBytes (64 MiB) and exists on every GPU that
 // loads the library, until the process exits.  All calls share it and it
-// keeps whatever the last call left there.  Nothing in it needs to start at
-// zero: every call rewrites the plan arrays, and phase 1 writes every
-// partial that phase 2 reads.  Calls that can overlap on the GPU (different
-// streams, or different host threads without ordering) race on the array.
+// keeps whatever the last call left there.  Each call rewrites the plan
+// arrays (the work queues among them start at zero) before its kernels run;
+// nothing else in it has to start at zero: phase 1 writes every partial that
+// the merge reads.  Calls that can overlap on the GPU (different streams, or
+// different host threads without ordering) race on the array.
 #include <atomic>
-#include <cmath>
 #include <cstdint>
-#include <cstdlib>
+#include <cstring>
+#include <new>
 
 #include <cuda_runtime.h>
 
@@ -31,7 +33,7 @@
 namespace {
 
 constexpr size_t kNoallocScratchBytes = DEFT_NOALLOC_SCRATCH_BYTES;
-constexpr size_t kAlign = 256;
+constexpr size_t kAlign = deft::kWorkAlign;
 constexpr int kMaxDevices = 64;
 
 }  // namespace
@@ -61,6 +63,18 @@ int scratch_address(int dev, unsigned char **out)
     return DEFT_OK;
 }
 
+// Offsets of the tree partition's arrays at the start of the scratch array;
+// returns the end of the last one.
+size_t array_offsets(const deft::Partition &p, size_t *off)
+{
+    const auto arrays = deft::partition_arrays(p);
+    size_t cursor = 0;
+    for (int i = 0; i < deft::kPartArrays; ++i) {
+        off[i] = cursor;
+        cursor = align_up(cursor + (arrays[i].bytes ? arrays[i].bytes : 4));
+    }
+    return cursor;
+}
 
 }  // namespace
 
@@ -71,79 +85,60 @@ extern "C" int deft_tree_attn_noalloc(const void *q, const void *k_pages, const 
                                       float scale, const deft_plan_t *plan, void *out,
                                       int32_t out_dtype, float *lse, void *stream)
 {
-    if (!plan || !q || !k_pages || !v_pages || !node_page_off || !page_id || !out || !lse)
-        return DEFT_EINVAL;
-    if (out_dtype != DEFT_OUT_BF16 && out_dtype != DEFT_OUT_F32)
-        return DEFT_EINVAL;
-    if (!(scale > 0.f) || !std::isfinite(scale) || num_pages < 1)
-        return DEFT_EINVAL;
-    if (num_kv_heads < 1 || num_q_heads < 1 || num_q_heads % num_kv_heads != 0)
-        return DEFT_EINVAL;
-    if (((uintptr_t)q | (uintptr_t)k_pages | (uintptr_t)v_pages) & 15u)
-        return DEFT_EINVAL;   // the kernels copy q and KV rows in 16-byte pieces
-    if ((head_dim != 64 && head_dim != 128) || page_size != deft::kPageSize)
-        return DEFT_EUNSUPPORTED;
-    if (num_q_heads / num_kv_heads != plan->gqa_group)
-        return DEFT_ESTATE;
-    const char *dis = std::getenv("DEFT_DISABLE_MMA");
-    const bool use_mma = deft::mma_supported(head_dim) && !(dis && dis[0] && dis[0] != '0');
-    if (plan->gqa_group > deft::kFmaMaxRows && !use_mma)
-        return DEFT_EUNSUPPORTED;
+    deft::AttnArgs a;
+    bool use_mma = false;
+    int rc = deft::prepare_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads, num_kv_heads,
+                                head_dim, page_size, scale, plan, out, out_dtype, lse, 0, a, use_mma);
+    if (rc != DEFT_OK)
+        return rc;
 
-    // Scratch layout: the tree partition's arrays, then the partials.
+    // Scratch layout: the tree partition's arrays, then the workspace (the
+    // partials).
     const deft::Partition &p = plan->tree;
-    const auto arrays = deft::partition_arrays(p);
     size_t off[deft::kPartArrays];
-    size_t cursor = 0;
-    for (int i = 0; i < deft::kPartArrays; ++i) {
-        off[i] = cursor;
-        cursor = align_up(cursor + (arrays[i].bytes ? arrays[i].bytes : 4));
-    }
-    const size_t slots = (size_t)p.num_slots();
-    const size_t o_off = cursor;
-    const size_t lse_off = align_up(o_off + slots * num_q_heads * head_dim * sizeof(float));
-    const size_t total = align_up(lse_off + slots * num_q_heads * sizeof(float));
-    if (total > kNoallocScratchBytes)
+    const size_t arrays_end = array_offsets(p, off);
+    const int64_t slots = p.num_slots();
+    const deft::WorkLayout wl = deft::work_layout(slots > 0 ? slots : 1, num_q_heads, head_dim);
+    if (arrays_end + wl.total > kNoallocScratchBytes)
         return DEFT_EWORKSPACE;   // this plan and head shape need more than the fixed array
     if (plan->num_queries == 0)
         return DEFT_OK;
+
+    // The host image of the arrays, packed once per plan build (host memory
+    // only; its capacity is kept across rebuilds).
+    deft_plan_t *mp = const_cast<deft_plan_t *>(plan);
+    if (!mp->noalloc_image_ok) {
+        try {
+            mp->noalloc_image.assign(arrays_end, 0u);
+        } catch (const std::bad_alloc &) {
+            return DEFT_ENOMEM;
+        }
+        const auto arrays = deft::partition_arrays(p);
+        for (int i = 0; i < deft::kPartArrays; ++i)
+            if (arrays[i].bytes)
+                std::memcpy(mp->noalloc_image.data() + off[i], arrays[i].ptr, arrays[i].bytes);
+        mp->noalloc_image_ok = true;
+    }
 
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess)
         return DEFT_ECUDA;
     unsigned char *base = nullptr;
-    int rc = scratch_address(dev, &base);
+    rc = scratch_address(dev, &base);
     if (rc != DEFT_OK)
         return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    for (int i = 0; i < deft::kPartArrays; ++i)
-        if (arrays[i].bytes &&
-            cudaMemcpyAsync(base + off[i], arrays[i].ptr, arrays[i].bytes, cudaMemcpyHostToDevice, st) !=
-                cudaSuccess)
-            return DEFT_ECUDA;
+    unsigned char *ws = base + arrays_end;
+    if (cudaMemcpyAsync(base, mp->noalloc_image.data(), arrays_end, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return DEFT_ECUDA;
 
     deft::DevPartition d{};
-    deft::bind_partition(p, base, off, cursor, plan->num_nodes, plan->num_queries, plan->mask_words, d);
-
-    deft::AttnArgs a{};
-    a.q = q;
-    a.k_pages = k_pages;
-    a.v_pages = v_pages;
-    a.node_page_off = node_page_off;
-    a.page_id = page_id;
-    a.num_pages = num_pages;
-    a.num_q_heads = num_q_heads;
-    a.num_kv_heads = num_kv_heads;
-    a.head_dim = head_dim;
-    a.gqa_group = plan->gqa_group;
-    a.scale_log2 = scale * 1.44269504088896340736f;
-    a.wait_prior = 1;
-    a.kv_once = 1;
-    a.o_part = reinterpret_cast<float *>(base + o_off);
-    a.lse_part = reinterpret_cast<float *>(base + lse_off);
+    deft::bind_partition(p, base, off, arrays_end, plan->num_nodes, plan->num_queries, plan->mask_words, d);
+    a.o_part = reinterpret_cast<float *>(ws + wl.o_off);
+    a.lse_part = reinterpret_cast<float *>(ws + wl.lse_off);
 
     const deft::LaunchTracer untraced = [](const deft_trace_record &, void *, const std::function<int()> &launch) {
         return launch();
     };
-    return deft::dispatch_step(a, d, p, use_mma, 0, out, out_dtype, lse, stream, untraced) ? DEFT_ECUDA : DEFT_OK;
+    return deft::dispatch_step(a, d, p, use_mma, 0, stream, untraced) ? DEFT_ECUDA : DEFT_OK;
 }

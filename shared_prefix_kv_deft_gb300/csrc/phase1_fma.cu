@@ -49,9 +49,7 @@
 // of a unit the group's warp states are merged through shared-memory
 // atomics.
 // Every wait on an mbarrier is bounded.
-#include "common.cuh"
-#include "deft_internal.h"
-#include "kprof.cuh"
+#include "merge.cuh"
 #include "tcgen05.cuh"
 
 namespace deft {
@@ -66,7 +64,7 @@ constexpr uint32_t fma_fixed_bytes(int NG)
 {
     return 2 * NG * RMAX * D * 2 + 2 * NG * 32 + NG * RMAX * D * 4 + 3 * 8 * NG * RMAX * 4 + NG * 8 * (RMAX < 8 ? RMAX : 8) * D * 4 +
            2 * kMaxSegsPerChunk * 20 +
-           2 * kPageList * 4 + 2 * 16 + 64 + 384 + 1024 + NG * 16 + 2 * NG * 8;
+           2 * kPageList * 4 + 2 * 16 + 64 + 384 + 1024 + NG * 16 + 2 * NG * 8 + 4 * NG * RMAX * 4;
 }
 
 template <int D, int RMAX>
@@ -96,7 +94,13 @@ struct FmaCfg {
     static constexpr uint32_t seg_off = mdesc_off + NG * 16;                   // [2][5][256]
     static constexpr uint32_t pl_off = seg_off + 2 * kMaxSegsPerChunk * 20;    // [2][kPageList]
     static constexpr uint32_t iinfo_off = pl_off + 2 * kPageList * 4;          // [2] ItemInfo
-    static constexpr uint32_t useq_off = iinfo_off + 2 * 16;                    // [UQ] unit numbers, error and queue flags
+    // Row r's query (bit 31: its only slot) per unit slot [UB][RMAX], the
+    // group's copy handed to the merge warp [NG][RMAX], and the merge warp's
+    // destination row of each row [NG][RMAX].
+    static constexpr uint32_t urow_off = iinfo_off + 2 * 16;
+    static constexpr uint32_t mrow_off = urow_off + UB * RMAX * 4;
+    static constexpr uint32_t mdst_off = mrow_off + NG * RMAX * 4;
+    static constexpr uint32_t useq_off = mdst_off + NG * RMAX * 4;             // [UQ] unit numbers, error and queue flags
     static constexpr uint32_t bar_off = useq_off + 16 * 4;
     static constexpr uint32_t nbars = 2 * ST + 2 * UB + 4 + 2 * 8 + 2 * NG;
     static constexpr uint32_t total = bar_off + nbars * 8;
@@ -134,8 +138,9 @@ struct MergeDesc {
 template <int D, int RMAX>
 __global__ void __launch_bounds__(FmaCfg<D, RMAX>::THREADS, 1)
 phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
-                  const uint32_t *__restrict__ rmask, const int32_t *__restrict__ rmask_off, int32_t n_units,
-                  int32_t static_units, int32_t early, uint32_t *__restrict__ queue)
+                  const uint32_t *__restrict__ rmask, const int32_t *__restrict__ rmask_off,
+                  const uint32_t *__restrict__ direct, int32_t n_units, int32_t static_units, int32_t early,
+                  uint32_t *__restrict__ queue)
 {
     using C = FmaCfg<D, RMAX>;
     constexpr int NG = C::NG, NCW = C::NCW, ST = C::ST, RST = C::RST, UB = C::UB;
@@ -161,6 +166,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     ItemInfo *iinfo = reinterpret_cast<ItemInfo *>(smem + C::iinfo_off);
     volatile MergeDesc *mdesc = reinterpret_cast<volatile MergeDesc *>(smem + C::mdesc_off);
     volatile int32_t *useq = reinterpret_cast<volatile int32_t *>(smem + C::useq_off);
+    int32_t *urow = reinterpret_cast<int32_t *>(smem + C::urow_off);
+    int32_t *mrow = reinterpret_cast<int32_t *>(smem + C::mrow_off);
     volatile int32_t *err = useq + UQ;
     // qdone[0]: this CTA has counted itself done with the queue; qdone[1]:
     // it was the launch's last to do so.
@@ -169,8 +176,6 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     if (a.wait_prior)
         grid_dep_wait();
     if (tid == 0) {
-        if (blockIdx.x < 256)
-            KPROF_ANY(a, 3300 + blockIdx.x);
         grid_dep_launch();
         for (int s = 0; s < ST; ++s) {
             tc::mbar_init(fbar(bars, kFull + s), 33);
@@ -206,6 +211,7 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         int qrow[QJ];   // per q chunk of this lane: query * Hq + group member, or -1
         int rseq0 = 0, rseq1 = 0;   // next tile of each group's ring
         int iseq = -1, prev_item = -1, R = 0, cq0 = 0, ntiles = 0;
+        int qf = 0;   // urow entry of row `lane` of the current item
         // Only the launch's early CTAs own a block: the others start when
         // the step's earlier launches leave their SMs.
         const int own_units = (int)blockIdx.x < early ? static_units : 0;
@@ -268,6 +274,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     const int r = (lane + 32 * j) / (D / 8);
                     qrow[j] = r < R ? p.chunk_q[cq0 + r / G] * Hq + r % G : -1;
                 }
+                if (lane < R)
+                    qf = p.chunk_q[cq0 + lane / G] | (int)(((direct[item] >> lane) & 1u) << 31);
                 if (iseq >= 2 &&
                     !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kSEmpty + sbuf), ((iseq - 2) >> 1) & 1))) {
                     if (!*err) *err = 103;
@@ -339,10 +347,12 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
             }
             cp_async_mbar_arrive_noinc(fbar(bars, kUFull + ub));
+            if (lane < R)
+                urow[ub * RMAX + lane] = qf;
+            __syncwarp();
             if (lane == 0) {
                 info[ub] = UnitInfo{R, cq0, h, ntiles, (i % NG) ? rseq1 : rseq0, {0, 0, 0}};
                 tc::mbar_arrive(fbar(bars, kUFull + ub));
-                KPROF(a, 2000 + 8 * i + 0);
             }
             if (i % NG)
                 rseq1 += ntiles;
@@ -397,8 +407,6 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             const int32_t *plist = reinterpret_cast<const int32_t *>(smem + C::pl_off) + sbuf * kPageList;
             const ItemInfo ii = iinfo[sbuf];
             (void)i;
-            if (lane == 0)
-                KPROF(a, 2000 + 8 * i + 1);
             // Physical page of token tk of segment sg.
             auto page_of = [&](int sg, int tk) {
                 return ii.listed ? plist[seg[1024 + sg] + tk / kPageSize - seg[512 + sg] / kPageSize]
@@ -431,15 +439,11 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 if (nvalid == kTile && (tka % kPageSize) == 0 && seg_at(p0 + kTile - 1) == sga) {
                     // Fast path: four whole pages of one segment.
                     const int pg = lane < 4 ? page_of(sga, tka + kPageSize * lane) : -1;
-                    if (lane == 0 && ring == 0 && seq < 16)
-                        KPROF(a, 2100 + 8 * seq + 4);
                     if (seq >= RST &&
                         !__all_sync(0xffffffffu, tc::mbar_wait(fbar(bars, kEmpty + st), ((seq / RST) - 1) & 1))) {
                         ok = false;
                         break;
                     }
-                    if (lane == 0 && ring == 0 && seq < 16)
-                        KPROF(a, 2100 + 8 * seq + 5);
                     const uint32_t mrow = (uint32_t)seg[768 + sga];
                     meta[st * kTile + lane] = mrow;
                     meta[st * kTile + lane + 32] = mrow;
@@ -453,8 +457,6 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         tc::bulk_load(vdst + rb, vg + o, kPageBytes, full, kv_pol);
                     }
                     tc::mbar_arrive(full);
-                    if (lane == 0 && ring == 0 && seq < 16)
-                        KPROF(a, 2100 + 8 * seq + 1);
                     continue;
                 }
                 // General path: segment and token of the tile positions lane and lane + 32.
@@ -555,13 +557,9 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     cp_async_wait<0>();
                 }
                 tc::mbar_arrive(full);
-                if (lane == 0 && ring == 0 && seq < 16)
-                    KPROF(a, 2100 + 8 * seq + 1);
             }
             if (!ok)
                 if (!*err) *err = 107;
-            if (lane == 0)
-                KPROF(a, 2000 + 8 * i + 2);
         }
         cp_async_wait<0>();
         // Do not leave while bulk copies of ours may still be landing: wait for
@@ -633,16 +631,12 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             const UnitInfo ui = info[ub];
             if (ui.R < 0)
                 break;   // no more units
-            if (gtid == 0)
-                KPROF(a, 2000 + 8 * i + 3);
             const int R = ui.R;
             const __nv_bfloat16 *qst = reinterpret_cast<const __nv_bfloat16 *>(smem + C::qst_off) + ub * RMAX * D;
             // qs[r][e]: q pre-scaled by scale * log2 e; rows past R are 0.
             for (int x = gtid; x < RMAX * D; x += nthr)
                 qs[x] = x < R * D ? __bfloat162float(qst[x]) * a.scale_log2 : 0.f;
             tc::named_sync(bar_id, nthr);
-            if (gtid == 0 && g == 0 && i < 16)
-                KPROF(a, 2300 + 4 * i + 3);
             f32x2 qv[RL][NCH * 4];
 #pragma unroll
             for (int rl = 0; rl < RL; ++rl)
@@ -677,8 +671,6 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     tile_ok = false;
                     break;
                 }
-                if (gtid == 0 && g == 0 && sq < 16)
-                    KPROF(a, 2100 + 8 * sq + 2);
                 const uint8_t *Ks = smem + C::stage_off + (size_t)(st * 2) * C::op_bytes;
                 const uint8_t *Vs = Ks + C::op_bytes;
 #pragma unroll
@@ -834,10 +826,6 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     }
                 }
                 __syncwarp();
-                if (gtid == 0 && g == 0 && sq < 16)
-                    KPROF(a, 2100 + 8 * sq + 3);
-                if (gtid == 7 * 32 && g == 0 && sq < 16)
-                    KPROF(a, 2100 + 8 * sq + 6);
                 if (lane == 0)
                     tc::mbar_arrive(fbar(bars, kEmpty + st));
             }
@@ -865,12 +853,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             // time after it has read the previous ones; the group goes on
             // with its next unit meanwhile.
             bool merr = false;
-            if (gtid == 0 && g == 0 && i < 16)
-                KPROF(a, 2300 + 4 * i + 0);
             for (int rb = 0; rb < R; rb += C::MRB) {
                 const bool okm = mseq == 0 || tc::mbar_wait(fbar(bars, kMEmpty + g), (mseq - 1) & 1);
-                if (gtid == 0 && g == 0 && i < 16 && rb == 0)
-                    KPROF(a, 2300 + 4 * i + 1);
                 if (tc::named_sync_or(bar_id, nthr, !okm)) {
                     if (!*err) *err = 110;
                     merr = true;
@@ -884,6 +868,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         lwb[lw * RMAX + r] = l_run[k];
                     }
                 }
+                if (rb == 0 && gtid < R)
+                    mrow[g * RMAX + gtid] = urow[ub * RMAX + gtid];
 #pragma unroll
                 for (int rl = 0; rl < RL; ++rl) {
                     const int r = rg * RL + rl;
@@ -905,16 +891,12 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     mdesc[g].rb = rb;
                 }
                 tc::named_sync(bar_id, nthr);
-                if (gtid == 0 && g == 0 && i < 16 && rb == 0)
-                    KPROF(a, 2300 + 4 * i + 2);
                 if (gtid == 0)
                     tc::mbar_arrive(fbar(bars, kMFull + g));
                 ++mseq;
             }
             if (merr)
                 break;
-            if (gtid == 0)
-                KPROF(a, 2000 + 8 * i + 4);
             if (lane == 0)
                 tc::mbar_arrive(fbar(bars, kUEmpty + ub));
         }
@@ -952,6 +934,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 const float *lwb = mw + NCW * RMAX;
                 float *wts = reinterpret_cast<float *>(smem + C::ml_off) + 2 * NCW * RMAX + g * 8 * RMAX;
                 const float *obuf = reinterpret_cast<const float *>(smem + C::obuf_off) + g * 8 * C::MRB * D;
+                int32_t *mdst = reinterpret_cast<int32_t *>(smem + C::mdst_off) + g * RMAX;
+                const int32_t *mq = mrow + g * RMAX;
                 if (md.rb == 0 && lane < md.R) {
                     float M = -INFINITY;
 #pragma unroll
@@ -968,8 +952,19 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                     for (int w = 0; w < 8; ++w)
                         wts[w * RMAX + lane] = c[w] * inv;
-                    const size_t row = (size_t)(md.cq0 + lane / G) * Hq + md.h * G + (lane % G);
-                    a.lse_part[row] = L > 0.f ? M + log2f(L) : -INFINITY;
+                    const float l2 = L > 0.f ? M + log2f(L) : -INFINITY;
+                    const int head = md.h * G + (lane % G), qf = mq[lane];
+                    // Destination row: the partial slot's, or (a query with
+                    // this one slot) -1 - the output row.
+                    if (a.direct && qf < 0) {
+                        const int orow = (qf & 0x7fffffff) * Hq + head;
+                        a.lse_out[orow] = direct_lse(l2);
+                        mdst[lane] = -1 - orow;
+                    } else {
+                        const int prow = (md.cq0 + lane / G) * Hq + head;
+                        a.lse_part[prow] = l2;
+                        mdst[lane] = prow;
+                    }
                 }
                 __syncwarp();
                 const int rows = md.R - md.rb < C::MRB ? md.R - md.rb : C::MRB;
@@ -985,9 +980,16 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         acc.z = fmaf(v.z, wt, acc.z);
                         acc.w = fmaf(v.w, wt, acc.w);
                     }
-                    const int rr = md.rb + r;
-                    const size_t row = (size_t)(md.cq0 + rr / G) * Hq + md.h * G + (rr % G);
-                    *reinterpret_cast<float4 *>(a.o_part + row * D + e4) = acc;
+                    const int dr = mdst[md.rb + r];
+                    if (dr >= 0) {
+                        *reinterpret_cast<float4 *>(a.o_part + (size_t)dr * D + e4) = acc;
+                    } else {
+                        const size_t orow = (size_t)(-1 - dr);
+                        store_out(a, orow, e4 + 0, D, acc.x);
+                        store_out(a, orow, e4 + 1, D, acc.y);
+                        store_out(a, orow, e4 + 2, D, acc.z);
+                        store_out(a, orow, e4 + 3, D, acc.w);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -1002,12 +1004,13 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             }
         }
     }
-    if (tid == 96 && blockIdx.x < 256)
-        KPROF_ANY(a, 3600 + blockIdx.x);
     __syncthreads();
     if (*err) {
-        // A wait ran out: mark every partial of the launch as failed (the
+        // A wait ran out: record it in the partition's status word and mark
+        // every partial and output row of the launch's units as failed (the
         // step's output then shows it); the units are not tracked per CTA.
+        if (tid == 0)
+            report_failure(p.status, *err);
         for (int u = 0; u < n_units; ++u) {
             const int item = u / Hkv, h = u - item * Hkv;
             const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
@@ -1015,9 +1018,13 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             for (int x = tid; x < (qe - qb) * G * D; x += C::THREADS) {
                 const int r = x / D, e = x - r * D;
                 const size_t prw = (size_t)(cq0 + r / G) * Hq + h * G + (r % G);
+                const size_t orw = (size_t)p.chunk_q[cq0 + r / G] * Hq + h * G + (r % G);
                 a.o_part[prw * D + e] = __int_as_float(0x7fc00000);
-                if (e == 0)
+                store_out(a, orw, e, D, __int_as_float(0x7fc00000));
+                if (e == 0) {
                     a.lse_part[prw] = __int_as_float(0x7fc00000);
+                    a.lse_out[orw] = __int_as_float(0x7fc00000);
+                }
             }
         }
     }
@@ -1035,7 +1042,8 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 
 template <int D, int RMAX>
 int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-               const int32_t *rmask_off, int32_t n, uint32_t *queue, LaunchShape sh, cudaStream_t st)
+               const int32_t *rmask_off, const uint32_t *direct, int32_t n, uint32_t *queue, LaunchShape sh,
+               cudaStream_t st)
 {
     using C = FmaCfg<D, RMAX>;
     static bool configured = false;
@@ -1050,36 +1058,36 @@ int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, c
     const int32_t grid = sh.grid < units ? sh.grid : units;
     const int32_t early = sh.early < grid ? sh.early : grid;
     return (int)launch_dependent(phase1_fma_kernel<D, RMAX>, dim3(grid), dim3(C::THREADS), C::alloc, st, a, p,
-                                 items, rmask, rmask_off, units, static_block(units, early), early, queue);
+                                 items, rmask, rmask_off, direct, units, static_block(units, early), early, queue);
 }
 
 template <int D>
 int launch_bucket(int bucket, const AttnArgs &a, const DevPartition &p, const int32_t *items,
-                  const uint32_t *rmask, const int32_t *rmask_off, int32_t n, uint32_t *queue, LaunchShape sh,
-                  cudaStream_t st)
+                  const uint32_t *rmask, const int32_t *rmask_off, const uint32_t *direct, int32_t n,
+                  uint32_t *queue, LaunchShape sh, cudaStream_t st)
 {
     switch (bucket) {
-    case 0: return launch_one<D, 1>(a, p, items, rmask, rmask_off, n, queue, sh, st);
-    case 1: return launch_one<D, 2>(a, p, items, rmask, rmask_off, n, queue, sh, st);
-    case 2: return launch_one<D, 4>(a, p, items, rmask, rmask_off, n, queue, sh, st);
-    case 3: return launch_one<D, 8>(a, p, items, rmask, rmask_off, n, queue, sh, st);
-    default: return launch_one<D, 16>(a, p, items, rmask, rmask_off, n, queue, sh, st);
+    case 0: return launch_one<D, 1>(a, p, items, rmask, rmask_off, direct, n, queue, sh, st);
+    case 1: return launch_one<D, 2>(a, p, items, rmask, rmask_off, direct, n, queue, sh, st);
+    case 2: return launch_one<D, 4>(a, p, items, rmask, rmask_off, direct, n, queue, sh, st);
+    case 3: return launch_one<D, 8>(a, p, items, rmask, rmask_off, direct, n, queue, sh, st);
+    default: return launch_one<D, 16>(a, p, items, rmask, rmask_off, direct, n, queue, sh, st);
     }
 }
 
 }  // namespace
 
 int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *items, const uint32_t *rmask,
-                      const int32_t *rmask_off, int32_t n, int bucket, uint32_t *queue, LaunchShape shape,
-                      void *stream)
+                      const int32_t *rmask_off, const uint32_t *direct, int32_t n, int bucket, uint32_t *queue,
+                      LaunchShape shape, void *stream)
 {
     if (n <= 0)
         return 0;
     if ((int64_t)n * a.num_kv_heads > INT32_MAX || !queue || shape.grid < 1 || shape.early < 1)
         return (int)cudaErrorInvalidValue;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, rmask, rmask_off, n, queue, shape, st)
-                             : launch_bucket<64>(bucket, a, p, items, rmask, rmask_off, n, queue, shape, st);
+    return a.head_dim == 128 ? launch_bucket<128>(bucket, a, p, items, rmask, rmask_off, direct, n, queue, shape, st)
+                             : launch_bucket<64>(bucket, a, p, items, rmask, rmask_off, direct, n, queue, shape, st);
 }
 
 }  // namespace deft

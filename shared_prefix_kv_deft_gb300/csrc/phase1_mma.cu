@@ -57,9 +57,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include "common.cuh"
-#include "deft_internal.h"
-#include "kprof.cuh"
+#include "merge.cuh"
 #include "tcgen05.cuh"
 
 namespace deft {
@@ -214,15 +212,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         grid_dep_wait();
     if (tid == 0) {
         grid_dep_launch();
-        KPROF(a, 0);
-        if (blockIdx.x < 1024)
-            KPROF_ANY(a, 3072 + blockIdx.x);
     }
     if (warp == 9) {
         tc::tmem_alloc(smem_u32(tmem_slot), kTmemCols);
         tc::tmem_relinquish();
-        if (lane == 0)
-            KPROF(a, 2);
     }
     if (tid == 0) {
         for (int i = kBarFullK; i < kBarEmptyK; ++i)
@@ -251,21 +244,16 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         qdone[0] = 0;
         qdone[1] = 0;
         tc::fence_mbar_init();
-        KPROF(a, 3);
     }
     // Operands start finite: rows past a chunk's end are never loaded and
     // their P is 0, which must not meet a NaN.
     for (uint32_t i = tid; i < L::meta_off / 16; i += kThreadsMma)
         reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
-    if (tid == 0)
-        KPROF(a, 5);
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    if (tid == 0)
-        KPROF(a, 1);
     float *epi = reinterpret_cast<float *>(smem + L::epi_off);
     volatile int32_t *epi_info = reinterpret_cast<volatile int32_t *>(smem + L::epi_off + 2 * 2 * 128 * 4);
 
@@ -358,8 +346,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     ++iseq;
                     const int sbuf = iseq & 1;
                     const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];
-                    if (lane == 0 && i == 0)
-                        KPROF(a, 30);
                     R = (qe - qb) * G;
                     const int sb = p.chunk_seg_off[c], nseg = p.chunk_seg_off[c + 1] - sb;
                     cq0 = p.chunk_q_off[c] + qb;
@@ -370,14 +356,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         const int r = lane + 32 * k;
                         qrow[k] = r < R ? p.chunk_q[cq0 + r / G] * Hq + r % G : 0;
                     }
-                    if (lane == 0 && i == 0)
-                        KPROF(a, 31 + 0 * (sb + nseg + cq0 + T));
                     if (i == 0) {
                         issue_q(h, 0);
                         q_issued = true;
                     }
-                    if (lane == 0 && i == 0)
-                        KPROF(a, 32);
                     if (iseq >= 2 &&
                         !__all_sync(0xffffffffu, tc::mbar_wait(bar(kBarSegEmpty + sbuf), ((iseq - 2) >> 1) & 1))) {
                         if (!*err) *err = 203;
@@ -396,14 +378,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         asm volatile("prefetch.global.L2 [%0];\n" ::"l"(a.page_id + pgb + tb / kPageSize));
                         s_rmask[s] = item_rm[s];
                     }
-                    if (lane == 0 && i == 0)
-                        KPROF(a, 33);
                     if (lane == 0)
                         iinfo[sbuf] = ItemInfo{nseg, T, {0, 0}};
                     __syncwarp();
                     tc::mbar_arrive(bar(kBarSegFull + sbuf));
-                    if (lane == 0 && i < 8)
-                        KPROF(a, 10 + i);
                 }
                 if (!q_issued) {
                     // Q^T buffer i % QB, once unit i - QB's last S has read it.
@@ -422,8 +400,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     uinfo[ub] = UnitInfo{R, cq0, h, ntiles, {0, 0, 0, 0}};
                 __syncwarp();
                 tc::mbar_arrive(bar(kBarUFull + ub));
-                if (lane == 0 && i < 8)
-                    KPROF(a, 20 + i);
                 // Warm L2 with the rows of the item's next KV head, likely this
                 // CTA's next unit (the queue hands out units in order).
                 if (h + 1 < Hkv)
@@ -566,12 +542,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 T = ii.T;
                 nseg = ii.nseg;
                 const int ntiles = (T + kTileTok - 1) / kTileTok;
-                if (lane == 0 && kv == 0 && gseq == 0)
-                    KPROF(a, 40);
                 Res res;
                 resolve(0, res);
-                if (lane == 0 && kv == 0 && gseq == 0)
-                    KPROF(a, 41 + 0 * res.page_y);
                 for (int t = 0; t < ntiles; ++t, ++gseq) {
                     const int st = gseq % NS;
                     if (gseq >= NS) {
@@ -583,8 +555,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             break;
                         }
                     }
-                    if (lane == 0 && kv == 0 && gseq < 16)
-                        KPROF(a, 800 + 4 * gseq);
                     if (kv == 0) {
     #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -596,8 +566,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     if (lane == 0)
                         tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
                     __syncwarp();
-                    if (lane == 0 && kv == 0 && gseq == 0)
-                        KPROF(a, 42);
                     // Eight whole, consecutive pages: one box per column half.
                     bool run8 = false;
                     const int pg0 = __shfl_sync(0xffffffffu, res.page_y, 0);
@@ -610,14 +578,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         }
                     } else if (res.page_y >= 0) {
                         const int y = (res.page_y * Hkv + h) * kPageSize;
-                        if (lane == 0 && kv == 0 && gseq == 0)
-                            KPROF(a, 43);
                         const uint32_t row_b = (uint32_t)(16 * lane) * 128;
                         tc::tma_load_2d(dst + row_b, tm, 0, y, full, kv_pol);
                         tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full, kv_pol);
                     }
-                    if (lane == 0 && kv == 0 && gseq < 16)
-                        KPROF(a, 801 + 4 * gseq);
                     // Ragged rows: two rows per warp step, 16 lanes (16-byte chunks) each.
                     bool any_cp = false;
                     const __nv_bfloat16 *src0 = src_base + (lane & 15) * 8;
@@ -655,12 +619,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         tc::fence_proxy_async();
                     }
                     tc::mbar_arrive(full);
-                    if (lane == 0 && gseq < 64)
-                        KPROF(a, 100 + 100 * kv + gseq);
                     if (t + 1 < ntiles)
                         resolve(t + 1, res);
-                    if (lane == 0 && kv == 0 && gseq < 16)
-                        KPROF(a, 802 + 4 * gseq);
                 }
             }
             cp_async_wait<0>();
@@ -717,8 +677,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             }
                             tc::mma_commit(bar(kBarSFull + b));
                             tc::mma_commit(bar(kBarEmptyK + st));
-                            if (gs < 64)
-                                KPROF(a, 300 + gs);
                             ++gs;
                             if (++ts == nts) {
                                 tc::mma_commit(bar(qfree_bar(is % L::QB)));
@@ -746,8 +704,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             }
                             tc::mma_commit(bar(kBarPvDone));
                             tc::mma_commit(bar(kBarEmptyV + stp));
-                            if (gp < 64)
-                                KPROF(a, 400 + gp);
                             ++gp;
                             if (++tp == ((ip & 1) ? ntq1 : ntq0)) {
                                 ++ip;
@@ -818,16 +774,12 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 tc::named_sync(3, 128);
                 if (je == 0)
                     tc::mbar_arrive(bar(kBarOFree + ob));
-                if (je == 0 && i < 8)
-                    KPROF(a, 700 + i);
                 if (R < 0)
                     break;
             }
     }
     } else {
         tc::setmaxnreg_inc<kRegsSoftmax>();
-        if (tid == 0)
-            KPROF(a, 6);
         // ---------------- softmax warpgroups ----------------
         // Warpgroup w owns columns [w*NPH, w*NPH + NPH) of S^T and O^T.
         const int w = warp >> 2, wt = warp & 3, j = tid & 127;
@@ -862,9 +814,16 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             }
         };
         // Tells the epilogue warpgroup that no unit follows (R = -1) or that
-        // this one failed and none follows (R = -2).
-        auto end_epilogue = [&](int ob, int code) {
+        // this one failed and none follows (R = -2), at unit index i: first
+        // waits until the epilogue has read unit i - 2 out of buffer ob (a
+        // real unit is held back by its P.V; this mark is not), so that the
+        // mark neither overwrites that unit's description nor completes a
+        // second phase of the buffer's barrier ahead of the epilogue.
+        auto end_epilogue = [&](int i, int code) {
+            const int ob = i & 1;
             if (j == 0) {
+                if (i >= 2 && !tc::mbar_wait(bar(kBarOFree + ob), ((i - 2) >> 1) & 1))
+                    if (!*err) *err = 212;
                 if (w == 0)
                     epi_info[ob * 4] = code;
                 tc::mbar_arrive(bar(kBarEpiFull + ob));
@@ -882,13 +841,13 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             const bool okw = dry || tc::mbar_wait(bar(kBarUFull + ub), (i >> 1) & 1);
             if (tc::named_sync_or(nb_id, 128, !okw)) {
                 if (!*err) *err = 209;
-                end_epilogue(ob, -2);
+                end_epilogue(i, -2);
                 break;
             }
             const UnitInfo ui = dry ? UnitInfo{2 * NPH, 0, 0, 1, {0, 0, 0, 0}} : uinfo[ub];
             tc::named_sync(nb_id, 128);
             if (ui.ntiles < 0) {
-                end_epilogue(ob, -1);   // no more units
+                end_epilogue(i, -1);   // no more units
                 break;
             }
             if (j == 0 && !dry)
@@ -910,8 +869,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 const int b = gseq & 1;
                 ok = dry || tc::mbar_wait(bar(kBarSFull + b), (gseq >> 1) & 1);
                 tc::fence_after_sync();
-                if (tid == 0 && gseq < 64)
-                    KPROF(a, 500 + gseq);
                 float s[NPH];
                 load_cols(tmem + (uint32_t)(b * 128) + lane_off + col0, s);
                 const uint4 mk = meta[(gseq & 3) * kTileTok + j];
@@ -1006,16 +963,12 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
                 if (j == 0 && !dry)
                     tc::mbar_arrive(bar(kBarPFull));
-                if (tid == 0 && gseq < 64)
-                    KPROF(a, 600 + gseq);
             }
             // The unit's last P.V, then O / l for this warpgroup's rows.
             if (ok && !dry) {
                 ok = tc::mbar_wait(bar(kBarPvDone), (gseq - 1) & 1);
                 tc::fence_after_sync();
             }
-            if (tid == 0 && i >= 0 && i < 8)
-                KPROF(a, 710 + 4 * i);
             if (!ok)
                 if (!*err) *err = 210;
             const bool failed = tc::named_sync_or(nb_id, 128, !ok || *err != 0);
@@ -1028,8 +981,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 redw[wt * 64 + g + lane] = reduce_scatter32<false>(tmp, lane);
             }
             tc::named_sync(nb_id, 128);
-            if (tid == 0 && i >= 0 && i < 8)
-                KPROF(a, 712 + 4 * i);
             // Column sums and partial rows for the epilogue warpgroup, which
             // reads O (buffer ob) out of TMEM; the lse partials go out here.
             float *linv_e = epi + (ob * 2 + w) * 128;
@@ -1053,13 +1004,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 tc::mbar_arrive(bar(kBarEpiFull + ob));
             if (dry) {
                 gseq = 0;
-                if (tid == 0)
-                    KPROF(a, 8);
             }
-            if (tid == 0 && i >= 0 && i < 8)
-                KPROF(a, 711 + 4 * i);
-            if (tid == 0 && blockIdx.x < 1024)
-                KPROF_ANY(a, 1024 + blockIdx.x);
             if (failed)
                 break;
         }
@@ -1067,8 +1012,11 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     tc::fence_before_sync();
     __syncthreads();
     if (*err && tid < 128) {
-        // A wait ran out: mark every partial of the launch as failed (the
-        // step's output then shows it); the units are not tracked per CTA.
+        // A wait ran out: record it in the partition's status word and mark
+        // every partial of the launch as failed (the merged output then
+        // shows it); the units are not tracked per CTA.
+        if (tid == 0)
+            report_failure(p.status, *err);
         for (int u = 0; u < n_units; ++u) {
             const int item = u / Hkv, h = u - item * Hkv;
             const int c = items[3 * item], qb = items[3 * item + 1], qe = items[3 * item + 2];

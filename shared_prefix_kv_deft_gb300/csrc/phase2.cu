@@ -1,4 +1,7 @@
-// phase2.cu -- per-query log-sum-exp merge of the phase-1 partials.
+// phase2.cu -- the per-query log-sum-exp merge of the phase-1 partials, a
+// launch of its own after phase 1: over the queries whose path spans more
+// than one chunk and those whose path is empty (out = 0, lse = -inf); the
+// rows of single-chunk queries were written by phase 1.
 //
 // DeFT abstract (partial results of a query's KV partitions are combined per
 // query) and DeFT Guide, "Deep Dive": the online-softmax identity that makes
@@ -17,33 +20,29 @@
 // the grid dependency, then issues the partials' loads of up to 16 slots
 // before the first arithmetic.  The partials were written moments earlier
 // and are mostly still in L2.
-#include "common.cuh"
-#include "deft_internal.h"
-#include "kprof.cuh"
+#include "merge.cuh"
 
 namespace deft {
 namespace {
 
 template <int D>
-__global__ void __launch_bounds__(256) phase2_merge_kernel(
-    const float *__restrict__ o_part, const float *__restrict__ lse_part,
-    const int32_t *__restrict__ q_slot_off, const int32_t *__restrict__ q_slot, int32_t num_queries,
-    int32_t num_q_heads, void *__restrict__ out, int32_t out_dtype, float *__restrict__ lse_out,
-    KprofArg kp)
+__global__ void __launch_bounds__(256) phase2_merge_kernel(AttnArgs a, const int32_t *__restrict__ q_slot_off,
+                                                           const int32_t *__restrict__ q_slot,
+                                                           const int32_t *__restrict__ queries, int32_t nq)
 {
     constexpr int E = D / 32;  // elements per lane
     constexpr int KP = 16;     // slots whose partial rows are loaded before any arithmetic
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0)
         grid_dep_launch();
-        if (blockIdx.x < 96)
-            KPROF_ANY(kp, 3760 + blockIdx.x);
-    }
     const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
-    if (warp >= num_queries * num_q_heads)
+    const int num_q_heads = a.num_q_heads;
+    if (warp >= nq * num_q_heads)
         return;
-    const int q = warp / num_q_heads;
-    const int h = warp - q * num_q_heads;
+    const int i = warp / num_q_heads;
+    const int h = warp - i * num_q_heads;
+    const int q = queries ? queries[i] : i;
+    const float *o_part = a.o_part, *lse_part = a.lse_part;
     // Slot rows come from the plan, so they are read before the partials are
     // ready (lane j: the query's slot j, for the first 32).
     const int s0 = q_slot_off[q], n = q_slot_off[q + 1] - s0;
@@ -51,8 +50,6 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
     if (lane < n)
         row = (size_t)q_slot[s0 + lane] * num_q_heads + h;
     grid_dep_wait();   // the phase-1 launches have completed
-    if ((threadIdx.x & 255) == 0 && blockIdx.x < 96)
-        KPROF_ANY(kp, 3856 + blockIdx.x);
 
     // Every load of the first KP slots goes out before the first use.
     const float l = lane < n ? lse_part[row] : -INFINITY;
@@ -80,9 +77,9 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
     }
     float M = l;
     for (int b = 32; b < n; b += 32) {
-        const int i = b + lane;
-        if (i < n)
-            M = fmaxf(M, lse_part[(size_t)q_slot[s0 + i] * num_q_heads + h]);
+        const int k = b + lane;
+        if (k < n)
+            M = fmaxf(M, lse_part[(size_t)q_slot[s0 + k] * num_q_heads + h]);
     }
     M = warp_max(M);
 
@@ -119,11 +116,11 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
         for (int j = KP; j < n32; ++j)
             add_row(__shfl_sync(0xffffffffu, row, j), __shfl_sync(0xffffffffu, w, j));
         for (int b = 32; b < n; b += 32) {
-            const int i = b + lane;
+            const int k = b + lane;
             size_t rb = 0;
             float wb = 0.f;
-            if (i < n) {
-                rb = (size_t)q_slot[s0 + i] * num_q_heads + h;
+            if (k < n) {
+                rb = (size_t)q_slot[s0 + k] * num_q_heads + h;
                 wb = exp2f(lse_part[rb] - M);
             }
             wsum += wb;
@@ -135,44 +132,36 @@ __global__ void __launch_bounds__(256) phase2_merge_kernel(
     }
     const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
     const size_t orow = ((size_t)q * num_q_heads + h) * D + lane * E;
-    if (out_dtype == DEFT_OUT_F32) {
-        float *o = reinterpret_cast<float *>(out) + orow;
+    if (a.out_dtype == DEFT_OUT_F32) {
+        float *o = reinterpret_cast<float *>(a.out) + orow;
 #pragma unroll
         for (int e = 0; e < E; ++e)
             o[e] = acc[e] * inv;
     } else {
-        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(out) + orow;
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(a.out) + orow;
 #pragma unroll
         for (int e = 0; e < E; e += 2)
-            *reinterpret_cast<__nv_bfloat162 *>(o + e) =
-                __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
+            *reinterpret_cast<__nv_bfloat162 *>(o + e) = __floats2bfloat162_rn(acc[e] * inv, acc[e + 1] * inv);
     }
     if (lane == 0)
-        lse_out[(size_t)q * num_q_heads + h] =
-            wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
-    if (threadIdx.x == 0 && blockIdx.x < 96)
-        KPROF_ANY(kp, 3952 + blockIdx.x);
+        a.lse_out[(size_t)q * num_q_heads + h] = wsum > 0.f ? (M + log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 }  // namespace
 
-int launch_phase2(const AttnArgs &a, const DevPartition &p, void *out, int32_t out_dtype,
-                  float *lse, void *stream)
+int launch_phase2(const AttnArgs &a, const DevPartition &p, const int32_t *queries, int32_t nq, void *stream)
 {
-    const int64_t warps = (int64_t)p.num_queries * a.num_q_heads;
+    const int64_t warps = (int64_t)nq * a.num_q_heads;
     if (warps == 0)
         return 0;
     const int threads = 256;
     const unsigned blocks = (unsigned)((warps * 32 + threads - 1) / threads);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    const float *op = a.o_part, *lp = a.lse_part;
-    const int32_t *so = p.q_slot_off, *sl = p.q_slot;
-    const int32_t nq = p.num_queries, hq = a.num_q_heads;
     if (a.head_dim == 128)
-        return (int)launch_dependent(phase2_merge_kernel<128>, dim3(blocks), dim3(threads), 0, st, op, lp, so, sl,
-                                     nq, hq, out, out_dtype, lse, KprofArg{a.kprof});
-    return (int)launch_dependent(phase2_merge_kernel<64>, dim3(blocks), dim3(threads), 0, st, op, lp, so, sl, nq,
-                                 hq, out, out_dtype, lse, KprofArg{a.kprof});
+        return (int)launch_dependent(phase2_merge_kernel<128>, dim3(blocks), dim3(threads), 0, st, a, p.q_slot_off,
+                                     p.q_slot, queries, nq);
+    return (int)launch_dependent(phase2_merge_kernel<64>, dim3(blocks), dim3(threads), 0, st, a, p.q_slot_off,
+                                 p.q_slot, queries, nq);
 }
 
 }  // namespace deft

@@ -147,6 +147,23 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     std::vector<int32_t> fill(p.q_slot_off.begin(), p.q_slot_off.end() - 1);
     for (int32_t s = 0; s < p.num_slots(); ++s)
         p.q_slot[fill[p.chunk_q[s]]++] = s;
+    // A query whose path lies in one chunk of fewer than kMmaMinRows rows
+    // (a CUDA-core chunk) has its rows written to out / lse by phase 1; the
+    // merge launch takes every other query.
+    std::vector<uint8_t> direct_q(num_queries, 0);
+    for (int32_t c = 0; c < C; ++c) {
+        const int32_t k = p.chunk_q_off[c + 1] - p.chunk_q_off[c];
+        if ((int64_t)k * G >= kMmaMinRows)
+            continue;
+        for (int32_t s = p.chunk_q_off[c]; s < p.chunk_q_off[c + 1]; ++s) {
+            const int32_t q = p.chunk_q[s];
+            direct_q[q] = p.q_slot_off[q + 1] - p.q_slot_off[q] == 1 ? 1 : 0;
+        }
+    }
+    p.merge_q.clear();
+    for (int32_t q = 0; q < num_queries; ++q)
+        if (!direct_q[q])
+            p.merge_q.push_back(q);
 
     // Work items.  rows = queries * G.  Chunks under kMmaMinRows rows run on
     // the CUDA-core kernel in row blocks of at most kFmaItemRows rows (whole
@@ -244,6 +261,20 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
         }
         p.mma_rmask_off.push_back((int32_t)(p.mma_rmask.size() / 4));
     }
+    // Rows of the direct queries (none in the fallback items: their chunks
+    // have kMmaMinRows rows or more).
+    auto direct_rows = [&](const std::vector<Item> &v, std::vector<uint32_t> &out) {
+        out.assign(v.size(), 0u);
+        for (size_t i = 0; i < v.size(); ++i) {
+            const Item &it = v[i];
+            const int32_t rows = (it.e - it.b) * G;
+            for (int32_t r = 0; r < rows; ++r)
+                if (direct_q[p.chunk_q[p.chunk_q_off[it.c] + it.b + r / G]])
+                    out[i] |= 1u << r;
+        }
+    };
+    direct_rows(fma, p.fma_direct);
+    direct_rows(fb, p.fallback_direct);
     bucket_offsets(fma, p.fma_bucket_off);
     bucket_offsets(fb, p.fallback_bucket_off);
     bucket_offsets(mma, p.mma_bucket_off);
@@ -499,6 +530,7 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
     st.naive_num_chunks = plan->naive.num_chunks();
     st.naive_num_slots = plan->naive.num_slots();
     st.naive_num_segments = plan->naive.num_segments();
+    st.num_merge_queries = (int32_t)plan->tree.merge_q.size();
     st.unique_tokens = unique_tokens;
     st.naive_tokens = naive_tokens;
     return DEFT_OK;

@@ -52,9 +52,15 @@ class Case:
         self.plan.upload()
         self.deft = deft
 
-    def run(self, naive=False, out_dtype=0):
-        fn = self.deft.deft_naive_attn if naive else self.deft.deft_tree_attn
-        out, lse = fn(self.q, self.k, self.v, self.npo, self.pid, self.plan, out_dtype=out_dtype)
+    def run(self, naive=False, out_dtype=0, flags=0):
+        """One step; flags (STEP_*) go through deft_tree_attn_ex."""
+        if flags:
+            flags |= self.deft.STEP_NAIVE if naive else 0
+            out, lse = self.deft.deft_tree_attn(self.q, self.k, self.v, self.npo, self.pid, self.plan,
+                                                out_dtype=out_dtype, flags=flags)
+        else:
+            fn = self.deft.deft_naive_attn if naive else self.deft.deft_tree_attn
+            out, lse = fn(self.q, self.k, self.v, self.npo, self.pid, self.plan, out_dtype=out_dtype)
         torch.cuda.synchronize()
         return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
 
@@ -94,13 +100,20 @@ SMALL = small_shapes()
 @pytest.mark.parametrize("spec", SMALL, ids=lambda s: s.name)
 @pytest.mark.parametrize("ct", [16, 100, 256])
 def test_tree_and_naive_match_oracle(deft, spec, ct):
+    """Both partitions against the oracle; merging in phase 1 (the default)
+    and in a separate launch give the same values (same partials, same merge
+    arithmetic), and no kernel reports a failed wait."""
     inp = dense_inputs(spec, seed=ct + spec.num_nodes)
     ref, ref_lse = run_oracle(inp)
     case = Case(deft, inp, ct)
-    out, lse = case.run()
-    assert_parity(out, lse, ref, ref_lse, f"tree ct={ct}")
-    out, lse = case.run(naive=True)
-    assert_parity(out, lse, ref, ref_lse, f"naive ct={ct}")
+    for naive in (False, True):
+        what = f"{'naive' if naive else 'tree'} ct={ct}"
+        out, lse = case.run(naive=naive)
+        assert_parity(out, lse, ref, ref_lse, what)
+        out_s, lse_s = case.run(naive=naive, flags=deft.STEP_SEPARATE_MERGE)
+        np.testing.assert_array_equal(out_s, out, err_msg=what + " separate merge")
+        np.testing.assert_array_equal(lse_s, lse, err_msg=what + " separate merge")
+    assert case.plan.step_status() == 0
 
 
 EXTREME = [W.tiny_tree(),
@@ -185,7 +198,7 @@ def test_abi_rejects_bad_calls(deft):
     out = torch.empty((Q, Hq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((Q, Hq), dtype=torch.float32, device="cuda")
     ws_bytes = case.plan.workspace_bytes(Hq, d)
-    ws = torch.empty(ws_bytes + 512, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(ws_bytes + 512, dtype=torch.uint8, device="cuda")
     P = ctypes.c_void_p
 
     def call(plan=case.plan.handle, hq=Hq, hkv=4, hd=d, ps=16, wsp=ws.data_ptr(), wsb=ws_bytes,
@@ -211,7 +224,22 @@ def test_abi_rejects_bad_calls(deft):
     assert call(plan=tree_only.handle) == 0
     assert call(plan=tree_only.handle, fn=lib.deft_naive_attn) == -8   # no naive partition
     assert call(fn=lib.deft_naive_attn) == 0
+
+    def call_ex(flags, plan=case.plan.handle):
+        return lib.deft_tree_attn_ex(P(case.q.data_ptr()), P(case.k.data_ptr()), P(case.v.data_ptr()),
+                                     P(case.npo.data_ptr()), P(case.pid.data_ptr()), case.k.shape[0],
+                                     Hq, 4, d, 16, 0.125, plan, P(out.data_ptr()), 0,
+                                     P(lse.data_ptr()), P(ws.data_ptr()), ws_bytes, flags,
+                                     P(torch.cuda.current_stream().cuda_stream))
+    assert call_ex(0) == 0
+    assert call_ex(deft.STEP_NAIVE | deft.STEP_SEPARATE_MERGE | deft.STEP_CUDA_CORES) == 0
+    assert call_ex(8) == -1             # unknown flag bit
+    assert call_ex(deft.STEP_NAIVE, plan=tree_only.handle) == -8
     torch.cuda.synchronize()
+    assert case.plan.step_status() == 0
+    code = ctypes.c_int32(5)
+    assert lib.deft_step_status(unuploaded.handle, None, ctypes.byref(code)) == -8
+    assert lib.deft_step_status(case.plan.handle, None, None) == -1
 
 
 @pytest.mark.parametrize("cfg", [2, 7])
@@ -284,7 +312,7 @@ MMA_SHAPES = [
 
 @pytest.mark.parametrize("spec", MMA_SHAPES, ids=lambda s: s.name)
 @pytest.mark.parametrize("ct", [64, 256])
-def test_tensor_core_and_cuda_core_paths_agree_with_oracle(deft, spec, ct, monkeypatch):
+def test_tensor_core_and_cuda_core_paths_agree_with_oracle(deft, spec, ct):
     inp = dense_inputs(spec, seed=11 + ct)
     ref, ref_lse = run_oracle(inp)
     case = Case(deft, inp, ct)
@@ -296,9 +324,11 @@ def test_tensor_core_and_cuda_core_paths_agree_with_oracle(deft, spec, ct, monke
     kinds = {r["kernel"] for r in deft.trace_read()}
     assert "phase1_mma" in kinds
     assert_parity(out, lse, ref, ref_lse, "tcgen05 path")
-    monkeypatch.setenv("DEFT_DISABLE_MMA", "1")
-    out2, lse2 = case.run()
+    out2, lse2 = case.run(flags=deft.STEP_CUDA_CORES)
     assert_parity(out2, lse2, ref, ref_lse, "CUDA-core fallback")
+    out3, lse3 = case.run(flags=deft.STEP_CUDA_CORES | deft.STEP_SEPARATE_MERGE)
+    assert_parity(out3, lse3, ref, ref_lse, "CUDA-core fallback, separate merge")
+    assert case.plan.step_status() == 0
 
 
 POSITION_SHAPES = [W.positions_tree(s, max_nodes=14, max_len=120, max_queries=24, q_heads=8,

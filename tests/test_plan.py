@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol():
     assert set(names) == set(deft.EXPORTS)
     for n in names:
         assert hasattr(lib, n), f"libdeft.so does not export {n}"
-    assert deft.version() == 100
+    assert deft.version() == 200
 
 
 @pytest.mark.parametrize("parent,node_len,query,ct,g,status", [
@@ -357,3 +357,122 @@ def test_failed_rebuild_leaves_the_plan_unchanged():
         assert p.stats == stats
         for name in deft.ARRAYS:
             np.testing.assert_array_equal(p.get(name), before[name])
+
+
+# ---------------------------------------------------------------------------
+# Host-side checks of the step ABI (no GPU: every case below returns before
+# the library makes a CUDA call).
+# ---------------------------------------------------------------------------
+
+def _tiny_plan():
+    spec = W.tiny_tree()
+    return spec, deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, spec.gqa_group)
+
+
+def test_workspace_holds_the_partials_of_the_larger_partition():
+    spec, plan = _tiny_plan()
+    st = plan.stats
+    slots = max(st["num_slots"], st["naive_num_slots"])
+    up = lambda x: (x + 255) // 256 * 256   # noqa: E731
+    for hq, d in ((4, 64), (8, 128)):
+        assert plan.workspace_bytes(hq, d) == up(slots * hq * d * 4) + up(slots * hq * 4)
+    assert plan.workspace_bytes(0, 64) == 0
+
+
+def test_direct_rows_and_merge_queries_follow_the_slot_counts():
+    """A row goes to out / lse from phase 1 exactly when its query has one
+    partial slot and that slot's chunk has fewer than 16 rows (a CUDA-core
+    chunk); the merge launch takes every other query."""
+    cases = [(W.tiny_tree(), 256), (W.tiny_tree(), 16), (W.config(2), 256),
+             (W.reasoning_tree(levels=3, len_lo=5, len_hi=40, num_queries=12, q_heads=4, kv_heads=2), 32),
+             (W.imbalance_tree(leaves=12, control=True, control_len=150, q_heads=8, kv_heads=2), 64),
+             (W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4, head_dim=128), 8192)]
+    cases += [(s, ct) for s in RANDOM[:10] for ct in (1, 16, 512)]
+    seen_direct = seen_merge = 0
+    for spec, ct in cases:
+        plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, ct, spec.gqa_group)
+        G = spec.gqa_group
+        nslots = np.diff(plan.get("q_slot_off"))
+        chunk_q, q_off = plan.get("chunk_q"), plan.get("chunk_q_off")
+        rows = np.diff(q_off) * G
+        slot_chunk = np.repeat(np.arange(len(rows)), np.diff(q_off))
+        first = plan.get("q_slot")[plan.get("q_slot_off")[:-1].clip(max=max(len(slot_chunk) - 1, 0))] \
+            if len(slot_chunk) else np.zeros(len(nslots), int)
+        direct_q = (nslots == 1) & (rows[slot_chunk[first]] < 16) if len(slot_chunk) else nslots < 0
+        np.testing.assert_array_equal(plan.get("merge_q"), np.nonzero(~direct_q)[0])
+        for kind in ("fma", "fallback"):
+            items = plan.get(kind + "_items").reshape(-1, 3)
+            direct = plan.get(kind + "_direct")
+            assert len(direct) == len(items)
+            for (c, b, e), dw in zip(items, direct):
+                want = 0
+                for r in range((e - b) * G):
+                    want |= int(direct_q[chunk_q[q_off[c] + b + r // G]]) << r
+                assert int(dw) == want, (spec.name, ct, kind, c)
+                seen_direct += bin(want).count("1")
+        seen_merge += len(plan.get("merge_q"))
+    # The tiny tree in one 256-token chunk: every query single-slot, no merge launch.
+    tiny = deft.Plan(cases[0][0].parent, cases[0][0].node_len, cases[0][0].query_node, 256, 1)
+    assert tiny.stats["num_merge_queries"] == 0
+    # One chunk of >= 16 rows holding whole paths: single-slot, but merged by phase 2.
+    fs = cases[-1][0]
+    big = deft.Plan(fs.parent, fs.node_len, fs.query_node, 8192, fs.gqa_group)
+    assert big.stats["num_merge_queries"] > 0
+    assert seen_direct > 0 and seen_merge > 0
+
+
+def test_step_calls_reject_bad_flags_and_state_before_any_cuda_call():
+    spec, plan = _tiny_plan()
+    lib = deft.load()
+    P = ctypes.c_void_p
+    fake = P(1 << 20)   # 16-byte aligned, never dereferenced
+
+    def call_ex(flags, handle=plan.handle):
+        return lib.deft_tree_attn_ex(fake, fake, fake, fake, fake, 4, 4, 4, 64, 16, 0.125, handle, fake, 0,
+                                     fake, fake, 1 << 20, flags, None)
+    assert call_ex(8) == -1                 # unknown flag bit
+    assert call_ex(1 << 30) == -1
+    assert call_ex(0) == -8                 # never uploaded
+    assert call_ex(deft.STEP_NAIVE | deft.STEP_SEPARATE_MERGE) == -8
+    tree_only = deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, 1, naive=False)
+    assert call_ex(deft.STEP_NAIVE, tree_only.handle) == -8
+    code = ctypes.c_int32(7)
+    assert lib.deft_step_status(plan.handle, None, ctypes.byref(code)) == -8
+    assert code.value == 0
+    assert lib.deft_step_status(None, None, ctypes.byref(code)) == -1
+    assert lib.deft_step_status(plan.handle, None, None) == -1
+
+
+def test_check_pages_accepts_a_layout_and_rejects_each_bad_table():
+    spec = W.reasoning_tree(levels=3, len_lo=5, len_hi=40, num_queries=12, q_heads=4, kv_heads=2)
+    lay = W.paged_layout(spec)
+    npo, pid, pages = lay.node_page_off, lay.page_id, int(lay.page_id.max()) + 1
+    ln = spec.node_len
+    assert deft.deft_check_pages(ln, npo, pid, pages) == 0
+    assert deft.deft_check_pages(ln, npo, pid, pages + 5) == 0
+    n = int(np.argmax(ln))                   # a node with tokens
+    bad = pid.copy()
+    bad[npo[n]] = pages                      # a page past the pool
+    assert deft.deft_check_pages(ln, npo, bad, pages) == -3
+    bad[npo[n]] = -1                         # a negative page id
+    assert deft.deft_check_pages(ln, npo, bad, pages) == -3
+    off = npo.copy()
+    off[n] = -1                              # page-table offset before the table
+    assert deft.deft_check_pages(ln, off, pid, pages) == -3
+    off[n] = len(pid) - 1                    # the node's pages run past the table's end
+    assert ln[n] > 16
+    assert deft.deft_check_pages(ln, off, pid, pages) == -3
+    last = int(np.argmax(npo[:-1]))          # the node whose pages end the table
+    longer = ln.copy()
+    longer[last] = (len(pid) - npo[last]) * 16 + 1   # one token more than its pages hold
+    assert deft.deft_check_pages(longer, npo, pid, pages) == -3
+    assert deft.deft_check_pages(ln, npo, pid, 0) == -1
+    neg = ln.copy()
+    neg[0] = -1
+    assert deft.deft_check_pages(neg, npo, pid, pages) == -1
+    # Zero-length nodes need no page.
+    z = ln.copy()
+    z[n] = 0
+    off2 = npo.copy()
+    off2[n] = -7
+    assert deft.deft_check_pages(z, off2, pid, pages) == 0

@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--impl", choices=["deft", "reference"], default="deft")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the naive, e2e and CPU-baseline legs")
+    ap.add_argument("--tensor-pack", type=int, default=-1,
+                    help="plan with DEFT_PLAN_TENSOR_PACK (1), without (0), or when head_dim is 128 (-1)")
     ap.add_argument("--step-flags", type=int, default=0,
                     help="deft_tree_attn_ex flags for the timed step (4: merge in a separate launch)")
     ap.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
@@ -88,7 +90,8 @@ def run_profile_case(args):
     t = W.make_tensors(spec, lay, device="cuda")
     npo = torch.from_numpy(lay.node_page_off).cuda()
     pid = torch.from_numpy(lay.page_id).cuda()
-    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group)
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
+                     tensor_pack=tensor_pack(args, spec))
     plan.upload()
     bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim)
 
@@ -106,6 +109,11 @@ def run_profile_case(args):
         raise RuntimeError("a kernel reported a failed wait")
     print("ok", spec.name)
     return 0
+
+
+def tensor_pack(args, spec) -> bool:
+    """Tensor-packed plans for head_dim 128 (the tcgen05 path) unless told."""
+    return bool(args.tensor_pack) if args.tensor_pack >= 0 else spec.head_dim == 128
 
 
 def dist_env():
@@ -407,8 +415,9 @@ def main():
     t = W.make_tensors(spec, layout, device=dev)
     npo = torch.from_numpy(layout.node_page_off).to(dev)
     pid = torch.from_numpy(layout.page_id).to(dev)
+    tp = tensor_pack(args, spec)
     plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
-                     query_pos=spec.query_pos)
+                     query_pos=spec.query_pos, tensor_pack=tp)
     plan.upload()
     bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim, dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -510,7 +519,7 @@ def main():
         "config": {"workload": spec.name, "config_index": args.config, "global_batch": Q * world,
                    "seq_len": int(max(1, st["naive_tokens"] // max(1, Q))),
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "chunk_target": args.chunk_target, "l2": "flushed between timed steps (2 x L2 memset, then 2 x L2 read: cold, clean)",
+                   "chunk_target": args.chunk_target, "tensor_pack": tp, "l2": "flushed between timed steps (2 x L2 memset, then 2 x L2 read: cold, clean)",
                    "q_heads": Hq, "kv_heads": Hkv, "head_dim": d},
         "us_per_step_median": statistics.median(ms) * 1e3,
         "us_per_step_p10": float(np.percentile(ms, 10)) * 1e3,
@@ -569,12 +578,12 @@ def main():
         ek = max(3, min(args.steps, 200))
         e2e_t = []
         p = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
-                      query_pos=spec.query_pos, naive=False)
+                      query_pos=spec.query_pos, naive=False, tensor_pack=tp)
         for i in range(ek + 3):
             barrier()
             t0 = time.perf_counter()
             p.rebuild(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
-                      query_pos=spec.query_pos, naive=False)
+                      query_pos=spec.query_pos, naive=False, tensor_pack=tp)
             p.upload()
             q_dev.copy_(q_host, non_blocking=True)
             deft.deft_tree_attn(q_dev, t.k_pages, t.v_pages, npo, pid, p, bufs=bufs)

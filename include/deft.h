@@ -58,7 +58,7 @@ typedef enum deft_status {
 enum { DEFT_OUT_BF16 = 0, DEFT_OUT_F32 = 1 };
 
 /* deft_plan_ex flags. */
-enum { DEFT_PLAN_TREE_ONLY = 1 };
+enum { DEFT_PLAN_TREE_ONLY = 1, DEFT_PLAN_TENSOR_PACK = 2 };
 
 /* deft_tree_attn_ex flags. */
 enum {
@@ -178,6 +178,15 @@ int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nod
  *   have no element but naive_q_slot_off's num_queries + 1 zeros) and
  *   deft_naive_attn on it returns DEFT_ESTATE.  naive_tokens is still
  *   counted.
+ *   DEFT_PLAN_TENSOR_PACK: for layers run at head_dim 128 (the tensor-core
+ *   path).  Segments whose queries make fewer than 16 rows (queries x
+ *   gqa_group) are laid side by side in chunks of 16 to 128 rows, a piece of
+ *   about chunk_target / m tokens from each of m consecutive such segments
+ *   (the Guide's flattened-tree tile shared by several branches, other
+ *   branches' queries masked), so that they run on the tensor cores instead
+ *   of the CUDA cores.  Every token is still read once; a query gets one
+ *   partial per piece.  At other head sizes the packed chunks run on CUDA
+ *   cores at their full row count: leave the flag off there.
  * Unknown flag bits: DEFT_EINVAL.  Other arguments, results and errors as
  * deft_plan_at.
  */

@@ -45,7 +45,8 @@ EXPORTS = ["deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_rebuild", "de
            "deft_trace_read", "deft_tree_attn_noalloc"]
 
 KERNEL_NAMES = {0: "phase1_fma", 1: "phase1_mma", 2: "phase2_merge"}
-PLAN_TREE_ONLY = 1   # deft_plan_ex flag
+PLAN_TREE_ONLY = 1   # deft_plan_ex flags
+PLAN_TENSOR_PACK = 2
 # deft_tree_attn_ex flags
 STEP_NAIVE = 1
 STEP_CUDA_CORES = 2
@@ -135,6 +136,10 @@ def _i32(a) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
 
+def _plan_flags(naive: bool, tensor_pack: bool) -> int:
+    return (0 if naive else PLAN_TREE_ONLY) | (PLAN_TENSOR_PACK if tensor_pack else 0)
+
+
 def _ptr(a: np.ndarray) -> int:
     # The address as an int (ctypes converts it for c_void_p parameters);
     # cheaper than building a ctypes pointer object.
@@ -148,7 +153,7 @@ class Plan:
     (DEFT_PLAN_TREE_ONLY; deft_naive_attn refuses it)."""
 
     def __init__(self, parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
-                 query_pos=None, naive: bool = True):
+                 query_pos=None, naive: bool = True, tensor_pack: bool = False):
         lib = load()
         self._parent, self._len, self._qn = _i32(parent), _i32(node_len), _i32(query_node)
         self._pos = None if query_pos is None else _i32(query_pos)
@@ -157,7 +162,7 @@ class Plan:
                                                 int(self._parent.shape[0]), _ptr(self._qn),
                                                 None if self._pos is None else _ptr(self._pos),
                                                 int(self._qn.shape[0]), int(chunk_target),
-                                                int(gqa_group), 0 if naive else PLAN_TREE_ONLY,
+                                                int(gqa_group), _plan_flags(naive, tensor_pack),
                                                 ctypes.byref(h)))
         self.handle = h
         self._stats = None
@@ -172,7 +177,7 @@ class Plan:
         return self._stats
 
     def rebuild(self, parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
-                query_pos=None, naive: bool = True):
+                query_pos=None, naive: bool = True, tensor_pack: bool = False):
         """deft_plan_rebuild: plan a new tree into this plan, keeping its device
         allocation and staging buffer; upload() again before the next step.
         On error (DeftError) the plan is unchanged."""
@@ -181,7 +186,7 @@ class Plan:
         _check("deft_plan_rebuild", load().deft_plan_rebuild(
             self.handle, _ptr(par), _ptr(ln), int(par.shape[0]), _ptr(qn),
             None if pos is None else _ptr(pos), int(qn.shape[0]), int(chunk_target), int(gqa_group),
-            0 if naive else PLAN_TREE_ONLY))
+            _plan_flags(naive, tensor_pack)))
         self._parent, self._len, self._qn, self._pos = par, ln, qn, pos
         self._stats = None
 
@@ -305,8 +310,8 @@ def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, buf
 
 
 def deft_plan(parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
-              query_pos=None, naive: bool = True) -> Plan:
-    return Plan(parent, node_len, query_node, chunk_target, gqa_group, query_pos, naive)
+              query_pos=None, naive: bool = True, tensor_pack: bool = False) -> Plan:
+    return Plan(parent, node_len, query_node, chunk_target, gqa_group, query_pos, naive, tensor_pack)
 
 
 def deft_check_pages(node_len, node_page_off, page_id, num_pages: int, page_size: int = 16) -> int:

@@ -225,12 +225,13 @@ int build_host(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
                const int32_t *query_pos, int32_t num_queries, int32_t chunk_target, int32_t gqa_group,
                int32_t flags, deft_plan_t *p)
 {
-    if (flags & ~(int32_t)DEFT_PLAN_TREE_ONLY)
+    if (flags & ~(int32_t)(DEFT_PLAN_TREE_ONLY | DEFT_PLAN_TENSOR_PACK))
         return DEFT_EINVAL;
     int rc;
     try {
         rc = deft::build_plan(parent, node_len, num_nodes, query_node, query_pos, num_queries,
-                              chunk_target, gqa_group, (flags & DEFT_PLAN_TREE_ONLY) == 0, p);
+                              chunk_target, gqa_group, (flags & DEFT_PLAN_TREE_ONLY) == 0,
+                              (flags & DEFT_PLAN_TENSOR_PACK) != 0, p);
     } catch (const std::bad_alloc &) {
         rc = DEFT_ENOMEM;
     }

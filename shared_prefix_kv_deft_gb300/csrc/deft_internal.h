@@ -29,6 +29,9 @@ constexpr int kFmaItemRows = 8;        // rows per CUDA-core item of a chunk und
 constexpr int kMmaMaxRows = 128;       // rows per tensor-core item (one MMA N extent)
 constexpr int kMmaMinRows = 16;        // a chunk with this many rows goes to the tensor path
 constexpr int kSharedTokensPerRow = 16;  // long-chunk rule for shared nodes (see planner.cpp)
+// Tensor packing: pieces of at least two 128-token tensor-core tiles, so that
+// a tile lies in one segment and its pages go by one box per operand half.
+constexpr int kTensorPiece = 256;
 // Work-queue slots: tensor-core buckets 0-3, CUDA-core buckets 4-8, the
 // CUDA-core fallback for tensor-core chunks 9-13.
 constexpr int kQueueSlots = 14;
@@ -245,7 +248,8 @@ namespace deft {
 // planner.cpp
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
-               int32_t chunk_target, int32_t gqa_group, bool with_naive, deft_plan_t *plan);
+               int32_t chunk_target, int32_t gqa_group, bool with_naive, bool tensor_pack,
+               deft_plan_t *plan);
 
 // Workspace of a step (caller memory, or the allocation-free entry point's
 // static array): fp32 partial outputs [slots][Hq][d], then fp32 partial lse
@@ -312,10 +316,12 @@ int prepare_step(const void *q, const void *k_pages, const void *v_pages, const 
 struct LaunchShape {
     int32_t grid;
     int32_t early;   // 1 <= early <= grid
+    int32_t block;   // units of each early CTA's block; -1: about 3/4 of an even share
 };
-inline int32_t static_block(int32_t units, int32_t early)
+inline int32_t static_block(int32_t units, int32_t early, int32_t block = -1)
 {
-    return early > 0 ? (int32_t)((int64_t)units * 3 / (4 * (int64_t)early)) : 0;
+    const int32_t even = early > 0 ? (int32_t)((int64_t)units * 3 / (4 * (int64_t)early)) : 0;
+    return block >= 0 && block < even ? block : even;
 }
 // One CUDA-core launch over `n` items (device triples at `items`), all of row
 // bucket `bucket` (rows <= 2^bucket).

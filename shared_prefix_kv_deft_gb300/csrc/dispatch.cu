@@ -67,7 +67,7 @@ void shape_launches(const double *cost, const int32_t *units, int n, int sms, La
         // rounds take as long with ceil(units / rounds) CTAs.
         const int rounds = (int)((units[i] + g - 1) / g);
         g = (int)((units[i] + rounds - 1) / rounds);
-        out[i] = LaunchShape{g, g};
+        out[i] = LaunchShape{g, g, -1};
         used += g;
     }
     // Leave the last launch at least a quarter of the SMs at the start.
@@ -84,8 +84,37 @@ void shape_launches(const double *cost, const int32_t *units, int n, int sms, La
         --used;
     }
     const int g = std::max(1, std::min((int)units[n - 1], sms));
-    out[n - 1] = LaunchShape{g, std::max(1, std::min(g, sms - used))};
+    out[n - 1] = LaunchShape{g, std::max(1, std::min(g, sms - used)), -1};
 }
+
+namespace {
+
+// The early CTAs' static blocks when the units' costs differ: the first
+// block (items are sorted by cost, largest first) holds no more than 3/4 of
+// an even share of the launch's estimated cost.  Units are item-major,
+// `hkv` per item; unit_cost(i) is item i's cost per unit.
+template <typename F>
+int32_t cost_block(int32_t n_items, int32_t hkv, int32_t early, F unit_cost)
+{
+    double total = 0.0;
+    for (int32_t i = 0; i < n_items; ++i)
+        total += unit_cost(i) * hkv;
+    const double cap = 0.75 * total / std::max(1, early);
+    double acc = 0.0;
+    int32_t s = 0;
+    for (int32_t i = 0; i < n_items; ++i) {
+        const double u = unit_cost(i);
+        for (int32_t h = 0; h < hkv; ++h) {
+            if (acc + u > cap)
+                return s;
+            acc += u;
+            ++s;
+        }
+    }
+    return s;
+}
+
+}  // namespace
 
 int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool use_mma, int32_t family,
                   void *stream, const LaunchTracer &trace)
@@ -93,6 +122,8 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
     const int32_t hkv = a.num_kv_heads;
     Launch ls[14];
     int n = 0;
+    // One tensor-core launch per column bucket: each is built for its
+    // width (stage counts and buffers depend on it).
     if (dp.num_mma_items > 0 && use_mma) {
         for (int b = 0; b < 4; ++b) {
             const int32_t c = hp.mma_bucket_off[b + 1] - hp.mma_bucket_off[b];
@@ -101,7 +132,25 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
                                  (double)hp.mma_bucket_tok[b] * hkv * mma_ns_per_token(b)};
         }
     }
+    // CUDA-core items: one launch per row bucket, or one launch at the
+    // largest bucket present when that costs little more in all (its smaller
+    // items then run at its row count).
     auto add_fma = [&](int kind, const std::array<int32_t, 6> &off, const std::array<int64_t, 5> &tok) {
+        int nb = 0, maxb = 0;
+        double split = 0.0;
+        int64_t all_tok = 0;
+        for (int b = 0; b < 5; ++b)
+            if (off[b + 1] > off[b]) {
+                ++nb;
+                maxb = b;
+                split += (double)tok[b] * hkv * fma_ns_per_token(b);
+                all_tok += tok[b];
+            }
+        const double one = (double)all_tok * hkv * fma_ns_per_token(maxb);
+        if (nb > 1 && one <= 1.3 * split) {
+            ls[n++] = Launch{kind, maxb, 0, off[5], one};
+            return;
+        }
         for (int b = 0; b < 5; ++b) {
             const int32_t c = off[b + 1] - off[b];
             if (c > 0)
@@ -131,6 +180,19 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
         units[i] = ls[i].n * hkv;
     }
     shape_launches(cost, units, n, num_sms(), shape);
+    // Static blocks by cost (a launch's items differ in size: a block of
+    // whole long items would keep its CTA long after the others).
+    for (int i = 0; i < n; ++i) {
+        const Launch &l = ls[i];
+        const std::vector<int32_t> &it = l.kind == 0 ? hp.mma_items : l.kind == 1 ? hp.fma_items : hp.fallback_items;
+        const int32_t G = a.gqa_group;
+        shape[i].block = cost_block(l.n, hkv, shape[i].early, [&](int32_t k) {
+            const int32_t *t = &it[3 * (size_t)(l.off + k)];
+            const int rows = (t[2] - t[1]) * G;
+            const double ns = l.kind == 0 ? mma_ns_per_token(mma_bucket(rows)) : fma_ns_per_token(row_bucket(rows));
+            return (double)hp.chunk_tokens[t[0]] * ns;
+        });
+    }
 
     // Only the step's first launch waits for the stream's earlier work
     // before reading inputs (wait_prior); the rest follow it.

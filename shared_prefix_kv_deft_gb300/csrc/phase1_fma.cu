@@ -1058,7 +1058,8 @@ int launch_one(const AttnArgs &a, const DevPartition &p, const int32_t *items, c
     const int32_t grid = sh.grid < units ? sh.grid : units;
     const int32_t early = sh.early < grid ? sh.early : grid;
     return (int)launch_dependent(phase1_fma_kernel<D, RMAX>, dim3(grid), dim3(C::THREADS), C::alloc, st, a, p,
-                                 items, rmask, rmask_off, direct, units, static_block(units, early), early, queue);
+                                 items, rmask, rmask_off, direct, units, static_block(units, early, sh.block), early,
+                                 queue);
 }
 
 template <int D>

@@ -1127,7 +1127,7 @@ int launch_cols(const AttnArgs &a, const DevPartition &p, const int32_t *items, 
     const int32_t early = sh.early < grid ? sh.early : grid;
     return (int)launch_dependent(phase1_mma_kernel<NPH>, dim3(grid), dim3(kThreadsMma), Smem<NPH>::alloc, st, a, p,
                                  items, reinterpret_cast<const uint4 *>(rmask), rmask_off, units,
-                                 static_block(units, early), early, queue, maps);
+                                 static_block(units, early, sh.block), early, queue, maps);
 }
 
 }  // namespace

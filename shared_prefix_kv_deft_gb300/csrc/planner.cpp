@@ -29,6 +29,20 @@
 //     In-SRAM Online Softmax Merging", is read as "made small", which is what
 //     the abstract's "nearly 100% IO reduction for partial results" says.)
 //   * Nodes with no token or no query on them produce no segment.
+//   * With tensor packing (DEFT_PLAN_TENSOR_PACK, for head_dim 128), the
+//     segments of kMmaMinRows / 4 to kMmaMinRows - 1 rows and more than
+//     chunk_target / 4 tokens (tiny ones pack as above), which would run on
+//     CUDA cores at a cost per token that grows with their rows, are instead
+//     laid side by side: a chunk takes a piece of max(kTensorPiece,
+//     chunk_target / m) tokens from each of the next m such segments
+//     (longest first), m the fewest that bring
+//     the chunk to kMmaMinRows rows (at most kMmaMaxRows), so that it runs
+//     on the tensor cores, each row masked to its own segments.  This is the
+//     Guide's tile of the flattened tree shared by several branches, the
+//     queries of the other branches masked ("Deep Dive", the fused tiling
+//     layout; "Flattened Tree KV Splitting": equal-sized tiles).  Each token
+//     is still read once; a query gets one partial per piece of its
+//     segments.
 #include <algorithm>
 #include <cstring>
 #include <numeric>
@@ -294,7 +308,8 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
 
 int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
-               int32_t chunk_target, int32_t gqa_group, bool with_naive, deft_plan_t *plan)
+               int32_t chunk_target, int32_t gqa_group, bool with_naive, bool tensor_pack,
+               deft_plan_t *plan)
 {
     if (!parent || !node_len || !plan || num_nodes < 1 || num_queries < 0 ||
         (num_queries > 0 && !query_node))
@@ -406,9 +421,23 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
         for (int32_t n = 0; n < N; ++n)
             tokens += node_len[n];
         Builder b(plan->tree, W, tokens / chunk_target + N, tokens / chunk_target + 2 * (int64_t)N);
+        // Segments set aside for tensor packing: tokens [b0, b0 + L) of node
+        // n, `left` of them not yet placed, queries at mask_off in thin_mask.
+        struct Thin {
+            int32_t n, b0, L, left;
+            size_t mask_off;
+        };
+        std::vector<Thin> thin;
+        std::vector<uint64_t> thin_mask;
         // Tokens [b0, b0 + L) of node n, attended by the queries in m (k of them).
         auto emit = [&](int32_t n, int32_t b0, int32_t L, const uint64_t *m, int k) {
             unique_tokens += L;
+            if (tensor_pack && (int64_t)k * gqa_group < kMmaMinRows && (int64_t)k * gqa_group >= kMmaMinRows / 4 &&
+                4 * (int64_t)L > chunk_target) {
+                thin.push_back(Thin{n, b0, L, L, thin_mask.size()});
+                thin_mask.insert(thin_mask.end(), m, m + W);
+                return;
+            }
             if (2 * (int64_t)L <= chunk_target) {
                 // A segment that would add queries to the open chunk (its
                 // rows grow for every token of it) joins only when tiny.
@@ -466,6 +495,49 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
             }
         }
         b.close();
+        // Tensor packing of the thin segments, longest first, so that the
+        // segments of a chunk run out together and the last ones, which may
+        // not reach kMmaMinRows rows together, are the shortest.
+        std::stable_sort(thin.begin(), thin.end(), [](const Thin &x, const Thin &y) { return x.L > y.L; });
+        std::vector<uint64_t> um(W, 0);
+        std::vector<size_t> group;
+        size_t head = 0;
+        while (true) {
+            while (head < thin.size() && thin[head].left == 0)
+                ++head;
+            if (head == thin.size())
+                break;
+            // The next segments with tokens left, until their queries make
+            // kMmaMinRows rows (never more than kMmaMaxRows).
+            group.clear();
+            std::fill(um.begin(), um.end(), 0);
+            int urows = 0;
+            for (size_t i = head; i < thin.size() && (int)group.size() < kMaxSegsPerChunk; ++i) {
+                if (thin[i].left == 0)
+                    continue;
+                const uint64_t *m = &thin_mask[thin[i].mask_off];
+                int k = 0;
+                for (int32_t w = 0; w < W; ++w)
+                    k += __builtin_popcountll(um[w] | m[w]);
+                if (!group.empty() && (int64_t)k * gqa_group > kMmaMaxRows)
+                    break;
+                group.push_back(i);
+                for (int32_t w = 0; w < W; ++w)
+                    um[w] |= m[w];
+                urows = k * gqa_group;
+                if (urows >= kMmaMinRows)
+                    break;
+            }
+            int64_t piece = std::max<int64_t>(kTensorPiece, chunk_target / (int64_t)group.size());
+            piece = piece / kPageSize * kPageSize;
+            for (size_t i : group) {
+                Thin &t = thin[i];
+                const int32_t take = (int32_t)std::min<int64_t>(piece, t.left);
+                b.add_segment(t.n, t.b0 + (t.L - t.left), take, &thin_mask[t.mask_off]);
+                t.left -= take;
+            }
+            b.close();
+        }
     }
     finish_partition(plan->tree, Q, W, gqa_group);
 

@@ -39,7 +39,7 @@ def bits_to_cuda(b: np.ndarray):
 class Case:
     """Device copies of one input set plus its plan."""
 
-    def __init__(self, deft, inp, chunk_target):
+    def __init__(self, deft, inp, chunk_target, tensor_pack=False):
         self.inp, self.spec = inp, inp.spec
         self.q = bits_to_cuda(inp.q_bits)
         self.k = bits_to_cuda(inp.k_pages)
@@ -48,7 +48,7 @@ class Case:
         self.pid = torch.from_numpy(inp.layout.page_id).cuda()
         s = self.spec
         self.plan = deft.Plan(s.parent, s.node_len, s.query_node, chunk_target, s.gqa_group,
-                              query_pos=s.query_pos)
+                              query_pos=s.query_pos, tensor_pack=tensor_pack)
         self.plan.upload()
         self.deft = deft
 
@@ -113,6 +113,25 @@ def test_tree_and_naive_match_oracle(deft, spec, ct):
         out_s, lse_s = case.run(naive=naive, flags=deft.STEP_SEPARATE_MERGE)
         np.testing.assert_array_equal(out_s, out, err_msg=what + " separate merge")
         np.testing.assert_array_equal(lse_s, lse, err_msg=what + " separate merge")
+    assert case.plan.step_status() == 0
+
+
+TENSOR_PACK_SHAPES = [s for s in SMALL if s.head_dim == 128]
+
+
+@pytest.mark.parametrize("spec", TENSOR_PACK_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [16, 256])
+def test_tensor_packed_plans_match_oracle(deft, spec, ct):
+    """Plans built with DEFT_PLAN_TENSOR_PACK (thin segments laid side by
+    side into chunks of >= 16 rows) against the oracle, on both kernel
+    paths."""
+    inp = dense_inputs(spec, seed=ct + 17 + spec.num_nodes)
+    ref, ref_lse = run_oracle(inp)
+    case = Case(deft, inp, ct, tensor_pack=True)
+    out, lse = case.run()
+    assert_parity(out, lse, ref, ref_lse, f"tensor-packed ct={ct}")
+    out, lse = case.run(flags=deft.STEP_CUDA_CORES)
+    assert_parity(out, lse, ref, ref_lse, f"tensor-packed on CUDA cores ct={ct}")
     assert case.plan.step_status() == 0
 
 
@@ -269,24 +288,30 @@ def test_tree_only_plan_gives_the_same_step(deft, cfg):
 # ---------------------------------------------------------------------------
 
 FULL = {2: 256, 3: 256, 4: 256, 5: 256, 6: 256, 1: 64, 7: 256}
+# (config, tensor-packed plan): the plain plans, and the packed ones the
+# benchmark runs at head_dim 128.
+FULL_CASES = [(c, False) for c in sorted(FULL)] + [(c, True) for c in sorted(FULL) if c != 1]
 
 
-@pytest.mark.parametrize("cfg", sorted(FULL))
-def test_full_size_workloads_sampled(deft, cfg):
+@pytest.mark.parametrize("cfg,tp", FULL_CASES)
+def test_full_size_workloads_sampled(deft, cfg, tp):
     spec = W.config(cfg)
     layout = W.paged_layout(spec)
     t = W.make_tensors(spec, layout, device="cuda")
     npo = torch.from_numpy(layout.node_page_off).cuda()
     pid = torch.from_numpy(layout.page_id).cuda()
     plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, FULL[cfg], spec.gqa_group,
-                     query_pos=spec.query_pos)
+                     query_pos=spec.query_pos, tensor_pack=tp)
     plan.upload()
     out, lse = deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
     nout, nlse = deft.deft_naive_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
     torch.cuda.synchronize()
+    assert plan.step_status() == 0
+    # The first and last query and 30 drawn at random (all of them when
+    # there are fewer).
     rng = np.random.default_rng(cfg)
     sample = np.unique(np.concatenate([[0, spec.num_queries - 1],
-                                       rng.choice(spec.num_queries, size=min(6, spec.num_queries),
+                                       rng.choice(spec.num_queries, size=min(30, spec.num_queries),
                                                   replace=False)]))
     ref, ref_lse = oracle.tree_attn(W.bf16_bits(t.q), W.bf16_bits(t.k_pages), W.bf16_bits(t.v_pages),
                                     layout.node_page_off, layout.page_id, layout.page_size,
@@ -447,11 +472,17 @@ def test_every_query_attends_each_of_its_tokens_once(deft, cfg):
     plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, FULL[cfg], spec.gqa_group,
                      query_pos=spec.query_pos)
     plan.upload()
+    packed = deft.Plan(spec.parent, spec.node_len, spec.query_node, FULL[cfg], spec.gqa_group,
+                       query_pos=spec.query_pos, tensor_pack=True, naive=False)
+    packed.upload()
     want = path_token_counts(spec)
-    for fn in (deft.deft_tree_attn, deft.deft_naive_attn):
-        _, lse = fn(t.q, t.k_pages, t.v_pages, npo, pid, plan)
+    runs = [("tree", lambda: deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)),
+            ("naive", lambda: deft.deft_naive_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan)),
+            ("tree, tensor-packed", lambda: deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, packed))]
+    for name, fn in runs:
+        _, lse = fn()
         torch.cuda.synchronize()
         got = np.rint(np.exp(lse.cpu().numpy().astype(np.float64))).astype(np.int64)
         bad = np.argwhere(got != want[:, None])
-        assert bad.size == 0, f"{fn.__name__}: query {bad[0][0]} head {bad[0][1]} attends " \
+        assert bad.size == 0, f"{name}: query {bad[0][0]} head {bad[0][1]} attends " \
                               f"{got[tuple(bad[0])]} tokens, expected {want[bad[0][0]]}"

@@ -70,9 +70,9 @@ def test_plan_validation(parent, node_len, query, ct, g, status):
         assert not h.value
 
 
-def check_plan(spec: W.TreeSpec, chunk_target: int, G: int):
+def check_plan(spec: W.TreeSpec, chunk_target: int, G: int, tensor_pack: bool = False):
     plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, chunk_target, G,
-                     query_pos=spec.query_pos)
+                     query_pos=spec.query_pos, tensor_pack=tensor_pack)
     st = plan.stats
     Q, N = spec.num_queries, spec.num_nodes
     Wd = (Q + 63) // 64
@@ -145,7 +145,9 @@ def check_plan(spec: W.TreeSpec, chunk_target: int, G: int):
             if not naive_part:
                 assert bits(chunk_mask[c]) == qs
                 if nseg > 1:
-                    assert tok <= chunk_limit and nseg <= 256
+                    # Tensor-packed chunks: pieces of up to max(256, limit / nseg) tokens.
+                    limit = max(chunk_limit, 256 * nseg) if tensor_pack else chunk_limit
+                    assert tok <= limit and nseg <= 256
             else:
                 assert tok <= chunk_limit
         # Exactly once: every (query, node on its path, token) in one chunk.
@@ -315,13 +317,15 @@ def test_plan_ex_rejects_unknown_flags():
     qn = np.array([1], np.int32)
     h = ctypes.c_void_p()
     vp = ctypes.c_void_p
-    rc = lib.deft_plan_ex(p.ctypes.data_as(vp), L.ctypes.data_as(vp), 2, qn.ctypes.data_as(vp), None, 1,
-                          64, 1, 2, ctypes.byref(h))
-    assert rc == -1 and not h.value
-    rc = lib.deft_plan_ex(p.ctypes.data_as(vp), L.ctypes.data_as(vp), 2, qn.ctypes.data_as(vp), None, 1,
-                          64, 1, deft.PLAN_TREE_ONLY, ctypes.byref(h))
-    assert rc == 0 and h.value
-    lib.deft_plan_free(h)
+    for bad in (4, 8, 1 << 20):
+        rc = lib.deft_plan_ex(p.ctypes.data_as(vp), L.ctypes.data_as(vp), 2, qn.ctypes.data_as(vp), None, 1,
+                              64, 1, bad, ctypes.byref(h))
+        assert rc == -1 and not h.value
+    for good in (deft.PLAN_TREE_ONLY, deft.PLAN_TENSOR_PACK, deft.PLAN_TREE_ONLY | deft.PLAN_TENSOR_PACK):
+        rc = lib.deft_plan_ex(p.ctypes.data_as(vp), L.ctypes.data_as(vp), 2, qn.ctypes.data_as(vp), None, 1,
+                              64, 1, good, ctypes.byref(h))
+        assert rc == 0 and h.value
+        lib.deft_plan_free(h)
 
 
 REBUILDS = [(2, 4), (4, 7), (7, 1), (1, 3)]
@@ -476,3 +480,51 @@ def test_check_pages_accepts_a_layout_and_rejects_each_bad_table():
     off2 = npo.copy()
     off2[n] = -7
     assert deft.deft_check_pages(z, off2, pid, pages) == 0
+
+
+@pytest.mark.parametrize("spec", RANDOM[:20], ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [1, 16, 100, 512])
+def test_tensor_packed_plan_random_trees(spec, ct):
+    """DEFT_PLAN_TENSOR_PACK keeps every (query, node, token) triple in
+    exactly one chunk that lists the query, with exact segment masks."""
+    check_plan(spec, ct, spec.gqa_group, tensor_pack=True)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 6, 7])
+def test_tensor_packed_plan_workload_shapes(cfg):
+    spec = W.config(cfg)
+    plan = check_plan(spec, 256, spec.gqa_group, tensor_pack=True) if cfg != 5 else \
+        deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, spec.gqa_group, tensor_pack=True)
+    st = plan.stats
+    plain = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, spec.gqa_group)
+    assert st["unique_tokens"] == plain.stats["unique_tokens"] == st["planned_tokens"]
+    # Segments of 4 to 15 rows and more than a quarter chunk no longer run
+    # on CUDA cores, but for a remainder that could not reach 16 rows.
+    G = spec.gqa_group
+    q_off = plan.get("chunk_q_off")
+    fma_chunks = set(plan.get("fma_items").reshape(-1, 3)[:, 0].tolist())
+    seg_off, seg_l = plan.get("chunk_seg_off"), plan.get("seg_tok_len")
+    rows = np.diff(q_off) * G
+    left = sum(int(seg_l[seg_off[c]:seg_off[c + 1]].sum()) for c in fma_chunks
+               if rows[c] >= 4 and (seg_l[seg_off[c]:seg_off[c + 1]] > 64).any())
+    assert left <= 0.02 * st["unique_tokens"] or cfg == 1
+
+
+def test_tensor_pack_rows_and_pieces():
+    """GQA 4, one query per sequence (4 rows): four sequences per chunk, a
+    256-token piece of each, so every chunk reaches 16 rows on the tensor
+    path; one-row segments are left to the CUDA cores."""
+    spec = W.imbalance_tree(leaves=12, control=True, control_len=1024, q_heads=8, kv_heads=2)
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, spec.gqa_group, tensor_pack=True)
+    q_off, seg_off = plan.get("chunk_q_off"), plan.get("chunk_seg_off")
+    seg_l = plan.get("seg_tok_len")
+    assert plan.stats["num_fma_items"] == 0
+    assert plan.stats["num_chunks"] == 3 * 4
+    for c in range(len(q_off) - 1):
+        assert (q_off[c + 1] - q_off[c]) * spec.gqa_group == 16
+        assert (seg_l[seg_off[c]:seg_off[c + 1]] == 256).all()
+    few = W.few_shot_tree(prefix=600, branches=32, branch_len=256, heads=4, head_dim=128)
+    p1 = deft.Plan(few.parent, few.node_len, few.query_node, 256, 1, tensor_pack=True)
+    p0 = deft.Plan(few.parent, few.node_len, few.query_node, 256, 1)
+    for name in ("chunk_seg_off", "seg_node", "seg_tok_len", "fma_items", "mma_items"):
+        np.testing.assert_array_equal(p1.get(name), p0.get(name))

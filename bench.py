@@ -20,6 +20,7 @@ whole job's time per step (max over ranks of the timed region / (K * N)).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -51,7 +52,11 @@ def parse():
     ap.add_argument("--chunk-target", type=int, default=256)
     ap.add_argument("--impl", choices=["deft", "reference"], default="deft")
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the naive, e2e and CPU-baseline legs")
+                    help="skip the naive, e2e, CPU-baseline and per-workload legs")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-workload entries (configs 1-7) of the line")
+    ap.add_argument("--shard", choices=["replicas", "heads"], default="replicas",
+                    help="N > 1: independent replicas of the step, or one step split by KV head")
     ap.add_argument("--tensor-pack", type=int, default=-1,
                     help="plan with DEFT_PLAN_TENSOR_PACK (1), without (0), or when head_dim is 128 (-1)")
     ap.add_argument("--step-flags", type=int, default=0,
@@ -75,8 +80,9 @@ PROFILE_CASES = {
     "few_shot": lambda: W.config(2),
     # the reasoning tree (4 levels, 128 queries, GQA 32/8)
     "reasoning": lambda: W.config(4),
-    # the imbalance shape with 16 leaves: the 32768-token prefix at 64 rows, split over CTAs
-    "imbalance_16leaves": lambda: W.imbalance_tree(leaves=16),
+    # the imbalance shape with 64 leaves: the 32768-token prefix at 256 rows (two 128-row
+    # blocks reading the same KV), 64 leaves of 64-8192 tokens
+    "imbalance_64leaves": lambda: W.imbalance_tree(leaves=64),
 }
 
 
@@ -158,10 +164,11 @@ def algorithmic_bytes(plan, spec, family="tree"):
             continue
         rows = (items[:, 2] - items[:, 1]) * G
         if kern == 1:
-            groups = {0: np.ones(len(items), bool)}
+            b = (((rows + 1) // 2 + 15) // 16) - 1          # column bucket (16 (b + 1) per warpgroup)
         else:
             b = np.select([rows <= 1, rows <= 2, rows <= 4, rows <= 8], [0, 1, 2, 3], 4)
-            groups = {int(x): b == x for x in np.unique(b)}
+        groups = {int(x): b == x for x in np.unique(b)}
+        groups[-1] = np.ones(len(items), bool)             # every bucket (one launch for all)
         for bucket, sel in groups.items():
             chunks = np.unique(items[sel, 0])
             kv = int(tok[chunks].sum()) * kv_tok
@@ -319,16 +326,17 @@ def time_oracle(oracle, spec, layout, bits, budget_s, threads=0):
                                            f"{reps} run(s), scaled to the full step"
 
 
-def cpu_baseline(spec, layout, bits, budget_s=12.0):
+def cpu_baseline(spec, layout, bits, budget_s=12.0, single_thread=True):
     """Time the oracle, as it stands, on a bounded sample of the workload: on
     all host threads (the value) and on one thread."""
     import oracle
     oracle.load()
     us, sample = time_oracle(oracle, spec, layout, bits, budget_s)
-    us1, sample1 = time_oracle(oracle, spec, layout, bits, budget_s / 2, threads=1)
-    return {"value": us, "unit": "us/step", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": sample,
-            "single_thread": {"value": us1, "unit": "us/step", "cores": 1, "sample": sample1}}
+    out = {"value": us, "unit": "us/step", "cores": oracle.max_threads(), "kind": "oracle", "sample": sample}
+    if single_thread:
+        us1, sample1 = time_oracle(oracle, spec, layout, bits, budget_s / 2, threads=1)
+        out["single_thread"] = {"value": us1, "unit": "us/step", "cores": 1, "sample": sample1}
+    return out
 
 
 def max_over_ranks(x: float, pg, device) -> float:
@@ -391,6 +399,238 @@ def run_reference(args, rank, world):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def head_shard(num_q_heads: int, num_kv_heads: int, rank: int, world: int):
+    """KV heads [k0, k1) and their query heads [q0, q1) of rank `rank` when a
+    step is split by KV head over `world` devices (whole GQA groups, no
+    exchange: every query head reads only its own KV head)."""
+    if num_kv_heads % world:
+        raise ValueError(f"{num_kv_heads} KV heads do not split over {world} ranks")
+    G = num_q_heads // num_kv_heads
+    per = num_kv_heads // world
+    k0, k1 = rank * per, (rank + 1) * per
+    return k0 * G, k1 * G, k0, k1
+
+
+class Runner:
+    """One workload on one device: inputs resident in HBM, a plan, buffers,
+    and the timing legs of the benchmark."""
+
+    def __init__(self, deft, torch, dev, spec, args, pg=None, shard=None):
+        self.deft, self.torch, self.dev, self.args, self.pg = deft, torch, dev, args, pg
+        if shard is not None:
+            # This rank's KV heads and their query heads, the same tree and plan.
+            q0, q1, k0, k1 = shard
+            spec = dataclasses.replace(spec, name=spec.name + f"_kvheads{k0}-{k1}", num_q_heads=q1 - q0,
+                                       num_kv_heads=k1 - k0)
+        self.spec = spec
+        self.layout = W.paged_layout(spec)
+        self.t = W.make_tensors(spec, self.layout, device=dev)
+        self.npo = torch.from_numpy(self.layout.node_page_off).to(dev)
+        self.pid = torch.from_numpy(self.layout.page_id).to(dev)
+        self.tp = tensor_pack(args, spec)
+        self.plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
+                              query_pos=spec.query_pos, tensor_pack=self.tp)
+        self.plan.upload()
+        self.bufs = deft.alloc_buffers(self.plan, spec.num_queries, spec.num_q_heads, spec.head_dim, dev)
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+        self.flush_rd = torch.zeros(2 * l2 // 8, dtype=torch.int64, device=dev)
+        self.stream = torch.cuda.current_stream(dev)
+
+    def flush_l2(self):
+        self.flush.zero_()
+        self.flush_rd.sum()
+
+    def step(self):
+        t = self.t
+        self.deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, self.npo, self.pid, self.plan, bufs=self.bufs,
+                                 flags=self.args.step_flags)
+
+    def naive_step(self):
+        t = self.t
+        self.deft.deft_naive_attn(t.q, t.k_pages, t.v_pages, self.npo, self.pid, self.plan, bufs=self.bufs)
+
+    def barrier(self):
+        self.torch.cuda.synchronize(self.dev)
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def timed(self, fn, n, trace=False):
+        """n steps, each after an L2 flush outside its events; ms per step."""
+        torch, deft = self.torch, self.deft
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        if trace:
+            deft.trace_read()
+            deft.trace_enable(True)
+        self.barrier()
+        w0 = time.time()
+        for i in range(n):
+            self.flush_l2()
+            starts[i].record(self.stream)
+            fn()
+            ends[i].record(self.stream)
+        self.barrier()
+        w1 = time.time()
+        recs = []
+        if trace:
+            deft.trace_enable(False)
+            recs = deft.trace_read()
+        return [s.elapsed_time(e) for s, e in zip(starts, ends)], recs, w0, w1
+
+    def warm(self, n):
+        for _ in range(n):
+            self.flush_l2()
+            self.step()
+        self.torch.cuda.synchronize(self.dev)
+
+    def kernels(self, recs, steps):
+        """Per-kernel durations (library event trace) and algorithmic bytes."""
+        spec, plan = self.spec, self.plan
+        alg = algorithmic_bytes(plan, spec)
+        p2 = phase2_bytes(plan, spec)
+        # A CUDA-core launch whose item count is not its bucket's covers every bucket.
+        fma_items = plan.get("fma_items").reshape(-1, 3)
+        rows = (fma_items[:, 2] - fma_items[:, 1]) * spec.gqa_group
+        fb = np.select([rows <= 1, rows <= 2, rows <= 4, rows <= 8], [0, 1, 2, 3], 4)
+        out = {}
+        for r in recs:
+            if r["kernel"] == "phase2_merge":
+                key, ab = "phase2_merge", p2
+            else:
+                kk = 1 if r["kernel"] == "phase1_mma" else 0
+                key = f'{r["kernel"]}[bucket={r["bucket"]}{",fallback" if r["fallback"] else ""}]'
+                b = r["bucket"]
+                if kk == 0 and not r["fallback"] and int((fb == b).sum()) != r["items"]:
+                    b = -1
+                ab = alg.get((kk, b, r["fallback"]), {}).get("total", 0)
+            k = out.setdefault(key, {"launches": 0, "total_ms": 0.0, "alg_bytes": ab, "items": r["items"]})
+            k["launches"] += 1
+            k["total_ms"] += r["ms"]
+        tot = sum(k["total_ms"] for k in out.values()) or 1.0
+        for k in out.values():
+            k["avg_us"] = k["total_ms"] / k["launches"] * 1e3
+            k["share"] = k["total_ms"] / tot
+            k["achieved_gbs"] = k["alg_bytes"] / (k["avg_us"] * 1e-6) / 1e9 if k["avg_us"] else None
+        return out
+
+    def unique_kv(self):
+        s = self.spec
+        return self.plan.stats["unique_tokens"] * 2 * s.num_kv_heads * s.head_dim * 2
+
+    def naive_kv(self):
+        s = self.spec
+        return self.plan.stats["naive_tokens"] * 2 * s.num_kv_heads * s.head_dim * 2
+
+    def naive_leg(self, n):
+        for _ in range(3):
+            self.naive_step()
+        nms, _, _, _ = self.timed(self.naive_step, n)
+        return statistics.mean(nms) * 1e3
+
+    def e2e_leg(self, n):
+        """End to end through the public API, as a decode loop runs it: the
+        tree planned afresh every step (tree-only, rebuilt into the loop's
+        plan so that its device copy and staging buffer are reused), the plan
+        uploaded, Q copied from pinned host memory, the step run, out + lse
+        copied back to pinned host memory."""
+        torch, deft, spec, t, a = self.torch, self.deft, self.spec, self.t, self.args
+        q_host = t.q.cpu().pin_memory()
+        out_host = torch.empty(self.bufs.out.shape, dtype=self.bufs.out.dtype).pin_memory()
+        lse_host = torch.empty(self.bufs.lse.shape, dtype=self.bufs.lse.dtype).pin_memory()
+        q_dev = torch.empty_like(t.q)
+        times = []
+        p = deft.Plan(spec.parent, spec.node_len, spec.query_node, a.chunk_target, spec.gqa_group,
+                      query_pos=spec.query_pos, naive=False, tensor_pack=self.tp)
+        for i in range(n + 3):
+            self.barrier()
+            t0 = time.perf_counter()
+            p.rebuild(spec.parent, spec.node_len, spec.query_node, a.chunk_target, spec.gqa_group,
+                      query_pos=spec.query_pos, naive=False, tensor_pack=self.tp)
+            p.upload()
+            q_dev.copy_(q_host, non_blocking=True)
+            deft.deft_tree_attn(q_dev, t.k_pages, t.v_pages, self.npo, self.pid, p, bufs=self.bufs)
+            out_host.copy_(self.bufs.out, non_blocking=True)
+            lse_host.copy_(self.bufs.lse, non_blocking=True)
+            torch.cuda.synchronize(self.dev)
+            if i >= 3:
+                times.append(time.perf_counter() - t0)
+        plan_bytes = p.stats["device_bytes"]
+        del p
+        return (statistics.mean(times) * 1e6, int(q_host.numel() * 2 + plan_bytes),
+                int(out_host.numel() * out_host.element_size() + lse_host.numel() * 4))
+
+    def graph_leg(self, n):
+        """The same step captured once into a CUDA graph and replayed."""
+        torch = self.torch
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream(self.dev)
+            side.wait_stream(self.stream)
+            with torch.cuda.stream(side):
+                self.step()
+            self.stream.wait_stream(side)
+            torch.cuda.synchronize(self.dev)
+            with torch.cuda.graph(g):
+                self.step()
+            for _ in range(3):
+                self.flush_l2()
+                g.replay()
+            gms, _, _, _ = self.timed(g.replay, n)
+            return {"us_per_step": statistics.mean(gms) * 1e3, "us_per_step_median": statistics.median(gms) * 1e3,
+                    "steps": n}
+        except Exception as e:   # report, do not fail the bench line
+            return {"error": str(e).splitlines()[0][:200]}
+
+
+def roofline_of(kernels, ms_per_step, unique_kv, hbm_peak, peak_kind, cfg):
+    """Whole step against the unique-KV roofline, and the dominant kernel's
+    own fraction (its event window overlaps the other phase-1 launches, which
+    share the SMs with it: an SM-share-limited figure)."""
+    dom_name = max(kernels, key=lambda n: kernels[n]["total_ms"]) if kernels else None
+    dom = kernels.get(dom_name, {})
+    step_gbs = unique_kv / (ms_per_step * 1e-3) / 1e9
+    return {"bound": "hbm", "kernel": dom_name, "achieved": dom.get("achieved_gbs"), "peak": hbm_peak,
+            "unit": "GB/s", "frac": (dom.get("achieved_gbs") or 0) / hbm_peak,
+            "traffic": ncu_traffic(dom_name, cfg) if dom_name else None,
+            "peak_source": f"{peak_kind} HBM copy bandwidth",
+            "alg_bytes_per_launch": dom.get("alg_bytes"), "avg_launch_us": dom.get("avg_us"),
+            "kernel_frac_note": "the dominant launch's algorithmic bytes over its own event window; the "
+                                "phase-1 launches run concurrently and share the SMs, so this is an "
+                                "SM-share-limited figure, not the chip's",
+            "whole_step": {"achieved": step_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": step_gbs / hbm_peak,
+                           "bytes": "unique KV bytes per step / step time"}}
+
+
+def measure_config(deft, torch, dev, cfg, args, hbm_peak, peak_kind, steps, warmup, oracle_budget):
+    """The sweep entry of one workload: device time, whole-step roofline,
+    dominant kernel, naive form, e2e and the oracle on the host cores."""
+    r = Runner(deft, torch, dev, W.config(cfg), args)
+    r.warm(warmup)
+    ms, _, _, _ = r.timed(r.step, steps)
+    _, recs, _, _ = r.timed(r.step, max(3, steps // 4), trace=True)
+    kernels = r.kernels(recs, steps)
+    med = statistics.median(ms)
+    roof = roofline_of(kernels, med, r.unique_kv(), hbm_peak, peak_kind, cfg)
+    e2e_us, _, _ = r.e2e_leg(max(3, steps // 4))
+    entry = {"workload": r.spec.name, "chunk_target": args.chunk_target, "tensor_pack": r.tp,
+             "us_per_step_median": med * 1e3, "us_per_step_p10": float(np.percentile(ms, 10)) * 1e3,
+             "us_per_step_p90": float(np.percentile(ms, 90)) * 1e3, "steps": steps,
+             "unique_kv_bytes": r.unique_kv(), "frac_of_measured_hbm": roof["whole_step"]["frac"],
+             "whole_step_roofline": roof["whole_step"],
+             "dominant_kernel": {"name": roof["kernel"], "avg_us": roof["avg_launch_us"],
+                                 "frac_sm_share_limited": roof["frac"]},
+             "naive_us_per_step": r.naive_leg(max(3, steps // 2)), "e2e_us_per_step": e2e_us}
+    if oracle_budget > 0:
+        cb = cpu_baseline(r.spec, r.layout, host_inputs(r.spec, r.layout, r.t), budget_s=oracle_budget,
+                          single_thread=False)
+        entry["oracle_us_per_step"] = cb["value"]
+        entry["oracle_cores"] = cb["cores"]
+    del r
+    torch.cuda.empty_cache()
+    return entry
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -411,199 +651,85 @@ def main():
         pg = dist
 
     spec = W.config(args.config)
-    layout = W.paged_layout(spec)
-    t = W.make_tensors(spec, layout, device=dev)
-    npo = torch.from_numpy(layout.node_page_off).to(dev)
-    pid = torch.from_numpy(layout.page_id).to(dev)
-    tp = tensor_pack(args, spec)
-    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
-                     query_pos=spec.query_pos, tensor_pack=tp)
-    plan.upload()
-    bufs = deft.alloc_buffers(plan, spec.num_queries, spec.num_q_heads, spec.head_dim, dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
-    flush_rd = torch.zeros(2 * l2 // 8, dtype=torch.int64, device=dev)
-
-    def flush_l2():
-        flush.zero_()
-        flush_rd.sum()
-    stream = torch.cuda.current_stream(dev)
-
-    def step():
-        deft.deft_tree_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs, flags=args.step_flags)
-
-    def barrier():
-        torch.cuda.synchronize(dev)
-        if pg is not None:
-            pg.barrier()
-
-    def timed(fn, n, trace=False):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        if trace:
-            deft.trace_read()
-            deft.trace_enable(True)
-        barrier()
-        w0 = time.time()
-        for i in range(n):
-            flush_l2()
-            starts[i].record(stream)
-            fn()
-            ends[i].record(stream)
-        barrier()
-        w1 = time.time()
-        recs = []
-        if trace:
-            deft.trace_enable(False)
-            recs = deft.trace_read()
-        ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-        return ms, recs, w0, w1
-
-    for _ in range(args.warmup):
-        flush_l2()
-        step()
+    shard = head_shard(spec.num_q_heads, spec.num_kv_heads, rank, world) \
+        if args.shard == "heads" and world > 1 else None
+    run = Runner(deft, torch, dev, spec, args, pg=pg, shard=shard)
+    spec = run.spec
+    run.warm(args.warmup)
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ms, _, w0, w1 = timed(step, args.steps)                # timed region: the value
+    ms, _, w0, w1 = run.timed(run.step, args.steps)          # timed region: the value
     clocks = sampler.summary(w0, w1)
     sampler.stop()
-    tms, recs, _, _ = timed(step, args.steps, trace=True)  # per-kernel durations
+    _, recs, _, _ = run.timed(run.step, args.steps, trace=True)  # per-kernel durations
     elapsed = max_over_ranks(sum(ms), pg, dev)
     ms_per_step = elapsed / args.steps
-    value_us = job_us_per_step(ms_per_step, world)
+    # Replicas: the job finishes `world` steps in the slowest rank's time.
+    # Head shards: the ranks share one step, done when the slowest is.
+    value_us = job_us_per_step(ms_per_step, world) if shard is None else ms_per_step * 1e3
 
-    st = plan.stats
+    st = run.plan.stats
     d, Hq, Hkv, Q = spec.head_dim, spec.num_q_heads, spec.num_kv_heads, spec.num_queries
-    unique_kv = st["unique_tokens"] * 2 * Hkv * d * 2
-    naive_kv = st["naive_tokens"] * 2 * Hkv * d * 2
     hbm_peak, peak_kind = measured_peaks()
-
-    # Per-kernel durations and algorithmic bytes.
-    alg = algorithmic_bytes(plan, spec)
-    p2 = phase2_bytes(plan, spec)
+    kernels = run.kernels(recs, args.steps)
     per_step = len(recs) // max(1, args.steps)
-    kernels = {}
-    for r in recs:
-        if r["kernel"] == "phase2_merge":
-            key, ab = "phase2_merge", p2
-        else:
-            kk = 1 if r["kernel"] == "phase1_mma" else 0
-            key = f'{r["kernel"]}[bucket={r["bucket"]}{",fallback" if r["fallback"] else ""}]'
-            ab = alg.get((kk, r["bucket"] if kk == 0 else 0, r["fallback"]), {}).get("total", 0)
-        k = kernels.setdefault(key, {"launches": 0, "total_ms": 0.0, "alg_bytes": ab,
-                                     "items": r["items"]})
-        k["launches"] += 1
-        k["total_ms"] += r["ms"]
-    tot_ms = sum(k["total_ms"] for k in kernels.values()) or 1.0
-    for k in kernels.values():
-        k["avg_us"] = k["total_ms"] / k["launches"] * 1e3
-        k["share"] = k["total_ms"] / tot_ms
-        k["achieved_gbs"] = k["alg_bytes"] / (k["avg_us"] * 1e-6) / 1e9 if k["avg_us"] else None
-    dom_name = max(kernels, key=lambda n: kernels[n]["total_ms"]) if kernels else None
-    dom = kernels.get(dom_name, {})
-    traffic = ncu_traffic(dom_name, args.config) if dom_name else None
-    roofline = {"bound": "hbm", "kernel": dom_name,
-                "achieved": dom.get("achieved_gbs"), "peak": hbm_peak, "unit": "GB/s",
-                "frac": (dom.get("achieved_gbs") or 0) / hbm_peak, "traffic": traffic,
-                "peak_source": f"{peak_kind} HBM copy bandwidth",
-                "alg_bytes_per_launch": dom.get("alg_bytes"),
-                "avg_launch_us": dom.get("avg_us")}
-    step_gbs = unique_kv / (ms_per_step * 1e-3) / 1e9
+    roofline = roofline_of(kernels, ms_per_step, run.unique_kv(), hbm_peak, peak_kind, args.config)
+    step_gbs = roofline["whole_step"]["achieved"]
 
     line = {
         "metric": METRIC, "value": value_us, "unit": "us/step", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": False, "scaling": "weak" if shard is None else "strong",
+        "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16 Q/K/V, random-init; no dataset)",
-        "config": {"workload": spec.name, "config_index": args.config, "global_batch": Q * world,
+        "config": {"workload": spec.name, "config_index": args.config, "global_batch": Q * (1 if shard else world),
                    "seq_len": int(max(1, st["naive_tokens"] // max(1, Q))),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "chunk_target": args.chunk_target, "tensor_pack": tp, "l2": "flushed between timed steps (2 x L2 memset, then 2 x L2 read: cold, clean)",
+                   "parallelism": ("single GPU" if world == 1 else
+                                   f"kv-head shards x{world}" if shard else f"replicas x{world}"),
+                   "chunk_target": args.chunk_target, "tensor_pack": run.tp,
+                   "l2": "flushed between timed steps (2 x L2 memset, then 2 x L2 read: cold, clean)",
                    "q_heads": Hq, "kv_heads": Hkv, "head_dim": d},
         "us_per_step_median": statistics.median(ms) * 1e3,
         "us_per_step_p10": float(np.percentile(ms, 10)) * 1e3,
         "us_per_step_p90": float(np.percentile(ms, 90)) * 1e3,
-        "unique_kv_bytes": unique_kv, "naive_kv_bytes": naive_kv,
+        "unique_kv_bytes": run.unique_kv(), "naive_kv_bytes": run.naive_kv(),
         "achieved_gbs_vs_unique_kv": step_gbs,
         "frac_of_measured_hbm": step_gbs / hbm_peak, "frac_of_spec_8tbs": step_gbs / SPEC_HBM_GBS,
         "roofline": roofline, "kernels": kernels,
         "gpu_launches": per_step * args.steps,
         "clocks": clocks,
         "plan": {k: st[k] for k in ("num_chunks", "num_segments", "num_slots", "num_fma_items",
-                                    "num_mma_items", "num_fallback_items", "max_chunk_tokens")},
+                                    "num_mma_items", "num_fallback_items", "max_chunk_tokens",
+                                    "num_merge_queries")},
     }
 
     if not args.no_extras:
-        # The same step captured once into a CUDA graph and replayed (launch
-        # overhead of the host call removed; the kernels are the same).
-        try:
-            g = torch.cuda.CUDAGraph()
-            side = torch.cuda.Stream(dev)
-            side.wait_stream(stream)
-            with torch.cuda.stream(side):
-                step()   # warm the side stream
-            stream.wait_stream(side)
-            torch.cuda.synchronize(dev)
-            with torch.cuda.graph(g):
-                step()
-            for _ in range(3):
-                flush_l2()
-                g.replay()
-            gms, _, _, _ = timed(g.replay, args.steps)
-            line["cuda_graph"] = {"us_per_step": statistics.mean(gms) * 1e3,
-                                  "us_per_step_median": statistics.median(gms) * 1e3,
-                                  "steps": args.steps}
-        except Exception as e:   # report, do not fail the bench line
-            line["cuda_graph"] = {"error": str(e).splitlines()[0][:200]}
-        # In-run IO comparison: the per-query flash-decoding form.
-        def naive_step():
-            deft.deft_naive_attn(t.q, t.k_pages, t.v_pages, npo, pid, plan, bufs=bufs)
+        line["cuda_graph"] = run.graph_leg(args.steps)
         nk = max(3, min(args.steps, 200))
-        for _ in range(3):
-            naive_step()
-        nms, _, _, _ = timed(naive_step, nk)
-        line["naive"] = {"us_per_step": statistics.mean(nms) * 1e3, "steps": nk,
-                         "kv_bytes": naive_kv,
-                         "speedup_of_tree": statistics.mean(nms) / ms_per_step}
-        # End to end through the public API, as a decode loop runs it: the
-        # tree is planned afresh every step (tree-only, rebuilt into the
-        # loop's plan so that its device copy and staging buffer are reused),
-        # the plan uploaded, Q copied from pinned host memory, the step run,
-        # out + lse copied back to pinned host memory.
-        q_host = t.q.cpu().pin_memory()
-        out_host = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
-        lse_host = torch.empty(bufs.lse.shape, dtype=bufs.lse.dtype).pin_memory()
-        q_dev = torch.empty_like(t.q)
-        ek = max(3, min(args.steps, 200))
-        e2e_t = []
-        p = deft.Plan(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
-                      query_pos=spec.query_pos, naive=False, tensor_pack=tp)
-        for i in range(ek + 3):
-            barrier()
-            t0 = time.perf_counter()
-            p.rebuild(spec.parent, spec.node_len, spec.query_node, args.chunk_target, spec.gqa_group,
-                      query_pos=spec.query_pos, naive=False, tensor_pack=tp)
-            p.upload()
-            q_dev.copy_(q_host, non_blocking=True)
-            deft.deft_tree_attn(q_dev, t.k_pages, t.v_pages, npo, pid, p, bufs=bufs)
-            out_host.copy_(bufs.out, non_blocking=True)
-            lse_host.copy_(bufs.lse, non_blocking=True)
-            torch.cuda.synchronize(dev)
-            if i >= 3:
-                e2e_t.append(time.perf_counter() - t0)
-        plan_bytes = p.stats["device_bytes"]
-        del p
-        e2e_us = max_over_ranks(statistics.mean(e2e_t) * 1e6, pg, dev)
-        line["e2e"] = {"value": job_us_per_step(e2e_us * 1e-3, world), "unit": "us/step",
-                       "h2d_bytes_per_step": int(q_host.numel() * 2 + plan_bytes),
-                       "d2h_bytes_per_step": int(out_host.numel() * out_host.element_size()
-                                                 + lse_host.numel() * 4),
+        nus = run.naive_leg(nk)
+        line["naive"] = {"us_per_step": nus, "steps": nk, "kv_bytes": run.naive_kv(),
+                         "speedup_of_tree": nus / (ms_per_step * 1e3)}
+        e2e_us, h2d, d2h = run.e2e_leg(max(3, min(args.steps, 200)))
+        e2e_us = max_over_ranks(e2e_us, pg, dev)
+        line["e2e"] = {"value": job_us_per_step(e2e_us * 1e-3, world) if shard is None else e2e_us,
+                       "unit": "us/step", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                        "includes": "host planning (rebuilt into the loop's plan) + plan upload + Q H2D "
                                    "+ step + out/lse D2H",
-                       "steps": ek}
+                       "steps": max(3, min(args.steps, 200))}
         if rank == 0 and world == 1:
-            line["cpu_baseline"] = cpu_baseline(spec, layout, host_inputs(spec, layout, t))
+            line["cpu_baseline"] = cpu_baseline(spec, run.layout, host_inputs(spec, run.layout, run.t))
+        del run
+        torch.cuda.empty_cache()
+        # Every workload, measured in the same process (rank 0 alone).
+        if rank == 0 and world == 1 and not args.no_sweep:
+            sweep = {}
+            for cfg in range(1, 8):
+                big = cfg in (5, 6)
+                sweep[str(cfg)] = measure_config(deft, torch, dev, cfg, args, hbm_peak, peak_kind,
+                                                 steps=min(args.steps, 40 if big else 200),
+                                                 warmup=3, oracle_budget=2.0 if big else 3.0)
+            line["configs"] = sweep
     if rank == 0:
         print(json.dumps(line))
     if pg is not None:

@@ -290,9 +290,11 @@ struct AttnArgs {
     // covered and write disjoint partials, and each waits for its
     // predecessor before it exits, so the merge's single wait covers them all.
     int32_t wait_prior;
-    // 1 when the partition reads each KV line once (the tree partition): the
-    // KV copies then carry an L2 evict-first policy so that the partials stay
-    // in L2; 0 for the naive partition, whose prefix re-reads hit L2.
+    // 1 when the launch reads each KV line once (the tree partition, no
+    // chunk cut into row blocks): the KV copies then carry an L2 evict-first
+    // policy so that the partials stay in L2; 0 for the naive partition,
+    // whose prefix re-reads hit L2, and for launches whose row blocks of a
+    // chunk each read its KV.
     int32_t kv_once;
 };
 

@@ -196,9 +196,22 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
 
     // Only the step's first launch waits for the stream's earlier work
     // before reading inputs (wait_prior); the rest follow it.
+    const int32_t kv_once = a.kv_once;
     for (int i = 0; i < n; ++i) {
         const Launch &l = ls[i];
         int r;
+        // A launch whose items include row blocks of one chunk reads that
+        // chunk's KV once per block: its copies keep the normal L2 policy so
+        // that the later blocks find the KV in L2.
+        {
+            const std::vector<int32_t> &it = l.kind == 0 ? hp.mma_items : l.kind == 1 ? hp.fma_items : hp.fallback_items;
+            bool blocks = false;
+            for (int32_t k = 0; k < l.n && !blocks; ++k) {
+                const int32_t *t = &it[3 * (size_t)(l.off + k)];
+                blocks = t[1] > 0 || t[2] < hp.chunk_q_off[t[0] + 1] - hp.chunk_q_off[t[0]];
+            }
+            a.kv_once = kv_once && !blocks;
+        }
         if (l.kind == 0) {
             const int32_t *it = dp.mma_items + 3 * (size_t)l.off;
             uint32_t *queue = dp.queues + 2 * queue_slot(0, l.bucket);

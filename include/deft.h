@@ -212,6 +212,30 @@ int deft_plan_rebuild(deft_plan_t *plan, const int32_t *parent, const int32_t *n
                       const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
                       int32_t chunk_target, int32_t gqa_group, int32_t flags);
 
+/*
+ * deft_plan_update -- re-plan the plan's tree after its node lengths changed
+ * (DeFT Guide, "Production Engineering and Kernel Deployment Best
+ * Practices": the tree grows and is pruned between decode steps): tokens
+ * appended to nodes, or subtrees pruned by setting their nodes' lengths to
+ * 0 (a pruned node produces no segment; a query whose whole path is pruned
+ * gets out = 0, lse = -inf).  The parents, queries, positions, chunk_target,
+ * gqa_group and flags stay those of the last build; a change to any of them
+ * (new nodes, queries moved) goes through deft_plan_rebuild.
+ *   - The result equals, array for array, what deft_plan_rebuild makes of
+ *     the same tree.  The work done is smaller: the forest check, coverage
+ *     bitsets and DFS order are kept, and the chunks are re-emitted from the
+ *     last point at or before the first changed node (in DFS order) where no
+ *     chunk was open; the query lists, work items and the naive partition
+ *     are recomputed.
+ *   - num_nodes must be the plan's; node_len >= 0 (DEFT_EINVAL); a query
+ *     position beyond its node's new length: DEFT_ERANGE.  On these errors
+ *     the plan is left as it was.  DEFT_ENOMEM leaves it unusable until a
+ *     deft_plan_rebuild (steps on it return DEFT_ESTATE).
+ *   - When a length changed, the plan is marked not uploaded (upload again
+ *     before the next step); when none did, nothing changes.
+ */
+int deft_plan_update(deft_plan_t *plan, const int32_t *node_len, int32_t num_nodes);
+
 /* Plan statistics (host).  DEFT_EINVAL on null arguments. */
 int deft_plan_stats_get(const deft_plan_t *plan, deft_plan_stats *out);
 
@@ -392,6 +416,36 @@ enum { DEFT_K_PHASE1_FMA = 0, DEFT_K_PHASE1_MMA = 1, DEFT_K_PHASE2 = 2 };
 
 int deft_trace_enable(int32_t on);
 int deft_trace_read(deft_trace_record *out, int32_t cap, int32_t *count);
+
+/*
+ * KV page pool with reference counts (DeFT Guide, "Production Engineering
+ * and Kernel Deployment Best Practices", "Paged KV-Cache Compatibility" and
+ * "Tree Pruning Memory Management": the pages of pruned branches go back to
+ * the pool at once, O(1) a page, without copying).  Host bookkeeping only:
+ * the pool hands out page numbers of the caller's k_pages / v_pages, and the
+ * caller builds node_page_off / page_id from them.  A page holds one
+ * reference per owner (deft_pages_retain adds one: a page shared by two page
+ * tables); it is free again when the last is released.
+ *   deft_pages_create: a pool of num_pages pages, all free (page 0 handed out
+ *     first).  DEFT_EINVAL for num_pages < 1.
+ *   deft_pages_alloc: n free pages, each with one reference, into page_ids;
+ *     DEFT_ENOMEM if fewer than n are free (nothing taken).
+ *   deft_pages_retain / deft_pages_release: one more / one less reference on
+ *     each listed page (a page may be listed more than once).  A page id out
+ *     of range: DEFT_ERANGE; a free page, or more releases than references:
+ *     DEFT_ESTATE.  On an error nothing changes.
+ *   deft_pages_free_count: free pages (-1 for a null pool).
+ *   deft_pages_refcount: references of one page (-1 out of range).
+ * Not thread-safe; deft_pages_free(NULL) is a no-op.
+ */
+typedef struct deft_pages_t deft_pages_t;
+int deft_pages_create(int32_t num_pages, deft_pages_t **out);
+void deft_pages_free(deft_pages_t *pool);
+int deft_pages_alloc(deft_pages_t *pool, int32_t n, int32_t *page_ids);
+int deft_pages_retain(deft_pages_t *pool, int32_t n, const int32_t *page_ids);
+int deft_pages_release(deft_pages_t *pool, int32_t n, const int32_t *page_ids);
+int32_t deft_pages_free_count(const deft_pages_t *pool);
+int32_t deft_pages_refcount(const deft_pages_t *pool, int32_t page);
 
 /* Free a plan and its device copy (the caller must ensure no kernel using it
  * is still running).  NULL is a no-op. */

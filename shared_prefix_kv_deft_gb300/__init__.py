@@ -41,6 +41,8 @@ ARRAYS = {
 EXPORTS = ["deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_rebuild", "deft_plan_stats_get",
            "deft_plan_get", "deft_plan_upload", "deft_workspace_bytes", "deft_tree_attn",
            "deft_naive_attn", "deft_tree_attn_ex", "deft_step_status", "deft_check_pages",
+           "deft_plan_update", "deft_pages_create", "deft_pages_free", "deft_pages_alloc",
+           "deft_pages_retain", "deft_pages_release", "deft_pages_free_count", "deft_pages_refcount",
            "deft_plan_free", "deft_status_str", "deft_version", "deft_trace_enable",
            "deft_trace_read", "deft_tree_attn_noalloc"]
 
@@ -105,6 +107,14 @@ def load(path: str = LIB_PATH):
     lib.deft_tree_attn_ex.argtypes = attn[:-1] + [i32, P]
     lib.deft_step_status.argtypes = [P, P, ctypes.POINTER(i32)]
     lib.deft_check_pages.argtypes = [P, i32, P, P, ctypes.c_int64, i32, i32]
+    lib.deft_plan_update.argtypes = [P, P, i32]
+    lib.deft_pages_create.argtypes = [i32, ctypes.POINTER(P)]
+    lib.deft_pages_free.argtypes = [P]
+    lib.deft_pages_free.restype = None
+    for fn in ("deft_pages_alloc", "deft_pages_retain", "deft_pages_release"):
+        getattr(lib, fn).argtypes = [P, i32, P]
+    lib.deft_pages_free_count.argtypes = [P]
+    lib.deft_pages_refcount.argtypes = [P, i32]
     lib.deft_tree_attn_noalloc.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, f32, P, P,
                                            i32, P, P]
     lib.deft_plan_free.argtypes = [P]
@@ -117,7 +127,9 @@ def load(path: str = LIB_PATH):
     for fn in ("deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_rebuild", "deft_plan_stats_get",
                "deft_plan_get", "deft_plan_upload", "deft_tree_attn", "deft_naive_attn", "deft_version",
                "deft_trace_enable", "deft_trace_read", "deft_tree_attn_noalloc", "deft_tree_attn_ex",
-               "deft_step_status", "deft_check_pages"):
+               "deft_step_status", "deft_check_pages", "deft_plan_update", "deft_pages_create",
+               "deft_pages_alloc", "deft_pages_retain", "deft_pages_release", "deft_pages_free_count",
+               "deft_pages_refcount"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -229,6 +241,14 @@ class Plan:
     def workspace_bytes(self, num_q_heads: int, head_dim: int) -> int:
         return int(load().deft_workspace_bytes(self.handle, int(num_q_heads), int(head_dim)))
 
+    def update(self, node_len):
+        """deft_plan_update: the same tree with new node lengths (tokens
+        appended, pruned subtrees at 0); upload() again before the next step."""
+        ln = _i32(node_len)
+        _check("deft_plan_update", load().deft_plan_update(self.handle, _ptr(ln), int(ln.shape[0])))
+        self._len = ln
+        self._stats = None
+
     def step_status(self, stream=None) -> int:
         """deft_step_status: 0, or the code of a kernel wait that ran out in an
         earlier step (the codes are cleared by the call)."""
@@ -312,6 +332,43 @@ def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, buf
 def deft_plan(parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
               query_pos=None, naive: bool = True, tensor_pack: bool = False) -> Plan:
     return Plan(parent, node_len, query_node, chunk_target, gqa_group, query_pos, naive, tensor_pack)
+
+
+class PagePool:
+    """deft_pages_*: a host pool of KV page numbers with reference counts."""
+
+    def __init__(self, num_pages: int):
+        h = ctypes.c_void_p()
+        _check("deft_pages_create", load().deft_pages_create(int(num_pages), ctypes.byref(h)))
+        self.handle = h
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            _lib.deft_pages_free(h)
+            self.handle = None
+
+    def alloc(self, n: int) -> np.ndarray:
+        out = np.zeros(max(int(n), 1), dtype=np.int32)
+        _check("deft_pages_alloc", load().deft_pages_alloc(self.handle, int(n), _ptr(out)))
+        return out[: int(n)]
+
+    def retain(self, ids):
+        ids = _i32(ids)
+        _check("deft_pages_retain", load().deft_pages_retain(self.handle, int(ids.size),
+                                                             _ptr(ids) if ids.size else None))
+
+    def release(self, ids):
+        ids = _i32(ids)
+        _check("deft_pages_release", load().deft_pages_release(self.handle, int(ids.size),
+                                                               _ptr(ids) if ids.size else None))
+
+    @property
+    def free_count(self) -> int:
+        return int(load().deft_pages_free_count(self.handle))
+
+    def refcount(self, page: int) -> int:
+        return int(load().deft_pages_refcount(self.handle, int(page)))
 
 
 def deft_check_pages(node_len, node_page_off, page_id, num_pages: int, page_size: int = 16) -> int:

@@ -62,7 +62,7 @@ int prepare_step(const void *q, const void *k_pages, const void *v_pages, const 
     if ((head_dim != 64 && head_dim != 128) || page_size != kPageSize)
         return DEFT_EUNSUPPORTED;
     const bool naive = (flags & DEFT_STEP_NAIVE) != 0;
-    if (num_q_heads / num_kv_heads != plan->gqa_group || (naive && !plan->has_naive))
+    if (num_q_heads / num_kv_heads != plan->gqa_group || (naive && !plan->has_naive) || plan->broken)
         return DEFT_ESTATE;
     use_mma = mma_supported(head_dim) && !(flags & DEFT_STEP_CUDA_CORES);
     // The CUDA-core kernel holds at most kFmaMaxRows rows per item; one query
@@ -290,6 +290,43 @@ int deft_plan_rebuild(deft_plan_t *plan, const int32_t *parent, const int32_t *n
     plan->naive = std::move(fresh.naive);
     plan->has_naive = fresh.has_naive;
     plan->stats = fresh.stats;
+    plan->in_parent = std::move(fresh.in_parent);
+    plan->in_len = std::move(fresh.in_len);
+    plan->in_qnode = std::move(fresh.in_qnode);
+    plan->in_qpos = std::move(fresh.in_qpos);
+    plan->in_tensor_pack = fresh.in_tensor_pack;
+    plan->own_off = std::move(fresh.own_off);
+    plan->own_q = std::move(fresh.own_q);
+    plan->order_pos = std::move(fresh.order_pos);
+    plan->ckpt = std::move(fresh.ckpt);
+    plan->thin = std::move(fresh.thin);
+    plan->thin_mask = std::move(fresh.thin_mask);
+    plan->uploaded = false;
+    plan->noalloc_image_ok = false;
+    plan->broken = false;
+    return DEFT_OK;
+}
+
+int deft_plan_update(deft_plan_t *plan, const int32_t *node_len, int32_t num_nodes)
+{
+    if (!plan)
+        return DEFT_EINVAL;
+    const std::vector<int32_t> before = plan->in_len;
+    int rc;
+    try {
+        rc = deft::update_plan(plan, node_len, num_nodes);   // checks everything before it changes anything
+    } catch (const std::bad_alloc &) {
+        plan->uploaded = false;
+        plan->broken = true;
+        return DEFT_ENOMEM;
+    }
+    if (rc != DEFT_OK || plan->in_len == before)
+        return rc;   // an error (the plan as it was), or no length changed (its device copy stands)
+    size_t cursor = 0;
+    Layout lt, ln;
+    plan_partition_layout(plan->tree, cursor, lt);
+    plan_partition_layout(plan->naive, cursor, ln);
+    plan->stats.device_bytes = (int64_t)cursor;
     plan->uploaded = false;
     plan->noalloc_image_ok = false;
     return DEFT_OK;
@@ -359,6 +396,8 @@ int deft_plan_upload(deft_plan_t *plan, void *stream)
 {
     if (!plan)
         return DEFT_EINVAL;
+    if (plan->broken)
+        return DEFT_ESTATE;
     size_t cursor = 0;
     Layout lt, ln;
     plan_partition_layout(plan->tree, cursor, lt);

@@ -100,6 +100,20 @@ struct Partition {
     int32_t num_slots() const { return (int32_t)chunk_q.size(); }
 };
 
+// A segment set aside for tensor packing (tokens [b0, b0 + L) of node n; its
+// query mask is entry `mask` of the plan's thin_mask, W words each).
+struct ThinSeg {
+    int32_t n, b0, L, mask;
+};
+// The tree partition's emission state before one DFS position: chunks and
+// segments closed so far, thin segments set aside, tokens emitted, and
+// whether a chunk was open there (only a clean position can be resumed).
+struct EmitCkpt {
+    int32_t chunks, segs, thin;
+    int64_t unique;
+    bool clean;
+};
+
 // Device view of one partition: plain pointers into the plan's device blob,
 // passed to kernels by value.
 struct DevPartition {
@@ -241,6 +255,16 @@ struct deft_plan_t {
     // the capacity is kept across rebuilds).
     std::vector<uint8_t> noalloc_image;
     bool noalloc_image_ok = false;
+    // The tree the plan was built from and the state deft_plan_update
+    // resumes from: the inputs, the queries inside each node (CSR), each
+    // node's DFS position, the emission checkpoints and the thin segments.
+    std::vector<int32_t> in_parent, in_len, in_qnode, in_qpos;   // in_qpos empty: no positions
+    bool in_tensor_pack = false;
+    std::vector<int32_t> own_off, own_q, order_pos;
+    std::vector<deft::EmitCkpt> ckpt;
+    std::vector<deft::ThinSeg> thin;
+    std::vector<uint64_t> thin_mask;
+    bool broken = false;   // an update ran out of memory half way: rebuild before use
 };
 
 namespace deft {
@@ -250,6 +274,10 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
                const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
                int32_t chunk_target, int32_t gqa_group, bool with_naive, bool tensor_pack,
                deft_plan_t *plan);
+// The same plan for new node lengths (same structure, queries and options),
+// resuming the emission at the last clean checkpoint before the first
+// changed node.
+int update_plan(deft_plan_t *plan, const int32_t *node_len, int32_t num_nodes);
 
 // Workspace of a step (caller memory, or the allocation-free entry point's
 // static array): fp32 partial outputs [slots][Hq][d], then fp32 partial lse

@@ -82,6 +82,20 @@ struct Builder {
         p.seg_mask.reserve(segs * W);
         p.chunk_seg_off.push_back(0);
     }
+    // Resumes `part` with its first `chunks` chunks and `segs` segments, no
+    // chunk open (a checkpoint of an earlier build).
+    Builder(Partition &part, int32_t words, int32_t chunks, int32_t segs, bool)
+        : p(part), W(words), cur_mask(words, 0)
+    {
+        p.chunk_seg_off.resize((size_t)chunks + 1);
+        p.chunk_tokens.resize(chunks);
+        p.chunk_mask.resize((size_t)chunks * W);
+        p.seg_node.resize(segs);
+        p.seg_tok_begin.resize(segs);
+        p.seg_tok_len.resize(segs);
+        p.seg_chunk_pos.resize(segs);
+        p.seg_mask.resize((size_t)segs * W);
+    }
     void close()
     {
         if (!open)
@@ -306,247 +320,220 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
 
 }  // namespace
 
-int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
-               const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
-               int32_t chunk_target, int32_t gqa_group, bool with_naive, bool tensor_pack,
-               deft_plan_t *plan)
+namespace {
+
+// The per-query parts of a plan that depend on the node lengths: the
+// queries sitting inside each node (CSR, for the cuts of positioned
+// queries) and the token counts.
+void query_parts(deft_plan_t *plan, int64_t &naive_tokens, int64_t &path_nodes)
 {
-    if (!parent || !node_len || !plan || num_nodes < 1 || num_queries < 0 ||
-        (num_queries > 0 && !query_node))
-        return DEFT_EINVAL;
-    if (chunk_target < 1 || chunk_target > kMaxChunkTarget || gqa_group < 1 || gqa_group > 128)
-        return DEFT_EINVAL;
-    const int32_t N = num_nodes, Q = num_queries;
-    for (int32_t n = 0; n < N; ++n) {
-        if (parent[n] < -1 || parent[n] >= N)
-            return DEFT_ERANGE;
-        if (node_len[n] < 0)
-            return DEFT_EINVAL;
-    }
-    for (int32_t q = 0; q < Q; ++q)
-        if (query_node[q] < 0 || query_node[q] >= N)
-            return DEFT_ERANGE;
-    // A query at position p of its node attends tokens 0..p of it (-1: all).
-    for (int32_t q = 0; q < Q && query_pos; ++q)
-        if (query_pos[q] < -1 || query_pos[q] >= node_len[query_node[q]])
-            return DEFT_ERANGE;
+    const int32_t N = plan->num_nodes, Q = plan->num_queries;
+    const int32_t *parent = plan->in_parent.data(), *node_len = plan->in_len.data();
+    const int32_t *query_node = plan->in_qnode.data();
+    const int32_t *query_pos = plan->in_qpos.empty() ? nullptr : plan->in_qpos.data();
     auto taken = [&](int32_t q, int32_t n) {
         return (query_pos && n == query_node[q] && query_pos[q] >= 0) ? query_pos[q] + 1 : node_len[n];
     };
-
-    // Forest check by colouring: 0 unseen, 1 on the current upward walk, 2 done.
-    {
-        std::vector<uint8_t> colour(N, 0);
-        std::vector<int32_t> walk;
-        for (int32_t n = 0; n < N; ++n) {
-            int32_t cur = n;
-            walk.clear();
-            while (cur != -1 && colour[cur] == 0) {
-                colour[cur] = 1;
-                walk.push_back(cur);
-                cur = parent[cur];
-            }
-            if (cur != -1 && colour[cur] == 1)
-                return DEFT_ECYCLE;
-            for (int32_t x : walk)
-                colour[x] = 2;
-        }
-    }
-
-    const int32_t W = (Q + 63) / 64;
-    plan->num_nodes = N;
-    plan->num_queries = Q;
-    plan->gqa_group = gqa_group;
-    plan->chunk_target = chunk_target;
-    plan->mask_words = W;
-
-    // Coverage bitsets: walk every query's path.
-    plan->cover.assign((size_t)N * W, 0);
-    int64_t naive_tokens = 0, path_nodes = 0;
+    naive_tokens = path_nodes = 0;
     for (int32_t q = 0; q < Q; ++q)
         for (int32_t cur = query_node[q]; cur != -1; cur = parent[cur]) {
-            plan->cover[(size_t)cur * W + q / 64] |= 1ull << (q % 64);
             naive_tokens += taken(q, cur);
             path_nodes += 1;
         }
     // Per node, the queries that sit at a position before its last token
-    // (their part of the node ends there), as CSR.
-    std::vector<int32_t> own_off(N + 1, 0), own_q;
+    // (their part of the node ends there).
+    plan->own_off.assign((size_t)N + 1, 0);
+    plan->own_q.clear();
     if (query_pos) {
         for (int32_t q = 0; q < Q; ++q)
             if (query_pos[q] >= 0 && query_pos[q] + 1 < node_len[query_node[q]])
-                own_off[query_node[q] + 1] += 1;
+                plan->own_off[query_node[q] + 1] += 1;
         for (int32_t n = 0; n < N; ++n)
-            own_off[n + 1] += own_off[n];
-        own_q.resize(own_off[N]);
-        std::vector<int32_t> fill(own_off.begin(), own_off.end() - 1);
+            plan->own_off[n + 1] += plan->own_off[n];
+        plan->own_q.resize(plan->own_off[N]);
+        std::vector<int32_t> fill(plan->own_off.begin(), plan->own_off.end() - 1);
         for (int32_t q = 0; q < Q; ++q)
             if (query_pos[q] >= 0 && query_pos[q] + 1 < node_len[query_node[q]])
-                own_q[fill[query_node[q]]++] = q;
+                plan->own_q[fill[query_node[q]]++] = q;
     }
+}
 
-    // Children lists (ascending ids) and DFS preorder.
-    std::vector<int32_t> child_off(N + 1, 0), child(N > 0 ? N : 1);
-    for (int32_t n = 0; n < N; ++n)
-        if (parent[n] >= 0)
-            child_off[parent[n] + 1] += 1;
-    for (int32_t n = 0; n < N; ++n)
-        child_off[n + 1] += child_off[n];
-    {
-        std::vector<int32_t> fill(child_off.begin(), child_off.end() - 1);
-        for (int32_t n = 0; n < N; ++n)
-            if (parent[n] >= 0)
-                child[fill[parent[n]]++] = n;
-    }
-    plan->order.clear();
-    {
-        std::vector<int32_t> stack;
-        for (int32_t r = N - 1; r >= 0; --r)
-            if (parent[r] == -1)
-                stack.push_back(r);
-        while (!stack.empty()) {
-            int32_t n = stack.back();
-            stack.pop_back();
-            plan->order.push_back(n);
-            for (int32_t i = child_off[n + 1] - 1; i >= child_off[n]; --i)
-                stack.push_back(child[i]);
-        }
-    }
-
-    // DeFT partition.
-    plan->tree = Partition();
+// The tree partition's segments and chunks, emitted from DFS position
+// `start` on (0: from scratch), with the partition, the unique-token count
+// and the tensor-packing list as the checkpoint at `start` recorded them
+// (which must be clean: no chunk open).  Records a checkpoint before every
+// position.
+int64_t emit_tree(deft_plan_t *plan, size_t start)
+{
+    const int32_t N = plan->num_nodes, W = plan->mask_words;
+    const int32_t chunk_target = plan->chunk_target, gqa_group = plan->gqa_group;
+    const bool tensor_pack = plan->in_tensor_pack;
+    const int32_t *node_len = plan->in_len.data();
+    const int32_t *query_pos = plan->in_qpos.empty() ? nullptr : plan->in_qpos.data();
+    const std::vector<int32_t> &own_off = plan->own_off, &own_q = plan->own_q;
+    Partition &part = plan->tree;
+    std::vector<ThinSeg> &thin = plan->thin;
+    std::vector<uint64_t> &thin_mask = plan->thin_mask;
     int64_t unique_tokens = 0;
-    {
-        int64_t tokens = 0;
-        for (int32_t n = 0; n < N; ++n)
-            tokens += node_len[n];
-        Builder b(plan->tree, W, tokens / chunk_target + N, tokens / chunk_target + 2 * (int64_t)N);
-        // Segments set aside for tensor packing: tokens [b0, b0 + L) of node
-        // n, `left` of them not yet placed, queries at mask_off in thin_mask.
-        struct Thin {
-            int32_t n, b0, L, left;
-            size_t mask_off;
-        };
-        std::vector<Thin> thin;
-        std::vector<uint64_t> thin_mask;
-        // Tokens [b0, b0 + L) of node n, attended by the queries in m (k of them).
-        auto emit = [&](int32_t n, int32_t b0, int32_t L, const uint64_t *m, int k) {
-            unique_tokens += L;
-            if (tensor_pack && (int64_t)k * gqa_group < kMmaMinRows && (int64_t)k * gqa_group >= kMmaMinRows / 4 &&
-                4 * (int64_t)L > chunk_target) {
-                thin.push_back(Thin{n, b0, L, L, thin_mask.size()});
-                thin_mask.insert(thin_mask.end(), m, m + W);
-                return;
-            }
-            if (2 * (int64_t)L <= chunk_target) {
-                // A segment that would add queries to the open chunk (its
-                // rows grow for every token of it) joins only when tiny.
-                const bool tiny = 4 * (int64_t)L <= chunk_target;
-                if (b.open && (b.cur_chunk_tokens + L > chunk_target ||
-                               b.cur_chunk_segs >= kMaxSegsPerChunk || (!tiny && !b.nested(m))))
-                    b.close();
-                b.add_segment(n, b0, L, m);
-                return;
-            }
-            b.close();
-            int64_t T = std::max<int64_t>(chunk_target, (int64_t)kSharedTokensPerRow * k * gqa_group);
-            T = (T + kPageSize - 1) / kPageSize * kPageSize;
-            const int64_t pieces = (L + T - 1) / T;
-            int64_t piece = (L + pieces - 1) / pieces;
-            piece = (piece + kPageSize - 1) / kPageSize * kPageSize;
-            for (int64_t s = 0; s < L; s += piece) {
-                b.add_segment(n, (int32_t)(b0 + s), (int32_t)std::min<int64_t>(piece, L - s), m);
+    std::vector<EmitCkpt> &ck = plan->ckpt;
+    int64_t tokens = 0;
+    for (int32_t n = 0; n < N; ++n)
+        tokens += node_len[n];
+    if (start == 0) {
+        part = Partition();
+        thin.clear();
+        thin_mask.clear();
+    } else {
+        unique_tokens = ck[start].unique;
+        thin.resize(ck[start].thin);
+        thin_mask.resize((size_t)ck[start].thin * W);
+    }
+    Builder b = start == 0 ? Builder(part, W, tokens / chunk_target + N, tokens / chunk_target + 2 * (int64_t)N)
+                           : Builder(part, W, ck[start].chunks, ck[start].segs, true);
+    ck.resize((size_t)N + 1);
+    // Tokens [b0, b0 + L) of node n, attended by the queries in m (k of them).
+    auto emit = [&](int32_t n, int32_t b0, int32_t L, const uint64_t *m, int k) {
+        unique_tokens += L;
+        if (tensor_pack && (int64_t)k * gqa_group < kMmaMinRows && (int64_t)k * gqa_group >= kMmaMinRows / 4 &&
+            4 * (int64_t)L > chunk_target) {
+            thin.push_back(ThinSeg{n, b0, L, (int32_t)(thin_mask.size() / W)});
+            thin_mask.insert(thin_mask.end(), m, m + W);
+            return;
+        }
+        if (2 * (int64_t)L <= chunk_target) {
+            // A segment that would add queries to the open chunk (its
+            // rows grow for every token of it) joins only when tiny.
+            const bool tiny = 4 * (int64_t)L <= chunk_target;
+            if (b.open && (b.cur_chunk_tokens + L > chunk_target ||
+                           b.cur_chunk_segs >= kMaxSegsPerChunk || (!tiny && !b.nested(m))))
                 b.close();
-            }
-        };
-        std::vector<int32_t> cuts;
-        std::vector<uint64_t> pm(W, 0);
-        for (int32_t n : plan->order) {
-            const int32_t L = node_len[n];
-            const uint64_t *m = &plan->cover[(size_t)n * W];
-            const int k = popcount_words(m, W);
-            if (L == 0 || k == 0)
-                continue;
-            if (own_off[n] == own_off[n + 1]) {
-                emit(n, 0, L, m, k);
-                continue;
-            }
-            // Queries sitting inside the node cut it where their part ends:
-            // every piece has one query set (the node's, less the queries
-            // whose position lies before the piece).
-            cuts.clear();
-            for (int32_t i = own_off[n]; i < own_off[n + 1]; ++i)
-                cuts.push_back(query_pos[own_q[i]] + 1);
-            std::sort(cuts.begin(), cuts.end());
-            cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
-            cuts.push_back(L);
-            int32_t b0 = 0;
-            for (int32_t e : cuts) {
-                std::copy(m, m + W, pm.begin());
-                for (int32_t i = own_off[n]; i < own_off[n + 1]; ++i) {
-                    const int32_t q = own_q[i];
-                    if (query_pos[q] < b0)
-                        pm[q / 64] &= ~(1ull << (q % 64));
-                }
-                const int kp = popcount_words(pm.data(), W);
-                if (kp > 0)
-                    emit(n, b0, e - b0, pm.data(), kp);
-                b0 = e;
-            }
+            b.add_segment(n, b0, L, m);
+            return;
         }
         b.close();
-        // Tensor packing of the thin segments, longest first, so that the
-        // segments of a chunk run out together and the last ones, which may
-        // not reach kMmaMinRows rows together, are the shortest.
-        std::stable_sort(thin.begin(), thin.end(), [](const Thin &x, const Thin &y) { return x.L > y.L; });
-        std::vector<uint64_t> um(W, 0);
-        std::vector<size_t> group;
-        size_t head = 0;
-        while (true) {
-            while (head < thin.size() && thin[head].left == 0)
-                ++head;
-            if (head == thin.size())
-                break;
-            // The next segments with tokens left, until their queries make
-            // kMmaMinRows rows (never more than kMmaMaxRows).
-            group.clear();
-            std::fill(um.begin(), um.end(), 0);
-            int urows = 0;
-            for (size_t i = head; i < thin.size() && (int)group.size() < kMaxSegsPerChunk; ++i) {
-                if (thin[i].left == 0)
-                    continue;
-                const uint64_t *m = &thin_mask[thin[i].mask_off];
-                int k = 0;
-                for (int32_t w = 0; w < W; ++w)
-                    k += __builtin_popcountll(um[w] | m[w]);
-                if (!group.empty() && (int64_t)k * gqa_group > kMmaMaxRows)
-                    break;
-                group.push_back(i);
-                for (int32_t w = 0; w < W; ++w)
-                    um[w] |= m[w];
-                urows = k * gqa_group;
-                if (urows >= kMmaMinRows)
-                    break;
-            }
-            int64_t piece = std::max<int64_t>(kTensorPiece, chunk_target / (int64_t)group.size());
-            piece = piece / kPageSize * kPageSize;
-            for (size_t i : group) {
-                Thin &t = thin[i];
-                const int32_t take = (int32_t)std::min<int64_t>(piece, t.left);
-                b.add_segment(t.n, t.b0 + (t.L - t.left), take, &thin_mask[t.mask_off]);
-                t.left -= take;
-            }
+        int64_t T = std::max<int64_t>(chunk_target, (int64_t)kSharedTokensPerRow * k * gqa_group);
+        T = (T + kPageSize - 1) / kPageSize * kPageSize;
+        const int64_t pieces = (L + T - 1) / T;
+        int64_t piece = (L + pieces - 1) / pieces;
+        piece = (piece + kPageSize - 1) / kPageSize * kPageSize;
+        for (int64_t s = 0; s < L; s += piece) {
+            b.add_segment(n, (int32_t)(b0 + s), (int32_t)std::min<int64_t>(piece, L - s), m);
             b.close();
         }
+    };
+    auto checkpoint = [&](size_t pos) {
+        ck[pos] = EmitCkpt{(int32_t)part.chunk_tokens.size(), (int32_t)part.seg_node.size(), (int32_t)thin.size(),
+                           unique_tokens, !b.open};
+    };
+    std::vector<int32_t> cuts;
+    std::vector<uint64_t> pm(W, 0);
+    for (size_t pos = start; pos < (size_t)N; ++pos) {
+        checkpoint(pos);
+        const int32_t n = plan->order[pos];
+        const int32_t L = node_len[n];
+        const uint64_t *m = &plan->cover[(size_t)n * W];
+        const int k = popcount_words(m, W);
+        if (L == 0 || k == 0)
+            continue;
+        if (own_off[n] == own_off[n + 1]) {
+            emit(n, 0, L, m, k);
+            continue;
+        }
+        // Queries sitting inside the node cut it where their part ends:
+        // every piece has one query set (the node's, less the queries
+        // whose position lies before the piece).
+        cuts.clear();
+        for (int32_t i = own_off[n]; i < own_off[n + 1]; ++i)
+            cuts.push_back(query_pos[own_q[i]] + 1);
+        std::sort(cuts.begin(), cuts.end());
+        cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
+        cuts.push_back(L);
+        int32_t b0 = 0;
+        for (int32_t e : cuts) {
+            std::copy(m, m + W, pm.begin());
+            for (int32_t i = own_off[n]; i < own_off[n + 1]; ++i) {
+                const int32_t q = own_q[i];
+                if (query_pos[q] < b0)
+                    pm[q / 64] &= ~(1ull << (q % 64));
+            }
+            const int kp = popcount_words(pm.data(), W);
+            if (kp > 0)
+                emit(n, b0, e - b0, pm.data(), kp);
+            b0 = e;
+        }
     }
+    b.close();
+    checkpoint((size_t)N);
+    // Tensor packing of the thin segments, longest first, so that the
+    // segments of a chunk run out together and the last ones, which may
+    // not reach kMmaMinRows rows together, are the shortest.  (The list
+    // keeps emission order for later resumes; the packing walks a sorted
+    // index.)
+    std::vector<size_t> byl(thin.size());
+    std::iota(byl.begin(), byl.end(), (size_t)0);
+    std::stable_sort(byl.begin(), byl.end(), [&](size_t x, size_t y) { return thin[x].L > thin[y].L; });
+    std::vector<int32_t> left(thin.size());
+    for (size_t i = 0; i < thin.size(); ++i)
+        left[i] = thin[i].L;
+    std::vector<uint64_t> um(W, 0);
+    std::vector<size_t> group;
+    size_t head = 0;
+    while (true) {
+        while (head < byl.size() && left[byl[head]] == 0)
+            ++head;
+        if (head == byl.size())
+            break;
+        // The next segments with tokens left, until their queries make
+        // kMmaMinRows rows (never more than kMmaMaxRows).
+        group.clear();
+        std::fill(um.begin(), um.end(), 0);
+        for (size_t h = head; h < byl.size() && (int)group.size() < kMaxSegsPerChunk; ++h) {
+            const size_t i = byl[h];
+            if (left[i] == 0)
+                continue;
+            const uint64_t *m = &thin_mask[(size_t)thin[i].mask * W];
+            int k = 0;
+            for (int32_t w = 0; w < W; ++w)
+                k += __builtin_popcountll(um[w] | m[w]);
+            if (!group.empty() && (int64_t)k * gqa_group > kMmaMaxRows)
+                break;
+            group.push_back(i);
+            for (int32_t w = 0; w < W; ++w)
+                um[w] |= m[w];
+            if ((int64_t)k * gqa_group >= kMmaMinRows)
+                break;
+        }
+        int64_t piece = std::max<int64_t>(kTensorPiece, chunk_target / (int64_t)group.size());
+        piece = piece / kPageSize * kPageSize;
+        for (size_t i : group) {
+            const ThinSeg &t = thin[i];
+            const int32_t take = (int32_t)std::min<int64_t>(piece, left[i]);
+            b.add_segment(t.n, t.b0 + (t.L - left[i]), take, &thin_mask[(size_t)t.mask * W]);
+            left[i] -= take;
+        }
+        b.close();
+    }
+    return unique_tokens;
+}
+
+// Naive partition, query lists of both partitions, work items, statistics.
+void finish_plan(deft_plan_t *plan, int64_t unique_tokens, int64_t naive_tokens, int64_t path_nodes)
+{
+    const int32_t N = plan->num_nodes, Q = plan->num_queries, W = plan->mask_words;
+    const int32_t chunk_target = plan->chunk_target, gqa_group = plan->gqa_group;
+    const int32_t *parent = plan->in_parent.data(), *node_len = plan->in_len.data();
+    const int32_t *query_node = plan->in_qnode.data();
+    const int32_t *query_pos = plan->in_qpos.empty() ? nullptr : plan->in_qpos.data();
+    auto taken = [&](int32_t q, int32_t n) {
+        return (query_pos && n == query_node[q] && query_pos[q] >= 0) ? query_pos[q] + 1 : node_len[n];
+    };
     finish_partition(plan->tree, Q, W, gqa_group);
 
     // Naive partition: each query's path (root first) cut every chunk_target
     // tokens; every chunk serves that one query.  Left empty (no chunk) when
     // the caller will not run it.
     plan->naive = Partition();
-    plan->has_naive = with_naive;
-    if (!with_naive) {
+    if (!plan->has_naive) {
         Builder b(plan->naive, W, 0, 0);
     } else {
         Builder b(plan->naive, W, naive_tokens / chunk_target + Q, naive_tokens / chunk_target + Q + path_nodes);
@@ -605,6 +592,144 @@ int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
     st.num_merge_queries = (int32_t)plan->tree.merge_q.size();
     st.unique_tokens = unique_tokens;
     st.naive_tokens = naive_tokens;
+}
+
+}  // namespace
+
+int build_plan(const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
+               const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,
+               int32_t chunk_target, int32_t gqa_group, bool with_naive, bool tensor_pack,
+               deft_plan_t *plan)
+{
+    if (!parent || !node_len || !plan || num_nodes < 1 || num_queries < 0 ||
+        (num_queries > 0 && !query_node))
+        return DEFT_EINVAL;
+    if (chunk_target < 1 || chunk_target > kMaxChunkTarget || gqa_group < 1 || gqa_group > 128)
+        return DEFT_EINVAL;
+    const int32_t N = num_nodes, Q = num_queries;
+    for (int32_t n = 0; n < N; ++n) {
+        if (parent[n] < -1 || parent[n] >= N)
+            return DEFT_ERANGE;
+        if (node_len[n] < 0)
+            return DEFT_EINVAL;
+    }
+    for (int32_t q = 0; q < Q; ++q)
+        if (query_node[q] < 0 || query_node[q] >= N)
+            return DEFT_ERANGE;
+    // A query at position p of its node attends tokens 0..p of it (-1: all).
+    for (int32_t q = 0; q < Q && query_pos; ++q)
+        if (query_pos[q] < -1 || query_pos[q] >= node_len[query_node[q]])
+            return DEFT_ERANGE;
+
+    // Forest check by colouring: 0 unseen, 1 on the current upward walk, 2 done.
+    {
+        std::vector<uint8_t> colour(N, 0);
+        std::vector<int32_t> walk;
+        for (int32_t n = 0; n < N; ++n) {
+            int32_t cur = n;
+            walk.clear();
+            while (cur != -1 && colour[cur] == 0) {
+                colour[cur] = 1;
+                walk.push_back(cur);
+                cur = parent[cur];
+            }
+            if (cur != -1 && colour[cur] == 1)
+                return DEFT_ECYCLE;
+            for (int32_t x : walk)
+                colour[x] = 2;
+        }
+    }
+
+    const int32_t W = (Q + 63) / 64;
+    plan->num_nodes = N;
+    plan->num_queries = Q;
+    plan->gqa_group = gqa_group;
+    plan->chunk_target = chunk_target;
+    plan->mask_words = W;
+    plan->has_naive = with_naive;
+    plan->in_tensor_pack = tensor_pack;
+    plan->in_parent.assign(parent, parent + N);
+    plan->in_len.assign(node_len, node_len + N);
+    plan->in_qnode.assign(query_node, query_node + Q);
+    if (query_pos)
+        plan->in_qpos.assign(query_pos, query_pos + Q);
+    else
+        plan->in_qpos.clear();
+
+    // Coverage bitsets: walk every query's path.
+    plan->cover.assign((size_t)N * W, 0);
+    for (int32_t q = 0; q < Q; ++q)
+        for (int32_t cur = query_node[q]; cur != -1; cur = parent[cur])
+            plan->cover[(size_t)cur * W + q / 64] |= 1ull << (q % 64);
+    int64_t naive_tokens = 0, path_nodes = 0;
+    query_parts(plan, naive_tokens, path_nodes);
+
+    // Children lists (ascending ids) and DFS preorder.
+    std::vector<int32_t> child_off(N + 1, 0), child(N > 0 ? N : 1);
+    for (int32_t n = 0; n < N; ++n)
+        if (parent[n] >= 0)
+            child_off[parent[n] + 1] += 1;
+    for (int32_t n = 0; n < N; ++n)
+        child_off[n + 1] += child_off[n];
+    {
+        std::vector<int32_t> fill(child_off.begin(), child_off.end() - 1);
+        for (int32_t n = 0; n < N; ++n)
+            if (parent[n] >= 0)
+                child[fill[parent[n]]++] = n;
+    }
+    plan->order.clear();
+    {
+        std::vector<int32_t> stack;
+        for (int32_t r = N - 1; r >= 0; --r)
+            if (parent[r] == -1)
+                stack.push_back(r);
+        while (!stack.empty()) {
+            int32_t n = stack.back();
+            stack.pop_back();
+            plan->order.push_back(n);
+            for (int32_t i = child_off[n + 1] - 1; i >= child_off[n]; --i)
+                stack.push_back(child[i]);
+        }
+    }
+    plan->order_pos.assign(N, 0);
+    for (int32_t i = 0; i < N; ++i)
+        plan->order_pos[plan->order[i]] = i;
+
+    // DeFT partition, then the rest.
+    const int64_t unique_tokens = emit_tree(plan, 0);
+    finish_plan(plan, unique_tokens, naive_tokens, path_nodes);
+    return DEFT_OK;
+}
+
+int update_plan(deft_plan_t *plan, const int32_t *node_len, int32_t num_nodes)
+{
+    if (!plan || !node_len || num_nodes != plan->num_nodes)
+        return DEFT_EINVAL;
+    const int32_t N = num_nodes, Q = plan->num_queries;
+    for (int32_t n = 0; n < N; ++n)
+        if (node_len[n] < 0)
+            return DEFT_EINVAL;
+    const int32_t *query_node = plan->in_qnode.data();
+    for (int32_t q = 0; q < Q && !plan->in_qpos.empty(); ++q)
+        if (plan->in_qpos[q] >= node_len[query_node[q]])
+            return DEFT_ERANGE;
+    // The first changed node in DFS order.
+    size_t first = (size_t)N;
+    for (int32_t n = 0; n < N; ++n)
+        if (node_len[n] != plan->in_len[n])
+            first = std::min(first, (size_t)plan->order_pos[n]);
+    plan->in_len.assign(node_len, node_len + N);
+    if (first == (size_t)N)
+        return DEFT_OK;   // nothing changed
+    // Resume at the last position at or before it where no chunk was open:
+    // everything emitted before it is what a fresh plan emits.
+    size_t start = first;
+    while (start > 0 && !plan->ckpt[start].clean)
+        --start;
+    int64_t naive_tokens = 0, path_nodes = 0;
+    query_parts(plan, naive_tokens, path_nodes);
+    const int64_t unique_tokens = emit_tree(plan, start);
+    finish_plan(plan, unique_tokens, naive_tokens, path_nodes);
     return DEFT_OK;
 }
 

@@ -440,6 +440,47 @@ def test_rebuilt_plan_runs_like_a_fresh_one(deft):
         np.testing.assert_array_equal(lse.cpu().numpy(), lse2.cpu().numpy())
 
 
+def test_updated_plan_runs_like_a_fresh_one(deft):
+    """deft_plan_update across decode steps (tokens appended to branches,
+    then a branch pruned to length 0): each updated plan, uploaded, runs the
+    step of a fresh plan of the same tree bit for bit and matches the oracle
+    on sampled queries."""
+    spec0 = W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4, head_dim=128)
+    extra = 40   # room in every node's pages for the appended tokens
+    grown = W.TreeSpec(spec0.name, spec0.parent, spec0.node_len + extra, spec0.query_node, spec0.num_q_heads,
+                       spec0.num_kv_heads, spec0.head_dim, seed=spec0.seed)
+    layout = W.paged_layout(grown)
+    inp = dense_inputs(grown, seed=3)
+    q, k, v = bits_to_cuda(inp.q_bits), bits_to_cuda(inp.k_pages), bits_to_cuda(inp.v_pages)
+    npo = torch.from_numpy(inp.layout.node_page_off).cuda()
+    pid = torch.from_numpy(inp.layout.page_id).cuda()
+    plan = deft.Plan(spec0.parent, spec0.node_len, spec0.query_node, 128, 1, naive=False)
+    ln = spec0.node_len.astype(np.int32).copy()
+    rng = np.random.default_rng(0)
+    for step in range(4):
+        ln = ln.copy()
+        ln[rng.choice(len(ln), size=3, replace=False)] += 10
+        if step == 3:
+            ln[5] = 0                                   # a branch pruned
+        plan.update(ln)
+        plan.upload()
+        out, lse = deft.deft_tree_attn(q, k, v, npo, pid, plan)
+        fresh = deft.Plan(spec0.parent, ln, spec0.query_node, 128, 1, naive=False)
+        fresh.upload()
+        out2, lse2 = deft.deft_tree_attn(q, k, v, npo, pid, fresh)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.float().cpu().numpy(), out2.float().cpu().numpy())
+        np.testing.assert_array_equal(lse.cpu().numpy(), lse2.cpu().numpy())
+        cur = W.TreeSpec(spec0.name, spec0.parent, ln, spec0.query_node, spec0.num_q_heads, spec0.num_kv_heads,
+                         spec0.head_dim, seed=spec0.seed)
+        ref, ref_lse = oracle.tree_attn(inp.q_bits, inp.k_pages, inp.v_pages, inp.layout.node_page_off,
+                                        inp.layout.page_id, inp.layout.page_size, cur.parent, cur.node_len,
+                                        cur.query_node, cur.num_q_heads, cur.num_kv_heads, cur.head_dim,
+                                        1.0 / math.sqrt(cur.head_dim))
+        assert_parity(out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+                      ref, ref_lse, f"updated plan, step {step}")
+
+
 def path_token_counts(spec):
     """|T(q)| per query from the oracle's own path walk: the tokens query q
     attends (its own node up to its position)."""

@@ -30,7 +30,7 @@ def _built():
 
 def header_functions():
     src = open(os.path.join(ROOT, "include", "deft.h")).read()
-    return sorted(set(re.findall(r"^\s*(?:int|size_t|void|const char \*)\s*(deft_\w+)\s*\(", src, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int32_t|int|size_t|void|const char \*)\s*(deft_\w+)\s*\(", src, re.M)))
 
 
 def test_library_exports_every_declared_symbol():

@@ -180,7 +180,7 @@ int deft_plan_at(const int32_t *parent, const int32_t *node_len, int32_t num_nod
  *   counted.
  *   DEFT_PLAN_TENSOR_PACK: for layers run at head_dim 128 (the tensor-core
  *   path).  Segments whose queries make fewer than 16 rows (queries x
- *   gqa_group) are laid side by side in chunks of 16 to 128 rows, a piece of
+ *   gqa_group) are laid side by side in chunks of 16 to 64 rows, a piece of
  *   about chunk_target / m tokens from each of m consecutive such segments
  *   (the Guide's flattened-tree tile shared by several branches, other
  *   branches' queries masked), so that they run on the tensor cores instead

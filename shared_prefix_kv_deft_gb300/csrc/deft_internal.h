@@ -26,7 +26,7 @@ constexpr int kMaxChunkTarget = 8192;  // bound on the chunk_target argument
 constexpr int kMaxSegsPerChunk = 256;  // packed chunks close at this many segments
 constexpr int kFmaMaxRows = 16;        // rows (queries x GQA group) per CUDA-core item
 constexpr int kFmaItemRows = 8;        // rows per CUDA-core item of a chunk under kMmaMinRows rows
-constexpr int kMmaMaxRows = 128;       // rows per tensor-core item (one MMA N extent)
+constexpr int kMmaMaxRows = 64;        // rows per tensor-core item (at most 32 columns per softmax warpgroup)
 constexpr int kMmaMinRows = 16;        // a chunk with this many rows goes to the tensor path
 constexpr int kSharedTokensPerRow = 16;  // long-chunk rule for shared nodes (see planner.cpp)
 // Tensor packing: pieces of at least two 128-token tensor-core tiles, so that

@@ -173,6 +173,13 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     // it was the launch's last to do so.
     volatile int32_t *qdone = useq + UQ + 1;
 
+    // Warm L2 with this CTA's share of the plan's arrays, the node page
+    // offsets and q, which the metadata and copy warps walk in chains of
+    // dependent loads as soon as the set-up is done.  Prefetches change no
+    // data, so they go out before the wait for the stream's earlier work.
+    prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid, C::THREADS);
+    prefetch_l2_share(a.node_page_off, (size_t)(p.num_nodes + 1) * 4, blockIdx.x, gridDim.x, tid, C::THREADS);
+    prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * D * 2, blockIdx.x, gridDim.x, tid, C::THREADS);
     if (a.wait_prior)
         grid_dep_wait();
     if (tid == 0) {
@@ -516,6 +523,16 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
 #pragma unroll
                 for (int k = 0; k < 2; ++k)
                     meta[st * kTile + lane + 32 * k] = sgk[k] >= 0 ? (uint32_t)seg[768 + sgk[k]] : 0u;
+                // Rows past the chunk's end: zero V so that p.v may run over
+                // all 64 rows (their p is 0; stale shared memory could be NaN).
+                if (nvalid < kTile) {
+                    uint4 *vz = reinterpret_cast<uint4 *>(smem + (vdst - base) + nvalid * kRowBytes);
+                    for (int x = lane; x < (kTile - nvalid) * (D / 8); x += 32)
+                        vz[x] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                // Lane 0's arrival releases the warp's row masks and zeros
+                // (the lanes' own arrivals below may be deferred).
+                __syncwarp();
                 if (lane == 0)
                     tc::mbar_arrive_expect_tx(full, __popc(tp) * 2 * kPageBytes);
                 __syncwarp();
@@ -545,18 +562,12 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         }
                     }
                 }
-                // Rows past the chunk's end: zero V so that p.v may run over
-                // all 64 rows (their p is 0; stale shared memory could be NaN).
-                if (nvalid < kTile) {
-                    uint4 *vz = reinterpret_cast<uint4 *>(smem + (vdst - base) + nvalid * kRowBytes);
-                    for (int x = lane; x < (kTile - nvalid) * CPR; x += 32)
-                        vz[x] = make_uint4(0u, 0u, 0u, 0u);
-                }
-                if (any_cp) {
-                    cp_async_commit();
-                    cp_async_wait<0>();
-                }
-                tc::mbar_arrive(full);
+                // With ragged rows, each lane's arrival waits for its own
+                // copies to land; the warp goes on with the next tile.
+                if (any_cp)
+                    cp_async_mbar_arrive_noinc(full);
+                else
+                    tc::mbar_arrive(full);
             }
             if (!ok)
                 if (!*err) *err = 107;
@@ -570,13 +581,6 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
         }
     } else if (warp < 3 + NCW) {
         // ------------------------------------------------------------ compute
-        // While the first tiles load: warm L2 with the plan's arrays, the
-        // node page offsets and q, which the metadata and copy warps walk in
-        // chains of dependent loads (prefetches hold the issuing warp, so the
-        // idle warps issue them).
-        prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
-        prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
-        prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * D * 2, blockIdx.x, gridDim.x, tid - 96, NCW * 32);
         // Group g takes the CTA's units g, g + NG, ... whole; warp lw of the
         // group takes tokens 8 lw .. 8 lw + 7 of every tile.  Lane layout:
         //   part = lane % NPART   owns the head dims of 16-byte chunks part,

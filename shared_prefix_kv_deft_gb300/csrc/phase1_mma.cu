@@ -1,6 +1,8 @@
 // phase1_mma.cu -- phase-1 partial attention on tcgen05 tensor cores, for
-// work items with 16..128 rows (rows = queries of the item x GQA group) and
-// head_dim 128.
+// work items with 16..64 rows (rows = queries of the item x GQA group) and
+// head_dim 128.  Chunks with more rows are cut into several items, each
+// reading the chunk (the others mostly from L2): a wider item would cost
+// more in its softmax, at 48 or 64 columns a warpgroup, than the re-read.
 //
 // Same result as phase1_fma.cu (DeFT Guide, "Deep Dive": tree-constrained
 // attention, online-softmax tile accumulation; DeFT abstract: KV-Guided
@@ -46,8 +48,8 @@
 //   warp 11         takes the next unit from the queue and passes its number
 //                   to the producers through a shared-memory ring; per
 //                   item, the segment table (positions, page bases, row
-//                   masks); per unit, Q^T (two buffers up to 32 columns a
-//                   warpgroup, so the next unit's Q^T loads meanwhile);
+//                   masks); per unit, Q^T (two buffers, so the next unit's
+//                   Q^T loads meanwhile);
 //   warps 12-15     epilogue: O^T / l out of TMEM (two O buffers) into the
 //                   fp32 partials while the softmax warpgroups go on with
 //                   the next unit.
@@ -92,20 +94,21 @@ struct ItemInfo {
     int32_t pad[2];
 };
 
-// Shared-memory layout for NPH columns per warpgroup (RP = 2 NPH).  Q^T
-// and P^T are sized by RP, which leaves room for a third V stage when
-// NPH <= 32: a V stage is held through its tile's softmax, K only until S.
+// Shared-memory layout for NPH columns per warpgroup (RP = 2 NPH, NPH 16
+// or 32).  Q^T is sized by RP, which leaves room for a third V stage when
+// NPH = 16: a V stage is held through its tile's softmax, K only until S.
 template <int NPH>
 struct Smem {
+    static_assert(NPH == 16 || NPH == 32, "16 or 32 columns a warpgroup");
     static constexpr int RP = 2 * NPH;
     static constexpr int VST = NPH <= 16 ? 3 : 2;                    // V stages (K has 2)
-    static constexpr int QB = NPH <= 32 ? 2 : 1;                     // Q^T buffers
+    static constexpr int QB = 2;                                     // Q^T buffers
     static constexpr uint32_t q_half = RP * 128;                     // one 64-wide half of Q^T
     static constexpr uint32_t k_off = 0;                             // [2] K operands
     static constexpr uint32_t v_off = k_off + 2 * kTileBytes;       // [VST] V operands
     static constexpr uint32_t q_off = v_off + VST * kTileBytes;     // [QB] Q^T: [d half][RP rows][128 B]
     static constexpr uint32_t p_off = q_off + QB * 2 * q_half;      // P^T: [col block][128 tok][128 B]
-    static constexpr uint32_t meta_off = p_off + (RP > 64 ? 2 : 1) * kHalf;  // [4 slots][128] uint4 row masks
+    static constexpr uint32_t meta_off = p_off + kHalf;              // [4 slots][128] uint4 row masks
     static constexpr uint32_t seg_off = meta_off + 4 * kTileTok * 16;  // [2][kSegInts]
     static constexpr uint32_t red_off = seg_off + 2 * kSegInts * 4;  // [wg][warp][64]
     static constexpr uint32_t stat_off = red_off + 2 * 4 * 64 * 4;  // [wg][m, alpha, 1/l, out row][64]
@@ -208,6 +211,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     // The tensor maps are kernel parameters: fetch them before anything else.
     if (warp == 8 && lane < 4)
         tc::prefetch_tmap(lane == 0 ? &maps.k1 : lane == 1 ? &maps.k8 : lane == 2 ? &maps.v1 : &maps.v8);
+    // Then warm L2 with this CTA's share of the plan's arrays, the node page
+    // offsets and q, which the metadata warp and the producers walk in
+    // chains of dependent loads as soon as the set-up is done.  Prefetches
+    // change no data, so they go out before the wait for the stream's
+    // earlier work (a later write to these lines lands in L2 all the same).
+    prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, tid, kThreadsMma);
+    prefetch_l2_share(a.node_page_off, (size_t)(p.num_nodes + 1) * 4, blockIdx.x, gridDim.x, tid, kThreadsMma);
+    prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * kD * 2, blockIdx.x, gridDim.x, tid, kThreadsMma);
     if (a.wait_prior)
         grid_dep_wait();
     if (tid == 0) {
@@ -563,6 +574,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     }
                     const uint32_t full = bar((kv ? kBarFullV : kBarFullK) + st);
                     const uint32_t dst = base + (kv ? L::v_off : L::k_off) + (uint32_t)st * kTileBytes;
+                    // Lane 0's arrival releases the row masks of the whole
+                    // warp (the lanes' own arrivals below may be deferred).
+                    __syncwarp();
                     if (lane == 0)
                         tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
                     __syncwarp();
@@ -613,12 +627,14 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             }
                         }
                     }
-                    if (any_cp) {
-                        cp_async_commit();
-                        cp_async_wait<0>();
-                        tc::fence_proxy_async();
-                    }
-                    tc::mbar_arrive(full);
+                    // With ragged rows, each lane's arrival waits for its own
+                    // copies to land (the producer goes on with the next
+                    // tile meanwhile); the MMA issuer makes them visible to
+                    // the tensor core with a proxy fence after its wait.
+                    if (any_cp)
+                        cp_async_mbar_arrive_noinc(full);
+                    else
+                        tc::mbar_arrive(full);
                     if (t + 1 < ntiles)
                         resolve(t + 1, res);
                 }
@@ -667,6 +683,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         if (nts > 0 && tc::mbar_test(bar(kBarFullK + st), (gs >> 1) & 1) &&
                             (gs < 2 || tc::mbar_test(bar(kBarSFree + b), ((gs - 2) >> 1) & 1))) {
                             tc::fence_after_sync();
+                            tc::fence_proxy_async();   // ragged rows came by cp.async (generic proxy)
                             const uint32_t d_s = tmem + (uint32_t)(b * 128);
     #pragma unroll
                             for (int s = 0; s < 8; ++s) {
@@ -695,6 +712,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             tc::mbar_test(bar(kBarPFull), gp & 1) &&
                             (tp > 0 || ip < 2 || tc::mbar_test(bar(kBarOFree + ob), ((ip - 2) >> 1) & 1))) {
                             tc::fence_after_sync();
+                            tc::fence_proxy_async();
                             const uint32_t d_o = tmem + 256 + (uint32_t)(ob * 128);
     #pragma unroll
                             for (int s = 0; s < 8; ++s) {
@@ -728,13 +746,6 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             // then the buffer is free for the unit two on.
             const int je = tid - 384;
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-            // While the first unit runs: warm L2 with the plan's arrays, the
-            // node page offsets and q, which the metadata warp and the
-            // producers walk in chains of dependent loads (prefetches hold
-            // the issuing warp, so this otherwise idle warpgroup issues them).
-            prefetch_l2_share(p.arrays, p.array_bytes, blockIdx.x, gridDim.x, je, 128);
-            prefetch_l2_share(a.node_page_off, (size_t)p.num_nodes * 4, blockIdx.x, gridDim.x, je, 128);
-            prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * kD * 2, blockIdx.x, gridDim.x, je, 128);
             for (int i = 0;; ++i) {
                 const int ob = i & 1;
                 const bool okw = tc::mbar_wait(bar(kBarEpiFull + ob), (i >> 1) & 1);
@@ -1149,8 +1160,7 @@ int launch_phase1_mma(const AttnArgs &a, const DevPartition &p, const int32_t *i
     switch (bucket) {
     case 0: return launch_cols<16>(a, p, items, rmask, rmask_off, n, queue, shape, maps, st);
     case 1: return launch_cols<32>(a, p, items, rmask, rmask_off, n, queue, shape, maps, st);
-    case 2: return launch_cols<48>(a, p, items, rmask, rmask_off, n, queue, shape, maps, st);
-    default: return launch_cols<64>(a, p, items, rmask, rmask_off, n, queue, shape, maps, st);
+    default: return (int)cudaErrorInvalidValue;   // items have at most kMmaMaxRows = 64 rows
     }
 }
 

@@ -96,10 +96,59 @@ struct Builder {
         p.seg_chunk_pos.resize(segs);
         p.seg_mask.resize((size_t)segs * W);
     }
+    // When some whole page of the open chunk sits at a position that is not
+    // a multiple of kPageSize (after another segment's partial page), lays
+    // the whole pages first: each segment's page-aligned part in order, then
+    // the tokens before and after those parts.  The phase-1 kernels copy a
+    // whole page at an aligned position with one bulk or tensor copy, the
+    // rest row by row.  A chunk's result does not depend on the order of its
+    // tokens.  Skipped when the chunk would pass kMaxSegsPerChunk segments.
+    void realign()
+    {
+        const size_t s0 = p.chunk_seg_off.back(), s1 = p.seg_node.size();
+        struct Rec { int32_t node, begin, len; size_t src; };
+        std::vector<Rec> whole, rest;
+        bool moved = false;
+        for (size_t s = s0; s < s1; ++s) {
+            const int32_t n = p.seg_node[s], b = p.seg_tok_begin[s], L = p.seg_tok_len[s];
+            const int32_t h = std::min(L, (kPageSize - b % kPageSize) % kPageSize);
+            const int32_t w = (L - h) / kPageSize * kPageSize;
+            if (w == 0) {
+                rest.push_back({n, b, L, s});
+                continue;
+            }
+            if (h > 0)
+                rest.push_back({n, b, h, s});
+            whole.push_back({n, b + h, w, s});
+            if (L - h - w > 0)
+                rest.push_back({n, b + h + w, L - h - w, s});
+            moved = moved || (p.seg_chunk_pos[s] + h) % kPageSize != 0;
+        }
+        if (!moved || whole.size() + rest.size() > (size_t)kMaxSegsPerChunk)
+            return;
+        std::vector<uint64_t> masks(p.seg_mask.begin() + (std::ptrdiff_t)(s0 * W), p.seg_mask.end());
+        p.seg_node.resize(s0);
+        p.seg_tok_begin.resize(s0);
+        p.seg_tok_len.resize(s0);
+        p.seg_chunk_pos.resize(s0);
+        p.seg_mask.resize(s0 * W);
+        int32_t pos = 0;
+        for (const std::vector<Rec> *v : {&whole, &rest})
+            for (const Rec &r : *v) {
+                p.seg_node.push_back(r.node);
+                p.seg_tok_begin.push_back(r.begin);
+                p.seg_tok_len.push_back(r.len);
+                p.seg_chunk_pos.push_back(pos);
+                const uint64_t *m = &masks[(r.src - s0) * W];
+                p.seg_mask.insert(p.seg_mask.end(), m, m + W);
+                pos += r.len;
+            }
+    }
     void close()
     {
         if (!open)
             return;
+        realign();
         p.chunk_seg_off.push_back((int32_t)p.seg_node.size());
         p.chunk_tokens.push_back(cur_chunk_tokens);
         p.chunk_mask.insert(p.chunk_mask.end(), cur_mask.begin(), cur_mask.end());

@@ -124,10 +124,16 @@ def check_plan(spec: W.TreeSpec, chunk_target: int, G: int, tensor_pack: bool = 
             union = set()
             nseg = seg_off[c + 1] - seg_off[c]
             assert nseg >= 1
+            nodes = set()
             for s in range(seg_off[c], seg_off[c + 1]):
                 n, b, L = int(seg_node[s]), int(seg_b[s]), int(seg_l[s])
                 assert L > 0 and 0 <= b and b + L <= spec.node_len[n]
+                # A whole page (aligned in its node) sits at an aligned
+                # position of the chunk: one copy moves it.
+                if b % 16 == 0 and L >= 16:
+                    assert tok % 16 == 0, f"chunk {c}: page of node {n} at position {tok}"
                 tok += L
+                nodes.add(n)
                 if naive_part:
                     sq = qs
                 else:
@@ -144,9 +150,11 @@ def check_plan(spec: W.TreeSpec, chunk_target: int, G: int, tensor_pack: bool = 
             assert union == set(qs)
             if not naive_part:
                 assert bits(chunk_mask[c]) == qs
-                if nseg > 1:
-                    # Tensor-packed chunks: pieces of up to max(256, limit / nseg) tokens.
-                    limit = max(chunk_limit, 256 * nseg) if tensor_pack else chunk_limit
+                if len(nodes) > 1:
+                    # Chunks of several nodes: short nodes up to the chunk
+                    # target, or tensor-packed pieces of up to
+                    # max(256, limit / nodes) tokens.
+                    limit = max(chunk_limit, 256 * len(nodes)) if tensor_pack else chunk_limit
                     assert tok <= limit and nseg <= 256
             else:
                 assert tok <= chunk_limit

@@ -140,6 +140,28 @@ __device__ __forceinline__ void grid_dep_launch()
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
+// Whether every unit of a launch's work queue has been handed out already
+// (queued units: n_units less the early CTAs' blocks, `queued_from`).  Reads
+// the counter once without taking a unit; a stale value only sends the CTA
+// on to the normal path.  A CTA that starts after the launch's early ones
+// checks this before its set-up and, with nothing left, leaves at once.
+__device__ __forceinline__ bool queue_drained(const uint32_t *queue, int32_t n_units, int32_t queued_from)
+{
+    const uint32_t taken = *reinterpret_cast<const volatile uint32_t *>(queue);
+    return (int64_t)taken >= (int64_t)n_units - queued_from;
+}
+
+// queue_done for a CTA leaving before its set-up: the launch's last CTA to
+// count itself resets the queue and waits for the launch before this one.
+__device__ __forceinline__ void queue_done_idle(uint32_t *queue)
+{
+    if (atomicAdd(queue + 1, 1u) == gridDim.x - 1) {
+        queue[0] = 0u;
+        queue[1] = 0u;
+        grid_dep_wait();
+    }
+}
+
 __device__ __forceinline__ void cp_async_commit()
 {
     asm volatile("cp.async.commit_group;\n" ::);

@@ -91,10 +91,10 @@ struct Partition {
     // mma_items are sorted by column bucket b: each of the two softmax
     // warpgroups of an item holds NPH = 16 (b + 1) query rows; bucket b is
     // items [off[b], off[b+1]).
-    std::array<int32_t, 5> mma_bucket_off{};
+    std::array<int32_t, 3> mma_bucket_off{};
     // KV tokens of each bucket's items (chunk tokens summed over the items).
     std::array<int64_t, 5> fma_bucket_tok{}, fallback_bucket_tok{};
-    std::array<int64_t, 4> mma_bucket_tok{};
+    std::array<int64_t, 2> mma_bucket_tok{};
     int32_t num_chunks() const { return (int32_t)chunk_tokens.size(); }
     int32_t num_segments() const { return (int32_t)seg_node.size(); }
     int32_t num_slots() const { return (int32_t)chunk_q.size(); }
@@ -386,6 +386,25 @@ inline int row_bucket(int rows) { return rows <= 1 ? 0 : rows <= 2 ? 1 : rows <=
 // warpgroups share the rows; each takes a multiple of 16, at most 64).
 inline int mma_half_cols(int rows) { return (((rows + 1) / 2) + 15) & ~15; }
 inline int mma_bucket(int rows) { return mma_half_cols(rows) / 16 - 1; }
+// Estimated SM time per KV token and KV head (ns, with every SM streaming):
+// CUDA-core items by row bucket (up to 2 rows the kernel streams at the
+// memory rate; above, the per-row FMA work sets the pace), tensor-core items
+// by column bucket (the softmax over the item's columns grows with them).
+inline double fma_ns_per_token(int bucket)
+{
+    static const double ns[5] = {10.0, 12.0, 16.0, 32.0, 56.0};
+    return ns[bucket];
+}
+inline double mma_ns_per_token(int bucket)
+{
+    static const double ns[2] = {14.0, 18.0};
+    return ns[bucket];
+}
+// Buckets whose launches cost little more as one launch at the widest of
+// them (estimated SM time at most kCollapse times that of separate
+// launches) run as one: each launch pays its own start on every SM, and
+// launches of different widths cannot share their work.
+constexpr double kCollapse = 1.3;
 // The merge launch over `nq` queries: queries[i], or i when queries is null.
 int launch_phase2(const AttnArgs &a, const DevPartition &p, const int32_t *queries, int32_t nq, void *stream);
 bool mma_supported(int32_t head_dim);

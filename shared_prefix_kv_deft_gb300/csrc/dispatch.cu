@@ -8,7 +8,8 @@
 // launch but the last gets a share of the SMs in proportion to its estimated
 // cost, and the last, the costliest, gets the rest plus one CTA for each SM
 // the others will leave; those extra CTAs start as the others finish and
-// take units from the last launch's work queue.  Each launch has its own
+// take units from the last launch's work queue.  When the others are small
+// the costliest goes first instead (no extra CTAs).  Each launch has its own
 // queue (two words in the plan's device memory, zero between launches).
 #include <cuda_runtime.h>
 
@@ -28,21 +29,6 @@ struct Launch {
     int32_t n;     // items
     double cost;   // estimated SM time (KV tokens x KV heads x time per token)
 };
-
-// Estimated SM time per KV token and KV head (ns, with every SM streaming):
-// CUDA-core items by row bucket (up to 2 rows the kernel streams at the
-// memory rate; above, the per-row FMA work sets the pace), tensor-core items
-// by column bucket (the softmax over the item's columns grows with them).
-double fma_ns_per_token(int bucket)
-{
-    static const double ns[5] = {10.0, 12.0, 16.0, 32.0, 56.0};
-    return ns[bucket];
-}
-double mma_ns_per_token(int bucket)
-{
-    static const double ns[4] = {14.0, 18.0, 22.0, 28.0};
-    return ns[bucket];
-}
 
 }  // namespace
 
@@ -125,7 +111,7 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
     // One tensor-core launch per column bucket: each is built for its
     // width (stage counts and buffers depend on it).
     if (dp.num_mma_items > 0 && use_mma) {
-        for (int b = 0; b < 4; ++b) {
+        for (int b = 0; b < 2; ++b) {
             const int32_t c = hp.mma_bucket_off[b + 1] - hp.mma_bucket_off[b];
             if (c > 0)
                 ls[n++] = Launch{0, b, hp.mma_bucket_off[b], c,
@@ -147,7 +133,7 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
                 all_tok += tok[b];
             }
         const double one = (double)all_tok * hkv * fma_ns_per_token(maxb);
-        if (nb > 1 && one <= 1.3 * split) {
+        if (nb > 1 && one <= kCollapse * split) {
             ls[n++] = Launch{kind, maxb, 0, off[5], one};
             return;
         }
@@ -180,16 +166,32 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
         units[i] = ls[i].n * hkv;
     }
     shape_launches(cost, units, n, num_sms(), shape);
+    // When the other launches are small (under a tenth of the estimated SM
+    // time), the costliest goes first instead, on every SM but theirs: each
+    // launch ahead of it would hold back its start by the launch latency,
+    // which costs more than the few SMs those launches free later give.
+    if (n > 1) {
+        double others = 0.0;
+        int32_t used = 0;
+        for (int i = 0; i + 1 < n; ++i) {
+            others += cost[i];
+            used += shape[i].grid;
+        }
+        if (others < 0.1 * (others + cost[n - 1])) {
+            std::rotate(ls, ls + n - 1, ls + n);
+            std::rotate(shape, shape + n - 1, shape + n);
+            const int32_t g = std::max(1, std::min(units[n - 1], num_sms() - used));
+            shape[0] = LaunchShape{g, g, -1};
+        }
+    }
     // Static blocks by cost (a launch's items differ in size: a block of
     // whole long items would keep its CTA long after the others).
     for (int i = 0; i < n; ++i) {
         const Launch &l = ls[i];
         const std::vector<int32_t> &it = l.kind == 0 ? hp.mma_items : l.kind == 1 ? hp.fma_items : hp.fallback_items;
-        const int32_t G = a.gqa_group;
         shape[i].block = cost_block(l.n, hkv, shape[i].early, [&](int32_t k) {
             const int32_t *t = &it[3 * (size_t)(l.off + k)];
-            const int rows = (t[2] - t[1]) * G;
-            const double ns = l.kind == 0 ? mma_ns_per_token(mma_bucket(rows)) : fma_ns_per_token(row_bucket(rows));
+            const double ns = l.kind == 0 ? mma_ns_per_token(l.bucket) : fma_ns_per_token(l.bucket);
             return (double)hp.chunk_tokens[t[0]] * ns;
         });
     }

@@ -182,6 +182,13 @@ phase1_fma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
     prefetch_l2_share(a.q, (size_t)p.num_queries * Hq * D * 2, blockIdx.x, gridDim.x, tid, C::THREADS);
     if (a.wait_prior)
         grid_dep_wait();
+    // A CTA that starts late, when the queue has nothing left, leaves now.
+    if ((int)blockIdx.x >= early &&
+        __syncthreads_or(tid == 0 && queue_drained(queue, n_units, early * static_units))) {
+        if (tid == 0)
+            queue_done_idle(queue);
+        return;
+    }
     if (tid == 0) {
         grid_dep_launch();
         for (int s = 0; s < ST; ++s) {

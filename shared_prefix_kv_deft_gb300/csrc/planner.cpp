@@ -274,6 +274,19 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
             fb.push_back({c, b, std::min(k, b + perf), tok * (std::min(k, b + perf) - b),
                           row_bucket((std::min(k, b + perf) - b) * G)});
     }
+    // Tensor-core items of both widths run as one launch at 32 columns a
+    // warpgroup when that costs little more (kCollapse); their row masks are
+    // then laid out for that width.
+    {
+        double tok[2] = {0.0, 0.0};
+        for (const Item &it : mma)
+            tok[it.bucket] += (double)p.chunk_tokens[it.c];
+        const double split = tok[0] * mma_ns_per_token(0) + tok[1] * mma_ns_per_token(1);
+        const double one = (tok[0] + tok[1]) * mma_ns_per_token(1);
+        if (tok[0] > 0.0 && tok[1] > 0.0 && one <= kCollapse * split)
+            for (Item &it : mma)
+                it.bucket = 1;
+    }
     // Largest first, so the hardware block scheduler starts the long items
     // early (a longest-processing-time order).
     auto by_cost = [](const Item &x, const Item &y) {
@@ -327,7 +340,7 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     p.mma_rmask.clear();
     p.mma_rmask_off.assign(1, 0);
     for (const Item &it : mma) {
-        const int32_t rows = (it.e - it.b) * G, nph = mma_half_cols(rows);
+        const int32_t rows = (it.e - it.b) * G, nph = 16 * (it.bucket + 1);
         for (int32_t s = p.chunk_seg_off[it.c]; s < p.chunk_seg_off[it.c + 1]; ++s) {
             uint32_t w[4] = {0, 0, 0, 0};
             for (int32_t r = 0; r < rows; ++r) {

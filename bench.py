@@ -493,6 +493,11 @@ class Runner:
         fma_items = plan.get("fma_items").reshape(-1, 3)
         rows = (fma_items[:, 2] - fma_items[:, 1]) * spec.gqa_group
         fb = np.select([rows <= 1, rows <= 2, rows <= 4, rows <= 8], [0, 1, 2, 3], 4)
+        # Likewise a tensor-core launch whose item count is not its width's
+        # (the planner ran both widths as one launch).
+        mma_items = plan.get("mma_items").reshape(-1, 3)
+        mrows = (mma_items[:, 2] - mma_items[:, 1]) * spec.gqa_group
+        mb = (((mrows + 1) // 2 + 15) // 16) - 1
         out = {}
         for r in recs:
             if r["kernel"] == "phase2_merge":
@@ -502,6 +507,8 @@ class Runner:
                 key = f'{r["kernel"]}[bucket={r["bucket"]}{",fallback" if r["fallback"] else ""}]'
                 b = r["bucket"]
                 if kk == 0 and not r["fallback"] and int((fb == b).sum()) != r["items"]:
+                    b = -1
+                if kk == 1 and int((mb == b).sum()) != r["items"]:
                     b = -1
                 ab = alg.get((kk, b, r["fallback"]), {}).get("total", 0)
             k = out.setdefault(key, {"launches": 0, "total_ms": 0.0, "alg_bytes": ab, "items": r["items"]})

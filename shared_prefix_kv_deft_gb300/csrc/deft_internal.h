@@ -364,7 +364,7 @@ int launch_phase1_fma(const AttnArgs &a, const DevPartition &p, const int32_t *i
 // Streaming multiprocessors of the current device.
 int num_sms();
 // Shares `sms` SMs among n concurrent launches of estimated costs cost[i]
-// and units[i] units each (dispatch.cu).
+// and units[i] units each, the costliest last in the arrays (dispatch.cu).
 void shape_launches(const double *cost, const int32_t *units, int n, int sms, LaunchShape *out);
 // One tensor-core launch over `n` items of column bucket `bucket` (its rows
 // all go to the partials).

@@ -5,12 +5,10 @@
 // Every launch is a programmatic dependent of the one before and starts its
 // CTAs as soon as that one's CTAs are all running, so the phase-1 launches
 // run concurrently.  They share the SMs (one persistent CTA per SM): every
-// launch but the last gets a share of the SMs in proportion to its estimated
-// cost, and the last, the costliest, gets the rest plus one CTA for each SM
-// the others will leave; those extra CTAs start as the others finish and
-// take units from the last launch's work queue.  When the others are small
-// the costliest goes first instead (no extra CTAs).  Each launch has its own
-// queue (two words in the plan's device memory, zero between launches).
+// launch but the costliest gets a share of the SMs in proportion to its
+// estimated cost, and the costliest, launched first, gets the rest.  Each
+// launch has its own work queue (two words in the plan's device memory,
+// zero between launches).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -32,8 +30,9 @@ struct Launch {
 
 }  // namespace
 
-// SM shares of the step's phase-1 launches, in launch order (the costliest
-// last): grid and early CTAs of each.
+// SM shares of the step's phase-1 launches, the costliest last in `cost`
+// and `units` (it is launched first): grid and early CTAs of each.  Every
+// CTA of a launch starts with the step (grid = early).
 void shape_launches(const double *cost, const int32_t *units, int n, int sms, LaunchShape *out)
 {
     if (n <= 0)
@@ -43,9 +42,9 @@ void shape_launches(const double *cost, const int32_t *units, int n, int sms, La
         total += cost[i];
     int used = 0;
     for (int i = 0; i + 1 < n; ++i) {
-        // A quarter over the proportional share: a launch that finishes
-        // early hands its SMs to the last launch, one that finishes late
-        // is the step's tail.
+        // A quarter over the proportional share: the costliest launch can
+        // take no units of the others, so one of them finishing late is the
+        // step's tail.
         const double share = total > 0.0 ? 1.25 * sms * cost[i] / total : 1.0;
         int g = (int)std::ceil(share);
         g = std::max(1, std::min({g, (int)units[i], sms}));
@@ -56,7 +55,7 @@ void shape_launches(const double *cost, const int32_t *units, int n, int sms, La
         out[i] = LaunchShape{g, g, -1};
         used += g;
     }
-    // Leave the last launch at least a quarter of the SMs at the start.
+    // Leave the costliest launch at least a quarter of the SMs.
     const int cap = std::max(n - 1, sms - std::max(1, sms / 4));
     while (used > cap) {
         int j = 0;
@@ -69,8 +68,8 @@ void shape_launches(const double *cost, const int32_t *units, int n, int sms, La
         out[j].early = out[j].grid;
         --used;
     }
-    const int g = std::max(1, std::min((int)units[n - 1], sms));
-    out[n - 1] = LaunchShape{g, std::max(1, std::min(g, sms - used)), -1};
+    const int g = std::max(1, std::min((int)units[n - 1], sms - used));
+    out[n - 1] = LaunchShape{g, g, -1};
 }
 
 namespace {
@@ -150,7 +149,7 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
         add_fma(2, hp.fallback_bucket_off, hp.fallback_bucket_tok);
     if (dp.num_fma_items > 0)
         add_fma(1, hp.fma_bucket_off, hp.fma_bucket_tok);
-    // The costliest launch goes last: its CTAs fill the SMs the others leave.
+    // Shares are computed with the costliest launch last.
     if (n > 1) {
         int j = 0;
         for (int i = 1; i < n; ++i)
@@ -166,23 +165,13 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
         units[i] = ls[i].n * hkv;
     }
     shape_launches(cost, units, n, num_sms(), shape);
-    // When the other launches are small (under a tenth of the estimated SM
-    // time), the costliest goes first instead, on every SM but theirs: each
-    // launch ahead of it would hold back its start by the launch latency,
-    // which costs more than the few SMs those launches free later give.
+    // The costliest launch then goes first: each launch ahead of it would
+    // hold back its start by the launch latency (~2.5-3.5 us).  (Launched
+    // last, with extra CTAs for the SMs the others free, it mostly found its
+    // queue drained by the time they started: few-shot tree 50.4 -> 49.2 us.)
     if (n > 1) {
-        double others = 0.0;
-        int32_t used = 0;
-        for (int i = 0; i + 1 < n; ++i) {
-            others += cost[i];
-            used += shape[i].grid;
-        }
-        if (others < 0.1 * (others + cost[n - 1])) {
-            std::rotate(ls, ls + n - 1, ls + n);
-            std::rotate(shape, shape + n - 1, shape + n);
-            const int32_t g = std::max(1, std::min(units[n - 1], num_sms() - used));
-            shape[0] = LaunchShape{g, g, -1};
-        }
+        std::rotate(ls, ls + n - 1, ls + n);
+        std::rotate(shape, shape + n - 1, shape + n);
     }
     // Static blocks by cost (a launch's items differ in size: a block of
     // whole long items would keep its CTA long after the others).

@@ -116,6 +116,44 @@ def test_tree_and_naive_match_oracle(deft, spec, ct):
     assert case.plan.step_status() == 0
 
 
+DIRECT_CASES = [
+    # every query's path is one CUDA-core chunk: no merge launch at all
+    ("all", W.imbalance_tree(leaves=12, control=True, control_len=150, q_heads=8, kv_heads=2), 256),
+    # a mix of single-chunk paths and paths through shared nodes
+    ("some", W.random_tree(1, max_nodes=16, max_len=90, max_queries=12), 256),
+    ("some_gqa", W.random_tree(116, max_nodes=20, max_len=200, max_queries=40, q_heads=8, kv_heads=2,
+                               head_dim=128), 64),
+    # every path crosses the shared prefix: every query merged
+    ("none", W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4, head_dim=128), 256),
+]
+
+
+@pytest.mark.parametrize("which,spec,ct", DIRECT_CASES, ids=[c[0] for c in DIRECT_CASES])
+def test_direct_rows_for_all_some_and_no_queries(deft, which, spec, ct):
+    """Queries whose whole path is one CUDA-core chunk get their rows from
+    phase 1 (the merge of one partial is the identity); the merge launch
+    takes the others and is left out when there are none.  Against the
+    oracle, and bitwise equal to merging every query in phase 2."""
+    inp = dense_inputs(spec, seed=7 + ct)
+    ref, ref_lse = run_oracle(inp)
+    case = Case(deft, inp, ct)
+    merged = case.plan.stats["num_merge_queries"]
+    Q = spec.num_queries
+    assert {"all": merged == 0, "some": 0 < merged < Q, "some_gqa": 0 < merged < Q,
+            "none": merged == Q}[which], (which, merged, Q)
+    deft.trace_read()
+    deft.trace_enable(True)
+    out, lse = case.run()
+    deft.trace_enable(False)
+    launches = [r["kernel"] for r in deft.trace_read()]
+    assert launches.count("phase2_merge") == (0 if merged == 0 else 1), launches
+    assert_parity(out, lse, ref, ref_lse, f"direct rows ({which})")
+    out_s, lse_s = case.run(flags=deft.STEP_SEPARATE_MERGE)
+    np.testing.assert_array_equal(out_s, out)
+    np.testing.assert_array_equal(lse_s, lse)
+    assert case.plan.step_status() == 0
+
+
 TENSOR_PACK_SHAPES = [s for s in SMALL if s.head_dim == 128]
 
 

@@ -848,11 +848,11 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             }
         };
         int gseq = 0;
-        // Unit -1 is a dry run of one tile and a unit's end, made while the
-        // first tile loads: it runs the same instructions on whatever TMEM
-        // and shared memory hold, with no waits, signals or global stores,
-        // so that the instruction fetches of this code are not paid again
-        // on the real first tile.
+        // Unit -1 is a dry run of one tile (and, at 32 columns, a unit's
+        // end), made while the first tile loads: it runs the same
+        // instructions on whatever TMEM and shared memory hold, with no
+        // waits, signals or global stores, so that the instruction fetches
+        // of this code are not paid again on the real first tile.
         for (int i = -1;; ++i) {
             const bool dry = i < 0;
             const int ub = i & 1, ob = i & 1;
@@ -981,6 +981,15 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
                 if (j == 0 && !dry)
                     tc::mbar_arrive(bar(kBarPFull));
+            }
+            // At 16 columns the dry run stops here: the unit-end code's
+            // first fetch then overlaps the first unit's last tiles, which
+            // measured faster than fetching it before the first tile (few-
+            // shot tree 49.4 -> 48.4 us); at 32 columns the full dry unit
+            // measured faster (speculative forest 132.2 -> 130.8 us).
+            if (dry && NPH == 16) {
+                gseq = 0;
+                continue;
             }
             // The unit's last P.V, then O / l for this warpgroup's rows.
             if (ok && !dry) {

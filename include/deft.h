@@ -368,7 +368,8 @@ int deft_check_pages(const int32_t *node_len, int32_t num_nodes, const int32_t *
  * takes the same inputs and outputs as deft_tree_attn but no workspace, and
  * the plan need not be uploaded: the plan's tree arrays are copied, with one
  * cudaMemcpyAsync on `stream` from a host image the plan keeps (pageable
- * memory: CUDA returns from that copy once it has staged the bytes), into
+ * memory: CUDA may wait for the stream's earlier work before it stages the
+ * bytes, and returns once they are staged), into
  * one static device array of DEFT_NOALLOC_SCRATCH_BYTES (64 MiB) that every
  * GPU loading the library holds until the process exits; the partials live
  * there too.  It calls no cudaMalloc, cudaFree or other allocating routine.

@@ -103,11 +103,15 @@ struct Builder {
     // whole page at an aligned position with one bulk or tensor copy, the
     // rest row by row.  A chunk's result does not depend on the order of its
     // tokens.  Skipped when the chunk would pass kMaxSegsPerChunk segments.
+    // realign's scratch, kept across chunks.
+    struct Rec { int32_t node, begin, len; size_t src; };
+    std::vector<Rec> whole, rest;
+    std::vector<uint64_t> masks;
     void realign()
     {
         const size_t s0 = p.chunk_seg_off.back(), s1 = p.seg_node.size();
-        struct Rec { int32_t node, begin, len; size_t src; };
-        std::vector<Rec> whole, rest;
+        whole.clear();
+        rest.clear();
         bool moved = false;
         for (size_t s = s0; s < s1; ++s) {
             const int32_t n = p.seg_node[s], b = p.seg_tok_begin[s], L = p.seg_tok_len[s];
@@ -126,7 +130,7 @@ struct Builder {
         }
         if (!moved || whole.size() + rest.size() > (size_t)kMaxSegsPerChunk)
             return;
-        std::vector<uint64_t> masks(p.seg_mask.begin() + (std::ptrdiff_t)(s0 * W), p.seg_mask.end());
+        masks.assign(p.seg_mask.begin() + (std::ptrdiff_t)(s0 * W), p.seg_mask.end());
         p.seg_node.resize(s0);
         p.seg_tok_begin.resize(s0);
         p.seg_tok_len.resize(s0);
@@ -195,22 +199,29 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
                 p.chunk_q.push_back(w * 64 + __builtin_ctzll(bits));
         p.chunk_q_off.push_back((int32_t)p.chunk_q.size());
     }
-    // Local masks: bit k of segment s = the chunk's k-th query sees s.
+    // Local masks: bit k of segment s = the chunk's k-th query sees s.  A
+    // segment's queries are among its chunk's, so each set bit of its
+    // global mask maps to a local index (loc, filled per chunk).
     p.seg_lmask_off.assign(1, 0);
     p.seg_lmask.clear();
-    for (int32_t c = 0; c < C; ++c) {
-        const int32_t q0 = p.chunk_q_off[c], nq = p.chunk_q_off[c + 1] - q0;
-        const int32_t words = (nq + 31) / 32;
-        for (int32_t s = p.chunk_seg_off[c]; s < p.chunk_seg_off[c + 1]; ++s) {
-            const uint64_t *m = &p.seg_mask[(size_t)s * W];
-            const size_t at = p.seg_lmask.size();
-            p.seg_lmask.resize(at + words, 0u);
-            for (int32_t k = 0; k < nq; ++k) {
-                const int32_t q = p.chunk_q[q0 + k];
-                if ((m[q / 64] >> (q % 64)) & 1ull)
-                    p.seg_lmask[at + k / 32] |= 1u << (k % 32);
+    {
+        std::vector<int32_t> loc(num_queries > 0 ? num_queries : 1);
+        for (int32_t c = 0; c < C; ++c) {
+            const int32_t q0 = p.chunk_q_off[c], nq = p.chunk_q_off[c + 1] - q0;
+            const int32_t words = (nq + 31) / 32;
+            for (int32_t k = 0; k < nq; ++k)
+                loc[p.chunk_q[q0 + k]] = k;
+            for (int32_t s = p.chunk_seg_off[c]; s < p.chunk_seg_off[c + 1]; ++s) {
+                const uint64_t *m = &p.seg_mask[(size_t)s * W];
+                const size_t at = p.seg_lmask.size();
+                p.seg_lmask.resize(at + words, 0u);
+                for (int32_t w = 0; w < W; ++w)
+                    for (uint64_t bits = m[w]; bits; bits &= bits - 1) {
+                        const int32_t k = loc[w * 64 + __builtin_ctzll(bits)];
+                        p.seg_lmask[at + k / 32] |= 1u << (k % 32);
+                    }
+                p.seg_lmask_off.push_back((int32_t)p.seg_lmask.size());
             }
-            p.seg_lmask_off.push_back((int32_t)p.seg_lmask.size());
         }
     }
     // Per-query slot CSR, slots in chunk order.
@@ -318,20 +329,32 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
 
     // Row masks per (item, segment): row r of an item is its query
     // b + r / G, present in segment s when s's query mask has that bit.
-    auto qbit = [&](int32_t s, int32_t k) -> uint32_t {
-        return (p.seg_lmask[p.seg_lmask_off[s] + k / 32] >> (k % 32)) & 1u;
+    // qbits: local bits b .. b + n - 1 of segment s (n <= 64);
+    // row_bits: those queries' rows, G bits each (at most 64 rows).
+    auto qbits = [&](int32_t s, int32_t b, int32_t n) -> uint64_t {
+        const int32_t w0 = p.seg_lmask_off[s], nw = p.seg_lmask_off[s + 1] - w0;
+        const int32_t i = b / 32, sh = b % 32;
+        auto word = [&](int32_t j) -> uint64_t { return j < nw ? p.seg_lmask[w0 + j] : 0u; };
+        uint64_t x = (word(i) | (word(i + 1) << 32)) >> sh;
+        if (sh > 0)
+            x |= word(i + 2) << (64 - sh);
+        return n >= 64 ? x : x & ((1ull << n) - 1);
+    };
+    auto row_bits = [&](uint64_t qb) -> uint64_t {
+        if (G == 1)
+            return qb;
+        uint64_t r = 0;
+        const uint64_t g = G >= 64 ? ~0ull : (1ull << G) - 1;
+        for (; qb; qb &= qb - 1)
+            r |= g << (__builtin_ctzll(qb) * G);
+        return r;
     };
     auto row_masks = [&](const std::vector<Item> &v, std::vector<uint32_t> &mask, std::vector<int32_t> &off) {
         mask.clear();
         off.assign(1, 0);
         for (const Item &it : v) {
-            const int32_t rows = (it.e - it.b) * G;
-            for (int32_t s = p.chunk_seg_off[it.c]; s < p.chunk_seg_off[it.c + 1]; ++s) {
-                uint32_t m = 0;
-                for (int32_t r = 0; r < rows; ++r)
-                    m |= qbit(s, it.b + r / G) << r;
-                mask.push_back(m);
-            }
+            for (int32_t s = p.chunk_seg_off[it.c]; s < p.chunk_seg_off[it.c + 1]; ++s)
+                mask.push_back((uint32_t)row_bits(qbits(s, it.b, it.e - it.b)));
             off.push_back((int32_t)mask.size());
         }
     };
@@ -340,13 +363,13 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
     p.mma_rmask.clear();
     p.mma_rmask_off.assign(1, 0);
     for (const Item &it : mma) {
-        const int32_t rows = (it.e - it.b) * G, nph = 16 * (it.bucket + 1);
+        // Rows 0 .. nph-1 are warpgroup 0's columns (bits 0-63), the rest
+        // warpgroup 1's (bits 64-127).
+        const int32_t nph = 16 * (it.bucket + 1);
         for (int32_t s = p.chunk_seg_off[it.c]; s < p.chunk_seg_off[it.c + 1]; ++s) {
-            uint32_t w[4] = {0, 0, 0, 0};
-            for (int32_t r = 0; r < rows; ++r) {
-                const int32_t col = r < nph ? r : 64 + (r - nph);
-                w[col / 32] |= qbit(s, it.b + r / G) << (col % 32);
-            }
+            const uint64_t r = row_bits(qbits(s, it.b, it.e - it.b));
+            const uint64_t lo = nph >= 64 ? r : r & ((1ull << nph) - 1), hi = nph >= 64 ? 0 : r >> nph;
+            const uint32_t w[4] = {(uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32)};
             p.mma_rmask.insert(p.mma_rmask.end(), w, w + 4);
         }
         p.mma_rmask_off.push_back((int32_t)(p.mma_rmask.size() / 4));

@@ -260,12 +260,19 @@ class Plan:
 
 
 def _stream(stream):
+    """The raw cudaStream_t (an int) of `stream`, or of torch's current
+    stream when it is None."""
     if stream is None:
         import torch
-        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        if raw is not None:
+            # The current stream's handle without building a Stream object
+            # (~0.3 us against ~3 us for torch.cuda.current_stream()).
+            return raw(torch.cuda.current_device())
+        return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
-        return ctypes.c_void_p(stream)
-    return ctypes.c_void_p(stream.cuda_stream)
+        return stream
+    return stream.cuda_stream
 
 
 @dataclass

@@ -328,6 +328,28 @@ int deft_tree_attn_ex(const void *q, const void *k_pages, const void *v_pages,
                       void *workspace, size_t workspace_bytes, int32_t flags, void *stream);
 
 /*
+ * deft_tree_attn_host -- deft_tree_attn with the step's per-call inputs and
+ * outputs in host memory (no counterpart on the pages; the decode loop's
+ * round trip in one call).  On `stream`, in order: q_host (num_queries x
+ * num_q_heads x head_dim bf16) is copied into q, the step runs as
+ * deft_tree_attn, and out and lse are copied into out_host (out_dtype
+ * elements) and lse_host.  q, out, lse and workspace are device buffers as
+ * for deft_tree_attn; the KV cache and page table stay on the device.  With
+ * pinned host memory the copies are asynchronous and the call returns before
+ * they finish: synchronise the stream before reading out_host / lse_host and
+ * keep q_host unchanged until then.  Pageable host memory works too (CUDA
+ * then stages the copies, which may wait for the stream).  Null host
+ * pointers: DEFT_EINVAL; a failed copy: DEFT_ECUDA; other arguments and
+ * errors as deft_tree_attn (checked before anything is enqueued).
+ */
+int deft_tree_attn_host(const void *q_host, void *q, const void *k_pages, const void *v_pages,
+                        const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                        float scale, const deft_plan_t *plan, void *out, int32_t out_dtype, float *lse,
+                        void *workspace, size_t workspace_bytes, void *out_host, float *lse_host,
+                        void *stream);
+
+/*
  * deft_step_status -- device-side failures of earlier steps of this plan (no
  * counterpart on the pages).  Every wait of a kernel on another part of its
  * CTA is bounded; one that runs out writes NaN into the rows of its launch

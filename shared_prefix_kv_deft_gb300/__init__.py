@@ -44,7 +44,7 @@ EXPORTS = ["deft_plan", "deft_plan_at", "deft_plan_ex", "deft_plan_rebuild", "de
            "deft_plan_update", "deft_pages_create", "deft_pages_free", "deft_pages_alloc",
            "deft_pages_retain", "deft_pages_release", "deft_pages_free_count", "deft_pages_refcount",
            "deft_plan_free", "deft_status_str", "deft_version", "deft_trace_enable",
-           "deft_trace_read", "deft_tree_attn_noalloc"]
+           "deft_trace_read", "deft_tree_attn_noalloc", "deft_tree_attn_host"]
 
 KERNEL_NAMES = {0: "phase1_fma", 1: "phase1_mma", 2: "phase2_merge"}
 PLAN_TREE_ONLY = 1   # deft_plan_ex flags
@@ -105,6 +105,7 @@ def load(path: str = LIB_PATH):
     lib.deft_tree_attn.argtypes = attn
     lib.deft_naive_attn.argtypes = attn
     lib.deft_tree_attn_ex.argtypes = attn[:-1] + [i32, P]
+    lib.deft_tree_attn_host.argtypes = [P] + attn[:-1] + [P, P, P]
     lib.deft_step_status.argtypes = [P, P, ctypes.POINTER(i32)]
     lib.deft_check_pages.argtypes = [P, i32, P, P, ctypes.c_int64, i32, i32]
     lib.deft_plan_update.argtypes = [P, P, i32]
@@ -327,6 +328,35 @@ def deft_tree_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs
     flags (STEP_*): deft_tree_attn_ex's options; 0 calls deft_tree_attn."""
     return _attn("deft_tree_attn_ex" if flags else "deft_tree_attn", q, k_pages, v_pages,
                  node_page_off, page_id, plan, bufs, scale, out_dtype, stream, flags)
+
+
+def deft_tree_attn_host(q_host, q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs: StepBuffers,
+                        out_host, lse_host, scale=None, stream=None):
+    """deft_tree_attn_host: q_host (host, pinned for an asynchronous copy) is
+    copied into the device buffer q, the step runs, and out / lse are copied
+    into out_host / lse_host, all on the stream; synchronise it before
+    reading the host outputs."""
+    import torch
+    lib = load()
+    Q, Hq, d = q.shape
+    Hkv, P = k_pages.shape[1], k_pages.shape[2]
+    for t in (q, k_pages, v_pages):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k_pages and v_pages must be contiguous bf16 CUDA tensors")
+    if q_host.dtype != torch.bfloat16 or not q_host.is_contiguous() or q_host.is_cuda or q_host.shape != q.shape:
+        raise ValueError("q_host must be a contiguous bf16 host tensor shaped like q")
+    for h, dv in ((out_host, bufs.out), (lse_host, bufs.lse)):
+        if h.is_cuda or not h.is_contiguous() or h.dtype != dv.dtype or h.shape != dv.shape:
+            raise ValueError("out_host / lse_host must be contiguous host tensors shaped like the outputs")
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    odt = DEFT_OUT_BF16 if bufs.out.dtype == torch.bfloat16 else DEFT_OUT_F32
+    rc = lib.deft_tree_attn_host(q_host.data_ptr(), q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                 node_page_off.data_ptr(), page_id.data_ptr(), int(k_pages.shape[0]), int(Hq),
+                                 int(Hkv), int(d), int(P), float(scale), plan.handle, bufs.out.data_ptr(), odt,
+                                 bufs.lse.data_ptr(), bufs.workspace.data_ptr(), int(bufs.workspace.numel()),
+                                 out_host.data_ptr(), lse_host.data_ptr(), _stream(stream))
+    _check("deft_tree_attn_host", rc)
+    return out_host, lse_host
 
 
 def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs=None,

@@ -177,15 +177,24 @@ int traced(const deft_trace_record &rec, void *stream, F &&launch)
     return rc;
 }
 
-int run_step(const void *q, const void *k_pages, const void *v_pages, const int32_t *node_page_off,
-             const int32_t *page_id, int32_t num_pages, int32_t num_q_heads, int32_t num_kv_heads,
-             int32_t head_dim, int32_t page_size, float scale, const deft_plan_t *plan, void *out,
-             int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes, int32_t flags, void *stream)
-{
+// A step whose arguments have been checked: what dispatch_step needs.
+struct Step {
     deft::AttnArgs a;
     bool use_mma = false;
+    bool naive = false;
+    bool empty = false;   // no query: nothing to launch
+    const deft::Partition *hp = nullptr;
+    const deft::DevPartition *dp = nullptr;
+};
+
+// Every check of a step, before anything is enqueued.
+int check_step(const void *q, const void *k_pages, const void *v_pages, const int32_t *node_page_off,
+               const int32_t *page_id, int32_t num_pages, int32_t num_q_heads, int32_t num_kv_heads,
+               int32_t head_dim, int32_t page_size, float scale, const deft_plan_t *plan, void *out,
+               int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes, int32_t flags, Step &st)
+{
     int rc = deft::prepare_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads, num_kv_heads,
-                                head_dim, page_size, scale, plan, out, out_dtype, lse, flags, a, use_mma);
+                                head_dim, page_size, scale, plan, out, out_dtype, lse, flags, st.a, st.use_mma);
     if (rc != DEFT_OK)
         return rc;
     if (!plan->uploaded)
@@ -195,23 +204,42 @@ int run_step(const void *q, const void *k_pages, const void *v_pages, const int3
         return DEFT_ECUDA;
     if (dev != plan->dev_device)
         return DEFT_ESTATE;
-    const bool naive = (flags & DEFT_STEP_NAIVE) != 0;
-    const deft::Partition &hp = naive ? plan->naive : plan->tree;
-    const deft::DevPartition &dp = naive ? plan->dev_naive : plan->dev_tree;
+    st.naive = (flags & DEFT_STEP_NAIVE) != 0;
+    st.hp = st.naive ? &plan->naive : &plan->tree;
+    st.dp = st.naive ? &plan->dev_naive : &plan->dev_tree;
     const size_t need = deft_workspace_bytes(plan, num_q_heads, head_dim);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 || workspace_bytes < need)
         return DEFT_EWORKSPACE;
-    if (plan->num_queries == 0)
-        return DEFT_OK;
+    st.empty = plan->num_queries == 0;
     const int64_t slots = std::max(plan->tree.num_slots(), plan->naive.num_slots());
     const deft::WorkLayout wl = deft::work_layout(slots > 0 ? slots : 1, num_q_heads, head_dim);
     uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
-    a.o_part = reinterpret_cast<float *>(ws + wl.o_off);
-    a.lse_part = reinterpret_cast<float *>(ws + wl.lse_off);
-    const deft::LaunchTracer trace = [](const deft_trace_record &rec, void *st, const std::function<int()> &launch) {
-        return traced(rec, st, launch);
+    st.a.o_part = reinterpret_cast<float *>(ws + wl.o_off);
+    st.a.lse_part = reinterpret_cast<float *>(ws + wl.lse_off);
+    return DEFT_OK;
+}
+
+int launch_step(const Step &st, void *stream)
+{
+    if (st.empty)
+        return DEFT_OK;
+    const deft::LaunchTracer trace = [](const deft_trace_record &rec, void *s, const std::function<int()> &launch) {
+        return traced(rec, s, launch);
     };
-    return deft::dispatch_step(a, dp, hp, use_mma, naive ? 1 : 0, stream, trace) ? DEFT_ECUDA : DEFT_OK;
+    return deft::dispatch_step(st.a, *st.dp, *st.hp, st.use_mma, st.naive ? 1 : 0, stream, trace) ? DEFT_ECUDA
+                                                                                                 : DEFT_OK;
+}
+
+int run_step(const void *q, const void *k_pages, const void *v_pages, const int32_t *node_page_off,
+             const int32_t *page_id, int32_t num_pages, int32_t num_q_heads, int32_t num_kv_heads,
+             int32_t head_dim, int32_t page_size, float scale, const deft_plan_t *plan, void *out,
+             int32_t out_dtype, float *lse, void *workspace, size_t workspace_bytes, int32_t flags, void *stream)
+{
+    Step st;
+    const int rc = check_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads, num_kv_heads,
+                              head_dim, page_size, scale, plan, out, out_dtype, lse, workspace, workspace_bytes,
+                              flags, st);
+    return rc != DEFT_OK ? rc : launch_step(st, stream);
 }
 
 }  // namespace
@@ -478,6 +506,35 @@ int deft_tree_attn(const void *q, const void *k_pages, const void *v_pages,
     return run_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads,
                     num_kv_heads, head_dim, page_size, scale, plan, out, out_dtype, lse, workspace,
                     workspace_bytes, 0, stream);
+}
+
+int deft_tree_attn_host(const void *q_host, void *q, const void *k_pages, const void *v_pages,
+                        const int32_t *node_page_off, const int32_t *page_id, int32_t num_pages,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                        float scale, const deft_plan_t *plan, void *out, int32_t out_dtype, float *lse,
+                        void *workspace, size_t workspace_bytes, void *out_host, float *lse_host, void *stream)
+{
+    if (!q_host || !out_host || !lse_host)
+        return DEFT_EINVAL;
+    Step st;
+    int rc = check_step(q, k_pages, v_pages, node_page_off, page_id, num_pages, num_q_heads, num_kv_heads, head_dim,
+                        page_size, scale, plan, out, out_dtype, lse, workspace, workspace_bytes, 0, st);
+    if (rc != DEFT_OK)
+        return rc;
+    const size_t rows = (size_t)plan->num_queries * (size_t)num_q_heads;
+    if (rows == 0)
+        return DEFT_OK;
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+    const size_t out_elem = out_dtype == DEFT_OUT_F32 ? 4 : 2;
+    if (cudaMemcpyAsync(q, q_host, rows * head_dim * 2, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+        return DEFT_ECUDA;
+    rc = launch_step(st, stream);
+    if (rc != DEFT_OK)
+        return rc;
+    if (cudaMemcpyAsync(out_host, out, rows * head_dim * out_elem, cudaMemcpyDeviceToHost, cs) != cudaSuccess ||
+        cudaMemcpyAsync(lse_host, lse, rows * sizeof(float), cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+        return DEFT_ECUDA;
+    return DEFT_OK;
 }
 
 int deft_naive_attn(const void *q, const void *k_pages, const void *v_pages,

@@ -154,6 +154,28 @@ def test_direct_rows_for_all_some_and_no_queries(deft, which, spec, ct):
     assert case.plan.step_status() == 0
 
 
+@pytest.mark.parametrize("spec", [W.tiny_tree(), W.few_shot_tree(prefix=600, branches=20, branch_len=70, heads=4,
+                                                                  head_dim=128)], ids=lambda s: s.name)
+def test_host_buffer_step_equals_the_device_step(deft, spec):
+    """deft_tree_attn_host (q in, out and lse back, all on the stream) gives
+    the device step's values bit for bit, in both output dtypes."""
+    inp = dense_inputs(spec, seed=11)
+    case = Case(deft, inp, 64)
+    for odt in (0, 1):
+        out_d, lse_d = case.run(out_dtype=odt)
+        bufs = deft.alloc_buffers(case.plan, spec.num_queries, spec.num_q_heads, spec.head_dim, out_dtype=odt)
+        q_host = case.q.cpu().pin_memory()
+        q_dev = torch.empty_like(case.q)
+        out_h = torch.empty(bufs.out.shape, dtype=bufs.out.dtype).pin_memory()
+        lse_h = torch.empty(bufs.lse.shape, dtype=bufs.lse.dtype).pin_memory()
+        deft.deft_tree_attn_host(q_host, q_dev, case.k, case.v, case.npo, case.pid, case.plan, bufs, out_h, lse_h)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out_h.float().numpy().astype(np.float64), out_d)
+        np.testing.assert_array_equal(lse_h.numpy().astype(np.float64), lse_d)
+        torch.testing.assert_close(q_dev, case.q, rtol=0, atol=0)
+    assert case.plan.step_status() == 0
+
+
 TENSOR_PACK_SHAPES = [s for s in SMALL if s.head_dim == 128]
 
 

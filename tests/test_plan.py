@@ -454,6 +454,14 @@ def test_step_calls_reject_bad_flags_and_state_before_any_cuda_call():
     assert lib.deft_step_status(None, None, ctypes.byref(code)) == -1
     assert lib.deft_step_status(plan.handle, None, None) == -1
 
+    def call_host(q_host, out_host, lse_host):
+        return lib.deft_tree_attn_host(q_host, fake, fake, fake, fake, fake, 4, 4, 4, 64, 16, 0.125, plan.handle,
+                                       fake, 0, fake, fake, 1 << 20, out_host, lse_host, None)
+    assert call_host(None, fake, fake) == -1      # host buffers are required
+    assert call_host(fake, None, fake) == -1
+    assert call_host(fake, fake, None) == -1
+    assert call_host(fake, fake, fake) == -8      # never uploaded: nothing enqueued
+
 
 def test_check_pages_accepts_a_layout_and_rejects_each_bad_table():
     spec = W.reasoning_tree(levels=3, len_lo=5, len_hi=40, num_queries=12, q_heads=4, kv_heads=2)

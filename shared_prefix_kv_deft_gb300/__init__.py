@@ -13,7 +13,7 @@ import ctypes
 import math
 import os
 from dataclasses import dataclass
-from typing import Optional
+from typing import Tuple, Optional
 
 import numpy as np
 
@@ -168,17 +168,31 @@ class Plan:
     def __init__(self, parent, node_len, query_node, chunk_target: int = 256, gqa_group: int = 1,
                  query_pos=None, naive: bool = True, tensor_pack: bool = False):
         lib = load()
-        self._parent, self._len, self._qn = _i32(parent), _i32(node_len), _i32(query_node)
-        self._pos = None if query_pos is None else _i32(query_pos)
+        par, ln, qn = _i32(parent), _i32(node_len), _i32(query_node)
+        pos = None if query_pos is None else _i32(query_pos)
         h = ctypes.c_void_p()
-        _check("deft_plan_ex", lib.deft_plan_ex(_ptr(self._parent), _ptr(self._len),
-                                                int(self._parent.shape[0]), _ptr(self._qn),
-                                                None if self._pos is None else _ptr(self._pos),
-                                                int(self._qn.shape[0]), int(chunk_target),
-                                                int(gqa_group), _plan_flags(naive, tensor_pack),
-                                                ctypes.byref(h)))
+        _check("deft_plan_ex", lib.deft_plan_ex(_ptr(par), _ptr(ln), int(par.shape[0]), _ptr(qn),
+                                                None if pos is None else _ptr(pos), int(qn.shape[0]),
+                                                int(chunk_target), int(gqa_group),
+                                                _plan_flags(naive, tensor_pack), ctypes.byref(h)))
         self.handle = h
         self._stats = None
+        self._staged = {}
+
+    def _stage(self, slot: int, a) -> Tuple[int, int]:
+        """a copied into this plan's int32 staging buffer `slot` (kept across
+        rebuilds, its address taken once): (length, address).  The library
+        copies the inputs it keeps, so the buffers are only read during the
+        call."""
+        a = np.asarray(a)
+        n = int(a.shape[0])
+        buf, addr = self._staged.get(slot, (None, 0))
+        if buf is None or buf.shape[0] < n:
+            buf = np.empty(max(2 * n, 64), dtype=np.int32)
+            addr = buf.ctypes.data
+            self._staged[slot] = (buf, addr)
+        buf[:n] = a
+        return n, addr
 
     @property
     def stats(self) -> dict:
@@ -194,13 +208,15 @@ class Plan:
         """deft_plan_rebuild: plan a new tree into this plan, keeping its device
         allocation and staging buffer; upload() again before the next step.
         On error (DeftError) the plan is unchanged."""
-        par, ln, qn = _i32(parent), _i32(node_len), _i32(query_node)
-        pos = None if query_pos is None else _i32(query_pos)
+        n, par = self._stage(0, parent)
+        n_len, ln = self._stage(1, node_len)
+        nq, qn = self._stage(2, query_node)
+        pos = None if query_pos is None else self._stage(3, query_pos)[1]
+        if n_len != n:
+            raise ValueError("parent and node_len differ in length")
         _check("deft_plan_rebuild", load().deft_plan_rebuild(
-            self.handle, _ptr(par), _ptr(ln), int(par.shape[0]), _ptr(qn),
-            None if pos is None else _ptr(pos), int(qn.shape[0]), int(chunk_target), int(gqa_group),
+            self.handle, par, ln, n, qn, pos, nq, int(chunk_target), int(gqa_group),
             _plan_flags(naive, tensor_pack)))
-        self._parent, self._len, self._qn, self._pos = par, ln, qn, pos
         self._stats = None
 
     def __del__(self):
@@ -245,9 +261,8 @@ class Plan:
     def update(self, node_len):
         """deft_plan_update: the same tree with new node lengths (tokens
         appended, pruned subtrees at 0); upload() again before the next step."""
-        ln = _i32(node_len)
-        _check("deft_plan_update", load().deft_plan_update(self.handle, _ptr(ln), int(ln.shape[0])))
-        self._len = ln
+        n, ln = self._stage(1, node_len)
+        _check("deft_plan_update", load().deft_plan_update(self.handle, ln, n))
         self._stats = None
 
     def step_status(self, stream=None) -> int:

@@ -75,8 +75,8 @@ void shape_launches(const double *cost, const int32_t *units, int n, int sms, La
 namespace {
 
 // The early CTAs' static blocks when the units' costs differ: the first
-// block (items are sorted by cost, largest first) holds no more than 3/4 of
-// an even share of the launch's estimated cost.  Units are item-major,
+// block (items are sorted by cost, largest first) holds no more than 9/10 of
+// an even share of the launch's estimated cost; the queue evens out the rest.  Units are item-major,
 // `hkv` per item; unit_cost(i) is item i's cost per unit.
 template <typename F>
 int32_t cost_block(int32_t n_items, int32_t hkv, int32_t early, F unit_cost)
@@ -84,7 +84,7 @@ int32_t cost_block(int32_t n_items, int32_t hkv, int32_t early, F unit_cost)
     double total = 0.0;
     for (int32_t i = 0; i < n_items; ++i)
         total += unit_cost(i) * hkv;
-    const double cap = 0.75 * total / std::max(1, early);
+    const double cap = 0.9 * total / std::max(1, early);
     double acc = 0.0;
     int32_t s = 0;
     for (int32_t i = 0; i < n_items; ++i) {

@@ -23,8 +23,8 @@
 //
 // Persistent CTAs (one per SM): the launch's early CTAs, those that start
 // with the step, first take a contiguous block of units (unit = item x KV
-// head, item-major, largest items first; about 3/4 of an even share among
-// them); then every CTA takes units one at a time from the launch's work
+// head, item-major, largest items first; 9/10 of an even share of the
+// estimated cost among them); then every CTA takes units one at a time from the launch's work
 // queue (an atomic counter), so a CTA that starts late or runs fast takes
 // more;
 // all roles walk the CTA's units in order and its tiles form one sequence
@@ -37,8 +37,8 @@
 //                   the partial rows, to the epilogue warpgroup;
 //   warps 8, 10     K and V producers: resolve a tile's pages through the
 //                   page table one tile ahead, load full aligned pages with
-//                   TMA (one 4-D box for eight consecutive pages, 2 KB boxes
-//                   of the 128-byte-swizzled layout otherwise) and ragged
+//                   TMA (one box for eight consecutive pages, a 4 KB box a
+//                   page otherwise) and ragged
 //                   rows (node tails, packed one-token nodes) with 16-byte
 //                   cp.async at the exact token count; K of a stage is
 //                   refilled as soon as S of the tile two back is done, V
@@ -75,7 +75,11 @@ static_assert(2 * 128 * kRegsSoftmax + 2 * 128 * kRegsOther == kThreadsMma * 128
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kHalf = 128 * 128;       // one 64-wide half of a 128-row operand (16 KB)
 constexpr uint32_t kTileBytes = 2 * kHalf;  // one 128 x 128 bf16 operand (32 KB)
-constexpr uint32_t kHalfPage = 2 * 2048;    // K (or V) of one 16-token page: two TMA boxes
+// K and V tiles: [16 groups of 8 tokens][d half][8 tokens][128 B], 128-byte
+// swizzled.  A group is two 1 KB swizzle atoms (dims 0-63, 64-127), so a
+// 16-token page is 4 KB contiguous in the tile and lands with one TMA box.
+constexpr uint32_t kRowGroup = 2048;        // 8 tokens x 128 dims
+constexpr uint32_t kPageBytes = 4096;       // K (or V) of one 16-token page
 constexpr int kSegInts = 7 * kMaxSegsPerChunk;  // pos, page base, token begin, row mask (4)
 
 constexpr int kUnitQueue = 8;   // unit numbers passed from the metadata warp to the producers
@@ -147,10 +151,13 @@ constexpr int kNumBars = 46;
 __device__ __forceinline__ int qfree_bar(int qb) { return qb == 0 ? kBarQFree : kBarQFree1; }
 static_assert(kNumBars * 8 <= Smem<16>::misc_off - Smem<16>::bar_off, "mbarrier space");
 
-// Tensor maps over the paged K and V.  *1: the pool as [pages*Hkv*16 rows]
-// [128], boxes of one page's 16 rows x 64 columns; *8: the pool as
-// [pages][Hkv][16][128], boxes of eight consecutive pages of one head x 64
-// columns (a tile whose pages were allocated back to back in one copy).
+// Tensor maps over the paged K and V, both viewing the pool [pages][Hkv][16]
+// [128] as five dimensions, innermost first: 64 dims (one 128-byte swizzle
+// row), 8 tokens (256 B apart), the two d halves (128 B apart), 2 Hkv token
+// groups (head h's two groups of 8 at 2h, 2h + 1; 2 KB apart) and pages.  A
+// box lands in the tile layout above.  *1: boxes of one page of one head;
+// *8: of eight consecutive pages of one head (a tile whose pages were
+// allocated back to back in one copy).
 struct KvMaps {
     CUtensorMap k1, v1, k8, v8;
 };
@@ -585,28 +592,24 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     // warp (the lanes' own arrivals below may be deferred).
                     __syncwarp();
                     if (lane == 0)
-                        tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kHalfPage);
+                        tc::mbar_arrive_expect_tx(full, __popc(res.tma_pages) * kPageBytes);
                     __syncwarp();
-                    // Eight whole, consecutive pages: one box per column half.
+                    // Eight whole, consecutive pages: one box; else one box a page.
                     bool run8 = false;
                     const int pg0 = __shfl_sync(0xffffffffu, res.page_y, 0);
                     if (res.tma_pages == 0xffu)
                         run8 = __all_sync(0xffffffffu, lane >= 8 || res.page_y == pg0 + lane);
                     if (run8) {
-                        if (lane == 0) {
-                            tc::tma_load_4d(dst, tm8, 0, 0, h, pg0, full, kv_pol);
-                            tc::tma_load_4d(dst + kHalf, tm8, 64, 0, h, pg0, full, kv_pol);
-                        }
+                        if (lane == 0)
+                            tc::tma_load_5d(dst, tm8, 0, 0, 0, 2 * h, pg0, full, kv_pol);
                     } else if (res.page_y >= 0) {
-                        const int y = (res.page_y * Hkv + h) * kPageSize;
-                        const uint32_t row_b = (uint32_t)(16 * lane) * 128;
-                        tc::tma_load_2d(dst + row_b, tm, 0, y, full, kv_pol);
-                        tc::tma_load_2d(dst + kHalf + row_b, tm, 64, y, full, kv_pol);
+                        tc::tma_load_5d(dst + (uint32_t)lane * kPageBytes, tm, 0, 0, 0, 2 * h, res.page_y, full,
+                                        kv_pol);
                     }
                     // Ragged rows: two rows per warp step, 16 lanes (16-byte chunks) each.
                     bool any_cp = false;
                     const __nv_bfloat16 *src0 = src_base + (lane & 15) * 8;
-                    const uint32_t dst0 = dst + ((lane & 15) >> 3) * kHalf;
+                    const uint32_t dst0 = dst + ((lane & 15) >> 3) * 1024u;
     #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         uint32_t nb = __ballot_sync(0xffffffffu, res.pid[k] >= 0);
@@ -630,7 +633,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                                 const int tk = lane < 16 ? t0 : t1;
                                 const long long o = (((long long)pg * Hkv + h) * kPageSize + (tk % kPageSize)) * kD;
                                 const int ch = lane & 7;
-                                cp_async_16(dst0 + row * 128 + ((ch ^ (row & 7)) << 4), src0 + o);
+                                cp_async_16(dst0 + (uint32_t)(row >> 3) * kRowGroup + (row & 7) * 128 +
+                                                ((ch ^ (row & 7)) << 4),
+                                            src0 + o);
                             }
                         }
                     }
@@ -660,8 +665,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 // Descriptors of k-step 0; step s adds an address offset (16-byte units).
                 const uint64_t dq = tc::smem_desc(base + L::q_off, 16, 1024);
                 const uint64_t dp = tc::smem_desc(base + L::p_off, kHalf, 1024);
-                const uint64_t dk0 = tc::smem_desc(base + L::k_off, 16, 1024);
-                const uint64_t dv0 = tc::smem_desc(base + L::v_off, kHalf, 1024);
+                // K: K-major, 8-token groups kRowGroup apart; V: MN-major, its
+                // d halves 1 KB apart and its 8-token groups kRowGroup apart.
+                const uint64_t dk0 = tc::smem_desc(base + L::k_off, 16, kRowGroup);
+                const uint64_t dv0 = tc::smem_desc(base + L::v_off, 1024, kRowGroup);
                 constexpr uint64_t kStageStep = kTileBytes >> 4;   // descriptor address units
                 int nunits = 0x7fffffff;   // known once the end mark is read
                 // S cursor: unit is, its tile ts (nts tiles, -1 before its
@@ -694,7 +701,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             const uint32_t d_s = tmem + (uint32_t)(b * 128);
     #pragma unroll
                             for (int s = 0; s < 8; ++s) {
-                                const uint64_t ko = (uint64_t)(((s >> 2) * kHalf + (s & 3) * 32) >> 4);
+                                const uint64_t ko = (uint64_t)(((s >> 2) * 1024 + (s & 3) * 32) >> 4);
                                 const uint64_t qo = (uint64_t)(((is % L::QB) * 2 * L::q_half + (s >> 2) * L::q_half +
                                                                 (s & 3) * 32) >> 4);
                                 tc::mma_bf16(d_s, dk0 + (uint64_t)st * kStageStep + ko, dq + qo, idesc_s, s > 0 ? 1u : 0u);
@@ -723,8 +730,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             const uint32_t d_o = tmem + 256 + (uint32_t)(ob * 128);
     #pragma unroll
                             for (int s = 0; s < 8; ++s) {
-                                const uint64_t so = (uint64_t)((s * 2048) >> 4);
-                                tc::mma_bf16(d_o, dv0 + (uint64_t)stp * kStageStep + so, dp + so, idesc_o,
+                                // k-step s: tokens 16 s .. 16 s + 15 (two groups of V, 2 KB of P^T).
+                                const uint64_t sv = (uint64_t)((s * 2 * kRowGroup) >> 4);
+                                const uint64_t sp = (uint64_t)((s * 2048) >> 4);
+                                tc::mma_bf16(d_o, dv0 + (uint64_t)stp * kStageStep + sv, dp + sp, idesc_o,
                                              (tp > 0 || s > 0) ? 1u : 0u);
                             }
                             tc::mma_commit(bar(kBarPvDone));
@@ -1090,24 +1099,15 @@ bool encode_pool_map(const void *ptr, int32_t pages, int32_t hkv, bool run8, CUt
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encoder();
     if (!enc)
         return false;
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r;
-    if (!run8) {
-        const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)pages * hkv * kPageSize};
-        const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-        const cuuint32_t box[2] = {64, 16};
-        r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kPageSize, (cuuint64_t)hkv, (cuuint64_t)pages};
-        const cuuint64_t row = (cuuint64_t)kD * 2;
-        const cuuint64_t strides[3] = {row, row * kPageSize, row * kPageSize * hkv};
-        const cuuint32_t box[4] = {64, (cuuint32_t)kPageSize, 1, 8};
-        r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
-                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    }
+    static_assert(kPageSize == 16 && kD == 128, "a page is two groups of 8 tokens x 128 dims");
+    const cuuint64_t row = (cuuint64_t)kD * 2;
+    const cuuint64_t dims[5] = {64, 8, 2, 2 * (cuuint64_t)hkv, (cuuint64_t)pages};
+    const cuuint64_t strides[4] = {row, 128, 8 * row, row * kPageSize * hkv};
+    const cuuint32_t box[5] = {64, 8, 2, 2, run8 ? 8u : 1u};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(ptr), dims, strides, box, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 

@@ -261,6 +261,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// 5-D tiled TMA load global -> shared, completion counted on `bar` in bytes,
+// L2 cache policy `pol`.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void *tmap, int c0, int c1, int c2, int c3, int c4,
+                                            uint32_t bar, uint64_t pol)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar), "l"(pol)
+        : "memory");
+}
+
 // Contiguous bulk copy global -> shared (no tensor map): `bytes` from
 // `src` to `dst`, completion counted on `bar`, L2 cache policy `pol`.  Both
 // addresses 16-byte aligned, `bytes` a multiple of 16.

@@ -447,23 +447,19 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             const int32_t *s_pos = nullptr, *s_pgb = nullptr, *s_tb = nullptr;
             const uint4 *s_rmask = nullptr;
             int T = 0, nseg = 0;
-            // Segment holding position pos (warp-uniform: broadcast reads).
-            auto seg_at = [&](int pos) {
-                int lo = 0, hi = nseg - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (s_pos[mid] <= pos)
-                        lo = mid;
-                    else
-                        hi = mid - 1;
-                }
-                return lo;
-            };
+            // Segment of the current tile's first token: tiles go in order, so
+            // it only moves forward (reset to 0 at each unit's first tile).
+            int cur = 0;
             auto resolve = [&](int t, Res &r) {
                 const int p0 = t * kTileTok;
-                const int sga = seg_at(p0);
+                if (t == 0)
+                    cur = 0;
+                while (cur + 1 < nseg && s_pos[cur + 1] <= p0)
+                    ++cur;
+                const int sga = cur;
                 const int tka = s_tb[sga] + p0 - s_pos[sga];
-                if (T - p0 >= kTileTok && (tka % kPageSize) == 0 && seg_at(p0 + kTileTok - 1) == sga) {
+                const int send = sga + 1 < nseg ? s_pos[sga + 1] : T;   // segment sga ends before send
+                if (T - p0 >= kTileTok && (tka % kPageSize) == 0 && send >= p0 + kTileTok) {
                     // Fast path: eight whole pages of one segment.
     #pragma unroll
                     for (int k = 0; k < 4; ++k) {
@@ -481,7 +477,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                     r.seg[k] = -1;
                     r.tok[k] = 1;
                     if (pos < T) {
-                        int lo = 0, hi = nseg - 1;
+                        int lo = sga, hi = nseg - 1;
                         while (lo < hi) {
                             const int mid = (lo + hi + 1) >> 1;
                             if (s_pos[mid] <= pos)
@@ -528,6 +524,8 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 }
             };
             int iseq = -1, prev_item = -1, gseq = 0, sbuf = 0;
+            int st = 0;          // stage of tile gseq (gseq % NS)
+            uint32_t wrap = 0;   // parity of gseq / NS
             bool ok = true;
             for (int i = 0; ok; ++i) {
                 // The next unit number from the metadata warp (-1: no more).
@@ -570,10 +568,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 Res res;
                 resolve(0, res);
                 for (int t = 0; t < ntiles; ++t, ++gseq) {
-                    const int st = gseq % NS;
                     if (gseq >= NS) {
                         const bool okw = __all_sync(
-                            0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), ((gseq / NS) - 1) & 1));
+                            0xffffffffu, tc::mbar_wait(bar((kv ? kBarEmptyV : kBarEmptyK) + st), wrap ^ 1u));
                         if (!okw) {
                             if (!*err) *err = 207;
                             ok = false;
@@ -647,6 +644,10 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                         cp_async_mbar_arrive_noinc(full);
                     else
                         tc::mbar_arrive(full);
+                    if (++st == NS) {
+                        st = 0;
+                        wrap ^= 1u;
+                    }
                     if (t + 1 < ntiles)
                         resolve(t + 1, res);
                 }

@@ -405,6 +405,12 @@ inline double mma_ns_per_token(int bucket)
 // launches) run as one: each launch pays its own start on every SM, and
 // launches of different widths cannot share their work.
 constexpr double kCollapse = 1.3;
+// The same for the two tensor-core widths.  A narrower margin: at 32 columns
+// a warpgroup the softmax of every tile costs twice that at 16.  Measured:
+// reasoning tree (1.20 by the estimate) 53.5 us as one launch, 51.7 us as
+// two; imbalance tree (1.12) 554 us as one, 582 us as two (its long prefix
+// units keep the 32-column launch busy after the 16-column one ends).
+constexpr double kCollapseMma = 1.15;
 // The merge launch over `nq` queries: queries[i], or i when queries is null.
 int launch_phase2(const AttnArgs &a, const DevPartition &p, const int32_t *queries, int32_t nq, void *stream);
 bool mma_supported(int32_t head_dim);

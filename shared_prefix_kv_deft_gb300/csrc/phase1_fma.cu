@@ -11,8 +11,8 @@
 // Logits are carried in base 2 (q pre-scaled by scale * log2 e).
 //
 // Persistent CTAs (one per SM): the launch's early CTAs, those that start
-// with the step, first take a contiguous block of units (about 3/4 of an
-// even share among them; units are item-major, so the block holds runs of
+// with the step, first take a contiguous block of units (9/10 of an even
+// share of the estimated cost among them; units are item-major, so the block holds runs of
 // one item's KV heads, which share the item's segment table and page list);
 // then every CTA takes units one at a time from the launch's work queue (an
 // atomic counter), so a CTA that starts late or runs fast takes more.  Each

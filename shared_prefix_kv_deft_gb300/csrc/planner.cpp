@@ -286,7 +286,7 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
                           row_bucket((std::min(k, b + perf) - b) * G)});
     }
     // Tensor-core items of both widths run as one launch at 32 columns a
-    // warpgroup when that costs little more (kCollapse); their row masks are
+    // warpgroup when that costs little more (kCollapseMma); their row masks are
     // then laid out for that width.
     {
         double tok[2] = {0.0, 0.0};
@@ -294,7 +294,7 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
             tok[it.bucket] += (double)p.chunk_tokens[it.c];
         const double split = tok[0] * mma_ns_per_token(0) + tok[1] * mma_ns_per_token(1);
         const double one = (tok[0] + tok[1]) * mma_ns_per_token(1);
-        if (tok[0] > 0.0 && tok[1] > 0.0 && one <= kCollapse * split)
+        if (tok[0] > 0.0 && tok[1] > 0.0 && one <= kCollapseMma * split)
             for (Item &it : mma)
                 it.bucket = 1;
     }

@@ -41,7 +41,10 @@ class DenseInputs:
 
 
 def dense_inputs(spec: W.TreeSpec, seed: int = 0, spare_pages: int = 3, zero_q=False,
-                 equal_keys=False, poison=True) -> DenseInputs:
+                 equal_keys=False, poison=True, k_ramp: float = 0.0) -> DenseInputs:
+    """k_ramp > 0 scales the key of the token at position p of its node by
+    1 + k_ramp * p, so that logits grow along a node (later tiles of a chunk
+    then exceed the column maxima of its first tile)."""
     rng = np.random.default_rng(seed)
     Q, Hq, Hkv, d = spec.num_queries, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
     T = int(spec.node_len.sum())
@@ -51,6 +54,9 @@ def dense_inputs(spec: W.TreeSpec, seed: int = 0, spare_pages: int = 3, zero_q=F
     k = rng.standard_normal((T, Hkv, d), dtype=np.float32) * np.float32(spec.k_scale)
     if equal_keys:
         k[:] = k[:1]
+    if k_ramp:
+        pos = np.concatenate([np.arange(L) for L in spec.node_len]) if T else np.zeros(0, int)
+        k *= (1.0 + k_ramp * pos).astype(np.float32)[:, None, None]
     v = rng.standard_normal((T, Hkv, d), dtype=np.float32)
     q_bits, k_bits, v_bits = to_bf16_bits(q), to_bf16_bits(k), to_bf16_bits(v)
     tok_node = np.repeat(np.arange(spec.num_nodes), spec.node_len)

@@ -412,6 +412,27 @@ def test_tensor_core_and_cuda_core_paths_agree_with_oracle(deft, spec, ct):
     assert case.plan.step_status() == 0
 
 
+@pytest.mark.parametrize("spec", MMA_SHAPES[:2], ids=lambda s: s.name)
+@pytest.mark.parametrize("ct,tp", [(64, False), (256, False), (256, True)])
+def test_growing_logits_take_the_rescale_path(deft, spec, ct, tp):
+    """Keys scaled up along each node: a chunk's later tiles hold logits far
+    above the maxima of its first tile, so the kernels' rescale of the
+    running output and sums (online softmax) is exercised, not just the
+    common path; both the tensor-core and CUDA-core steps against the
+    oracle.  The softmax is then sharply peaked, so an output is close to a
+    single value row (|out| up to ~5): fp32 output, since rounding such a
+    value to bf16 alone can be 1.6e-2 off."""
+    inp = dense_inputs(spec, seed=5, k_ramp=0.1)
+    ref, ref_lse = run_oracle(inp)
+    case = Case(deft, inp, ct, tensor_pack=tp)
+    assert case.plan.stats["num_mma_items"] > 0
+    out, lse = case.run(out_dtype=1)
+    assert_parity(out, lse, ref, ref_lse, "tcgen05 path, growing logits")
+    out2, lse2 = case.run(flags=deft.STEP_CUDA_CORES, out_dtype=1)
+    assert_parity(out2, lse2, ref, ref_lse, "CUDA-core path, growing logits")
+    assert case.plan.step_status() == 0
+
+
 POSITION_SHAPES = [W.positions_tree(s, max_nodes=14, max_len=120, max_queries=24, q_heads=8,
                                     kv_heads=2, head_dim=128) for s in range(6)]
 POSITION_SHAPES += [W.positions_tree(50 + s, max_nodes=10, max_len=60, max_queries=12)

@@ -276,14 +276,14 @@ void finish_partition(Partition &p, int32_t num_queries, int32_t W, int32_t G)
         }
         const int32_t nb = (k + qmax_mma - 1) / qmax_mma;
         const int32_t per = (k + nb - 1) / nb;
+        // Within a width (row bucket) a unit's time follows its tokens, not
+        // its rows: the order of the launch's queue and of its static blocks.
         for (int32_t b = 0; b < k; b += per)
-            mma.push_back({c, b, std::min(k, b + per), tok * (std::min(k, b + per) - b),
-                           mma_bucket((std::min(k, b + per) - b) * G)});
+            mma.push_back({c, b, std::min(k, b + per), tok, mma_bucket((std::min(k, b + per) - b) * G)});
         const int32_t nf = (k + qmax_fb - 1) / qmax_fb;
         const int32_t perf = (k + nf - 1) / nf;
         for (int32_t b = 0; b < k; b += perf)
-            fb.push_back({c, b, std::min(k, b + perf), tok * (std::min(k, b + perf) - b),
-                          row_bucket((std::min(k, b + perf) - b) * G)});
+            fb.push_back({c, b, std::min(k, b + perf), tok, row_bucket((std::min(k, b + perf) - b) * G)});
     }
     // Tensor-core items of both widths run as one launch at 32 columns a
     // warpgroup when that costs little more (kCollapseMma); their row masks are

@@ -173,6 +173,17 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
         std::rotate(ls, ls + n - 1, ls + n);
         std::rotate(shape, shape + n - 1, shape + n);
     }
+    // Whether a launch's items include row blocks of one chunk (items
+    // reading the same KV).
+    auto row_blocks = [&](const Launch &l) {
+        const std::vector<int32_t> &it = l.kind == 0 ? hp.mma_items : l.kind == 1 ? hp.fma_items : hp.fallback_items;
+        for (int32_t k = 0; k < l.n; ++k) {
+            const int32_t *t = &it[3 * (size_t)(l.off + k)];
+            if (t[1] > 0 || t[2] < hp.chunk_q_off[t[0] + 1] - hp.chunk_q_off[t[0]])
+                return true;
+        }
+        return false;
+    };
     // Static blocks by cost (a launch's items differ in size: a block of
     // whole long items would keep its CTA long after the others).
     for (int i = 0; i < n; ++i) {
@@ -183,6 +194,19 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
             const double ns = l.kind == 0 ? mma_ns_per_token(l.bucket) : fma_ns_per_token(l.bucket);
             return (double)hp.chunk_tokens[t[0]] * ns;
         });
+        // Row blocks of one chunk find its KV in L2 only when they run at
+        // about the same time.  The blocks are consecutive items, so their
+        // units for head h are Hkv apart; with a static block that divides
+        // Hkv they come at the same step of their CTAs' blocks, which start
+        // together.  (A block of 3 units at Hkv = 8 had the imbalance shape
+        // read its 32768-token prefix from DRAM ~3 times: 1.44x the unique
+        // KV instead of 1.03x.)
+        if (shape[i].block > 1 && row_blocks(l)) {
+            int32_t b = std::min<int32_t>(shape[i].block, hkv);
+            while (b > 1 && hkv % b != 0)
+                --b;
+            shape[i].block = b;
+        }
     }
 
     // Only the step's first launch waits for the stream's earlier work
@@ -194,15 +218,7 @@ int dispatch_step(AttnArgs a, const DevPartition &dp, const Partition &hp, bool 
         // A launch whose items include row blocks of one chunk reads that
         // chunk's KV once per block: its copies keep the normal L2 policy so
         // that the later blocks find the KV in L2.
-        {
-            const std::vector<int32_t> &it = l.kind == 0 ? hp.mma_items : l.kind == 1 ? hp.fma_items : hp.fallback_items;
-            bool blocks = false;
-            for (int32_t k = 0; k < l.n && !blocks; ++k) {
-                const int32_t *t = &it[3 * (size_t)(l.off + k)];
-                blocks = t[1] > 0 || t[2] < hp.chunk_q_off[t[0] + 1] - hp.chunk_q_off[t[0]];
-            }
-            a.kv_once = kv_once && !blocks;
-        }
+        a.kv_once = kv_once && !row_blocks(l);
         if (l.kind == 0) {
             const int32_t *it = dp.mma_items + 3 * (size_t)l.off;
             uint32_t *queue = dp.queues + 2 * queue_slot(0, l.bucket);

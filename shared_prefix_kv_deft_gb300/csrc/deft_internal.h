@@ -12,6 +12,7 @@
 #pragma once
 
 #include <array>
+#include <initializer_list>
 #include <cstddef>
 #include <cstdint>
 #include <functional>
@@ -98,6 +99,28 @@ struct Partition {
     int32_t num_chunks() const { return (int32_t)chunk_tokens.size(); }
     int32_t num_segments() const { return (int32_t)seg_node.size(); }
     int32_t num_slots() const { return (int32_t)chunk_q.size(); }
+    // Back to a fresh partition, keeping the arrays' storage (a plan rebuilt
+    // every decode step then allocates nothing once its arrays have grown).
+    void reset()
+    {
+        for (std::vector<int32_t> *v : {&chunk_seg_off, &chunk_q_off, &chunk_tokens, &chunk_q, &seg_node,
+                                        &seg_tok_begin, &seg_tok_len, &seg_chunk_pos, &seg_lmask_off, &q_slot_off,
+                                        &q_slot, &fma_items, &mma_items, &fallback_items, &fma_rmask_off,
+                                        &fallback_rmask_off, &mma_rmask_off, &merge_q})
+            v->clear();
+        for (std::vector<uint32_t> *v : {&seg_lmask, &fma_rmask, &fallback_rmask, &mma_rmask, &fma_direct,
+                                         &fallback_direct})
+            v->clear();
+        seg_mask.clear();
+        chunk_mask.clear();
+        queue_words.assign(kQueueWords, 0u);
+        fma_bucket_off.fill(0);
+        fallback_bucket_off.fill(0);
+        mma_bucket_off.fill(0);
+        fma_bucket_tok.fill(0);
+        fallback_bucket_tok.fill(0);
+        mma_bucket_tok.fill(0);
+    }
 };
 
 // A segment set aside for tensor packing (tokens [b0, b0 + L) of node n; its

@@ -465,7 +465,7 @@ int64_t emit_tree(deft_plan_t *plan, size_t start)
     for (int32_t n = 0; n < N; ++n)
         tokens += node_len[n];
     if (start == 0) {
-        part = Partition();
+        part.reset();
         thin.clear();
         thin_mask.clear();
     } else {
@@ -617,7 +617,7 @@ void finish_plan(deft_plan_t *plan, int64_t unique_tokens, int64_t naive_tokens,
     // Naive partition: each query's path (root first) cut every chunk_target
     // tokens; every chunk serves that one query.  Left empty (no chunk) when
     // the caller will not run it.
-    plan->naive = Partition();
+    plan->naive.reset();
     if (!plan->has_naive) {
         Builder b(plan->naive, W, 0, 0);
     } else {

@@ -52,7 +52,9 @@
 //                   Q^T loads meanwhile);
 //   warps 12-15     epilogue: O^T / l out of TMEM (two O buffers) into the
 //                   fp32 partials while the softmax warpgroups go on with
-//                   the next unit.
+//                   the next unit; it waits for the unit's last P.V itself
+//                   (the softmax warpgroups hand over their column sums
+//                   without waiting for it).
 // Every hand-off is an mbarrier, every wait on one is bounded.  A CTA whose
 // wait runs out writes NaN partials for its units (the step's output then
 // shows the failure), waits for its own copies, frees TMEM and returns.
@@ -147,7 +149,8 @@ constexpr int kBarQFull = 27;    // [kUnitQueue] a unit number written (metadata
 constexpr int kBarQEmpty = 35;   // [kUnitQueue] ... read (lane 0 of each producer)
 constexpr int kBarQFree1 = 43;   // ... the same for Q^T buffer 1
 constexpr int kBarEpiFull = 44;  // [2] a unit's column sums and rows handed to the epilogue (one per warpgroup)
-constexpr int kNumBars = 46;
+constexpr int kBarOFull = 46;    // [2] a unit's last P.V finished: its O buffer holds the unit's output (MMA commit)
+constexpr int kNumBars = 48;
 __device__ __forceinline__ int qfree_bar(int qb) { return qb == 0 ? kBarQFree : kBarQFree1; }
 static_assert(kNumBars * 8 <= Smem<16>::misc_off - Smem<16>::bar_off, "mbarrier space");
 
@@ -258,6 +261,7 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             tc::mbar_init(bar(kBarUEmpty + i), 3);
             tc::mbar_init(bar(kBarOFree + i), 1);
             tc::mbar_init(bar(kBarEpiFull + i), 2);
+            tc::mbar_init(bar(kBarOFull + i), 1);
         }
         tc::mbar_init(bar(kBarQFree), 1);
         tc::mbar_init(bar(kBarQFree1), 1);
@@ -741,16 +745,22 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                             tc::mma_commit(bar(kBarEmptyV + stp));
                             ++gp;
                             if (++tp == ((ip & 1) ? ntq1 : ntq0)) {
+                                tc::mma_commit(bar(kBarOFull + ob));   // the unit's O is complete
                                 ++ip;
                                 tp = 0;
                             }
                             progressed = true;
                         }
                     }
+                    // An idle pass naps briefly: a lane spinning at full rate
+                    // takes issue slots from the softmax warps that share its
+                    // scheduler (speculative forest 128.1 -> 126.2 us).
                     if (progressed)
                         polls = 0;
                     else if (++polls > (1u << 24))
                         ok = false;
+                    else
+                        __nanosleep(32);
                 }
                 if (!ok)
                     if (!*err) *err = 208;
@@ -763,9 +773,12 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
             // then the buffer is free for the unit two on.
             const int je = tid - 384;
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            // One thread waits on each mbarrier and the named barrier
+            // releases the others, so that 128 spinning threads do not take
+            // issue slots from the softmax warps on the same schedulers.
             for (int i = 0;; ++i) {
                 const int ob = i & 1;
-                const bool okw = tc::mbar_wait(bar(kBarEpiFull + ob), (i >> 1) & 1);
+                const bool okw = je != 0 || tc::mbar_wait(bar(kBarEpiFull + ob), (i >> 1) & 1);
                 if (tc::named_sync_or(3, 128, !okw)) {
                     if (!*err) *err = 211;
                     break;
@@ -775,6 +788,13 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 if (R == -1)
                     break;
                 if (R >= 0) {
+                    // The unit's last P.V (the softmax warpgroups do not wait for it).
+                    const bool okf = je != 0 || tc::mbar_wait(bar(kBarOFull + ob), (i >> 1) & 1);
+                    if (tc::named_sync_or(3, 128, !okf)) {
+                        if (!*err) *err = 213;
+                        break;
+                    }
+                    tc::fence_after_sync();
                     const uint32_t tmem_ob = tmem + 256 + (uint32_t)(ob * 128) + lane_off;
     #pragma unroll
                     for (int w = 0; w < 2; ++w) {
@@ -1001,11 +1021,9 @@ phase1_mma_kernel(AttnArgs a, DevPartition p, const int32_t *__restrict__ items,
                 gseq = 0;
                 continue;
             }
-            // The unit's last P.V, then O / l for this warpgroup's rows.
-            if (ok && !dry) {
-                ok = tc::mbar_wait(bar(kBarPvDone), (gseq - 1) & 1);
-                tc::fence_after_sync();
-            }
+            // 1 / l and the rows for the epilogue warpgroup, which waits for
+            // the unit's last P.V itself: the column sums are this
+            // warpgroup's own, so it goes on to the next unit meanwhile.
             if (!ok)
                 if (!*err) *err = 210;
             const bool failed = tc::named_sync_or(nb_id, 128, !ok || *err != 0);

@@ -539,9 +539,10 @@ class Runner:
         """End to end through the public API, as a decode loop runs it: the
         tree planned afresh every step (tree-only, rebuilt into the loop's
         plan so that its device copy and staging buffer are reused), the plan
-        uploaded, then one deft_tree_attn_host call: Q copied from pinned
-        host memory, the step run, out + lse copied back to pinned host
-        memory."""
+        uploaded, then one deft_tree_attn_host call (through a HostStep
+        bound to the loop's buffers once, as a decode loop holds them): Q
+        copied from pinned host memory, the step run, out + lse copied back
+        to pinned host memory."""
         torch, deft, spec, t, a = self.torch, self.deft, self.spec, self.t, self.args
         q_host = t.q.cpu().pin_memory()
         out_host = torch.empty(self.bufs.out.shape, dtype=self.bufs.out.dtype).pin_memory()
@@ -550,19 +551,20 @@ class Runner:
         times = []
         p = deft.Plan(spec.parent, spec.node_len, spec.query_node, a.chunk_target, spec.gqa_group,
                       query_pos=spec.query_pos, naive=False, tensor_pack=self.tp)
+        step = deft.HostStep(q_host, q_dev, t.k_pages, t.v_pages, self.npo, self.pid, p, self.bufs, out_host,
+                             lse_host)
         for i in range(n + 3):
             self.barrier()
             t0 = time.perf_counter()
             p.rebuild(spec.parent, spec.node_len, spec.query_node, a.chunk_target, spec.gqa_group,
                       query_pos=spec.query_pos, naive=False, tensor_pack=self.tp)
             p.upload()
-            deft.deft_tree_attn_host(q_host, q_dev, t.k_pages, t.v_pages, self.npo, self.pid, p, self.bufs,
-                                     out_host, lse_host)
+            step()
             torch.cuda.synchronize(self.dev)
             if i >= 3:
                 times.append(time.perf_counter() - t0)
         plan_bytes = p.stats["device_bytes"]
-        del p
+        del step, p
         return (statistics.mean(times) * 1e6, int(q_host.numel() * 2 + plan_bytes),
                 int(out_host.numel() * out_host.element_size() + lse_host.numel() * 4))
 

@@ -345,14 +345,10 @@ def deft_tree_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs
                  node_page_off, page_id, plan, bufs, scale, out_dtype, stream, flags)
 
 
-def deft_tree_attn_host(q_host, q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs: StepBuffers,
-                        out_host, lse_host, scale=None, stream=None):
-    """deft_tree_attn_host: q_host (host, pinned for an asynchronous copy) is
-    copied into the device buffer q, the step runs, and out / lse are copied
-    into out_host / lse_host, all on the stream; synchronise it before
-    reading the host outputs."""
+def _host_step_args(q_host, q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs: StepBuffers,
+                    out_host, lse_host, scale):
+    """The checked arguments of deft_tree_attn_host, the stream left out."""
     import torch
-    lib = load()
     Q, Hq, d = q.shape
     Hkv, P = k_pages.shape[1], k_pages.shape[2]
     for t in (q, k_pages, v_pages):
@@ -365,13 +361,45 @@ def deft_tree_attn_host(q_host, q, k_pages, v_pages, node_page_off, page_id, pla
             raise ValueError("out_host / lse_host must be contiguous host tensors shaped like the outputs")
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     odt = DEFT_OUT_BF16 if bufs.out.dtype == torch.bfloat16 else DEFT_OUT_F32
-    rc = lib.deft_tree_attn_host(q_host.data_ptr(), q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
-                                 node_page_off.data_ptr(), page_id.data_ptr(), int(k_pages.shape[0]), int(Hq),
-                                 int(Hkv), int(d), int(P), float(scale), plan.handle, bufs.out.data_ptr(), odt,
-                                 bufs.lse.data_ptr(), bufs.workspace.data_ptr(), int(bufs.workspace.numel()),
-                                 out_host.data_ptr(), lse_host.data_ptr(), _stream(stream))
-    _check("deft_tree_attn_host", rc)
+    return (q_host.data_ptr(), q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(), node_page_off.data_ptr(),
+            page_id.data_ptr(), int(k_pages.shape[0]), int(Hq), int(Hkv), int(d), int(P), float(scale), plan.handle,
+            bufs.out.data_ptr(), odt, bufs.lse.data_ptr(), bufs.workspace.data_ptr(), int(bufs.workspace.numel()),
+            out_host.data_ptr(), lse_host.data_ptr())
+
+
+def deft_tree_attn_host(q_host, q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs: StepBuffers,
+                        out_host, lse_host, scale=None, stream=None):
+    """deft_tree_attn_host: q_host (host, pinned for an asynchronous copy) is
+    copied into the device buffer q, the step runs, and out / lse are copied
+    into out_host / lse_host, all on the stream; synchronise it before
+    reading the host outputs."""
+    args = _host_step_args(q_host, q, k_pages, v_pages, node_page_off, page_id, plan, bufs, out_host, lse_host,
+                           scale)
+    _check("deft_tree_attn_host", load().deft_tree_attn_host(*args, _stream(stream)))
     return out_host, lse_host
+
+
+class HostStep:
+    """deft_tree_attn_host bound to one set of buffers, for a decode loop
+    that runs the same shapes every step: the arguments are checked and
+    marshalled once, each call is one library call on the stream.  The
+    object holds the tensors and the plan, so their addresses stay valid;
+    refill q_host (and rebuild or update the plan, then upload it) between
+    calls, and synchronise the stream before reading out_host / lse_host."""
+
+    def __init__(self, q_host, q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs: StepBuffers,
+                 out_host, lse_host, scale=None):
+        self._args = _host_step_args(q_host, q, k_pages, v_pages, node_page_off, page_id, plan, bufs, out_host,
+                                     lse_host, scale)
+        self._held = (q_host, q, k_pages, v_pages, node_page_off, page_id, plan, bufs, out_host, lse_host)
+        self._fn = load().deft_tree_attn_host
+        self.out_host, self.lse_host = out_host, lse_host
+
+    def __call__(self, stream=None):
+        rc = self._fn(*self._args, _stream(stream))
+        if rc:
+            _check("deft_tree_attn_host", rc)
+        return self.out_host, self.lse_host
 
 
 def deft_naive_attn(q, k_pages, v_pages, node_page_off, page_id, plan: Plan, bufs=None,

@@ -173,6 +173,16 @@ def test_host_buffer_step_equals_the_device_step(deft, spec):
         np.testing.assert_array_equal(out_h.float().numpy().astype(np.float64), out_d)
         np.testing.assert_array_equal(lse_h.numpy().astype(np.float64), lse_d)
         torch.testing.assert_close(q_dev, case.q, rtol=0, atol=0)
+        # The same call bound once (HostStep), twice, into cleared buffers.
+        step = deft.HostStep(q_host, q_dev, case.k, case.v, case.npo, case.pid, case.plan, bufs, out_h, lse_h)
+        for _ in range(2):
+            out_h.zero_()
+            lse_h.zero_()
+            q_dev.zero_()
+            step()
+            torch.cuda.synchronize()
+            np.testing.assert_array_equal(out_h.float().numpy().astype(np.float64), out_d)
+            np.testing.assert_array_equal(lse_h.numpy().astype(np.float64), lse_d)
     assert case.plan.step_status() == 0
 
 

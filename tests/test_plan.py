@@ -463,6 +463,28 @@ def test_step_calls_reject_bad_flags_and_state_before_any_cuda_call():
     assert call_host(fake, fake, fake) == -8      # never uploaded: nothing enqueued
 
 
+def test_host_step_checks_its_tensors_once():
+    """HostStep (deft_tree_attn_host bound to its buffers) makes the same
+    checks as the plain call, at construction; host tensors where device
+    ones belong, or the reverse, are rejected before any library call."""
+    torch = pytest.importorskip("torch")
+    spec = W.tiny_tree()
+    plan = deft.Plan(spec.parent, spec.node_len, spec.query_node, 64, spec.gqa_group)
+    Q, Hq, Hkv, d = spec.num_queries, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    q = torch.zeros((Q, Hq, d), dtype=torch.bfloat16)
+    kv = torch.zeros((4, Hkv, 16, d), dtype=torch.bfloat16)
+    idx = torch.zeros(8, dtype=torch.int32)
+
+    class Bufs:
+        out = torch.zeros((Q, Hq, d), dtype=torch.bfloat16)
+        lse = torch.zeros((Q, Hq), dtype=torch.float32)
+        workspace = torch.zeros(256, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        deft.HostStep(q.clone(), q, kv, kv, idx, idx, plan, Bufs, Bufs.out.clone(), Bufs.lse.clone())
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        deft.deft_tree_attn_host(q.clone(), q, kv, kv, idx, idx, plan, Bufs, Bufs.out.clone(), Bufs.lse.clone())
+
+
 def test_check_pages_accepts_a_layout_and_rejects_each_bad_table():
     spec = W.reasoning_tree(levels=3, len_lo=5, len_hi=40, num_queries=12, q_heads=4, kv_heads=2)
     lay = W.paged_layout(spec)

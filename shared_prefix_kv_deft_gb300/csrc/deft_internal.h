@@ -364,12 +364,14 @@ int prepare_step(const void *q, const void *k_pages, const void *v_pages, const 
 // units (item x KV head).  The step's launches run concurrently, so the
 // first `early` CTAs of a launch start at once and the rest only on SMs that
 // earlier launches leave; each early CTA first takes a contiguous block of
-// about 3/4 of an even share of the units (static_block), and every CTA
-// then takes single units from the launch's work queue.
+// units (`block`, sized by the dispatcher from the units' estimated costs,
+// and never more than 3/4 of an even share of the units by count:
+// static_block), and every CTA then takes single units from the launch's
+// work queue.
 struct LaunchShape {
     int32_t grid;
     int32_t early;   // 1 <= early <= grid
-    int32_t block;   // units of each early CTA's block; -1: about 3/4 of an even share
+    int32_t block;   // units of each early CTA's block; -1: 3/4 of an even share by count
 };
 inline int32_t static_block(int32_t units, int32_t early, int32_t block = -1)
 {

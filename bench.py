@@ -267,12 +267,39 @@ class ClockSampler:
 HOST_GLUE = ("capi.cu", "noalloc.cu")
 
 
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank lines (string and
+    character literals kept), so that a change to comments alone leaves the
+    source hash, and the counters recorded against it, as they were."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(l.rstrip() for l in "".join(out).split("\n") if l.strip())
+
+
 def kernel_source_hash():
+    """Hash of the kernel, launch and planner sources (comments left out)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "shared_prefix_kv_deft_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h", ".cpp")) and f not in HOST_GLUE:
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -83,3 +83,15 @@ def test_whole_step_roofline_and_job_value(bench):
     assert r["traffic"] is None          # no capture for an unknown workload
     # N replicas each finishing a step in the slowest rank's time.
     assert bench.job_us_per_step(0.05, 4) == pytest.approx(12.5)
+
+
+def test_source_hash_ignores_comments_only(bench):
+    """The counters in profiles/ncu_traffic.json are tied to a hash of the
+    kernel sources; a change to comments alone must not detach them, any
+    change to code must."""
+    src = 'int a = 1; // note\n/* block\n   note */ const char *s = "x // y /* z */"; char q = \'"\';\n\n int b;\n'
+    out = bench.strip_comments(src)
+    assert "note" not in out and "block" not in out
+    assert '"x // y /* z */"' in out and "'\"'" in out
+    assert bench.strip_comments(src.replace("// note", "// another note")) == out
+    assert bench.strip_comments(src.replace("int b;", "int b = 2;")) != out

@@ -144,7 +144,9 @@ typedef enum deft_plan_array {
  *     traffic stays small next to its KV traffic.  Every (query, node on its
  *     path, token) triple lands in exactly one chunk that lists the query.
  *   - gqa_group = num_q_heads / num_kv_heads of the layer the plan will run
- *     (decides which chunks reach 16 rows = |Q_c| * gqa_group); 1..128.
+ *     (decides which chunks reach 16 rows = |Q_c| * gqa_group); 1..64 (a
+ *     query's whole group shares one tensor-core item of at most 64 rows;
+ *     above 64, DEFT_EINVAL).
  *   - The naive per-query partition (deft_naive_attn) cuts each query's
  *     path tokens into pieces of chunk_target tokens.
  * On success *out owns the plan (free with deft_plan_free).  The input arrays

@@ -255,6 +255,11 @@ int build_host(const int32_t *parent, const int32_t *node_len, int32_t num_nodes
 {
     if (flags & ~(int32_t)(DEFT_PLAN_TREE_ONLY | DEFT_PLAN_TENSOR_PACK))
         return DEFT_EINVAL;
+    // A query's whole GQA group shares one tensor-core item, of at most
+    // kMmaMaxRows rows (a larger group once made wider items than the
+    // kernel has and overran the planner's per-width tables).
+    if (gqa_group > deft::kMmaMaxRows)
+        return DEFT_EINVAL;
     int rc;
     try {
         rc = deft::build_plan(parent, node_len, num_nodes, query_node, query_pos, num_queries,

@@ -443,6 +443,32 @@ def test_growing_logits_take_the_rescale_path(deft, spec, ct, tp):
     assert case.plan.step_status() == 0
 
 
+# Large GQA groups: a query alone makes G rows (8 .. 64), so one query can
+# fill a tensor-core item (G = 32, 64) and CUDA-core items hold one or two
+# queries (G = 8, 16).
+GQA_SHAPES = [
+    W.reasoning_tree(levels=3, len_lo=20, len_hi=150, num_queries=nq, q_heads=q, kv_heads=kv, seed=g)
+    for g, q, kv, nq in ((8, 16, 2, 12), (16, 32, 2, 9), (32, 32, 1, 7), (64, 64, 1, 5))
+]
+
+
+@pytest.mark.parametrize("spec", GQA_SHAPES, ids=lambda s: s.name)
+@pytest.mark.parametrize("ct,tp", [(64, False), (256, False), (256, True)])
+def test_large_gqa_groups_match_oracle(deft, spec, ct, tp):
+    inp = dense_inputs(spec, seed=7 + ct)
+    ref, ref_lse = run_oracle(inp)
+    case = Case(deft, inp, ct, tensor_pack=tp)
+    out, lse = case.run()
+    assert_parity(out, lse, ref, ref_lse, f"G={spec.gqa_group}")
+    out_s, lse_s = case.run(flags=deft.STEP_SEPARATE_MERGE)
+    np.testing.assert_array_equal(out_s, out)
+    np.testing.assert_array_equal(lse_s, lse)
+    if spec.gqa_group <= 16:
+        out2, lse2 = case.run(flags=deft.STEP_CUDA_CORES)
+        assert_parity(out2, lse2, ref, ref_lse, f"G={spec.gqa_group}, CUDA cores")
+    assert case.plan.step_status() == 0
+
+
 POSITION_SHAPES = [W.positions_tree(s, max_nodes=14, max_len=120, max_queries=24, q_heads=8,
                                     kv_heads=2, head_dim=128) for s in range(6)]
 POSITION_SHAPES += [W.positions_tree(50 + s, max_nodes=10, max_len=60, max_queries=12)

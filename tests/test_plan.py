@@ -463,6 +463,28 @@ def test_step_calls_reject_bad_flags_and_state_before_any_cuda_call():
     assert call_host(fake, fake, fake) == -8      # never uploaded: nothing enqueued
 
 
+def test_gqa_group_is_limited_to_one_tensor_core_item():
+    """A query's whole GQA group shares one tensor-core item (at most 64
+    rows): groups up to 64 plan, one query per item at 64; larger groups are
+    rejected (they once made items of more rows than the kernel's widths
+    and wrote past the planner's bucket tables)."""
+    spec = W.chain_tree([40, 30, 5], q_heads=64, kv_heads=1, head_dim=128)
+    for g in (1, 16, 32, 64):
+        for tp in (False, True):
+            p = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, g, tensor_pack=tp)
+            items = p.get("mma_items").reshape(-1, 3)
+            rows = (items[:, 2] - items[:, 1]) * g
+            assert (rows <= 64).all() and (rows >= 16).all()
+    p = deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, 64)
+    for g in (65, 100, 128, 129):
+        with pytest.raises(deft.DeftError) as e:
+            deft.Plan(spec.parent, spec.node_len, spec.query_node, 256, g, tensor_pack=True)
+        assert e.value.status == -1
+        with pytest.raises(deft.DeftError):
+            p.rebuild(spec.parent, spec.node_len, spec.query_node, 256, g)
+    assert p.stats["gqa_group"] == 64   # a failed rebuild leaves the plan as it was
+
+
 def test_host_step_checks_its_tensors_once():
     """HostStep (deft_tree_attn_host bound to its buffers) makes the same
     checks as the plain call, at construction; host tensors where device

@@ -463,6 +463,31 @@ def test_step_calls_reject_bad_flags_and_state_before_any_cuda_call():
     assert call_host(fake, fake, fake) == -8      # never uploaded: nothing enqueued
 
 
+def _extreme_shapes():
+    """The planner's limits: a comb of 300 one-token children (packed chunks
+    close at 256 segments), a 600-node chain of one-token nodes with a query
+    at every node, 1000 queries on six nodes (16 mask words)."""
+    comb = W.TreeSpec("comb300", np.array([-1] + [0] * 300, np.int32), np.ones(301, np.int32),
+                      np.arange(1, 301, dtype=np.int32), 4, 1, 128)
+    chain = W.TreeSpec("chain600", np.array([-1] + list(range(599)), np.int32), np.ones(600, np.int32),
+                       np.arange(600, dtype=np.int32), 8, 2, 128)
+    rng = np.random.default_rng(7)
+    manyq = W.TreeSpec("manyq1000", np.array([-1, 0, 0, 1, 1, 2], np.int32),
+                       np.array([300, 17, 0, 65, 1, 129], np.int32),
+                       rng.integers(0, 6, 1000).astype(np.int32), 8, 2, 128)
+    return [comb, chain, manyq]
+
+
+@pytest.mark.parametrize("spec", _extreme_shapes(), ids=lambda s: s.name)
+@pytest.mark.parametrize("ct", [16, 256])
+@pytest.mark.parametrize("G", [1, 16, 64])
+def test_extreme_shapes_keep_the_plan_invariants(spec, ct, G):
+    for tp in (False, True):
+        plan = check_plan(spec, ct, G, tensor_pack=tp)
+        so = plan.get("chunk_seg_off")
+        assert (np.diff(so) <= 256).all()   # kMaxSegsPerChunk
+
+
 def test_gqa_group_is_limited_to_one_tensor_core_item():
     """A query's whole GQA group shares one tensor-core item (at most 64
     rows): groups up to 64 plan, one query per item at 64; larger groups are

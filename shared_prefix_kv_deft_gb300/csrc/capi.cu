@@ -306,34 +306,38 @@ int deft_plan_rebuild(deft_plan_t *plan, const int32_t *parent, const int32_t *n
 {
     if (!plan)
         return DEFT_EINVAL;
-    deft_plan_t fresh;
+    // The new host side is built into this thread's spare one and swapped
+    // in: the plan is left as it was on an error, and the plan's old arrays
+    // become the spare's, so that a loop rebuilding a plan every step
+    // reuses their storage instead of allocating it again.
+    thread_local deft_plan_t spare;
     const int rc = build_host(parent, node_len, num_nodes, query_node, query_pos, num_queries, chunk_target,
-                              gqa_group, flags, &fresh);
+                              gqa_group, flags, &spare);
     if (rc != DEFT_OK)
         return rc;   // the plan is left as it was
-    // The host side moves in; the device copy, staging buffer and event stay.
-    plan->num_nodes = fresh.num_nodes;
-    plan->num_queries = fresh.num_queries;
-    plan->gqa_group = fresh.gqa_group;
-    plan->chunk_target = fresh.chunk_target;
-    plan->mask_words = fresh.mask_words;
-    plan->cover = std::move(fresh.cover);
-    plan->order = std::move(fresh.order);
-    plan->tree = std::move(fresh.tree);
-    plan->naive = std::move(fresh.naive);
-    plan->has_naive = fresh.has_naive;
-    plan->stats = fresh.stats;
-    plan->in_parent = std::move(fresh.in_parent);
-    plan->in_len = std::move(fresh.in_len);
-    plan->in_qnode = std::move(fresh.in_qnode);
-    plan->in_qpos = std::move(fresh.in_qpos);
-    plan->in_tensor_pack = fresh.in_tensor_pack;
-    plan->own_off = std::move(fresh.own_off);
-    plan->own_q = std::move(fresh.own_q);
-    plan->order_pos = std::move(fresh.order_pos);
-    plan->ckpt = std::move(fresh.ckpt);
-    plan->thin = std::move(fresh.thin);
-    plan->thin_mask = std::move(fresh.thin_mask);
+    // The host side swaps in; the device copy, staging buffer and event stay.
+    plan->num_nodes = spare.num_nodes;
+    plan->num_queries = spare.num_queries;
+    plan->gqa_group = spare.gqa_group;
+    plan->chunk_target = spare.chunk_target;
+    plan->mask_words = spare.mask_words;
+    std::swap(plan->cover, spare.cover);
+    std::swap(plan->order, spare.order);
+    std::swap(plan->tree, spare.tree);
+    std::swap(plan->naive, spare.naive);
+    plan->has_naive = spare.has_naive;
+    plan->stats = spare.stats;
+    std::swap(plan->in_parent, spare.in_parent);
+    std::swap(plan->in_len, spare.in_len);
+    std::swap(plan->in_qnode, spare.in_qnode);
+    std::swap(plan->in_qpos, spare.in_qpos);
+    plan->in_tensor_pack = spare.in_tensor_pack;
+    std::swap(plan->own_off, spare.own_off);
+    std::swap(plan->own_q, spare.own_q);
+    std::swap(plan->order_pos, spare.order_pos);
+    std::swap(plan->ckpt, spare.ckpt);
+    std::swap(plan->thin, spare.thin);
+    std::swap(plan->thin_mask, spare.thin_mask);
     plan->uploaded = false;
     plan->noalloc_image_ok = false;
     plan->broken = false;

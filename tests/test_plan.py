@@ -353,6 +353,29 @@ def test_rebuild_matches_a_fresh_plan(first, second, naive):
         np.testing.assert_array_equal(p.get(name), f.get(name))
 
 
+def test_plans_rebuilt_in_turn_each_match_a_fresh_plan():
+    """Rebuilds build into a spare host plan of the calling thread that the
+    plans share (its arrays keep their storage): two plans rebuilt in turn
+    over different trees, and one rebuilt after a failed rebuild, each hold
+    exactly a fresh plan of their last tree."""
+    specs = [W.config(c) for c in (2, 4, 7, 1)] + [W.random_tree(s, max_nodes=30, max_len=300, max_queries=50,
+                                                                 q_heads=8, kv_heads=2, head_dim=128)
+                                                   for s in range(4)]
+    plans = [deft.Plan(specs[0].parent, specs[0].node_len, specs[0].query_node, 256, specs[0].gqa_group)
+             for _ in range(2)]
+    for k, s in enumerate(specs * 2):
+        p = plans[k % 2]
+        if k == 5:
+            with pytest.raises(deft.DeftError):
+                p.rebuild(s.parent, s.node_len, s.query_node, 0, s.gqa_group)
+        tp = k % 3 == 0
+        p.rebuild(s.parent, s.node_len, s.query_node, 100, s.gqa_group, query_pos=s.query_pos, tensor_pack=tp)
+        f = deft.Plan(s.parent, s.node_len, s.query_node, 100, s.gqa_group, query_pos=s.query_pos, tensor_pack=tp)
+        assert p.stats == f.stats
+        for name in deft.ARRAYS:
+            np.testing.assert_array_equal(p.get(name), f.get(name), err_msg=f"step {k} {name}")
+
+
 def test_failed_rebuild_leaves_the_plan_unchanged():
     a = W.config(4)
     p = deft.Plan(a.parent, a.node_len, a.query_node, 256, a.gqa_group)

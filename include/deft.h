@@ -208,7 +208,10 @@ int deft_plan_ex(const int32_t *parent, const int32_t *node_len, int32_t num_nod
  * still reading it must be ordered before that upload (same stream, or
  * synchronised streams).  A CUDA graph that captured a step of this plan
  * holds the old launch shapes and device addresses: capture it again after
- * a rebuild.  DEFT_EINVAL for a null plan.
+ * a rebuild.  The new host arrays are built in a spare host plan of the
+ * calling thread and swapped in; the spare keeps the replaced arrays, whose
+ * storage the thread's next rebuild (of any plan) reuses, until the thread
+ * exits.  DEFT_EINVAL for a null plan.
  */
 int deft_plan_rebuild(deft_plan_t *plan, const int32_t *parent, const int32_t *node_len, int32_t num_nodes,
                       const int32_t *query_node, const int32_t *query_pos, int32_t num_queries,

@@ -654,7 +654,9 @@ def measure_config(deft, torch, dev, cfg, args, hbm_peak, peak_kind, steps, warm
              "unique_kv_bytes": r.unique_kv(), "frac_of_measured_hbm": roof["whole_step"]["frac"],
              "whole_step_roofline": roof["whole_step"],
              "dominant_kernel": {"name": roof["kernel"], "avg_us": roof["avg_launch_us"],
-                                 "frac_sm_share_limited": roof["frac"]},
+                                 "frac_sm_share_limited": roof["frac"],
+                                 "alg_bytes_per_launch": roof["alg_bytes_per_launch"],
+                                 "dram_bytes_per_launch": roof["traffic"]},
              "naive_us_per_step": r.naive_leg(max(3, steps // 2)), "e2e_us_per_step": e2e_us}
     if oracle_budget > 0:
         cb = cpu_baseline(r.spec, r.layout, host_inputs(r.spec, r.layout, r.t), budget_s=oracle_budget,
